@@ -1,0 +1,190 @@
+"""CPU oracle for the persistent KV-cache hot path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference arm may import this package.  The product library never loads it
+and shares no code with it (``kvc_oracle.c`` is compiled on its own with gcc).
+
+Every function takes numpy arrays (16-bit floats travel as ``uint16`` bit
+patterns) and returns numpy arrays; each one cites the page it restates:
+
+* ``tensor_scatter``  -- "TensorScatter" operator page (opset 24), spec and
+  pseudocode.
+* ``seq_lengths``     -- "GQA support sliding_window_cache" (onnxruntime PR
+  29904), section "Design" (lengths derived on device from ``seqlens_k``).
+* ``window_append``   -- same PR, "Design": windowed invariant, append formula,
+  in-place S == 1 compaction and C + S staging for S > 1.
+* ``rope_rows``       -- same PR (absolute-position RoPE bounded by the cos/sin
+  cache) and "Stateful decode & KV cache", "Sliding-window ring buffer" (RoPE
+  baked into K at write time).
+* ``gqa_attention``   -- "Persistent KV Cache and Decode Performance Roadmap",
+  "Phase 1" (what decode attention computes, GQA sharing) with the causal and
+  local-window mask of the PR.
+
+Pins: every function is checked in ``tests/test_oracle_*.py`` against the
+pages' worked examples, closed forms, brute-force simulations and library
+routines (see the docstrings there).  No function here is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kvc_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+F32, BF16, F16 = 0, 1, 2
+LINEAR, CIRCULAR = 0, 1
+
+# per-row flags (the oracle's own numbering, mirrored from kvc_oracle.c)
+BAD_INDEX, BAD_SEQLEN, BAD_CAPACITY, BAD_ROPE = 1, 2, 4, 8
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` with gcc (no contraction of float ops)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I32, I64, DBL = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        lib.orc_tensor_scatter.argtypes = [P, P, P, P, I32, P, I64, I32, I32, I32, P]
+        lib.orc_tensor_scatter.restype = I32
+        lib.orc_seq_lengths.argtypes = [P, I32, I32, I64, I32, P, P, P, P, P, P]
+        lib.orc_seq_lengths.restype = None
+        lib.orc_rope_rows.argtypes = [P, P, P, I64, I32, I32, P, P, I64]
+        lib.orc_rope_rows.restype = I32
+        lib.orc_window_append.argtypes = [P, P, P, P, P, P, P, P, P, P, I32, I32, I32, I64,
+                                          I32, I32, I32, P, P, I64, P]
+        lib.orc_window_append.restype = I32
+        lib.orc_gqa_attention.argtypes = [P, P, P, P, I64, P, P, I32, I32, I32, I32, I32,
+                                          I32, I32, DBL, P, P, I64, P]
+        lib.orc_gqa_attention.restype = I32
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _dtype_code(a) -> int:
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:
+        return BF16
+    if a.dtype == np.float16:
+        return F16
+    raise TypeError(f"unsupported element type {a.dtype}")
+
+
+def tensor_scatter(past, update, write_indices, axis=-2, mode=LINEAR, out=None):
+    """TensorScatter: returns (present, per-batch flags).  ``out is past`` runs
+    in place.  Any element type: rows are copied as bytes."""
+    past = np.ascontiguousarray(past)
+    update = np.ascontiguousarray(update)
+    present = np.empty_like(past) if out is None else out
+    shape = np.asarray(past.shape, dtype=np.int64)
+    wi = None if write_indices is None else np.ascontiguousarray(write_indices, dtype=np.int64)
+    flags = np.zeros(past.shape[0], dtype=np.int32)
+    seq_axis = axis if axis >= 0 else axis + past.ndim
+    rc = _load().orc_tensor_scatter(_ptr(present), _ptr(past), _ptr(update), _ptr(wi),
+                                    past.ndim, _ptr(shape), update.shape[seq_axis], axis,
+                                    mode, past.itemsize, _ptr(flags))
+    if rc != 0:
+        raise ValueError("tensor_scatter: arguments outside the operator's definition")
+    return present, flags
+
+
+def seq_lengths(seqlens_k, new_tokens, capacity, windowed):
+    """Returns dict(past_abs, total_abs, cache_past, cache_total, evict, flags)."""
+    sk = np.ascontiguousarray(seqlens_k, dtype=np.int32)
+    B = sk.shape[0]
+    outs = {k: np.zeros(B, dtype=np.int32) for k in
+            ("past_abs", "total_abs", "cache_past", "cache_total", "evict", "flags")}
+    _load().orc_seq_lengths(_ptr(sk), B, new_tokens, capacity, int(windowed),
+                            _ptr(outs["past_abs"]), _ptr(outs["total_abs"]),
+                            _ptr(outs["cache_past"]), _ptr(outs["cache_total"]),
+                            _ptr(outs["evict"]), _ptr(outs["flags"]))
+    return outs
+
+
+def rope_rows(x, pos, cos_cache, sin_cache):
+    """Rotate rows x[..., D] at the absolute positions ``pos`` (one per row)."""
+    x = np.ascontiguousarray(x)
+    D = x.shape[-1]
+    n = x.size // D
+    pos = np.ascontiguousarray(pos, dtype=np.int64).reshape(-1)
+    assert pos.shape[0] == n
+    out = np.empty_like(x)
+    rc = _load().orc_rope_rows(_ptr(out), _ptr(x), _ptr(pos), n, D, _dtype_code(x),
+                               _ptr(np.ascontiguousarray(cos_cache, dtype=np.float32)),
+                               _ptr(np.ascontiguousarray(sin_cache, dtype=np.float32)),
+                               cos_cache.shape[0])
+    if rc != 0:
+        raise ValueError("rope_rows: position outside the cos/sin cache")
+    return out
+
+
+def window_append(k_cache, v_cache, new_k, new_v, lengths, windowed, cos_cache=None,
+                  sin_cache=None, k_stage=None, v_stage=None):
+    """Append in place into ``k_cache``/``v_cache`` ([B, Hkv, C, D]); returns the
+    per-row flags.  For windowed S > 1 the stages ([B, Hkv, C + S, D]) are
+    filled with the seeded rows."""
+    B, Hkv, C, D = k_cache.shape
+    S = new_k.shape[2]
+    flags = np.zeros(B, dtype=np.int32)
+    cc = None if cos_cache is None else np.ascontiguousarray(cos_cache, dtype=np.float32)
+    ss = None if sin_cache is None else np.ascontiguousarray(sin_cache, dtype=np.float32)
+    rmax = 0 if cc is None else cc.shape[0]
+    rc = _load().orc_window_append(
+        _ptr(k_cache), _ptr(v_cache), _ptr(np.ascontiguousarray(new_k)),
+        _ptr(np.ascontiguousarray(new_v)), _ptr(k_stage), _ptr(v_stage),
+        _ptr(lengths["past_abs"]), _ptr(lengths["cache_past"]), _ptr(lengths["cache_total"]),
+        _ptr(lengths["evict"]), B, Hkv, S, C, D, _dtype_code(k_cache), int(windowed),
+        _ptr(cc), _ptr(ss), rmax, _ptr(flags))
+    if rc != 0:
+        raise ValueError("window_append: staging buffers required for windowed S > 1")
+    return flags
+
+
+def gqa_attention(q, k_rows, v_rows, n_rows, total_abs, window=0, scale=None,
+                  cos_cache=None, sin_cache=None):
+    """Attention of q [B, Hq, S, D] over k/v rows [B, Hkv, R, D]; returns
+    (out [B, Hq, S, D] in q's type, per-row flags)."""
+    q = np.ascontiguousarray(q)
+    B, Hq, S, D = q.shape
+    _, Hkv, R, _ = k_rows.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    out = np.zeros_like(q)
+    flags = np.zeros(B, dtype=np.int32)
+    cc = None if cos_cache is None else np.ascontiguousarray(cos_cache, dtype=np.float32)
+    ss = None if sin_cache is None else np.ascontiguousarray(sin_cache, dtype=np.float32)
+    rmax = 0 if cc is None else cc.shape[0]
+    rc = _load().orc_gqa_attention(
+        _ptr(out), _ptr(q), _ptr(np.ascontiguousarray(k_rows)), _ptr(np.ascontiguousarray(v_rows)),
+        R, _ptr(np.ascontiguousarray(n_rows, dtype=np.int32)),
+        _ptr(np.ascontiguousarray(total_abs, dtype=np.int32)), B, Hq, Hkv, S, D,
+        _dtype_code(q), int(window), float(scale), _ptr(cc), _ptr(ss), rmax, _ptr(flags))
+    if rc != 0:
+        raise ValueError("gqa_attention: q_heads must be a multiple of kv_heads")
+    return out, flags
