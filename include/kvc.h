@@ -1,0 +1,255 @@
+/*
+ * kvc.h -- C ABI of the GB300 persistent KV-cache library (libkvc.so).
+ *
+ * One step of the hot path appends new key/value rows to a persistent cache
+ * and runs grouped-query attention (GQA) over it:
+ *
+ *     kvc_seq_lengths      lengths derived on the device from seqlens_k
+ *     kvc_window_append    append (contiguous cache), in-place compaction +
+ *                          append (windowed cache, one token), or C + S
+ *                          staging seed / copy-back (windowed, several tokens)
+ *     kvc_gqa_decode       one-token GQA attention over the cache
+ *     kvc_gqa_prefill_chunk  multi-token GQA attention over staged rows
+ *     kvc_tensor_scatter   the ONNX TensorScatter cache update (linear/circular)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  * Ownership: the caller owns every buffer.  The library allocates nothing,
+ *    keeps no state between calls (apart from cached device attributes) and
+ *    never reads device memory on the host, so every call can be captured in
+ *    a CUDA graph.  Pointers marked "device" must be device (or managed)
+ *    memory of the current device; pointers marked "host" are read during
+ *    the call only.
+ *  * Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  Work
+ *    is enqueued, never waited for.
+ *  * Layout: caches and staging buffers are BNSH: [batch, kv_heads, rows, D],
+ *    row-major, rows of D contiguous elements.  Queries and outputs are
+ *    [batch, q_heads, new_tokens, D].  Query head h reads KV head
+ *    h / (q_heads / kv_heads).
+ *  * Errors: arguments are validated on the host before any launch and a
+ *    non-zero kvc_status is returned with nothing enqueued.  Errors that
+ *    depend on device data (an index out of range, a bad seqlens_k, a RoPE
+ *    position beyond the cos/sin cache) are OR-ed into the caller's device
+ *    word `dev_status` (may be NULL) as KVC_DEV_* bits, and the offending
+ *    batch row writes nothing.  A failed launch returns KVC_ERR_CUDA.
+ *  * Element types: KVC_F32, KVC_BF16, KVC_F16.  Attention accumulates in
+ *    fp32 and rounds the output to nearest-even in the input type.
+ *
+ * Sources (page title, section):
+ *   "TensorScatter" operator page (ai.onnx, since version 24): spec,
+ *     pseudocode, examples.
+ *   "GQA support sliding_window_cache" (onnxruntime pull request 29904):
+ *     section "Design" (windowed invariant, append formula, device-side
+ *     lengths, C + S staging) and the follow-up commits (int64 widening,
+ *     RoPE bounded by the cos/sin cache length, not by the capacity).
+ *   "Persistent KV Cache and Decode Performance Roadmap", section "Phase 1"
+ *     (streaming decode with online softmax, GQA heads sharing a KV block,
+ *     split of one query row across workers with an (m, l, o) merge).
+ *   "Stateful decode & KV cache", section "Sliding-window ring buffer"
+ *     (RoPE baked into K at write time; the mask depends on positions only).
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVC_ABI_VERSION 1
+
+typedef enum {
+    KVC_OK = 0,
+    KVC_ERR_NULL = 1,        /* a required pointer is NULL                       */
+    KVC_ERR_SHAPE = 2,       /* a size is out of range or buffers overlap badly  */
+    KVC_ERR_DTYPE = 3,       /* element type not supported by this entry point   */
+    KVC_ERR_ALIGN = 4,       /* a buffer is not 16-byte aligned where required   */
+    KVC_ERR_UNSUPPORTED = 5, /* a valid combination this build does not cover    */
+    KVC_ERR_CAPACITY = 6,    /* capacity < 1 or too small for the request        */
+    KVC_ERR_WINDOW = 7,      /* windowed cache needs 0 < local_window_size <= C  */
+    KVC_ERR_WORKSPACE = 8,   /* workspace NULL or smaller than required          */
+    KVC_ERR_CUDA = 9         /* a CUDA call failed (launch or driver)            */
+} kvc_status;
+
+typedef enum { KVC_F32 = 0, KVC_BF16 = 1, KVC_F16 = 2 } kvc_dtype;
+typedef enum { KVC_LINEAR = 0, KVC_CIRCULAR = 1 } kvc_mode;
+typedef enum { KVC_APPEND = 0, KVC_COPY_BACK = 1 } kvc_phase;
+
+/* device status bits (OR-ed into *dev_status) */
+#define KVC_DEV_INDEX_OOB 1u    /* TensorScatter linear: wi < 0 or wi + S > max_seq    */
+#define KVC_DEV_SEQLEN_RANGE 2u /* seqlens_k + 1 < new_tokens, or >= 2^31             */
+#define KVC_DEV_CAPACITY 4u     /* contiguous cache: seqlens_k + 1 > capacity          */
+#define KVC_DEV_ROPE_RANGE 8u   /* an absolute position >= rope_max_pos                */
+#define KVC_DEV_TIMEOUT 16u     /* a bounded wait inside a kernel gave up              */
+
+/*
+ * Per-batch lengths, five device int32 arrays of [batch] each, written by
+ * kvc_seq_lengths and read by the other calls ("GQA support
+ * sliding_window_cache", "Design": absolute lengths for RoPE, cache-relative
+ * lengths for addressing, and the evict count).  A rejected row holds -1 in
+ * all five.
+ *   past_abs    P  = T - S        absolute tokens before this step
+ *   total_abs   T  = seqlens_k+1  absolute tokens after this step
+ *   cache_past  Lp                rows resident before the step
+ *   cache_total L                 rows resident after the step
+ *   evict       E                 rows evicted by the step
+ */
+typedef struct {
+    int32_t *past_abs;
+    int32_t *total_abs;
+    int32_t *cache_past;
+    int32_t *cache_total;
+    int32_t *evict;
+} kvc_lengths;
+
+/*
+ * kvc_tensor_scatter -- ONNX TensorScatter ("TensorScatter" operator page,
+ * opset 24: spec and pseudocode).
+ *
+ * present_cache  device, shape cache_shape, elem_bytes per element.
+ * past_cache     device, same shape.  present_cache == past_cache runs in
+ *                place (only the updated rows move); distinct buffers run the
+ *                functional form (every row of present is written once, from
+ *                update or from past).  Partially overlapping buffers ->
+ *                KVC_ERR_SHAPE.
+ * update         device, cache_shape with dimension `axis` = update_seq_len.
+ * write_indices  device int64 [cache_shape[0]], or NULL (all zeros).
+ * rank           2..8; cache_shape is a HOST array of `rank` sizes.
+ * axis           sequence axis, != 0 (negative counts from the end; the
+ *                operator's default is -2).
+ * mode           KVC_LINEAR: row b writes [wi, wi + S); wi < 0 or
+ *                wi + S > max_seq sets KVC_DEV_INDEX_OOB and leaves row b of
+ *                present equal to past.  KVC_CIRCULAR: index mod max_seq
+ *                (floor modulo, so negative wi wraps).
+ * update_seq_len 0..max_seq (a longer update is a shape error).
+ * elem_bytes     1, 2, 4 or 8: rows are copied as bytes, any element type.
+ */
+kvc_status kvc_tensor_scatter(void *present_cache, const void *past_cache, const void *update,
+                              const int64_t *write_indices, int rank, const int64_t *cache_shape,
+                              int64_t update_seq_len, int axis, int mode, int elem_bytes,
+                              int32_t *dev_status, void *stream);
+
+/*
+ * kvc_seq_lengths -- derive the five length arrays on the device ("GQA
+ * support sliding_window_cache", "Design"; int64 arithmetic per the PR's
+ * widening commit).  T = seqlens_k[b] + 1 computed in 64 bits, P = T - S.
+ *   windowed != 0:  Lp = min(P, C), E = max(0, Lp + S - C), L = Lp - E + S
+ *   windowed == 0:  Lp = P, E = 0, L = T; T > C sets KVC_DEV_CAPACITY.
+ * T < S or T >= 2^31 sets KVC_DEV_SEQLEN_RANGE.  A rejected row gets -1 in
+ * every array.
+ * seqlens_k        device int32 [batch].
+ * new_tokens       S >= 1.
+ * capacity         C >= 1 rows per head.
+ * local_window_size  windowed cache: must satisfy 0 < W <= C
+ *                  (KVC_ERR_WINDOW otherwise); ignored for a contiguous cache.
+ */
+kvc_status kvc_seq_lengths(const int32_t *seqlens_k, int batch, int new_tokens, int64_t capacity,
+                           int windowed, int local_window_size, kvc_lengths out,
+                           int32_t *dev_status, void *stream);
+
+/*
+ * kvc_window_append -- write S new K/V rows per (batch, kv head) ("GQA
+ * support sliding_window_cache", "Design").  K rows are rotated (RoPE,
+ * rotate-half pairs (i, i + D/2), float32 with every product and sum
+ * rounded separately) at their ABSOLUTE position P + i before they are
+ * stored; V rows are stored as given.
+ *
+ * k_cache, v_cache  device [batch, kv_heads, capacity, head_dim].
+ * new_k, new_v      device [batch, kv_heads, new_tokens, head_dim].
+ * k_stage, v_stage  device [batch, kv_heads, capacity + new_tokens, head_dim]
+ *                   for a windowed cache with S > 1, else ignored (may be NULL).
+ * len               outputs of kvc_seq_lengths for the same S and C.
+ * phase = KVC_APPEND:
+ *   contiguous cache:      rows [P, P + S) of the cache.
+ *   windowed, S == 1:      in place: rows [E, Lp) move to [0, Lp - E)
+ *                          (E <= 1), then the new row goes to Lp - E.
+ *   windowed, S > 1:       seeds the stage: stage[0, Lp) = cache[0, Lp),
+ *                          stage[Lp + i] = new row i.  Attention then runs on
+ *                          the stage (kvc_gqa_prefill_chunk).
+ * phase = KVC_COPY_BACK (windowed, S > 1 only):
+ *                          cache[0, L) = stage[E, Lp + S).
+ * rope_cos, rope_sin  device float32 [rope_max_pos, head_dim / 2] indexed by
+ *                   absolute position, or both NULL for no rotation.  A row
+ *                   with P + S > rope_max_pos sets KVC_DEV_ROPE_RANGE and is
+ *                   not written.
+ * head_dim          even, 2..1024; dtype KVC_F32/KVC_BF16/KVC_F16.
+ */
+kvc_status kvc_window_append(void *k_cache, void *v_cache, const void *new_k, const void *new_v,
+                             void *k_stage, void *v_stage, kvc_lengths len, int batch,
+                             int kv_heads, int new_tokens, int64_t capacity, int head_dim,
+                             int dtype, int windowed, int phase, const float *rope_cos,
+                             const float *rope_sin, int64_t rope_max_pos, int32_t *dev_status,
+                             void *stream);
+
+/*
+ * kvc_gqa_decode -- one-token grouped-query attention over the cache after
+ * the append ("Persistent KV Cache and Decode Performance Roadmap", Phase 1:
+ * streaming online softmax, a KV block read once per query-head group, a
+ * split of long rows across CTAs merged by (m, l, o); masks from "GQA support
+ * sliding_window_cache").
+ *
+ * For batch row b: rows [0, L) of each head (L = len.cache_total[b]) hold
+ * absolute positions T - L + r (T = len.total_abs[b]); the query is at
+ * T - 1 and is rotated there when rope tables are given.  Row r is visible
+ * iff local_window_size <= 0 or (T - 1) - pos(r) < local_window_size.
+ *
+ * out, q        device [batch, q_heads, 1, head_dim], same dtype as the cache.
+ * k_cache/v_cache device [batch, kv_heads, capacity, head_dim].
+ * scale         0 -> 1/sqrt(head_dim).
+ * workspace     device scratch of kvc_gqa_decode_workspace_size(...) bytes
+ *               (holds per-split partial (m, l, o)); 256-byte aligned.
+ * Supported: KVC_BF16/KVC_F16 with head_dim in {64, 128} and
+ * q_heads / kv_heads <= 16 (tensor-core path); KVC_F32 with head_dim <= 256.
+ * All buffers 16-byte aligned (KVC_ERR_ALIGN).
+ */
+kvc_status kvc_gqa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                          kvc_lengths len, int batch, int q_heads, int kv_heads, int64_t capacity,
+                          int head_dim, int dtype, int local_window_size, float scale,
+                          const float *rope_cos, const float *rope_sin, int64_t rope_max_pos,
+                          void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                          void *stream);
+
+/* Bytes of workspace kvc_gqa_decode needs for these sizes (0 on bad sizes). */
+size_t kvc_gqa_decode_workspace_size(int batch, int q_heads, int kv_heads, int64_t capacity,
+                                     int head_dim, int dtype);
+
+/*
+ * kvc_gqa_prefill_chunk -- attention of an S-token chunk over staged rows
+ * ("GQA support sliding_window_cache", "Design": multi-token steps run
+ * against the C + S staging cache; causal plus local-window mask).
+ *
+ * For batch row b with Lp = len.cache_past[b], P = len.past_abs[b]: rows
+ * [0, Lp + S) of each head of k_rows/v_rows hold positions P - Lp + r (the
+ * stage after kvc_window_append(KVC_APPEND), or a contiguous cache after its
+ * append, where Lp = P).  Query i is at P + i and sees row r iff
+ * pos(r) <= P + i and (local_window_size <= 0 or P + i - pos(r) <
+ * local_window_size).  Queries are rotated at P + i when rope tables are
+ * given.
+ *
+ * out, q          device [batch, q_heads, new_tokens, head_dim].
+ * k_rows, v_rows  device [batch, kv_heads, rows_per_head, head_dim],
+ *                 rows_per_head >= Lp + S for every row (C + S for a stage).
+ * Supported: KVC_BF16/KVC_F16 with head_dim in {64, 128, 256} and
+ * q_heads / kv_heads in {1, 2, 4, 8, 16} (tcgen05 tensor-core path);
+ * KVC_F32 with head_dim <= 256.  Buffers 16-byte aligned.
+ */
+kvc_status kvc_gqa_prefill_chunk(void *out, const void *q, const void *k_rows, const void *v_rows,
+                                 int64_t rows_per_head, kvc_lengths len, int batch, int q_heads,
+                                 int kv_heads, int new_tokens, int head_dim, int dtype,
+                                 int local_window_size, float scale, const float *rope_cos,
+                                 const float *rope_sin, int64_t rope_max_pos,
+                                 int32_t *dev_status, void *stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *kvc_status_string(kvc_status status);
+
+/* KVC_ABI_VERSION of the loaded library. */
+int kvc_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */

@@ -1,0 +1,411 @@
+// kvc_cache.cu -- device-side sequence lengths and the persistent-cache
+// append ("GQA support sliding_window_cache", onnxruntime PR 29904, section
+// "Design"):
+//
+//   windowed cache of capacity C, S new tokens on past length P:
+//     Lp = min(P, C), E = max(0, Lp + S - C)
+//     shift cache[E .. Lp) -> cache[0 .. Lp - E), new rows -> [Lp - E, Lp - E + S)
+//   S == 1 runs in place (E <= 1); S > 1 runs through a C + S staging cache
+//   that is seeded, attended over, and copied back.
+//
+// K rows are rotated at their absolute position while they are written (RoPE
+// baked into K: "Stateful decode & KV cache", "Sliding-window ring buffer").
+//
+// Kernels (all K and V in one launch; blockIdx.z selects K or V):
+//   seq_lengths_kernel   one thread per batch row, int64 arithmetic
+//   new_rows_kernel      writes the S new rows (RoPE on K) at a per-row offset
+//   copy_range_kernel    per-(b, head) contiguous row range copy (stage seed,
+//                        copy-back), 16-byte vectors
+//   compact_kernel       windowed S == 1: in-place one-row left shift of the
+//                        resident rows in ascending tiles, then the new row
+#include "kvc_common.cuh"
+
+namespace {
+
+__global__ void seq_lengths_kernel(const int32_t *__restrict__ seqlens_k, int batch, int S,
+                                   int64_t C, int windowed, kvc_lengths out, int32_t *status)
+{
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= batch)
+        return;
+    const int64_t T = (int64_t)seqlens_k[b] + 1;
+    uint32_t bad = 0;
+    if (T < S || T > (int64_t)INT32_MAX)
+        bad = KVC_DEV_SEQLEN_RANGE;
+    else if (!windowed && T > C)
+        bad = KVC_DEV_CAPACITY;
+    if (bad) {
+        kvc::raise_status(status, bad);
+        out.past_abs[b] = out.total_abs[b] = out.cache_past[b] = out.cache_total[b] =
+            out.evict[b] = -1;
+        return;
+    }
+    const int64_t P = T - S;
+    int64_t Lp, E, L;
+    if (windowed) {
+        Lp = P < C ? P : C;
+        E = Lp + S - C;
+        E = E > 0 ? E : 0;
+        L = Lp - E + S;
+    } else {
+        Lp = P;
+        E = 0;
+        L = T;
+    }
+    out.past_abs[b] = (int32_t)P;
+    out.total_abs[b] = (int32_t)T;
+    out.cache_past[b] = (int32_t)Lp;
+    out.cache_total[b] = (int32_t)L;
+    out.evict[b] = (int32_t)E;
+}
+
+// one thread per (row, pair-vector): loads VEC elements of the low half and
+// the matching VEC of the high half of a new row, rotates K, stores both
+template <typename T, int VEC>
+struct alignas(sizeof(T) * VEC) Vec {
+    T v[VEC];
+};
+
+template <typename T, int VEC>
+__device__ __forceinline__ void write_new_pair(T *__restrict__ dst_row,
+                                               const T *__restrict__ src_row, int D, int j,
+                                               bool rotate, const float *__restrict__ cs,
+                                               const float *__restrict__ sn)
+{
+    const int half = D / 2;
+    Vec<T, VEC> lo = *reinterpret_cast<const Vec<T, VEC> *>(src_row + j * VEC);
+    Vec<T, VEC> hi = *reinterpret_cast<const Vec<T, VEC> *>(src_row + half + j * VEC);
+    if (rotate) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            float a = kvc::Elem<T>::to_f32(lo.v[e]);
+            float b = kvc::Elem<T>::to_f32(hi.v[e]);
+            kvc::rope_pair(a, b, cs[j * VEC + e], sn[j * VEC + e]);
+            lo.v[e] = kvc::Elem<T>::from_f32(a);
+            hi.v[e] = kvc::Elem<T>::from_f32(b);
+        }
+    }
+    *reinterpret_cast<Vec<T, VEC> *>(dst_row + j * VEC) = lo;
+    *reinterpret_cast<Vec<T, VEC> *>(dst_row + half + j * VEC) = hi;
+}
+
+// grid: x over (i, pair-vector) of one (b, head) slice, y = b * Hkv + h, z = K/V
+// dst row of token i = dst_base_rows(b) + i, in a buffer with dst_rows rows/head
+template <typename T, int VEC>
+__global__ void __launch_bounds__(128)
+new_rows_kernel(T *__restrict__ k_dst, T *__restrict__ v_dst, const T *__restrict__ new_k,
+                const T *__restrict__ new_v, kvc_lengths len, int kv_heads, int S, int D,
+                int64_t dst_rows, int offset_from_cache_past, const float *__restrict__ cos_t,
+                const float *__restrict__ sin_t, int64_t rope_max_pos, int32_t *status)
+{
+    const int slice = blockIdx.y;
+    const int b = slice / kv_heads;
+    const bool is_k = blockIdx.z == 0;
+    const int L = len.cache_total[b];
+    if (L < 0)
+        return;
+    const int P = len.past_abs[b];
+    const bool rotate = is_k && cos_t != nullptr;
+    if (cos_t != nullptr && (int64_t)P + S > rope_max_pos) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0 && slice % kv_heads == 0)
+            kvc::raise_status(status, KVC_DEV_ROPE_RANGE);
+        return;
+    }
+    const int base = offset_from_cache_past ? len.cache_past[b] : P;
+    if (base < 0 || (int64_t)base + S > dst_rows) {
+        // lengths computed for another capacity: refuse rather than overrun
+        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0 && slice % kv_heads == 0)
+            kvc::raise_status(status, KVC_DEV_CAPACITY);
+        return;
+    }
+    const int pairs = D / (2 * VEC);
+    const int64_t work = (int64_t)S * pairs;
+    T *dst = (is_k ? k_dst : v_dst) + (int64_t)slice * dst_rows * D;
+    const T *src = (is_k ? new_k : new_v) + (int64_t)slice * S * D;
+    for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < work;
+         w += (int64_t)gridDim.x * blockDim.x) {
+        const int i = (int)(w / pairs);
+        const int j = (int)(w - (int64_t)i * pairs);
+        const int64_t pos = (int64_t)P + i;
+        const float *cs = rotate ? cos_t + pos * (D / 2) : nullptr;
+        const float *sn = rotate ? sin_t + pos * (D / 2) : nullptr;
+        write_new_pair<T, VEC>(dst + ((int64_t)base + i) * D, src + (int64_t)i * D, D, j, rotate,
+                               cs, sn);
+    }
+}
+
+// Copies, for every (b, head), rows [src0, src0 + n) of src to rows [0, n) of
+// dst.  copy_back = 0: stage seed, src0 = 0, n = Lp.  copy_back = 1: src0 = E,
+// n = L.  Row counts come from the device lengths; the grid covers the
+// largest possible range.
+template <typename V>
+__global__ void __launch_bounds__(256)
+copy_range_kernel(char *__restrict__ k_dst, char *__restrict__ v_dst,
+                  const char *__restrict__ k_src, const char *__restrict__ v_src,
+                  kvc_lengths len, int kv_heads, int64_t row_bytes, int64_t dst_rows,
+                  int64_t src_rows, int copy_back, int64_t rope_limit_rows, int S,
+                  int32_t *status)
+{
+    const int slice = blockIdx.y;
+    const int b = slice / kv_heads;
+    const bool is_k = blockIdx.z == 0;
+    const int L = len.cache_total[b];
+    if (L < 0)
+        return;
+    // a row rejected for its RoPE range is rejected as a whole
+    if (rope_limit_rows >= 0 && (int64_t)len.past_abs[b] + S > rope_limit_rows)
+        return;
+    const int64_t src0 = copy_back ? len.evict[b] : 0;
+    const int64_t n = copy_back ? L : len.cache_past[b];
+    if (src0 < 0 || n < 0 || n > dst_rows || src0 + n > src_rows) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0 && slice % kv_heads == 0)
+            kvc::raise_status(status, KVC_DEV_CAPACITY);
+        return;
+    }
+    const int64_t nv = n * row_bytes / (int64_t)sizeof(V);
+    const V *src = reinterpret_cast<const V *>((is_k ? k_src : v_src) +
+                                               ((int64_t)slice * src_rows + src0) * row_bytes);
+    V *dst = reinterpret_cast<V *>((is_k ? k_dst : v_dst) + (int64_t)slice * dst_rows * row_bytes);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + stride < nv; i += 2 * stride) {
+        V a = src[i], c = src[i + stride];
+        dst[i] = a;
+        dst[i + stride] = c;
+    }
+    if (i < nv)
+        dst[i] = src[i];
+}
+
+// Windowed S == 1, in place.  One CTA per (b, head, K/V).  When E == 1 the
+// rows [1, Lp) move down by one row: the slice is walked in ascending tiles,
+// each tile loaded into registers, then (after a barrier) stored one row
+// lower.  A tile's stores only touch rows its own loads or earlier tiles'
+// loads already consumed, so the move needs no scratch buffer.  The new row
+// is written after the last tile.
+template <typename T, int VEC>
+__global__ void __launch_bounds__(256)
+compact_kernel(T *__restrict__ k_cache, T *__restrict__ v_cache, const T *__restrict__ new_k,
+               const T *__restrict__ new_v, kvc_lengths len, int kv_heads, int D, int64_t C,
+               const float *__restrict__ cos_t, const float *__restrict__ sin_t,
+               int64_t rope_max_pos, int32_t *status)
+{
+    constexpr int U = 4;
+    const int slice = blockIdx.x;
+    const int b = slice / kv_heads;
+    const bool is_k = blockIdx.y == 0;
+    const int L = len.cache_total[b];
+    if (L < 0)
+        return;
+    const int P = len.past_abs[b];
+    if (cos_t != nullptr && (int64_t)P + 1 > rope_max_pos) {
+        if (threadIdx.x == 0 && is_k && slice % kv_heads == 0)
+            kvc::raise_status(status, KVC_DEV_ROPE_RANGE);
+        return;
+    }
+    const int Lp = len.cache_past[b];
+    const int E = len.evict[b];
+    if (Lp < 0 || E < 0 || E > 1 || Lp - E + 1 > C || (E == 1 && Lp < 1)) {
+        if (threadIdx.x == 0 && is_k && slice % kv_heads == 0)
+            kvc::raise_status(status, KVC_DEV_CAPACITY);
+        return;
+    }
+    T *cache = (is_k ? k_cache : v_cache) + (int64_t)slice * C * D;
+    if (E > 0) {
+        // move (Lp - 1) rows down by one: flat copy of 16-byte vectors
+        uint4 *base = reinterpret_cast<uint4 *>(cache);
+        const int64_t row_v = (int64_t)D * sizeof(T) / 16;
+        const int64_t n = (int64_t)(Lp - 1) * row_v;
+        const int64_t tile = (int64_t)blockDim.x * U;
+        for (int64_t t0 = 0; t0 < n; t0 += tile) {
+            uint4 r[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = t0 + (int64_t)u * blockDim.x + threadIdx.x;
+                if (i < n)
+                    r[u] = base[i + row_v];
+            }
+            __syncthreads();
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = t0 + (int64_t)u * blockDim.x + threadIdx.x;
+                if (i < n)
+                    base[i] = r[u];
+            }
+            __syncthreads();
+        }
+    }
+    const int dst_row = Lp - E;
+    const bool rotate = is_k && cos_t != nullptr;
+    const int pairs = D / (2 * VEC);
+    const T *src = (is_k ? new_k : new_v) + (int64_t)slice * D;
+    for (int j = threadIdx.x; j < pairs; j += blockDim.x) {
+        const float *cs = rotate ? cos_t + (int64_t)P * (D / 2) : nullptr;
+        const float *sn = rotate ? sin_t + (int64_t)P * (D / 2) : nullptr;
+        write_new_pair<T, VEC>(cache + (int64_t)dst_row * D, src, D, j, rotate, cs, sn);
+    }
+}
+
+template <typename T>
+kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const void *new_v,
+                        void *k_stage, void *v_stage, const kvc_lengths &len, int batch,
+                        int kv_heads, int S, int64_t C, int D, int windowed, int phase,
+                        const float *cos_t, const float *sin_t, int64_t rope_max_pos,
+                        int32_t *status, cudaStream_t stream)
+{
+    constexpr int VEC = 16 / sizeof(T);
+    const int slices = batch * kv_heads;
+    const bool vec_ok = (D / 2) % VEC == 0;
+    T *kc = static_cast<T *>(k_cache);
+    T *vc = static_cast<T *>(v_cache);
+    const T *nk = static_cast<const T *>(new_k);
+    const T *nv = static_cast<const T *>(new_v);
+    auto launch_new_rows = [&](T *kd, T *vd, int64_t dst_rows, int from_cache_past) {
+        const int pairs = vec_ok ? D / (2 * VEC) : D / 2;
+        const int64_t work = (int64_t)S * pairs;
+        int gx = (int)((work + 127) / 128);
+        gx = gx < 1 ? 1 : (gx > 64 ? 64 : gx);
+        dim3 grid(gx, slices, 2);
+        if (vec_ok)
+            new_rows_kernel<T, VEC><<<grid, 128, 0, stream>>>(kd, vd, nk, nv, len, kv_heads, S, D,
+                                                              dst_rows, from_cache_past, cos_t,
+                                                              sin_t, rope_max_pos, status);
+        else
+            new_rows_kernel<T, 1><<<grid, 128, 0, stream>>>(kd, vd, nk, nv, len, kv_heads, S, D,
+                                                            dst_rows, from_cache_past, cos_t,
+                                                            sin_t, rope_max_pos, status);
+    };
+    auto launch_copy = [&](char *kd, char *vd, const char *ks, const char *vs, int64_t dst_rows,
+                           int64_t src_rows, int copy_back, int64_t max_rows) {
+        const int64_t row_bytes = (int64_t)D * sizeof(T);
+        const int64_t max_v = max_rows * row_bytes / 16;
+        int gx = (int)((max_v + 511) / 512);
+        const int cap = kvc_host::sm_count() * 8 / (slices * 2 > 0 ? slices * 2 : 1) + 1;
+        gx = gx < 1 ? 1 : (gx > cap ? cap : gx);
+        dim3 grid(gx, slices, 2);
+        const int64_t rope_rows = cos_t ? rope_max_pos : -1;
+        if (row_bytes % 16 == 0)
+            copy_range_kernel<uint4><<<grid, 256, 0, stream>>>(kd, vd, ks, vs, len, kv_heads,
+                                                               row_bytes, dst_rows, src_rows,
+                                                               copy_back, rope_rows, S, status);
+        else
+            copy_range_kernel<uint32_t><<<grid, 256, 0, stream>>>(kd, vd, ks, vs, len, kv_heads,
+                                                                  row_bytes, dst_rows, src_rows,
+                                                                  copy_back, rope_rows, S,
+                                                                  status);
+    };
+
+    if (!windowed) {
+        if (phase != KVC_APPEND)
+            return KVC_ERR_UNSUPPORTED;
+        launch_new_rows(kc, vc, C, 0);
+    } else if (S == 1) {
+        if (phase != KVC_APPEND)
+            return KVC_ERR_UNSUPPORTED;
+        dim3 grid(slices, 2);
+        if (vec_ok && (D * sizeof(T)) % 16 == 0)
+            compact_kernel<T, VEC><<<grid, 256, 0, stream>>>(kc, vc, nk, nv, len, kv_heads, D, C,
+                                                             cos_t, sin_t, rope_max_pos, status);
+        else
+            return KVC_ERR_UNSUPPORTED;
+    } else if (phase == KVC_APPEND) {
+        launch_copy(static_cast<char *>(k_stage), static_cast<char *>(v_stage),
+                    reinterpret_cast<const char *>(kc), reinterpret_cast<const char *>(vc), C + S,
+                    C, 0, C);
+        launch_new_rows(static_cast<T *>(k_stage), static_cast<T *>(v_stage), C + S, 1);
+    } else {
+        launch_copy(reinterpret_cast<char *>(kc), reinterpret_cast<char *>(vc),
+                    static_cast<const char *>(k_stage), static_cast<const char *>(v_stage), C,
+                    C + S, 1, C);
+    }
+    return kvc_host::launch_status();
+}
+
+} // namespace
+
+KVC_API kvc_status kvc_seq_lengths(const int32_t *seqlens_k, int batch, int new_tokens,
+                                   int64_t capacity, int windowed, int local_window_size,
+                                   kvc_lengths out, int32_t *dev_status, void *stream)
+{
+    if (batch < 0 || new_tokens < 1)
+        return KVC_ERR_SHAPE;
+    if (capacity < 1 || capacity > (int64_t)INT32_MAX)
+        return KVC_ERR_CAPACITY;
+    if (windowed && (local_window_size <= 0 || local_window_size > capacity))
+        return KVC_ERR_WINDOW;
+    if (batch == 0)
+        return KVC_OK;
+    if (!seqlens_k || !kvc_host::lengths_ok(out))
+        return KVC_ERR_NULL;
+    seq_lengths_kernel<<<(batch + 127) / 128, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+        seqlens_k, batch, new_tokens, capacity, windowed ? 1 : 0, out, dev_status);
+    return kvc_host::launch_status();
+}
+
+KVC_API kvc_status kvc_window_append(void *k_cache, void *v_cache, const void *new_k,
+                                     const void *new_v, void *k_stage, void *v_stage,
+                                     kvc_lengths len, int batch, int kv_heads, int new_tokens,
+                                     int64_t capacity, int head_dim, int dtype, int windowed,
+                                     int phase, const float *rope_cos, const float *rope_sin,
+                                     int64_t rope_max_pos, int32_t *dev_status, void *stream_)
+{
+    const int eb = kvc_host::elem_bytes_of(dtype);
+    if (eb == 0)
+        return KVC_ERR_DTYPE;
+    if (batch < 0 || kv_heads < 1 || new_tokens < 1 || head_dim < 2 || head_dim > 1024 ||
+        (head_dim & 1))
+        return KVC_ERR_SHAPE;
+    if (capacity < 1 || capacity > (int64_t)INT32_MAX)
+        return KVC_ERR_CAPACITY;
+    if (phase != KVC_APPEND && phase != KVC_COPY_BACK)
+        return KVC_ERR_UNSUPPORTED;
+    if ((rope_cos == nullptr) != (rope_sin == nullptr))
+        return KVC_ERR_NULL;
+    if (rope_cos && rope_max_pos < 1)
+        return KVC_ERR_SHAPE;
+    if (batch == 0)
+        return KVC_OK;
+    if (!k_cache || !v_cache || !kvc_host::lengths_ok(len))
+        return KVC_ERR_NULL;
+    const bool staged = windowed && new_tokens > 1;
+    if (phase == KVC_APPEND && (!new_k || !new_v))
+        return KVC_ERR_NULL;
+    if (staged && (!k_stage || !v_stage))
+        return KVC_ERR_NULL;
+    if (phase == KVC_COPY_BACK && !staged)
+        return KVC_ERR_UNSUPPORTED;
+    const size_t cache_bytes = (size_t)batch * kv_heads * capacity * head_dim * eb;
+    if (kvc_host::overlaps(k_cache, cache_bytes, v_cache, cache_bytes))
+        return KVC_ERR_SHAPE;
+    if (staged) {
+        const size_t st = (size_t)batch * kv_heads * (capacity + new_tokens) * head_dim * eb;
+        if (kvc_host::overlaps(k_stage, st, v_stage, st) ||
+            kvc_host::overlaps(k_stage, st, k_cache, cache_bytes) ||
+            kvc_host::overlaps(v_stage, st, v_cache, cache_bytes) ||
+            kvc_host::overlaps(k_stage, st, v_cache, cache_bytes) ||
+            kvc_host::overlaps(v_stage, st, k_cache, cache_bytes))
+            return KVC_ERR_SHAPE;
+    }
+    const void *ptrs[6] = {k_cache, v_cache, new_k, new_v, staged ? k_stage : nullptr,
+                           staged ? v_stage : nullptr};
+    for (const void *p : ptrs)
+        if (p && !kvc_host::aligned16(p))
+            return KVC_ERR_ALIGN;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const int w = windowed ? 1 : 0;
+    switch (dtype) {
+    case KVC_F32:
+        return append_typed<float>(k_cache, v_cache, new_k, new_v, k_stage, v_stage, len, batch,
+                                   kv_heads, new_tokens, capacity, head_dim, w, phase, rope_cos,
+                                   rope_sin, rope_max_pos, dev_status, stream);
+    case KVC_BF16:
+        return append_typed<__nv_bfloat16>(k_cache, v_cache, new_k, new_v, k_stage, v_stage, len,
+                                           batch, kv_heads, new_tokens, capacity, head_dim, w,
+                                           phase, rope_cos, rope_sin, rope_max_pos, dev_status,
+                                           stream);
+    default:
+        return append_typed<__half>(k_cache, v_cache, new_k, new_v, k_stage, v_stage, len, batch,
+                                    kv_heads, new_tokens, capacity, head_dim, w, phase, rope_cos,
+                                    rope_sin, rope_max_pos, dev_status, stream);
+    }
+}

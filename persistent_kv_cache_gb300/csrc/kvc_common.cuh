@@ -1,0 +1,204 @@
+// kvc_common.cuh -- shared device/host helpers of the GB300 KV-cache library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvc.h"
+
+#define KVC_API extern "C" __attribute__((visibility("default")))
+
+namespace kvc {
+
+// --------------------------------------------------------------------------
+// status reporting
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ void raise_status(int32_t *st, uint32_t bit)
+{
+    if (st)
+        atomicOr(reinterpret_cast<int *>(st), (int)bit);
+}
+
+// a wait gives up after this many nanoseconds of %globaltimer
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// --------------------------------------------------------------------------
+// element types
+// --------------------------------------------------------------------------
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static __device__ __forceinline__ float to_f32(float x) { return x; }
+    static __device__ __forceinline__ float from_f32(float x) { return x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+    static __device__ __forceinline__ __nv_bfloat16 from_f32(float x) { return __float2bfloat16_rn(x); }
+};
+template <> struct Elem<__half> {
+    static __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+    static __device__ __forceinline__ __half from_f32(float x) { return __float2half_rn(x); }
+};
+
+// rotate-half RoPE of one pair, every product and sum rounded separately
+// (no fused multiply-add), so that the stored row is reproducible bit for bit
+__device__ __forceinline__ void rope_pair(float &lo, float &hi, float c, float s)
+{
+    float lo_c = __fmul_rn(lo, c);
+    float hi_s = __fmul_rn(hi, s);
+    float hi_c = __fmul_rn(hi, c);
+    float lo_s = __fmul_rn(lo, s);
+    lo = __fsub_rn(lo_c, hi_s);
+    hi = __fadd_rn(hi_c, lo_s);
+}
+
+// --------------------------------------------------------------------------
+// shared-memory barriers and TMA (inline PTX)
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity; returns false after about one
+// second (the caller records KVC_DEV_TIMEOUT and winds down).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    uint64_t t0 = global_ns();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((i & 255u) == 255u && global_ns() - t0 > kWaitLimitNs)
+            return false;
+    }
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 2-D tiled TMA load of one box into shared memory, completing on `bar`.
+// x (innermost, elements) must keep x * elem_size a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, int32_t x,
+                                            int32_t y, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// byte offset of 16-byte chunk `c` (0..7) of row `r` inside a box written by
+// TMA with 128-byte swizzle (rows of 128 bytes, 1024-byte aligned box)
+__device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c)
+{
+    return r * 128u + ((c ^ (r & 7u)) << 4);
+}
+
+} // namespace kvc
+
+// --------------------------------------------------------------------------
+// host helpers
+// --------------------------------------------------------------------------
+namespace kvc_host {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// [a, a + na) and [b, b + nb) share at least one byte
+inline bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+inline int elem_bytes_of(int dtype)
+{
+    return dtype == KVC_F32 ? 4 : (dtype == KVC_BF16 || dtype == KVC_F16) ? 2 : 0;
+}
+
+inline kvc_status launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+}
+
+inline bool lengths_ok(const kvc_lengths &l)
+{
+    return l.past_abs && l.total_abs && l.cache_past && l.cache_total && l.evict;
+}
+
+// number of SMs of the current device (cached per device)
+int sm_count();
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point
+// (no link-time dependency on libcuda)
+bool encode_2d_bf16_sw128(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                          uint32_t box_rows, CUtensorMapDataType type);
+
+} // namespace kvc_host
+
+// fp32 attention on CUDA cores (kvc_decode.cu); n_rows_mode 0 attends over
+// rows [0, cache_total) with S = 1, mode 1 over rows [0, cache_past + S)
+namespace kvc_f32 {
+kvc_status launch(void *out, const void *q, const void *k_rows, const void *v_rows,
+                  int64_t rows_per_head, const kvc_lengths &len, int batch, int q_heads,
+                  int kv_heads, int S, int D, int window, float scale, const float *cos_t,
+                  const float *sin_t, int64_t rope_max_pos, int n_rows_mode, int32_t *status,
+                  cudaStream_t stream);
+}

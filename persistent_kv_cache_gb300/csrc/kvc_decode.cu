@@ -1,0 +1,695 @@
+// kvc_decode.cu -- one-token grouped-query attention over the persistent cache
+// ("Persistent KV Cache and Decode Performance Roadmap", section "Phase 1":
+// stream KV blocks, update the online-softmax state, accumulate V, never store
+// the score vector; heads that share a KV head read each block once; one
+// query row may be split across workers when the outer dimensions cannot fill
+// the machine, with an (m, l, o) merge.  Masks and cache-relative addressing
+// from "GQA support sliding_window_cache", section "Design").
+//
+// 16-bit path (bf16 / fp16), one CTA per (split, kv head, batch row):
+//   * warp 4 is the producer: one lane issues 2-D TMA loads of 64-row K and V
+//     tiles (128-byte swizzled boxes of 64 columns) into an NS-stage ring of
+//     shared-memory buffers guarded by full/empty mbarriers;
+//   * warps 0-3 consume 16 rows of every tile each: S = Q K^T and O += P V on
+//     the tensor cores (mma.sync m16n8k16, fp32 accumulate) with the GQA group's
+//     query heads as the M dimension, online softmax in registers with quad
+//     shuffles, then a 4-way (m, l, o) merge through shared memory;
+//   * a split whose row holds more than one split writes (m, l, o) partials to
+//     the workspace and decode_combine_kernel merges them; a single split
+//     writes the output directly.
+// fp32 path: attn_f32_kernel, one warp per query row on CUDA cores (also used
+// by the multi-token call for fp32).
+#include <type_traits>
+
+#include "kvc_common.cuh"
+
+namespace {
+
+constexpr int kTile = 64;      // cache rows per TMA tile
+constexpr int kConsumers = 4;  // consumer warps
+constexpr float kLog2e = 1.4426950408889634f;
+
+__host__ __device__ constexpr int decode_stages(int D) { return D >= 128 ? 3 : 4; }
+
+// rows handled by one CTA (a multiple of the tile); shared by the kernel launch
+// and the workspace size so both agree
+inline int64_t decode_split_rows(int64_t C)
+{
+    if (C >= 2048)
+        return 512;
+    return (C + kTile - 1) / kTile * kTile;
+}
+inline int64_t decode_max_splits(int64_t C)
+{
+    const int64_t sr = decode_split_rows(C);
+    return (C + sr - 1) / sr;
+}
+
+template <typename T> struct Mma;
+template <> struct Mma<__nv_bfloat16> {
+    static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1)
+    {
+        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                     "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                     : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                     : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi)
+    {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&v);
+    }
+};
+template <> struct Mma<__half> {
+    static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1)
+    {
+        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+                     "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                     : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                     : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi)
+    {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&v);
+    }
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                          uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+struct DecodeArgs {
+    void *out;
+    const void *q;
+    kvc_lengths len;
+    int q_heads, kv_heads, group;
+    int64_t capacity;
+    int window;
+    float scale_log2;
+    const float *cos_t, *sin_t;
+    int64_t rope_max_pos;
+    float *ws_o, *ws_m, *ws_l;
+    int64_t split_rows;
+    int max_splits;
+    int32_t *status;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(160)
+decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                    const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a)
+{
+    constexpr int NS = decode_stages(D);
+    constexpr int BOXES = D / 64;
+    constexpr int KT_BYTES = kTile * D * 2;  // one K (or V) tile
+    constexpr int STAGE_BYTES = 2 * KT_BYTES;
+    constexpr int QS = D + 8;                // padded Q row (elements)
+    constexpr int NB = D / 8;                // n-blocks of the output
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *stages = smem;
+    T *qs = reinterpret_cast<T *>(smem + NS * STAGE_BYTES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * STAGE_BYTES + 16 * QS * 2);
+    uint64_t *empty = full + NS;
+    int *abort_flag = reinterpret_cast<int *>(empty + NS);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int L = a.len.cache_total[b];
+    if (L <= 0)
+        return;
+    if ((int64_t)L > a.capacity) {
+        // lengths computed for another capacity: refuse rather than overrun
+        if (threadIdx.x == 0 && split == 0 && kvh == 0)
+            kvc::raise_status(a.status, KVC_DEV_CAPACITY);
+        return;
+    }
+    const int tot = a.len.total_abs[b];
+    if (a.cos_t && (int64_t)tot > a.rope_max_pos) {
+        if (threadIdx.x == 0 && split == 0 && kvh == 0)
+            kvc::raise_status(a.status, KVC_DEV_ROPE_RANGE);
+        return;
+    }
+    const int vis0 = (a.window > 0 && L > a.window) ? L - a.window : 0;
+    const int vis = L - vis0;
+    const int nsplit = (int)((vis + a.split_rows - 1) / a.split_rows);
+    if (split >= nsplit)
+        return;
+    const int r0 = vis0 + (int)(split * a.split_rows);
+    const int r1 = min((int64_t)L, (int64_t)r0 + a.split_rows);
+    const int ntiles = (r1 - r0 + kTile - 1) / kTile;
+    const int64_t row_base = ((int64_t)b * a.kv_heads + kvh) * a.capacity;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            kvc::mbar_init(&full[s], 1);
+            kvc::mbar_init(&empty[s], kConsumers);
+        }
+        *abort_flag = 0;
+        kvc::fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumers) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            kvc::tma_prefetch_desc(&tmap_k);
+            kvc::tma_prefetch_desc(&tmap_v);
+            for (int t = 0; t < ntiles; ++t) {
+                const int s = t % NS, k = t / NS;
+                if (t >= NS && !kvc::mbar_wait(&empty[s], (k - 1) & 1)) {
+                    kvc::raise_status(a.status, KVC_DEV_TIMEOUT);
+                    break;
+                }
+                if (*reinterpret_cast<volatile int *>(abort_flag))
+                    break;
+                uint8_t *kb = stages + s * STAGE_BYTES;
+                uint8_t *vb = kb + KT_BYTES;
+                kvc::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+                const int32_t y = (int32_t)(row_base + r0 + t * kTile);
+#pragma unroll
+                for (int bx = 0; bx < BOXES; ++bx) {
+                    kvc::tma_load_2d(kb + bx * 8192, &tmap_k, bx * 64, y, &full[s]);
+                    kvc::tma_load_2d(vb + bx * 8192, &tmap_v, bx * 64, y, &full[s]);
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    const int g = a.group;
+    {
+        // rotated query rows of the group (rows >= g stay zero)
+        const T *qg = static_cast<const T *>(a.q) + ((int64_t)b * a.q_heads + kvh * g) * D;
+        const float *cs = a.cos_t ? a.cos_t + (int64_t)(tot - 1) * (D / 2) : nullptr;
+        const float *sn = a.cos_t ? a.sin_t + (int64_t)(tot - 1) * (D / 2) : nullptr;
+        for (int idx = threadIdx.x; idx < 16 * (D / 2); idx += 128) {
+            const int h = idx / (D / 2), i = idx % (D / 2);
+            float lo = 0.f, hi = 0.f;
+            if (h < g) {
+                lo = kvc::Elem<T>::to_f32(qg[h * D + i]);
+                hi = kvc::Elem<T>::to_f32(qg[h * D + i + D / 2]);
+                if (cs)
+                    kvc::rope_pair(lo, hi, cs[i], sn[i]);
+            }
+            qs[h * QS + i] = kvc::Elem<T>::from_f32(lo);
+            qs[h * QS + i + D / 2] = kvc::Elem<T>::from_f32(hi);
+        }
+    }
+    consumer_sync();
+    uint32_t qa[D / 16][4];
+    {
+        const int row = lane >> 2, col = (lane & 3) * 2;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            qa[kk][0] = *reinterpret_cast<const uint32_t *>(&qs[row * QS + kk * 16 + col]);
+            qa[kk][1] = *reinterpret_cast<const uint32_t *>(&qs[(row + 8) * QS + kk * 16 + col]);
+            qa[kk][2] = *reinterpret_cast<const uint32_t *>(&qs[row * QS + kk * 16 + 8 + col]);
+            qa[kk][3] =
+                *reinterpret_cast<const uint32_t *>(&qs[(row + 8) * QS + kk * 16 + 8 + col]);
+        }
+    }
+
+    float o[NB][4];
+#pragma unroll
+    for (int n = 0; n < NB; ++n)
+        o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+    bool timed_out = false;
+
+    for (int t = 0; t < ntiles; ++t) {
+        const int s = t % NS, k = t / NS;
+        if (!kvc::mbar_wait(&full[s], k & 1)) {
+            timed_out = true;
+            break;
+        }
+        const uint32_t kb = kvc::smem_u32(stages + s * STAGE_BYTES);
+        const uint32_t vb = kb + KT_BYTES;
+        const int tile_r0 = r0 + t * kTile;
+        const int my_valid = min(16, max(0, r1 - tile_r0 - 16 * warp));
+        if (my_valid > 0) {
+            if (my_valid < 16) {
+                // rows past the split end: zero V so that 0 * garbage stays 0
+                uint8_t *vgen = stages + s * STAGE_BYTES + KT_BYTES;
+                for (int idx = lane; idx < (16 - my_valid) * BOXES * 8; idx += 32) {
+                    const int rr = 16 * warp + my_valid + idx / (BOXES * 8);
+                    const int bx = (idx / 8) % BOXES, c = idx % 8;
+                    *reinterpret_cast<uint4 *>(vgen + bx * 8192 + rr * 128 + c * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+            // S = Q K^T over this warp's 16 rows
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            const int mat = lane >> 3;
+            const int krow = 16 * warp + ((mat >> 1) << 3) + (lane & 7);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int cidx = 2 * kk + (mat & 1);
+                uint32_t r_0, r_1, r_2, r_3;
+                ldsm_x4(kb + (cidx >> 3) * 8192 + kvc::sw128(krow, cidx & 7), r_0, r_1, r_2, r_3);
+                Mma<T>::run(sc[0], qa[kk], r_0, r_1);
+                Mma<T>::run(sc[1], qa[kk], r_2, r_3);
+            }
+            // online softmax (log2 domain); columns >= my_valid are masked
+            float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int col = 8 * j + 2 * (lane & 3) + (e & 1);
+                    float v = sc[j][e] * a.scale_log2;
+                    v = col < my_valid ? v : -INFINITY;
+                    sc[j][e] = v;
+                    if (e < 2)
+                        mx_lo = fmaxf(mx_lo, v);
+                    else
+                        mx_hi = fmaxf(mx_hi, v);
+                }
+            mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+            mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+            mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+            mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+            const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+            const float al_lo = exp2f(m_lo - mn_lo), al_hi = exp2f(m_hi - mn_hi);
+            m_lo = mn_lo;
+            m_hi = mn_hi;
+            float ps_lo = 0.f, ps_hi = 0.f;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                sc[j][0] = exp2f(sc[j][0] - mn_lo);
+                sc[j][1] = exp2f(sc[j][1] - mn_lo);
+                sc[j][2] = exp2f(sc[j][2] - mn_hi);
+                sc[j][3] = exp2f(sc[j][3] - mn_hi);
+                ps_lo += sc[j][0] + sc[j][1];
+                ps_hi += sc[j][2] + sc[j][3];
+            }
+            l_lo = l_lo * al_lo + ps_lo;
+            l_hi = l_hi * al_hi + ps_hi;
+#pragma unroll
+            for (int n = 0; n < NB; ++n) {
+                o[n][0] *= al_lo;
+                o[n][1] *= al_lo;
+                o[n][2] *= al_hi;
+                o[n][3] *= al_hi;
+            }
+            uint32_t pa[4];
+            pa[0] = Mma<T>::pack(sc[0][0], sc[0][1]);
+            pa[1] = Mma<T>::pack(sc[0][2], sc[0][3]);
+            pa[2] = Mma<T>::pack(sc[1][0], sc[1][1]);
+            pa[3] = Mma<T>::pack(sc[1][2], sc[1][3]);
+            // O += P V over this warp's 16 rows
+            const int vrow = 16 * warp + ((mat & 1) << 3) + (lane & 7);
+#pragma unroll
+            for (int nn = 0; nn < D / 16; ++nn) {
+                const int cidx = 2 * nn + (mat >> 1);
+                uint32_t r_0, r_1, r_2, r_3;
+                ldsm_x4_t(vb + (cidx >> 3) * 8192 + kvc::sw128(vrow, cidx & 7), r_0, r_1, r_2,
+                          r_3);
+                Mma<T>::run(o[2 * nn], pa, r_0, r_1);
+                Mma<T>::run(o[2 * nn + 1], pa, r_2, r_3);
+            }
+        }
+        if (my_valid > 0 && my_valid < 16)
+            kvc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+            kvc::mbar_arrive(&empty[s]);
+    }
+    if (timed_out) {
+        if (lane == 0) {
+            kvc::raise_status(a.status, KVC_DEV_TIMEOUT);
+            atomicExch(abort_flag, 1);
+        }
+    }
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+
+    // ---- merge the four warps' (m, l, o) through shared memory ----
+    consumer_sync();  // every warp is done with the stage buffers
+    float *cm = reinterpret_cast<float *>(stages);        // [4][16]
+    float *cl = cm + kConsumers * 16;                      // [4][16]
+    float *co = cl + kConsumers * 16;                      // [4][16][D]
+    {
+        const int row = lane >> 2, col = 2 * (lane & 3);
+        if ((lane & 3) == 0) {
+            cm[warp * 16 + row] = m_lo;
+            cl[warp * 16 + row] = l_lo;
+            cm[warp * 16 + row + 8] = m_hi;
+            cl[warp * 16 + row + 8] = l_hi;
+        }
+#pragma unroll
+        for (int n = 0; n < NB; ++n) {
+            if (row < g) {
+                co[(warp * 16 + row) * D + 8 * n + col] = o[n][0];
+                co[(warp * 16 + row) * D + 8 * n + col + 1] = o[n][1];
+            }
+            if (row + 8 < g) {
+                co[(warp * 16 + row + 8) * D + 8 * n + col] = o[n][2];
+                co[(warp * 16 + row + 8) * D + 8 * n + col + 1] = o[n][3];
+            }
+        }
+    }
+    consumer_sync();
+    const int hq0 = kvh * g;
+    for (int idx = threadIdx.x; idx < g * D; idx += 128) {
+        const int h = idx / D, d = idx % D;
+        float mstar = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w)
+            mstar = fmaxf(mstar, cm[w * 16 + h]);
+        float lsum = 0.f, osum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w) {
+            const float f = exp2f(cm[w * 16 + h] - mstar);
+            lsum += cl[w * 16 + h] * f;
+            osum += co[(w * 16 + h) * D + d] * f;
+        }
+        const int64_t qrow = (int64_t)b * a.q_heads + hq0 + h;
+        if (nsplit == 1) {
+            static_cast<T *>(a.out)[qrow * D + d] = kvc::Elem<T>::from_f32(osum / lsum);
+        } else {
+            const int64_t pr = qrow * a.max_splits + split;
+            a.ws_o[pr * D + d] = osum;
+            if (d == 0) {
+                a.ws_m[pr] = mstar;
+                a.ws_l[pr] = lsum;
+            }
+        }
+    }
+}
+
+// merges the per-split partials of rows that used more than one split
+template <typename T>
+__global__ void __launch_bounds__(128)
+decode_combine_kernel(const DecodeArgs a, int D)
+{
+    extern __shared__ float wsh[];  // [max_splits] weights
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int L = a.len.cache_total[b];
+    if (L <= 0 || (int64_t)L > a.capacity)
+        return;
+    const int tot = a.len.total_abs[b];
+    if (a.cos_t && (int64_t)tot > a.rope_max_pos)
+        return;
+    const int vis0 = (a.window > 0 && L > a.window) ? L - a.window : 0;
+    const int nsplit = (int)((L - vis0 + a.split_rows - 1) / a.split_rows);
+    if (nsplit <= 1)
+        return;
+    const int64_t qrow = (int64_t)b * a.q_heads + h;
+    const int64_t p0 = qrow * a.max_splits;
+    float mstar = -INFINITY;
+    for (int j = 0; j < nsplit; ++j)
+        mstar = fmaxf(mstar, a.ws_m[p0 + j]);
+    float lsum = 0.f;
+    for (int j = threadIdx.x; j < nsplit; j += blockDim.x)
+        wsh[j] = exp2f(a.ws_m[p0 + j] - mstar);
+    __syncthreads();
+    for (int j = 0; j < nsplit; ++j)
+        lsum += a.ws_l[p0 + j] * wsh[j];
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        float acc = 0.f;
+        for (int j = 0; j < nsplit; ++j)
+            acc += a.ws_o[(p0 + j) * D + d] * wsh[j];
+        static_cast<T *>(a.out)[qrow * D + d] = kvc::Elem<T>::from_f32(acc / lsum);
+    }
+}
+
+} // namespace
+
+// --------------------------------------------------------------------------
+// fp32 attention on CUDA cores (decode and multi-token), one warp per query
+// --------------------------------------------------------------------------
+namespace kvc_f32 {
+
+// n_rows_mode 0: rows [0, cache_total) (decode); 1: rows [0, cache_past + S)
+// (multi-token chunk over staged or contiguous rows)
+__global__ void __launch_bounds__(128)
+attn_f32_kernel(float *__restrict__ out, const float *__restrict__ q,
+                const float *__restrict__ k_rows, const float *__restrict__ v_rows,
+                int64_t rows_per_head, kvc_lengths len, int batch, int q_heads, int kv_heads,
+                int S, int D, int window, float scale, const float *__restrict__ cos_t,
+                const float *__restrict__ sin_t, int64_t rope_max_pos, int n_rows_mode,
+                int32_t *status)
+{
+    extern __shared__ float qsh[];  // [4][D]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t qrow = (int64_t)blockIdx.x * 4 + warp;  // over (b, h, i)
+    if (qrow >= (int64_t)batch * q_heads * S)
+        return;
+    const int i = (int)(qrow % S);
+    const int h = (int)((qrow / S) % q_heads);
+    const int b = (int)(qrow / ((int64_t)S * q_heads));
+    const int L = len.cache_total[b];
+    if (L < 0)
+        return;
+    const int64_t T = len.total_abs[b];
+    if (cos_t && T > rope_max_pos) {
+        if (lane == 0 && h == 0 && i == 0)
+            kvc::raise_status(status, KVC_DEV_ROPE_RANGE);
+        return;
+    }
+    const int64_t n = n_rows_mode == 0 ? L : (int64_t)len.cache_past[b] + S;
+    if (n > rows_per_head || n < S) {
+        if (lane == 0 && h == 0 && i == 0)
+            kvc::raise_status(status, KVC_DEV_CAPACITY);
+        return;
+    }
+    const int64_t first_pos = T - n;
+    const int64_t qpos = T - S + i;
+    float *qv = qsh + warp * D;
+    const float *qsrc = q + qrow * D;
+    for (int d = lane; d < D / 2; d += 32) {
+        float lo = qsrc[d], hi = qsrc[d + D / 2];
+        if (cos_t)
+            kvc::rope_pair(lo, hi, cos_t[qpos * (D / 2) + d], sin_t[qpos * (D / 2) + d]);
+        qv[d] = lo;
+        qv[d + D / 2] = hi;
+    }
+    __syncwarp();
+    // visible rows: kpos in [qpos - window + 1, qpos], row r holds first_pos + r
+    int64_t lo_r = 0, hi_r = qpos - first_pos;  // inclusive
+    if (window > 0 && qpos - window + 1 - first_pos > lo_r)
+        lo_r = qpos - window + 1 - first_pos;
+    if (hi_r > n - 1)
+        hi_r = n - 1;
+    const int kvh = h / (q_heads / kv_heads);
+    const float *kb = k_rows + ((int64_t)b * kv_heads + kvh) * rows_per_head * D;
+    const float *vb = v_rows + ((int64_t)b * kv_heads + kvh) * rows_per_head * D;
+    float m = -INFINITY;
+    for (int64_t r = lo_r + lane; r <= hi_r; r += 32) {
+        float dot = 0.f;
+        for (int d = 0; d < D; ++d)
+            dot += qv[d] * kb[r * D + d];
+        m = fmaxf(m, dot * scale);
+    }
+    for (int off = 16; off > 0; off >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // d = lane + 32 j, D <= 256
+    float l = 0.f;
+    for (int64_t c0 = lo_r; c0 <= hi_r; c0 += 32) {
+        const int64_t r = c0 + lane;
+        float p = 0.f;
+        if (r <= hi_r) {
+            float dot = 0.f;
+            for (int d = 0; d < D; ++d)
+                dot += qv[d] * kb[r * D + d];
+            p = expf(dot * scale - m);
+        }
+        l += p;
+        const int cnt = (int)min((int64_t)32, hi_r - c0 + 1);
+        for (int j = 0; j < cnt; ++j) {
+            const float pj = __shfl_sync(0xffffffffu, p, j);
+            const float *vr = vb + (c0 + j) * D;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (lane + 32 * u < D)
+                    acc[u] += pj * vr[lane + 32 * u];
+        }
+    }
+    for (int off = 16; off > 0; off >>= 1)
+        l += __shfl_xor_sync(0xffffffffu, l, off);
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+        if (lane + 32 * u < D)
+            out[qrow * D + lane + 32 * u] = acc[u] / l;
+}
+
+kvc_status launch(void *out, const void *q, const void *k_rows, const void *v_rows,
+                  int64_t rows_per_head, const kvc_lengths &len, int batch, int q_heads,
+                  int kv_heads, int S, int D, int window, float scale, const float *cos_t,
+                  const float *sin_t, int64_t rope_max_pos, int n_rows_mode, int32_t *status,
+                  cudaStream_t stream)
+{
+    const int64_t rows = (int64_t)batch * q_heads * S;
+    const int64_t blocks = (rows + 3) / 4;
+    if (blocks > INT32_MAX)
+        return KVC_ERR_SHAPE;
+    attn_f32_kernel<<<(unsigned)blocks, 128, 4 * D * sizeof(float), stream>>>(
+        static_cast<float *>(out), static_cast<const float *>(q),
+        static_cast<const float *>(k_rows), static_cast<const float *>(v_rows), rows_per_head, len,
+        batch, q_heads, kv_heads, S, D, window, scale, cos_t, sin_t, rope_max_pos, n_rows_mode,
+        status);
+    return kvc_host::launch_status();
+}
+
+} // namespace kvc_f32
+
+namespace {
+
+template <typename T, int D>
+kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const void *v_cache,
+                           const kvc_lengths &len, int batch, int q_heads, int kv_heads,
+                           int64_t C, int window, float scale, const float *cos_t,
+                           const float *sin_t, int64_t rope_max_pos, void *workspace,
+                           int32_t *status, cudaStream_t stream)
+{
+    constexpr int NS = decode_stages(D);
+    const CUtensorMapDataType tt = std::is_same<T, __half>::value
+                                       ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap tk, tv;
+    const uint64_t rows = (uint64_t)batch * kv_heads * C;
+    if (rows > (uint64_t)INT32_MAX)
+        return KVC_ERR_SHAPE;
+    if (!kvc_host::encode_2d_bf16_sw128(&tk, k_cache, rows, D, kTile, tt) ||
+        !kvc_host::encode_2d_bf16_sw128(&tv, v_cache, rows, D, kTile, tt))
+        return KVC_ERR_CUDA;
+    DecodeArgs a;
+    a.out = out;
+    a.q = q;
+    a.len = len;
+    a.q_heads = q_heads;
+    a.kv_heads = kv_heads;
+    a.group = q_heads / kv_heads;
+    a.capacity = C;
+    a.window = window;
+    a.scale_log2 = scale * kLog2e;
+    a.cos_t = cos_t;
+    a.sin_t = sin_t;
+    a.rope_max_pos = rope_max_pos;
+    a.split_rows = decode_split_rows(C);
+    a.max_splits = (int)decode_max_splits(C);
+    const int64_t np = (int64_t)batch * q_heads * a.max_splits;
+    a.ws_o = static_cast<float *>(workspace);
+    a.ws_m = a.ws_o + np * D;
+    a.ws_l = a.ws_m + np;
+    a.status = status;
+    const size_t smem = 1024 + (size_t)NS * 2 * kTile * D * 2 + 16 * (D + 8) * 2 +
+                        2 * NS * sizeof(uint64_t) + 16;
+    auto kern = decode_split_kernel<T, D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return KVC_ERR_CUDA;
+    dim3 grid(a.max_splits, kv_heads, batch);
+    kern<<<grid, 160, smem, stream>>>(tk, tv, a);
+    if (a.max_splits > 1) {
+        dim3 g2(q_heads, batch);
+        decode_combine_kernel<T><<<g2, 128, a.max_splits * sizeof(float), stream>>>(a, D);
+    }
+    return kvc_host::launch_status();
+}
+
+template <typename T>
+kvc_status dispatch_decode16(int D, void *out, const void *q, const void *k, const void *v,
+                             const kvc_lengths &len, int B, int Hq, int Hkv, int64_t C, int W,
+                             float scale, const float *cs, const float *sn, int64_t rmax,
+                             void *ws, int32_t *st, cudaStream_t stream)
+{
+    if (D == 64)
+        return launch_decode16<T, 64>(out, q, k, v, len, B, Hq, Hkv, C, W, scale, cs, sn, rmax,
+                                      ws, st, stream);
+    if (D == 128)
+        return launch_decode16<T, 128>(out, q, k, v, len, B, Hq, Hkv, C, W, scale, cs, sn, rmax,
+                                       ws, st, stream);
+    return KVC_ERR_UNSUPPORTED;
+}
+
+} // namespace
+
+KVC_API size_t kvc_gqa_decode_workspace_size(int batch, int q_heads, int kv_heads,
+                                             int64_t capacity, int head_dim, int dtype)
+{
+    if (batch < 0 || q_heads < 1 || kv_heads < 1 || capacity < 1 || head_dim < 1)
+        return 0;
+    if (dtype == KVC_F32)
+        return 256;  // the CUDA-core path keeps everything on chip
+    const int64_t ns = decode_max_splits(capacity);
+    if (ns <= 1)
+        return 256;
+    const int64_t np = (int64_t)batch * q_heads * ns;
+    return (size_t)(np * (head_dim + 2) * sizeof(float));
+}
+
+KVC_API kvc_status kvc_gqa_decode(void *out, const void *q, const void *k_cache,
+                                  const void *v_cache, kvc_lengths len, int batch, int q_heads,
+                                  int kv_heads, int64_t capacity, int head_dim, int dtype,
+                                  int local_window_size, float scale, const float *rope_cos,
+                                  const float *rope_sin, int64_t rope_max_pos, void *workspace,
+                                  size_t workspace_bytes, int32_t *dev_status, void *stream_)
+{
+    const int eb = kvc_host::elem_bytes_of(dtype);
+    if (eb == 0)
+        return KVC_ERR_DTYPE;
+    if (batch < 0 || q_heads < 1 || kv_heads < 1 || q_heads % kv_heads != 0 || head_dim < 2 ||
+        (head_dim & 1))
+        return KVC_ERR_SHAPE;
+    if (capacity < 1 || capacity > (int64_t)INT32_MAX)
+        return KVC_ERR_CAPACITY;
+    if ((rope_cos == nullptr) != (rope_sin == nullptr))
+        return KVC_ERR_NULL;
+    if (rope_cos && rope_max_pos < 1)
+        return KVC_ERR_SHAPE;
+    const int g = q_heads / kv_heads;
+    if (dtype == KVC_F32 ? head_dim > 256 : ((head_dim != 64 && head_dim != 128) || g > 16))
+        return KVC_ERR_UNSUPPORTED;
+    if (batch == 0)
+        return KVC_OK;
+    if (!out || !q || !k_cache || !v_cache || !kvc_host::lengths_ok(len))
+        return KVC_ERR_NULL;
+    for (const void *p : {(const void *)out, q, k_cache, v_cache})
+        if (!kvc_host::aligned16(p))
+            return KVC_ERR_ALIGN;
+    const size_t need =
+        kvc_gqa_decode_workspace_size(batch, q_heads, kv_heads, capacity, head_dim, dtype);
+    if (need > 256 && (!workspace || workspace_bytes < need))
+        return KVC_ERR_WORKSPACE;
+    if (need > 256 && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return KVC_ERR_ALIGN;
+    if (scale == 0.f)
+        scale = 1.0f / sqrtf((float)head_dim);
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (dtype == KVC_F32)
+        return kvc_f32::launch(out, q, k_cache, v_cache, capacity, len, batch, q_heads, kv_heads,
+                               1, head_dim, local_window_size, scale, rope_cos, rope_sin,
+                               rope_max_pos, 0, dev_status, stream);
+    if (dtype == KVC_BF16)
+        return dispatch_decode16<__nv_bfloat16>(head_dim, out, q, k_cache, v_cache, len, batch,
+                                                q_heads, kv_heads, capacity, local_window_size,
+                                                scale, rope_cos, rope_sin, rope_max_pos,
+                                                workspace, dev_status, stream);
+    return dispatch_decode16<__half>(head_dim, out, q, k_cache, v_cache, len, batch, q_heads,
+                                     kv_heads, capacity, local_window_size, scale, rope_cos,
+                                     rope_sin, rope_max_pos, workspace, dev_status, stream);
+}

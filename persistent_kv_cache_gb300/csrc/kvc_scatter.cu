@@ -1,0 +1,241 @@
+// kvc_scatter.cu -- ONNX TensorScatter ("TensorScatter" operator page,
+// ai.onnx opset 24: spec and pseudocode), plus the library's shared host
+// helpers (status strings, SM count, tensor-map encoding).
+//
+// In place (present == past) only the S updated rows of every prefix move:
+// one warp copies one trailing slice ("row") with the widest vector the
+// alignment allows.  The functional form first copies past -> present with a
+// bandwidth-bound vector copy, then runs the same in-place scatter on present.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kvc_common.cuh"
+
+namespace {
+
+template <typename V>
+__global__ void __launch_bounds__(256)
+scatter_rows_kernel(char *__restrict__ present, const char *__restrict__ update,
+                    const int64_t *__restrict__ write_indices, int64_t n_prefix,
+                    int64_t prefixes_per_batch, int64_t max_seq, int64_t seq_len,
+                    int64_t row_vecs, int circular, int32_t *status)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t n_rows = n_prefix * seq_len;
+    for (int64_t row = warp; row < n_rows; row += n_warps) {
+        const int64_t p = row / seq_len;
+        const int64_t s = row - p * seq_len;
+        const int64_t b = p / prefixes_per_batch;
+        const int64_t wi = write_indices ? write_indices[b] : 0;
+        int64_t idx = wi + s;
+        if (circular) {
+            idx %= max_seq;
+            if (idx < 0)
+                idx += max_seq;
+        } else if (wi < 0 || wi + seq_len > max_seq) {
+            if (lane == 0 && s == 0 && p == b * prefixes_per_batch)
+                kvc::raise_status(status, KVC_DEV_INDEX_OOB);
+            continue;
+        }
+        V *dst = reinterpret_cast<V *>(present) + (p * max_seq + idx) * row_vecs;
+        const V *src = reinterpret_cast<const V *>(update) + row * row_vecs;
+        for (int64_t c = lane; c < row_vecs; c += 32)
+            dst[c] = src[c];
+    }
+}
+
+// dst[i] = src[i] for i < n (16-byte vectors, four in flight per thread)
+__global__ void __launch_bounds__(256)
+copy_vec16_kernel(uint4 *__restrict__ dst, const uint4 *__restrict__ src, int64_t n)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n; i += 4 * stride) {
+        uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
+        dst[i] = a;
+        dst[i + stride] = b;
+        dst[i + 2 * stride] = c;
+        dst[i + 3 * stride] = d;
+    }
+    for (; i < n; i += stride)
+        dst[i] = src[i];
+}
+
+__global__ void copy_bytes_kernel(char *__restrict__ dst, const char *__restrict__ src, int64_t n)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+        dst[i] = src[i];
+}
+
+template <typename V>
+void launch_scatter(char *present, const char *update, const int64_t *wi, int64_t n_prefix,
+                    int64_t ppb, int64_t max_seq, int64_t S, int64_t slice_bytes, int circular,
+                    int32_t *status, cudaStream_t stream)
+{
+    const int64_t rows = n_prefix * S;
+    const int64_t warps_needed = rows;
+    int64_t blocks = (warps_needed + 7) / 8;
+    const int64_t cap = (int64_t)kvc_host::sm_count() * 16;
+    if (blocks > cap)
+        blocks = cap;
+    if (blocks < 1)
+        blocks = 1;
+    scatter_rows_kernel<V><<<(unsigned)blocks, 256, 0, stream>>>(
+        present, update, wi, n_prefix, ppb, max_seq, S, slice_bytes / (int64_t)sizeof(V),
+        circular, status);
+}
+
+} // namespace
+
+namespace kvc_host {
+
+int sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 148;
+    if (cached[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 148;
+    }
+    return cached[dev];
+}
+
+bool encode_2d_bf16_sw128(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                          uint32_t box_rows, CUtensorMapDataType type)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, type, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+} // namespace kvc_host
+
+KVC_API kvc_status kvc_tensor_scatter(void *present_cache, const void *past_cache,
+                                      const void *update, const int64_t *write_indices, int rank,
+                                      const int64_t *cache_shape, int64_t update_seq_len,
+                                      int axis, int mode, int elem_bytes, int32_t *dev_status,
+                                      void *stream_)
+{
+    if (!present_cache || !past_cache || !cache_shape)
+        return KVC_ERR_NULL;
+    if (rank < 2 || rank > 8)
+        return KVC_ERR_SHAPE;
+    if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)
+        return KVC_ERR_DTYPE;
+    if (mode != KVC_LINEAR && mode != KVC_CIRCULAR)
+        return KVC_ERR_UNSUPPORTED;
+    if (axis < 0)
+        axis += rank;
+    if (axis <= 0 || axis >= rank)
+        return KVC_ERR_SHAPE;
+    int64_t n_elems = 1, n_prefix = 1, slice = elem_bytes;
+    for (int d = 0; d < rank; ++d) {
+        if (cache_shape[d] < 0)
+            return KVC_ERR_SHAPE;
+        n_elems *= cache_shape[d];
+        if (d < axis)
+            n_prefix *= cache_shape[d];
+        if (d > axis)
+            slice *= cache_shape[d];
+    }
+    const int64_t max_seq = cache_shape[axis];
+    if (update_seq_len < 0 || update_seq_len > max_seq)
+        return KVC_ERR_SHAPE;
+    if (update_seq_len > 0 && !update)
+        return KVC_ERR_NULL;
+    const size_t total = (size_t)n_elems * (size_t)elem_bytes;
+    const bool in_place = present_cache == past_cache;
+    if (!in_place && kvc_host::overlaps(present_cache, total, past_cache, total))
+        return KVC_ERR_SHAPE;
+    if (update_seq_len > 0 &&
+        kvc_host::overlaps(present_cache, total, update,
+                           (size_t)(n_prefix * update_seq_len * slice)))
+        return KVC_ERR_SHAPE;
+    if (n_elems == 0)
+        return KVC_OK;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+
+    if (!in_place) {
+        char *dst = static_cast<char *>(present_cache);
+        const char *src = static_cast<const char *>(past_cache);
+        const int blocks = kvc_host::sm_count() * 8;
+        if (kvc_host::aligned16(dst) && kvc_host::aligned16(src)) {
+            const int64_t nv = (int64_t)(total / 16);
+            if (nv > 0)
+                copy_vec16_kernel<<<blocks, 256, 0, stream>>>(
+                    reinterpret_cast<uint4 *>(dst), reinterpret_cast<const uint4 *>(src), nv);
+            const int64_t tail = (int64_t)(total - (size_t)nv * 16);
+            if (tail > 0)
+                copy_bytes_kernel<<<1, 256, 0, stream>>>(dst + nv * 16, src + nv * 16, tail);
+        } else {
+            copy_bytes_kernel<<<blocks, 256, 0, stream>>>(dst, src, (int64_t)total);
+        }
+    }
+    if (update_seq_len == 0)
+        return kvc_host::launch_status();
+
+    const int64_t ppb = n_prefix / cache_shape[0];
+    char *present = static_cast<char *>(present_cache);
+    const char *upd = static_cast<const char *>(update);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(present) | reinterpret_cast<uintptr_t>(upd);
+    const int circ = mode == KVC_CIRCULAR;
+    if (slice % 16 == 0 && (a & 15u) == 0)
+        launch_scatter<uint4>(present, upd, write_indices, n_prefix, ppb, max_seq,
+                              update_seq_len, slice, circ, dev_status, stream);
+    else if (slice % 8 == 0 && (a & 7u) == 0)
+        launch_scatter<uint2>(present, upd, write_indices, n_prefix, ppb, max_seq,
+                              update_seq_len, slice, circ, dev_status, stream);
+    else if (slice % 4 == 0 && (a & 3u) == 0)
+        launch_scatter<uint32_t>(present, upd, write_indices, n_prefix, ppb, max_seq,
+                                 update_seq_len, slice, circ, dev_status, stream);
+    else if (slice % 2 == 0 && (a & 1u) == 0)
+        launch_scatter<uint16_t>(present, upd, write_indices, n_prefix, ppb, max_seq,
+                                 update_seq_len, slice, circ, dev_status, stream);
+    else
+        launch_scatter<uint8_t>(present, upd, write_indices, n_prefix, ppb, max_seq,
+                                update_seq_len, slice, circ, dev_status, stream);
+    return kvc_host::launch_status();
+}
+
+KVC_API const char *kvc_status_string(kvc_status s)
+{
+    switch (s) {
+    case KVC_OK: return "ok";
+    case KVC_ERR_NULL: return "a required pointer is NULL";
+    case KVC_ERR_SHAPE: return "size out of range or overlapping buffers";
+    case KVC_ERR_DTYPE: return "element type not supported";
+    case KVC_ERR_ALIGN: return "buffer not 16-byte aligned";
+    case KVC_ERR_UNSUPPORTED: return "combination not supported by this build";
+    case KVC_ERR_CAPACITY: return "capacity out of range";
+    case KVC_ERR_WINDOW: return "windowed cache needs 0 < local_window_size <= capacity";
+    case KVC_ERR_WORKSPACE: return "workspace missing or too small";
+    case KVC_ERR_CUDA: return "CUDA launch or driver call failed";
+    }
+    return "unknown status";
+}
+
+KVC_API int kvc_abi_version(void) { return KVC_ABI_VERSION; }

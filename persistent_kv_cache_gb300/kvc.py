@@ -1,0 +1,202 @@
+"""Python binding of the C ABI in include/kvc.h (argument marshalling only).
+
+Every function has the C entry point's name and forwards torch tensors as raw
+pointers plus the current CUDA stream; all the work happens in libkvc.so's
+kernels.  There is no CPU path: a missing library raises ``KvcLibraryMissing``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvc.so")
+
+KVC_F32, KVC_BF16, KVC_F16 = 0, 1, 2
+KVC_LINEAR, KVC_CIRCULAR = 0, 1
+KVC_APPEND, KVC_COPY_BACK = 0, 1
+
+KVC_OK = 0
+STATUS_NAMES = {
+    0: "KVC_OK", 1: "KVC_ERR_NULL", 2: "KVC_ERR_SHAPE", 3: "KVC_ERR_DTYPE", 4: "KVC_ERR_ALIGN",
+    5: "KVC_ERR_UNSUPPORTED", 6: "KVC_ERR_CAPACITY", 7: "KVC_ERR_WINDOW",
+    8: "KVC_ERR_WORKSPACE", 9: "KVC_ERR_CUDA",
+}
+KVC_DEV_INDEX_OOB = 1
+KVC_DEV_SEQLEN_RANGE = 2
+KVC_DEV_CAPACITY = 4
+KVC_DEV_ROPE_RANGE = 8
+KVC_DEV_TIMEOUT = 16
+
+EXPORTS = ("kvc_tensor_scatter", "kvc_seq_lengths", "kvc_window_append", "kvc_gqa_decode",
+           "kvc_gqa_decode_workspace_size", "kvc_gqa_prefill_chunk", "kvc_status_string",
+           "kvc_abi_version")
+
+
+class KvcLibraryMissing(RuntimeError):
+    pass
+
+
+class KvcError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(status, status)}")
+
+
+class KvcLengths(ctypes.Structure):
+    _fields_ = [("past_abs", ctypes.c_void_p), ("total_abs", ctypes.c_void_p),
+                ("cache_past", ctypes.c_void_p), ("cache_total", ctypes.c_void_p),
+                ("evict", ctypes.c_void_p)]
+
+
+class Lengths:
+    """Five int32 device tensors of [batch] (past_abs, total_abs, cache_past,
+    cache_total, evict) written by kvc_seq_lengths."""
+
+    FIELDS = ("past_abs", "total_abs", "cache_past", "cache_total", "evict")
+
+    def __init__(self, batch: int, device):
+        self.buf = torch.empty((5, batch), dtype=torch.int32, device=device)
+
+    def __getattr__(self, name):
+        if name in Lengths.FIELDS:
+            return self.buf[Lengths.FIELDS.index(name)]
+        raise AttributeError(name)
+
+    def c(self) -> KvcLengths:
+        return KvcLengths(*[self.buf[i].data_ptr() for i in range(5)])
+
+
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise KvcLibraryMissing(
+                f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I, I64, F, SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                            ctypes.c_size_t)
+        L = KvcLengths
+        sig = {
+            "kvc_tensor_scatter": [P, P, P, P, I, P, I64, I, I, I, P, P],
+            "kvc_seq_lengths": [P, I, I, I64, I, I, L, P, P],
+            "kvc_window_append": [P, P, P, P, P, P, L, I, I, I, I64, I, I, I, I, P, P, I64, P, P],
+            "kvc_gqa_decode": [P, P, P, P, L, I, I, I, I64, I, I, I, F, P, P, I64, P, SZ, P, P],
+            "kvc_gqa_decode_workspace_size": [I, I, I, I64, I, I],
+            "kvc_gqa_prefill_chunk": [P, P, P, P, I64, L, I, I, I, I, I, I, I, F, P, P, I64, P, P],
+            "kvc_status_string": [I],
+            "kvc_abi_version": [],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = I
+        lib.kvc_gqa_decode_workspace_size.restype = SZ
+        lib.kvc_status_string.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    return {torch.float32: KVC_F32, torch.bfloat16: KVC_BF16, torch.float16: KVC_F16}[t.dtype]
+
+
+def _check(fn: str, status: int):
+    if status != KVC_OK:
+        raise KvcError(fn, status)
+
+
+def _rope(rope):
+    if rope is None:
+        return None, None, 0
+    cos, sin = rope
+    return cos.data_ptr(), sin.data_ptr(), cos.shape[0]
+
+
+def kvc_tensor_scatter(present, past, update, write_indices=None, axis=-2, mode=KVC_LINEAR,
+                       status=None, stream=None):
+    shape = (ctypes.c_int64 * past.dim())(*past.shape)
+    seq_axis = axis if axis >= 0 else axis + past.dim()
+    _check("kvc_tensor_scatter", library().kvc_tensor_scatter(
+        _ptr(present), _ptr(past), _ptr(update), _ptr(write_indices), past.dim(), shape,
+        update.shape[seq_axis], axis, mode, past.element_size(), _ptr(status), _stream(stream)))
+    return present
+
+
+def kvc_seq_lengths(seqlens_k, new_tokens, capacity, windowed, local_window_size=0, out=None,
+                    status=None, stream=None):
+    out = Lengths(seqlens_k.shape[0], seqlens_k.device) if out is None else out
+    _check("kvc_seq_lengths", library().kvc_seq_lengths(
+        _ptr(seqlens_k), seqlens_k.shape[0], new_tokens, capacity, int(windowed),
+        local_window_size, out.c(), _ptr(status), _stream(stream)))
+    return out
+
+
+def kvc_window_append(k_cache, v_cache, new_k, new_v, lengths, windowed, phase=KVC_APPEND,
+                      k_stage=None, v_stage=None, rope=None, status=None, stream=None):
+    B, Hkv, C, D = k_cache.shape
+    S = new_k.shape[2] if new_k is not None else (k_stage.shape[2] - C)
+    cs, sn, rmax = _rope(rope)
+    _check("kvc_window_append", library().kvc_window_append(
+        _ptr(k_cache), _ptr(v_cache), _ptr(new_k), _ptr(new_v), _ptr(k_stage), _ptr(v_stage),
+        lengths.c(), B, Hkv, S, C, D, _dtype_code(k_cache), int(windowed), phase, cs, sn, rmax,
+        _ptr(status), _stream(stream)))
+
+
+def kvc_gqa_decode_workspace_size(batch, q_heads, kv_heads, capacity, head_dim, dtype):
+    return library().kvc_gqa_decode_workspace_size(batch, q_heads, kv_heads, capacity, head_dim,
+                                                   dtype)
+
+
+def decode_workspace(q, k_cache):
+    B, Hq, _, D = q.shape
+    n = kvc_gqa_decode_workspace_size(B, Hq, k_cache.shape[1], k_cache.shape[2], D,
+                                      _dtype_code(q))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+
+
+def kvc_gqa_decode(out, q, k_cache, v_cache, lengths, local_window_size=0, scale=0.0, rope=None,
+                   workspace=None, status=None, stream=None):
+    B, Hq, _, D = q.shape
+    _, Hkv, C, _ = k_cache.shape
+    ws = decode_workspace(q, k_cache) if workspace is None else workspace
+    cs, sn, rmax = _rope(rope)
+    _check("kvc_gqa_decode", library().kvc_gqa_decode(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), lengths.c(), B, Hq, Hkv, C, D,
+        _dtype_code(q), local_window_size, scale, cs, sn, rmax, _ptr(ws), ws.numel(),
+        _ptr(status), _stream(stream)))
+    return out
+
+
+def kvc_gqa_prefill_chunk(out, q, k_rows, v_rows, lengths, local_window_size=0, scale=0.0,
+                          rope=None, status=None, stream=None):
+    B, Hq, S, D = q.shape
+    _, Hkv, R, _ = k_rows.shape
+    cs, sn, rmax = _rope(rope)
+    _check("kvc_gqa_prefill_chunk", library().kvc_gqa_prefill_chunk(
+        _ptr(out), _ptr(q), _ptr(k_rows), _ptr(v_rows), R, lengths.c(), B, Hq, Hkv, S, D,
+        _dtype_code(q), local_window_size, scale, cs, sn, rmax, _ptr(status), _stream(stream)))
+    return out
+
+
+def kvc_status_string(code: int) -> str:
+    return library().kvc_status_string(code).decode()
+
+
+def kvc_abi_version() -> int:
+    return library().kvc_abi_version()

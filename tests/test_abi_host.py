@@ -1,0 +1,125 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point that
+include/kvc.h declares, and rejects bad arguments on the host before any CUDA
+call (the host checks return before a kernel is enqueued, so fake non-NULL
+pointers are never touched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvc():
+    from persistent_kv_cache_gb300 import build as B
+    B.build()
+    from persistent_kv_cache_gb300 import kvc as K
+    return K
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "kvc.h")).read()
+    return sorted(set(re.findall(r"^\w[\w \*]*?\b(kvc_\w+)\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(kvc):
+    names = _declared()
+    assert "kvc_gqa_decode" in names and len(names) >= 8
+    lib = kvc.library()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(kvc.EXPORTS) <= set(names)
+
+
+def test_version_and_strings(kvc):
+    assert kvc.kvc_abi_version() == 1
+    assert kvc.kvc_status_string(0) == "ok"
+    assert "window" in kvc.kvc_status_string(7)
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced on the paths below
+L5 = None
+
+
+def _lengths(kvc):
+    return kvc.KvcLengths(FAKE, FAKE, FAKE, FAKE, FAKE)
+
+
+def test_scatter_host_checks(kvc):
+    lib = kvc.library()
+    shape = (ctypes.c_int64 * 4)(2, 2, 16, 8)
+    f = lib.kvc_tensor_scatter
+    assert f(None, FAKE, FAKE, None, 4, shape, 1, -2, 0, 4, None, None) == 1   # NULL
+    assert f(FAKE, FAKE, FAKE, None, 4, shape, 1, 0, 0, 4, None, None) == 2   # axis 0
+    assert f(FAKE, FAKE, FAKE, None, 4, shape, 1, 4, 0, 4, None, None) == 2   # axis out of range
+    assert f(FAKE, FAKE, FAKE, None, 4, shape, 17, -2, 0, 4, None, None) == 2  # S > max_seq
+    assert f(FAKE, FAKE, FAKE, None, 4, shape, 1, -2, 0, 3, None, None) == 3  # elem bytes
+    assert f(FAKE, FAKE, FAKE, None, 4, shape, 1, -2, 2, 4, None, None) == 5  # mode
+    assert f(FAKE, FAKE, FAKE, None, 1, shape, 1, -1, 0, 4, None, None) == 2  # rank 1
+    # partial overlap of present and past
+    assert f(FAKE, FAKE + 16, FAKE * 4, None, 4, shape, 1, -2, 0, 4, None, None) == 2
+
+
+def test_lengths_host_checks(kvc):
+    lib = kvc.library()
+    f = lib.kvc_seq_lengths
+    L = _lengths(kvc)
+    assert f(FAKE, 4, 0, 128, 1, 128, L, None, None) == 2       # S < 1
+    assert f(FAKE, 4, 1, 0, 1, 128, L, None, None) == 6         # C < 1
+    assert f(FAKE, 4, 1, 128, 1, 129, L, None, None) == 7       # W > C
+    assert f(FAKE, 4, 1, 128, 1, 0, L, None, None) == 7         # W missing
+    assert f(None, 4, 1, 128, 1, 128, L, None, None) == 1
+    assert f(FAKE, 0, 1, 128, 1, 128, L, None, None) == 0       # empty batch: nothing to do
+
+
+def test_append_host_checks(kvc):
+    lib = kvc.library()
+    f = lib.kvc_window_append
+    L = _lengths(kvc)
+    args = dict(kc=FAKE, vc=FAKE * 2, nk=FAKE * 3, nv=FAKE * 4, ks=None, vs=None)
+    base = [args["kc"], args["vc"], args["nk"], args["nv"], None, None, L]
+    assert f(*base, 2, 2, 1, 16, 8, 7, 1, 0, None, None, 0, None, None) == 3        # dtype
+    assert f(*base, 2, 2, 1, 16, 7, 1, 1, 0, None, None, 0, None, None) == 2        # odd D
+    assert f(*base, 2, 2, 4, 16, 8, 1, 1, 0, None, None, 0, None, None) == 1        # no stage
+    assert f(*base, 2, 2, 1, 16, 8, 1, 1, 1, None, None, 0, None, None) == 5        # copy-back S=1
+    assert f(*base, 2, 2, 1, 0, 8, 1, 1, 0, None, None, 0, None, None) == 6         # C < 1
+    assert f(*base, 2, 2, 1, 16, 8, 1, 1, 0, FAKE, None, 16, None, None) == 1       # half a table
+    unaligned = [FAKE + 2] + base[1:]
+    assert f(*unaligned, 2, 2, 1, 16, 8, 1, 1, 0, None, None, 0, None, None) == 4   # alignment
+
+
+def test_decode_host_checks(kvc):
+    lib = kvc.library()
+    f = lib.kvc_gqa_decode
+    L = _lengths(kvc)
+    base = [FAKE, FAKE * 2, FAKE * 3, FAKE * 4, L]
+    assert f(*base, 2, 6, 4, 64, 128, 1, 0, 0.0, None, None, 0, FAKE, 1 << 20, None, None) == 2
+    assert f(*base, 2, 8, 2, 64, 96, 1, 0, 0.0, None, None, 0, FAKE, 1 << 20, None, None) == 5
+    assert f(*base, 2, 64, 2, 64, 128, 1, 0, 0.0, None, None, 0, FAKE, 1 << 20, None, None) == 5
+    assert f(*base, 2, 8, 2, 8192, 128, 1, 0, 0.0, None, None, 0, None, 0, None, None) == 8
+    need = lib.kvc_gqa_decode_workspace_size(2, 8, 2, 8192, 128, 1)
+    assert need == 2 * 8 * 16 * 130 * 4
+    assert f(*base, 2, 8, 2, 8192, 128, 1, 0, 0.0, None, None, 0, FAKE, need - 4, None, None) == 8
+    bad = [FAKE + 8] + base[1:]
+    assert f(*bad, 2, 8, 2, 64, 128, 1, 0, 0.0, None, None, 0, FAKE, 256, None, None) == 4
+    assert lib.kvc_gqa_decode_workspace_size(2, 8, 2, 128, 64, 1) == 256
+
+
+def test_prefill_host_checks(kvc):
+    lib = kvc.library()
+    f = lib.kvc_gqa_prefill_chunk
+    L = _lengths(kvc)
+    base = [FAKE, FAKE * 2, FAKE * 3, FAKE * 4]
+    assert f(*base, 100, L, 2, 8, 2, 0, 64, 1, 0, 0.0, None, None, 0, None, None) == 2  # S = 0
+    assert f(*base, 10, L, 2, 8, 2, 16, 64, 1, 0, 0.0, None, None, 0, None, None) == 6  # R < S
+    assert f(*base, 100, L, 2, 8, 3, 16, 64, 1, 0, 0.0, None, None, 0, None, None) == 2  # heads
+    assert f(*base, 100, L, 2, 8, 2, 16, 64, 9, 0, 0.0, None, None, 0, None, None) == 3  # dtype
+
+
+def test_binding_requires_library(monkeypatch, kvc):
+    monkeypatch.setattr(kvc, "LIB_PATH", "/nonexistent/libkvc.so")
+    monkeypatch.setattr(kvc, "_lib", None)
+    with pytest.raises(kvc.KvcLibraryMissing):
+        kvc.library()
