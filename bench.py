@@ -338,6 +338,19 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile(args):
+    """Setup, W + K device steps and nothing else: the command profiled by
+    ncu (no end-to-end pass, no oracle timing)."""
+    import torch
+    dev = torch.device("cuda", 0)
+    wl = WORKLOADS[args.workload](dev, seed=0)
+    for _ in range(args.warmup + args.steps):
+        wl.step()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_run": args.workload, "steps": args.steps, "warmup": args.warmup,
+                      "device_status": int(wl.st.item())}), flush=True)
+
+
 def run_reference(args):
     """The oracle timed on the host cores, each step a bounded sample (two
     batch rows) of the same workload."""
@@ -376,7 +389,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="contig-decode")
+    ap.add_argument("--profile", action="store_true",
+                    help="device steps only (the command run under ncu)")
     args = ap.parse_args()
+    if args.profile:
+        from persistent_kv_cache_gb300 import build as B
+        B.build()
+        run_profile(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
