@@ -15,9 +15,10 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  * Ownership: the caller owns every buffer.  The library allocates nothing,
- *    keeps no state between calls (apart from cached device attributes) and
- *    never reads device memory on the host, so every call can be captured in
- *    a CUDA graph.  Pointers marked "device" must be device (or managed)
+ *    keeps no state between calls (apart from cached device attributes and
+ *    the scratch array of kvc_gqa_decode_noalloc) and never reads device
+ *    memory on the host, so the calls listed above can be captured in a CUDA
+ *    graph.  Pointers marked "device" must be device (or managed)
  *    memory of the current device; pointers marked "host" are read during
  *    the call only.
  *  * Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  Work
@@ -214,6 +215,48 @@ kvc_status kvc_gqa_decode(void *out, const void *q, const void *k_cache, const v
 /* Bytes of workspace kvc_gqa_decode needs for these sizes (0 on bad sizes). */
 size_t kvc_gqa_decode_workspace_size(int batch, int q_heads, int kv_heads, int64_t capacity,
                                      int head_dim, int dtype);
+
+/* Size of the library's own decode scratch array (see kvc_gqa_decode_noalloc). */
+#define KVC_DECODE_STATIC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * kvc_gqa_decode_noalloc -- kvc_gqa_decode for callers that cannot allocate
+ * device memory.  The source pages have no counterpart of this call; it is a
+ * convenience of this library.
+ *
+ * Who needs it: code that runs where it has no device allocator to call, or
+ * is not allowed to use one -- for example a plugin or operator inside a host
+ * framework that owns all device memory through its own pool and gives its
+ * kernels no way to request scratch, or a caller that has sized its memory
+ * up front and must not grow it while serving.  Such a caller still owns and
+ * passes every input and output; only the decode's split partials (the
+ * workspace of kvc_gqa_decode) move into memory the library provides.
+ *
+ * The scratch is one file-scope device array of
+ * KVC_DECODE_STATIC_SCRATCH_BYTES (16 MiB) that every device loading the
+ * library keeps until the process exits.  Sizes whose workspace
+ * (kvc_gqa_decode_workspace_size) exceeds it are rejected with
+ * KVC_ERR_WORKSPACE before anything is enqueued.  The call itself allocates
+ * nothing: no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the one array and it keeps the
+ * previous call's contents: nothing in it needs to start at zero (every
+ * partial is written before it is read within a call), but two calls whose
+ * kernels overlap on the GPU -- on different streams, or different threads
+ * -- race on it and may return wrong results.  Serialise them (one stream,
+ * or events).
+ *
+ * Arguments, layouts, supported sizes and errors are those of
+ * kvc_gqa_decode without the workspace pair.
+ */
+kvc_status kvc_gqa_decode_noalloc(void *out, const void *q, const void *k_cache,
+                                  const void *v_cache, kvc_lengths len, int batch, int q_heads,
+                                  int kv_heads, int64_t capacity, int head_dim, int dtype,
+                                  int local_window_size, float scale, const float *rope_cos,
+                                  const float *rope_sin, int64_t rope_max_pos,
+                                  int32_t *dev_status, void *stream);
 
 /*
  * kvc_gqa_prefill_chunk -- attention of an S-token chunk over staged rows

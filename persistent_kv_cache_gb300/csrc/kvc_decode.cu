@@ -19,6 +19,7 @@
 //     writes the output directly.
 // fp32 path: attn_f32_kernel, one warp per query row on CUDA cores (also used
 // by the multi-token call for fp32).
+#include <mutex>
 #include <type_traits>
 
 #include "kvc_common.cuh"
@@ -692,4 +693,60 @@ KVC_API kvc_status kvc_gqa_decode(void *out, const void *q, const void *k_cache,
     return dispatch_decode16<__half>(head_dim, out, q, k_cache, v_cache, len, batch, q_heads,
                                      kv_heads, capacity, local_window_size, scale, rope_cos,
                                      rope_sin, rope_max_pos, workspace, dev_status, stream);
+}
+
+// --------------------------------------------------------------------------
+// kvc_gqa_decode_noalloc: the same decode for callers that cannot allocate
+// device memory themselves.  Its split partials live in one file-scope device
+// array of KVC_DECODE_STATIC_SCRATCH_BYTES; the module holds that array on
+// every device that loads the library until the process exits.
+// --------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_decode_scratch[KVC_DECODE_STATIC_SCRATCH_BYTES];
+
+std::mutex g_scratch_mutex;
+void *g_scratch_addr[256] = {};  // device address of g_decode_scratch, per device ordinal
+
+// Host code may not pass g_decode_scratch itself to a kernel (on the host it
+// names a stand-in, not device memory); the device address is looked up once
+// per device, with that device current.
+kvc_status scratch_address(void **addr)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256)
+        return KVC_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr)
+            return KVC_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *addr = g_scratch_addr[dev];
+    return KVC_OK;
+}
+
+} // namespace
+
+KVC_API kvc_status kvc_gqa_decode_noalloc(void *out, const void *q, const void *k_cache,
+                                          const void *v_cache, kvc_lengths len, int batch,
+                                          int q_heads, int kv_heads, int64_t capacity,
+                                          int head_dim, int dtype, int local_window_size,
+                                          float scale, const float *rope_cos,
+                                          const float *rope_sin, int64_t rope_max_pos,
+                                          int32_t *dev_status, void *stream)
+{
+    const size_t need =
+        kvc_gqa_decode_workspace_size(batch, q_heads, kv_heads, capacity, head_dim, dtype);
+    if (need > KVC_DECODE_STATIC_SCRATCH_BYTES)
+        return KVC_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    const kvc_status st = scratch_address(&scratch);
+    if (st != KVC_OK)
+        return st;
+    return kvc_gqa_decode(out, q, k_cache, v_cache, len, batch, q_heads, kv_heads, capacity,
+                          head_dim, dtype, local_window_size, scale, rope_cos, rope_sin,
+                          rope_max_pos, scratch, KVC_DECODE_STATIC_SCRATCH_BYTES, dev_status,
+                          stream);
 }
