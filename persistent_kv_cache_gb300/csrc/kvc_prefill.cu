@@ -6,26 +6,33 @@
 // 16-bit path: one CTA per (query block, kv head, batch row) on the 5th-gen
 // tensor cores.  The M = 128 tile packs the GQA group: row m holds query head
 // m / QB of the group and query qb * QB + m % QB (QB = 128 / group), so every
-// K/V tile is read once for all heads of the group.
+// K/V tile is read once for all heads of the group.  Q, S, P and O all live
+// in tensor memory, which leaves shared memory to the K and V rings:
 //
-//   warp 0      TMA producer: 64-row K and V tiles (128-byte swizzled boxes
-//               of 64 columns) into a 2-stage ring (full/empty mbarriers)
-//   warp 1      allocates tensor memory and issues tcgen05.mma:
-//                 S_j = Q K_j^T   (M 128, N 64,  K = D)  -> TMEM, 2 buffers
-//                 O  += P_j V_j   (M 128, N = D, K = 64)  -> TMEM
-//               S_{j+1} is issued before waiting for P_j, so the tensor
-//               cores compute the next scores while the softmax runs
-//   warps 2-5   one thread per row (= TMEM lane): rotate and stage the query
-//               row, then per tile read S_j from TMEM, mask, online softmax
-//               (log2 domain, the running max is only raised when it grows
-//               by more than 2^8, which keeps the result exact after the
-//               final division), write P_j as bf16 into a swizzled shared
-//               tile, rescale the O row in TMEM when the max moved, and at
-//               the end divide by l and store the output row.
+//   TMEM columns  O [0, D) fp32 | S/P double buffer [D, D + 128) | Q [.., + D/2)
+//   warp 0        TMA producer of 64-row K tiles (128-byte swizzled boxes of
+//                 64 columns) into an NK-stage ring; a stage is refilled as
+//                 soon as the S MMA that read it has completed
+//   warp 2        the same for V (NV stages), refilled after the PV MMA
+//   warp 1        allocates tensor memory and issues tcgen05.mma in the order
+//                 S_0, S_1, PV_0, S_2, PV_1, ...:
+//                   S_j = Q K_j^T   A = Q in TMEM, B = K tile (K-major)
+//                   O  += P_j V_j   A = P_j in TMEM, B = V tile (MN-major)
+//                 so the next scores are always queued behind the current PV
+//   warps 3-10    two threads per row (= TMEM lane), each owning half of the
+//                 score columns and half of O: rotate the query row into
+//                 TMEM, then per tile read its S_j half, mask only tiles the
+//                 window or diagonal cuts, exchange the row max with the
+//                 partner thread, online softmax in the log2 domain (the
+//                 running max is only raised when it grows by more than 2^8,
+//                 exact after the final division), write P_j as 16-bit pairs
+//                 over S_j, rescale its half of O when the max moved, and at
+//                 the end divide by l and store its half of the output row.
 // Every mbarrier wait is bounded; a timeout sets KVC_DEV_TIMEOUT, every role
 // winds down, outstanding tensor-core work is drained and TMEM is freed.
 //
 // fp32 path: the CUDA-core attn_f32_kernel (kvc_decode.cu).
+#include <algorithm>
 #include <type_traits>
 
 #include "kvc_common.cuh"
@@ -34,8 +41,7 @@ namespace {
 
 constexpr int kBM = 128;       // rows of the M tile (query heads x queries)
 constexpr int kBN = 64;        // KV rows per tile
-constexpr int kStages = 2;     // K/V ring depth
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kThreads = 352;  // 11 warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -67,14 +73,34 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar)
         : "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16, one CTA
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate)
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16: A's rows are TMEM lanes and
+// its 16-bit elements are packed two per 32-bit column
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate)
 {
     asm volatile("{\n\t.reg .pred p;\n\t"
                  "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// 32-bit words to consecutive columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_st_words(uint32_t taddr, const uint32_t (&w)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                     taddr),
+                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                 "r"(w[7])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st_words(uint32_t taddr, const uint32_t (&w)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                 "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]),
+                 "r"(w[13]), "r"(w[14]), "r"(w[15])
                  : "memory");
 }
 
@@ -122,7 +148,42 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
                  : "memory");
 }
 
+__device__ __forceinline__ void tmem_st_words(uint32_t taddr, const uint32_t (&w)[32])
+{
+    float f[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        f[i] = __uint_as_float(w[i]);
+    tmem_st32(taddr, f);
+}
+
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 2^x on the special-function unit (ex2.approx, flush-to-zero; 2^-inf = 0)
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+template <typename T> __device__ __forceinline__ uint32_t pack2(float lo, float hi)
+{
+    if constexpr (std::is_same<T, __half>::value) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    } else {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+}
+
+__device__ __forceinline__ int t_lo_of(int lo, int j) { return lo + j * 64; }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand: rows of
 // 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), `lbo` bytes
@@ -163,19 +224,21 @@ struct PrefillArgs {
 };
 
 template <int D> struct PrefillSmem {
-    static constexpr int Q_BYTES = kBM * D * 2;        // D/64 boxes of 128 x 64
-    static constexpr int KV_TILE = kBN * D * 2;        // D/64 boxes of 64 x 64
-    static constexpr int P_BYTES = kBM * kBN * 2;      // one 128 x 64 box
-    static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = Q_OFF + Q_BYTES;
-    static constexpr int V_OFF = K_OFF + kStages * KV_TILE;
-    static constexpr int P_OFF = V_OFF + kStages * KV_TILE;
-    static constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
-    // barriers: k_full[2], v_full[2], kv_empty[2], s_full[2], s_empty[2],
-    //           p_full[2], o_done[2], q_full, drain  -> 16 x 8 bytes
-    static constexpr int MISC_OFF = BAR_OFF + 16 * 8;  // tmem addr, abort flag
-    static constexpr int TOTAL = MISC_OFF + 16;
-    static constexpr uint32_t TMEM_COLS = (D + 2 * kBN) <= 256 ? 256 : 512;
+    static constexpr int KV_TILE = kBN * D * 2;          // D/64 boxes of 64 x 64
+    static constexpr int NK = D >= 256 ? 3 : 4;          // K ring depth
+    static constexpr int NV = D >= 256 ? 3 : 4;          // V ring depth
+    static constexpr int K_OFF = 0;
+    static constexpr int V_OFF = K_OFF + NK * KV_TILE;
+    static constexpr int BAR_OFF = V_OFF + NV * KV_TILE;
+    // barriers: k_full[4], k_empty[4], v_full[4], v_empty[4], s_full[2],
+    //           p_full[2], o_done[2], q_full, drain -> 24 x 8 bytes
+    static constexpr int MISC_OFF = BAR_OFF + 24 * 8;  // tmem addr, abort flag
+    static constexpr int RED_OFF = MISC_OFF + 16;      // row max / sum exchange, 4 x 128 floats
+    static constexpr int TOTAL = RED_OFF + 4 * kBM * 4;
+    // TMEM columns: O [0, D), S double buffer [D, D + 128), Q [D + 128, D + 128 + D/2)
+    static constexpr uint32_t COL_O = 0, COL_S = D, COL_Q = D + 2 * kBN;
+    static constexpr uint32_t TMEM_NEED = D + 2 * kBN + D / 2;
+    static constexpr uint32_t TMEM_COLS = TMEM_NEED <= 256 ? 256 : 512;
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
@@ -199,6 +262,36 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     }
 }
 
+// Stream one operand's 64-row tiles through a ring of NST shared-memory
+// stages: stage j % NST is reloaded once the MMA that read its previous
+// tile has completed (`empty`, signalled by tcgen05.commit).
+template <int NST, int BOXES, int KV_TILE>
+__device__ __forceinline__ void produce_tiles(const CUtensorMap *map, uint8_t *ring,
+                                              uint64_t *full, uint64_t *empty, int64_t row0,
+                                              int ntiles, volatile int *abort_flag,
+                                              int32_t *status)
+{
+    kvc::tma_prefetch_desc(map);
+    int issued = 0;
+    for (int j = 0; j < ntiles; ++j) {
+        const int st = j % NST;
+        if (j >= NST && !wait_or_abort(&empty[st], ((j / NST) - 1) & 1, abort_flag, status))
+            break;
+        uint8_t *dst = ring + st * KV_TILE;
+        kvc::mbar_arrive_expect_tx(&full[st], KV_TILE);
+        const int32_t y = (int32_t)(row0 + j * kBN);
+#pragma unroll
+        for (int bx = 0; bx < BOXES; ++bx)
+            kvc::tma_load_2d(dst + bx * (kBN * 128), map, bx * 64, y, &full[st]);
+        issued = j + 1;
+    }
+    if (*abort_flag) {
+        // wind-down: let the loads already in flight land before the CTA exits
+        for (int j = max(0, issued - NST); j < issued; ++j)
+            kvc::mbar_wait(&full[j % NST], (j / NST) & 1);
+    }
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -206,18 +299,30 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 {
     using SM = PrefillSmem<D>;
     constexpr int BOXES = D / 64;
+    constexpr int NK = SM::NK, NV = SM::NV;
     constexpr uint32_t AB = std::is_same<T, __half>::value ? 0u : 1u;
     constexpr uint32_t IDESC_S = f16_idesc(AB, 0, kBM, kBN);
     constexpr uint32_t IDESC_O = f16_idesc(AB, 1, kBM, D);
-    constexpr uint32_t COL_O = 0, COL_S = D;  // TMEM columns: O [0, D), S buffers after
+    constexpr uint32_t COL_O = SM::COL_O, COL_S = SM::COL_S, COL_Q = SM::COL_Q;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    {
+        // the swizzled tiles need a 1024-byte aligned base; check the layout
+        // fits the dynamic allocation the launch obtained
+        uint32_t dyn;
+        asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+        if ((uint32_t)(smem - smem_raw) + SM::TOTAL > dyn) {
+            if (threadIdx.x == 0)
+                kvc::raise_status(a.status, KVC_DEV_CAPACITY);
+            return;
+        }
+    }
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SM::BAR_OFF);
-    uint64_t *k_full = bars + 0, *v_full = bars + 2, *kv_empty = bars + 4, *s_full = bars + 6,
-             *s_empty = bars + 8, *p_full = bars + 10, *o_done = bars + 12, *q_full = bars + 14,
-             *drain = bars + 15;
+    uint64_t *k_full = bars + 0, *k_empty = bars + 4, *v_full = bars + 8, *v_empty = bars + 12,
+             *s_full = bars + 16, *p_full = bars + 18, *o_done = bars + 20, *q_full = bars + 22,
+             *drain = bars + 23;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SM::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::MISC_OFF + 4);
 
@@ -253,16 +358,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int64_t row_base = ((int64_t)b * a.kv_heads + kvh) * a.rows_per_head;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4; ++i) {
             kvc::mbar_init(&k_full[i], 1);
+            kvc::mbar_init(&k_empty[i], 1);
             kvc::mbar_init(&v_full[i], 1);
-            kvc::mbar_init(&kv_empty[i], 1);
+            kvc::mbar_init(&v_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             kvc::mbar_init(&s_full[i], 1);
-            kvc::mbar_init(&s_empty[i], 4);
-            kvc::mbar_init(&p_full[i], 4);
+            kvc::mbar_init(&p_full[i], 8);
             kvc::mbar_init(&o_done[i], 1);
         }
-        kvc::mbar_init(q_full, 4);
+        kvc::mbar_init(q_full, 8);
         kvc::mbar_init(drain, 1);
         *abort_flag = 0;
         kvc::fence_mbar_init();
@@ -277,89 +384,58 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const uint32_t smem_base = kvc::smem_u32(smem);
 
     if (warp == 0) {
-        // ======================= TMA producer =======================
-        if (lane == 0) {
-            kvc::tma_prefetch_desc(&tmap_k);
-            kvc::tma_prefetch_desc(&tmap_v);
-            int issued = 0;
-            for (int j = 0; j < ntiles; ++j) {
-                const int s = j & 1;
-                if (j >= kStages &&
-                    !wait_or_abort(&kv_empty[s], ((j >> 1) - 1) & 1, abort_flag, a.status))
-                    break;
-                const int32_t y = (int32_t)(row_base + lo + j * kBN);
-                uint8_t *kd = smem + SM::K_OFF + s * SM::KV_TILE;
-                uint8_t *vd = smem + SM::V_OFF + s * SM::KV_TILE;
-                kvc::mbar_arrive_expect_tx(&k_full[s], SM::KV_TILE);
-#pragma unroll
-                for (int bx = 0; bx < BOXES; ++bx)
-                    kvc::tma_load_2d(kd + bx * (kBN * 128), &tmap_k, bx * 64, y, &k_full[s]);
-                kvc::mbar_arrive_expect_tx(&v_full[s], SM::KV_TILE);
-#pragma unroll
-                for (int bx = 0; bx < BOXES; ++bx)
-                    kvc::tma_load_2d(vd + bx * (kBN * 128), &tmap_v, bx * 64, y, &v_full[s]);
-                issued = j + 1;
-            }
-            if (*abort_flag) {
-                // wind-down: let the last loads land before the CTA exits
-                for (int j = max(0, issued - kStages); j < issued; ++j) {
-                    kvc::mbar_wait(&k_full[j & 1], (j >> 1) & 1);
-                    kvc::mbar_wait(&v_full[j & 1], (j >> 1) & 1);
-                }
-            }
-        }
+        // ======================= K producer =======================
+        if (lane == 0)
+            produce_tiles<NK, BOXES, SM::KV_TILE>(&tmap_k, smem + SM::K_OFF, k_full, k_empty,
+                                                  row_base + lo, ntiles, abort_flag, a.status);
+    } else if (warp == 2) {
+        // ======================= V producer =======================
+        if (lane == 0)
+            produce_tiles<NV, BOXES, SM::KV_TILE>(&tmap_v, smem + SM::V_OFF, v_full, v_empty,
+                                                  row_base + lo, ntiles, abort_flag, a.status);
     } else if (warp == 1) {
         // ======================= MMA issuer =======================
+        // tensor-pipe order: S_0, S_1, PV_0, S_2, PV_1, S_3, ...  S_{j+2}
+        // reuses the TMEM buffer that holds P_j, after PV_j in issue order
         if (lane == 0) {
             bool ok = wait_or_abort(q_full, 0, abort_flag, a.status);
-            auto issue_s = [&](int j) {
-                const int s = j & 1;
-                const uint32_t qa = smem_base + SM::Q_OFF;
-                const uint32_t kb = smem_base + SM::K_OFF + s * SM::KV_TILE;
+            auto issue_s = [&](int j) -> bool {
+                const int ks = j % NK;
+                if (!wait_or_abort(&k_full[ks], (j / NK) & 1, abort_flag, a.status))
+                    return false;
+                tc_fence_after();
+                const uint32_t kb = smem_base + SM::K_OFF + ks * SM::KV_TILE;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t box = kk >> 2, within = (kk & 3) * 32;
-                    const uint64_t ad = sw128_desc(qa + box * (kBM * 128) + within, 16);
                     const uint64_t bd = sw128_desc(kb + box * (kBN * 128) + within, 16);
-                    tc_mma(tmem + COL_S + s * kBN, ad, bd, IDESC_S, kk > 0);
+                    tc_mma_ts(tmem + COL_S + (j & 1) * kBN, tmem + COL_Q + kk * 8, bd, IDESC_S,
+                              kk > 0);
                 }
-                tc_commit(&s_full[s]);
+                tc_commit(&s_full[j & 1]);
+                tc_commit(&k_empty[ks]);
+                return true;
             };
-            if (ok && ntiles > 0) {
-                ok = wait_or_abort(&k_full[0], 0, abort_flag, a.status);
-                if (ok) {
-                    tc_fence_after();
-                    issue_s(0);
-                }
-            }
+            for (int j = 0; ok && j < 2 && j < ntiles; ++j)
+                ok = issue_s(j);
             for (int j = 0; ok && j < ntiles; ++j) {
-                const int s = j & 1;
-                if (j + 1 < ntiles) {
-                    const int n = j + 1, sn = n & 1;
-                    if (n >= 2)
-                        ok = wait_or_abort(&s_empty[sn], ((n >> 1) - 1) & 1, abort_flag, a.status);
-                    if (ok)
-                        ok = wait_or_abort(&k_full[sn], (n >> 1) & 1, abort_flag, a.status);
-                    if (!ok)
-                        break;
-                    tc_fence_after();
-                    issue_s(n);
-                }
+                const int s = j & 1, vs = j % NV;
                 ok = wait_or_abort(&p_full[s], (j >> 1) & 1, abort_flag, a.status) &&
-                     wait_or_abort(&v_full[s], (j >> 1) & 1, abort_flag, a.status);
+                     wait_or_abort(&v_full[vs], (j / NV) & 1, abort_flag, a.status);
                 if (!ok)
                     break;
                 tc_fence_after();
-                const uint32_t pa = smem_base + SM::P_OFF + s * SM::P_BYTES;
-                const uint32_t vb = smem_base + SM::V_OFF + s * SM::KV_TILE;
+                const uint32_t vb = smem_base + SM::V_OFF + vs * SM::KV_TILE;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t ad = sw128_desc(pa + kk * 32, 16);
                     const uint64_t bd = sw128_desc(vb + kk * 2048, kBN * 128);
-                    tc_mma(tmem + COL_O, ad, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+                    tc_mma_ts(tmem + COL_O, tmem + COL_S + s * kBN + kk * 8, bd, IDESC_O,
+                              (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&o_done[s]);
-                tc_commit(&kv_empty[s]);
+                tc_commit(&v_empty[vs]);
+                if (j + 2 < ntiles)
+                    ok = issue_s(j + 2);
             }
             // drain: everything issued above has completed once this arrives
             // (a plain bounded wait, also on the abort path)
@@ -368,23 +444,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
     } else {
         // ======================= softmax / epilogue =======================
+        // two warps per TMEM lane quadrant: `half` 0 owns score columns
+        // [0, 32) of every tile and O columns [0, D/2), `half` 1 the rest
+        const int sw = warp - 3;                   // 0..7
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
+        const int half = sw >> 2;
         const int m = quad * 32 + lane;            // tile row == TMEM lane
         const int hh = m / QB;                     // head within the group
         const int ii = q0 + (m - hh * QB);         // query index in the chunk
         const bool row_valid = ii < S && hh < g;
         const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
         const int64_t qrow = ((int64_t)b * a.q_heads + kvh * g + hh) * S + ii;
+        float *red = reinterpret_cast<float *>(smem + SM::RED_OFF);  // [2 tiles][2 halves][128]
+        const uint32_t pair_bar = 1 + quad;       // named barrier of the two warps of a quadrant
 
-        // query row: rotate at absolute position P + ii, stage as bf16/f16 in
-        // the swizzled Q tile (row m of each 64-column box)
+        // query row: rotate at absolute position P + ii and store it as packed
+        // 16-bit pairs in TMEM (row m = lane m; element e in column COL_Q + e/2).
+        // Each half takes half of the rotation pairs (i, i + D/2).
         {
+            constexpr int NW = D / 8;  // words of each half's lo (and hi) part
+            uint32_t wlo[NW], whi[NW];
             const T *qsrc = static_cast<const T *>(a.q) + qrow * D;
             const float *cs = (a.cos_t && row_valid) ? a.cos_t + (int64_t)(P + ii) * (D / 2) : nullptr;
             const float *sn = (a.cos_t && row_valid) ? a.sin_t + (int64_t)(P + ii) * (D / 2) : nullptr;
-            uint8_t *qt = smem + SM::Q_OFF;
-#pragma unroll 1
-            for (int c = 0; c < D / 16; ++c) {  // chunk of 8 elements in each half
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                const int c = half * (D / 32) + cc;  // chunk of 8 elements in the low half
                 uint4 lo4 = make_uint4(0, 0, 0, 0), hi4 = make_uint4(0, 0, 0, 0);
                 if (row_valid) {
                     lo4 = *reinterpret_cast<const uint4 *>(qsrc + c * 8);
@@ -401,11 +486,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         hv[e] = kvc::Elem<T>::from_f32(y);
                     }
                 }
-                const int clo = c, chi = D / 16 + c;  // 16-byte chunk index along D
-                *reinterpret_cast<uint4 *>(qt + (clo >> 3) * (kBM * 128) + kvc::sw128(m, clo & 7)) = lo4;
-                *reinterpret_cast<uint4 *>(qt + (chi >> 3) * (kBM * 128) + kvc::sw128(m, chi & 7)) = hi4;
+                wlo[cc * 4 + 0] = lo4.x; wlo[cc * 4 + 1] = lo4.y;
+                wlo[cc * 4 + 2] = lo4.z; wlo[cc * 4 + 3] = lo4.w;
+                whi[cc * 4 + 0] = hi4.x; whi[cc * 4 + 1] = hi4.y;
+                whi[cc * 4 + 2] = hi4.z; whi[cc * 4 + 3] = hi4.w;
             }
-            kvc::fence_proxy_async_smem();
+            tmem_st_words(lane_addr + COL_Q + half * NW, wlo);
+            tmem_st_words(lane_addr + COL_Q + D / 4 + half * NW, whi);
+            tmem_wait_st();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 kvc::mbar_arrive(q_full);
@@ -414,97 +503,89 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         // visible rows of this query: [r_lo, r_hi]
         const int r_hi = Lp + ii;
         const int r_lo = a.window > 0 ? max(0, r_hi - a.window + 1) : 0;
+        const float c_log2 = a.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
             const int s = j & 1;
-            const int t_lo = lo + j * kBN;
+            const int t_lo = t_lo_of(lo, j);
+            const int c0 = t_lo + 32 * half;  // key row of my first column
             if (!wait_or_abort(&s_full[s], (j >> 1) & 1, abort_flag, a.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            float sc[kBN];
-            {
-                float v[32];
-                tmem_ld32(lane_addr + COL_S + s * kBN, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    sc[i] = v[i];
-                tmem_ld32(lane_addr + COL_S + s * kBN + 32, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    sc[32 + i] = v[i];
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                kvc::mbar_arrive(&s_empty[s]);
+            float v[32];
+            tmem_ld32(lane_addr + COL_S + s * kBN + 32 * half, v);
 
-            float mt = -INFINITY;
+            // mask only where the window or the diagonal cuts these columns
+            const bool all_in = row_valid && c0 >= r_lo && c0 + 31 <= r_hi;
+            if (!all_in) {
 #pragma unroll
-            for (int c = 0; c < kBN; ++c) {
-                const int r = t_lo + c;
-                const bool vis = row_valid && r >= r_lo && r <= r_hi;
-                sc[c] = vis ? sc[c] * a.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, sc[c]);
+                for (int c = 0; c < 32; ++c) {
+                    const int r = c0 + c;
+                    v[c] = (row_valid && r >= r_lo && r <= r_hi) ? v[c] : -INFINITY;
+                }
             }
+            float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
+#pragma unroll
+            for (int c = 4; c < 32; c += 4) {
+                mx0 = fmaxf(mx0, fmaxf(v[c], v[c + 1]));
+                mx1 = fmaxf(mx1, fmaxf(v[c + 2], v[c + 3]));
+            }
+            float mx = fmaxf(mx0, mx1);
+            // the exchange barrier also orders both halves' S reads before
+            // either half overwrites the buffer with P
+            red[((j & 1) * 2 + half) * kBM + m] = mx;
+            named_bar_sync(pair_bar, 64);
+            mx = fmaxf(mx, red[((j & 1) * 2 + (half ^ 1)) * kBM + m]);
+            const float mt = mx * c_log2;  // tile max in log2 units (c_log2 > 0)
+
             float alpha = 1.f;
             bool rescale = false;
             if (mt > m_run + kRescaleThreshold || (m_run == -INFINITY && mt > -INFINITY)) {
                 if (j > 0 && m_run > -INFINITY) {
-                    alpha = exp2f(m_run - mt);
+                    alpha = fast_exp2(m_run - mt);
                     rescale = true;
                 }
                 m_run = mt;
             }
-            const float m_use = m_run == -INFINITY ? 0.f : m_run;
-            float psum = 0.f;
-            uint32_t pk[kBN / 2];
+            const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+            float ps0 = 0.f, ps1 = 0.f;
+            uint32_t pk[16];
 #pragma unroll
-            for (int c = 0; c < kBN; c += 2) {
-                const float p0 = exp2f(sc[c] - m_use), p1 = exp2f(sc[c + 1] - m_use);
-                psum += p0 + p1;
-                if constexpr (std::is_same<T, __half>::value) {
-                    __half2 h = __floats2half2_rn(p0, p1);
-                    pk[c / 2] = *reinterpret_cast<uint32_t *>(&h);
-                } else {
-                    __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-                    pk[c / 2] = *reinterpret_cast<uint32_t *>(&h);
-                }
+            for (int c = 0; c < 32; c += 2) {
+                const float p0 = fast_exp2(fmaf(v[c], c_log2, neg_m));
+                const float p1 = fast_exp2(fmaf(v[c + 1], c_log2, neg_m));
+                ps0 += p0;
+                ps1 += p1;
+                pk[c / 2] = pack2<T>(p0, p1);
             }
-            l_run = l_run * alpha + psum;
-
-            // P_j goes to buffer s, last read by PV_{j-2}
-            if (j >= 2 && !wait_or_abort(&o_done[s], ((j >> 1) - 1) & 1, abort_flag, a.status)) {
-                ok = false;
-                break;
-            }
-            uint8_t *pt = smem + SM::P_OFF + s * SM::P_BYTES;
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4 *>(pt + kvc::sw128(m, c)) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            l_run = l_run * alpha + (ps0 + ps1);
+            // P_j (16-bit pairs) over the S_j columns of this row
+            tmem_st_words(lane_addr + COL_S + s * kBN + 16 * half, pk);
 
             // rows past the last visible row of the block: zero V so that
             // 0 * (stale or uninitialised bytes) stays 0 in O += P V
             if (t_lo + kBN - 1 > hi) {
-                if (!wait_or_abort(&v_full[s], (j >> 1) & 1, abort_flag, a.status)) {
+                const int vs = j % NV;
+                if (!wait_or_abort(&v_full[vs], (j / NV) & 1, abort_flag, a.status)) {
                     ok = false;
                     break;
                 }
                 const int first_bad = hi + 1 - t_lo;  // rows [first_bad, 64) of the tile
-                uint8_t *vt = smem + SM::V_OFF + s * SM::KV_TILE;
+                uint8_t *vt = smem + SM::V_OFF + vs * SM::KV_TILE;
                 const int nbad = kBN - first_bad;
-                for (int idx = threadIdx.x - 64; idx < nbad * BOXES * 8; idx += 128) {
+                for (int idx = threadIdx.x - 96; idx < nbad * BOXES * 8; idx += 256) {
                     const int rr = first_bad + idx / (BOXES * 8);
-                    const int bx = (idx / 8) % BOXES, c = idx % 8;
-                    *reinterpret_cast<uint4 *>(vt + bx * (kBN * 128) + rr * 128 + c * 16) =
+                    const int bx = (idx / 8) % BOXES, cc = idx % 8;
+                    *reinterpret_cast<uint4 *>(vt + bx * (kBN * 128) + rr * 128 + cc * 16) =
                         make_uint4(0, 0, 0, 0);
                 }
+                kvc::fence_proxy_async_smem();
             }
 
-            // the running max moved: rescale this row of O (PV_{j-1} must be done)
+            // the running max moved: rescale my half of this O row (PV_{j-1} done)
             if (__any_sync(0xffffffffu, rescale)) {
                 if (!wait_or_abort(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag,
                                    a.status)) {
@@ -513,34 +594,38 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
                 tc_fence_after();
 #pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(lane_addr + COL_O + c0, v);
+                for (int cc = half * (D / 2); cc < (half + 1) * (D / 2); cc += 32) {
+                    float o[32];
+                    tmem_ld32(lane_addr + COL_O + cc, o);
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        v[i] *= alpha;
-                    tmem_st32(lane_addr + COL_O + c0, v);
+                        o[i] *= alpha;
+                    tmem_st32(lane_addr + COL_O + cc, o);
                 }
-                tmem_wait_st();
             }
-            kvc::fence_proxy_async_smem();
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 kvc::mbar_arrive(&p_full[s]);
         }
 
-        // epilogue: wait for the last PV, divide by l, store the row
+        // epilogue: combine the two halves' sums, wait for the last PV,
+        // divide by l and store my half of the output row
+        // (the buffer of parity ntiles & 1 was last read before the final tile's barrier)
+        red[((ntiles & 1) * 2 + half) * kBM + m] = l_run;
+        named_bar_sync(pair_bar, 64);
+        const float l_tot = l_run + red[((ntiles & 1) * 2 + (half ^ 1)) * kBM + m];
         if (ok && ntiles > 0 &&
             wait_or_abort(&o_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_flag,
                           a.status)) {
             tc_fence_after();
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
             T *dst = static_cast<T *>(a.out) + qrow * D;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                float v[32];
-                tmem_ld32(lane_addr + COL_O + c0, v);
+            for (int cc = half * (D / 2); cc < (half + 1) * (D / 2); cc += 32) {
+                float o[32];
+                tmem_ld32(lane_addr + COL_O + cc, o);
                 if (row_valid) {
 #pragma unroll
                     for (int c = 0; c < 32; c += 8) {
@@ -548,8 +633,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         T *e = reinterpret_cast<T *>(&pkt);
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
-                            e[u] = kvc::Elem<T>::from_f32(v[c + u] * inv);
-                        *reinterpret_cast<uint4 *>(dst + c0 + c) = pkt;
+                            e[u] = kvc::Elem<T>::from_f32(o[c + u] * inv);
+                        *reinterpret_cast<uint4 *>(dst + cc + c) = pkt;
                     }
                 }
             }
@@ -598,7 +683,12 @@ kvc_status launch_prefill_tc(void *out, const void *q, const void *k_rows, const
     a.sin_t = sin_t;
     a.rope_max_pos = rope_max_pos;
     a.status = status;
-    const size_t smem = SM::TOTAL + 1024;
+    int dev = 0, optin = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    const size_t smem = std::min<size_t>((size_t)SM::TOTAL + 1024, (size_t)optin);
+    if (smem < (size_t)SM::TOTAL)
+        return KVC_ERR_UNSUPPORTED;
     auto kern = prefill_tc_kernel<T, D>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)

@@ -60,6 +60,7 @@ class Lengths:
 
     def __init__(self, batch: int, device):
         self.buf = torch.empty((5, batch), dtype=torch.int32, device=device)
+        self._c = KvcLengths(*[self.buf[i].data_ptr() for i in range(5)])
 
     def __getattr__(self, name):
         if name in Lengths.FIELDS:
@@ -67,7 +68,7 @@ class Lengths:
         raise AttributeError(name)
 
     def c(self) -> KvcLengths:
-        return KvcLengths(*[self.buf[i].data_ptr() for i in range(5)])
+        return self._c
 
 
 _lib = None
