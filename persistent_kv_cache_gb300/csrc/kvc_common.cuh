@@ -113,6 +113,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, but the hardware may suspend the thread for up to
+// `hint_ns` nanoseconds while the phase is incomplete instead of returning at
+// once, so a waiting warp does not take issue slots from its neighbours.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                    uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+                 : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity; returns false after about one
 // second (the caller records KVC_DEV_TIMEOUT and winds down).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
@@ -142,6 +158,17 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 3-D tiled TMA load (see tma_load_2d; x is the innermost coordinate)
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map, int32_t x,
+                                            int32_t y, int32_t z, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -190,6 +217,12 @@ int sm_count();
 // (no link-time dependency on libcuda)
 bool encode_2d_bf16_sw128(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                           uint32_t box_rows, CUtensorMapDataType type);
+
+// 3-D view of a [rows, cols] 16-bit matrix as (64 columns, rows, cols / 64
+// column blocks) with 128-byte swizzle; a box of (64, box_rows, box_blocks)
+// lands in shared memory as box_blocks consecutive [box_rows][128 B] blocks
+bool encode_3d_sw128(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows, uint32_t box_blocks, CUtensorMapDataType type);
 
 } // namespace kvc_host
 

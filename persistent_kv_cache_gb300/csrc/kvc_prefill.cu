@@ -6,28 +6,29 @@
 // 16-bit path: one CTA per (query block, kv head, batch row) on the 5th-gen
 // tensor cores.  The M = 128 tile packs the GQA group: row m holds query head
 // m / QB of the group and query qb * QB + m % QB (QB = 128 / group), so every
-// K/V tile is read once for all heads of the group.  Q, S, P and O all live
-// in tensor memory, which leaves shared memory to the K and V rings:
+// K/V tile is read once for all heads of the group.  Key tiles are 128 rows.
 //
-//   TMEM columns  O [0, D) fp32 | S/P double buffer [D, D + 128) | Q [.., + D/2)
-//   warp 0        TMA producer of 64-row K tiles (128-byte swizzled boxes of
-//                 64 columns) into an NK-stage ring; a stage is refilled as
-//                 soon as the S MMA that read it has completed
-//   warp 2        the same for V (NV stages), refilled after the PV MMA
-//   warp 1        allocates tensor memory and issues tcgen05.mma in the order
+//   TMEM columns  O [0, D) fp32 | S/P double buffer [D, D + 256)
+//   shared mem    Q tile (128 x D, 128-byte swizzled) | ring of 16 KB slabs
+//   warp 0        allocates tensor memory and issues tcgen05.mma in the order
 //                 S_0, S_1, PV_0, S_2, PV_1, ...:
-//                   S_j = Q K_j^T   A = Q in TMEM, B = K tile (K-major)
-//                   O  += P_j V_j   A = P_j in TMEM, B = V tile (MN-major)
+//                   S_j = Q K_j^T   A = Q (shared), B = K slabs (K-major)
+//                   O  += P_j V_j   A = P_j in TMEM, B = V slabs (MN-major)
 //                 so the next scores are always queued behind the current PV
-//   warps 3-10    two threads per row (= TMEM lane), each owning half of the
-//                 score columns and half of O: rotate the query row into
-//                 TMEM, then per tile read its S_j half, mask only tiles the
+//   warps 1-8     two threads per row (= TMEM lane), each owning half of the
+//                 score columns and half of O: rotate the query row into the
+//                 Q tile, then per tile read its S_j half, mask only tiles the
 //                 window or diagonal cuts, exchange the row max with the
 //                 partner thread, online softmax in the log2 domain (the
 //                 running max is only raised when it grows by more than 2^8,
 //                 exact after the final division), write P_j as 16-bit pairs
 //                 over S_j, rescale its half of O when the max moved, and at
 //                 the end divide by l and store its half of the output row.
+//   warp 9        TMA producer: streams the K and V slabs into the ring in
+//                 the order the tensor pipe consumes them (K_0, K_1, V_0,
+//                 K_2, V_1, ...), one 3-D box of up to 32 KB per slot (the
+//                 cost of a TMA operation hardly grows from 16 KB to 32 KB,
+//                 so large boxes double the bytes a single stream delivers).
 // Every mbarrier wait is bounded; a timeout sets KVC_DEV_TIMEOUT, every role
 // winds down, outstanding tensor-core work is drained and TMEM is freed.
 //
@@ -40,8 +41,9 @@
 namespace {
 
 constexpr int kBM = 128;       // rows of the M tile (query heads x queries)
-constexpr int kBN = 64;        // KV rows per tile
-constexpr int kThreads = 352;  // 11 warps
+constexpr int kBN = 128;       // KV rows per tile
+constexpr int kSoftmaxWarps = 8;
+constexpr int kThreads = 32 * (1 + kSoftmaxWarps + 1);  // MMA, softmax x 8, TMA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -73,6 +75,17 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar)
         : "memory");
 }
 
+// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16, one CTA
+__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem desc], kind::f16: A's rows are TMEM lanes and
 // its 16-bit elements are packed two per 32-bit column
 __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
@@ -86,23 +99,6 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
 }
 
 // 32-bit words to consecutive columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_st_words(uint32_t taddr, const uint32_t (&w)[8])
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
-                     taddr),
-                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
-                 "r"(w[7])
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_st_words(uint32_t taddr, const uint32_t (&w)[16])
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
-                 "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]),
-                 "r"(w[13]), "r"(w[14]), "r"(w[15])
-                 : "memory");
-}
 
 // 32 consecutive fp32 columns of this thread's TMEM lane
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
@@ -183,7 +179,6 @@ template <typename T> __device__ __forceinline__ uint32_t pack2(float lo, float 
     }
 }
 
-__device__ __forceinline__ int t_lo_of(int lo, int j) { return lo + j * 64; }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand: rows of
 // 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), `lbo` bytes
@@ -224,21 +219,28 @@ struct PrefillArgs {
 };
 
 template <int D> struct PrefillSmem {
-    static constexpr int KV_TILE = kBN * D * 2;          // D/64 boxes of 64 x 64
-    static constexpr int NK = D >= 256 ? 3 : 4;          // K ring depth
-    static constexpr int NV = D >= 256 ? 3 : 4;          // V ring depth
-    static constexpr int K_OFF = 0;
-    static constexpr int V_OFF = K_OFF + NK * KV_TILE;
-    static constexpr int BAR_OFF = V_OFF + NV * KV_TILE;
-    // barriers: k_full[4], k_empty[4], v_full[4], v_empty[4], s_full[2],
-    //           p_full[2], o_done[2], q_full, drain -> 24 x 8 bytes
-    static constexpr int MISC_OFF = BAR_OFF + 24 * 8;  // tmem addr, abort flag
-    static constexpr int RED_OFF = MISC_OFF + 16;      // row max / sum exchange, 4 x 128 floats
+    // A TMA operation costs about the same for 16 KB as for 32 KB, so each
+    // ring slot is filled by one 3-D box of up to 32 KB.
+    static constexpr int TILE = kBN * D * 2;             // one K (or V) tile
+    static constexpr int SLAB = TILE < 32768 ? TILE : 32768;
+    static constexpr int NSLAB_T = TILE / SLAB;          // slabs per K (or V) tile
+    static constexpr int DB = SLAB / (kBN * 128);        // 64-column blocks per K slab
+    static constexpr int KPS = SLAB / (D * 2);           // keys per V slab
+    static constexpr int Q_BYTES = kBM * D * 2;          // D/64 boxes of 128 x 64
+    static constexpr int NSLAB_MAX = (220 * 1024 - Q_BYTES) / SLAB;
+    static constexpr int NSLAB = NSLAB_MAX < 12 ? NSLAB_MAX : 12;  // ring depth
+    static constexpr int Q_OFF = 0;
+    static constexpr int RING_OFF = Q_OFF + Q_BYTES;
+    static constexpr int BAR_OFF = RING_OFF + NSLAB * SLAB;
+    // barriers: full[NSLAB], empty[NSLAB], s_full[2], p_full[2], o_done[2],
+    //           q_full, drain
+    static constexpr int NBAR = 2 * NSLAB + 8;
+    static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;  // tmem addr, abort flag
+    static constexpr int RED_OFF = MISC_OFF + 16;        // row max / sum exchange, 4 x 128 floats
     static constexpr int TOTAL = RED_OFF + 4 * kBM * 4;
-    // TMEM columns: O [0, D), S double buffer [D, D + 128), Q [D + 128, D + 128 + D/2)
-    static constexpr uint32_t COL_O = 0, COL_S = D, COL_Q = D + 2 * kBN;
-    static constexpr uint32_t TMEM_NEED = D + 2 * kBN + D / 2;
-    static constexpr uint32_t TMEM_COLS = TMEM_NEED <= 256 ? 256 : 512;
+    // TMEM columns: O [0, D) fp32 | S/P double buffer [D, D + 256)
+    static constexpr uint32_t COL_O = 0, COL_S = D;
+    static constexpr uint32_t TMEM_COLS = 512;
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
@@ -248,9 +250,9 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
         return true;
     const uint64_t t0 = kvc::global_ns();
     for (uint32_t i = 0;; ++i) {
-        if (kvc::mbar_try_wait(bar, parity))
+        if (kvc::mbar_try_wait_sleep(bar, parity, 20000))
             return true;
-        if ((i & 63u) == 63u) {
+        if ((i & 7u) == 7u) {
             if (*abort_flag)
                 return false;
             if (kvc::global_ns() - t0 > kvc::kWaitLimitNs) {
@@ -262,33 +264,26 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     }
 }
 
-// Stream one operand's 64-row tiles through a ring of NST shared-memory
-// stages: stage j % NST is reloaded once the MMA that read its previous
-// tile has completed (`empty`, signalled by tcgen05.commit).
-template <int NST, int BOXES, int KV_TILE>
-__device__ __forceinline__ void produce_tiles(const CUtensorMap *map, uint8_t *ring,
-                                              uint64_t *full, uint64_t *empty, int64_t row0,
-                                              int ntiles, volatile int *abort_flag,
-                                              int32_t *status)
+// The K and V slabs stream through one ring in the order the tensor pipe
+// consumes them: K_0, K_1, then V_j followed by K_{j+2} while that tile
+// exists, so the tail is ..., V_{n-2}, V_{n-1}.  Group g of that order is
+// one (operand, tile); each group is D/64 slabs.
+__device__ __forceinline__ void slab_group(int g, int ntiles, bool &is_v, int &tile)
 {
-    kvc::tma_prefetch_desc(map);
-    int issued = 0;
-    for (int j = 0; j < ntiles; ++j) {
-        const int st = j % NST;
-        if (j >= NST && !wait_or_abort(&empty[st], ((j / NST) - 1) & 1, abort_flag, status))
-            break;
-        uint8_t *dst = ring + st * KV_TILE;
-        kvc::mbar_arrive_expect_tx(&full[st], KV_TILE);
-        const int32_t y = (int32_t)(row0 + j * kBN);
-#pragma unroll
-        for (int bx = 0; bx < BOXES; ++bx)
-            kvc::tma_load_2d(dst + bx * (kBN * 128), map, bx * 64, y, &full[st]);
-        issued = j + 1;
+    const int lead = ntiles < 2 ? ntiles : 2;
+    if (g < lead) {
+        is_v = false;
+        tile = g;
+        return;
     }
-    if (*abort_flag) {
-        // wind-down: let the loads already in flight land before the CTA exits
-        for (int j = max(0, issued - NST); j < issued; ++j)
-            kvc::mbar_wait(&full[j % NST], (j / NST) & 1);
+    const int r = g - lead;
+    const int paired = ntiles > 2 ? ntiles - 2 : 0;  // tiles j with a K_{j+2} after V_j
+    if (r < 2 * paired) {
+        is_v = (r & 1) == 0;
+        tile = is_v ? (r >> 1) : (r >> 1) + 2;
+    } else {
+        is_v = true;
+        tile = paired + (r - 2 * paired);
     }
 }
 
@@ -299,11 +294,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
 {
     using SM = PrefillSmem<D>;
     constexpr int BOXES = D / 64;
-    constexpr int NK = SM::NK, NV = SM::NV;
+    constexpr int NSLAB = SM::NSLAB, NST = SM::NSLAB_T, KPS = SM::KPS, DB = SM::DB;
     constexpr uint32_t AB = std::is_same<T, __half>::value ? 0u : 1u;
     constexpr uint32_t IDESC_S = f16_idesc(AB, 0, kBM, kBN);
     constexpr uint32_t IDESC_O = f16_idesc(AB, 1, kBM, D);
-    constexpr uint32_t COL_O = SM::COL_O, COL_S = SM::COL_S, COL_Q = SM::COL_Q;
+    constexpr uint32_t COL_O = SM::COL_O, COL_S = SM::COL_S;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -320,9 +315,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
     }
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SM::BAR_OFF);
-    uint64_t *k_full = bars + 0, *k_empty = bars + 4, *v_full = bars + 8, *v_empty = bars + 12,
-             *s_full = bars + 16, *p_full = bars + 18, *o_done = bars + 20, *q_full = bars + 22,
-             *drain = bars + 23;
+    uint64_t *full = bars, *empty = bars + NSLAB, *s_full = bars + 2 * NSLAB,
+             *p_full = s_full + 2, *o_done = s_full + 4, *q_full = s_full + 6,
+             *drain = s_full + 7;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SM::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::MISC_OFF + 4);
 
@@ -355,14 +350,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     if (a.window > 0)
         lo = max(0, Lp + q0 - a.window + 1);
     const int ntiles = (hi - lo + kBN) / kBN;
+    const int nslabs = 2 * ntiles * NST;
     const int64_t row_base = ((int64_t)b * a.kv_heads + kvh) * a.rows_per_head;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 4; ++i) {
-            kvc::mbar_init(&k_full[i], 1);
-            kvc::mbar_init(&k_empty[i], 1);
-            kvc::mbar_init(&v_full[i], 1);
-            kvc::mbar_init(&v_empty[i], 1);
+        for (int i = 0; i < NSLAB; ++i) {
+            kvc::mbar_init(&full[i], 1);
+            kvc::mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             kvc::mbar_init(&s_full[i], 1);
@@ -374,7 +368,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         *abort_flag = 0;
         kvc::fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == 0) {
         tmem_alloc(tmem_slot, SM::TMEM_COLS);
         tc_fence_before();
     }
@@ -383,57 +377,98 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const uint32_t tmem = *tmem_slot;
     const uint32_t smem_base = kvc::smem_u32(smem);
 
-    if (warp == 0) {
-        // ======================= K producer =======================
-        if (lane == 0)
-            produce_tiles<NK, BOXES, SM::KV_TILE>(&tmap_k, smem + SM::K_OFF, k_full, k_empty,
-                                                  row_base + lo, ntiles, abort_flag, a.status);
-    } else if (warp == 2) {
-        // ======================= V producer =======================
-        if (lane == 0)
-            produce_tiles<NV, BOXES, SM::KV_TILE>(&tmap_v, smem + SM::V_OFF, v_full, v_empty,
-                                                  row_base + lo, ntiles, abort_flag, a.status);
-    } else if (warp == 1) {
+    if (warp == 1 + kSoftmaxWarps) {
+        // ======================= TMA producer =======================
+        // one 3-D box per ring slot: a K slab is DB column blocks of 128 rows,
+        // a V slab is KPS rows of every column block (128-byte swizzled rows)
+        if (lane == 0) {
+            kvc::tma_prefetch_desc(&tmap_k);
+            kvc::tma_prefetch_desc(&tmap_v);
+            int issued = 0;
+            for (int q = 0; q < nslabs; ++q) {
+                const int slot = q % NSLAB;
+                if (q >= NSLAB &&
+                    !wait_or_abort(&empty[slot], ((q / NSLAB) - 1) & 1, abort_flag, a.status))
+                    break;
+                bool is_v;
+                int tile;
+                slab_group(q / NST, ntiles, is_v, tile);
+                const int sl = q % NST;
+                uint8_t *dst = smem + SM::RING_OFF + slot * SM::SLAB;
+                const int32_t y0 = (int32_t)(row_base + lo + tile * kBN);
+                kvc::mbar_arrive_expect_tx(&full[slot], SM::SLAB);
+                if (!is_v)
+                    kvc::tma_load_3d(dst, &tmap_k, 0, y0, sl * DB, &full[slot]);
+                else
+                    kvc::tma_load_3d(dst, &tmap_v, 0, y0 + sl * KPS, 0, &full[slot]);
+                issued = q + 1;
+            }
+            if (*abort_flag) {
+                // wind-down: let the loads already in flight land before the CTA exits
+                for (int q = max(0, issued - NSLAB); q < issued; ++q)
+                    kvc::mbar_wait(&full[q % NSLAB], (q / NSLAB) & 1);
+            }
+        }
+    } else if (warp == 0) {
         // ======================= MMA issuer =======================
-        // tensor-pipe order: S_0, S_1, PV_0, S_2, PV_1, S_3, ...  S_{j+2}
-        // reuses the TMEM buffer that holds P_j, after PV_j in issue order
+        // tensor-pipe order: S_0, S_1, PV_0, S_2, PV_1, ...  S_{j+2} reuses the
+        // TMEM buffer that holds P_j, after PV_j in issue order
         if (lane == 0) {
             bool ok = wait_or_abort(q_full, 0, abort_flag, a.status);
+            int q = 0;  // next slab of the ring, in consumption order
             auto issue_s = [&](int j) -> bool {
-                const int ks = j % NK;
-                if (!wait_or_abort(&k_full[ks], (j / NK) & 1, abort_flag, a.status))
-                    return false;
-                tc_fence_after();
-                const uint32_t kb = smem_base + SM::K_OFF + ks * SM::KV_TILE;
+                const uint32_t qa = smem_base + SM::Q_OFF;
+                for (int sl = 0; sl < NST; ++sl, ++q) {
+                    const int slot = q % NSLAB;
+                    if (!wait_or_abort(&full[slot], (q / NSLAB) & 1, abort_flag, a.status))
+                        return false;
+                    tc_fence_after();
+                    const uint32_t kb = smem_base + SM::RING_OFF + slot * SM::SLAB;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t box = kk >> 2, within = (kk & 3) * 32;
-                    const uint64_t bd = sw128_desc(kb + box * (kBN * 128) + within, 16);
-                    tc_mma_ts(tmem + COL_S + (j & 1) * kBN, tmem + COL_Q + kk * 8, bd, IDESC_S,
-                              kk > 0);
+                    for (int blk = 0; blk < DB; ++blk) {
+                        const int box = sl * DB + blk;  // 64-column block of D
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4) {
+                            const int kk = box * 4 + k4;
+                            const uint64_t ad = sw128_desc(qa + box * (kBM * 128) + k4 * 32, 16);
+                            const uint64_t bd = sw128_desc(kb + blk * (kBN * 128) + k4 * 32, 16);
+                            tc_mma_ss(tmem + COL_S + (j & 1) * kBN, ad, bd, IDESC_S, kk > 0);
+                        }
+                    }
+                    tc_commit(&empty[slot]);
                 }
                 tc_commit(&s_full[j & 1]);
-                tc_commit(&k_empty[ks]);
                 return true;
             };
             for (int j = 0; ok && j < 2 && j < ntiles; ++j)
                 ok = issue_s(j);
             for (int j = 0; ok && j < ntiles; ++j) {
-                const int s = j & 1, vs = j % NV;
-                ok = wait_or_abort(&p_full[s], (j >> 1) & 1, abort_flag, a.status) &&
-                     wait_or_abort(&v_full[vs], (j / NV) & 1, abort_flag, a.status);
+                const int s = j & 1;
+                if (!wait_or_abort(&p_full[s], (j >> 1) & 1, abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int sl = 0; sl < NST && ok; ++sl, ++q) {
+                    const int slot = q % NSLAB;
+                    if (!wait_or_abort(&full[slot], (q / NSLAB) & 1, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t vb = smem_base + SM::RING_OFF + slot * SM::SLAB;
+#pragma unroll
+                    for (int k2 = 0; k2 < KPS / 16; ++k2) {
+                        const int kk = sl * (KPS / 16) + k2;  // 16-key step within the tile
+                        const uint64_t bd = sw128_desc(vb + k2 * 2048, KPS * 128);
+                        tc_mma_ts(tmem + COL_O, tmem + COL_S + s * kBN + kk * 8, bd, IDESC_O,
+                                  (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&empty[slot]);
+                }
                 if (!ok)
                     break;
-                tc_fence_after();
-                const uint32_t vb = smem_base + SM::V_OFF + vs * SM::KV_TILE;
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t bd = sw128_desc(vb + kk * 2048, kBN * 128);
-                    tc_mma_ts(tmem + COL_O, tmem + COL_S + s * kBN + kk * 8, bd, IDESC_O,
-                              (j > 0 || kk > 0) ? 1u : 0u);
-                }
                 tc_commit(&o_done[s]);
-                tc_commit(&v_empty[vs]);
                 if (j + 2 < ntiles)
                     ok = issue_s(j + 2);
             }
@@ -445,8 +480,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     } else {
         // ======================= softmax / epilogue =======================
         // two warps per TMEM lane quadrant: `half` 0 owns score columns
-        // [0, 32) of every tile and O columns [0, D/2), `half` 1 the rest
-        const int sw = warp - 3;                   // 0..7
+        // [0, 64) of every tile and O columns [0, D/2), `half` 1 the rest
+        const int sw = warp - 1;                   // 0..7
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
         const int half = sw >> 2;
         const int m = quad * 32 + lane;            // tile row == TMEM lane
@@ -458,18 +493,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         float *red = reinterpret_cast<float *>(smem + SM::RED_OFF);  // [2 tiles][2 halves][128]
         const uint32_t pair_bar = 1 + quad;       // named barrier of the two warps of a quadrant
 
-        // query row: rotate at absolute position P + ii and store it as packed
-        // 16-bit pairs in TMEM (row m = lane m; element e in column COL_Q + e/2).
-        // Each half takes half of the rotation pairs (i, i + D/2).
+        // query row: rotate at absolute position P + ii and stage it as 16-bit
+        // in the swizzled Q tile (row m of each 64-column box); each half
+        // takes half of the rotation pairs (i, i + D/2)
         {
-            constexpr int NW = D / 8;  // words of each half's lo (and hi) part
-            uint32_t wlo[NW], whi[NW];
             const T *qsrc = static_cast<const T *>(a.q) + qrow * D;
             const float *cs = (a.cos_t && row_valid) ? a.cos_t + (int64_t)(P + ii) * (D / 2) : nullptr;
             const float *sn = (a.cos_t && row_valid) ? a.sin_t + (int64_t)(P + ii) * (D / 2) : nullptr;
-#pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                const int c = half * (D / 32) + cc;  // chunk of 8 elements in the low half
+            uint8_t *qt = smem + SM::Q_OFF;
+#pragma unroll 1
+            for (int c = half * (D / 32); c < (half + 1) * (D / 32); ++c) {
                 uint4 lo4 = make_uint4(0, 0, 0, 0), hi4 = make_uint4(0, 0, 0, 0);
                 if (row_valid) {
                     lo4 = *reinterpret_cast<const uint4 *>(qsrc + c * 8);
@@ -486,15 +519,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         hv[e] = kvc::Elem<T>::from_f32(y);
                     }
                 }
-                wlo[cc * 4 + 0] = lo4.x; wlo[cc * 4 + 1] = lo4.y;
-                wlo[cc * 4 + 2] = lo4.z; wlo[cc * 4 + 3] = lo4.w;
-                whi[cc * 4 + 0] = hi4.x; whi[cc * 4 + 1] = hi4.y;
-                whi[cc * 4 + 2] = hi4.z; whi[cc * 4 + 3] = hi4.w;
+                const int clo = c, chi = D / 16 + c;  // 16-byte chunk index along D
+                *reinterpret_cast<uint4 *>(qt + (clo >> 3) * (kBM * 128) + kvc::sw128(m, clo & 7)) = lo4;
+                *reinterpret_cast<uint4 *>(qt + (chi >> 3) * (kBM * 128) + kvc::sw128(m, chi & 7)) = hi4;
             }
-            tmem_st_words(lane_addr + COL_Q + half * NW, wlo);
-            tmem_st_words(lane_addr + COL_Q + D / 4 + half * NW, whi);
-            tmem_wait_st();
-            tc_fence_before();
+            kvc::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
                 kvc::mbar_arrive(q_full);
@@ -508,28 +537,38 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
             const int s = j & 1;
-            const int t_lo = t_lo_of(lo, j);
-            const int c0 = t_lo + 32 * half;  // key row of my first column
+            const int t_lo = lo + j * kBN;
+            const int c0 = t_lo + 64 * half;  // key row of my first column
             if (!wait_or_abort(&s_full[s], (j >> 1) & 1, abort_flag, a.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            float v[32];
-            tmem_ld32(lane_addr + COL_S + s * kBN + 32 * half, v);
+            float v[64];
+            {
+                float w[32];
+                tmem_ld32(lane_addr + COL_S + s * kBN + 64 * half, w);
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    v[c] = w[c];
+                tmem_ld32(lane_addr + COL_S + s * kBN + 64 * half + 32, w);
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    v[32 + c] = w[c];
+            }
 
             // mask only where the window or the diagonal cuts these columns
-            const bool all_in = row_valid && c0 >= r_lo && c0 + 31 <= r_hi;
+            const bool all_in = row_valid && c0 >= r_lo && c0 + 63 <= r_hi;
             if (!all_in) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
+                for (int c = 0; c < 64; ++c) {
                     const int r = c0 + c;
                     v[c] = (row_valid && r >= r_lo && r <= r_hi) ? v[c] : -INFINITY;
                 }
             }
             float mx0 = fmaxf(v[0], v[1]), mx1 = fmaxf(v[2], v[3]);
 #pragma unroll
-            for (int c = 4; c < 32; c += 4) {
+            for (int c = 4; c < 64; c += 4) {
                 mx0 = fmaxf(mx0, fmaxf(v[c], v[c + 1]));
                 mx1 = fmaxf(mx1, fmaxf(v[c + 2], v[c + 3]));
             }
@@ -552,9 +591,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             }
             const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
             float ps0 = 0.f, ps1 = 0.f;
-            uint32_t pk[16];
+            uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) {
+            for (int c = 0; c < 64; c += 2) {
                 const float p0 = fast_exp2(fmaf(v[c], c_log2, neg_m));
                 const float p1 = fast_exp2(fmaf(v[c + 1], c_log2, neg_m));
                 ps0 += p0;
@@ -563,25 +602,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             }
             l_run = l_run * alpha + (ps0 + ps1);
             // P_j (16-bit pairs) over the S_j columns of this row
-            tmem_st_words(lane_addr + COL_S + s * kBN + 16 * half, pk);
+            tmem_st_words(lane_addr + COL_S + s * kBN + 32 * half, pk);
 
-            // rows past the last visible row of the block: zero V so that
-            // 0 * (stale or uninitialised bytes) stays 0 in O += P V
+            // rows past the last visible row of the block (last tile only):
+            // zero them in the V slabs so that 0 * (stale or uninitialised
+            // bytes) stays 0 in O += P V
             if (t_lo + kBN - 1 > hi) {
-                const int vs = j % NV;
-                if (!wait_or_abort(&v_full[vs], (j / NV) & 1, abort_flag, a.status)) {
-                    ok = false;
+                const int first_bad = hi + 1 - t_lo;  // rows [first_bad, 128) of the tile
+                const int q_first = (2 * ntiles - 1) * NST;  // V_{n-1} is the last group
+                for (int sl = first_bad / KPS; sl < NST; ++sl) {
+                    const int q = q_first + sl;
+                    if (!wait_or_abort(&full[q % NSLAB], (q / NSLAB) & 1, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *vt = smem + SM::RING_OFF + (q % NSLAB) * SM::SLAB;
+                    const int r0 = max(0, first_bad - sl * KPS);  // first bad row in this slab
+                    const int nbad = KPS - r0;
+                    for (int idx = threadIdx.x - 32; idx < nbad * BOXES * 8; idx += 256) {
+                        const int rr = r0 + idx / (BOXES * 8);
+                        const int bx = (idx / 8) % BOXES, cc = idx % 8;
+                        *reinterpret_cast<uint4 *>(vt + bx * (KPS * 128) + rr * 128 + cc * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                }
+                if (!ok)
                     break;
-                }
-                const int first_bad = hi + 1 - t_lo;  // rows [first_bad, 64) of the tile
-                uint8_t *vt = smem + SM::V_OFF + vs * SM::KV_TILE;
-                const int nbad = kBN - first_bad;
-                for (int idx = threadIdx.x - 96; idx < nbad * BOXES * 8; idx += 256) {
-                    const int rr = first_bad + idx / (BOXES * 8);
-                    const int bx = (idx / 8) % BOXES, cc = idx % 8;
-                    *reinterpret_cast<uint4 *>(vt + bx * (kBN * 128) + rr * 128 + cc * 16) =
-                        make_uint4(0, 0, 0, 0);
-                }
                 kvc::fence_proxy_async_smem();
             }
 
@@ -643,7 +689,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
 
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, SM::TMEM_COLS);
     }
@@ -657,15 +703,15 @@ kvc_status launch_prefill_tc(void *out, const void *q, const void *k_rows, const
                              cudaStream_t stream)
 {
     using SM = PrefillSmem<D>;
-    const CUtensorMapDataType tt = std::is_same<T, __half>::value
-                                       ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const uint64_t rows = (uint64_t)batch * kv_heads * R;
     if (rows > (uint64_t)INT32_MAX)
         return KVC_ERR_SHAPE;
+    const CUtensorMapDataType tt = std::is_same<T, __half>::value
+                                       ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap tk, tv;
-    if (!kvc_host::encode_2d_bf16_sw128(&tk, k_rows, rows, D, kBN, tt) ||
-        !kvc_host::encode_2d_bf16_sw128(&tv, v_rows, rows, D, kBN, tt))
+    if (!kvc_host::encode_3d_sw128(&tk, k_rows, rows, D, kBN, SM::DB, tt) ||
+        !kvc_host::encode_3d_sw128(&tv, v_rows, rows, D, SM::KPS, D / 64, tt))
         return KVC_ERR_CUDA;
     PrefillArgs a;
     a.out = out;

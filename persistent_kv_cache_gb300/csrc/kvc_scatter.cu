@@ -107,8 +107,7 @@ int sm_count()
     return cached[dev];
 }
 
-bool encode_2d_bf16_sw128(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
-                          uint32_t box_rows, CUtensorMapDataType type)
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -120,6 +119,29 @@ bool encode_2d_bf16_sw128(CUtensorMap *map, const void *base, uint64_t rows, uin
             q == cudaDriverEntryPointSuccess)
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     });
+    return fn;
+}
+
+bool encode_3d_sw128(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows, uint32_t box_blocks, CUtensorMapDataType type)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn || cols % 64 != 0)
+        return false;
+    cuuint64_t dims[3] = {64, rows, cols / 64};
+    cuuint64_t strides[2] = {cols * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, box_blocks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, type, 3, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool encode_2d_bf16_sw128(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                          uint32_t box_rows, CUtensorMapDataType type)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn)
         return false;
     cuuint64_t dims[2] = {cols, rows};
