@@ -10,7 +10,9 @@ The ~570 MB the step reads exceed the 129 MB L2, so no flush is needed.
 Other workloads (--workload):
   window-decode   64 x 64/8 heads x 64, C = W = 128, T0 ~ U[1, 32768];
                   one step = lengths + in-place compaction/append + decode on
-                  one of 16 replica caches in turn (268 MB > L2, "cold")
+                  one of 16 replica caches in turn (268 MB > L2, "cold"), as
+                  one fused kvc_window_decode_step launch
+  window-decode-unfused  the same as three launches
   window-prefill  8 x 16/8 heads x 256, C = W = 4096, P ~ U[0, 20000],
                   --chunk S in {64, 512, 2048}; one step = lengths + staging
                   seed/append + tcgen05 chunk attention + copy-back
@@ -254,13 +256,18 @@ class ContigDecode(Workload):
 
 class WindowDecode(Workload):
     """Sliding-window ring cache decode with in-place compaction (E <= 1),
-    cycling over 16 replica caches (one per model layer, 268 MB in all)."""
-    roofline_kernel = "kvc_gqa_decode (window decode)"
-    traffic_key = ("kvc_decode.cu", "decode_split_kernel_window")
+    cycling over 16 replica caches (one per model layer, 268 MB in all).
+    fused=True runs each step as one kvc_window_decode_step launch; otherwise
+    as kvc_seq_lengths + kvc_window_append + kvc_gqa_decode."""
     bound = "hbm"
     replicas = 16
+    fused = True
 
     def __init__(self, dev, seed=0, with_kernels=True, chunk=None, max_steps=4096):
+        self.roofline_kernel = ("kvc_window_decode_step (fused step)" if self.fused
+                                else "kvc_gqa_decode (window decode)")
+        self.traffic_key = ("kvc_decode.cu",
+                            "window_step_kernel" if self.fused else "decode_split_kernel_window")
         import torch
 
         from persistent_kv_cache_gb300 import synth
@@ -287,14 +294,16 @@ class WindowDecode(Workload):
         cos, sin = synth.rope_cache(int(self.T0.max()) + n_rounds + 1, D, w.theta)
         self.rope = (cos.to(dev), sin.to(dev))
         e = self.e
-        # resident rows after the step: min(T, C); the shift moves C - 1 rows once full
+        # Algorithmic bytes of one step: the window's K/V rows read once, the
+        # rows the eviction moves written back one row lower, the new K/V
+        # rows read and written, q read, out written.
         T = self.T0.astype(np.int64) + 1
         L = np.minimum(T, C)
         moved = np.where(T > C, C - 1, 0)
-        self.kernel_bytes = int(L.sum()) * Hkv * D * 2 * e + 2 * B * Hq * D * e
-        self.append_bytes = (2 * 2 * int(moved.sum()) * Hkv * D * e
-                             + 2 * 2 * B * Hkv * D * e)
-        self.bytes_per_step = self.kernel_bytes + self.append_bytes
+        attn = int(L.sum()) * Hkv * D * 2 * e + 2 * B * Hq * D * e
+        self.bytes_per_step = (attn + int(moved.sum()) * Hkv * D * 2 * e
+                               + 2 * 2 * B * Hkv * D * e)
+        self.kernel_bytes = self.bytes_per_step if self.fused else attn
         self.tokens_per_step = B
         if not with_kernels:
             return
@@ -304,11 +313,16 @@ class WindowDecode(Workload):
         self.ws = K.decode_workspace(self.out, self.kc[0])
         self.L = K.Lengths(B, dev)
         self.st = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.launches_per_step = 3
+        self.launches_per_step = 1 if self.fused else 3
 
     def step(self, i):
         K, w, R = self.K, self.w, self.replicas
         r = i % R
+        if self.fused:
+            K.kvc_window_decode_step(self.out, self.q, self.kc[r], self.vc[r], self.nk, self.nv,
+                                     self.sk_all[i // R], w.window, lengths=self.L,
+                                     rope=self.rope, status=self.st)
+            return
         K.kvc_seq_lengths(self.sk_all[i // R], 1, w.capacity, 1, local_window_size=w.window,
                           out=self.L, status=self.st)
         K.kvc_window_append(self.kc[r], self.vc[r], self.nk, self.nv, self.L, 1, rope=self.rope,
@@ -316,6 +330,9 @@ class WindowDecode(Workload):
         self.kernel(i)
 
     def kernel(self, i):
+        if self.fused:
+            self.step(i)
+            return
         r = i % self.replicas
         self.K.kvc_gqa_decode(self.out, self.q, self.kc[r], self.vc[r], self.L,
                               local_window_size=self.w.window, rope=self.rope, workspace=self.ws,
@@ -326,7 +343,7 @@ class WindowDecode(Workload):
         return {"workload": w.name, "batch": w.batch, "q_heads": w.q_heads,
                 "kv_heads": w.kv_heads, "head_dim": w.head_dim, "capacity": w.capacity,
                 "window": w.window, "start_total": f"U[{w.total_lo},{w.total_hi}]",
-                "replica_caches": self.replicas, "new_tokens": 1,
+                "replica_caches": self.replicas, "new_tokens": 1, "fused_step": self.fused,
                 "l2": "16 replica caches cycled (268 MB > L2)",
                 "bytes_per_step": self.bytes_per_step}
 
@@ -529,8 +546,13 @@ class Scatter(Workload):
         return "TensorScatter circular in place: GB/s of update bytes, steps/s", "GB/s"
 
 
+class WindowDecodeUnfused(WindowDecode):
+    fused = False
+
+
 WORKLOADS = {"contig-decode": ContigDecode, "window-decode": WindowDecode,
-             "window-prefill": WindowPrefill, "scatter": Scatter}
+             "window-decode-unfused": WindowDecodeUnfused, "window-prefill": WindowPrefill,
+             "scatter": Scatter}
 
 
 def kernel_traffic(key):
@@ -560,7 +582,7 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     n_steps = args.warmup * 2 + args.steps * 3 + 8
     kw = {"chunk": args.chunk}
-    if args.workload in ("window-decode", "scatter"):
+    if args.workload in ("window-decode", "window-decode-unfused", "scatter"):
         kw["max_steps"] = n_steps
     wl = WORKLOADS[args.workload](dev, seed=rank, **kw)
     peaks, peak_kind = load_peaks()

@@ -9,6 +9,7 @@
  *                          append (windowed cache, one token), or C + S
  *                          staging seed / copy-back (windowed, several tokens)
  *     kvc_gqa_decode       one-token GQA attention over the cache
+ *     kvc_window_decode_step  the three above fused for a windowed cache
  *     kvc_gqa_prefill_chunk  multi-token GQA attention over staged rows
  *     kvc_tensor_scatter   the ONNX TensorScatter cache update (linear/circular)
  *
@@ -254,6 +255,36 @@ size_t kvc_gqa_decode_workspace_size(int batch, int q_heads, int kv_heads, int64
 kvc_status kvc_gqa_decode_noalloc(void *out, const void *q, const void *k_cache,
                                   const void *v_cache, kvc_lengths len, int batch, int q_heads,
                                   int kv_heads, int64_t capacity, int head_dim, int dtype,
+                                  int local_window_size, float scale, const float *rope_cos,
+                                  const float *rope_sin, int64_t rope_max_pos,
+                                  int32_t *dev_status, void *stream);
+
+/*
+ * kvc_window_decode_step -- one fused one-token step on a windowed cache:
+ * kvc_seq_lengths + kvc_window_append (S = 1) + kvc_gqa_decode in a single
+ * launch, with the same results ("GQA support sliding_window_cache",
+ * "Design": Lp = min(P, C), E = max(0, Lp + 1 - C), rows [E, Lp) move to
+ * [0, Lp - E), the new row goes to Lp - E; attention over the window that
+ * results).  One CTA owns a (batch row, kv head) slice and reads it once:
+ * the whole window is loaded into shared memory, written back one row lower
+ * when a row was evicted, and attended over from there.  For small windows:
+ * capacity * head_dim <= 32768 (C <= 512 at D = 64, C <= 256 at D = 128),
+ * else KVC_ERR_UNSUPPORTED.
+ *
+ * out, q          device [batch, q_heads, 1, head_dim].
+ * k_cache/v_cache device [batch, kv_heads, capacity, head_dim], updated in place.
+ * new_k, new_v    device [batch, kv_heads, 1, head_dim].
+ * seqlens_k       device int32 [batch] (total after this token, minus one).
+ * len             the five length arrays to fill (as kvc_seq_lengths would,
+ *                 windowed, S = 1), or all five NULL.
+ * Requires 0 < local_window_size <= capacity (KVC_ERR_WINDOW).  Supported:
+ * KVC_BF16/KVC_F16, head_dim in {64, 128}, q_heads / kv_heads <= 16.
+ * Device errors as kvc_seq_lengths / kvc_window_append / kvc_gqa_decode.
+ */
+kvc_status kvc_window_decode_step(void *out, const void *q, void *k_cache, void *v_cache,
+                                  const void *new_k, const void *new_v, const int32_t *seqlens_k,
+                                  kvc_lengths len, int batch, int q_heads, int kv_heads,
+                                  int64_t capacity, int head_dim, int dtype,
                                   int local_window_size, float scale, const float *rope_cos,
                                   const float *rope_sin, int64_t rope_max_pos,
                                   int32_t *dev_status, void *stream);

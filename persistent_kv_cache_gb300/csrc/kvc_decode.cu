@@ -95,6 +95,166 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// Attention state of one consumer warp over 64-row K/V tiles held in shared
+// memory (128-byte swizzled boxes of 64 columns, 8 KB per box): the GQA
+// group's query heads are the M = 16 rows of mma.sync m16n8k16, the warp
+// owns rows [16 w, 16 w + 16) of every tile, and (m, l, o) follow the online
+// softmax in the log2 domain.  Thread t holds heads t/4 and t/4 + 8.
+template <typename T, int D> struct GroupAttn {
+    static constexpr int NB = D / 8;  // 8-column blocks of the output
+    uint32_t qa[D / 16][4];
+    float o[NB][4];
+    float m_lo, m_hi, l_lo, l_hi;
+
+    __device__ __forceinline__ void init()
+    {
+#pragma unroll
+        for (int n = 0; n < NB; ++n)
+            o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        m_lo = m_hi = -INFINITY;
+        l_lo = l_hi = 0.f;
+    }
+
+    // A fragments of the rotated query rows staged as qs[16][QS]
+    __device__ __forceinline__ void load_q(const T *qs, int QS, int lane)
+    {
+        const int row = lane >> 2, col = (lane & 3) * 2;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            qa[kk][0] = *reinterpret_cast<const uint32_t *>(&qs[row * QS + kk * 16 + col]);
+            qa[kk][1] = *reinterpret_cast<const uint32_t *>(&qs[(row + 8) * QS + kk * 16 + col]);
+            qa[kk][2] = *reinterpret_cast<const uint32_t *>(&qs[row * QS + kk * 16 + 8 + col]);
+            qa[kk][3] =
+                *reinterpret_cast<const uint32_t *>(&qs[(row + 8) * QS + kk * 16 + 8 + col]);
+        }
+    }
+
+    // One tile: rows [lo, hi) of this warp's 16 rows are visible (the caller
+    // guarantees that V rows at and past `hi` hold finite values).
+    __device__ __forceinline__ void tile(uint32_t kb, uint32_t vb, int warp, int lane, int lo,
+                                         int hi, float scale_log2)
+    {
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        const int mat = lane >> 3;
+        const int krow = 16 * warp + ((mat >> 1) << 3) + (lane & 7);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int cidx = 2 * kk + (mat & 1);
+            uint32_t r_0, r_1, r_2, r_3;
+            ldsm_x4(kb + (cidx >> 3) * 8192 + kvc::sw128(krow, cidx & 7), r_0, r_1, r_2, r_3);
+            Mma<T>::run(sc[0], qa[kk], r_0, r_1);
+            Mma<T>::run(sc[1], qa[kk], r_2, r_3);
+        }
+        float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int col = 8 * j + 2 * (lane & 3) + (e & 1);
+                float v = sc[j][e] * scale_log2;
+                v = (col >= lo && col < hi) ? v : -INFINITY;
+                sc[j][e] = v;
+                if (e < 2)
+                    mx_lo = fmaxf(mx_lo, v);
+                else
+                    mx_hi = fmaxf(mx_hi, v);
+            }
+        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+        const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+        // a row with nothing visible yet keeps m = -inf and contributes 0
+        const float ref_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
+        const float ref_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
+        const float al_lo = exp2f(m_lo - ref_lo), al_hi = exp2f(m_hi - ref_hi);
+        m_lo = mn_lo;
+        m_hi = mn_hi;
+        float ps_lo = 0.f, ps_hi = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            sc[j][0] = exp2f(sc[j][0] - ref_lo);
+            sc[j][1] = exp2f(sc[j][1] - ref_lo);
+            sc[j][2] = exp2f(sc[j][2] - ref_hi);
+            sc[j][3] = exp2f(sc[j][3] - ref_hi);
+            ps_lo += sc[j][0] + sc[j][1];
+            ps_hi += sc[j][2] + sc[j][3];
+        }
+        l_lo = l_lo * al_lo + ps_lo;
+        l_hi = l_hi * al_hi + ps_hi;
+#pragma unroll
+        for (int n = 0; n < NB; ++n) {
+            o[n][0] *= al_lo;
+            o[n][1] *= al_lo;
+            o[n][2] *= al_hi;
+            o[n][3] *= al_hi;
+        }
+        uint32_t pa[4];
+        pa[0] = Mma<T>::pack(sc[0][0], sc[0][1]);
+        pa[1] = Mma<T>::pack(sc[0][2], sc[0][3]);
+        pa[2] = Mma<T>::pack(sc[1][0], sc[1][1]);
+        pa[3] = Mma<T>::pack(sc[1][2], sc[1][3]);
+        const int vrow = 16 * warp + ((mat & 1) << 3) + (lane & 7);
+#pragma unroll
+        for (int nn = 0; nn < D / 16; ++nn) {
+            const int cidx = 2 * nn + (mat >> 1);
+            uint32_t r_0, r_1, r_2, r_3;
+            ldsm_x4_t(vb + (cidx >> 3) * 8192 + kvc::sw128(vrow, cidx & 7), r_0, r_1, r_2, r_3);
+            Mma<T>::run(o[2 * nn], pa, r_0, r_1);
+            Mma<T>::run(o[2 * nn + 1], pa, r_2, r_3);
+        }
+    }
+
+    // finish l across the quad and publish (m, l, o) of heads < g for the
+    // 4-warp merge: cm/cl [4][16], co [4][16][D]
+    __device__ __forceinline__ void publish(float *cm, float *cl, float *co, int warp, int lane,
+                                            int g)
+    {
+        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+        const int row = lane >> 2, col = 2 * (lane & 3);
+        if ((lane & 3) == 0) {
+            cm[warp * 16 + row] = m_lo;
+            cl[warp * 16 + row] = l_lo;
+            cm[warp * 16 + row + 8] = m_hi;
+            cl[warp * 16 + row + 8] = l_hi;
+        }
+#pragma unroll
+        for (int n = 0; n < NB; ++n) {
+            if (row < g) {
+                co[(warp * 16 + row) * D + 8 * n + col] = o[n][0];
+                co[(warp * 16 + row) * D + 8 * n + col + 1] = o[n][1];
+            }
+            if (row + 8 < g) {
+                co[(warp * 16 + row + 8) * D + 8 * n + col] = o[n][2];
+                co[(warp * 16 + row + 8) * D + 8 * n + col + 1] = o[n][3];
+            }
+        }
+    }
+};
+
+// merged (unnormalised o, l, reference max) of head h, column d over the
+// four warps' published partials
+__device__ __forceinline__ void merge4(const float *cm, const float *cl, const float *co, int D,
+                                       int h, int d, float &mstar, float &lsum, float &osum)
+{
+    mstar = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumers; ++w)
+        mstar = fmaxf(mstar, cm[w * 16 + h]);
+    const float ref = mstar == -INFINITY ? 0.f : mstar;
+    lsum = 0.f;
+    osum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumers; ++w) {
+        const float f = exp2f(cm[w * 16 + h] - ref);
+        lsum += cl[w * 16 + h] * f;
+        osum += co[(w * 16 + h) * D + d] * f;
+    }
+}
+
 struct DecodeArgs {
     void *out;
     const void *q;
@@ -121,7 +281,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     constexpr int KT_BYTES = kTile * D * 2;  // one K (or V) tile
     constexpr int STAGE_BYTES = 2 * KT_BYTES;
     constexpr int QS = D + 8;                // padded Q row (elements)
-    constexpr int NB = D / 8;                // n-blocks of the output
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -217,24 +376,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
     }
     consumer_sync();
-    uint32_t qa[D / 16][4];
-    {
-        const int row = lane >> 2, col = (lane & 3) * 2;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            qa[kk][0] = *reinterpret_cast<const uint32_t *>(&qs[row * QS + kk * 16 + col]);
-            qa[kk][1] = *reinterpret_cast<const uint32_t *>(&qs[(row + 8) * QS + kk * 16 + col]);
-            qa[kk][2] = *reinterpret_cast<const uint32_t *>(&qs[row * QS + kk * 16 + 8 + col]);
-            qa[kk][3] =
-                *reinterpret_cast<const uint32_t *>(&qs[(row + 8) * QS + kk * 16 + 8 + col]);
-        }
-    }
-
-    float o[NB][4];
-#pragma unroll
-    for (int n = 0; n < NB; ++n)
-        o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+    GroupAttn<T, D> ga;
+    ga.init();
+    ga.load_q(qs, QS, lane);
     bool timed_out = false;
 
     for (int t = 0; t < ntiles; ++t) {
@@ -259,76 +403,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
                 __syncwarp();
             }
-            // S = Q K^T over this warp's 16 rows
-            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            const int mat = lane >> 3;
-            const int krow = 16 * warp + ((mat >> 1) << 3) + (lane & 7);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const int cidx = 2 * kk + (mat & 1);
-                uint32_t r_0, r_1, r_2, r_3;
-                ldsm_x4(kb + (cidx >> 3) * 8192 + kvc::sw128(krow, cidx & 7), r_0, r_1, r_2, r_3);
-                Mma<T>::run(sc[0], qa[kk], r_0, r_1);
-                Mma<T>::run(sc[1], qa[kk], r_2, r_3);
-            }
-            // online softmax (log2 domain); columns >= my_valid are masked
-            float mx_lo = -INFINITY, mx_hi = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int col = 8 * j + 2 * (lane & 3) + (e & 1);
-                    float v = sc[j][e] * a.scale_log2;
-                    v = col < my_valid ? v : -INFINITY;
-                    sc[j][e] = v;
-                    if (e < 2)
-                        mx_lo = fmaxf(mx_lo, v);
-                    else
-                        mx_hi = fmaxf(mx_hi, v);
-                }
-            mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-            mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-            mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-            mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-            const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-            const float al_lo = exp2f(m_lo - mn_lo), al_hi = exp2f(m_hi - mn_hi);
-            m_lo = mn_lo;
-            m_hi = mn_hi;
-            float ps_lo = 0.f, ps_hi = 0.f;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                sc[j][0] = exp2f(sc[j][0] - mn_lo);
-                sc[j][1] = exp2f(sc[j][1] - mn_lo);
-                sc[j][2] = exp2f(sc[j][2] - mn_hi);
-                sc[j][3] = exp2f(sc[j][3] - mn_hi);
-                ps_lo += sc[j][0] + sc[j][1];
-                ps_hi += sc[j][2] + sc[j][3];
-            }
-            l_lo = l_lo * al_lo + ps_lo;
-            l_hi = l_hi * al_hi + ps_hi;
-#pragma unroll
-            for (int n = 0; n < NB; ++n) {
-                o[n][0] *= al_lo;
-                o[n][1] *= al_lo;
-                o[n][2] *= al_hi;
-                o[n][3] *= al_hi;
-            }
-            uint32_t pa[4];
-            pa[0] = Mma<T>::pack(sc[0][0], sc[0][1]);
-            pa[1] = Mma<T>::pack(sc[0][2], sc[0][3]);
-            pa[2] = Mma<T>::pack(sc[1][0], sc[1][1]);
-            pa[3] = Mma<T>::pack(sc[1][2], sc[1][3]);
-            // O += P V over this warp's 16 rows
-            const int vrow = 16 * warp + ((mat & 1) << 3) + (lane & 7);
-#pragma unroll
-            for (int nn = 0; nn < D / 16; ++nn) {
-                const int cidx = 2 * nn + (mat >> 1);
-                uint32_t r_0, r_1, r_2, r_3;
-                ldsm_x4_t(vb + (cidx >> 3) * 8192 + kvc::sw128(vrow, cidx & 7), r_0, r_1, r_2,
-                          r_3);
-                Mma<T>::run(o[2 * nn], pa, r_0, r_1);
-                Mma<T>::run(o[2 * nn + 1], pa, r_2, r_3);
-            }
+            ga.tile(kb, vb, warp, lane, 0, my_valid, a.scale_log2);
         }
         if (my_valid > 0 && my_valid < 16)
             kvc::fence_proxy_async_smem();
@@ -342,51 +417,18 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
             atomicExch(abort_flag, 1);
         }
     }
-    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-
     // ---- merge the four warps' (m, l, o) through shared memory ----
     consumer_sync();  // every warp is done with the stage buffers
     float *cm = reinterpret_cast<float *>(stages);        // [4][16]
     float *cl = cm + kConsumers * 16;                      // [4][16]
     float *co = cl + kConsumers * 16;                      // [4][16][D]
-    {
-        const int row = lane >> 2, col = 2 * (lane & 3);
-        if ((lane & 3) == 0) {
-            cm[warp * 16 + row] = m_lo;
-            cl[warp * 16 + row] = l_lo;
-            cm[warp * 16 + row + 8] = m_hi;
-            cl[warp * 16 + row + 8] = l_hi;
-        }
-#pragma unroll
-        for (int n = 0; n < NB; ++n) {
-            if (row < g) {
-                co[(warp * 16 + row) * D + 8 * n + col] = o[n][0];
-                co[(warp * 16 + row) * D + 8 * n + col + 1] = o[n][1];
-            }
-            if (row + 8 < g) {
-                co[(warp * 16 + row + 8) * D + 8 * n + col] = o[n][2];
-                co[(warp * 16 + row + 8) * D + 8 * n + col + 1] = o[n][3];
-            }
-        }
-    }
+    ga.publish(cm, cl, co, warp, lane, g);
     consumer_sync();
     const int hq0 = kvh * g;
     for (int idx = threadIdx.x; idx < g * D; idx += 128) {
         const int h = idx / D, d = idx % D;
-        float mstar = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumers; ++w)
-            mstar = fmaxf(mstar, cm[w * 16 + h]);
-        float lsum = 0.f, osum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumers; ++w) {
-            const float f = exp2f(cm[w * 16 + h] - mstar);
-            lsum += cl[w * 16 + h] * f;
-            osum += co[(w * 16 + h) * D + d] * f;
-        }
+        float mstar, lsum, osum;
+        merge4(cm, cl, co, D, h, d, mstar, lsum, osum);
         const int64_t qrow = (int64_t)b * a.q_heads + hq0 + h;
         if (nsplit == 1) {
             static_cast<T *>(a.out)[qrow * D + d] = kvc::Elem<T>::from_f32(osum / lsum);
@@ -434,6 +476,205 @@ decode_combine_kernel(const DecodeArgs a, int D)
         for (int j = 0; j < nsplit; ++j)
             acc += a.ws_o[(p0 + j) * D + d] * wsh[j];
         static_cast<T *>(a.out)[qrow * D + d] = kvc::Elem<T>::from_f32(acc / lsum);
+    }
+}
+
+
+// --------------------------------------------------------------------------
+// Fused one-token step on a windowed cache: lengths, compaction, RoPE append
+// and GQA attention in one launch ("GQA support sliding_window_cache",
+// "Design": Lp = min(P, C), E = max(0, Lp + 1 - C), rows [E, Lp) move to
+// [0, Lp - E) and the new row goes to Lp - E).  One CTA owns one (batch row,
+// kv head) slice and keeps the whole new window in shared memory: cp.async
+// brings every old row in at once (from cache row r + E) while the threads
+// rotate the query and the new row, then the window is written back one row
+// lower when a row was evicted (all reads have completed, so the in-place
+// move needs no scratch) and attended over from shared memory.  The slice is
+// read once instead of twice (shift, then attention), in one launch.
+// --------------------------------------------------------------------------
+struct WindowStepArgs {
+    void *out;
+    const void *q;
+    void *k_cache, *v_cache;
+    const void *new_k, *new_v;
+    const int32_t *seqlens_k;
+    kvc_lengths len;  // all NULL: not written
+    int q_heads, kv_heads, group;
+    int64_t capacity;
+    int window;
+    float scale_log2;
+    const float *cos_t, *sin_t;
+    int64_t rope_max_pos;
+    int32_t *status;
+};
+
+// largest capacity whose whole window (K and V) the fused step keeps in
+// shared memory
+__host__ __device__ constexpr int64_t window_step_max_capacity(int D) { return 32768 / D; }
+
+template <typename T, int D>
+__global__ void __launch_bounds__(128, 4)
+window_step_kernel(const WindowStepArgs a)
+{
+    constexpr int KT_BYTES = kTile * D * 2;  // one 64-row K (or V) tile
+    constexpr int QS = D + 8;
+    constexpr int CPR = D / 8;               // 16-byte chunks per row
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int64_t C = a.capacity;
+    const int ntile_max = (int)((C + kTile - 1) / kTile);
+    uint8_t *tiles = smem;  // tile t: K at t * 2 * KT_BYTES, V after it
+    T *qs = reinterpret_cast<T *>(smem + (size_t)ntile_max * 2 * KT_BYTES);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x / a.kv_heads, kvh = blockIdx.x % a.kv_heads;
+    const int64_t T_ = (int64_t)a.seqlens_k[b] + 1;
+    const bool write_len = kvh == 0 && threadIdx.x == 0 && a.len.cache_total != nullptr;
+    if (T_ < 1 || T_ > (int64_t)INT32_MAX) {
+        if (write_len) {
+            a.len.past_abs[b] = a.len.total_abs[b] = a.len.cache_past[b] = a.len.cache_total[b] =
+                a.len.evict[b] = -1;
+        }
+        if (kvh == 0 && threadIdx.x == 0)
+            kvc::raise_status(a.status, KVC_DEV_SEQLEN_RANGE);
+        return;
+    }
+    const int P = (int)(T_ - 1);
+    const int Lp = (int)(P < C ? P : C);
+    const int E = (int)(Lp + 1 - C > 0 ? Lp + 1 - C : 0);
+    const int L = Lp - E + 1;
+    if (write_len) {
+        a.len.past_abs[b] = P;
+        a.len.total_abs[b] = (int32_t)T_;
+        a.len.cache_past[b] = Lp;
+        a.len.cache_total[b] = L;
+        a.len.evict[b] = E;
+    }
+    if (a.cos_t && T_ > a.rope_max_pos) {
+        if (kvh == 0 && threadIdx.x == 0)
+            kvc::raise_status(a.status, KVC_DEV_ROPE_RANGE);
+        return;
+    }
+    const int g = a.group;
+    const int vis0 = (a.window > 0 && L > a.window) ? L - a.window : 0;
+    const int64_t slice = (int64_t)b * a.kv_heads + kvh;
+    T *kc = static_cast<T *>(a.k_cache) + slice * C * D;
+    T *vc = static_cast<T *>(a.v_cache) + slice * C * D;
+    const int ntiles = (L + kTile - 1) / kTile;
+
+    // 1. every window row except the new one, straight from cache row r + E
+    //    into the swizzled tiles; the rows after the window's end are zeroed
+    const int nchunks = ntiles * kTile * CPR;
+    for (int idx = threadIdx.x; idx < 2 * nchunks; idx += 128) {
+        const bool is_v = idx >= nchunks;
+        const int w = is_v ? idx - nchunks : idx;
+        const int r = w / CPR, c = w % CPR;  // window row, 16-byte chunk
+        uint8_t *dst = tiles + (size_t)(r / kTile) * 2 * KT_BYTES + (is_v ? KT_BYTES : 0) +
+                       (c >> 3) * 8192 + kvc::sw128(r % kTile, c & 7);
+        if (r < L - 1) {
+            const T *src = (is_v ? vc : kc) + (int64_t)(r + E) * D + c * 8;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(kvc::smem_u32(dst)),
+                         "l"(src)
+                         : "memory");
+        } else if (r >= L) {
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+        }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+
+    // 2. meanwhile: the group's query rows rotated at T - 1, and the new row
+    //    (K rotated at P = T - 1, V as given) placed at window row L - 1
+    {
+        const T *qg = static_cast<const T *>(a.q) + ((int64_t)b * a.q_heads + kvh * g) * D;
+        const T *nk = static_cast<const T *>(a.new_k) + slice * D;
+        const T *nv = static_cast<const T *>(a.new_v) + slice * D;
+        const float *cs = a.cos_t ? a.cos_t + (int64_t)P * (D / 2) : nullptr;
+        const float *sn = a.cos_t ? a.sin_t + (int64_t)P * (D / 2) : nullptr;
+        const int rl = L - 1;
+        uint8_t *ktl = tiles + (size_t)(rl / kTile) * 2 * KT_BYTES;
+        for (int idx = threadIdx.x; idx < 18 * (D / 2); idx += 128) {
+            const int h = idx / (D / 2), i = idx % (D / 2);
+            if (h < 16) {
+                float lo = 0.f, hi = 0.f;
+                if (h < g) {
+                    lo = kvc::Elem<T>::to_f32(qg[h * D + i]);
+                    hi = kvc::Elem<T>::to_f32(qg[h * D + i + D / 2]);
+                    if (cs)
+                        kvc::rope_pair(lo, hi, cs[i], sn[i]);
+                }
+                qs[h * QS + i] = kvc::Elem<T>::from_f32(lo);
+                qs[h * QS + i + D / 2] = kvc::Elem<T>::from_f32(hi);
+            } else {
+                // h == 16: K pair (i, i + D/2); h == 17: the same V elements
+                const bool is_v = h == 17;
+                T lo_t, hi_t;
+                if (!is_v) {
+                    float lo = kvc::Elem<T>::to_f32(nk[i]), hi = kvc::Elem<T>::to_f32(nk[i + D / 2]);
+                    if (cs)
+                        kvc::rope_pair(lo, hi, cs[i], sn[i]);
+                    lo_t = kvc::Elem<T>::from_f32(lo);
+                    hi_t = kvc::Elem<T>::from_f32(hi);
+                } else {
+                    lo_t = nv[i];
+                    hi_t = nv[i + D / 2];
+                }
+                uint8_t *tb = ktl + (is_v ? KT_BYTES : 0);
+                const int c_lo = i / 8, c_hi = (i + D / 2) / 8;
+                *reinterpret_cast<T *>(tb + (c_lo >> 3) * 8192 + kvc::sw128(rl % kTile, c_lo & 7) +
+                                       (i % 8) * 2) = lo_t;
+                *reinterpret_cast<T *>(tb + (c_hi >> 3) * 8192 + kvc::sw128(rl % kTile, c_hi & 7) +
+                                       ((i + D / 2) % 8) * 2) = hi_t;
+            }
+        }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+
+    // 3. write the window back: every row one lower when a row was evicted,
+    //    otherwise only the new row (at Lp).  All reads of the old rows are
+    //    complete, so the in-place move needs no scratch.
+    {
+        const int r_first = E > 0 ? 0 : L - 1;
+        const int n = (L - r_first) * CPR;
+        for (int idx = threadIdx.x; idx < 2 * n; idx += 128) {
+            const bool is_v = idx >= n;
+            const int w = is_v ? idx - n : idx;
+            const int r = r_first + w / CPR, c = w % CPR;
+            const uint8_t *src = tiles + (size_t)(r / kTile) * 2 * KT_BYTES + (is_v ? KT_BYTES : 0) +
+                                 (c >> 3) * 8192 + kvc::sw128(r % kTile, c & 7);
+            *reinterpret_cast<uint4 *>((is_v ? vc : kc) + (int64_t)r * D + c * 8) =
+                *reinterpret_cast<const uint4 *>(src);
+        }
+    }
+
+    // 4. attention over the window held in shared memory
+    GroupAttn<T, D> ga;
+    ga.init();
+    ga.load_q(qs, QS, lane);
+    for (int t = 0; t < ntiles; ++t) {
+        const int t0 = t * kTile;
+        const int lo = min(16, max(0, vis0 - t0 - 16 * warp));
+        const int hi = min(16, max(0, L - t0 - 16 * warp));
+        const uint32_t kb = kvc::smem_u32(tiles + (size_t)t * 2 * KT_BYTES);
+        if (hi > lo)
+            ga.tile(kb, kb + KT_BYTES, warp, lane, lo, hi, a.scale_log2);
+    }
+    __syncthreads();
+
+    // 5. merge the four warps and write the group's output rows
+    float *cm = reinterpret_cast<float *>(smem);
+    float *cl = cm + kConsumers * 16;
+    float *co = cl + kConsumers * 16;
+    ga.publish(cm, cl, co, warp, lane, g);
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < g * D; idx += 128) {
+        const int h = idx / D, d = idx % D;
+        float mstar, lsum, osum;
+        merge4(cm, cl, co, D, h, d, mstar, lsum, osum);
+        const int64_t qrow = (int64_t)b * a.q_heads + kvh * g + h;
+        static_cast<T *>(a.out)[qrow * D + d] = kvc::Elem<T>::from_f32(osum / lsum);
     }
 }
 
@@ -693,6 +934,94 @@ KVC_API kvc_status kvc_gqa_decode(void *out, const void *q, const void *k_cache,
     return dispatch_decode16<__half>(head_dim, out, q, k_cache, v_cache, len, batch, q_heads,
                                      kv_heads, capacity, local_window_size, scale, rope_cos,
                                      rope_sin, rope_max_pos, workspace, dev_status, stream);
+}
+
+namespace {
+
+template <typename T, int D>
+kvc_status launch_window_step(const WindowStepArgs &a, int batch, cudaStream_t stream)
+{
+    const int64_t ntile_max = (a.capacity + kTile - 1) / kTile;
+    size_t smem = 1024 + (size_t)ntile_max * 2 * kTile * D * 2 + 16 * (D + 8) * 2;
+    const size_t merge = 1024 + kConsumers * 16 * (2 + D) * sizeof(float);
+    smem = smem > merge ? smem : merge;
+    auto kern = window_step_kernel<T, D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return KVC_ERR_CUDA;
+    kern<<<(unsigned)(batch * a.kv_heads), 128, smem, stream>>>(a);
+    return kvc_host::launch_status();
+}
+
+} // namespace
+
+KVC_API kvc_status kvc_window_decode_step(void *out, const void *q, void *k_cache, void *v_cache,
+                                          const void *new_k, const void *new_v,
+                                          const int32_t *seqlens_k, kvc_lengths len, int batch,
+                                          int q_heads, int kv_heads, int64_t capacity,
+                                          int head_dim, int dtype, int local_window_size,
+                                          float scale, const float *rope_cos,
+                                          const float *rope_sin, int64_t rope_max_pos,
+                                          int32_t *dev_status, void *stream)
+{
+    if (kvc_host::elem_bytes_of(dtype) == 0)
+        return KVC_ERR_DTYPE;
+    if (batch < 0 || q_heads < 1 || kv_heads < 1 || q_heads % kv_heads != 0)
+        return KVC_ERR_SHAPE;
+    if (capacity < 1 || capacity > (int64_t)INT32_MAX)
+        return KVC_ERR_CAPACITY;
+    if (local_window_size <= 0 || local_window_size > capacity)
+        return KVC_ERR_WINDOW;
+    if ((rope_cos == nullptr) != (rope_sin == nullptr))
+        return KVC_ERR_NULL;
+    if (rope_cos && rope_max_pos < 1)
+        return KVC_ERR_SHAPE;
+    const int g = q_heads / kv_heads;
+    if (dtype == KVC_F32 || (head_dim != 64 && head_dim != 128) || g > 16 ||
+        capacity > window_step_max_capacity(head_dim))
+        return KVC_ERR_UNSUPPORTED;
+    const bool some_len = len.past_abs || len.total_abs || len.cache_past || len.cache_total ||
+                          len.evict;
+    if (some_len && !kvc_host::lengths_ok(len))
+        return KVC_ERR_NULL;
+    if (batch == 0)
+        return KVC_OK;
+    if (!out || !q || !k_cache || !v_cache || !new_k || !new_v || !seqlens_k)
+        return KVC_ERR_NULL;
+    for (const void *p : {(const void *)out, q, (const void *)k_cache, (const void *)v_cache, new_k,
+                          new_v})
+        if (!kvc_host::aligned16(p))
+            return KVC_ERR_ALIGN;
+    const size_t cache_bytes = (size_t)batch * kv_heads * capacity * head_dim * 2;
+    if (kvc_host::overlaps(k_cache, cache_bytes, v_cache, cache_bytes))
+        return KVC_ERR_SHAPE;
+    if (scale == 0.f)
+        scale = 1.0f / sqrtf((float)head_dim);
+    WindowStepArgs a;
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.new_k = new_k;
+    a.new_v = new_v;
+    a.seqlens_k = seqlens_k;
+    a.len = some_len ? len : kvc_lengths{nullptr, nullptr, nullptr, nullptr, nullptr};
+    a.q_heads = q_heads;
+    a.kv_heads = kv_heads;
+    a.group = g;
+    a.capacity = capacity;
+    a.window = local_window_size;
+    a.scale_log2 = scale * kLog2e;
+    a.cos_t = rope_cos;
+    a.sin_t = rope_sin;
+    a.rope_max_pos = rope_max_pos;
+    a.status = dev_status;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == KVC_BF16)
+        return head_dim == 64 ? launch_window_step<__nv_bfloat16, 64>(a, batch, st)
+                              : launch_window_step<__nv_bfloat16, 128>(a, batch, st);
+    return head_dim == 64 ? launch_window_step<__half, 64>(a, batch, st)
+                          : launch_window_step<__half, 128>(a, batch, st);
 }
 
 // --------------------------------------------------------------------------

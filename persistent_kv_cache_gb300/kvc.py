@@ -31,8 +31,8 @@ KVC_DEV_ROPE_RANGE = 8
 KVC_DEV_TIMEOUT = 16
 
 EXPORTS = ("kvc_tensor_scatter", "kvc_seq_lengths", "kvc_window_append", "kvc_gqa_decode",
-           "kvc_gqa_decode_workspace_size", "kvc_gqa_decode_noalloc", "kvc_gqa_prefill_chunk",
-           "kvc_status_string", "kvc_abi_version")
+           "kvc_gqa_decode_workspace_size", "kvc_gqa_decode_noalloc", "kvc_window_decode_step",
+           "kvc_gqa_prefill_chunk", "kvc_status_string", "kvc_abi_version")
 KVC_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -91,6 +91,8 @@ def library() -> ctypes.CDLL:
             "kvc_gqa_decode": [P, P, P, P, L, I, I, I, I64, I, I, I, F, P, P, I64, P, SZ, P, P],
             "kvc_gqa_decode_workspace_size": [I, I, I, I64, I, I],
             "kvc_gqa_decode_noalloc": [P, P, P, P, L, I, I, I, I64, I, I, I, F, P, P, I64, P, P],
+            "kvc_window_decode_step": [P, P, P, P, P, P, P, L, I, I, I, I64, I, I, I, F, P, P, I64,
+                                       P, P],
             "kvc_gqa_prefill_chunk": [P, P, P, P, I64, L, I, I, I, I, I, I, I, F, P, P, I64, P, P],
             "kvc_status_string": [I],
             "kvc_abi_version": [],
@@ -195,6 +197,20 @@ def kvc_gqa_decode_noalloc(out, q, k_cache, v_cache, lengths, local_window_size=
     _check("kvc_gqa_decode_noalloc", library().kvc_gqa_decode_noalloc(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), lengths.c(), B, Hq, Hkv, C, D,
         _dtype_code(q), local_window_size, scale, cs, sn, rmax, _ptr(status), _stream(stream)))
+    return out
+
+
+def kvc_window_decode_step(out, q, k_cache, v_cache, new_k, new_v, seqlens_k, local_window_size,
+                           lengths=None, scale=0.0, rope=None, status=None, stream=None):
+    """Fused lengths + windowed one-token append + GQA decode (include/kvc.h)."""
+    B, Hq, _, D = q.shape
+    _, Hkv, C, _ = k_cache.shape
+    cs, sn, rmax = _rope(rope)
+    lc = lengths.c() if lengths is not None else KvcLengths(None, None, None, None, None)
+    _check("kvc_window_decode_step", library().kvc_window_decode_step(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(new_k), _ptr(new_v),
+        _ptr(seqlens_k), lc, B, Hq, Hkv, C, D, _dtype_code(q), local_window_size, scale, cs, sn,
+        rmax, _ptr(status), _stream(stream)))
     return out
 
 

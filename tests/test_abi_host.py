@@ -123,3 +123,17 @@ def test_binding_requires_library(monkeypatch, kvc):
     monkeypatch.setattr(kvc, "_lib", None)
     with pytest.raises(kvc.KvcLibraryMissing):
         kvc.library()
+
+
+def test_window_step_host_checks(kvc):
+    lib = kvc.library()
+    f = lib.kvc_window_decode_step
+    none = kvc.KvcLengths(None, None, None, None, None)
+    base = [FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, FAKE * 7]
+    assert f(*base, none, 2, 8, 2, 128, 64, 1, 129, 0.0, None, None, 0, None, None) == 7  # W > C
+    assert f(*base, none, 2, 8, 2, 128, 64, 1, 0, 0.0, None, None, 0, None, None) == 7    # W = 0
+    assert f(*base, none, 2, 8, 2, 128, 64, 0, 128, 0.0, None, None, 0, None, None) == 5  # fp32
+    assert f(*base, none, 2, 8, 2, 128, 96, 1, 128, 0.0, None, None, 0, None, None) == 5  # D
+    half = kvc.KvcLengths(FAKE, None, None, None, None)
+    assert f(*base, half, 2, 8, 2, 128, 64, 1, 128, 0.0, None, None, 0, None, None) == 1
+    assert f(*base, none, 0, 8, 2, 128, 64, 1, 128, 0.0, None, None, 0, None, None) == 0

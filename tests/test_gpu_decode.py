@@ -218,3 +218,111 @@ def test_graph_captured_step(K, orc):
                                 cos_cache=cos.numpy(), sin_cache=sin.numpy())
     assert_bytes_equal(gk, wk, "k")
     assert_close(out, want, 2e-2, "graph decode")
+
+
+# --------------------------------------------------------------------------
+# fused one-token step on a windowed cache (kvc_window_decode_step)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("D,g", [(64, 8), (128, 4), (128, 16)])
+def test_window_step_fused_consecutive(K, orc, D, g):
+    """Consecutive fused steps on a C = W cache: every cache byte and the
+    written lengths match the oracle after each step, the attention every
+    third step (window rows 1, 127, 128, 129 and long totals included)."""
+    B, Hkv, C = 6, 2, 128
+    W = C
+    Hq = Hkv * g
+    T0 = np.array([1, 127, 128, 129, 700, 30000])
+    steps = 9
+    cos, sin = synth.rope_cache(int(T0.max()) + steps + 1, D)
+    rope_d = (cos.to(dev()), sin.to(dev()))
+    kc = synth.normal((B, Hkv, C, D), 50 + D, 1)
+    vc = synth.normal((B, Hkv, C, D), 50 + D, 2)
+    wk, wv = synth.bits(kc).copy(), synth.bits(vc).copy()
+    gk, gv = kc.to(dev()), vc.to(dev())
+    st = status()
+    out = torch.empty(B, Hq, 1, D, dtype=torch.bfloat16, device=dev())
+    Lg = K.Lengths(B, dev())
+    for s in range(steps):
+        T = T0 + s
+        sk = (T - 1).astype(np.int32)
+        nk = synth.normal((B, Hkv, 1, D), 51, s)
+        nv = synth.normal((B, Hkv, 1, D), 52, s)
+        q = synth.normal((B, Hq, 1, D), 53, s)
+        K.kvc_window_decode_step(out, q.to(dev()), gk, gv, nk.to(dev()), nv.to(dev()),
+                                 torch.from_numpy(sk).to(dev()), W, lengths=Lg, rope=rope_d,
+                                 status=st)
+        lens = orc.seq_lengths(sk, 1, C, 1)
+        orc.window_append(wk, wv, synth.bits(nk), synth.bits(nv), lens, 1, cos.numpy(),
+                          sin.numpy())
+        torch.cuda.synchronize()
+        assert_bytes_equal(gk, wk, f"k step {s}")
+        assert_bytes_equal(gv, wv, f"v step {s}")
+        got_len = lengths_np(Lg)
+        for f in Lg.FIELDS:
+            np.testing.assert_array_equal(got_len[f], lens[f], err_msg=f)
+        if s % 3 == 2:
+            want, _ = orc.gqa_attention(synth.bits(q), wk, wv, lens["cache_total"],
+                                        lens["total_abs"], window=W, cos_cache=cos.numpy(),
+                                        sin_cache=sin.numpy())
+            assert_close(out, want, 2e-2, f"fused step {s}")
+    assert st.item() == 0
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_window_step_fused_matches_unfused(K, orc, dtype):
+    """Window narrower than the capacity (W = 90 < C = 200): the fused step
+    and lengths + append + decode produce the same cache bytes and outputs
+    within the attention tolerance."""
+    B, Hq, Hkv, D, C, W = 5, 16, 4, 128, 200, 90
+    T = np.array([1, 90, 150, 200, 5000])
+    sk = torch.from_numpy((T - 1).astype(np.int32)).to(dev())
+    cos, sin = synth.rope_cache(int(T.max()) + 1, D)
+    rope_d = (cos.to(dev()), sin.to(dev()))
+    kc = synth.normal((B, Hkv, C, D), 60, 1, dtype).to(dev())
+    vc = synth.normal((B, Hkv, C, D), 60, 2, dtype).to(dev())
+    nk = synth.normal((B, Hkv, 1, D), 60, 3, dtype).to(dev())
+    nv = synth.normal((B, Hkv, 1, D), 60, 4, dtype).to(dev())
+    q = synth.normal((B, Hq, 1, D), 60, 5, dtype).to(dev())
+    st = status()
+    k1, v1 = kc.clone(), vc.clone()
+    o1 = torch.empty(B, Hq, 1, D, dtype=dtype, device=dev())
+    K.kvc_window_decode_step(o1, q, k1, v1, nk, nv, sk, W, rope=rope_d, status=st)
+    k2, v2 = kc.clone(), vc.clone()
+    o2 = torch.empty_like(o1)
+    L = K.kvc_seq_lengths(sk, 1, C, 1, local_window_size=W, status=st)
+    K.kvc_window_append(k2, v2, nk, nv, L, 1, rope=rope_d, status=st)
+    K.kvc_gqa_decode(o2, q, k2, v2, L, local_window_size=W, rope=rope_d, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(k1, k2) and torch.equal(v1, v2)
+    assert (o1.float() - o2.float()).abs().max().item() <= 2e-2
+    lens = orc.seq_lengths((T - 1).astype(np.int32), 1, C, 1)
+    wk, wv = synth.bits(kc.cpu()).copy(), synth.bits(vc.cpu()).copy()
+    orc.window_append(wk, wv, synth.bits(nk.cpu()), synth.bits(nv.cpu()), lens, 1, cos.numpy(),
+                      sin.numpy())
+    want, _ = orc.gqa_attention(synth.bits(q.cpu()), wk, wv, lens["cache_total"],
+                                lens["total_abs"], window=W, cos_cache=cos.numpy(),
+                                sin_cache=sin.numpy())
+    assert_close(o1, want, 2e-2, "fused vs oracle")
+
+
+def test_window_step_fused_rejects_bad_rows(K, orc):
+    B, Hq, Hkv, D, C = 3, 8, 2, 64, 64
+    sk = torch.tensor([-1, 10, 2**31 - 1], dtype=torch.int32, device=dev())
+    kc = synth.normal((B, Hkv, C, D), 61, 1).to(dev())
+    vc = synth.normal((B, Hkv, C, D), 61, 2).to(dev())
+    before_k, before_v = kc.clone(), vc.clone()
+    nk = synth.normal((B, Hkv, 1, D), 61, 3).to(dev())
+    nv = synth.normal((B, Hkv, 1, D), 61, 4).to(dev())
+    q = synth.normal((B, Hq, 1, D), 61, 5).to(dev())
+    out = torch.zeros(B, Hq, 1, D, dtype=torch.bfloat16, device=dev())
+    Lg = K.Lengths(B, dev())
+    st = status()
+    K.kvc_window_decode_step(out, q, kc, vc, nk, nv, sk, C, lengths=Lg, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == K.KVC_DEV_SEQLEN_RANGE
+    for b in (0, 2):
+        assert torch.equal(kc[b], before_k[b]) and torch.equal(vc[b], before_v[b])
+        assert (Lg.buf[:, b] == -1).all()
+    assert not torch.equal(kc[1], before_k[1])
