@@ -65,7 +65,7 @@ def _load():
         I32, I64, DBL = ctypes.c_int, ctypes.c_int64, ctypes.c_double
         lib.orc_tensor_scatter.argtypes = [P, P, P, P, I32, P, I64, I32, I32, I32, P]
         lib.orc_tensor_scatter.restype = I32
-        lib.orc_seq_lengths.argtypes = [P, I32, I32, I64, I32, P, P, P, P, P, P]
+        lib.orc_seq_lengths.argtypes = [P, I32, I32, I64, I32, I32, P, P, P, P, P, P]
         lib.orc_seq_lengths.restype = None
         lib.orc_rope_rows.argtypes = [P, P, P, I64, I32, I32, P, P, I64]
         lib.orc_rope_rows.restype = I32
@@ -114,13 +114,18 @@ def tensor_scatter(past, update, write_indices, axis=-2, mode=LINEAR, out=None):
     return present, flags
 
 
-def seq_lengths(seqlens_k, new_tokens, capacity, windowed):
-    """Returns dict(past_abs, total_abs, cache_past, cache_total, evict, flags)."""
+CONTIGUOUS, WINDOWED, DRIFTING = 0, 1, 2
+
+
+def seq_lengths(seqlens_k, new_tokens, capacity, windowed, window=0):
+    """Returns dict(past_abs, total_abs, cache_past, cache_total, evict, flags).
+    windowed: 0 contiguous, 1 windowed (compact every step), 2 drifting
+    (needs the window)."""
     sk = np.ascontiguousarray(seqlens_k, dtype=np.int32)
     B = sk.shape[0]
     outs = {k: np.zeros(B, dtype=np.int32) for k in
             ("past_abs", "total_abs", "cache_past", "cache_total", "evict", "flags")}
-    _load().orc_seq_lengths(_ptr(sk), B, new_tokens, capacity, int(windowed),
+    _load().orc_seq_lengths(_ptr(sk), B, new_tokens, capacity, int(windowed), int(window),
                             _ptr(outs["past_abs"]), _ptr(outs["total_abs"]),
                             _ptr(outs["cache_past"]), _ptr(outs["cache_total"]),
                             _ptr(outs["evict"]), _ptr(outs["flags"]))

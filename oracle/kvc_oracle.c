@@ -198,18 +198,38 @@ int orc_tensor_scatter(void *present, const void *past, const void *update,
 /* ------------------------------------------------------------------ */
 
 /*
+ * [GQA] CPU commit "drifting layout": with gap = C - W + 1 the resident rows
+ * of a windowed cache are [0, end(T)) where
+ *     end(T) = T                              while T <= C
+ *            = T - gap * ceil((T - C) / gap)  afterwards  (so W <= end <= C)
+ * a pure function of the absolute length, so compaction happens once every
+ * gap steps instead of every step.
+ */
+static int64_t drift_end(int64_t T, int64_t C, int64_t W)
+{
+    if (T <= C)
+        return T;
+    int64_t gap = C - W + 1;
+    int64_t k = (T - C + gap - 1) / gap;
+    return T - gap * k;
+}
+
+/*
  * seqlens_k[b] holds the running total after this step minus one, so the
  * absolute total is T = seqlens_k[b] + 1 (computed in 64-bit) and the absolute
- * past length is P = T - S.  Windowed cache of capacity C:
+ * past length is P = T - S.  Windowed cache of capacity C (policy 1):
  *     Lp = min(P, C)          resident tokens before the step
  *     E  = max(0, Lp + S - C) tokens evicted by the step
  *     L  = Lp - E + S         resident tokens after the step
- * Contiguous cache: Lp = P, E = 0, L = T, and T must not exceed C.
+ * Drifting windowed cache (policy 2, window W): Lp = end(P), L = end(T),
+ * E = Lp + S - L.
+ * Contiguous cache (policy 0): Lp = P, E = 0, L = T, and T must not exceed C.
  * A row is rejected (all five outputs -1, flag set) when T < S, when T does
- * not fit in int32, or (contiguous) when T > C.
+ * not fit in int32, (contiguous) when T > C, or (drifting) when W is outside
+ * [1, C].
  */
 void orc_seq_lengths(const int32_t *seqlens_k, int batch, int new_tokens,
-                     int64_t capacity, int windowed, int32_t *past_abs,
+                     int64_t capacity, int windowed, int window, int32_t *past_abs,
                      int32_t *total_abs, int32_t *cache_past, int32_t *cache_total,
                      int32_t *evict, int32_t *batch_flags)
 {
@@ -221,6 +241,8 @@ void orc_seq_lengths(const int32_t *seqlens_k, int batch, int new_tokens,
             flag |= ORC_BAD_SEQLEN;
         else if (!windowed && T > capacity)
             flag |= ORC_BAD_CAPACITY;
+        else if (windowed == 2 && (window < 1 || window > capacity))
+            flag |= ORC_BAD_CAPACITY;   /* the layout needs W <= C */
         batch_flags[b] = flag;
         if (flag) {
             past_abs[b] = total_abs[b] = cache_past[b] = cache_total[b] = evict[b] = -1;
@@ -228,7 +250,11 @@ void orc_seq_lengths(const int32_t *seqlens_k, int batch, int new_tokens,
         }
         int64_t P = T - S;
         int64_t Lp, E, L;
-        if (windowed) {
+        if (windowed == 2) {
+            Lp = drift_end(P, capacity, window);
+            L = drift_end(T, capacity, window);
+            E = Lp + S - L;
+        } else if (windowed) {
             Lp = P < capacity ? P : capacity;
             E = Lp + S - capacity;
             if (E < 0)

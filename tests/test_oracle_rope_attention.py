@@ -170,10 +170,11 @@ def _full_history_attention(orc, q, hist_k, hist_v, T, window, cos, sin):
                              sin_cache=sin)[0]
 
 
-@pytest.mark.parametrize("seed", range(4))
-def test_compacted_window_equals_full_history(orc, seed):
+@pytest.mark.parametrize("seed,policy", [(s, p) for s in range(4) for p in (1, 2)])
+def test_compacted_window_equals_full_history(orc, seed, policy):
     """Exactness: any S schedule on a windowed cache with C >= W gives exactly
-    the full-history result under the window mask (decode and chunk queries)."""
+    the full-history result under the window mask (decode and chunk queries),
+    for the compact-every-step layout and for the drifting one."""
     rng = np.random.default_rng(30 + seed)
     B, Hkv, g, D = 2, 2, 2, 8
     W = int(rng.integers(2, 7))
@@ -191,7 +192,7 @@ def test_compacted_window_equals_full_history(orc, seed):
         nk = synth.bits(synth.normal((B, Hkv, S, D), seed, 100 + T))
         nv = synth.bits(synth.normal((B, Hkv, S, D), seed, 200 + T))
         q = synth.bits(synth.normal((B, Hkv * g, S, D), seed, 300 + T))
-        lens = orc.seq_lengths(np.full(B, T + S - 1, np.int32), S, C, True)
+        lens = orc.seq_lengths(np.full(B, T + S - 1, np.int32), S, C, policy, W)
         ks = vs = None
         if S > 1:
             ks = np.zeros((B, Hkv, C + S, D), np.uint16)

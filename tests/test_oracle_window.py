@@ -10,6 +10,12 @@
   the last L tokens of a plain history list byte for byte, rows [L, C) keep
   their previous bytes, and the staging buffer holds the old resident rows
   followed by the new ones.
+* Drifting layout (the PR's CPU commit, gap = C - W + 1): a brute-force
+  simulation that drops a whole gap-sized block when the list would overflow
+  gives L and E for every C in [1, 11], W in [1, C] over 6C + 5 decode steps;
+  the page's small-slack case (C = W + 8, 400 decode steps) compacts about 44
+  times; gap 1 reduces to the compact-every-step layout; random S schedules
+  keep the history invariant with W <= L <= C.
 """
 import numpy as np
 import pytest
@@ -69,7 +75,7 @@ def test_lengths_int32_edges(orc):
     assert all(out[k][3] == -1 for k in ("past_abs", "cache_total", "evict"))
 
 
-def _run_schedule(orc, C, schedule, windowed, seed, Hkv=2, D=4, B=3):
+def _run_schedule(orc, C, schedule, windowed, seed, Hkv=2, D=4, B=3, window=0):
     rng = np.random.default_rng(seed)
     k_cache = rng.integers(0, 2**16, size=(B, Hkv, C, D), dtype=np.uint16)
     v_cache = rng.integers(0, 2**16, size=(B, Hkv, C, D), dtype=np.uint16)
@@ -83,7 +89,7 @@ def _run_schedule(orc, C, schedule, windowed, seed, Hkv=2, D=4, B=3):
         new_k = (rng.integers(0, 2**14, size=(B, Hkv, S, D))).astype(np.uint16)
         new_v = (rng.integers(0, 2**14, size=(B, Hkv, S, D))).astype(np.uint16)
         T_new = T + S
-        lens = orc.seq_lengths((T_new - 1).astype(np.int32), S, C, windowed)
+        lens = orc.seq_lengths((T_new - 1).astype(np.int32), S, C, windowed, window)
         assert not lens["flags"].any()
         before_k = k_cache.copy()
         before_v = v_cache.copy()
@@ -97,7 +103,10 @@ def _run_schedule(orc, C, schedule, windowed, seed, Hkv=2, D=4, B=3):
         for b in range(B):
             L = int(lens["cache_total"][b])
             Lp = int(lens["cache_past"][b])
-            assert L == (min(T_new[b], C) if windowed else T_new[b])
+            if windowed == 2:
+                assert min(T_new[b], window) <= L <= C   # the window stays resident
+            else:
+                assert L == (min(T_new[b], C) if windowed else T_new[b])
             for h in range(Hkv):
                 if k_st is not None:
                     np.testing.assert_array_equal(k_st[b, h, :Lp], before_k[b, h, :Lp])
@@ -109,8 +118,8 @@ def _run_schedule(orc, C, schedule, windowed, seed, Hkv=2, D=4, B=3):
                 want_v = np.array(hist_v[b][h][len(hist_v[b][h]) - L:])
                 np.testing.assert_array_equal(k_cache[b, h, :L], want_k)
                 np.testing.assert_array_equal(v_cache[b, h, :L], want_v)
-                if windowed and S == 1 and int(lens["evict"][b]) == 1:
-                    pass  # every row of [0, L) was checked above, L == C
+                if windowed and S == 1 and int(lens["evict"][b]) >= 1:
+                    pass  # a shift rewrote [0, L); rows past L keep stale bytes
                 else:
                     # rows beyond the resident window are never written
                     np.testing.assert_array_equal(k_cache[b, h, L:], before_k[b, h, L:])
@@ -164,3 +173,80 @@ def test_rope_applied_to_k_only_at_absolute_positions(orc):
     assert flags[0] == orc.BAD_ROPE and flags[1] == 0
     np.testing.assert_array_equal(k2[0], k[0])
     np.testing.assert_array_equal(v2[0], v[0])
+
+
+# --------------------------------------------------------------------------
+# drifting layout ("GQA support sliding_window_cache", CPU commit: resident
+# rows [0, end(T)) with gap = C - W + 1, compaction once every gap steps)
+# --------------------------------------------------------------------------
+
+def _drift_simulation(C, W, n_steps):
+    """One-token steps on a list of resident positions: append the token;
+    when the list would exceed C, drop the oldest gap = C - W + 1 entries
+    first (a whole gap-sized block is reclaimed at once)."""
+    gap = C - W + 1
+    resident, out = [], []
+    for T in range(1, n_steps + 1):
+        evicted = 0
+        if len(resident) + 1 > C:
+            resident = resident[gap:]
+            evicted = gap
+        resident.append(T - 1)
+        out.append((len(resident), evicted, list(resident)))
+    return out
+
+
+def test_drift_lengths_against_simulation(orc):
+    for C in range(1, 12):
+        for W in range(1, C + 1):
+            sim = _drift_simulation(C, W, 6 * C + 5)
+            sk = np.arange(0, len(sim), dtype=np.int32)
+            out = orc.seq_lengths(sk, 1, C, orc.DRIFTING, W)
+            for j, (L, E, resident) in enumerate(sim):
+                T = j + 1
+                assert (out["cache_total"][j], out["evict"][j]) == (L, E), (C, W, T)
+                assert out["cache_past"][j] == L - 1 + E
+                assert resident == list(range(T - L, T))
+                assert L >= min(T, W) and L <= C
+
+
+def test_drift_page_compaction_count(orc):
+    """C = W + 8 over 400 decode steps: one compaction every gap = 9 steps,
+    about 44 events (the page's small-slack test)."""
+    W = 128
+    C = W + 8
+    T0 = 2048  # after a long prompt
+    sk = np.arange(T0, T0 + 400, dtype=np.int32)
+    out = orc.seq_lengths(sk, 1, C, orc.DRIFTING, W)
+    events = int((out["evict"] > 0).sum())
+    assert events in (44, 45)
+    assert set(np.unique(out["evict"]).tolist()) == {0, C - W + 1}
+
+
+def test_drift_gap_one_is_windowed(orc):
+    """C = W gives gap = 1: the drifting layout is the compact-every-step one."""
+    for C in (1, 5, 128):
+        sk = np.arange(-1 + 1, 4 * C + 3, dtype=np.int32)
+        for S in (1, 3):
+            a = orc.seq_lengths(sk + S - 1, S, C, orc.DRIFTING, C)
+            b = orc.seq_lengths(sk + S - 1, S, C, orc.WINDOWED)
+            for f in ("past_abs", "total_abs", "cache_past", "cache_total", "evict"):
+                np.testing.assert_array_equal(a[f], b[f])
+
+
+def test_drift_rejects_bad_window(orc):
+    sk = np.array([3, 40], dtype=np.int32)
+    for W in (0, 17):
+        out = orc.seq_lengths(sk, 1, 16, orc.DRIFTING, W)
+        assert (out["flags"] == orc.BAD_CAPACITY).all()
+        assert (out["cache_total"] == -1).all()
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_drift_invariant_random_schedules(orc, seed):
+    rng = np.random.default_rng(300 + seed)
+    C = int(rng.integers(3, 12))
+    W = int(rng.integers(1, C + 1))
+    schedule = [1] * 30 + [int(x) for x in rng.integers(2, 2 * C + 2, size=6)]
+    rng.shuffle(schedule)
+    _run_schedule(orc, C, schedule, 2, seed, window=W)
