@@ -13,6 +13,8 @@ Other workloads (--workload):
                   one of 16 replica caches in turn (268 MB > L2, "cold"), as
                   one fused kvc_window_decode_step launch
   window-decode-unfused  the same as three launches
+  window-decode-drift    the same with the drifting layout, C = W + 16 = 144
+                  (a block of 17 rows reclaimed every 17 steps; fused step)
   window-prefill  8 x 16/8 heads x 256, C = W = 4096, P ~ U[0, 20000],
                   --chunk S in {64, 512, 2048}; one step = lengths + staging
                   seed/append + tcgen05 chunk attention + copy-back
@@ -254,14 +256,30 @@ class ContigDecode(Workload):
         return METRIC, "GB/s"
 
 
+def _cache_lengths(policy, T, S, C, W):
+    """Lp, E, L per row for the byte accounting (include/kvc.h, kvc_seq_lengths)."""
+    T = np.asarray(T, dtype=np.int64)
+
+    def end(t):
+        gap = C - W + 1
+        return np.where(t <= C, t, t - gap * ((t - C + gap - 1) // gap))
+    if policy == 2:
+        Lp, L = end(T - S), end(T)
+        return Lp, Lp + S - L, L
+    Lp = np.minimum(T - S, C)
+    E = np.maximum(0, Lp + S - C)
+    return Lp, E, Lp - E + S
+
+
 class WindowDecode(Workload):
-    """Sliding-window ring cache decode with in-place compaction (E <= 1),
-    cycling over 16 replica caches (one per model layer, 268 MB in all).
-    fused=True runs each step as one kvc_window_decode_step launch; otherwise
-    as kvc_seq_lengths + kvc_window_append + kvc_gqa_decode."""
+    """Sliding-window cache decode with in-place compaction, cycling over 16
+    replica caches (one per model layer, 268 MB in all).  fused=True runs each
+    step as one kvc_window_decode_step launch; otherwise as kvc_seq_lengths +
+    kvc_window_append + kvc_gqa_decode."""
     bound = "hbm"
     replicas = 16
     fused = True
+    spec = "WINDOW_DECODE"
 
     def __init__(self, dev, seed=0, with_kernels=True, chunk=None, max_steps=4096):
         self.roofline_kernel = ("kvc_window_decode_step (fused step)" if self.fused
@@ -272,7 +290,8 @@ class WindowDecode(Workload):
 
         from persistent_kv_cache_gb300 import synth
         self.torch = torch
-        w = self.w = synth.WINDOW_DECODE
+        w = self.w = getattr(synth, self.spec)
+        self.policy = w.extra.get("policy", 1)
         B, Hq, Hkv, D, C = w.batch, w.q_heads, w.kv_heads, w.head_dim, w.capacity
         R = self.replicas
         g = torch.Generator(device=dev)
@@ -294,15 +313,20 @@ class WindowDecode(Workload):
         cos, sin = synth.rope_cache(int(self.T0.max()) + n_rounds + 1, D, w.theta)
         self.rope = (cos.to(dev), sin.to(dev))
         e = self.e
-        # Algorithmic bytes of one step: the window's K/V rows read once, the
-        # rows the eviction moves written back one row lower, the new K/V
-        # rows read and written, q read, out written.
-        T = self.T0.astype(np.int64) + 1
-        L = np.minimum(T, C)
-        moved = np.where(T > C, C - 1, 0)
-        attn = int(L.sum()) * Hkv * D * 2 * e + 2 * B * Hq * D * e
-        self.bytes_per_step = (attn + int(moved.sum()) * Hkv * D * 2 * e
-                               + 2 * 2 * B * Hkv * D * e)
+        # Algorithmic bytes of one step, averaged over the rounds the run
+        # cycles through: the old rows read once (all resident rows when they
+        # move, else only those the window sees), the moved rows written back
+        # E rows lower, the new K/V rows read and written, q read, out
+        # written.  The unfused decode kernel alone reads the visible rows.
+        W = w.window
+        T = self.T0.astype(np.int64)[None, :] + 1 + np.arange(n_rounds)[:, None]
+        Lp, E, L = _cache_lengths(self.policy, T, 1, C, W)
+        moved = np.where(E > 0, L - 1, 0)
+        old = np.where(E > 0, L - 1, np.minimum(L, W) - 1)
+        row = Hkv * D * 2 * e
+        self.bytes_per_step = int(round(float((old + moved).sum(axis=1).mean()) * row
+                                        + 2 * 2 * B * Hkv * D * e + 2 * B * Hq * D * e))
+        attn = int(round(float(np.minimum(L, W).sum(axis=1).mean()) * row)) + 2 * B * Hq * D * e
         self.kernel_bytes = self.bytes_per_step if self.fused else attn
         self.tokens_per_step = B
         if not with_kernels:
@@ -321,12 +345,12 @@ class WindowDecode(Workload):
         if self.fused:
             K.kvc_window_decode_step(self.out, self.q, self.kc[r], self.vc[r], self.nk, self.nv,
                                      self.sk_all[i // R], w.window, lengths=self.L,
-                                     rope=self.rope, status=self.st)
+                                     rope=self.rope, status=self.st, windowed=self.policy)
             return
-        K.kvc_seq_lengths(self.sk_all[i // R], 1, w.capacity, 1, local_window_size=w.window,
-                          out=self.L, status=self.st)
-        K.kvc_window_append(self.kc[r], self.vc[r], self.nk, self.nv, self.L, 1, rope=self.rope,
-                            status=self.st)
+        K.kvc_seq_lengths(self.sk_all[i // R], 1, w.capacity, self.policy,
+                          local_window_size=w.window, out=self.L, status=self.st)
+        K.kvc_window_append(self.kc[r], self.vc[r], self.nk, self.nv, self.L, self.policy,
+                            rope=self.rope, status=self.st)
         self.kernel(i)
 
     def kernel(self, i):
@@ -344,6 +368,7 @@ class WindowDecode(Workload):
                 "kv_heads": w.kv_heads, "head_dim": w.head_dim, "capacity": w.capacity,
                 "window": w.window, "start_total": f"U[{w.total_lo},{w.total_hi}]",
                 "replica_caches": self.replicas, "new_tokens": 1, "fused_step": self.fused,
+                "layout": "drifting" if self.policy == 2 else "compact every step",
                 "l2": "16 replica caches cycled (268 MB > L2)",
                 "bytes_per_step": self.bytes_per_step}
 
@@ -357,7 +382,7 @@ class WindowDecode(Workload):
         cos, sin = (t.cpu().numpy() for t in self.rope)
         sk = (self.T0[rows]).astype(np.int32)  # the first step: T = T0 + 1
         t0 = time.perf_counter()
-        lens = oracle.seq_lengths(sk, 1, w.capacity, 1)
+        lens = oracle.seq_lengths(sk, 1, w.capacity, self.policy, w.window)
         oracle.window_append(kc, vc, synth.bits(self.nk_host[rows]),
                              synth.bits(self.nv_host[rows]), lens, 1, cos, sin)
         oracle.gqa_attention(synth.bits(self.q_host[rows]), kc, vc, lens["cache_total"],
@@ -550,8 +575,13 @@ class WindowDecodeUnfused(WindowDecode):
     fused = False
 
 
+class WindowDecodeDrift(WindowDecode):
+    spec = "WINDOW_DECODE_DRIFT"
+
+
 WORKLOADS = {"contig-decode": ContigDecode, "window-decode": WindowDecode,
-             "window-decode-unfused": WindowDecodeUnfused, "window-prefill": WindowPrefill,
+             "window-decode-unfused": WindowDecodeUnfused,
+             "window-decode-drift": WindowDecodeDrift, "window-prefill": WindowPrefill,
              "scatter": Scatter}
 
 
@@ -582,7 +612,8 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     n_steps = args.warmup * 2 + args.steps * 3 + 8
     kw = {"chunk": args.chunk}
-    if args.workload in ("window-decode", "window-decode-unfused", "scatter"):
+    if args.workload in ("window-decode", "window-decode-unfused", "window-decode-drift",
+                         "scatter"):
         kw["max_steps"] = n_steps
     wl = WORKLOADS[args.workload](dev, seed=rank, **kw)
     peaks, peak_kind = load_peaks()

@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define KVC_ABI_VERSION 1
+#define KVC_ABI_VERSION 2
 
 typedef enum {
     KVC_OK = 0,
@@ -78,6 +78,16 @@ typedef enum {
 typedef enum { KVC_F32 = 0, KVC_BF16 = 1, KVC_F16 = 2 } kvc_dtype;
 typedef enum { KVC_LINEAR = 0, KVC_CIRCULAR = 1 } kvc_mode;
 typedef enum { KVC_APPEND = 0, KVC_COPY_BACK = 1 } kvc_phase;
+/* How the resident rows of a cache follow the absolute length T (the
+ * `windowed` argument of the calls below). */
+typedef enum {
+    KVC_CONTIGUOUS = 0, /* every token stays: rows [0, T), T <= C               */
+    KVC_WINDOWED = 1,   /* the last min(T, C) tokens; compaction on every step
+                           once the cache is full                              */
+    KVC_DRIFTING = 2    /* the last end(T) tokens, W <= end(T) <= C: compaction
+                           reclaims C - W + 1 rows at once, every C - W + 1
+                           one-token steps                                     */
+} kvc_cache_policy;
 
 /* device status bits (OR-ed into *dev_status) */
 #define KVC_DEV_INDEX_OOB 1u    /* TensorScatter linear: wi < 0 or wi + S > max_seq    */
@@ -137,14 +147,18 @@ kvc_status kvc_tensor_scatter(void *present_cache, const void *past_cache, const
  * kvc_seq_lengths -- derive the five length arrays on the device ("GQA
  * support sliding_window_cache", "Design"; int64 arithmetic per the PR's
  * widening commit).  T = seqlens_k[b] + 1 computed in 64 bits, P = T - S.
- *   windowed != 0:  Lp = min(P, C), E = max(0, Lp + S - C), L = Lp - E + S
- *   windowed == 0:  Lp = P, E = 0, L = T; T > C sets KVC_DEV_CAPACITY.
+ *   KVC_WINDOWED:   Lp = min(P, C), E = max(0, Lp + S - C), L = Lp - E + S
+ *   KVC_DRIFTING:   Lp = end(P), L = end(T), E = Lp + S - L, where (the PR's
+ *                   CPU commit, "drifting layout") gap = C - W + 1 and
+ *                   end(T) = T for T <= C, else T - gap * ceil((T - C) / gap)
+ *   KVC_CONTIGUOUS: Lp = P, E = 0, L = T; T > C sets KVC_DEV_CAPACITY.
  * T < S or T >= 2^31 sets KVC_DEV_SEQLEN_RANGE.  A rejected row gets -1 in
  * every array.
  * seqlens_k        device int32 [batch].
  * new_tokens       S >= 1.
  * capacity         C >= 1 rows per head.
- * local_window_size  windowed cache: must satisfy 0 < W <= C
+ * windowed         a kvc_cache_policy (other values: KVC_ERR_UNSUPPORTED).
+ * local_window_size  windowed or drifting cache: must satisfy 0 < W <= C
  *                  (KVC_ERR_WINDOW otherwise); ignored for a contiguous cache.
  */
 kvc_status kvc_seq_lengths(const int32_t *seqlens_k, int batch, int new_tokens, int64_t capacity,
@@ -163,10 +177,14 @@ kvc_status kvc_seq_lengths(const int32_t *seqlens_k, int batch, int new_tokens, 
  * k_stage, v_stage  device [batch, kv_heads, capacity + new_tokens, head_dim]
  *                   for a windowed cache with S > 1, else ignored (may be NULL).
  * len               outputs of kvc_seq_lengths for the same S and C.
+ * windowed          a kvc_cache_policy; KVC_WINDOWED and KVC_DRIFTING append
+ *                   alike (what differs is in `len`) and are called
+ *                   "windowed" below.
  * phase = KVC_APPEND:
  *   contiguous cache:      rows [P, P + S) of the cache.
  *   windowed, S == 1:      in place: rows [E, Lp) move to [0, Lp - E)
- *                          (E <= 1), then the new row goes to Lp - E.
+ *                          (E <= 1 for KVC_WINDOWED, 0 or C - W + 1 for
+ *                          KVC_DRIFTING), then the new row goes to Lp - E.
  *   windowed, S > 1:       seeds the stage: stage[0, Lp) = cache[0, Lp),
  *                          stage[Lp + i] = new row i.  Attention then runs on
  *                          the stage (kvc_gqa_prefill_chunk).
@@ -263,11 +281,12 @@ kvc_status kvc_gqa_decode_noalloc(void *out, const void *q, const void *k_cache,
  * kvc_window_decode_step -- one fused one-token step on a windowed cache:
  * kvc_seq_lengths + kvc_window_append (S = 1) + kvc_gqa_decode in a single
  * launch, with the same results ("GQA support sliding_window_cache",
- * "Design": Lp = min(P, C), E = max(0, Lp + 1 - C), rows [E, Lp) move to
- * [0, Lp - E), the new row goes to Lp - E; attention over the window that
- * results).  One CTA owns a (batch row, kv head) slice and reads it once:
- * the whole window is loaded into shared memory, written back one row lower
- * when a row was evicted, and attended over from there.  For small windows:
+ * "Design": rows [E, Lp) move to [0, Lp - E), the new row goes to Lp - E;
+ * attention over the window that results).  One CTA owns a (batch row, kv
+ * head) slice and reads it once: the resident rows are loaded into shared
+ * memory (when nothing is evicted, only those the window can see), written
+ * back E rows lower when rows were evicted (else only the new row is
+ * stored), and attended over from there.  For small windows:
  * capacity * head_dim <= 32768 (C <= 512 at D = 64, C <= 256 at D = 128),
  * else KVC_ERR_UNSUPPORTED.
  *
@@ -276,7 +295,8 @@ kvc_status kvc_gqa_decode_noalloc(void *out, const void *q, const void *k_cache,
  * new_k, new_v    device [batch, kv_heads, 1, head_dim].
  * seqlens_k       device int32 [batch] (total after this token, minus one).
  * len             the five length arrays to fill (as kvc_seq_lengths would,
- *                 windowed, S = 1), or all five NULL.
+ *                 same policy, S = 1), or all five NULL.
+ * windowed        KVC_WINDOWED or KVC_DRIFTING (else KVC_ERR_UNSUPPORTED).
  * Requires 0 < local_window_size <= capacity (KVC_ERR_WINDOW).  Supported:
  * KVC_BF16/KVC_F16, head_dim in {64, 128}, q_heads / kv_heads <= 16.
  * Device errors as kvc_seq_lengths / kvc_window_append / kvc_gqa_decode.
@@ -284,7 +304,7 @@ kvc_status kvc_gqa_decode_noalloc(void *out, const void *q, const void *k_cache,
 kvc_status kvc_window_decode_step(void *out, const void *q, void *k_cache, void *v_cache,
                                   const void *new_k, const void *new_v, const int32_t *seqlens_k,
                                   kvc_lengths len, int batch, int q_heads, int kv_heads,
-                                  int64_t capacity, int head_dim, int dtype,
+                                  int64_t capacity, int head_dim, int dtype, int windowed,
                                   int local_window_size, float scale, const float *rope_cos,
                                   const float *rope_sin, int64_t rope_max_pos,
                                   int32_t *dev_status, void *stream);

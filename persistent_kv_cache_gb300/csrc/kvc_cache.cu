@@ -5,8 +5,10 @@
 //   windowed cache of capacity C, S new tokens on past length P:
 //     Lp = min(P, C), E = max(0, Lp + S - C)
 //     shift cache[E .. Lp) -> cache[0 .. Lp - E), new rows -> [Lp - E, Lp - E + S)
-//   S == 1 runs in place (E <= 1); S > 1 runs through a C + S staging cache
-//   that is seeded, attended over, and copied back.
+//   drifting layout (the PR's CPU commit): Lp = end(P), L = end(T),
+//     E = Lp + S - L, the same shift and append with E = 0 on most steps
+//   S == 1 runs in place; S > 1 runs through a C + S staging cache that is
+//   seeded, attended over, and copied back.
 //
 // K rows are rotated at their absolute position while they are written (RoPE
 // baked into K: "Stateful decode & KV cache", "Sliding-window ring buffer").
@@ -16,14 +18,15 @@
 //   new_rows_kernel      writes the S new rows (RoPE on K) at a per-row offset
 //   copy_range_kernel    per-(b, head) contiguous row range copy (stage seed,
 //                        copy-back), 16-byte vectors
-//   compact_kernel       windowed S == 1: in-place one-row left shift of the
+//   compact_kernel       windowed S == 1: in-place E-row left shift of the
 //                        resident rows in ascending tiles, then the new row
 #include "kvc_common.cuh"
 
 namespace {
 
 __global__ void seq_lengths_kernel(const int32_t *__restrict__ seqlens_k, int batch, int S,
-                                   int64_t C, int windowed, kvc_lengths out, int32_t *status)
+                                   int64_t C, int policy, int64_t W, kvc_lengths out,
+                                   int32_t *status)
 {
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= batch)
@@ -32,7 +35,7 @@ __global__ void seq_lengths_kernel(const int32_t *__restrict__ seqlens_k, int ba
     uint32_t bad = 0;
     if (T < S || T > (int64_t)INT32_MAX)
         bad = KVC_DEV_SEQLEN_RANGE;
-    else if (!windowed && T > C)
+    else if (policy == KVC_CONTIGUOUS && T > C)
         bad = KVC_DEV_CAPACITY;
     if (bad) {
         kvc::raise_status(status, bad);
@@ -40,19 +43,9 @@ __global__ void seq_lengths_kernel(const int32_t *__restrict__ seqlens_k, int ba
             out.evict[b] = -1;
         return;
     }
-    const int64_t P = T - S;
     int64_t Lp, E, L;
-    if (windowed) {
-        Lp = P < C ? P : C;
-        E = Lp + S - C;
-        E = E > 0 ? E : 0;
-        L = Lp - E + S;
-    } else {
-        Lp = P;
-        E = 0;
-        L = T;
-    }
-    out.past_abs[b] = (int32_t)P;
+    kvc::cache_lengths(policy, T, S, C, W, Lp, E, L);
+    out.past_abs[b] = (int32_t)(T - S);
     out.total_abs[b] = (int32_t)T;
     out.cache_past[b] = (int32_t)Lp;
     out.cache_total[b] = (int32_t)L;
@@ -177,12 +170,12 @@ copy_range_kernel(char *__restrict__ k_dst, char *__restrict__ v_dst,
         dst[i] = src[i];
 }
 
-// Windowed S == 1, in place.  One CTA per (b, head, K/V).  When E == 1 the
-// rows [1, Lp) move down by one row: the slice is walked in ascending tiles,
-// each tile loaded into registers, then (after a barrier) stored one row
-// lower.  A tile's stores only touch rows its own loads or earlier tiles'
-// loads already consumed, so the move needs no scratch buffer.  The new row
-// is written after the last tile.
+// Windowed S == 1, in place.  One CTA per (b, head, K/V).  When E > 0 the
+// rows [E, Lp) move down by E rows: the slice is walked in ascending tiles,
+// each tile loaded into registers, then (after a barrier) stored E rows
+// lower.  A tile's stores land below everything that it or any later tile
+// still has to load, so the move needs no scratch buffer.  The new row is
+// written after the last tile.
 template <typename T, int VEC>
 __global__ void __launch_bounds__(256)
 compact_kernel(T *__restrict__ k_cache, T *__restrict__ v_cache, const T *__restrict__ new_k,
@@ -205,17 +198,17 @@ compact_kernel(T *__restrict__ k_cache, T *__restrict__ v_cache, const T *__rest
     }
     const int Lp = len.cache_past[b];
     const int E = len.evict[b];
-    if (Lp < 0 || E < 0 || E > 1 || Lp - E + 1 > C || (E == 1 && Lp < 1)) {
+    if (Lp < 0 || Lp > C || E < 0 || E > Lp || Lp - E + 1 > C) {
         if (threadIdx.x == 0 && is_k && slice % kv_heads == 0)
             kvc::raise_status(status, KVC_DEV_CAPACITY);
         return;
     }
     T *cache = (is_k ? k_cache : v_cache) + (int64_t)slice * C * D;
     if (E > 0) {
-        // move (Lp - 1) rows down by one: flat copy of 16-byte vectors
+        // move (Lp - E) rows down by E: flat copy of 16-byte vectors
         uint4 *base = reinterpret_cast<uint4 *>(cache);
-        const int64_t row_v = (int64_t)D * sizeof(T) / 16;
-        const int64_t n = (int64_t)(Lp - 1) * row_v;
+        const int64_t shift_v = (int64_t)E * D * sizeof(T) / 16;
+        const int64_t n = (int64_t)(Lp - E) * D * sizeof(T) / 16;
         const int64_t tile = (int64_t)blockDim.x * U;
         for (int64_t t0 = 0; t0 < n; t0 += tile) {
             uint4 r[U];
@@ -223,7 +216,7 @@ compact_kernel(T *__restrict__ k_cache, T *__restrict__ v_cache, const T *__rest
             for (int u = 0; u < U; ++u) {
                 const int64_t i = t0 + (int64_t)u * blockDim.x + threadIdx.x;
                 if (i < n)
-                    r[u] = base[i + row_v];
+                    r[u] = base[i + shift_v];
             }
             __syncthreads();
 #pragma unroll
@@ -331,14 +324,16 @@ KVC_API kvc_status kvc_seq_lengths(const int32_t *seqlens_k, int batch, int new_
         return KVC_ERR_SHAPE;
     if (capacity < 1 || capacity > (int64_t)INT32_MAX)
         return KVC_ERR_CAPACITY;
-    if (windowed && (local_window_size <= 0 || local_window_size > capacity))
+    if (windowed != KVC_CONTIGUOUS && windowed != KVC_WINDOWED && windowed != KVC_DRIFTING)
+        return KVC_ERR_UNSUPPORTED;
+    if (windowed != KVC_CONTIGUOUS && (local_window_size <= 0 || local_window_size > capacity))
         return KVC_ERR_WINDOW;
     if (batch == 0)
         return KVC_OK;
     if (!seqlens_k || !kvc_host::lengths_ok(out))
         return KVC_ERR_NULL;
     seq_lengths_kernel<<<(batch + 127) / 128, 128, 0, static_cast<cudaStream_t>(stream)>>>(
-        seqlens_k, batch, new_tokens, capacity, windowed ? 1 : 0, out, dev_status);
+        seqlens_k, batch, new_tokens, capacity, windowed, local_window_size, out, dev_status);
     return kvc_host::launch_status();
 }
 
@@ -358,6 +353,8 @@ KVC_API kvc_status kvc_window_append(void *k_cache, void *v_cache, const void *n
     if (capacity < 1 || capacity > (int64_t)INT32_MAX)
         return KVC_ERR_CAPACITY;
     if (phase != KVC_APPEND && phase != KVC_COPY_BACK)
+        return KVC_ERR_UNSUPPORTED;
+    if (windowed != KVC_CONTIGUOUS && windowed != KVC_WINDOWED && windowed != KVC_DRIFTING)
         return KVC_ERR_UNSUPPORTED;
     if ((rope_cos == nullptr) != (rope_sin == nullptr))
         return KVC_ERR_NULL;

@@ -34,6 +34,46 @@ __device__ __forceinline__ uint64_t global_ns()
 }
 
 // --------------------------------------------------------------------------
+// cache-relative lengths of one batch row ("GQA support sliding_window_cache")
+// --------------------------------------------------------------------------
+
+// Rows resident after T absolute tokens under the drifting layout of the
+// PR's CPU commit: the append point runs on to C, then a whole block of
+// gap = C - W + 1 rows is reclaimed at once, so W <= end(T) <= C.
+__host__ __device__ __forceinline__ int64_t drift_end(int64_t T, int64_t C, int64_t W)
+{
+    if (T <= C)
+        return T;
+    const int64_t gap = C - W + 1;
+    return T - gap * ((T - C + gap - 1) / gap);
+}
+
+// Lp (resident before), E (evicted) and L (resident after) for a step of S
+// tokens that ends at absolute length T.  policy KVC_CONTIGUOUS: the cache
+// holds every token; KVC_WINDOWED: the last min(T, C) tokens; KVC_DRIFTING:
+// the last drift_end(T) tokens.  T >= S >= 1 and 1 <= W <= C are the
+// caller's to check.
+__host__ __device__ __forceinline__ void cache_lengths(int policy, int64_t T, int64_t S,
+                                                       int64_t C, int64_t W, int64_t &Lp,
+                                                       int64_t &E, int64_t &L)
+{
+    const int64_t P = T - S;
+    if (policy == KVC_DRIFTING) {
+        Lp = drift_end(P, C, W);
+        L = drift_end(T, C, W);
+        E = Lp + S - L;
+    } else if (policy == KVC_WINDOWED) {
+        Lp = P < C ? P : C;
+        E = Lp + S - C > 0 ? Lp + S - C : 0;
+        L = Lp - E + S;
+    } else {
+        Lp = P;
+        E = 0;
+        L = T;
+    }
+}
+
+// --------------------------------------------------------------------------
 // element types
 // --------------------------------------------------------------------------
 

@@ -261,6 +261,7 @@ struct DecodeArgs {
     kvc_lengths len;
     int q_heads, kv_heads, group;
     int64_t capacity;
+    int policy;  // KVC_WINDOWED or KVC_DRIFTING
     int window;
     float scale_log2;
     const float *cos_t, *sin_t;
@@ -483,14 +484,15 @@ decode_combine_kernel(const DecodeArgs a, int D)
 // --------------------------------------------------------------------------
 // Fused one-token step on a windowed cache: lengths, compaction, RoPE append
 // and GQA attention in one launch ("GQA support sliding_window_cache",
-// "Design": Lp = min(P, C), E = max(0, Lp + 1 - C), rows [E, Lp) move to
-// [0, Lp - E) and the new row goes to Lp - E).  One CTA owns one (batch row,
-// kv head) slice and keeps the whole new window in shared memory: cp.async
-// brings every old row in at once (from cache row r + E) while the threads
-// rotate the query and the new row, then the window is written back one row
-// lower when a row was evicted (all reads have completed, so the in-place
-// move needs no scratch) and attended over from shared memory.  The slice is
-// read once instead of twice (shift, then attention), in one launch.
+// "Design": rows [E, Lp) move to [0, Lp - E) and the new row goes to Lp - E;
+// Lp, E, L from the windowed formula or from the drifting layout of the PR's
+// CPU commit).  One CTA owns one (batch row, kv head) slice and keeps the new
+// window in shared memory: cp.async brings the old rows in at once (from
+// cache row r + E) while the threads rotate the query and the new row.  When
+// rows were evicted the window is then written back E rows lower (all reads
+// have completed, so the in-place move needs no scratch); otherwise only the
+// rows the window can see are loaded and only the new row is stored.  The
+// attention runs from shared memory, so the slice is read once, in one launch.
 // --------------------------------------------------------------------------
 struct WindowStepArgs {
     void *out;
@@ -501,6 +503,7 @@ struct WindowStepArgs {
     kvc_lengths len;  // all NULL: not written
     int q_heads, kv_heads, group;
     int64_t capacity;
+    int policy;  // KVC_WINDOWED or KVC_DRIFTING
     int window;
     float scale_log2;
     const float *cos_t, *sin_t;
@@ -542,9 +545,9 @@ window_step_kernel(const WindowStepArgs a)
         return;
     }
     const int P = (int)(T_ - 1);
-    const int Lp = (int)(P < C ? P : C);
-    const int E = (int)(Lp + 1 - C > 0 ? Lp + 1 - C : 0);
-    const int L = Lp - E + 1;
+    int64_t Lp64, E64, L64;
+    kvc::cache_lengths(a.policy, T_, 1, C, a.window, Lp64, E64, L64);
+    const int Lp = (int)Lp64, E = (int)E64, L = (int)L64;
     if (write_len) {
         a.len.past_abs[b] = P;
         a.len.total_abs[b] = (int32_t)T_;
@@ -564,8 +567,10 @@ window_step_kernel(const WindowStepArgs a)
     T *vc = static_cast<T *>(a.v_cache) + slice * C * D;
     const int ntiles = (L + kTile - 1) / kTile;
 
-    // 1. every window row except the new one, straight from cache row r + E
-    //    into the swizzled tiles; the rows after the window's end are zeroed
+    // 1. the old rows, straight from cache row r + E into the swizzled tiles:
+    //    all of them when they move, else only those the window sees; rows
+    //    not loaded are zeroed (a masked row must still be finite for P.V)
+    const int r_load0 = E > 0 ? 0 : vis0;
     const int nchunks = ntiles * kTile * CPR;
     for (int idx = threadIdx.x; idx < 2 * nchunks; idx += 128) {
         const bool is_v = idx >= nchunks;
@@ -573,12 +578,12 @@ window_step_kernel(const WindowStepArgs a)
         const int r = w / CPR, c = w % CPR;  // window row, 16-byte chunk
         uint8_t *dst = tiles + (size_t)(r / kTile) * 2 * KT_BYTES + (is_v ? KT_BYTES : 0) +
                        (c >> 3) * 8192 + kvc::sw128(r % kTile, c & 7);
-        if (r < L - 1) {
+        if (r >= r_load0 && r < L - 1) {
             const T *src = (is_v ? vc : kc) + (int64_t)(r + E) * D + c * 8;
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(kvc::smem_u32(dst)),
                          "l"(src)
                          : "memory");
-        } else if (r >= L) {
+        } else if (r != L - 1) {
             *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
         }
     }
@@ -632,7 +637,7 @@ window_step_kernel(const WindowStepArgs a)
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
 
-    // 3. write the window back: every row one lower when a row was evicted,
+    // 3. write the window back: every row E lower when rows were evicted,
     //    otherwise only the new row (at Lp).  All reads of the old rows are
     //    complete, so the in-place move needs no scratch.
     {
@@ -959,13 +964,16 @@ KVC_API kvc_status kvc_window_decode_step(void *out, const void *q, void *k_cach
                                           const void *new_k, const void *new_v,
                                           const int32_t *seqlens_k, kvc_lengths len, int batch,
                                           int q_heads, int kv_heads, int64_t capacity,
-                                          int head_dim, int dtype, int local_window_size,
-                                          float scale, const float *rope_cos,
-                                          const float *rope_sin, int64_t rope_max_pos,
-                                          int32_t *dev_status, void *stream)
+                                          int head_dim, int dtype, int windowed,
+                                          int local_window_size, float scale,
+                                          const float *rope_cos, const float *rope_sin,
+                                          int64_t rope_max_pos, int32_t *dev_status,
+                                          void *stream)
 {
     if (kvc_host::elem_bytes_of(dtype) == 0)
         return KVC_ERR_DTYPE;
+    if (windowed != KVC_WINDOWED && windowed != KVC_DRIFTING)
+        return KVC_ERR_UNSUPPORTED;
     if (batch < 0 || q_heads < 1 || kv_heads < 1 || q_heads % kv_heads != 0)
         return KVC_ERR_SHAPE;
     if (capacity < 1 || capacity > (int64_t)INT32_MAX)
@@ -1010,6 +1018,7 @@ KVC_API kvc_status kvc_window_decode_step(void *out, const void *q, void *k_cach
     a.kv_heads = kv_heads;
     a.group = g;
     a.capacity = capacity;
+    a.policy = windowed;
     a.window = local_window_size;
     a.scale_log2 = scale * kLog2e;
     a.cos_t = rope_cos;

@@ -24,6 +24,8 @@ STATUS_NAMES = {
     5: "KVC_ERR_UNSUPPORTED", 6: "KVC_ERR_CAPACITY", 7: "KVC_ERR_WINDOW",
     8: "KVC_ERR_WORKSPACE", 9: "KVC_ERR_CUDA",
 }
+# cache policies (the `windowed` argument)
+KVC_CONTIGUOUS, KVC_WINDOWED, KVC_DRIFTING = 0, 1, 2
 KVC_DEV_INDEX_OOB = 1
 KVC_DEV_SEQLEN_RANGE = 2
 KVC_DEV_CAPACITY = 4
@@ -91,8 +93,8 @@ def library() -> ctypes.CDLL:
             "kvc_gqa_decode": [P, P, P, P, L, I, I, I, I64, I, I, I, F, P, P, I64, P, SZ, P, P],
             "kvc_gqa_decode_workspace_size": [I, I, I, I64, I, I],
             "kvc_gqa_decode_noalloc": [P, P, P, P, L, I, I, I, I64, I, I, I, F, P, P, I64, P, P],
-            "kvc_window_decode_step": [P, P, P, P, P, P, P, L, I, I, I, I64, I, I, I, F, P, P, I64,
-                                       P, P],
+            "kvc_window_decode_step": [P, P, P, P, P, P, P, L, I, I, I, I64, I, I, I, I, F, P, P,
+                                       I64, P, P],
             "kvc_gqa_prefill_chunk": [P, P, P, P, I64, L, I, I, I, I, I, I, I, F, P, P, I64, P, P],
             "kvc_status_string": [I],
             "kvc_abi_version": [],
@@ -201,16 +203,19 @@ def kvc_gqa_decode_noalloc(out, q, k_cache, v_cache, lengths, local_window_size=
 
 
 def kvc_window_decode_step(out, q, k_cache, v_cache, new_k, new_v, seqlens_k, local_window_size,
-                           lengths=None, scale=0.0, rope=None, status=None, stream=None):
-    """Fused lengths + windowed one-token append + GQA decode (include/kvc.h)."""
+                           lengths=None, scale=0.0, rope=None, status=None, stream=None,
+                           windowed=None):
+    """Fused lengths + windowed one-token append + GQA decode (include/kvc.h).
+    ``windowed``: KVC_WINDOWED (default) or KVC_DRIFTING."""
+    windowed = KVC_WINDOWED if windowed is None else int(windowed)
     B, Hq, _, D = q.shape
     _, Hkv, C, _ = k_cache.shape
     cs, sn, rmax = _rope(rope)
     lc = lengths.c() if lengths is not None else KvcLengths(None, None, None, None, None)
     _check("kvc_window_decode_step", library().kvc_window_decode_step(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(new_k), _ptr(new_v),
-        _ptr(seqlens_k), lc, B, Hq, Hkv, C, D, _dtype_code(q), local_window_size, scale, cs, sn,
-        rmax, _ptr(status), _stream(stream)))
+        _ptr(seqlens_k), lc, B, Hq, Hkv, C, D, _dtype_code(q), windowed, local_window_size,
+        scale, cs, sn, rmax, _ptr(status), _stream(stream)))
     return out
 
 

@@ -118,6 +118,13 @@ CONTIG_DECODE = DecodeWorkload("contiguous-decode-bf16-b32-h32kv8-d128-c8192", b
 WINDOW_DECODE = DecodeWorkload("window-decode-bf16-b64-h64kv8-d64-w128", batch=64, q_heads=64,
                                kv_heads=8, head_dim=64, capacity=128, window=128, windowed=True,
                                total_lo=1, total_hi=32768, steps=256)
+# the drifting layout at the capacity the sliding-window PR's CPU commit finds
+# best for decode latency (C = W + 16, so a block of 17 rows is reclaimed
+# every 17 one-token steps)
+WINDOW_DECODE_DRIFT = DecodeWorkload("window-decode-drift-bf16-b64-h64kv8-d64-c144-w128",
+                                     batch=64, q_heads=64, kv_heads=8, head_dim=64,
+                                     capacity=144, window=128, windowed=True, total_lo=1,
+                                     total_hi=32768, steps=256, extra={"policy": 2})
 WINDOW_PREFILL = DecodeWorkload("window-prefill-bf16-b8-h16kv8-d256-w4096", batch=8,
                                 q_heads=16, kv_heads=8, head_dim=256, capacity=4096,
                                 window=4096, windowed=True, total_lo=0, total_hi=20000,

@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(kvc):
 
 
 def test_version_and_strings(kvc):
-    assert kvc.kvc_abi_version() == 1
+    assert kvc.kvc_abi_version() == 2
     assert kvc.kvc_status_string(0) == "ok"
     assert "window" in kvc.kvc_status_string(7)
 
@@ -72,6 +72,9 @@ def test_lengths_host_checks(kvc):
     assert f(FAKE, 4, 1, 128, 1, 0, L, None, None) == 7         # W missing
     assert f(None, 4, 1, 128, 1, 128, L, None, None) == 1
     assert f(FAKE, 0, 1, 128, 1, 128, L, None, None) == 0       # empty batch: nothing to do
+    assert f(FAKE, 4, 1, 128, 3, 128, L, None, None) == 5       # unknown policy
+    assert f(FAKE, 4, 1, 128, 2, 129, L, None, None) == 7       # drifting needs W <= C
+    assert f(FAKE, 4, 1, 128, 2, 0, L, None, None) == 7
 
 
 def test_append_host_checks(kvc):
@@ -84,6 +87,7 @@ def test_append_host_checks(kvc):
     assert f(*base, 2, 2, 1, 16, 7, 1, 1, 0, None, None, 0, None, None) == 2        # odd D
     assert f(*base, 2, 2, 4, 16, 8, 1, 1, 0, None, None, 0, None, None) == 1        # no stage
     assert f(*base, 2, 2, 1, 16, 8, 1, 1, 1, None, None, 0, None, None) == 5        # copy-back S=1
+    assert f(*base, 2, 2, 1, 16, 8, 1, 3, 0, None, None, 0, None, None) == 5        # policy
     assert f(*base, 2, 2, 1, 0, 8, 1, 1, 0, None, None, 0, None, None) == 6         # C < 1
     assert f(*base, 2, 2, 1, 16, 8, 1, 1, 0, FAKE, None, 16, None, None) == 1       # half a table
     unaligned = [FAKE + 2] + base[1:]
@@ -130,10 +134,13 @@ def test_window_step_host_checks(kvc):
     f = lib.kvc_window_decode_step
     none = kvc.KvcLengths(None, None, None, None, None)
     base = [FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, FAKE * 7]
-    assert f(*base, none, 2, 8, 2, 128, 64, 1, 129, 0.0, None, None, 0, None, None) == 7  # W > C
-    assert f(*base, none, 2, 8, 2, 128, 64, 1, 0, 0.0, None, None, 0, None, None) == 7    # W = 0
-    assert f(*base, none, 2, 8, 2, 128, 64, 0, 128, 0.0, None, None, 0, None, None) == 5  # fp32
-    assert f(*base, none, 2, 8, 2, 128, 96, 1, 128, 0.0, None, None, 0, None, None) == 5  # D
+    for pol in (1, 2):
+        assert f(*base, none, 2, 8, 2, 128, 64, 1, pol, 129, 0.0, None, None, 0, None, None) == 7
+        assert f(*base, none, 2, 8, 2, 128, 64, 1, pol, 0, 0.0, None, None, 0, None, None) == 7
+    assert f(*base, none, 2, 8, 2, 128, 64, 1, 0, 128, 0.0, None, None, 0, None, None) == 5  # contig
+    assert f(*base, none, 2, 8, 2, 128, 64, 1, 3, 128, 0.0, None, None, 0, None, None) == 5  # policy
+    assert f(*base, none, 2, 8, 2, 128, 64, 0, 1, 128, 0.0, None, None, 0, None, None) == 5  # fp32
+    assert f(*base, none, 2, 8, 2, 128, 96, 1, 1, 128, 0.0, None, None, 0, None, None) == 5  # D
     half = kvc.KvcLengths(FAKE, None, None, None, None)
-    assert f(*base, half, 2, 8, 2, 128, 64, 1, 128, 0.0, None, None, 0, None, None) == 1
-    assert f(*base, none, 0, 8, 2, 128, 64, 1, 128, 0.0, None, None, 0, None, None) == 0
+    assert f(*base, half, 2, 8, 2, 128, 64, 1, 2, 128, 0.0, None, None, 0, None, None) == 1
+    assert f(*base, none, 0, 8, 2, 128, 64, 1, 2, 128, 0.0, None, None, 0, None, None) == 0

@@ -25,16 +25,17 @@ def K():
     return kvc
 
 
-@pytest.mark.parametrize("windowed", [0, 1])
+@pytest.mark.parametrize("windowed", [0, 1, 2])
 def test_lengths(K, orc, windowed):
     rng = np.random.default_rng(7 + windowed)
     for S, C in [(1, 128), (5, 16), (64, 4096), (2048, 4096), (3, 1)]:
         sk = rng.integers(-3, 3 * C + S, size=97).astype(np.int32)
         sk[:4] = [-1, S - 1, INT32_MAX - 1, INT32_MAX]
-        want = orc.seq_lengths(sk, S, C, windowed)
+        W = max(1, C - 8) if windowed == 2 else C
+        want = orc.seq_lengths(sk, S, C, windowed, W)
         st = status()
         L = K.kvc_seq_lengths(torch.from_numpy(sk).to(dev()), S, C, windowed,
-                              local_window_size=C, status=st)
+                              local_window_size=W, status=st)
         got = lengths_np(L)
         for f in L.FIELDS:
             np.testing.assert_array_equal(got[f], want[f], err_msg=f"{f} S={S} C={C}")

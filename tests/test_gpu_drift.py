@@ -1,0 +1,161 @@
+"""GPU parity for the drifting windowed layout (the sliding-window PR's CPU
+commit: gap = C - W + 1, resident rows [0, end(T)), a whole gap-sized block
+reclaimed once every gap one-token steps) against the oracle.
+
+* one-token steps through kvc_seq_lengths + kvc_window_append +
+  kvc_gqa_decode and through the fused kvc_window_decode_step, on C = W + 8
+  over more than three gaps, rows starting before the window fills, at the
+  capacity and far past it: lengths and every cache byte after each step,
+  attention within 2e-2 (bf16) on every step that compacts and every fourth
+  one otherwise;
+* a large gap (C = 256, W = 56, so 201 rows leave at once and the surviving
+  55 rows do not overlap their old places);
+* 32-token chunks at C = W + 8 (the gap is smaller than the chunk: the
+  chunk stages from a drifted append point), interleaved with one-token
+  steps.
+"""
+import numpy as np
+import pytest
+import torch
+
+from _gpu_helpers import assert_bytes_equal, assert_close, dev, lengths_np, status
+from persistent_kv_cache_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def K():
+    from persistent_kv_cache_gb300 import kvc
+    return kvc
+
+
+def _one_token_run(K, orc, fused, B, g, Hkv, D, C, W, T0, steps, seed):
+    Hq = Hkv * g
+    T0 = np.asarray(T0, dtype=np.int64)
+    cos, sin = synth.rope_cache(int(T0.max()) + steps + 1, D)
+    rope_d = (cos.to(dev()), sin.to(dev()))
+    kc = synth.normal((B, Hkv, C, D), seed, 1)
+    vc = synth.normal((B, Hkv, C, D), seed, 2)
+    wk, wv = synth.bits(kc).copy(), synth.bits(vc).copy()
+    gk, gv = kc.to(dev()), vc.to(dev())
+    st = status()
+    out = torch.empty(B, Hq, 1, D, dtype=torch.bfloat16, device=dev())
+    Lg = K.Lengths(B, dev())
+    compactions = 0
+    for s in range(steps):
+        T = T0 + s
+        sk = (T - 1).astype(np.int32)
+        skd = torch.from_numpy(sk).to(dev())
+        nk = synth.normal((B, Hkv, 1, D), seed + 1, s)
+        nv = synth.normal((B, Hkv, 1, D), seed + 2, s)
+        q = synth.normal((B, Hq, 1, D), seed + 3, s)
+        if fused:
+            K.kvc_window_decode_step(out, q.to(dev()), gk, gv, nk.to(dev()), nv.to(dev()), skd,
+                                     W, lengths=Lg, rope=rope_d, status=st,
+                                     windowed=K.KVC_DRIFTING)
+        else:
+            K.kvc_seq_lengths(skd, 1, C, K.KVC_DRIFTING, local_window_size=W, out=Lg, status=st)
+            K.kvc_window_append(gk, gv, nk.to(dev()), nv.to(dev()), Lg, K.KVC_DRIFTING,
+                                rope=rope_d, status=st)
+            K.kvc_gqa_decode(out, q.to(dev()), gk, gv, Lg, local_window_size=W, rope=rope_d,
+                             status=st)
+        lens = orc.seq_lengths(sk, 1, C, orc.DRIFTING, W)
+        orc.window_append(wk, wv, synth.bits(nk), synth.bits(nv), lens, 1, cos.numpy(),
+                          sin.numpy())
+        torch.cuda.synchronize()
+        got_len = lengths_np(Lg)
+        for f in Lg.FIELDS:
+            np.testing.assert_array_equal(got_len[f], lens[f], err_msg=f"{f} step {s}")
+        assert_bytes_equal(gk, wk, f"k step {s}")
+        assert_bytes_equal(gv, wv, f"v step {s}")
+        compacting = bool((lens["evict"] > 0).any())
+        compactions += int((lens["evict"] > 0).sum())
+        if compacting or s % 4 == 3:
+            want, _ = orc.gqa_attention(synth.bits(q), wk, wv, lens["cache_total"],
+                                        lens["total_abs"], window=W, cos_cache=cos.numpy(),
+                                        sin_cache=sin.numpy())
+            assert_close(out, want, 2e-2, f"{'fused' if fused else 'unfused'} step {s}")
+    assert st.item() == 0
+    return compactions
+
+
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("D,g", [(64, 8), (128, 4)])
+def test_drift_one_token_steps(K, orc, fused, D, g):
+    W = 120
+    C = W + 8
+    # before the window fills, at the capacity, past it, far past it
+    T0 = [1, 119, 127, 128, 129, 700, 30000]
+    n = _one_token_run(K, orc, fused, len(T0), g, 2, D, C, W, T0, 30, 70 + D + fused)
+    assert n >= 3 * (len(T0) - 2)   # several compactions on every row that passes C
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_drift_large_gap(K, orc, fused):
+    """gap = 201: the surviving rows move farther than their own extent."""
+    W, C = 56, 256
+    T0 = [250, 256, 257, 5000]
+    n = _one_token_run(K, orc, fused, len(T0), 4, 2, 128, C, W, T0, 12, 90 + fused)
+    assert n >= 2
+
+
+def test_drift_chunks_small_slack(K, orc):
+    """32-token chunks at C = W + 8 with one-token steps between them: the
+    stage, the copy-back and the prefill attention under the drifting
+    lengths."""
+    B, Hq, Hkv, D, W = 2, 8, 2, 128, 40
+    C = W + 8
+    cos, sin = synth.rope_cache(1024, D)
+    rope_d = (cos.to(dev()), sin.to(dev()))
+    kc = torch.zeros(B, Hkv, C, D, dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    wk, wv = synth.bits(kc).copy(), synth.bits(vc).copy()
+    gk, gv = kc.to(dev()), vc.to(dev())
+    st = status()
+    T = np.array([0, 3], dtype=np.int64)
+    for step, S in enumerate([32, 32, 1, 1, 1, 32, 5, 1, 32, 32, 1]):
+        nk = synth.normal((B, Hkv, S, D), 11, 10 + step)
+        nv = synth.normal((B, Hkv, S, D), 11, 40 + step)
+        q = synth.normal((B, Hq, S, D), 11, 70 + step)
+        sk = (T + S - 1).astype(np.int32)
+        L = K.kvc_seq_lengths(torch.from_numpy(sk).to(dev()), S, C, K.KVC_DRIFTING,
+                              local_window_size=W, status=st)
+        lens = orc.seq_lengths(sk, S, C, orc.DRIFTING, W)
+        out = torch.empty(B, Hq, S, D, dtype=torch.bfloat16, device=dev())
+        if S == 1:
+            K.kvc_window_append(gk, gv, nk.to(dev()), nv.to(dev()), L, K.KVC_DRIFTING,
+                                rope=rope_d, status=st)
+            K.kvc_gqa_decode(out, q.to(dev()), gk, gv, L, local_window_size=W, rope=rope_d,
+                             status=st)
+            orc.window_append(wk, wv, synth.bits(nk), synth.bits(nv), lens, 1, cos.numpy(),
+                              sin.numpy())
+            want, _ = orc.gqa_attention(synth.bits(q), wk, wv, lens["cache_total"],
+                                        lens["total_abs"], window=W, cos_cache=cos.numpy(),
+                                        sin_cache=sin.numpy())
+        else:
+            ks = torch.empty(B, Hkv, C + S, D, dtype=torch.bfloat16, device=dev())
+            vs = torch.empty_like(ks)
+            K.kvc_window_append(gk, gv, nk.to(dev()), nv.to(dev()), L, K.KVC_DRIFTING,
+                                K.KVC_APPEND, ks, vs, rope=rope_d, status=st)
+            K.kvc_gqa_prefill_chunk(out, q.to(dev()), ks, vs, L, local_window_size=W,
+                                    rope=rope_d, status=st)
+            K.kvc_window_append(gk, gv, None, None, L, K.KVC_DRIFTING, K.KVC_COPY_BACK, ks, vs,
+                                rope=rope_d, status=st)
+            wks = np.zeros((B, Hkv, C + S, D), np.uint16)
+            wvs = np.zeros_like(wks)
+            orc.window_append(wk, wv, synth.bits(nk), synth.bits(nv), lens, 1, cos.numpy(),
+                              sin.numpy(), wks, wvs)
+            want, _ = orc.gqa_attention(synth.bits(q), wks, wvs,
+                                        (lens["cache_past"] + S).astype(np.int32),
+                                        lens["total_abs"], window=W, cos_cache=cos.numpy(),
+                                        sin_cache=sin.numpy())
+        torch.cuda.synchronize()
+        got_len = lengths_np(L)
+        for f in L.FIELDS:
+            np.testing.assert_array_equal(got_len[f], lens[f], err_msg=f"{f} step {step}")
+        assert_bytes_equal(gk, wk, f"k cache step {step}")
+        assert_bytes_equal(gv, wv, f"v cache step {step}")
+        assert_close(out, want, 2e-2, f"step {step}")
+        T += S
+    assert st.item() == 0
