@@ -19,6 +19,11 @@ patterns) and returns numpy arrays; each one cites the page it restates:
 * ``gqa_attention``   -- "Persistent KV Cache and Decode Performance Roadmap",
   "Phase 1" (what decode attention computes, GQA sharing) with the causal and
   local-window mask of the PR.
+* ``ring_slot_positions``, ``ring_append``, ``ring_attention`` -- "Stateful
+  decode & KV cache", "Sliding-window ring buffer": token p lives in slot
+  p mod C (TensorScatter circular with write index P, K rotated at write
+  time); attention lists the ring's slots in position order and is then the
+  plain attention above.
 
 Pins: every function is checked in ``tests/test_oracle_*.py`` against the
 pages' worked examples, closed forms, brute-force simulations and library
@@ -114,13 +119,16 @@ def tensor_scatter(past, update, write_indices, axis=-2, mode=LINEAR, out=None):
     return present, flags
 
 
-CONTIGUOUS, WINDOWED, DRIFTING = 0, 1, 2
+CONTIGUOUS, WINDOWED, DRIFTING, RING = 0, 1, 2, 3
 
 
 def seq_lengths(seqlens_k, new_tokens, capacity, windowed, window=0):
     """Returns dict(past_abs, total_abs, cache_past, cache_total, evict, flags).
     windowed: 0 contiguous, 1 windowed (compact every step), 2 drifting
-    (needs the window)."""
+    (needs the window), 3 ring (a ring of C slots holds the last min(T, C)
+    tokens, so its counts are the windowed ones)."""
+    if int(windowed) == RING:
+        windowed = WINDOWED
     sk = np.ascontiguousarray(seqlens_k, dtype=np.int32)
     B = sk.shape[0]
     outs = {k: np.zeros(B, dtype=np.int32) for k in
@@ -193,3 +201,67 @@ def gqa_attention(q, k_rows, v_rows, n_rows, total_abs, window=0, scale=None,
     if rc != 0:
         raise ValueError("gqa_attention: q_heads must be a multiple of kv_heads")
     return out, flags
+
+
+# --------------------------------------------------------------------------
+# ring buffer ("Stateful decode & KV cache", "Sliding-window ring buffer")
+# --------------------------------------------------------------------------
+
+def ring_slot_positions(T, C):
+    """Absolute position held by each of the C slots after T tokens were
+    written one by one at slot (position mod C); -1 for a slot never written.
+    Slot r holds the newest p < T with p = r (mod C)."""
+    pos = np.full(C, -1, dtype=np.int64)
+    for r in range(C):
+        p = (T - 1) - ((T - 1 - r) % C)
+        pos[r] = p if p >= 0 else -1
+    return pos
+
+
+def ring_append(k_ring, v_ring, new_k, new_v, past_abs, cos_cache=None, sin_cache=None):
+    """Write S new rows per (b, kv head) into rings [B, Hkv, C, D] in place:
+    row i of batch row b (absolute position P_b + i) goes to slot
+    (P_b + i) mod C, K rotated there first when the cos/sin tables are given.
+    This is TensorScatter circular with write index P_b on the rotated rows
+    (when S > C the later rows overwrite the earlier ones)."""
+    B, Hkv, S, D = new_k.shape
+    P = np.asarray(past_abs, dtype=np.int64)
+    nk = np.ascontiguousarray(new_k)
+    if cos_cache is not None:
+        pos = np.broadcast_to((P[:, None, None] + np.arange(S)[None, None, :]), (B, Hkv, S))
+        nk = rope_rows(nk, np.ascontiguousarray(pos).reshape(-1), cos_cache, sin_cache)
+    nv = np.ascontiguousarray(new_v)
+    C = k_ring.shape[2]
+    if S > C:
+        # TensorScatter takes at most max_seq rows; the earlier ones would be
+        # overwritten by the later ones anyway
+        nk = np.ascontiguousarray(nk[:, :, S - C:])
+        nv = np.ascontiguousarray(nv[:, :, S - C:])
+        P = P + (S - C)
+    _, fk = tensor_scatter(k_ring, nk, P, mode=CIRCULAR, out=k_ring)
+    _, fv = tensor_scatter(v_ring, nv, P, mode=CIRCULAR, out=v_ring)
+    return fk | fv
+
+
+def ring_attention(q, k_ring, v_ring, total_abs, window=0, scale=None, cos_cache=None,
+                   sin_cache=None):
+    """Attention of q [B, Hq, S, D] (query i at position T - S + i) over a
+    ring [B, Hkv, C, D] after T tokens: the ring's newest n = min(T, C, W)
+    positions (W <= 0: no window) are read from their slots in position
+    order, then the causal and window mask apply as in gqa_attention.  Exact
+    for the last query; earlier queries of a chunk that wrapped the ring miss
+    the keys it overwrote.  Returns (out, flags) like gqa_attention."""
+    B, Hkv, C, D = k_ring.shape
+    T = np.asarray(total_abs, dtype=np.int64)
+    k = np.zeros_like(k_ring)
+    v = np.zeros_like(v_ring)
+    n = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        nb = min(int(T[b]), C) if window <= 0 else min(int(T[b]), C, window)
+        held = ring_slot_positions(int(T[b]), C)
+        order = [int(np.nonzero(held == p)[0][0]) for p in range(int(T[b]) - nb, int(T[b]))]
+        k[b, :, :nb] = k_ring[b][:, order]
+        v[b, :, :nb] = v_ring[b][:, order]
+        n[b] = nb
+    return gqa_attention(q, k, v, n, T.astype(np.int32), window=window, scale=scale,
+                         cos_cache=cos_cache, sin_cache=sin_cache)
