@@ -15,6 +15,8 @@ Other workloads (--workload):
   window-decode-unfused  the same as three launches
   window-decode-drift    the same with the drifting layout, C = W + 16 = 144
                   (a block of 17 rows reclaimed every 17 steps; fused step)
+  window-decode-ring     the same window as a ring of C = W = 128 slots
+                  (token p in slot p mod C, nothing moves; fused step)
   window-prefill  8 x 16/8 heads x 256, C = W = 4096, P ~ U[0, 20000],
                   --chunk S in {64, 512, 2048}; one step = lengths + staging
                   seed/append + tcgen05 chunk attention + copy-back
@@ -266,6 +268,7 @@ def _cache_lengths(policy, T, S, C, W):
     if policy == 2:
         Lp, L = end(T - S), end(T)
         return Lp, Lp + S - L, L
+    # windowed and ring share the counts (a ring overwrites instead of moving)
     Lp = np.minimum(T - S, C)
     E = np.maximum(0, Lp + S - C)
     return Lp, E, Lp - E + S
@@ -321,8 +324,9 @@ class WindowDecode(Workload):
         W = w.window
         T = self.T0.astype(np.int64)[None, :] + 1 + np.arange(n_rounds)[:, None]
         Lp, E, L = _cache_lengths(self.policy, T, 1, C, W)
-        moved = np.where(E > 0, L - 1, 0)
-        old = np.where(E > 0, L - 1, np.minimum(L, W) - 1)
+        moves = (E > 0) & (self.policy != 3)
+        moved = np.where(moves, L - 1, 0)
+        old = np.where(moves, L - 1, np.minimum(L, W) - 1)
         row = Hkv * D * 2 * e
         self.bytes_per_step = int(round(float((old + moved).sum(axis=1).mean()) * row
                                         + 2 * 2 * B * Hkv * D * e + 2 * B * Hq * D * e))
@@ -347,6 +351,8 @@ class WindowDecode(Workload):
                                      self.sk_all[i // R], w.window, lengths=self.L,
                                      rope=self.rope, status=self.st, windowed=self.policy)
             return
+        if self.policy == 3:
+            raise ValueError("the ring workload runs as the fused step")
         K.kvc_seq_lengths(self.sk_all[i // R], 1, w.capacity, self.policy,
                           local_window_size=w.window, out=self.L, status=self.st)
         K.kvc_window_append(self.kc[r], self.vc[r], self.nk, self.nv, self.L, self.policy,
@@ -368,7 +374,7 @@ class WindowDecode(Workload):
                 "kv_heads": w.kv_heads, "head_dim": w.head_dim, "capacity": w.capacity,
                 "window": w.window, "start_total": f"U[{w.total_lo},{w.total_hi}]",
                 "replica_caches": self.replicas, "new_tokens": 1, "fused_step": self.fused,
-                "layout": "drifting" if self.policy == 2 else "compact every step",
+                "layout": {1: "compact every step", 2: "drifting", 3: "ring"}[self.policy],
                 "l2": "16 replica caches cycled (268 MB > L2)",
                 "bytes_per_step": self.bytes_per_step}
 
@@ -383,10 +389,17 @@ class WindowDecode(Workload):
         sk = (self.T0[rows]).astype(np.int32)  # the first step: T = T0 + 1
         t0 = time.perf_counter()
         lens = oracle.seq_lengths(sk, 1, w.capacity, self.policy, w.window)
-        oracle.window_append(kc, vc, synth.bits(self.nk_host[rows]),
-                             synth.bits(self.nv_host[rows]), lens, 1, cos, sin)
-        oracle.gqa_attention(synth.bits(self.q_host[rows]), kc, vc, lens["cache_total"],
-                             lens["total_abs"], window=w.window, cos_cache=cos, sin_cache=sin)
+        if self.policy == 3:
+            oracle.ring_append(kc, vc, synth.bits(self.nk_host[rows]),
+                               synth.bits(self.nv_host[rows]), lens["past_abs"], cos, sin)
+            oracle.ring_attention(synth.bits(self.q_host[rows]), kc, vc, lens["total_abs"],
+                                  w.window, cos_cache=cos, sin_cache=sin)
+        else:
+            oracle.window_append(kc, vc, synth.bits(self.nk_host[rows]),
+                                 synth.bits(self.nv_host[rows]), lens, 1, cos, sin)
+            oracle.gqa_attention(synth.bits(self.q_host[rows]), kc, vc, lens["cache_total"],
+                                 lens["total_abs"], window=w.window, cos_cache=cos,
+                                 sin_cache=sin)
         dt = time.perf_counter() - t0
         return dt, self.bytes_per_step * len(rows) / w.batch
 
@@ -579,9 +592,14 @@ class WindowDecodeDrift(WindowDecode):
     spec = "WINDOW_DECODE_DRIFT"
 
 
+class WindowDecodeRing(WindowDecode):
+    spec = "WINDOW_DECODE_RING"
+
+
 WORKLOADS = {"contig-decode": ContigDecode, "window-decode": WindowDecode,
              "window-decode-unfused": WindowDecodeUnfused,
-             "window-decode-drift": WindowDecodeDrift, "window-prefill": WindowPrefill,
+             "window-decode-drift": WindowDecodeDrift, "window-decode-ring": WindowDecodeRing,
+             "window-prefill": WindowPrefill,
              "scatter": Scatter}
 
 
@@ -613,7 +631,7 @@ def run_ours(args):
     n_steps = args.warmup * 2 + args.steps * 3 + 8
     kw = {"chunk": args.chunk}
     if args.workload in ("window-decode", "window-decode-unfused", "window-decode-drift",
-                         "scatter"):
+                         "window-decode-ring", "scatter"):
         kw["max_steps"] = n_steps
     wl = WORKLOADS[args.workload](dev, seed=rank, **kw)
     peaks, peak_kind = load_peaks()

@@ -9,6 +9,7 @@
  *                          append (windowed cache, one token), or C + S
  *                          staging seed / copy-back (windowed, several tokens)
  *     kvc_gqa_decode       one-token GQA attention over the cache
+ *     kvc_gqa_decode_ring  the same over a ring of C slots (circular addressing)
  *     kvc_window_decode_step  the three above fused for a windowed cache
  *     kvc_gqa_prefill_chunk  multi-token GQA attention over staged rows
  *     kvc_tensor_scatter   the ONNX TensorScatter cache update (linear/circular)
@@ -84,9 +85,12 @@ typedef enum {
     KVC_CONTIGUOUS = 0, /* every token stays: rows [0, T), T <= C               */
     KVC_WINDOWED = 1,   /* the last min(T, C) tokens; compaction on every step
                            once the cache is full                              */
-    KVC_DRIFTING = 2    /* the last end(T) tokens, W <= end(T) <= C: compaction
+    KVC_DRIFTING = 2,   /* the last end(T) tokens, W <= end(T) <= C: compaction
                            reclaims C - W + 1 rows at once, every C - W + 1
                            one-token steps                                     */
+    KVC_RING = 3        /* a ring of C slots: token p lives in slot p mod C and
+                           nothing ever moves ("Stateful decode & KV cache",
+                           "Sliding-window ring buffer")                       */
 } kvc_cache_policy;
 
 /* device status bits (OR-ed into *dev_status) */
@@ -147,7 +151,10 @@ kvc_status kvc_tensor_scatter(void *present_cache, const void *past_cache, const
  * kvc_seq_lengths -- derive the five length arrays on the device ("GQA
  * support sliding_window_cache", "Design"; int64 arithmetic per the PR's
  * widening commit).  T = seqlens_k[b] + 1 computed in 64 bits, P = T - S.
- *   KVC_WINDOWED:   Lp = min(P, C), E = max(0, Lp + S - C), L = Lp - E + S
+ *   KVC_WINDOWED, KVC_RING:
+ *                   Lp = min(P, C), E = max(0, Lp + S - C), L = Lp - E + S
+ *                   (for a ring: slots holding a token before / after the
+ *                   step, and old tokens the step overwrites)
  *   KVC_DRIFTING:   Lp = end(P), L = end(T), E = Lp + S - L, where (the PR's
  *                   CPU commit, "drifting layout") gap = C - W + 1 and
  *                   end(T) = T for T <= C, else T - gap * ceil((T - C) / gap)
@@ -158,7 +165,7 @@ kvc_status kvc_tensor_scatter(void *present_cache, const void *past_cache, const
  * new_tokens       S >= 1.
  * capacity         C >= 1 rows per head.
  * windowed         a kvc_cache_policy (other values: KVC_ERR_UNSUPPORTED).
- * local_window_size  windowed or drifting cache: must satisfy 0 < W <= C
+ * local_window_size  windowed, drifting or ring cache: must satisfy 0 < W <= C
  *                  (KVC_ERR_WINDOW otherwise); ignored for a contiguous cache.
  */
 kvc_status kvc_seq_lengths(const int32_t *seqlens_k, int batch, int new_tokens, int64_t capacity,
@@ -179,7 +186,10 @@ kvc_status kvc_seq_lengths(const int32_t *seqlens_k, int batch, int new_tokens, 
  * len               outputs of kvc_seq_lengths for the same S and C.
  * windowed          a kvc_cache_policy; KVC_WINDOWED and KVC_DRIFTING append
  *                   alike (what differs is in `len`) and are called
- *                   "windowed" below.
+ *                   "windowed" below.  KVC_RING: row i goes to slot
+ *                   (P + i) mod C for any S, nothing moves and no stage is
+ *                   used (when S > C only the last C rows are written, the
+ *                   ones that would survive); phase must be KVC_APPEND.
  * phase = KVC_APPEND:
  *   contiguous cache:      rows [P, P + S) of the cache.
  *   windowed, S == 1:      in place: rows [E, Lp) move to [0, Lp - E)
@@ -278,6 +288,25 @@ kvc_status kvc_gqa_decode_noalloc(void *out, const void *q, const void *k_cache,
                                   int32_t *dev_status, void *stream);
 
 /*
+ * kvc_gqa_decode_ring -- kvc_gqa_decode over a ring of C slots ("Stateful
+ * decode & KV cache", "Sliding-window ring buffer"; the ring written by
+ * kvc_window_append(KVC_RING) or by kvc_tensor_scatter in KVC_CIRCULAR mode
+ * at write index P): slot r holds position T - 1 - ((T - 1 - r) mod C).  The
+ * query at T - 1 sees the newest n = min(L, W) positions (n = L when
+ * local_window_size <= 0), where L = len.cache_total[b] (min(T, C) from
+ * kvc_seq_lengths) and T = len.total_abs[b]; they occupy slots
+ * (T - n) mod C onwards, wrapping at C.  Equal to kvc_gqa_decode over the
+ * full history whenever W <= C.  Arguments, layouts, supported sizes,
+ * workspace and errors are those of kvc_gqa_decode.
+ */
+kvc_status kvc_gqa_decode_ring(void *out, const void *q, const void *k_cache, const void *v_cache,
+                               kvc_lengths len, int batch, int q_heads, int kv_heads,
+                               int64_t capacity, int head_dim, int dtype, int local_window_size,
+                               float scale, const float *rope_cos, const float *rope_sin,
+                               int64_t rope_max_pos, void *workspace, size_t workspace_bytes,
+                               int32_t *dev_status, void *stream);
+
+/*
  * kvc_window_decode_step -- one fused one-token step on a windowed cache:
  * kvc_seq_lengths + kvc_window_append (S = 1) + kvc_gqa_decode in a single
  * launch, with the same results ("GQA support sliding_window_cache",
@@ -296,7 +325,10 @@ kvc_status kvc_gqa_decode_noalloc(void *out, const void *q, const void *k_cache,
  * seqlens_k       device int32 [batch] (total after this token, minus one).
  * len             the five length arrays to fill (as kvc_seq_lengths would,
  *                 same policy, S = 1), or all five NULL.
- * windowed        KVC_WINDOWED or KVC_DRIFTING (else KVC_ERR_UNSUPPORTED).
+ * windowed        KVC_WINDOWED, KVC_DRIFTING or KVC_RING (else
+ *                 KVC_ERR_UNSUPPORTED).  For a ring the new row goes to slot
+ *                 (T - 1) mod C, nothing else is written, and attention
+ *                 reads the slots as kvc_gqa_decode_ring does.
  * Requires 0 < local_window_size <= capacity (KVC_ERR_WINDOW).  Supported:
  * KVC_BF16/KVC_F16, head_dim in {64, 128}, q_heads / kv_heads <= 16.
  * Device errors as kvc_seq_lengths / kvc_window_append / kvc_gqa_decode.

@@ -9,6 +9,8 @@
 //     E = Lp + S - L, the same shift and append with E = 0 on most steps
 //   S == 1 runs in place; S > 1 runs through a C + S staging cache that is
 //   seeded, attended over, and copied back.
+//   ring of C slots ("Stateful decode & KV cache", "Sliding-window ring
+//   buffer"): new row i goes to slot (P + i) mod C, nothing moves.
 //
 // K rows are rotated at their absolute position while they are written (RoPE
 // baked into K: "Stateful decode & KV cache", "Sliding-window ring buffer").
@@ -83,12 +85,14 @@ __device__ __forceinline__ void write_new_pair(T *__restrict__ dst_row,
 }
 
 // grid: x over (i, pair-vector) of one (b, head) slice, y = b * Hkv + h, z = K/V
-// dst row of token i = dst_base_rows(b) + i, in a buffer with dst_rows rows/head
+// dst row of token i, in a buffer with dst_rows rows/head: P + i (base_mode
+// 0), cache_past + i (1), or (P + i) mod dst_rows for a ring (2, where only
+// the last dst_rows tokens are written)
 template <typename T, int VEC>
 __global__ void __launch_bounds__(128)
 new_rows_kernel(T *__restrict__ k_dst, T *__restrict__ v_dst, const T *__restrict__ new_k,
                 const T *__restrict__ new_v, kvc_lengths len, int kv_heads, int S, int D,
-                int64_t dst_rows, int offset_from_cache_past, const float *__restrict__ cos_t,
+                int64_t dst_rows, int base_mode, const float *__restrict__ cos_t,
                 const float *__restrict__ sin_t, int64_t rope_max_pos, int32_t *status)
 {
     const int slice = blockIdx.y;
@@ -104,26 +108,29 @@ new_rows_kernel(T *__restrict__ k_dst, T *__restrict__ v_dst, const T *__restric
             kvc::raise_status(status, KVC_DEV_ROPE_RANGE);
         return;
     }
-    const int base = offset_from_cache_past ? len.cache_past[b] : P;
-    if (base < 0 || (int64_t)base + S > dst_rows) {
+    const bool ring = base_mode == 2;
+    const int base = base_mode == 1 ? len.cache_past[b] : P;
+    if (base < 0 || (!ring && (int64_t)base + S > dst_rows)) {
         // lengths computed for another capacity: refuse rather than overrun
         if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0 && slice % kv_heads == 0)
             kvc::raise_status(status, KVC_DEV_CAPACITY);
         return;
     }
     const int pairs = D / (2 * VEC);
-    const int64_t work = (int64_t)S * pairs;
+    // a ring keeps only the last dst_rows tokens of the step
+    const int i0 = ring && (int64_t)S > dst_rows ? (int)(S - dst_rows) : 0;
+    const int64_t work = (int64_t)(S - i0) * pairs;
     T *dst = (is_k ? k_dst : v_dst) + (int64_t)slice * dst_rows * D;
     const T *src = (is_k ? new_k : new_v) + (int64_t)slice * S * D;
     for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < work;
          w += (int64_t)gridDim.x * blockDim.x) {
-        const int i = (int)(w / pairs);
-        const int j = (int)(w - (int64_t)i * pairs);
+        const int i = i0 + (int)(w / pairs);
+        const int j = (int)(w % pairs);
         const int64_t pos = (int64_t)P + i;
         const float *cs = rotate ? cos_t + pos * (D / 2) : nullptr;
         const float *sn = rotate ? sin_t + pos * (D / 2) : nullptr;
-        write_new_pair<T, VEC>(dst + ((int64_t)base + i) * D, src + (int64_t)i * D, D, j, rotate,
-                               cs, sn);
+        const int64_t row = ring ? pos % dst_rows : (int64_t)base + i;
+        write_new_pair<T, VEC>(dst + row * D, src + (int64_t)i * D, D, j, rotate, cs, sn);
     }
 }
 
@@ -253,7 +260,7 @@ kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const v
     T *vc = static_cast<T *>(v_cache);
     const T *nk = static_cast<const T *>(new_k);
     const T *nv = static_cast<const T *>(new_v);
-    auto launch_new_rows = [&](T *kd, T *vd, int64_t dst_rows, int from_cache_past) {
+    auto launch_new_rows = [&](T *kd, T *vd, int64_t dst_rows, int base_mode) {
         const int pairs = vec_ok ? D / (2 * VEC) : D / 2;
         const int64_t work = (int64_t)S * pairs;
         int gx = (int)((work + 127) / 128);
@@ -261,11 +268,11 @@ kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const v
         dim3 grid(gx, slices, 2);
         if (vec_ok)
             new_rows_kernel<T, VEC><<<grid, 128, 0, stream>>>(kd, vd, nk, nv, len, kv_heads, S, D,
-                                                              dst_rows, from_cache_past, cos_t,
+                                                              dst_rows, base_mode, cos_t,
                                                               sin_t, rope_max_pos, status);
         else
             new_rows_kernel<T, 1><<<grid, 128, 0, stream>>>(kd, vd, nk, nv, len, kv_heads, S, D,
-                                                            dst_rows, from_cache_past, cos_t,
+                                                            dst_rows, base_mode, cos_t,
                                                             sin_t, rope_max_pos, status);
     };
     auto launch_copy = [&](char *kd, char *vd, const char *ks, const char *vs, int64_t dst_rows,
@@ -288,10 +295,10 @@ kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const v
                                                                   status);
     };
 
-    if (!windowed) {
+    if (windowed == KVC_CONTIGUOUS || windowed == KVC_RING) {
         if (phase != KVC_APPEND)
             return KVC_ERR_UNSUPPORTED;
-        launch_new_rows(kc, vc, C, 0);
+        launch_new_rows(kc, vc, C, windowed == KVC_RING ? 2 : 0);
     } else if (S == 1) {
         if (phase != KVC_APPEND)
             return KVC_ERR_UNSUPPORTED;
@@ -324,7 +331,7 @@ KVC_API kvc_status kvc_seq_lengths(const int32_t *seqlens_k, int batch, int new_
         return KVC_ERR_SHAPE;
     if (capacity < 1 || capacity > (int64_t)INT32_MAX)
         return KVC_ERR_CAPACITY;
-    if (windowed != KVC_CONTIGUOUS && windowed != KVC_WINDOWED && windowed != KVC_DRIFTING)
+    if (windowed < KVC_CONTIGUOUS || windowed > KVC_RING)
         return KVC_ERR_UNSUPPORTED;
     if (windowed != KVC_CONTIGUOUS && (local_window_size <= 0 || local_window_size > capacity))
         return KVC_ERR_WINDOW;
@@ -354,7 +361,7 @@ KVC_API kvc_status kvc_window_append(void *k_cache, void *v_cache, const void *n
         return KVC_ERR_CAPACITY;
     if (phase != KVC_APPEND && phase != KVC_COPY_BACK)
         return KVC_ERR_UNSUPPORTED;
-    if (windowed != KVC_CONTIGUOUS && windowed != KVC_WINDOWED && windowed != KVC_DRIFTING)
+    if (windowed < KVC_CONTIGUOUS || windowed > KVC_RING)
         return KVC_ERR_UNSUPPORTED;
     if ((rope_cos == nullptr) != (rope_sin == nullptr))
         return KVC_ERR_NULL;
@@ -364,7 +371,8 @@ KVC_API kvc_status kvc_window_append(void *k_cache, void *v_cache, const void *n
         return KVC_OK;
     if (!k_cache || !v_cache || !kvc_host::lengths_ok(len))
         return KVC_ERR_NULL;
-    const bool staged = windowed && new_tokens > 1;
+    const bool staged =
+        (windowed == KVC_WINDOWED || windowed == KVC_DRIFTING) && new_tokens > 1;
     if (phase == KVC_APPEND && (!new_k || !new_v))
         return KVC_ERR_NULL;
     if (staged && (!k_stage || !v_stage))
@@ -389,7 +397,7 @@ KVC_API kvc_status kvc_window_append(void *k_cache, void *v_cache, const void *n
         if (p && !kvc_host::aligned16(p))
             return KVC_ERR_ALIGN;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-    const int w = windowed ? 1 : 0;
+    const int w = windowed;
     switch (dtype) {
     case KVC_F32:
         return append_typed<float>(k_cache, v_cache, new_k, new_v, k_stage, v_stage, len, batch,

@@ -50,8 +50,8 @@ __host__ __device__ __forceinline__ int64_t drift_end(int64_t T, int64_t C, int6
 
 // Lp (resident before), E (evicted) and L (resident after) for a step of S
 // tokens that ends at absolute length T.  policy KVC_CONTIGUOUS: the cache
-// holds every token; KVC_WINDOWED: the last min(T, C) tokens; KVC_DRIFTING:
-// the last drift_end(T) tokens.  T >= S >= 1 and 1 <= W <= C are the
+// holds every token; KVC_WINDOWED and KVC_RING: the last min(T, C) tokens;
+// KVC_DRIFTING: the last drift_end(T) tokens.  T >= S >= 1 and 1 <= W <= C are the
 // caller's to check.
 __host__ __device__ __forceinline__ void cache_lengths(int policy, int64_t T, int64_t S,
                                                        int64_t C, int64_t W, int64_t &Lp,
@@ -62,7 +62,7 @@ __host__ __device__ __forceinline__ void cache_lengths(int policy, int64_t T, in
         Lp = drift_end(P, C, W);
         L = drift_end(T, C, W);
         E = Lp + S - L;
-    } else if (policy == KVC_WINDOWED) {
+    } else if (policy == KVC_WINDOWED || policy == KVC_RING) {
         Lp = P < C ? P : C;
         E = Lp + S - C > 0 ? Lp + S - C : 0;
         L = Lp - E + S;

@@ -17,6 +17,11 @@
 //   * a split whose row holds more than one split writes (m, l, o) partials to
 //     the workspace and decode_combine_kernel merges them; a single split
 //     writes the output directly.
+// The visible rows are the newest n positions.  In a cache they are rows
+// [L - n, L); in a ring of C slots ("Stateful decode & KV cache",
+// "Sliding-window ring buffer") they start at slot (T - n) mod C and wrap, so
+// a split's rows are at most two contiguous runs of slots, each streamed as
+// its own sequence of tiles (a tile never crosses the wrap).
 // fp32 path: attn_f32_kernel, one warp per query row on CUDA cores (also used
 // by the multi-token call for fp32).
 #include <mutex>
@@ -261,7 +266,7 @@ struct DecodeArgs {
     kvc_lengths len;
     int q_heads, kv_heads, group;
     int64_t capacity;
-    int policy;  // KVC_WINDOWED or KVC_DRIFTING
+    int ring;    // slots addressed as a ring of `capacity` (kvc_gqa_decode_ring)
     int window;
     float scale_log2;
     const float *cos_t, *sin_t;
@@ -304,6 +309,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         return;
     }
     const int tot = a.len.total_abs[b];
+    if (a.ring && tot < L) {
+        // a ring holds at most T tokens
+        if (threadIdx.x == 0 && split == 0 && kvh == 0)
+            kvc::raise_status(a.status, KVC_DEV_CAPACITY);
+        return;
+    }
     if (a.cos_t && (int64_t)tot > a.rope_max_pos) {
         if (threadIdx.x == 0 && split == 0 && kvh == 0)
             kvc::raise_status(a.status, KVC_DEV_ROPE_RANGE);
@@ -314,9 +325,24 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int nsplit = (int)((vis + a.split_rows - 1) / a.split_rows);
     if (split >= nsplit)
         return;
-    const int r0 = vis0 + (int)(split * a.split_rows);
-    const int r1 = min((int64_t)L, (int64_t)r0 + a.split_rows);
-    const int ntiles = (r1 - r0 + kTile - 1) / kTile;
+    // this split's visible rows [j0, j0 + cnt) in position order, as two runs
+    // of slots: [q0, q0 + cnt_a) and [0, cnt - cnt_a)
+    const int C = (int)a.capacity;
+    const int j0 = (int)(split * a.split_rows);
+    const int cnt = (int)min((int64_t)vis - j0, a.split_rows);
+    const int first = a.ring ? (int)(((int64_t)tot - vis) % C) : vis0;
+    int q0 = first + j0;
+    if (q0 >= C)
+        q0 -= C;
+    const int cnt_a = min(cnt, C - q0);
+    const int nt_a = (cnt_a + kTile - 1) / kTile;
+    const int ntiles = nt_a + (cnt - cnt_a + kTile - 1) / kTile;
+    // first slot and number of valid rows of tile t
+    auto tile_start = [&](int t) { return t < nt_a ? q0 + t * kTile : (t - nt_a) * kTile; };
+    auto tile_rows = [&](int t) {
+        return t < nt_a ? min(kTile, cnt_a - t * kTile)
+                        : min(kTile, cnt - cnt_a - (t - nt_a) * kTile);
+    };
     const int64_t row_base = ((int64_t)b * a.kv_heads + kvh) * a.capacity;
 
     if (threadIdx.x == 0) {
@@ -345,7 +371,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 uint8_t *kb = stages + s * STAGE_BYTES;
                 uint8_t *vb = kb + KT_BYTES;
                 kvc::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-                const int32_t y = (int32_t)(row_base + r0 + t * kTile);
+                const int32_t y = (int32_t)(row_base + tile_start(t));
 #pragma unroll
                 for (int bx = 0; bx < BOXES; ++bx) {
                     kvc::tma_load_2d(kb + bx * 8192, &tmap_k, bx * 64, y, &full[s]);
@@ -390,8 +416,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
         const uint32_t kb = kvc::smem_u32(stages + s * STAGE_BYTES);
         const uint32_t vb = kb + KT_BYTES;
-        const int tile_r0 = r0 + t * kTile;
-        const int my_valid = min(16, max(0, r1 - tile_r0 - 16 * warp));
+        const int my_valid = min(16, max(0, tile_rows(t) - 16 * warp));
         if (my_valid > 0) {
             if (my_valid < 16) {
                 // rows past the split end: zero V so that 0 * garbage stays 0
@@ -455,6 +480,8 @@ decode_combine_kernel(const DecodeArgs a, int D)
     if (L <= 0 || (int64_t)L > a.capacity)
         return;
     const int tot = a.len.total_abs[b];
+    if (a.ring && tot < L)
+        return;
     if (a.cos_t && (int64_t)tot > a.rope_max_pos)
         return;
     const int vis0 = (a.window > 0 && L > a.window) ? L - a.window : 0;
@@ -491,7 +518,10 @@ decode_combine_kernel(const DecodeArgs a, int D)
 // cache row r + E) while the threads rotate the query and the new row.  When
 // rows were evicted the window is then written back E rows lower (all reads
 // have completed, so the in-place move needs no scratch); otherwise only the
-// rows the window can see are loaded and only the new row is stored.  The
+// rows the window can see are loaded and only the new row is stored.  A ring
+// of C slots ("Stateful decode & KV cache", "Sliding-window ring buffer")
+// never moves: window row r is read from slot (T - L + r) mod C and the new
+// row is stored at slot (T - 1) mod C.  The
 // attention runs from shared memory, so the slice is read once, in one launch.
 // --------------------------------------------------------------------------
 struct WindowStepArgs {
@@ -503,7 +533,7 @@ struct WindowStepArgs {
     kvc_lengths len;  // all NULL: not written
     int q_heads, kv_heads, group;
     int64_t capacity;
-    int policy;  // KVC_WINDOWED or KVC_DRIFTING
+    int policy;  // KVC_WINDOWED, KVC_DRIFTING or KVC_RING
     int window;
     float scale_log2;
     const float *cos_t, *sin_t;
@@ -567,10 +597,14 @@ window_step_kernel(const WindowStepArgs a)
     T *vc = static_cast<T *>(a.v_cache) + slice * C * D;
     const int ntiles = (L + kTile - 1) / kTile;
 
-    // 1. the old rows, straight from cache row r + E into the swizzled tiles:
-    //    all of them when they move, else only those the window sees; rows
-    //    not loaded are zeroed (a masked row must still be finite for P.V)
-    const int r_load0 = E > 0 ? 0 : vis0;
+    // 1. the old rows, straight from cache row r + E (ring: slot
+    //    (T - L + r) mod C) into the swizzled tiles: all of them when they
+    //    move, else only those the window sees; rows not loaded are zeroed
+    //    (a masked row must still be finite for P.V)
+    const bool ring = a.policy == KVC_RING;
+    const bool moves = !ring && E > 0;
+    const int ring0 = ring ? (int)((T_ - L) % C) : 0;  // slot of window row 0
+    const int r_load0 = moves ? 0 : vis0;
     const int nchunks = ntiles * kTile * CPR;
     for (int idx = threadIdx.x; idx < 2 * nchunks; idx += 128) {
         const bool is_v = idx >= nchunks;
@@ -579,7 +613,12 @@ window_step_kernel(const WindowStepArgs a)
         uint8_t *dst = tiles + (size_t)(r / kTile) * 2 * KT_BYTES + (is_v ? KT_BYTES : 0) +
                        (c >> 3) * 8192 + kvc::sw128(r % kTile, c & 7);
         if (r >= r_load0 && r < L - 1) {
-            const T *src = (is_v ? vc : kc) + (int64_t)(r + E) * D + c * 8;
+            int sr = r + E;
+            if (ring) {
+                sr = ring0 + r;
+                sr -= sr >= C ? (int)C : 0;
+            }
+            const T *src = (is_v ? vc : kc) + (int64_t)sr * D + c * 8;
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(kvc::smem_u32(dst)),
                          "l"(src)
                          : "memory");
@@ -638,18 +677,21 @@ window_step_kernel(const WindowStepArgs a)
     __syncthreads();
 
     // 3. write the window back: every row E lower when rows were evicted,
-    //    otherwise only the new row (at Lp).  All reads of the old rows are
-    //    complete, so the in-place move needs no scratch.
+    //    otherwise only the new row (at Lp, or a ring's slot (T - 1) mod C).
+    //    All reads of the old rows are complete, so the in-place move needs
+    //    no scratch.
     {
-        const int r_first = E > 0 ? 0 : L - 1;
+        const int r_first = moves ? 0 : L - 1;
         const int n = (L - r_first) * CPR;
+        const int new_dst = ring ? (int)((T_ - 1) % C) : L - 1;
         for (int idx = threadIdx.x; idx < 2 * n; idx += 128) {
             const bool is_v = idx >= n;
             const int w = is_v ? idx - n : idx;
             const int r = r_first + w / CPR, c = w % CPR;
             const uint8_t *src = tiles + (size_t)(r / kTile) * 2 * KT_BYTES + (is_v ? KT_BYTES : 0) +
                                  (c >> 3) * 8192 + kvc::sw128(r % kTile, c & 7);
-            *reinterpret_cast<uint4 *>((is_v ? vc : kc) + (int64_t)r * D + c * 8) =
+            const int dr = r == L - 1 ? new_dst : r;
+            *reinterpret_cast<uint4 *>((is_v ? vc : kc) + (int64_t)dr * D + c * 8) =
                 *reinterpret_cast<const uint4 *>(src);
         }
     }
@@ -691,7 +733,9 @@ window_step_kernel(const WindowStepArgs a)
 namespace kvc_f32 {
 
 // n_rows_mode 0: rows [0, cache_total) (decode); 1: rows [0, cache_past + S)
-// (multi-token chunk over staged or contiguous rows)
+// (multi-token chunk over staged or contiguous rows); 2: the newest
+// cache_total positions of a ring of rows_per_head slots (decode), position
+// p in slot p mod rows_per_head
 __global__ void __launch_bounds__(128)
 attn_f32_kernel(float *__restrict__ out, const float *__restrict__ q,
                 const float *__restrict__ k_rows, const float *__restrict__ v_rows,
@@ -717,8 +761,8 @@ attn_f32_kernel(float *__restrict__ out, const float *__restrict__ q,
             kvc::raise_status(status, KVC_DEV_ROPE_RANGE);
         return;
     }
-    const int64_t n = n_rows_mode == 0 ? L : (int64_t)len.cache_past[b] + S;
-    if (n > rows_per_head || n < S) {
+    const int64_t n = n_rows_mode != 1 ? L : (int64_t)len.cache_past[b] + S;
+    if (n > rows_per_head || n < S || (n_rows_mode == 2 && n > T)) {
         if (lane == 0 && h == 0 && i == 0)
             kvc::raise_status(status, KVC_DEV_CAPACITY);
         return;
@@ -742,13 +786,17 @@ attn_f32_kernel(float *__restrict__ out, const float *__restrict__ q,
     if (hi_r > n - 1)
         hi_r = n - 1;
     const int kvh = h / (q_heads / kv_heads);
+    // logical row r (position first_pos + r) lives in row slot(r)
+    const bool ring = n_rows_mode == 2;
+    auto slot = [&](int64_t r) { return ring ? (first_pos + r) % rows_per_head : r; };
     const float *kb = k_rows + ((int64_t)b * kv_heads + kvh) * rows_per_head * D;
     const float *vb = v_rows + ((int64_t)b * kv_heads + kvh) * rows_per_head * D;
     float m = -INFINITY;
     for (int64_t r = lo_r + lane; r <= hi_r; r += 32) {
         float dot = 0.f;
+        const float *kr = kb + slot(r) * D;
         for (int d = 0; d < D; ++d)
-            dot += qv[d] * kb[r * D + d];
+            dot += qv[d] * kr[d];
         m = fmaxf(m, dot * scale);
     }
     for (int off = 16; off > 0; off >>= 1)
@@ -760,15 +808,16 @@ attn_f32_kernel(float *__restrict__ out, const float *__restrict__ q,
         float p = 0.f;
         if (r <= hi_r) {
             float dot = 0.f;
+            const float *kr = kb + slot(r) * D;
             for (int d = 0; d < D; ++d)
-                dot += qv[d] * kb[r * D + d];
+                dot += qv[d] * kr[d];
             p = expf(dot * scale - m);
         }
         l += p;
         const int cnt = (int)min((int64_t)32, hi_r - c0 + 1);
         for (int j = 0; j < cnt; ++j) {
             const float pj = __shfl_sync(0xffffffffu, p, j);
-            const float *vr = vb + (c0 + j) * D;
+            const float *vr = vb + slot(c0 + j) * D;
 #pragma unroll
             for (int u = 0; u < 8; ++u)
                 if (lane + 32 * u < D)
@@ -810,7 +859,7 @@ kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const 
                            const kvc_lengths &len, int batch, int q_heads, int kv_heads,
                            int64_t C, int window, float scale, const float *cos_t,
                            const float *sin_t, int64_t rope_max_pos, void *workspace,
-                           int32_t *status, cudaStream_t stream)
+                           int ring, int32_t *status, cudaStream_t stream)
 {
     constexpr int NS = decode_stages(D);
     const CUtensorMapDataType tt = std::is_same<T, __half>::value
@@ -831,6 +880,7 @@ kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const 
     a.kv_heads = kv_heads;
     a.group = q_heads / kv_heads;
     a.capacity = C;
+    a.ring = ring;
     a.window = window;
     a.scale_log2 = scale * kLog2e;
     a.cos_t = cos_t;
@@ -862,14 +912,14 @@ template <typename T>
 kvc_status dispatch_decode16(int D, void *out, const void *q, const void *k, const void *v,
                              const kvc_lengths &len, int B, int Hq, int Hkv, int64_t C, int W,
                              float scale, const float *cs, const float *sn, int64_t rmax,
-                             void *ws, int32_t *st, cudaStream_t stream)
+                             void *ws, int ring, int32_t *st, cudaStream_t stream)
 {
     if (D == 64)
         return launch_decode16<T, 64>(out, q, k, v, len, B, Hq, Hkv, C, W, scale, cs, sn, rmax,
-                                      ws, st, stream);
+                                      ws, ring, st, stream);
     if (D == 128)
         return launch_decode16<T, 128>(out, q, k, v, len, B, Hq, Hkv, C, W, scale, cs, sn, rmax,
-                                       ws, st, stream);
+                                       ws, ring, st, stream);
     return KVC_ERR_UNSUPPORTED;
 }
 
@@ -889,12 +939,14 @@ KVC_API size_t kvc_gqa_decode_workspace_size(int batch, int q_heads, int kv_head
     return (size_t)(np * (head_dim + 2) * sizeof(float));
 }
 
-KVC_API kvc_status kvc_gqa_decode(void *out, const void *q, const void *k_cache,
-                                  const void *v_cache, kvc_lengths len, int batch, int q_heads,
-                                  int kv_heads, int64_t capacity, int head_dim, int dtype,
-                                  int local_window_size, float scale, const float *rope_cos,
-                                  const float *rope_sin, int64_t rope_max_pos, void *workspace,
-                                  size_t workspace_bytes, int32_t *dev_status, void *stream_)
+namespace {
+
+kvc_status decode_entry(void *out, const void *q, const void *k_cache, const void *v_cache,
+                        kvc_lengths len, int batch, int q_heads, int kv_heads, int64_t capacity,
+                        int head_dim, int dtype, int local_window_size, float scale,
+                        const float *rope_cos, const float *rope_sin, int64_t rope_max_pos,
+                        void *workspace, size_t workspace_bytes, int ring, int32_t *dev_status,
+                        void *stream_)
 {
     const int eb = kvc_host::elem_bytes_of(dtype);
     if (eb == 0)
@@ -930,15 +982,42 @@ KVC_API kvc_status kvc_gqa_decode(void *out, const void *q, const void *k_cache,
     if (dtype == KVC_F32)
         return kvc_f32::launch(out, q, k_cache, v_cache, capacity, len, batch, q_heads, kv_heads,
                                1, head_dim, local_window_size, scale, rope_cos, rope_sin,
-                               rope_max_pos, 0, dev_status, stream);
+                               rope_max_pos, ring ? 2 : 0, dev_status, stream);
     if (dtype == KVC_BF16)
         return dispatch_decode16<__nv_bfloat16>(head_dim, out, q, k_cache, v_cache, len, batch,
                                                 q_heads, kv_heads, capacity, local_window_size,
                                                 scale, rope_cos, rope_sin, rope_max_pos,
-                                                workspace, dev_status, stream);
+                                                workspace, ring, dev_status, stream);
     return dispatch_decode16<__half>(head_dim, out, q, k_cache, v_cache, len, batch, q_heads,
                                      kv_heads, capacity, local_window_size, scale, rope_cos,
-                                     rope_sin, rope_max_pos, workspace, dev_status, stream);
+                                     rope_sin, rope_max_pos, workspace, ring, dev_status, stream);
+}
+
+} // namespace
+
+KVC_API kvc_status kvc_gqa_decode(void *out, const void *q, const void *k_cache,
+                                  const void *v_cache, kvc_lengths len, int batch, int q_heads,
+                                  int kv_heads, int64_t capacity, int head_dim, int dtype,
+                                  int local_window_size, float scale, const float *rope_cos,
+                                  const float *rope_sin, int64_t rope_max_pos, void *workspace,
+                                  size_t workspace_bytes, int32_t *dev_status, void *stream)
+{
+    return decode_entry(out, q, k_cache, v_cache, len, batch, q_heads, kv_heads, capacity,
+                        head_dim, dtype, local_window_size, scale, rope_cos, rope_sin,
+                        rope_max_pos, workspace, workspace_bytes, 0, dev_status, stream);
+}
+
+KVC_API kvc_status kvc_gqa_decode_ring(void *out, const void *q, const void *k_cache,
+                                       const void *v_cache, kvc_lengths len, int batch,
+                                       int q_heads, int kv_heads, int64_t capacity, int head_dim,
+                                       int dtype, int local_window_size, float scale,
+                                       const float *rope_cos, const float *rope_sin,
+                                       int64_t rope_max_pos, void *workspace,
+                                       size_t workspace_bytes, int32_t *dev_status, void *stream)
+{
+    return decode_entry(out, q, k_cache, v_cache, len, batch, q_heads, kv_heads, capacity,
+                        head_dim, dtype, local_window_size, scale, rope_cos, rope_sin,
+                        rope_max_pos, workspace, workspace_bytes, 1, dev_status, stream);
 }
 
 namespace {
@@ -972,7 +1051,7 @@ KVC_API kvc_status kvc_window_decode_step(void *out, const void *q, void *k_cach
 {
     if (kvc_host::elem_bytes_of(dtype) == 0)
         return KVC_ERR_DTYPE;
-    if (windowed != KVC_WINDOWED && windowed != KVC_DRIFTING)
+    if (windowed != KVC_WINDOWED && windowed != KVC_DRIFTING && windowed != KVC_RING)
         return KVC_ERR_UNSUPPORTED;
     if (batch < 0 || q_heads < 1 || kv_heads < 1 || q_heads % kv_heads != 0)
         return KVC_ERR_SHAPE;

@@ -25,7 +25,7 @@ STATUS_NAMES = {
     8: "KVC_ERR_WORKSPACE", 9: "KVC_ERR_CUDA",
 }
 # cache policies (the `windowed` argument)
-KVC_CONTIGUOUS, KVC_WINDOWED, KVC_DRIFTING = 0, 1, 2
+KVC_CONTIGUOUS, KVC_WINDOWED, KVC_DRIFTING, KVC_RING = 0, 1, 2, 3
 KVC_DEV_INDEX_OOB = 1
 KVC_DEV_SEQLEN_RANGE = 2
 KVC_DEV_CAPACITY = 4
@@ -33,7 +33,8 @@ KVC_DEV_ROPE_RANGE = 8
 KVC_DEV_TIMEOUT = 16
 
 EXPORTS = ("kvc_tensor_scatter", "kvc_seq_lengths", "kvc_window_append", "kvc_gqa_decode",
-           "kvc_gqa_decode_workspace_size", "kvc_gqa_decode_noalloc", "kvc_window_decode_step",
+           "kvc_gqa_decode_workspace_size", "kvc_gqa_decode_noalloc", "kvc_gqa_decode_ring",
+           "kvc_window_decode_step",
            "kvc_gqa_prefill_chunk", "kvc_status_string", "kvc_abi_version")
 KVC_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -91,6 +92,8 @@ def library() -> ctypes.CDLL:
             "kvc_seq_lengths": [P, I, I, I64, I, I, L, P, P],
             "kvc_window_append": [P, P, P, P, P, P, L, I, I, I, I64, I, I, I, I, P, P, I64, P, P],
             "kvc_gqa_decode": [P, P, P, P, L, I, I, I, I64, I, I, I, F, P, P, I64, P, SZ, P, P],
+            "kvc_gqa_decode_ring": [P, P, P, P, L, I, I, I, I64, I, I, I, F, P, P, I64, P, SZ, P,
+                                    P],
             "kvc_gqa_decode_workspace_size": [I, I, I, I64, I, I],
             "kvc_gqa_decode_noalloc": [P, P, P, P, L, I, I, I, I64, I, I, I, F, P, P, I64, P, P],
             "kvc_window_decode_step": [P, P, P, P, P, P, P, L, I, I, I, I64, I, I, I, I, F, P, P,
@@ -190,6 +193,20 @@ def kvc_gqa_decode(out, q, k_cache, v_cache, lengths, local_window_size=0, scale
     return out
 
 
+def kvc_gqa_decode_ring(out, q, k_cache, v_cache, lengths, local_window_size=0, scale=0.0,
+                        rope=None, workspace=None, status=None, stream=None):
+    """kvc_gqa_decode over a ring of C slots (include/kvc.h)."""
+    B, Hq, _, D = q.shape
+    _, Hkv, C, _ = k_cache.shape
+    ws = decode_workspace(q, k_cache) if workspace is None else workspace
+    cs, sn, rmax = _rope(rope)
+    _check("kvc_gqa_decode_ring", library().kvc_gqa_decode_ring(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), lengths.c(), B, Hq, Hkv, C, D,
+        _dtype_code(q), local_window_size, scale, cs, sn, rmax, _ptr(ws), ws.numel(),
+        _ptr(status), _stream(stream)))
+    return out
+
+
 def kvc_gqa_decode_noalloc(out, q, k_cache, v_cache, lengths, local_window_size=0, scale=0.0,
                            rope=None, status=None, stream=None):
     """kvc_gqa_decode with the library's own scratch (see include/kvc.h)."""
@@ -206,7 +223,7 @@ def kvc_window_decode_step(out, q, k_cache, v_cache, new_k, new_v, seqlens_k, lo
                            lengths=None, scale=0.0, rope=None, status=None, stream=None,
                            windowed=None):
     """Fused lengths + windowed one-token append + GQA decode (include/kvc.h).
-    ``windowed``: KVC_WINDOWED (default) or KVC_DRIFTING."""
+    ``windowed``: KVC_WINDOWED (default), KVC_DRIFTING or KVC_RING."""
     windowed = KVC_WINDOWED if windowed is None else int(windowed)
     B, Hq, _, D = q.shape
     _, Hkv, C, _ = k_cache.shape

@@ -125,6 +125,11 @@ WINDOW_DECODE_DRIFT = DecodeWorkload("window-decode-drift-bf16-b64-h64kv8-d64-c1
                                      batch=64, q_heads=64, kv_heads=8, head_dim=64,
                                      capacity=144, window=128, windowed=True, total_lo=1,
                                      total_hi=32768, steps=256, extra={"policy": 2})
+# the same window held in a ring of C = W slots (token p in slot p mod C)
+WINDOW_DECODE_RING = DecodeWorkload("window-decode-ring-bf16-b64-h64kv8-d64-c128-w128",
+                                    batch=64, q_heads=64, kv_heads=8, head_dim=64,
+                                    capacity=128, window=128, windowed=True, total_lo=1,
+                                    total_hi=32768, steps=256, extra={"policy": 3})
 WINDOW_PREFILL = DecodeWorkload("window-prefill-bf16-b8-h16kv8-d256-w4096", batch=8,
                                 q_heads=16, kv_heads=8, head_dim=256, capacity=4096,
                                 window=4096, windowed=True, total_lo=0, total_hi=20000,

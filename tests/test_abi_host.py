@@ -72,7 +72,7 @@ def test_lengths_host_checks(kvc):
     assert f(FAKE, 4, 1, 128, 1, 0, L, None, None) == 7         # W missing
     assert f(None, 4, 1, 128, 1, 128, L, None, None) == 1
     assert f(FAKE, 0, 1, 128, 1, 128, L, None, None) == 0       # empty batch: nothing to do
-    assert f(FAKE, 4, 1, 128, 3, 128, L, None, None) == 5       # unknown policy
+    assert f(FAKE, 4, 1, 128, 4, 128, L, None, None) == 5       # unknown policy
     assert f(FAKE, 4, 1, 128, 2, 129, L, None, None) == 7       # drifting needs W <= C
     assert f(FAKE, 4, 1, 128, 2, 0, L, None, None) == 7
 
@@ -87,7 +87,8 @@ def test_append_host_checks(kvc):
     assert f(*base, 2, 2, 1, 16, 7, 1, 1, 0, None, None, 0, None, None) == 2        # odd D
     assert f(*base, 2, 2, 4, 16, 8, 1, 1, 0, None, None, 0, None, None) == 1        # no stage
     assert f(*base, 2, 2, 1, 16, 8, 1, 1, 1, None, None, 0, None, None) == 5        # copy-back S=1
-    assert f(*base, 2, 2, 1, 16, 8, 1, 3, 0, None, None, 0, None, None) == 5        # policy
+    assert f(*base, 2, 2, 1, 16, 8, 1, 4, 0, None, None, 0, None, None) == 5        # policy
+    assert f(*base, 2, 2, 4, 16, 8, 1, 3, 1, None, None, 0, None, None) == 5        # ring copy-back
     assert f(*base, 2, 2, 1, 0, 8, 1, 1, 0, None, None, 0, None, None) == 6         # C < 1
     assert f(*base, 2, 2, 1, 16, 8, 1, 1, 0, FAKE, None, 16, None, None) == 1       # half a table
     unaligned = [FAKE + 2] + base[1:]
@@ -109,6 +110,18 @@ def test_decode_host_checks(kvc):
     bad = [FAKE + 8] + base[1:]
     assert f(*bad, 2, 8, 2, 64, 128, 1, 0, 0.0, None, None, 0, FAKE, 256, None, None) == 4
     assert lib.kvc_gqa_decode_workspace_size(2, 8, 2, 128, 64, 1) == 256
+
+
+def test_decode_ring_host_checks(kvc):
+    lib = kvc.library()
+    f = lib.kvc_gqa_decode_ring
+    L = _lengths(kvc)
+    base = [FAKE, FAKE * 2, FAKE * 3, FAKE * 4, L]
+    assert f(*base, 2, 6, 4, 64, 128, 1, 0, 0.0, None, None, 0, FAKE, 1 << 20, None, None) == 2
+    assert f(*base, 2, 8, 2, 64, 96, 1, 0, 0.0, None, None, 0, FAKE, 1 << 20, None, None) == 5
+    assert f(*base, 2, 8, 2, 8192, 128, 1, 0, 0.0, None, None, 0, None, 0, None, None) == 8
+    bad = [FAKE + 8] + base[1:]
+    assert f(*bad, 2, 8, 2, 64, 128, 1, 0, 0.0, None, None, 0, FAKE, 256, None, None) == 4
 
 
 def test_prefill_host_checks(kvc):
@@ -138,7 +151,7 @@ def test_window_step_host_checks(kvc):
         assert f(*base, none, 2, 8, 2, 128, 64, 1, pol, 129, 0.0, None, None, 0, None, None) == 7
         assert f(*base, none, 2, 8, 2, 128, 64, 1, pol, 0, 0.0, None, None, 0, None, None) == 7
     assert f(*base, none, 2, 8, 2, 128, 64, 1, 0, 128, 0.0, None, None, 0, None, None) == 5  # contig
-    assert f(*base, none, 2, 8, 2, 128, 64, 1, 3, 128, 0.0, None, None, 0, None, None) == 5  # policy
+    assert f(*base, none, 2, 8, 2, 128, 64, 1, 4, 128, 0.0, None, None, 0, None, None) == 5  # policy
     assert f(*base, none, 2, 8, 2, 128, 64, 0, 1, 128, 0.0, None, None, 0, None, None) == 5  # fp32
     assert f(*base, none, 2, 8, 2, 128, 96, 1, 1, 128, 0.0, None, None, 0, None, None) == 5  # D
     half = kvc.KvcLengths(FAKE, None, None, None, None)
