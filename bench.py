@@ -4,7 +4,9 @@ A step is one pass of the whole path over one batch.  Default workload: the
 contiguous persistent-cache decode (batch 32, 32 query / 8 KV heads,
 head_dim 128, capacity 8192, per-sequence total length uniform in
 [512, 8192] after the append, bf16, RoPE theta 10000); one step = device-side
-lengths + RoPE append of the new K/V row + split-KV GQA decode (+ merge).
+lengths + RoPE append of the new K/V row + split-KV GQA decode + merge, as
+one kvc_decode_step call (two launches; --workload contig-decode-unfused:
+the same as four separate launches).
 The ~570 MB the step reads exceed the 129 MB L2, so no flush is needed.
 
 Other workloads (--workload):
@@ -166,13 +168,18 @@ class Workload:
 
 
 class ContigDecode(Workload):
-    """Contiguous persistent-cache GQA decode, one-token append then attention."""
-    roofline_kernel = "kvc_gqa_decode (split + merge launches)"
-    traffic_key = ("kvc_decode.cu", "decode_split_kernel")
+    """Contiguous persistent-cache GQA decode, one-token append then attention.
+    fused=True runs each step as one kvc_decode_step launch; otherwise as
+    kvc_seq_lengths + kvc_window_append + kvc_gqa_decode (split + merge)."""
     bound = "hbm"
+    fused = True
 
     def __init__(self, dev, seed=0, with_kernels=True, chunk=None):
         import torch
+        self.roofline_kernel = ("kvc_decode_step (fused step + merge)" if self.fused
+                                else "kvc_gqa_decode (split + merge launches)")
+        self.traffic_key = ("kvc_decode.cu",
+                            "decode_split_kernel_fused" if self.fused else "decode_split_kernel")
 
         from persistent_kv_cache_gb300 import synth
         self.torch = torch
@@ -197,26 +204,40 @@ class ContigDecode(Workload):
         self.kernel_bytes = int(self.T.sum()) * Hkv * D * 2 * e + 2 * B * Hq * D * e
         self.append_bytes = 2 * 2 * B * Hkv * D * e
         self.bytes_per_step = self.kernel_bytes + self.append_bytes
+        if self.fused:
+            self.kernel_bytes = self.bytes_per_step
         self.tokens_per_step = B
         if not with_kernels:
             return
         from persistent_kv_cache_gb300 import kvc as K
         self.K = K
         self.out = torch.empty(B, Hq, 1, D, dtype=bf, device=dev)
-        self.ws = K.decode_workspace(self.out, self.kc)
         self.L = K.Lengths(B, dev)
         self.st = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.launches_per_step = 3 + (1 if K.kvc_gqa_decode_workspace_size(
-            B, Hq, Hkv, C, D, K.KVC_BF16) > 256 else 0)
+        merge = 1 if K.kvc_gqa_decode_workspace_size(B, Hq, Hkv, C, D, K.KVC_BF16) > 256 else 0
+        if self.fused:
+            self.ws = K.decode_step_workspace(self.out, self.kc)
+            self.launches_per_step = 1 + merge
+        else:
+            self.ws = K.decode_workspace(self.out, self.kc)
+            self.launches_per_step = 3 + (1 if K.kvc_gqa_decode_workspace_size(
+                B, Hq, Hkv, C, D, K.KVC_BF16) > 256 else 0)
 
     def step(self, i):
         K = self.K
+        if self.fused:
+            K.kvc_decode_step(self.out, self.q, self.kc, self.vc, self.nk, self.nv, self.sk,
+                              lengths=self.L, rope=self.rope, workspace=self.ws, status=self.st)
+            return
         K.kvc_seq_lengths(self.sk, 1, self.w.capacity, 0, out=self.L, status=self.st)
         K.kvc_window_append(self.kc, self.vc, self.nk, self.nv, self.L, 0, rope=self.rope,
                             status=self.st)
         self.kernel(i)
 
     def kernel(self, i):
+        if self.fused:
+            self.step(i)
+            return
         self.K.kvc_gqa_decode(self.out, self.q, self.kc, self.vc, self.L, rope=self.rope,
                               workspace=self.ws, status=self.st)
 
@@ -225,7 +246,7 @@ class ContigDecode(Workload):
         return {"workload": w.name, "batch": w.batch, "q_heads": w.q_heads,
                 "kv_heads": w.kv_heads, "head_dim": w.head_dim, "capacity": w.capacity,
                 "total_len": f"U[{w.total_lo},{w.total_hi}] after the append",
-                "rope_theta": w.theta, "new_tokens": 1,
+                "rope_theta": w.theta, "new_tokens": 1, "fused_step": self.fused,
                 "l2": "inputs larger than L2 (~570 MB of K/V read per step)",
                 "bytes_per_step": self.bytes_per_step}
 
@@ -588,6 +609,10 @@ class WindowDecodeUnfused(WindowDecode):
     fused = False
 
 
+class ContigDecodeUnfused(ContigDecode):
+    fused = False
+
+
 class WindowDecodeDrift(WindowDecode):
     spec = "WINDOW_DECODE_DRIFT"
 
@@ -596,7 +621,8 @@ class WindowDecodeRing(WindowDecode):
     spec = "WINDOW_DECODE_RING"
 
 
-WORKLOADS = {"contig-decode": ContigDecode, "window-decode": WindowDecode,
+WORKLOADS = {"contig-decode": ContigDecode, "contig-decode-unfused": ContigDecodeUnfused,
+             "window-decode": WindowDecode,
              "window-decode-unfused": WindowDecodeUnfused,
              "window-decode-drift": WindowDecodeDrift, "window-decode-ring": WindowDecodeRing,
              "window-prefill": WindowPrefill,

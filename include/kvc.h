@@ -10,7 +10,9 @@
  *                          staging seed / copy-back (windowed, several tokens)
  *     kvc_gqa_decode       one-token GQA attention over the cache
  *     kvc_gqa_decode_ring  the same over a ring of C slots (circular addressing)
- *     kvc_window_decode_step  the three above fused for a windowed cache
+ *     kvc_decode_step      lengths + append + decode in one launch (contiguous
+ *                          cache or ring)
+ *     kvc_window_decode_step  the same for a windowed cache (small windows)
  *     kvc_gqa_prefill_chunk  multi-token GQA attention over staged rows
  *     kvc_tensor_scatter   the ONNX TensorScatter cache update (linear/circular)
  *
@@ -305,6 +307,45 @@ kvc_status kvc_gqa_decode_ring(void *out, const void *q, const void *k_cache, co
                                float scale, const float *rope_cos, const float *rope_sin,
                                int64_t rope_max_pos, void *workspace, size_t workspace_bytes,
                                int32_t *dev_status, void *stream);
+
+/*
+ * kvc_decode_step -- one fused one-token step on a contiguous cache or a
+ * ring: kvc_seq_lengths + kvc_window_append (S = 1) + kvc_gqa_decode (or
+ * kvc_gqa_decode_ring) with the same results, the lengths, the append and
+ * the attention in one launch ("Persistent KV Cache and Decode Performance
+ * Roadmap", Phase 1; "GQA support sliding_window_cache", "Design";
+ * "Stateful decode & KV cache", "Sliding-window ring buffer").  The CTA that
+ * holds the newest position places the new K (rotated at T - 1) and V row
+ * into its tile on chip and stores it to the cache (row T - 1, or slot
+ * (T - 1) mod C).  Rows long enough for several splits are merged by a
+ * second launch, as in kvc_gqa_decode.
+ *
+ * out, q          device [batch, q_heads, 1, head_dim].
+ * k_cache/v_cache device [batch, kv_heads, capacity, head_dim], updated in place.
+ * new_k, new_v    device [batch, kv_heads, 1, head_dim].
+ * seqlens_k       device int32 [batch] (total after this token, minus one).
+ * len             the five length arrays to fill (as kvc_seq_lengths would,
+ *                 same policy, S = 1), or all five NULL.
+ * windowed        KVC_CONTIGUOUS (T > C sets KVC_DEV_CAPACITY) or KVC_RING;
+ *                 else KVC_ERR_UNSUPPORTED.
+ * local_window_size, scale, rope_*: as kvc_gqa_decode.
+ * workspace       device, kvc_decode_step_workspace_size(...) bytes (the same
+ *                 as kvc_gqa_decode_workspace_size), 256-byte aligned.
+ * Supported: KVC_BF16/KVC_F16, head_dim in {64, 128}, q_heads / kv_heads <=
+ * 16 (KVC_ERR_UNSUPPORTED otherwise).
+ * Device errors as kvc_seq_lengths / kvc_window_append / kvc_gqa_decode.
+ */
+kvc_status kvc_decode_step(void *out, const void *q, void *k_cache, void *v_cache,
+                           const void *new_k, const void *new_v, const int32_t *seqlens_k,
+                           kvc_lengths len, int batch, int q_heads, int kv_heads, int64_t capacity,
+                           int head_dim, int dtype, int windowed, int local_window_size,
+                           float scale, const float *rope_cos, const float *rope_sin,
+                           int64_t rope_max_pos, void *workspace, size_t workspace_bytes,
+                           int32_t *dev_status, void *stream);
+
+/* Bytes of workspace kvc_decode_step needs for these sizes (0 on bad sizes). */
+size_t kvc_decode_step_workspace_size(int batch, int q_heads, int kv_heads, int64_t capacity,
+                                      int head_dim, int dtype);
 
 /*
  * kvc_window_decode_step -- one fused one-token step on a windowed cache:

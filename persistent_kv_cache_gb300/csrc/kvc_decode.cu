@@ -22,6 +22,11 @@
 // "Sliding-window ring buffer") they start at slot (T - n) mod C and wrap, so
 // a split's rows are at most two contiguous runs of slots, each streamed as
 // its own sequence of tiles (a tile never crosses the wrap).
+// The fused step (kvc_decode_step) runs the same kernel with the lengths
+// derived inline from seqlens_k, the new K/V row patched into the last tile
+// in shared memory (and stored to the cache) by the split that owns the
+// newest position, and the split merge done by whichever split of a
+// (batch row, kv head) finishes last: one launch per step.
 // fp32 path: attn_f32_kernel, one warp per query row on CUDA cores (also used
 // by the multi-token call for fp32).
 #include <mutex>
@@ -211,9 +216,9 @@ template <typename T, int D> struct GroupAttn {
     }
 
     // finish l across the quad and publish (m, l, o) of heads < g for the
-    // 4-warp merge: cm/cl [4][16], co [4][16][D]
+    // 4-warp merge: cm/cl [4][16], co [4][rows][D] (rows >= g)
     __device__ __forceinline__ void publish(float *cm, float *cl, float *co, int warp, int lane,
-                                            int g)
+                                            int g, int rows)
     {
         l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
         l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
@@ -229,12 +234,12 @@ template <typename T, int D> struct GroupAttn {
 #pragma unroll
         for (int n = 0; n < NB; ++n) {
             if (row < g) {
-                co[(warp * 16 + row) * D + 8 * n + col] = o[n][0];
-                co[(warp * 16 + row) * D + 8 * n + col + 1] = o[n][1];
+                co[(warp * rows + row) * D + 8 * n + col] = o[n][0];
+                co[(warp * rows + row) * D + 8 * n + col + 1] = o[n][1];
             }
             if (row + 8 < g) {
-                co[(warp * 16 + row + 8) * D + 8 * n + col] = o[n][2];
-                co[(warp * 16 + row + 8) * D + 8 * n + col + 1] = o[n][3];
+                co[(warp * rows + row + 8) * D + 8 * n + col] = o[n][2];
+                co[(warp * rows + row + 8) * D + 8 * n + col + 1] = o[n][3];
             }
         }
     }
@@ -243,7 +248,8 @@ template <typename T, int D> struct GroupAttn {
 // merged (unnormalised o, l, reference max) of head h, column d over the
 // four warps' published partials
 __device__ __forceinline__ void merge4(const float *cm, const float *cl, const float *co, int D,
-                                       int h, int d, float &mstar, float &lsum, float &osum)
+                                       int rows, int h, int d, float &mstar, float &lsum,
+                                       float &osum)
 {
     mstar = -INFINITY;
 #pragma unroll
@@ -256,7 +262,7 @@ __device__ __forceinline__ void merge4(const float *cm, const float *cl, const f
     for (int w = 0; w < kConsumers; ++w) {
         const float f = exp2f(cm[w * 16 + h] - ref);
         lsum += cl[w * 16 + h] * f;
-        osum += co[(w * 16 + h) * D + d] * f;
+        osum += co[(w * rows + h) * D + d] * f;
     }
 }
 
@@ -264,7 +270,7 @@ struct DecodeArgs {
     void *out;
     const void *q;
     kvc_lengths len;
-    int q_heads, kv_heads, group;
+    int batch, q_heads, kv_heads, group;
     int64_t capacity;
     int ring;    // slots addressed as a ring of `capacity` (kvc_gqa_decode_ring)
     int window;
@@ -275,9 +281,86 @@ struct DecodeArgs {
     int64_t split_rows;
     int max_splits;
     int32_t *status;
+    // fused step only
+    const int32_t *seqlens_k;
+    const void *new_k, *new_v;
+    void *k_cache, *v_cache;
 };
 
-template <typename T, int D>
+// (L, T) of batch row b: from the lengths arrays, or in the fused step from
+// seqlens_k (kvc_seq_lengths for S = 1 on a contiguous cache or a ring).
+// Returns the row's number of splits; 0 when it has nothing to attend
+// (rejected row, lengths that do not fit this cache, RoPE out of range).
+template <bool FUSED>
+__device__ __forceinline__ int row_splits(const DecodeArgs &a, int b, int &L, int &tot)
+{
+    if constexpr (FUSED) {
+        const int64_t T64 = (int64_t)a.seqlens_k[b] + 1;
+        if (T64 < 1 || T64 > (int64_t)INT32_MAX || (!a.ring && T64 > a.capacity))
+            return 0;
+        tot = (int)T64;
+        L = (int)(a.ring && T64 > a.capacity ? a.capacity : T64);
+    } else {
+        L = a.len.cache_total[b];
+        tot = a.len.total_abs[b];
+        if (L <= 0 || (int64_t)L > a.capacity || (a.ring && tot < L))
+            return 0;
+    }
+    if (a.cos_t && (int64_t)tot > a.rope_max_pos)
+        return 0;
+    const int vis0 = (a.window > 0 && L > a.window) ? L - a.window : 0;
+    return (int)((L - vis0 + a.split_rows - 1) / a.split_rows);
+}
+
+// Errors of batch row b, raised once per row; the fused step also writes
+// the row's lengths (as kvc_seq_lengths would).
+template <bool FUSED>
+__device__ __forceinline__ void row_check(const DecodeArgs &a, int b)
+{
+    if constexpr (FUSED) {
+        const int64_t T64 = (int64_t)a.seqlens_k[b] + 1;
+        const bool write_len = a.len.cache_total != nullptr;
+        uint32_t bad = 0;
+        if (T64 < 1 || T64 > (int64_t)INT32_MAX)
+            bad = KVC_DEV_SEQLEN_RANGE;
+        else if (!a.ring && T64 > a.capacity)
+            bad = KVC_DEV_CAPACITY;
+        if (bad) {
+            kvc::raise_status(a.status, bad);
+            if (write_len)
+                a.len.past_abs[b] = a.len.total_abs[b] = a.len.cache_past[b] =
+                    a.len.cache_total[b] = a.len.evict[b] = -1;
+            return;
+        }
+        int64_t Lp, E, L;
+        kvc::cache_lengths(a.ring ? KVC_RING : KVC_CONTIGUOUS, T64, 1, a.capacity, 1, Lp, E, L);
+        if (write_len) {
+            a.len.past_abs[b] = (int32_t)(T64 - 1);
+            a.len.total_abs[b] = (int32_t)T64;
+            a.len.cache_past[b] = (int32_t)Lp;
+            a.len.cache_total[b] = (int32_t)L;
+            a.len.evict[b] = (int32_t)E;
+        }
+        if (a.cos_t && T64 > a.rope_max_pos)
+            kvc::raise_status(a.status, KVC_DEV_ROPE_RANGE);
+    } else {
+        const int L = a.len.cache_total[b];
+        const int tot = a.len.total_abs[b];
+        if (L <= 0)
+            return;  // rejected when the lengths were derived
+        if ((int64_t)L > a.capacity || (a.ring && tot < L))
+            kvc::raise_status(a.status, KVC_DEV_CAPACITY);  // lengths for another cache
+        else if (a.cos_t && (int64_t)tot > a.rope_max_pos)
+            kvc::raise_status(a.status, KVC_DEV_ROPE_RANGE);
+    }
+}
+
+// One CTA per (split, kv head, batch row) for kvc_gqa_decode,
+// kvc_gqa_decode_ring and the fused kvc_decode_step; the split partials go
+// to decode_combine_kernel.  FUSED: lengths from seqlens_k, and the CTA
+// holding the newest position places the new K/V row in its tile on chip
+// and stores it to the cache.
+template <typename T, int D, bool FUSED>
 __global__ void __launch_bounds__(160)
 decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a)
@@ -299,32 +382,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-    const int L = a.len.cache_total[b];
-    if (L <= 0)
-        return;
-    if ((int64_t)L > a.capacity) {
-        // lengths computed for another capacity: refuse rather than overrun
-        if (threadIdx.x == 0 && split == 0 && kvh == 0)
-            kvc::raise_status(a.status, KVC_DEV_CAPACITY);
-        return;
-    }
-    const int tot = a.len.total_abs[b];
-    if (a.ring && tot < L) {
-        // a ring holds at most T tokens
-        if (threadIdx.x == 0 && split == 0 && kvh == 0)
-            kvc::raise_status(a.status, KVC_DEV_CAPACITY);
-        return;
-    }
-    if (a.cos_t && (int64_t)tot > a.rope_max_pos) {
-        if (threadIdx.x == 0 && split == 0 && kvh == 0)
-            kvc::raise_status(a.status, KVC_DEV_ROPE_RANGE);
-        return;
-    }
-    const int vis0 = (a.window > 0 && L > a.window) ? L - a.window : 0;
-    const int vis = L - vis0;
-    const int nsplit = (int)((vis + a.split_rows - 1) / a.split_rows);
+    if (threadIdx.x == 0 && split == 0 && kvh == 0)
+        row_check<FUSED>(a, b);
+    int L, tot;
+    const int nsplit = row_splits<FUSED>(a, b, L, tot);
     if (split >= nsplit)
         return;
+    const int vis0 = (a.window > 0 && L > a.window) ? L - a.window : 0;
+    const int vis = L - vis0;
     // this split's visible rows [j0, j0 + cnt) in position order, as two runs
     // of slots: [q0, q0 + cnt_a) and [0, cnt - cnt_a)
     const int C = (int)a.capacity;
@@ -416,7 +481,45 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
         const uint32_t kb = kvc::smem_u32(stages + s * STAGE_BYTES);
         const uint32_t vb = kb + KT_BYTES;
-        const int my_valid = min(16, max(0, tile_rows(t) - 16 * warp));
+        const int rows_t = tile_rows(t);
+        const int my_valid = min(16, max(0, rows_t - 16 * warp));
+        bool patched = false;
+        if (FUSED && split == nsplit - 1 && t == ntiles - 1 && my_valid > 0 &&
+            16 * warp + my_valid == rows_t) {
+            // this warp owns the newest row (position tot - 1): place the new
+            // K (rotated there) and V row in the tile and store it to the cache
+            const int rr = rows_t - 1;
+            const int64_t slice = (int64_t)b * a.kv_heads + kvh;
+            const int64_t dst_row = a.ring ? (int64_t)(tot - 1) % a.capacity : (int64_t)tot - 1;
+            const T *nk = static_cast<const T *>(a.new_k) + slice * D;
+            const T *nv = static_cast<const T *>(a.new_v) + slice * D;
+            T *kc = static_cast<T *>(a.k_cache) + (slice * a.capacity + dst_row) * D;
+            T *vc = static_cast<T *>(a.v_cache) + (slice * a.capacity + dst_row) * D;
+            const float *cs = a.cos_t ? a.cos_t + (int64_t)(tot - 1) * (D / 2) : nullptr;
+            const float *sn = a.cos_t ? a.sin_t + (int64_t)(tot - 1) * (D / 2) : nullptr;
+            uint8_t *kgen = stages + s * STAGE_BYTES;
+            uint8_t *vgen = kgen + KT_BYTES;
+            for (int i = lane; i < D / 2; i += 32) {
+                float lo = kvc::Elem<T>::to_f32(nk[i]), hi = kvc::Elem<T>::to_f32(nk[i + D / 2]);
+                if (cs)
+                    kvc::rope_pair(lo, hi, cs[i], sn[i]);
+                const T klo = kvc::Elem<T>::from_f32(lo), khi = kvc::Elem<T>::from_f32(hi);
+                const T vlo = nv[i], vhi = nv[i + D / 2];
+                kc[i] = klo;
+                kc[i + D / 2] = khi;
+                vc[i] = vlo;
+                vc[i + D / 2] = vhi;
+                const int c0 = i, c1 = i + D / 2;
+                const int o0 = (c0 >> 6) * 8192 + kvc::sw128(rr, (c0 & 63) >> 3) + (c0 & 7) * 2;
+                const int o1 = (c1 >> 6) * 8192 + kvc::sw128(rr, (c1 & 63) >> 3) + (c1 & 7) * 2;
+                *reinterpret_cast<T *>(kgen + o0) = klo;
+                *reinterpret_cast<T *>(kgen + o1) = khi;
+                *reinterpret_cast<T *>(vgen + o0) = vlo;
+                *reinterpret_cast<T *>(vgen + o1) = vhi;
+            }
+            patched = true;
+            __syncwarp();
+        }
         if (my_valid > 0) {
             if (my_valid < 16) {
                 // rows past the split end: zero V so that 0 * garbage stays 0
@@ -431,7 +534,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
             }
             ga.tile(kb, vb, warp, lane, 0, my_valid, a.scale_log2);
         }
-        if (my_valid > 0 && my_valid < 16)
+        if ((my_valid > 0 && my_valid < 16) || patched)
             kvc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0)
@@ -448,13 +551,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     float *cm = reinterpret_cast<float *>(stages);        // [4][16]
     float *cl = cm + kConsumers * 16;                      // [4][16]
     float *co = cl + kConsumers * 16;                      // [4][16][D]
-    ga.publish(cm, cl, co, warp, lane, g);
+    ga.publish(cm, cl, co, warp, lane, g, 16);
     consumer_sync();
     const int hq0 = kvh * g;
     for (int idx = threadIdx.x; idx < g * D; idx += 128) {
         const int h = idx / D, d = idx % D;
         float mstar, lsum, osum;
-        merge4(cm, cl, co, D, h, d, mstar, lsum, osum);
+        merge4(cm, cl, co, D, 16, h, d, mstar, lsum, osum);
         const int64_t qrow = (int64_t)b * a.q_heads + hq0 + h;
         if (nsplit == 1) {
             static_cast<T *>(a.out)[qrow * D + d] = kvc::Elem<T>::from_f32(osum / lsum);
@@ -469,41 +572,52 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
 }
 
-// merges the per-split partials of rows that used more than one split
-template <typename T>
+// merges the per-split partials of rows that used more than one split: the
+// splits' m and l are read in parallel into shared memory, the weights
+// 2^(m_j - max m) computed once, and each output column sums its partials
+// with four loads in flight
+template <typename T, bool FUSED>
 __global__ void __launch_bounds__(128)
 decode_combine_kernel(const DecodeArgs a, int D)
 {
-    extern __shared__ float wsh[];  // [max_splits] weights
+    extern __shared__ float wsh[];  // m [max_splits], then l * w [max_splits], w [max_splits]
     const int h = blockIdx.x, b = blockIdx.y;
-    const int L = a.len.cache_total[b];
-    if (L <= 0 || (int64_t)L > a.capacity)
-        return;
-    const int tot = a.len.total_abs[b];
-    if (a.ring && tot < L)
-        return;
-    if (a.cos_t && (int64_t)tot > a.rope_max_pos)
-        return;
-    const int vis0 = (a.window > 0 && L > a.window) ? L - a.window : 0;
-    const int nsplit = (int)((L - vis0 + a.split_rows - 1) / a.split_rows);
+    int L, tot;
+    const int nsplit = row_splits<FUSED>(a, b, L, tot);
     if (nsplit <= 1)
         return;
+    const int MS = a.max_splits;
+    float *sm = wsh, *slw = wsh + MS, *sw = wsh + 2 * MS;
     const int64_t qrow = (int64_t)b * a.q_heads + h;
-    const int64_t p0 = qrow * a.max_splits;
+    const int64_t p0 = qrow * MS;
+    for (int j = threadIdx.x; j < nsplit; j += blockDim.x)
+        sm[j] = a.ws_m[p0 + j];
+    __syncthreads();
     float mstar = -INFINITY;
     for (int j = 0; j < nsplit; ++j)
-        mstar = fmaxf(mstar, a.ws_m[p0 + j]);
-    float lsum = 0.f;
-    for (int j = threadIdx.x; j < nsplit; j += blockDim.x)
-        wsh[j] = exp2f(a.ws_m[p0 + j] - mstar);
+        mstar = fmaxf(mstar, sm[j]);
+    for (int j = threadIdx.x; j < nsplit; j += blockDim.x) {
+        const float w = exp2f(sm[j] - mstar);
+        sw[j] = w;
+        slw[j] = a.ws_l[p0 + j] * w;
+    }
     __syncthreads();
+    float lsum = 0.f;
     for (int j = 0; j < nsplit; ++j)
-        lsum += a.ws_l[p0 + j] * wsh[j];
+        lsum += slw[j];
+    const float inv_l = 1.f / lsum;
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        const float *src = a.ws_o + p0 * D + d;
         float acc = 0.f;
-        for (int j = 0; j < nsplit; ++j)
-            acc += a.ws_o[(p0 + j) * D + d] * wsh[j];
-        static_cast<T *>(a.out)[qrow * D + d] = kvc::Elem<T>::from_f32(acc / lsum);
+        int j = 0;
+        for (; j + 4 <= nsplit; j += 4) {
+            const float v0 = src[(int64_t)j * D], v1 = src[(int64_t)(j + 1) * D];
+            const float v2 = src[(int64_t)(j + 2) * D], v3 = src[(int64_t)(j + 3) * D];
+            acc += v0 * sw[j] + v1 * sw[j + 1] + v2 * sw[j + 2] + v3 * sw[j + 3];
+        }
+        for (; j < nsplit; ++j)
+            acc += src[(int64_t)j * D] * sw[j];
+        static_cast<T *>(a.out)[qrow * D + d] = kvc::Elem<T>::from_f32(acc * inv_l);
     }
 }
 
@@ -714,12 +828,12 @@ window_step_kernel(const WindowStepArgs a)
     float *cm = reinterpret_cast<float *>(smem);
     float *cl = cm + kConsumers * 16;
     float *co = cl + kConsumers * 16;
-    ga.publish(cm, cl, co, warp, lane, g);
+    ga.publish(cm, cl, co, warp, lane, g, 16);
     __syncthreads();
     for (int idx = threadIdx.x; idx < g * D; idx += 128) {
         const int h = idx / D, d = idx % D;
         float mstar, lsum, osum;
-        merge4(cm, cl, co, D, h, d, mstar, lsum, osum);
+        merge4(cm, cl, co, D, 16, h, d, mstar, lsum, osum);
         const int64_t qrow = (int64_t)b * a.q_heads + kvh * g + h;
         static_cast<T *>(a.out)[qrow * D + d] = kvc::Elem<T>::from_f32(osum / lsum);
     }
@@ -854,14 +968,21 @@ kvc_status launch(void *out, const void *q, const void *k_rows, const void *v_ro
 
 namespace {
 
+// inputs of the fused step (kvc_decode_step) on top of the decode's own
+struct StepExtra {
+    const int32_t *seqlens_k;
+    const void *new_k, *new_v;
+    void *k_cache, *v_cache;
+};
+
 template <typename T, int D>
 kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const void *v_cache,
                            const kvc_lengths &len, int batch, int q_heads, int kv_heads,
                            int64_t C, int window, float scale, const float *cos_t,
                            const float *sin_t, int64_t rope_max_pos, void *workspace,
-                           int ring, int32_t *status, cudaStream_t stream)
+                           int ring, int32_t *status, cudaStream_t stream,
+                           const StepExtra *fx = nullptr)
 {
-    constexpr int NS = decode_stages(D);
     const CUtensorMapDataType tt = std::is_same<T, __half>::value
                                        ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -872,10 +993,11 @@ kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const 
     if (!kvc_host::encode_2d_bf16_sw128(&tk, k_cache, rows, D, kTile, tt) ||
         !kvc_host::encode_2d_bf16_sw128(&tv, v_cache, rows, D, kTile, tt))
         return KVC_ERR_CUDA;
-    DecodeArgs a;
+    DecodeArgs a{};
     a.out = out;
     a.q = q;
     a.len = len;
+    a.batch = batch;
     a.q_heads = q_heads;
     a.kv_heads = kv_heads;
     a.group = q_heads / kv_heads;
@@ -893,17 +1015,32 @@ kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const 
     a.ws_m = a.ws_o + np * D;
     a.ws_l = a.ws_m + np;
     a.status = status;
+    const int64_t n_items = (int64_t)a.max_splits * kv_heads * batch;
+    if (n_items > (int64_t)INT32_MAX)
+        return KVC_ERR_SHAPE;
+    if (fx) {
+        a.seqlens_k = fx->seqlens_k;
+        a.new_k = fx->new_k;
+        a.new_v = fx->new_v;
+        a.k_cache = fx->k_cache;
+        a.v_cache = fx->v_cache;
+    }
+    constexpr int NS = decode_stages(D);
     const size_t smem = 1024 + (size_t)NS * 2 * kTile * D * 2 + 16 * (D + 8) * 2 +
                         2 * NS * sizeof(uint64_t) + 16;
-    auto kern = decode_split_kernel<T, D>;
+    auto kern = fx ? decode_split_kernel<T, D, true> : decode_split_kernel<T, D, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return KVC_ERR_CUDA;
-    dim3 grid(a.max_splits, kv_heads, batch);
+    const dim3 grid(a.max_splits, kv_heads, batch);
     kern<<<grid, 160, smem, stream>>>(tk, tv, a);
     if (a.max_splits > 1) {
         dim3 g2(q_heads, batch);
-        decode_combine_kernel<T><<<g2, 128, a.max_splits * sizeof(float), stream>>>(a, D);
+        const size_t cs = 3 * a.max_splits * sizeof(float);
+        if (fx)
+            decode_combine_kernel<T, true><<<g2, 128, cs, stream>>>(a, D);
+        else
+            decode_combine_kernel<T, false><<<g2, 128, cs, stream>>>(a, D);
     }
     return kvc_host::launch_status();
 }
@@ -1018,6 +1155,99 @@ KVC_API kvc_status kvc_gqa_decode_ring(void *out, const void *q, const void *k_c
     return decode_entry(out, q, k_cache, v_cache, len, batch, q_heads, kv_heads, capacity,
                         head_dim, dtype, local_window_size, scale, rope_cos, rope_sin,
                         rope_max_pos, workspace, workspace_bytes, 1, dev_status, stream);
+}
+
+// --------------------------------------------------------------------------
+// kvc_decode_step: lengths + one-token append + split decode of a contiguous
+// cache or a ring in one launch (plus the split merge for long rows)
+// --------------------------------------------------------------------------
+
+// the step's workspace holds the same split partials as the decode's
+KVC_API size_t kvc_decode_step_workspace_size(int batch, int q_heads, int kv_heads,
+                                              int64_t capacity, int head_dim, int dtype)
+{
+    if (dtype == KVC_F32)
+        return 0;
+    return kvc_gqa_decode_workspace_size(batch, q_heads, kv_heads, capacity, head_dim, dtype);
+}
+
+KVC_API kvc_status kvc_decode_step(void *out, const void *q, void *k_cache, void *v_cache,
+                                   const void *new_k, const void *new_v, const int32_t *seqlens_k,
+                                   kvc_lengths len, int batch, int q_heads, int kv_heads,
+                                   int64_t capacity, int head_dim, int dtype, int windowed,
+                                   int local_window_size, float scale, const float *rope_cos,
+                                   const float *rope_sin, int64_t rope_max_pos, void *workspace,
+                                   size_t workspace_bytes, int32_t *dev_status, void *stream)
+{
+    if (kvc_host::elem_bytes_of(dtype) == 0)
+        return KVC_ERR_DTYPE;
+    if (batch < 0 || q_heads < 1 || kv_heads < 1 || q_heads % kv_heads != 0)
+        return KVC_ERR_SHAPE;
+    if (capacity < 1 || capacity > (int64_t)INT32_MAX)
+        return KVC_ERR_CAPACITY;
+    if (windowed != KVC_CONTIGUOUS && windowed != KVC_RING)
+        return KVC_ERR_UNSUPPORTED;
+    if ((rope_cos == nullptr) != (rope_sin == nullptr))
+        return KVC_ERR_NULL;
+    if (rope_cos && rope_max_pos < 1)
+        return KVC_ERR_SHAPE;
+    const int g = q_heads / kv_heads;
+    // the merge keeps 3 x 16 x splits floats next to the 4-warp partials in
+    // the stage buffers: at most 128 splits (capacity 65536)
+    if (dtype == KVC_F32 || (head_dim != 64 && head_dim != 128) || g > 16 ||
+        decode_max_splits(capacity) > 128)
+        return KVC_ERR_UNSUPPORTED;
+    const bool some_len = len.past_abs || len.total_abs || len.cache_past || len.cache_total ||
+                          len.evict;
+    if (some_len && !kvc_host::lengths_ok(len))
+        return KVC_ERR_NULL;
+    if (batch == 0)
+        return KVC_OK;
+    if (!out || !q || !k_cache || !v_cache || !new_k || !new_v || !seqlens_k)
+        return KVC_ERR_NULL;
+    for (const void *p : {(const void *)out, q, (const void *)k_cache, (const void *)v_cache, new_k,
+                          new_v})
+        if (!kvc_host::aligned16(p))
+            return KVC_ERR_ALIGN;
+    const size_t cache_bytes = (size_t)batch * kv_heads * capacity * head_dim * 2;
+    if (kvc_host::overlaps(k_cache, cache_bytes, v_cache, cache_bytes))
+        return KVC_ERR_SHAPE;
+    const size_t need =
+        kvc_decode_step_workspace_size(batch, q_heads, kv_heads, capacity, head_dim, dtype);
+    if (need > 256 && (!workspace || workspace_bytes < need))
+        return KVC_ERR_WORKSPACE;
+    if (need > 256 && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return KVC_ERR_ALIGN;
+    if (scale == 0.f)
+        scale = 1.0f / sqrtf((float)head_dim);
+    StepExtra fx;
+    fx.seqlens_k = seqlens_k;
+    fx.new_k = new_k;
+    fx.new_v = new_v;
+    fx.k_cache = k_cache;
+    fx.v_cache = v_cache;
+    const kvc_lengths l = some_len ? len : kvc_lengths{nullptr, nullptr, nullptr, nullptr, nullptr};
+    const int ring = windowed == KVC_RING;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == KVC_BF16)
+        return head_dim == 64
+                   ? launch_decode16<__nv_bfloat16, 64>(out, q, k_cache, v_cache, l, batch, q_heads,
+                                                        kv_heads, capacity, local_window_size,
+                                                        scale, rope_cos, rope_sin, rope_max_pos,
+                                                        workspace, ring, dev_status, st, &fx)
+                   : launch_decode16<__nv_bfloat16, 128>(
+                         out, q, k_cache, v_cache, l, batch, q_heads, kv_heads, capacity,
+                         local_window_size, scale, rope_cos, rope_sin, rope_max_pos, workspace,
+                         ring, dev_status, st, &fx);
+    return head_dim == 64
+               ? launch_decode16<__half, 64>(out, q, k_cache, v_cache, l, batch, q_heads,
+                                             kv_heads, capacity, local_window_size, scale,
+                                             rope_cos, rope_sin, rope_max_pos, workspace, ring,
+                                             dev_status, st, &fx)
+               : launch_decode16<__half, 128>(out, q, k_cache, v_cache, l, batch, q_heads,
+                                              kv_heads, capacity, local_window_size, scale,
+                                              rope_cos, rope_sin, rope_max_pos, workspace, ring,
+                                              dev_status, st, &fx);
 }
 
 namespace {

@@ -34,7 +34,7 @@ KVC_DEV_TIMEOUT = 16
 
 EXPORTS = ("kvc_tensor_scatter", "kvc_seq_lengths", "kvc_window_append", "kvc_gqa_decode",
            "kvc_gqa_decode_workspace_size", "kvc_gqa_decode_noalloc", "kvc_gqa_decode_ring",
-           "kvc_window_decode_step",
+           "kvc_decode_step", "kvc_decode_step_workspace_size", "kvc_window_decode_step",
            "kvc_gqa_prefill_chunk", "kvc_status_string", "kvc_abi_version")
 KVC_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -95,6 +95,9 @@ def library() -> ctypes.CDLL:
             "kvc_gqa_decode_ring": [P, P, P, P, L, I, I, I, I64, I, I, I, F, P, P, I64, P, SZ, P,
                                     P],
             "kvc_gqa_decode_workspace_size": [I, I, I, I64, I, I],
+            "kvc_decode_step": [P, P, P, P, P, P, P, L, I, I, I, I64, I, I, I, I, F, P, P, I64, P,
+                                SZ, P, P],
+            "kvc_decode_step_workspace_size": [I, I, I, I64, I, I],
             "kvc_gqa_decode_noalloc": [P, P, P, P, L, I, I, I, I64, I, I, I, F, P, P, I64, P, P],
             "kvc_window_decode_step": [P, P, P, P, P, P, P, L, I, I, I, I64, I, I, I, I, F, P, P,
                                        I64, P, P],
@@ -107,6 +110,7 @@ def library() -> ctypes.CDLL:
             fn.argtypes = args
             fn.restype = I
         lib.kvc_gqa_decode_workspace_size.restype = SZ
+        lib.kvc_decode_step_workspace_size.restype = SZ
         lib.kvc_status_string.restype = ctypes.c_char_p
         _lib = lib
     return _lib
@@ -216,6 +220,32 @@ def kvc_gqa_decode_noalloc(out, q, k_cache, v_cache, lengths, local_window_size=
     _check("kvc_gqa_decode_noalloc", library().kvc_gqa_decode_noalloc(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), lengths.c(), B, Hq, Hkv, C, D,
         _dtype_code(q), local_window_size, scale, cs, sn, rmax, _ptr(status), _stream(stream)))
+    return out
+
+
+def decode_step_workspace(q, k_cache):
+    """Workspace for kvc_decode_step (the split partials)."""
+    B, Hq, _, D = q.shape
+    n = library().kvc_decode_step_workspace_size(B, Hq, k_cache.shape[1], k_cache.shape[2], D,
+                                                 _dtype_code(q))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+
+
+def kvc_decode_step(out, q, k_cache, v_cache, new_k, new_v, seqlens_k, local_window_size=0,
+                    lengths=None, scale=0.0, rope=None, workspace=None, status=None, stream=None,
+                    windowed=None):
+    """Fused lengths + one-token append + split decode on a contiguous cache
+    (default) or a ring (windowed=KVC_RING); include/kvc.h."""
+    windowed = KVC_CONTIGUOUS if windowed is None else int(windowed)
+    B, Hq, _, D = q.shape
+    _, Hkv, C, _ = k_cache.shape
+    ws = decode_step_workspace(q, k_cache) if workspace is None else workspace
+    cs, sn, rmax = _rope(rope)
+    lc = lengths.c() if lengths is not None else KvcLengths(None, None, None, None, None)
+    _check("kvc_decode_step", library().kvc_decode_step(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(new_k), _ptr(new_v),
+        _ptr(seqlens_k), lc, B, Hq, Hkv, C, D, _dtype_code(q), windowed, local_window_size,
+        scale, cs, sn, rmax, _ptr(ws), ws.numel(), _ptr(status), _stream(stream)))
     return out
 
 

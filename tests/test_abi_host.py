@@ -124,6 +124,28 @@ def test_decode_ring_host_checks(kvc):
     assert f(*bad, 2, 8, 2, 64, 128, 1, 0, 0.0, None, None, 0, FAKE, 256, None, None) == 4
 
 
+def test_decode_step_host_checks(kvc):
+    lib = kvc.library()
+    f = lib.kvc_decode_step
+    none = kvc.KvcLengths(None, None, None, None, None)
+    base = [FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, FAKE * 7]
+    # policy: contiguous or ring only
+    assert f(*base, none, 2, 8, 2, 128, 64, 1, 1, 0, 0.0, None, None, 0, FAKE, 1 << 20, None,
+             None) == 5
+    assert f(*base, none, 2, 8, 2, 128, 64, 0, 0, 0, 0.0, None, None, 0, FAKE, 1 << 20, None,
+             None) == 5                                                      # fp32
+    need = lib.kvc_decode_step_workspace_size(2, 8, 2, 8192, 128, 1)
+    assert need == lib.kvc_gqa_decode_workspace_size(2, 8, 2, 8192, 128, 1)
+    far = [FAKE, FAKE * 2, 1 << 32, 2 << 32, FAKE * 5, FAKE * 6, FAKE * 7]  # caches apart
+    assert f(*far, none, 2, 8, 2, 8192, 128, 1, 0, 0, 0.0, None, None, 0, FAKE, need - 4,
+             None, None) == 8
+    half = kvc.KvcLengths(FAKE, None, None, None, None)
+    assert f(*base, half, 2, 8, 2, 128, 64, 1, 3, 0, 0.0, None, None, 0, FAKE, 256, None,
+             None) == 1
+    assert f(*base, none, 0, 8, 2, 128, 64, 1, 3, 0, 0.0, None, None, 0, None, 0, None,
+             None) == 0
+
+
 def test_prefill_host_checks(kvc):
     lib = kvc.library()
     f = lib.kvc_gqa_prefill_chunk
