@@ -23,7 +23,11 @@ Other workloads (--workload):
                   --chunk S in {64, 512, 2048}; one step = lengths + staging
                   seed/append + tcgen05 chunk attention + copy-back
   scatter         TensorScatter circular, (16, 8, 4096, 128) bf16, in place,
-                  --chunk S in {1, 16, 64}; one step = one scatter call
+                  --chunk S in {1, 16, 64}; one step = one scatter call (the
+                  line also reports the per-launch floor of a graph node)
+  scatter-functional  the same into a separate present cache (the whole
+                  128 MiB cache copied, HBM-bound)
+  window-decode-hot   window-decode on one cache (16.8 MB, L2-resident)
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--workload ...] [--chunk S] [--profile]
@@ -396,7 +400,8 @@ class WindowDecode(Workload):
                 "window": w.window, "start_total": f"U[{w.total_lo},{w.total_hi}]",
                 "replica_caches": self.replicas, "new_tokens": 1, "fused_step": self.fused,
                 "layout": {1: "compact every step", 2: "drifting", 3: "ring"}[self.policy],
-                "l2": "16 replica caches cycled (268 MB > L2)",
+                "l2": ("16 replica caches cycled (268 MB > L2)" if self.replicas > 1
+                       else "one cache, L2-resident (hot)"),
                 "bytes_per_step": self.bytes_per_step}
 
     def oracle_sample(self, rows):
@@ -542,22 +547,27 @@ class WindowPrefill(Workload):
 
 
 class Scatter(Workload):
-    """TensorScatter circular, in place, on one (16, 8, 4096, 128) bf16 cache."""
-    roofline_kernel = "kvc_tensor_scatter (in place)"
-    traffic_key = ("kvc_scatter.cu", "scatter_rows_kernel")
+    """TensorScatter circular on one (16, 8, 4096, 128) bf16 cache: in place,
+    or (functional) into a separate present cache."""
     bound = "hbm"
+    in_place = True
 
     def __init__(self, dev, seed=0, with_kernels=True, chunk=64, max_steps=4096):
         import torch
 
         from persistent_kv_cache_gb300 import synth
         self.torch = torch
+        self.roofline_kernel = ("kvc_tensor_scatter (in place)" if self.in_place
+                                else "kvc_tensor_scatter (functional: cache copy + scatter)")
+        self.traffic_key = ("kvc_scatter.cu",
+                            "scatter_rows_kernel" if self.in_place else "scatter_functional")
         w = self.w = synth.SCATTER
         S = self.S = int(chunk or 64)
         shape = (w.batch, w.heads, w.max_seq, w.head_dim)
         g = torch.Generator(device=dev)
         g.manual_seed(seed)
         self.cache = torch.randn(*shape, generator=g, device=dev, dtype=torch.bfloat16)
+        self.present = self.cache if self.in_place else torch.empty_like(self.cache)
         self.upd_host = synth.normal((w.batch, w.heads, S, w.head_dim), seed, 2)
         self.n_wi = max_steps + 64
         self.wi_all = synth.randint(0, w.max_seq, (self.n_wi, w.batch), seed, 3).to(dev)
@@ -566,28 +576,57 @@ class Scatter(Workload):
         self.device_inputs = [t.to(dev) for t in self.host_inputs]
         self.upd, self.wi = self.device_inputs
         self.kernel_bytes = 2 * w.batch * w.heads * S * w.head_dim * self.e + 8 * w.batch
+        if not self.in_place:
+            # every present row written once, from past or from the update
+            self.kernel_bytes = 2 * self.cache.numel() * self.e + 8 * w.batch
         self.bytes_per_step = self.kernel_bytes
         self.tokens_per_step = w.batch * S
         if not with_kernels:
             return
         from persistent_kv_cache_gb300 import kvc as K
         self.K = K
-        self.out = self.cache[:1, :1, :S]  # the e2e result read back: one slice
+        self.out = self.present[:1, :1, :S]  # the e2e result read back: one slice
         self.st = torch.zeros(1, dtype=torch.int32, device=dev)
         self.launches_per_step = 1
 
     def step(self, i):
-        self.K.kvc_tensor_scatter(self.cache, self.cache, self.upd, self.wi_all[i % self.n_wi],
+        self.K.kvc_tensor_scatter(self.present, self.cache, self.upd, self.wi_all[i % self.n_wi],
                                   mode=self.K.KVC_CIRCULAR, status=self.st)
 
     def kernel(self, i):
         self.step(i)
 
+    def extra_measure(self):
+        """Per-launch floor of one graph node: the same call on a (1, 1, 16, 8)
+        float32 cache with one update row, 256 nodes replayed as one graph."""
+        if not self.in_place:
+            return {}
+        torch, K = self.torch, self.K
+        dev = self.cache.device
+        tiny = torch.zeros(1, 1, 16, 8, device=dev)
+        upd = torch.ones(1, 1, 1, 8, device=dev)
+        wi = torch.zeros(1, dtype=torch.int64, device=dev)
+        n = 256
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(n):
+                K.kvc_tensor_scatter(tiny, tiny, upd, wi, mode=K.KVC_CIRCULAR)
+        graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return {"graph_node_floor_us": e0.elapsed_time(e1) * 1e3 / n}
+
     def config(self):
         w = self.w
-        return {"workload": w.name, "shape": [w.batch, w.heads, w.max_seq, w.head_dim],
-                "axis": -2, "mode": "circular", "update_len": self.S, "in_place": True,
-                "l2": "launch-bound; 128 MiB cache, updates touch 32 KiB x S per step",
+        return {"workload": w.name + ("" if self.in_place else "-functional"),
+                "shape": [w.batch, w.heads, w.max_seq, w.head_dim],
+                "axis": -2, "mode": "circular", "update_len": self.S, "in_place": self.in_place,
+                "l2": ("launch-bound; 128 MiB cache, updates touch 32 KiB x S per step"
+                       if self.in_place else "past and present 128 MiB each (> L2)"),
                 "bytes_per_step": self.bytes_per_step}
 
     def oracle_sample(self, rows):
@@ -596,13 +635,21 @@ class Scatter(Workload):
         cache = synth.bits(self.cache.cpu()).copy()
         upd = synth.bits(self.upd_host)
         wi = self.wi_all[0].cpu().numpy()
+        n = 20 if self.in_place else 2
         t0 = time.perf_counter()
-        for _ in range(20):
-            oracle.tensor_scatter(cache, upd, wi, mode=oracle.CIRCULAR, out=cache)
-        return time.perf_counter() - t0, 20 * self.bytes_per_step
+        for _ in range(n):
+            oracle.tensor_scatter(cache, upd, wi, mode=oracle.CIRCULAR,
+                                  out=cache if self.in_place else None)
+        return time.perf_counter() - t0, n * self.bytes_per_step
 
     def metric(self):
-        return "TensorScatter circular in place: GB/s of update bytes, steps/s", "GB/s"
+        if self.in_place:
+            return "TensorScatter circular in place: GB/s of update bytes, steps/s", "GB/s"
+        return "TensorScatter circular functional: GB/s (whole cache), steps/s", "GB/s"
+
+
+class ScatterFunctional(Scatter):
+    in_place = False
 
 
 class WindowDecodeUnfused(WindowDecode):
@@ -611,6 +658,10 @@ class WindowDecodeUnfused(WindowDecode):
 
 class ContigDecodeUnfused(ContigDecode):
     fused = False
+
+
+class WindowDecodeHot(WindowDecode):
+    replicas = 1
 
 
 class WindowDecodeDrift(WindowDecode):
@@ -625,7 +676,8 @@ WORKLOADS = {"contig-decode": ContigDecode, "contig-decode-unfused": ContigDecod
              "window-decode": WindowDecode,
              "window-decode-unfused": WindowDecodeUnfused,
              "window-decode-drift": WindowDecodeDrift, "window-decode-ring": WindowDecodeRing,
-             "window-prefill": WindowPrefill,
+             "window-decode-hot": WindowDecodeHot, "window-prefill": WindowPrefill,
+             "scatter-functional": ScatterFunctional,
              "scatter": Scatter}
 
 
@@ -657,7 +709,8 @@ def run_ours(args):
     n_steps = args.warmup * 2 + args.steps * 3 + 8
     kw = {"chunk": args.chunk}
     if args.workload in ("window-decode", "window-decode-unfused", "window-decode-drift",
-                         "window-decode-ring", "scatter"):
+                         "window-decode-ring", "window-decode-hot", "scatter",
+                         "scatter-functional"):
         kw["max_steps"] = n_steps
     wl = WORKLOADS[args.workload](dev, seed=rank, **kw)
     peaks, peak_kind = load_peaks()
@@ -710,6 +763,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         e2e_s = time.perf_counter() - t0
         barrier(world)
+        measured = wl.extra_measure() if hasattr(wl, "extra_measure") else {}
     status = int(wl.st.item())
     ms = max_over_ranks(ms, world, dev)
     e2e_s = max_over_ranks(e2e_s, world, dev)
@@ -751,7 +805,7 @@ def run_ours(args):
         "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": wl.config(), **extra,
+        "config": wl.config(), **extra, **measured,
         "steps_per_s": args.steps * world / sec,
         "tokens_per_s": wl.tokens_per_step * args.steps * world / sec,
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": wl.h2d,
