@@ -19,6 +19,11 @@ patterns) and returns numpy arrays; each one cites the page it restates:
 * ``gqa_attention``   -- "Persistent KV Cache and Decode Performance Roadmap",
   "Phase 1" (what decode attention computes, GQA sharing) with the causal and
   local-window mask of the PR.
+* ``paged_rows``, ``paged_append``, ``paged_attention`` -- "Persistent KV
+  Cache and Decode Performance Roadmap", "Phase 2" and the CPU backend's
+  "fixed-size paged blocks and a page-table iterator": logical row r of batch
+  row b lives in page block_table[b][r // P] at slot r % P of a shared page
+  pool; attention over the logical rows is the plain attention above.
 * ``ring_slot_positions``, ``ring_append``, ``ring_attention`` -- "Stateful
   decode & KV cache", "Sliding-window ring buffer": token p lives in slot
   p mod C (TensorScatter circular with write index P, K rotated at write
@@ -265,3 +270,59 @@ def ring_attention(q, k_ring, v_ring, total_abs, window=0, scale=None, cos_cache
         n[b] = nb
     return gqa_attention(q, k, v, n, T.astype(np.int32), window=window, scale=scale,
                          cos_cache=cos_cache, sin_cache=sin_cache)
+
+
+# --------------------------------------------------------------------------
+# paged cache ("Persistent KV Cache and Decode Performance Roadmap", Phase 2:
+# fixed-size pages and a page table consumed directly by attention)
+# --------------------------------------------------------------------------
+
+def paged_rows(pool, block_table, n_rows, page_size):
+    """The first n_rows[b] logical rows of every batch row, gathered from a
+    page pool [n_pages, Hkv, P, D] through block_table [B, max_pages]: row r
+    of batch row b is slot r % P of page block_table[b][r // P].  Returns
+    [B, Hkv, max(n_rows), D] (rows past n_rows[b] are zero)."""
+    pool = np.asarray(pool)
+    bt = np.asarray(block_table)
+    B = bt.shape[0]
+    _, Hkv, P, D = pool.shape
+    assert P == page_size
+    n = np.asarray(n_rows, dtype=np.int64)
+    R = int(n.max()) if B else 0
+    out = np.zeros((B, Hkv, max(R, 1), D), dtype=pool.dtype)
+    for b in range(B):
+        for r in range(int(n[b])):
+            out[b, :, r] = pool[int(bt[b, r // P]), :, r % P]
+    return out
+
+
+def paged_append(k_pool, v_pool, block_table, page_size, new_k, new_v, past_abs,
+                 cos_cache=None, sin_cache=None):
+    """Write S new rows per (b, kv head) in place: row i of batch row b
+    (absolute position P_b + i) goes to slot (P_b + i) % P of page
+    block_table[b][(P_b + i) // P]; K is rotated at its position first when
+    the cos/sin tables are given."""
+    B, Hkv, S, D = new_k.shape
+    P = page_size
+    nk = np.ascontiguousarray(new_k)
+    Pb = np.asarray(past_abs, dtype=np.int64)
+    if cos_cache is not None:
+        pos = np.broadcast_to(Pb[:, None, None] + np.arange(S)[None, None, :], (B, Hkv, S))
+        nk = rope_rows(nk, np.ascontiguousarray(pos).reshape(-1), cos_cache, sin_cache)
+    for b in range(B):
+        for i in range(S):
+            r = int(Pb[b]) + i
+            page = int(block_table[b][r // P])
+            k_pool[page, :, r % P] = nk[b, :, i]
+            v_pool[page, :, r % P] = new_v[b, :, i]
+
+
+def paged_attention(q, k_pool, v_pool, block_table, page_size, n_rows, total_abs, window=0,
+                    scale=None, cos_cache=None, sin_cache=None):
+    """Attention of q [B, Hq, S, D] over the n_rows[b] logical rows of a paged
+    cache (row r at absolute position total_abs[b] - n_rows[b] + r).  Returns
+    (out, flags) like gqa_attention."""
+    k = paged_rows(k_pool, block_table, n_rows, page_size)
+    v = paged_rows(v_pool, block_table, n_rows, page_size)
+    return gqa_attention(q, k, v, np.asarray(n_rows, np.int32), np.asarray(total_abs, np.int32),
+                         window=window, scale=scale, cos_cache=cos_cache, sin_cache=sin_cache)
