@@ -28,6 +28,8 @@ Other workloads (--workload):
   scatter-functional  the same into a separate present cache (the whole
                   128 MiB cache copied, HBM-bound)
   window-decode-hot   window-decode on one cache (16.8 MB, L2-resident)
+  paged-decode    the contiguous decode workload held in 64-row pages of a
+                  shuffled page pool (lengths + paged append + paged decode)
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--workload ...] [--chunk S] [--profile]
@@ -660,6 +662,82 @@ class ContigDecodeUnfused(ContigDecode):
     fused = False
 
 
+class PagedDecode(ContigDecode):
+    """The contiguous decode workload in 64-row pages: K/V pools of
+    B * C / 64 pages in a random order, a per-row page table; one step =
+    kvc_seq_lengths + kvc_paged_append + kvc_gqa_decode_paged (+ merge)."""
+    fused = False
+    page_size = 64
+
+    def __init__(self, dev, seed=0, with_kernels=True, chunk=None):
+        import torch
+        super().__init__(dev, seed=seed, with_kernels=with_kernels, chunk=chunk)
+        self.roofline_kernel = "kvc_gqa_decode_paged (split + merge launches)"
+        self.traffic_key = ("kvc_decode.cu", "decode_split_kernel_paged")
+        w = self.w
+        B, Hkv, D, C = w.batch, w.kv_heads, w.head_dim, w.capacity
+        P = self.page_size
+        max_pages = C // P
+        rng = np.random.default_rng(1000 + seed)
+        self.table_host = rng.permutation(B * max_pages).reshape(B, max_pages).astype(np.int32)
+        table = torch.from_numpy(self.table_host).to(dev)
+        # the same rows as the contiguous caches, moved into the shuffled pages
+        kp = torch.empty(B * max_pages, Hkv, P, D, dtype=self.kc.dtype, device=dev)
+        vp = torch.empty_like(kp)
+        idx = table.reshape(-1).long()
+        kp[idx] = self.kc.reshape(B, Hkv, max_pages, P, D).transpose(1, 2).reshape(-1, Hkv, P, D)
+        vp[idx] = self.vc.reshape(B, Hkv, max_pages, P, D).transpose(1, 2).reshape(-1, Hkv, P, D)
+        self.kc, self.vc, self.table = kp, vp, table
+        # (the workspace from the contiguous setup has the right size)
+
+    def step(self, i):
+        K = self.K
+        K.kvc_seq_lengths(self.sk, 1, self.w.capacity, 0, out=self.L, status=self.st)
+        K.kvc_paged_append(self.kc, self.vc, self.nk, self.nv, self.table, self.L,
+                           rope=self.rope, status=self.st)
+        self.kernel(i)
+
+    def kernel(self, i):
+        self.K.kvc_gqa_decode_paged(self.out, self.q, self.kc, self.vc, self.table, self.L,
+                                    rope=self.rope, workspace=self.ws, status=self.st)
+
+    def config(self):
+        c = super().config()
+        c.update({"workload": self.w.name + "-paged64", "page_size": self.page_size,
+                  "pages": int(self.table_host.size), "page_order": "random permutation"})
+        return c
+
+    def oracle_sample(self, rows):
+        import oracle
+        from persistent_kv_cache_gb300 import synth
+        w = self.w
+        rows = list(rows)[:2]
+        P = self.page_size
+        tab = self.table_host[rows]
+        used = np.unique(tab)
+        remap = {int(p): j for j, p in enumerate(used)}
+        kp = synth.bits(self.kc[torch_index(used)].cpu()).copy()
+        vp = synth.bits(self.vc[torch_index(used)].cpu()).copy()
+        tab_local = np.vectorize(remap.get)(tab).astype(np.int32)
+        nk, nv = synth.bits(self.nk_host[rows]), synth.bits(self.nv_host[rows])
+        q = synth.bits(self.q_host[rows])
+        cos, sin = (t.cpu().numpy() for t in self.rope)
+        T = self.T[rows]
+        t0 = time.perf_counter()
+        oracle.paged_append(kp, vp, tab_local, P, nk, nv, T - 1, cos, sin)
+        oracle.paged_attention(q, kp, vp, tab_local, P, T, T, cos_cache=cos, sin_cache=sin)
+        dt = time.perf_counter() - t0
+        nbytes = (int(T.sum()) * w.kv_heads * w.head_dim * 2 * self.e
+                  + 2 * len(rows) * w.q_heads * w.head_dim * self.e
+                  + 2 * 2 * len(rows) * w.kv_heads * w.head_dim * self.e)
+        return dt, nbytes
+
+
+def torch_index(a):
+    import torch
+    return torch.from_numpy(np.asarray(a, dtype=np.int64))
+
+
 class WindowDecodeHot(WindowDecode):
     replicas = 1
 
@@ -673,6 +751,7 @@ class WindowDecodeRing(WindowDecode):
 
 
 WORKLOADS = {"contig-decode": ContigDecode, "contig-decode-unfused": ContigDecodeUnfused,
+             "paged-decode": PagedDecode,
              "window-decode": WindowDecode,
              "window-decode-unfused": WindowDecodeUnfused,
              "window-decode-drift": WindowDecodeDrift, "window-decode-ring": WindowDecodeRing,

@@ -10,6 +10,7 @@
  *                          staging seed / copy-back (windowed, several tokens)
  *     kvc_gqa_decode       one-token GQA attention over the cache
  *     kvc_gqa_decode_ring  the same over a ring of C slots (circular addressing)
+ *     kvc_paged_append, kvc_gqa_decode_paged  append and decode on a paged cache
  *     kvc_decode_step      lengths + append + decode in one launch (contiguous
  *                          cache or ring)
  *     kvc_window_decode_step  the same for a windowed cache (small windows)
@@ -52,6 +53,9 @@
  *     split of one query row across workers with an (m, l, o) merge).
  *   "Stateful decode & KV cache", section "Sliding-window ring buffer"
  *     (RoPE baked into K at write time; the mask depends on positions only).
+ *   "Persistent KV Cache and Decode Performance Roadmap", "Phase 2" and the
+ *     CPU backend's "fixed-size paged blocks and a page-table iterator
+ *     consumed directly by Attention" (the paged calls).
  */
 #ifndef KVC_H
 #define KVC_H
@@ -307,6 +311,47 @@ kvc_status kvc_gqa_decode_ring(void *out, const void *q, const void *k_cache, co
                                float scale, const float *rope_cos, const float *rope_sin,
                                int64_t rope_max_pos, void *workspace, size_t workspace_bytes,
                                int32_t *dev_status, void *stream);
+
+/*
+ * Paged cache ("Persistent KV Cache and Decode Performance Roadmap", Phase 2:
+ * fixed-size pages read through a page table, never gathered into one
+ * contiguous cache).  K and V live in page pools [n_pool_pages, kv_heads,
+ * page_size, head_dim] (one page holds page_size consecutive tokens of every
+ * KV head).  block_table is device int32 [batch, max_pages]: logical row r of
+ * batch row b is slot r % page_size of page block_table[b * max_pages +
+ * r / page_size].  The caller allocates the pages (the table entries a step
+ * touches must name pages of the pool); the lengths are those of a
+ * contiguous cache of capacity max_pages * page_size (kvc_seq_lengths with
+ * KVC_CONTIGUOUS).
+ *
+ * kvc_paged_append -- write the S new rows (K rotated at P + i as in
+ * kvc_window_append) at logical rows [P, P + S).  A row whose new tokens
+ * would land in a page id outside [0, n_pool_pages) sets KVC_DEV_INDEX_OOB
+ * and writes nothing.  Any even head_dim <= 1024; all dtypes.
+ */
+kvc_status kvc_paged_append(void *k_pool, void *v_pool, const void *new_k, const void *new_v,
+                            const int32_t *block_table, int max_pages, int64_t n_pool_pages,
+                            int page_size, kvc_lengths len, int batch, int kv_heads,
+                            int new_tokens, int head_dim, int dtype, const float *rope_cos,
+                            const float *rope_sin, int64_t rope_max_pos, int32_t *dev_status,
+                            void *stream);
+
+/*
+ * kvc_gqa_decode_paged -- kvc_gqa_decode over a paged cache: the split
+ * kernel streams 64-row tiles straight from the pages (page_size must be a
+ * positive multiple of 64, so that no tile straddles two pages).  A page id
+ * outside the pool sets KVC_DEV_INDEX_OOB; that row's output is then
+ * undefined.  Workspace: kvc_gqa_decode_workspace_size(batch, q_heads,
+ * kv_heads, max_pages * page_size, head_dim, dtype).  Supported:
+ * KVC_BF16/KVC_F16, head_dim in {64, 128}, q_heads / kv_heads <= 16.
+ */
+kvc_status kvc_gqa_decode_paged(void *out, const void *q, const void *k_pool,
+                                const void *v_pool, const int32_t *block_table, int max_pages,
+                                int64_t n_pool_pages, int page_size, kvc_lengths len, int batch,
+                                int q_heads, int kv_heads, int head_dim, int dtype,
+                                int local_window_size, float scale, const float *rope_cos,
+                                const float *rope_sin, int64_t rope_max_pos, void *workspace,
+                                size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
  * kvc_decode_step -- one fused one-token step on a contiguous cache or a

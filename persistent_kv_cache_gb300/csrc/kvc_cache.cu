@@ -84,16 +84,26 @@ __device__ __forceinline__ void write_new_pair(T *__restrict__ dst_row,
     *reinterpret_cast<Vec<T, VEC> *>(dst_row + half + j * VEC) = hi;
 }
 
+// page table of a paged cache: logical row r of batch row b is slot
+// r % page_size of page table[b * max_pages + r / page_size] of a pool
+// [n_pages, kv_heads, page_size, D]
+struct PageTable {
+    const int32_t *table;
+    int max_pages, page_size;
+    int64_t n_pages;
+};
+
 // grid: x over (i, pair-vector) of one (b, head) slice, y = b * Hkv + h, z = K/V
 // dst row of token i, in a buffer with dst_rows rows/head: P + i (base_mode
-// 0), cache_past + i (1), or (P + i) mod dst_rows for a ring (2, where only
-// the last dst_rows tokens are written)
+// 0), cache_past + i (1), (P + i) mod dst_rows for a ring (2, where only the
+// last dst_rows tokens are written), or row P + i of a paged cache (3)
 template <typename T, int VEC>
 __global__ void __launch_bounds__(128)
 new_rows_kernel(T *__restrict__ k_dst, T *__restrict__ v_dst, const T *__restrict__ new_k,
                 const T *__restrict__ new_v, kvc_lengths len, int kv_heads, int S, int D,
                 int64_t dst_rows, int base_mode, const float *__restrict__ cos_t,
-                const float *__restrict__ sin_t, int64_t rope_max_pos, int32_t *status)
+                const float *__restrict__ sin_t, int64_t rope_max_pos, int32_t *status,
+                PageTable pt)
 {
     const int slice = blockIdx.y;
     const int b = slice / kv_heads;
@@ -108,13 +118,28 @@ new_rows_kernel(T *__restrict__ k_dst, T *__restrict__ v_dst, const T *__restric
             kvc::raise_status(status, KVC_DEV_ROPE_RANGE);
         return;
     }
-    const bool ring = base_mode == 2;
+    const bool ring = base_mode == 2, paged = base_mode == 3;
+    const bool lead = threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0 &&
+                      slice % kv_heads == 0;
     const int base = base_mode == 1 ? len.cache_past[b] : P;
     if (base < 0 || (!ring && (int64_t)base + S > dst_rows)) {
         // lengths computed for another capacity: refuse rather than overrun
-        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0 && slice % kv_heads == 0)
+        if (lead)
             kvc::raise_status(status, KVC_DEV_CAPACITY);
         return;
+    }
+    if (paged) {
+        // every page the row's new tokens land in must exist, else the row
+        // writes nothing
+        const int p0 = P / pt.page_size, p1 = (P + S - 1) / pt.page_size;
+        for (int p = p0; p <= p1; ++p) {
+            const int id = pt.table[(int64_t)b * pt.max_pages + p];
+            if (id < 0 || (int64_t)id >= pt.n_pages) {
+                if (lead)
+                    kvc::raise_status(status, KVC_DEV_INDEX_OOB);
+                return;
+            }
+        }
     }
     const int pairs = D / (2 * VEC);
     // a ring keeps only the last dst_rows tokens of the step
@@ -129,8 +154,15 @@ new_rows_kernel(T *__restrict__ k_dst, T *__restrict__ v_dst, const T *__restric
         const int64_t pos = (int64_t)P + i;
         const float *cs = rotate ? cos_t + pos * (D / 2) : nullptr;
         const float *sn = rotate ? sin_t + pos * (D / 2) : nullptr;
-        const int64_t row = ring ? pos % dst_rows : (int64_t)base + i;
-        write_new_pair<T, VEC>(dst + row * D, src + (int64_t)i * D, D, j, rotate, cs, sn);
+        T *drow;
+        if (paged) {
+            const int64_t page = pt.table[(int64_t)b * pt.max_pages + pos / pt.page_size];
+            drow = (is_k ? k_dst : v_dst) +
+                   ((page * kv_heads + slice % kv_heads) * pt.page_size + pos % pt.page_size) * D;
+        } else {
+            drow = dst + (ring ? pos % dst_rows : (int64_t)base + i) * D;
+        }
+        write_new_pair<T, VEC>(drow, src + (int64_t)i * D, D, j, rotate, cs, sn);
     }
 }
 
@@ -260,7 +292,8 @@ kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const v
     T *vc = static_cast<T *>(v_cache);
     const T *nk = static_cast<const T *>(new_k);
     const T *nv = static_cast<const T *>(new_v);
-    auto launch_new_rows = [&](T *kd, T *vd, int64_t dst_rows, int base_mode) {
+    auto launch_new_rows = [&](T *kd, T *vd, int64_t dst_rows, int base_mode,
+                               PageTable pt = PageTable{nullptr, 0, 0, 0}) {
         const int pairs = vec_ok ? D / (2 * VEC) : D / 2;
         const int64_t work = (int64_t)S * pairs;
         int gx = (int)((work + 127) / 128);
@@ -269,11 +302,11 @@ kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const v
         if (vec_ok)
             new_rows_kernel<T, VEC><<<grid, 128, 0, stream>>>(kd, vd, nk, nv, len, kv_heads, S, D,
                                                               dst_rows, base_mode, cos_t,
-                                                              sin_t, rope_max_pos, status);
+                                                              sin_t, rope_max_pos, status, pt);
         else
             new_rows_kernel<T, 1><<<grid, 128, 0, stream>>>(kd, vd, nk, nv, len, kv_heads, S, D,
                                                             dst_rows, base_mode, cos_t,
-                                                            sin_t, rope_max_pos, status);
+                                                            sin_t, rope_max_pos, status, pt);
     };
     auto launch_copy = [&](char *kd, char *vd, const char *ks, const char *vs, int64_t dst_rows,
                            int64_t src_rows, int copy_back, int64_t max_rows) {
@@ -318,6 +351,35 @@ kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const v
                     static_cast<const char *>(k_stage), static_cast<const char *>(v_stage), C,
                     C + S, 1, C);
     }
+    return kvc_host::launch_status();
+}
+
+template <typename T>
+kvc_status paged_append_typed(void *k_pool, void *v_pool, const void *new_k, const void *new_v,
+                              const kvc_lengths &len, int batch, int kv_heads, int S, int D,
+                              const PageTable &pt, const float *cos_t, const float *sin_t,
+                              int64_t rope_max_pos, int32_t *status, cudaStream_t stream)
+{
+    constexpr int VEC = 16 / sizeof(T);
+    const bool vec_ok = (D / 2) % VEC == 0;
+    const int pairs = vec_ok ? D / (2 * VEC) : D / 2;
+    const int64_t work = (int64_t)S * pairs;
+    int gx = (int)((work + 127) / 128);
+    gx = gx < 1 ? 1 : (gx > 64 ? 64 : gx);
+    dim3 grid(gx, batch * kv_heads, 2);
+    const int64_t capacity = (int64_t)pt.max_pages * pt.page_size;
+    T *kp = static_cast<T *>(k_pool);
+    T *vp = static_cast<T *>(v_pool);
+    const T *nk = static_cast<const T *>(new_k);
+    const T *nv = static_cast<const T *>(new_v);
+    if (vec_ok)
+        new_rows_kernel<T, VEC><<<grid, 128, 0, stream>>>(kp, vp, nk, nv, len, kv_heads, S, D,
+                                                          capacity, 3, cos_t, sin_t,
+                                                          rope_max_pos, status, pt);
+    else
+        new_rows_kernel<T, 1><<<grid, 128, 0, stream>>>(kp, vp, nk, nv, len, kv_heads, S, D,
+                                                        capacity, 3, cos_t, sin_t, rope_max_pos,
+                                                        status, pt);
     return kvc_host::launch_status();
 }
 
@@ -412,5 +474,54 @@ KVC_API kvc_status kvc_window_append(void *k_cache, void *v_cache, const void *n
         return append_typed<__half>(k_cache, v_cache, new_k, new_v, k_stage, v_stage, len, batch,
                                     kv_heads, new_tokens, capacity, head_dim, w, phase, rope_cos,
                                     rope_sin, rope_max_pos, dev_status, stream);
+    }
+}
+
+KVC_API kvc_status kvc_paged_append(void *k_pool, void *v_pool, const void *new_k,
+                                    const void *new_v, const int32_t *block_table, int max_pages,
+                                    int64_t n_pool_pages, int page_size, kvc_lengths len,
+                                    int batch, int kv_heads, int new_tokens, int head_dim,
+                                    int dtype, const float *rope_cos, const float *rope_sin,
+                                    int64_t rope_max_pos, int32_t *dev_status, void *stream)
+{
+    const int eb = kvc_host::elem_bytes_of(dtype);
+    if (eb == 0)
+        return KVC_ERR_DTYPE;
+    if (batch < 0 || kv_heads < 1 || new_tokens < 1 || head_dim < 2 || head_dim > 1024 ||
+        (head_dim & 1))
+        return KVC_ERR_SHAPE;
+    if (page_size < 1 || max_pages < 1 || n_pool_pages < 1)
+        return KVC_ERR_SHAPE;
+    if ((int64_t)max_pages * page_size > (int64_t)INT32_MAX)
+        return KVC_ERR_CAPACITY;
+    if ((rope_cos == nullptr) != (rope_sin == nullptr))
+        return KVC_ERR_NULL;
+    if (rope_cos && rope_max_pos < 1)
+        return KVC_ERR_SHAPE;
+    if (batch == 0)
+        return KVC_OK;
+    if (!k_pool || !v_pool || !new_k || !new_v || !block_table || !kvc_host::lengths_ok(len))
+        return KVC_ERR_NULL;
+    const size_t pool_bytes = (size_t)n_pool_pages * kv_heads * page_size * head_dim * eb;
+    if (kvc_host::overlaps(k_pool, pool_bytes, v_pool, pool_bytes))
+        return KVC_ERR_SHAPE;
+    for (const void *p : {(const void *)k_pool, (const void *)v_pool, new_k, new_v})
+        if (!kvc_host::aligned16(p))
+            return KVC_ERR_ALIGN;
+    const PageTable pt{block_table, max_pages, page_size, n_pool_pages};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (dtype) {
+    case KVC_F32:
+        return paged_append_typed<float>(k_pool, v_pool, new_k, new_v, len, batch, kv_heads,
+                                         new_tokens, head_dim, pt, rope_cos, rope_sin,
+                                         rope_max_pos, dev_status, st);
+    case KVC_BF16:
+        return paged_append_typed<__nv_bfloat16>(k_pool, v_pool, new_k, new_v, len, batch,
+                                                 kv_heads, new_tokens, head_dim, pt, rope_cos,
+                                                 rope_sin, rope_max_pos, dev_status, st);
+    default:
+        return paged_append_typed<__half>(k_pool, v_pool, new_k, new_v, len, batch, kv_heads,
+                                          new_tokens, head_dim, pt, rope_cos, rope_sin,
+                                          rope_max_pos, dev_status, st);
     }
 }

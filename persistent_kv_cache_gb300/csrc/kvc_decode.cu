@@ -285,16 +285,33 @@ struct DecodeArgs {
     const int32_t *seqlens_k;
     const void *new_k, *new_v;
     void *k_cache, *v_cache;
+    // paged cache only: logical row r of batch row b is slot r % page_size of
+    // page block_table[b * max_pages + r / page_size] of the pool
+    const int32_t *block_table;
+    int max_pages, page_size;
+    int64_t n_pool_pages;
 };
+
+// what the split kernel reads: the lengths arrays over a cache or a ring
+// (plain), seqlens_k with the append fused in (fused), or a paged cache
+enum : int { kPlain = 0, kFused = 1, kPaged = 2 };
+
+// First logical row a split count starts from: the window's first visible
+// row, rounded down to a tile for a paged cache so that no tile straddles a
+// page (the rows below the window are masked).
+template <int MODE> __device__ __forceinline__ int split_origin(int vis0)
+{
+    return MODE == kPaged ? vis0 & ~(kTile - 1) : vis0;
+}
 
 // (L, T) of batch row b: from the lengths arrays, or in the fused step from
 // seqlens_k (kvc_seq_lengths for S = 1 on a contiguous cache or a ring).
 // Returns the row's number of splits; 0 when it has nothing to attend
 // (rejected row, lengths that do not fit this cache, RoPE out of range).
-template <bool FUSED>
+template <int MODE>
 __device__ __forceinline__ int row_splits(const DecodeArgs &a, int b, int &L, int &tot)
 {
-    if constexpr (FUSED) {
+    if constexpr (MODE == kFused) {
         const int64_t T64 = (int64_t)a.seqlens_k[b] + 1;
         if (T64 < 1 || T64 > (int64_t)INT32_MAX || (!a.ring && T64 > a.capacity))
             return 0;
@@ -309,15 +326,15 @@ __device__ __forceinline__ int row_splits(const DecodeArgs &a, int b, int &L, in
     if (a.cos_t && (int64_t)tot > a.rope_max_pos)
         return 0;
     const int vis0 = (a.window > 0 && L > a.window) ? L - a.window : 0;
-    return (int)((L - vis0 + a.split_rows - 1) / a.split_rows);
+    return (int)((L - split_origin<MODE>(vis0) + a.split_rows - 1) / a.split_rows);
 }
 
 // Errors of batch row b, raised once per row; the fused step also writes
 // the row's lengths (as kvc_seq_lengths would).
-template <bool FUSED>
+template <int MODE>
 __device__ __forceinline__ void row_check(const DecodeArgs &a, int b)
 {
-    if constexpr (FUSED) {
+    if constexpr (MODE == kFused) {
         const int64_t T64 = (int64_t)a.seqlens_k[b] + 1;
         const bool write_len = a.len.cache_total != nullptr;
         uint32_t bad = 0;
@@ -357,10 +374,11 @@ __device__ __forceinline__ void row_check(const DecodeArgs &a, int b)
 
 // One CTA per (split, kv head, batch row) for kvc_gqa_decode,
 // kvc_gqa_decode_ring and the fused kvc_decode_step; the split partials go
-// to decode_combine_kernel.  FUSED: lengths from seqlens_k, and the CTA
+// to decode_combine_kernel.  kFused: lengths from seqlens_k, and the CTA
 // holding the newest position places the new K/V row in its tile on chip
-// and stores it to the cache.
-template <typename T, int D, bool FUSED>
+// and stores it to the cache.  kPaged: tiles of 64 logical rows, each inside
+// one page; the producer warp reads the split's page ids at once.
+template <typename T, int D, int MODE>
 __global__ void __launch_bounds__(160)
 decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a)
@@ -379,27 +397,31 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * STAGE_BYTES + 16 * QS * 2);
     uint64_t *empty = full + NS;
     int *abort_flag = reinterpret_cast<int *>(empty + NS);
+    int *page_ids = abort_flag + 4;  // [32] paged: the split's pages
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     if (threadIdx.x == 0 && split == 0 && kvh == 0)
-        row_check<FUSED>(a, b);
+        row_check<MODE>(a, b);
     int L, tot;
-    const int nsplit = row_splits<FUSED>(a, b, L, tot);
+    const int nsplit = row_splits<MODE>(a, b, L, tot);
     if (split >= nsplit)
         return;
     const int vis0 = (a.window > 0 && L > a.window) ? L - a.window : 0;
-    const int vis = L - vis0;
-    // this split's visible rows [j0, j0 + cnt) in position order, as two runs
-    // of slots: [q0, q0 + cnt_a) and [0, cnt - cnt_a)
+    const int origin = split_origin<MODE>(vis0);
+    const int vis = L - origin;
+    // this split's rows [j0, j0 + cnt) from the origin, in position order, as
+    // two runs of slots: [q0, q0 + cnt_a) and [0, cnt - cnt_a)
     const int C = (int)a.capacity;
     const int j0 = (int)(split * a.split_rows);
     const int cnt = (int)min((int64_t)vis - j0, a.split_rows);
-    const int first = a.ring ? (int)(((int64_t)tot - vis) % C) : vis0;
+    const int first = a.ring ? (int)(((int64_t)tot - vis) % C) : origin;
     int q0 = first + j0;
     if (q0 >= C)
         q0 -= C;
     const int cnt_a = min(cnt, C - q0);
+    // rows of tile t below the window (a paged cache's first tile only)
+    auto tile_lo = [&](int t) { return MODE == kPaged ? max(0, vis0 - (q0 + t * kTile)) : 0; };
     const int nt_a = (cnt_a + kTile - 1) / kTile;
     const int ntiles = nt_a + (cnt - cnt_a + kTile - 1) / kTile;
     // first slot and number of valid rows of tile t
@@ -422,6 +444,21 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     if (warp == kConsumers) {
         // ---------------- producer ----------------
+        int page0 = 0;
+        if constexpr (MODE == kPaged) {
+            // the pages this split touches, one lane each (at most 32)
+            page0 = q0 / a.page_size;
+            const int npages = (q0 + cnt - 1) / a.page_size - page0 + 1;
+            if (lane < npages) {
+                int id = a.block_table[(int64_t)b * a.max_pages + page0 + lane];
+                if (id < 0 || (int64_t)id >= a.n_pool_pages) {
+                    kvc::raise_status(a.status, KVC_DEV_INDEX_OOB);
+                    id = 0;  // read a page that exists; the row's result is void
+                }
+                page_ids[lane] = id;
+            }
+            __syncwarp();
+        }
         if (lane == 0) {
             kvc::tma_prefetch_desc(&tmap_k);
             kvc::tma_prefetch_desc(&tmap_v);
@@ -436,7 +473,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 uint8_t *kb = stages + s * STAGE_BYTES;
                 uint8_t *vb = kb + KT_BYTES;
                 kvc::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-                const int32_t y = (int32_t)(row_base + tile_start(t));
+                int32_t y;
+                if constexpr (MODE == kPaged) {
+                    const int r = q0 + t * kTile;  // logical row, a multiple of 64
+                    const int64_t page = page_ids[r / a.page_size - page0];
+                    y = (int32_t)((page * a.kv_heads + kvh) * a.page_size + r % a.page_size);
+                } else {
+                    y = (int32_t)(row_base + tile_start(t));
+                }
 #pragma unroll
                 for (int bx = 0; bx < BOXES; ++bx) {
                     kvc::tma_load_2d(kb + bx * 8192, &tmap_k, bx * 64, y, &full[s]);
@@ -484,7 +528,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         const int rows_t = tile_rows(t);
         const int my_valid = min(16, max(0, rows_t - 16 * warp));
         bool patched = false;
-        if (FUSED && split == nsplit - 1 && t == ntiles - 1 && my_valid > 0 &&
+        if (MODE == kFused && split == nsplit - 1 && t == ntiles - 1 && my_valid > 0 &&
             16 * warp + my_valid == rows_t) {
             // this warp owns the newest row (position tot - 1): place the new
             // K (rotated there) and V row in the tile and store it to the cache
@@ -532,7 +576,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
                 __syncwarp();
             }
-            ga.tile(kb, vb, warp, lane, 0, my_valid, a.scale_log2);
+            const int my_lo = min(16, max(0, tile_lo(t) - 16 * warp));
+            if (my_lo < my_valid)
+                ga.tile(kb, vb, warp, lane, my_lo, my_valid, a.scale_log2);
         }
         if ((my_valid > 0 && my_valid < 16) || patched)
             kvc::fence_proxy_async_smem();
@@ -576,14 +622,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
 // splits' m and l are read in parallel into shared memory, the weights
 // 2^(m_j - max m) computed once, and each output column sums its partials
 // with four loads in flight
-template <typename T, bool FUSED>
+template <typename T, int MODE>
 __global__ void __launch_bounds__(128)
 decode_combine_kernel(const DecodeArgs a, int D)
 {
     extern __shared__ float wsh[];  // m [max_splits], then l * w [max_splits], w [max_splits]
     const int h = blockIdx.x, b = blockIdx.y;
     int L, tot;
-    const int nsplit = row_splits<FUSED>(a, b, L, tot);
+    const int nsplit = row_splits<MODE>(a, b, L, tot);
     if (nsplit <= 1)
         return;
     const int MS = a.max_splits;
@@ -968,6 +1014,13 @@ kvc_status launch(void *out, const void *q, const void *k_rows, const void *v_ro
 
 namespace {
 
+// the page table of a paged cache (kvc_gqa_decode_paged)
+struct PagedExtra {
+    const int32_t *block_table;
+    int max_pages, page_size;
+    int64_t n_pool_pages;
+};
+
 // inputs of the fused step (kvc_decode_step) on top of the decode's own
 struct StepExtra {
     const int32_t *seqlens_k;
@@ -981,13 +1034,15 @@ kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const 
                            int64_t C, int window, float scale, const float *cos_t,
                            const float *sin_t, int64_t rope_max_pos, void *workspace,
                            int ring, int32_t *status, cudaStream_t stream,
-                           const StepExtra *fx = nullptr)
+                           const StepExtra *fx = nullptr, const PagedExtra *px = nullptr)
 {
     const CUtensorMapDataType tt = std::is_same<T, __half>::value
                                        ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap tk, tv;
-    const uint64_t rows = (uint64_t)batch * kv_heads * C;
+    // a paged cache maps the whole page pool [pages, kv_heads, page_size, D]
+    const uint64_t rows = px ? (uint64_t)px->n_pool_pages * kv_heads * px->page_size
+                             : (uint64_t)batch * kv_heads * C;
     if (rows > (uint64_t)INT32_MAX)
         return KVC_ERR_SHAPE;
     if (!kvc_host::encode_2d_bf16_sw128(&tk, k_cache, rows, D, kTile, tt) ||
@@ -1025,10 +1080,18 @@ kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const 
         a.k_cache = fx->k_cache;
         a.v_cache = fx->v_cache;
     }
+    if (px) {
+        a.block_table = px->block_table;
+        a.max_pages = px->max_pages;
+        a.page_size = px->page_size;
+        a.n_pool_pages = px->n_pool_pages;
+    }
     constexpr int NS = decode_stages(D);
     const size_t smem = 1024 + (size_t)NS * 2 * kTile * D * 2 + 16 * (D + 8) * 2 +
-                        2 * NS * sizeof(uint64_t) + 16;
-    auto kern = fx ? decode_split_kernel<T, D, true> : decode_split_kernel<T, D, false>;
+                        2 * NS * sizeof(uint64_t) + 16 + 32 * sizeof(int);
+    auto kern = fx   ? decode_split_kernel<T, D, kFused>
+                : px ? decode_split_kernel<T, D, kPaged>
+                     : decode_split_kernel<T, D, kPlain>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return KVC_ERR_CUDA;
@@ -1038,9 +1101,11 @@ kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const 
         dim3 g2(q_heads, batch);
         const size_t cs = 3 * a.max_splits * sizeof(float);
         if (fx)
-            decode_combine_kernel<T, true><<<g2, 128, cs, stream>>>(a, D);
+            decode_combine_kernel<T, kFused><<<g2, 128, cs, stream>>>(a, D);
+        else if (px)
+            decode_combine_kernel<T, kPaged><<<g2, 128, cs, stream>>>(a, D);
         else
-            decode_combine_kernel<T, false><<<g2, 128, cs, stream>>>(a, D);
+            decode_combine_kernel<T, kPlain><<<g2, 128, cs, stream>>>(a, D);
     }
     return kvc_host::launch_status();
 }
@@ -1155,6 +1220,75 @@ KVC_API kvc_status kvc_gqa_decode_ring(void *out, const void *q, const void *k_c
     return decode_entry(out, q, k_cache, v_cache, len, batch, q_heads, kv_heads, capacity,
                         head_dim, dtype, local_window_size, scale, rope_cos, rope_sin,
                         rope_max_pos, workspace, workspace_bytes, 1, dev_status, stream);
+}
+
+KVC_API kvc_status kvc_gqa_decode_paged(void *out, const void *q, const void *k_pool,
+                                        const void *v_pool, const int32_t *block_table,
+                                        int max_pages, int64_t n_pool_pages, int page_size,
+                                        kvc_lengths len, int batch, int q_heads, int kv_heads,
+                                        int head_dim, int dtype, int local_window_size,
+                                        float scale, const float *rope_cos,
+                                        const float *rope_sin, int64_t rope_max_pos,
+                                        void *workspace, size_t workspace_bytes,
+                                        int32_t *dev_status, void *stream)
+{
+    if (dtype != KVC_BF16 && dtype != KVC_F16)
+        return dtype == KVC_F32 ? KVC_ERR_UNSUPPORTED : KVC_ERR_DTYPE;
+    if (batch < 0 || q_heads < 1 || kv_heads < 1 || q_heads % kv_heads != 0)
+        return KVC_ERR_SHAPE;
+    if ((head_dim != 64 && head_dim != 128) || q_heads / kv_heads > 16)
+        return KVC_ERR_UNSUPPORTED;
+    // pages hold whole 64-row tiles
+    if (page_size < kTile || page_size % kTile != 0 || max_pages < 1 || n_pool_pages < 1)
+        return KVC_ERR_SHAPE;
+    const int64_t capacity = (int64_t)max_pages * page_size;
+    if (capacity > (int64_t)INT32_MAX ||
+        n_pool_pages * kv_heads * (int64_t)page_size > (int64_t)INT32_MAX)
+        return KVC_ERR_CAPACITY;
+    if ((rope_cos == nullptr) != (rope_sin == nullptr))
+        return KVC_ERR_NULL;
+    if (rope_cos && rope_max_pos < 1)
+        return KVC_ERR_SHAPE;
+    if (batch == 0)
+        return KVC_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_table || !kvc_host::lengths_ok(len))
+        return KVC_ERR_NULL;
+    for (const void *p : {(const void *)out, q, k_pool, v_pool})
+        if (!kvc_host::aligned16(p))
+            return KVC_ERR_ALIGN;
+    const size_t pool_bytes = (size_t)n_pool_pages * kv_heads * page_size * head_dim * 2;
+    if (kvc_host::overlaps(k_pool, pool_bytes, v_pool, pool_bytes))
+        return KVC_ERR_SHAPE;
+    const size_t need =
+        kvc_gqa_decode_workspace_size(batch, q_heads, kv_heads, capacity, head_dim, dtype);
+    if (need > 256 && (!workspace || workspace_bytes < need))
+        return KVC_ERR_WORKSPACE;
+    if (need > 256 && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return KVC_ERR_ALIGN;
+    if (scale == 0.f)
+        scale = 1.0f / sqrtf((float)head_dim);
+    const PagedExtra px{block_table, max_pages, page_size, n_pool_pages};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == KVC_BF16)
+        return head_dim == 64
+                   ? launch_decode16<__nv_bfloat16, 64>(out, q, k_pool, v_pool, len, batch, q_heads,
+                                                        kv_heads, capacity, local_window_size,
+                                                        scale, rope_cos, rope_sin, rope_max_pos,
+                                                        workspace, 0, dev_status, st, nullptr,
+                                                        &px)
+                   : launch_decode16<__nv_bfloat16, 128>(
+                         out, q, k_pool, v_pool, len, batch, q_heads, kv_heads, capacity,
+                         local_window_size, scale, rope_cos, rope_sin, rope_max_pos, workspace, 0,
+                         dev_status, st, nullptr, &px);
+    return head_dim == 64
+               ? launch_decode16<__half, 64>(out, q, k_pool, v_pool, len, batch, q_heads, kv_heads,
+                                             capacity, local_window_size, scale, rope_cos,
+                                             rope_sin, rope_max_pos, workspace, 0, dev_status, st,
+                                             nullptr, &px)
+               : launch_decode16<__half, 128>(out, q, k_pool, v_pool, len, batch, q_heads,
+                                              kv_heads, capacity, local_window_size, scale,
+                                              rope_cos, rope_sin, rope_max_pos, workspace, 0,
+                                              dev_status, st, nullptr, &px);
 }
 
 // --------------------------------------------------------------------------

@@ -35,6 +35,7 @@ KVC_DEV_TIMEOUT = 16
 EXPORTS = ("kvc_tensor_scatter", "kvc_seq_lengths", "kvc_window_append", "kvc_gqa_decode",
            "kvc_gqa_decode_workspace_size", "kvc_gqa_decode_noalloc", "kvc_gqa_decode_ring",
            "kvc_decode_step", "kvc_decode_step_workspace_size", "kvc_window_decode_step",
+           "kvc_paged_append", "kvc_gqa_decode_paged",
            "kvc_gqa_prefill_chunk", "kvc_status_string", "kvc_abi_version")
 KVC_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -95,6 +96,9 @@ def library() -> ctypes.CDLL:
             "kvc_gqa_decode_ring": [P, P, P, P, L, I, I, I, I64, I, I, I, F, P, P, I64, P, SZ, P,
                                     P],
             "kvc_gqa_decode_workspace_size": [I, I, I, I64, I, I],
+            "kvc_paged_append": [P, P, P, P, P, I, I64, I, L, I, I, I, I, I, P, P, I64, P, P],
+            "kvc_gqa_decode_paged": [P, P, P, P, P, I, I64, I, L, I, I, I, I, I, I, F, P, P, I64,
+                                     P, SZ, P, P],
             "kvc_decode_step": [P, P, P, P, P, P, P, L, I, I, I, I64, I, I, I, I, F, P, P, I64, P,
                                 SZ, P, P],
             "kvc_decode_step_workspace_size": [I, I, I, I64, I, I],
@@ -208,6 +212,36 @@ def kvc_gqa_decode_ring(out, q, k_cache, v_cache, lengths, local_window_size=0, 
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), lengths.c(), B, Hq, Hkv, C, D,
         _dtype_code(q), local_window_size, scale, cs, sn, rmax, _ptr(ws), ws.numel(),
         _ptr(status), _stream(stream)))
+    return out
+
+
+def kvc_paged_append(k_pool, v_pool, new_k, new_v, block_table, lengths, rope=None, status=None,
+                     stream=None):
+    """Append on a paged cache: pools [pages, Hkv, page_size, D], block_table
+    int32 [B, max_pages] (include/kvc.h)."""
+    n_pages, Hkv, ps, D = k_pool.shape
+    B, _, S, _ = new_k.shape
+    cs, sn, rmax = _rope(rope)
+    _check("kvc_paged_append", library().kvc_paged_append(
+        _ptr(k_pool), _ptr(v_pool), _ptr(new_k), _ptr(new_v), _ptr(block_table),
+        block_table.shape[1], n_pages, ps, lengths.c(), B, Hkv, S, D, _dtype_code(k_pool), cs,
+        sn, rmax, _ptr(status), _stream(stream)))
+
+
+def kvc_gqa_decode_paged(out, q, k_pool, v_pool, block_table, lengths, local_window_size=0,
+                         scale=0.0, rope=None, workspace=None, status=None, stream=None):
+    """kvc_gqa_decode over a paged cache (include/kvc.h)."""
+    B, Hq, _, D = q.shape
+    n_pages, Hkv, ps, _ = k_pool.shape
+    max_pages = block_table.shape[1]
+    if workspace is None:
+        n = kvc_gqa_decode_workspace_size(B, Hq, Hkv, max_pages * ps, D, _dtype_code(q))
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    cs, sn, rmax = _rope(rope)
+    _check("kvc_gqa_decode_paged", library().kvc_gqa_decode_paged(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), max_pages, n_pages,
+        ps, lengths.c(), B, Hq, Hkv, D, _dtype_code(q), local_window_size, scale, cs, sn, rmax,
+        _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)))
     return out
 
 

@@ -146,6 +146,28 @@ def test_decode_step_host_checks(kvc):
              None) == 0
 
 
+def test_paged_host_checks(kvc):
+    lib = kvc.library()
+    L = _lengths(kvc)
+    d = lib.kvc_gqa_decode_paged
+    base = [FAKE, FAKE * 2, FAKE * 3, 1 << 32]
+    # (out, q, k_pool, v_pool, table, max_pages, n_pages, page_size, len, B, Hq, Hkv, D, dtype, W,
+    #  scale, cos, sin, rope_max, ws, ws_bytes, status, stream)
+    ok = [FAKE * 4, 8, 64, 64, L, 2, 8, 2, 128, 1, 0, 0.0, None, None, 0, FAKE, 1 << 24, None, None]
+    assert d(*base, *ok[:3], 48, *ok[4:]) == 2                      # page not a multiple of 64
+    assert d(*base, *ok[:3], 0, *ok[4:]) == 2
+    assert d(*base, *ok[:9], 0, *ok[10:]) == 5                      # fp32 not on this path
+    assert d(*base, *ok[:9], 9, *ok[10:]) == 3                      # unknown dtype
+    assert d(*base, None, *ok[1:]) == 1                             # no table
+    assert d(FAKE + 8, *base[1:], *ok) == 4                         # alignment
+    a = lib.kvc_paged_append
+    okp = [FAKE * 4, 8, 64, 64, L, 2, 2, 1, 128, 1, None, None, 0, None, None]
+    assert a(*base, *okp[:3], 0, *okp[4:]) == 2                     # page size
+    assert a(*base, *okp[:9], 7, *okp[10:]) == 3                    # dtype
+    assert a(*base, *okp[:7], 0, *okp[8:]) == 2                     # S = 0
+    assert a(*base, None, *okp[1:]) == 1
+
+
 def test_prefill_host_checks(kvc):
     lib = kvc.library()
     f = lib.kvc_gqa_prefill_chunk
