@@ -480,8 +480,8 @@ class WindowPrefill(Workload):
                 ql = min(S - 1, q0 + qb - 1)
                 hi = Lp[b] + ql
                 lo = max(0, Lp[b] + q0 - W + 1)
-                issued += (hi - lo + 64) // 64
-        self.issued_flops = int(issued) * Hkv * 4 * 128 * 64 * D
+                issued += (hi - lo + 128) // 128
+        self.issued_flops = int(issued) * Hkv * 4 * 128 * 128 * D
         self.stage_bytes = int(2 * Hkv * D * e * int((2 * Lp + 2 * L).sum()))  # seed + copy-back r+w
         self.kernel_bytes = 2 * B * Hq * S * D * e + 2 * Hkv * D * e * int((Lp + S).sum())
         self.bytes_per_step = self.stage_bytes + self.kernel_bytes + 2 * 2 * B * Hkv * S * D * e
@@ -493,7 +493,9 @@ class WindowPrefill(Workload):
         self.out = torch.empty(B, Hq, S, D, dtype=bf, device=dev)
         self.L = K.Lengths(B, dev)
         self.st = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.launches_per_step = 5
+        # the KV split's partials (small chunks only: the grid is under a wave)
+        self.pws = K.prefill_workspace(self.out, self.ks, w.window)
+        self.launches_per_step = 5 + (1 if self.pws is not None else 0)
 
     def step(self, i):
         K, w = self.K, self.w
@@ -508,7 +510,7 @@ class WindowPrefill(Workload):
     def kernel(self, i):
         self.K.kvc_gqa_prefill_chunk(self.out, self.q, self.ks, self.vs, self.L,
                                      local_window_size=self.w.window, rope=self.rope,
-                                     status=self.st)
+                                     status=self.st, workspace=self.pws)
 
     def config(self):
         w = self.w
@@ -516,6 +518,7 @@ class WindowPrefill(Workload):
                 "kv_heads": w.kv_heads, "head_dim": w.head_dim, "capacity": w.capacity,
                 "window": w.window, "past_len": f"U[{w.total_lo},{w.total_hi}]",
                 "chunk": self.S, "visible_flops_per_step": self.flops,
+                "kv_split": self.pws is not None,
                 "issued_flops_per_step": self.issued_flops,
                 "l2": "stage + cache ~1 GB per step > L2",
                 "bytes_per_step": self.bytes_per_step}

@@ -67,7 +67,7 @@
 extern "C" {
 #endif
 
-#define KVC_ABI_VERSION 2
+#define KVC_ABI_VERSION 3
 
 typedef enum {
     KVC_OK = 0,
@@ -443,16 +443,29 @@ kvc_status kvc_window_decode_step(void *out, const void *q, void *k_cache, void 
  * out, q          device [batch, q_heads, new_tokens, head_dim].
  * k_rows, v_rows  device [batch, kv_heads, rows_per_head, head_dim],
  *                 rows_per_head >= Lp + S for every row (C + S for a stage).
+ * workspace       device scratch of kvc_gqa_prefill_workspace_size(...) bytes,
+ *                 256-byte aligned, or NULL.  When the launch would not fill
+ *                 the GPU (few query blocks), each block's key range is split
+ *                 over several CTAs whose (o, m, l) partials go to the
+ *                 workspace and are merged by a second launch; with NULL (or
+ *                 too small a workspace) the call runs unsplit, with the same
+ *                 results up to floating-point rounding order.
  * Supported: KVC_BF16/KVC_F16 with head_dim in {64, 128, 256} and
  * q_heads / kv_heads in {1, 2, 4, 8, 16} (tcgen05 tensor-core path);
- * KVC_F32 with head_dim <= 256.  Buffers 16-byte aligned.
+ * KVC_F32 with head_dim <= 256 (no workspace used).  Buffers 16-byte aligned.
  */
 kvc_status kvc_gqa_prefill_chunk(void *out, const void *q, const void *k_rows, const void *v_rows,
                                  int64_t rows_per_head, kvc_lengths len, int batch, int q_heads,
                                  int kv_heads, int new_tokens, int head_dim, int dtype,
                                  int local_window_size, float scale, const float *rope_cos,
-                                 const float *rope_sin, int64_t rope_max_pos,
-                                 int32_t *dev_status, void *stream);
+                                 const float *rope_sin, int64_t rope_max_pos, void *workspace,
+                                 size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/* Bytes of workspace kvc_gqa_prefill_chunk uses for these sizes on the
+ * current device (0: it would not split). */
+size_t kvc_gqa_prefill_workspace_size(int batch, int q_heads, int kv_heads, int new_tokens,
+                                      int64_t rows_per_head, int head_dim, int dtype,
+                                      int local_window_size);
 
 /* Human-readable name of a status code (static storage). */
 const char *kvc_status_string(kvc_status status);

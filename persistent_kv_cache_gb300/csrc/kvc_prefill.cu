@@ -208,7 +208,7 @@ struct PrefillArgs {
     void *out;
     const void *q;
     kvc_lengths len;
-    int q_heads, kv_heads, group, qb_rows;  // qb_rows = 128 / group
+    int batch, q_heads, kv_heads, group, qb_rows;  // qb_rows = 128 / group
     int S;
     int64_t rows_per_head;
     int window;
@@ -216,6 +216,11 @@ struct PrefillArgs {
     const float *cos_t, *sin_t;
     int64_t rope_max_pos;
     int32_t *status;
+    // KV split (grids under one wave): blockIdx.x = q block * nsplit + split;
+    // each split writes fp32 (o, m, l) partials of its rows, merged by
+    // prefill_combine_kernel.  nsplit == 1: the output is written directly.
+    int nsplit;
+    float *ws_o, *ws_m, *ws_l;  // [nsplit][batch * q_heads * S] (x D for o)
 };
 
 template <int D> struct PrefillSmem {
@@ -322,7 +327,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::MISC_OFF + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qblk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int qblk = blockIdx.x / a.nsplit, split = blockIdx.x % a.nsplit;
+    const int kvh = blockIdx.y, b = blockIdx.z;
     const int g = a.group, QB = a.qb_rows, S = a.S;
 
     // ---- per batch row geometry (uniform over the CTA) ----
@@ -349,7 +355,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     int lo = 0;
     if (a.window > 0)
         lo = max(0, Lp + q0 - a.window + 1);
-    const int ntiles = (hi - lo + kBN) / kBN;
+    // this split's share [t0, t1) of the block's key tiles
+    const int ntiles_all = (hi - lo + kBN) / kBN;
+    const int t0 = (int)((int64_t)split * ntiles_all / a.nsplit);
+    const int t1 = (int)((int64_t)(split + 1) * ntiles_all / a.nsplit);
+    const int64_t rows_total = (int64_t)a.batch * a.q_heads * S;
+    if (t1 == t0) {
+        // nothing to attend: a partial that the merge skips
+        for (int m = threadIdx.x; m < kBM; m += kThreads) {
+            const int hh = m / QB, ii = q0 + (m - (m / QB) * QB);
+            if (ii < S && hh < g) {
+                const int64_t qrow = ((int64_t)b * a.q_heads + kvh * g + hh) * S + ii;
+                a.ws_m[split * rows_total + qrow] = -INFINITY;
+                a.ws_l[split * rows_total + qrow] = 0.f;
+            }
+        }
+        return;
+    }
+    lo += t0 * kBN;
+    const int ntiles = t1 - t0;
     const int nslabs = 2 * ntiles * NST;
     const int64_t row_base = ((int64_t)b * a.kv_heads + kvh) * a.rows_per_head;
 
@@ -666,22 +690,44 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             wait_or_abort(&o_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_flag,
                           a.status)) {
             tc_fence_after();
-            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-            T *dst = static_cast<T *>(a.out) + qrow * D;
+            if (a.nsplit == 1) {
+                const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+                T *dst = static_cast<T *>(a.out) + qrow * D;
 #pragma unroll 1
-            for (int cc = half * (D / 2); cc < (half + 1) * (D / 2); cc += 32) {
-                float o[32];
-                tmem_ld32(lane_addr + COL_O + cc, o);
-                if (row_valid) {
+                for (int cc = half * (D / 2); cc < (half + 1) * (D / 2); cc += 32) {
+                    float o[32];
+                    tmem_ld32(lane_addr + COL_O + cc, o);
+                    if (row_valid) {
 #pragma unroll
-                    for (int c = 0; c < 32; c += 8) {
-                        uint4 pkt;
-                        T *e = reinterpret_cast<T *>(&pkt);
+                        for (int c = 0; c < 32; c += 8) {
+                            uint4 pkt;
+                            T *e = reinterpret_cast<T *>(&pkt);
 #pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            e[u] = kvc::Elem<T>::from_f32(o[c + u] * inv);
-                        *reinterpret_cast<uint4 *>(dst + cc + c) = pkt;
+                            for (int u = 0; u < 8; ++u)
+                                e[u] = kvc::Elem<T>::from_f32(o[c + u] * inv);
+                            *reinterpret_cast<uint4 *>(dst + cc + c) = pkt;
+                        }
                     }
+                }
+            } else {
+                // this split's partial: o unnormalised, l, and the reference
+                // max m (log2 units) that o and l are relative to
+                const int64_t pr = split * rows_total + qrow;
+                float *dst = a.ws_o + pr * D;
+#pragma unroll 1
+                for (int cc = half * (D / 2); cc < (half + 1) * (D / 2); cc += 32) {
+                    float o[32];
+                    tmem_ld32(lane_addr + COL_O + cc, o);
+                    if (row_valid) {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 4)
+                            *reinterpret_cast<float4 *>(dst + cc + c) =
+                                make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+                    }
+                }
+                if (row_valid && half == 0) {
+                    a.ws_m[pr] = m_run;
+                    a.ws_l[pr] = l_tot;
                 }
             }
         }
@@ -695,12 +741,87 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
 }
 
+// Merges the KV splits' partials of every query row (one warp per row): the
+// weights 2^(m_j - max m) over the splits that saw a visible key, then
+// out = sum w_j o_j / sum w_j l_j, rounded to the output type.
+template <typename T, int D>
+__global__ void __launch_bounds__(128)
+prefill_combine_kernel(const PrefillArgs a)
+{
+    constexpr int PER = D / 32;  // columns per lane
+    const int lane = threadIdx.x & 31;
+    const int64_t rows_total = (int64_t)a.batch * a.q_heads * a.S;
+    const int64_t qrow = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (qrow >= rows_total)
+        return;
+    const int b = (int)(qrow / ((int64_t)a.q_heads * a.S));
+    // the rows the attention kernel refused (status already raised there)
+    const int L = a.len.cache_total[b];
+    if (L < 0)
+        return;
+    const int Lp = a.len.cache_past[b];
+    const int P = a.len.past_abs[b];
+    if (Lp < 0 || (int64_t)Lp + a.S > a.rows_per_head)
+        return;
+    if (a.cos_t && (int64_t)P + a.S > a.rope_max_pos)
+        return;
+    float mstar = -INFINITY;
+    for (int j = 0; j < a.nsplit; ++j)
+        mstar = fmaxf(mstar, a.ws_m[j * rows_total + qrow]);
+    float acc[PER];
+#pragma unroll
+    for (int c = 0; c < PER; ++c)
+        acc[c] = 0.f;
+    float l = 0.f;
+    for (int j = 0; j < a.nsplit; ++j) {
+        const float mj = a.ws_m[j * rows_total + qrow];
+        if (mj == -INFINITY)
+            continue;
+        const float w = exp2f(mj - mstar);
+        l += w * a.ws_l[j * rows_total + qrow];
+        const float *o = a.ws_o + (j * rows_total + qrow) * D;
+#pragma unroll
+        for (int c = 0; c < PER; ++c)
+            acc[c] += w * o[lane + 32 * c];
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    T *dst = static_cast<T *>(a.out) + qrow * D;
+#pragma unroll
+    for (int c = 0; c < PER; ++c)
+        dst[lane + 32 * c] = kvc::Elem<T>::from_f32(acc[c] * inv);
+}
+
+// KV splits for grids under one wave (one CTA per SM): as many as fill the
+// SMs without a second wave, each with at least two key tiles
+int prefill_splits(int batch, int q_heads, int kv_heads, int S, int64_t rows_per_head, int window)
+{
+    const int g = q_heads / kv_heads;
+    const int qb = kBM / g;
+    const int64_t ctas = (int64_t)((S + qb - 1) / qb) * kv_heads * batch;
+    const int sms = kvc_host::sm_count();
+    if (ctas <= 0 || ctas * 2 > sms)
+        return 1;
+    const int64_t keys = window > 0 ? std::min<int64_t>(rows_per_head, (int64_t)window + qb)
+                                    : rows_per_head;
+    const int64_t tiles = (keys + kBN - 1) / kBN;
+    int64_t n = sms / ctas;
+    n = std::min<int64_t>(n, std::max<int64_t>(1, tiles / 2));
+    return (int)std::min<int64_t>(n, 16);
+}
+
+size_t prefill_ws_bytes(int nsplit, int batch, int q_heads, int S, int head_dim)
+{
+    if (nsplit <= 1)
+        return 0;
+    return (size_t)nsplit * batch * q_heads * S * (head_dim + 2) * sizeof(float);
+}
+
 template <typename T, int D>
 kvc_status launch_prefill_tc(void *out, const void *q, const void *k_rows, const void *v_rows,
                              int64_t R, const kvc_lengths &len, int batch, int q_heads,
                              int kv_heads, int S, int window, float scale, const float *cos_t,
-                             const float *sin_t, int64_t rope_max_pos, int32_t *status,
-                             cudaStream_t stream)
+                             const float *sin_t, int64_t rope_max_pos, void *workspace,
+                             size_t workspace_bytes, int32_t *status, cudaStream_t stream)
 {
     using SM = PrefillSmem<D>;
     const uint64_t rows = (uint64_t)batch * kv_heads * R;
@@ -717,10 +838,20 @@ kvc_status launch_prefill_tc(void *out, const void *q, const void *k_rows, const
     a.out = out;
     a.q = q;
     a.len = len;
+    a.batch = batch;
     a.q_heads = q_heads;
     a.kv_heads = kv_heads;
     a.group = q_heads / kv_heads;
     a.qb_rows = kBM / a.group;
+    // a KV split when the grid is under one wave and the caller gave room
+    // for the partials; otherwise one CTA per query block
+    a.nsplit = prefill_splits(batch, q_heads, kv_heads, S, R, window);
+    if (!workspace || workspace_bytes < prefill_ws_bytes(a.nsplit, batch, q_heads, S, D))
+        a.nsplit = 1;
+    const int64_t rows_total = (int64_t)batch * q_heads * S;
+    a.ws_o = static_cast<float *>(workspace);
+    a.ws_m = a.ws_o ? a.ws_o + (int64_t)a.nsplit * rows_total * D : nullptr;
+    a.ws_l = a.ws_m ? a.ws_m + (int64_t)a.nsplit * rows_total : nullptr;
     a.S = S;
     a.rows_per_head = R;
     a.window = window;
@@ -740,8 +871,10 @@ kvc_status launch_prefill_tc(void *out, const void *q, const void *k_rows, const
         cudaSuccess)
         return KVC_ERR_CUDA;
     const int qblocks = (S + a.qb_rows - 1) / a.qb_rows;
-    dim3 grid(qblocks, kv_heads, batch);
+    dim3 grid(qblocks * a.nsplit, kv_heads, batch);
     kern<<<grid, kThreads, smem, stream>>>(tk, tv, a);
+    if (a.nsplit > 1)
+        prefill_combine_kernel<T, D><<<(unsigned)((rows_total + 3) / 4), 128, 0, stream>>>(a);
     return kvc_host::launch_status();
 }
 
@@ -749,18 +882,18 @@ template <typename T>
 kvc_status dispatch_prefill16(int D, void *out, const void *q, const void *k, const void *v,
                               int64_t R, const kvc_lengths &len, int B, int Hq, int Hkv, int S,
                               int W, float scale, const float *cs, const float *sn, int64_t rmax,
-                              int32_t *st, cudaStream_t stream)
+                              void *ws, size_t ws_bytes, int32_t *st, cudaStream_t stream)
 {
     switch (D) {
     case 64:
         return launch_prefill_tc<T, 64>(out, q, k, v, R, len, B, Hq, Hkv, S, W, scale, cs, sn,
-                                        rmax, st, stream);
+                                        rmax, ws, ws_bytes, st, stream);
     case 128:
         return launch_prefill_tc<T, 128>(out, q, k, v, R, len, B, Hq, Hkv, S, W, scale, cs, sn,
-                                         rmax, st, stream);
+                                         rmax, ws, ws_bytes, st, stream);
     case 256:
         return launch_prefill_tc<T, 256>(out, q, k, v, R, len, B, Hq, Hkv, S, W, scale, cs, sn,
-                                         rmax, st, stream);
+                                         rmax, ws, ws_bytes, st, stream);
     default:
         return KVC_ERR_UNSUPPORTED;
     }
@@ -768,13 +901,30 @@ kvc_status dispatch_prefill16(int D, void *out, const void *q, const void *k, co
 
 } // namespace
 
+KVC_API size_t kvc_gqa_prefill_workspace_size(int batch, int q_heads, int kv_heads,
+                                              int new_tokens, int64_t rows_per_head,
+                                              int head_dim, int dtype, int local_window_size)
+{
+    if (batch < 1 || q_heads < 1 || kv_heads < 1 || q_heads % kv_heads != 0 || new_tokens < 1 ||
+        head_dim < 1 || dtype == KVC_F32 || kvc_host::elem_bytes_of(dtype) == 0)
+        return 0;
+    const int g = q_heads / kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16)
+        return 0;
+    return prefill_ws_bytes(prefill_splits(batch, q_heads, kv_heads, new_tokens, rows_per_head,
+                                           local_window_size),
+                            batch, q_heads, new_tokens, head_dim);
+}
+
 KVC_API kvc_status kvc_gqa_prefill_chunk(void *out, const void *q, const void *k_rows,
                                          const void *v_rows, int64_t rows_per_head,
                                          kvc_lengths len, int batch, int q_heads, int kv_heads,
                                          int new_tokens, int head_dim, int dtype,
                                          int local_window_size, float scale,
                                          const float *rope_cos, const float *rope_sin,
-                                         int64_t rope_max_pos, int32_t *dev_status, void *stream_)
+                                         int64_t rope_max_pos, void *workspace,
+                                         size_t workspace_bytes, int32_t *dev_status,
+                                         void *stream_)
 {
     const int eb = kvc_host::elem_bytes_of(dtype);
     if (eb == 0)
@@ -803,6 +953,8 @@ KVC_API kvc_status kvc_gqa_prefill_chunk(void *out, const void *q, const void *k
     for (const void *p : {(const void *)out, q, k_rows, v_rows})
         if (!kvc_host::aligned16(p))
             return KVC_ERR_ALIGN;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return KVC_ERR_ALIGN;
     if (scale == 0.f)
         scale = 1.0f / sqrtf((float)head_dim);
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
@@ -814,8 +966,10 @@ KVC_API kvc_status kvc_gqa_prefill_chunk(void *out, const void *q, const void *k
         return dispatch_prefill16<__nv_bfloat16>(head_dim, out, q, k_rows, v_rows, rows_per_head,
                                                  len, batch, q_heads, kv_heads, new_tokens,
                                                  local_window_size, scale, rope_cos, rope_sin,
-                                                 rope_max_pos, dev_status, stream);
+                                                 rope_max_pos, workspace, workspace_bytes,
+                                                 dev_status, stream);
     return dispatch_prefill16<__half>(head_dim, out, q, k_rows, v_rows, rows_per_head, len, batch,
                                       q_heads, kv_heads, new_tokens, local_window_size, scale,
-                                      rope_cos, rope_sin, rope_max_pos, dev_status, stream);
+                                      rope_cos, rope_sin, rope_max_pos, workspace,
+                                      workspace_bytes, dev_status, stream);
 }

@@ -36,7 +36,8 @@ EXPORTS = ("kvc_tensor_scatter", "kvc_seq_lengths", "kvc_window_append", "kvc_gq
            "kvc_gqa_decode_workspace_size", "kvc_gqa_decode_noalloc", "kvc_gqa_decode_ring",
            "kvc_decode_step", "kvc_decode_step_workspace_size", "kvc_window_decode_step",
            "kvc_paged_append", "kvc_gqa_decode_paged",
-           "kvc_gqa_prefill_chunk", "kvc_status_string", "kvc_abi_version")
+           "kvc_gqa_prefill_chunk", "kvc_gqa_prefill_workspace_size", "kvc_status_string",
+           "kvc_abi_version")
 KVC_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -105,7 +106,9 @@ def library() -> ctypes.CDLL:
             "kvc_gqa_decode_noalloc": [P, P, P, P, L, I, I, I, I64, I, I, I, F, P, P, I64, P, P],
             "kvc_window_decode_step": [P, P, P, P, P, P, P, L, I, I, I, I64, I, I, I, I, F, P, P,
                                        I64, P, P],
-            "kvc_gqa_prefill_chunk": [P, P, P, P, I64, L, I, I, I, I, I, I, I, F, P, P, I64, P, P],
+            "kvc_gqa_prefill_chunk": [P, P, P, P, I64, L, I, I, I, I, I, I, I, F, P, P, I64, P, SZ,
+                                      P, P],
+            "kvc_gqa_prefill_workspace_size": [I, I, I, I, I64, I, I, I],
             "kvc_status_string": [I],
             "kvc_abi_version": [],
         }
@@ -115,6 +118,7 @@ def library() -> ctypes.CDLL:
             fn.restype = I
         lib.kvc_gqa_decode_workspace_size.restype = SZ
         lib.kvc_decode_step_workspace_size.restype = SZ
+        lib.kvc_gqa_prefill_workspace_size.restype = SZ
         lib.kvc_status_string.restype = ctypes.c_char_p
         _lib = lib
     return _lib
@@ -300,14 +304,28 @@ def kvc_window_decode_step(out, q, k_cache, v_cache, new_k, new_v, seqlens_k, lo
     return out
 
 
-def kvc_gqa_prefill_chunk(out, q, k_rows, v_rows, lengths, local_window_size=0, scale=0.0,
-                          rope=None, status=None, stream=None):
+def prefill_workspace(q, k_rows, local_window_size=0):
+    """Workspace for kvc_gqa_prefill_chunk's KV split (None when it would
+    not split)."""
     B, Hq, S, D = q.shape
     _, Hkv, R, _ = k_rows.shape
+    n = library().kvc_gqa_prefill_workspace_size(B, Hq, Hkv, S, R, D, _dtype_code(q),
+                                                 local_window_size)
+    return torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+
+
+def kvc_gqa_prefill_chunk(out, q, k_rows, v_rows, lengths, local_window_size=0, scale=0.0,
+                          rope=None, status=None, stream=None, workspace="auto"):
+    """workspace: "auto" allocates what the call can use, None runs unsplit."""
+    B, Hq, S, D = q.shape
+    _, Hkv, R, _ = k_rows.shape
+    if isinstance(workspace, str):
+        workspace = prefill_workspace(q, k_rows, local_window_size)
     cs, sn, rmax = _rope(rope)
     _check("kvc_gqa_prefill_chunk", library().kvc_gqa_prefill_chunk(
         _ptr(out), _ptr(q), _ptr(k_rows), _ptr(v_rows), R, lengths.c(), B, Hq, Hkv, S, D,
-        _dtype_code(q), local_window_size, scale, cs, sn, rmax, _ptr(status), _stream(stream)))
+        _dtype_code(q), local_window_size, scale, cs, sn, rmax, _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _ptr(status), _stream(stream)))
     return out
 
 

@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(kvc):
 
 
 def test_version_and_strings(kvc):
-    assert kvc.kvc_abi_version() == 2
+    assert kvc.kvc_abi_version() == 3
     assert kvc.kvc_status_string(0) == "ok"
     assert "window" in kvc.kvc_status_string(7)
 
@@ -173,10 +173,16 @@ def test_prefill_host_checks(kvc):
     f = lib.kvc_gqa_prefill_chunk
     L = _lengths(kvc)
     base = [FAKE, FAKE * 2, FAKE * 3, FAKE * 4]
-    assert f(*base, 100, L, 2, 8, 2, 0, 64, 1, 0, 0.0, None, None, 0, None, None) == 2  # S = 0
-    assert f(*base, 10, L, 2, 8, 2, 16, 64, 1, 0, 0.0, None, None, 0, None, None) == 6  # R < S
-    assert f(*base, 100, L, 2, 8, 3, 16, 64, 1, 0, 0.0, None, None, 0, None, None) == 2  # heads
-    assert f(*base, 100, L, 2, 8, 2, 16, 64, 9, 0, 0.0, None, None, 0, None, None) == 3  # dtype
+    ws = [None, 0, None, None]  # workspace, bytes, status, stream
+    assert f(*base, 100, L, 2, 8, 2, 0, 64, 1, 0, 0.0, None, None, 0, *ws) == 2  # S = 0
+    assert f(*base, 10, L, 2, 8, 2, 16, 64, 1, 0, 0.0, None, None, 0, *ws) == 6  # R < S
+    assert f(*base, 100, L, 2, 8, 3, 16, 64, 1, 0, 0.0, None, None, 0, *ws) == 2  # heads
+    assert f(*base, 100, L, 2, 8, 2, 16, 64, 9, 0, 0.0, None, None, 0, *ws) == 3  # dtype
+    assert f(*base, 100, L, 2, 8, 2, 16, 64, 1, 0, 0.0, None, None, 0, FAKE + 16, 1 << 20,
+             None, None) == 4                                                  # ws alignment
+    wsz = lib.kvc_gqa_prefill_workspace_size
+    assert wsz(8, 16, 8, 2048, 4096 + 2048, 256, 1, 4096) == 0   # a full grid: no split
+    assert wsz(2, 8, 2, 64, 4096, 128, 0, 0) == 0                # fp32: never split
 
 
 def test_binding_requires_library(monkeypatch, kvc):

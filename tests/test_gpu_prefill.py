@@ -39,7 +39,7 @@ def _oracle_queries(orc, q, k_rows, v_rows, lens, S, window, cos, sin, idx):
 
 
 def _chunk_case(K, orc, dtype, B, Hq, Hkv, D, C, S, P, window, windowed, rope, seed,
-                sample=None):
+                sample=None, workspace="auto"):
     P = np.asarray(P, dtype=np.int64)
     T = P + S
     kc = synth.normal((B, Hkv, C, D), seed, 1, dtype)
@@ -69,7 +69,7 @@ def _chunk_case(K, orc, dtype, B, Hq, Hkv, D, C, S, P, window, windowed, rope, s
         rows_k, rows_v = gk, gv
     out = torch.full((B, Hq, S, D), float("nan"), dtype=dtype, device=dev())
     K.kvc_gqa_prefill_chunk(out, q.to(dev()), rows_k, rows_v, L, local_window_size=window,
-                            rope=rope_d, status=st)
+                            rope=rope_d, status=st, workspace=workspace)
     if windowed:
         K.kvc_window_append(gk, gv, None, None, L, 1, K.KVC_COPY_BACK, ks, vs, rope=rope_d,
                             status=st)
@@ -102,6 +102,25 @@ def _chunk_case(K, orc, dtype, B, Hq, Hkv, D, C, S, P, window, windowed, rope, s
         return assert_close(out, want, tol(dtype), "prefill")
     want = _oracle_queries(orc, qn, rk, rv, lens, S, window, cn, sn, sample)
     return assert_close(out[:, :, list(sample)], want, tol(dtype), "prefill sampled")
+
+
+@pytest.mark.parametrize("D,g,S,W", [(256, 2, 64, 4096), (128, 4, 100, 300), (64, 1, 33, 0)])
+def test_kv_split_and_unsplit(K, orc, D, g, S, W):
+    """Small grids split each query block's keys over several CTAs (the
+    partials merged by a second launch); the same case without a workspace
+    runs unsplit.  Both match the oracle."""
+    Hkv, B = 2, 2
+    C = max(W, 2048)
+    P = [C + 700, 37] if W else [C - S - 5, 37]
+    for ws in ("auto", None):
+        _chunk_case(K, orc, torch.bfloat16, B, Hkv * g, Hkv, D, C, S, P, W, 1 if W else 0,
+                    True, 600 + D, workspace=ws)
+
+
+def test_kv_split_is_used(K):
+    # the small-chunk workload shape asks for a split, the full one does not
+    assert K.library().kvc_gqa_prefill_workspace_size(8, 16, 8, 64, 4096 + 64, 256, 1, 4096) > 0
+    assert K.library().kvc_gqa_prefill_workspace_size(8, 16, 8, 2048, 6144, 256, 1, 4096) == 0
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
