@@ -12,7 +12,9 @@ reclaimed once every gap one-token steps) against the oracle.
   55 rows do not overlap their old places);
 * 32-token chunks at C = W + 8 (the gap is smaller than the chunk: the
   chunk stages from a drifted append point), interleaved with one-token
-  steps.
+  steps;
+* the three windowed decode workloads the benchmark times (compact every
+  step, drifting, ring) at full size through the fused step.
 """
 import numpy as np
 import pytest
@@ -158,4 +160,61 @@ def test_drift_chunks_small_slack(K, orc):
         assert_bytes_equal(gv, wv, f"v cache step {step}")
         assert_close(out, want, 2e-2, f"step {step}")
         T += S
+    assert st.item() == 0
+
+
+@pytest.mark.parametrize("spec", ["WINDOW_DECODE", "WINDOW_DECODE_DRIFT", "WINDOW_DECODE_RING"])
+def test_fused_window_workloads_full_size(K, orc, spec):
+    """The three windowed decode workloads bench.py times (64 x 64/8 heads x
+    64, W = 128; C = 128 compact-every-step, C = 144 drifting, C = 128 ring)
+    at full size through the fused step, 20 consecutive steps from starting
+    totals U[1, 32768]: every cache byte and the lengths after each step, the
+    attention every fifth step and on every step where some row compacts."""
+    w = getattr(synth, spec)
+    policy = w.extra.get("policy", 1)
+    B, Hq, Hkv, D, C, W = w.batch, w.q_heads, w.kv_heads, w.head_dim, w.capacity, w.window
+    steps = 20
+    T0 = synth.randint(w.total_lo, w.total_hi + 1, (B,), 11, 1).numpy()
+    T0[:4] = [1, W - 1, C, C + 1]
+    cos, sin = synth.rope_cache(int(T0.max()) + steps + 1, D, w.theta)
+    rope_d = (cos.to(dev()), sin.to(dev()))
+    kc = synth.normal((B, Hkv, C, D), 12, 1)
+    vc = synth.normal((B, Hkv, C, D), 12, 2)
+    wk, wv = synth.bits(kc).copy(), synth.bits(vc).copy()
+    gk, gv = kc.to(dev()), vc.to(dev())
+    st = status()
+    out = torch.empty(B, Hq, 1, D, dtype=torch.bfloat16, device=dev())
+    Lg = K.Lengths(B, dev())
+    for s in range(steps):
+        T = T0 + s
+        sk = (T - 1).astype(np.int32)
+        nk = synth.normal((B, Hkv, 1, D), 13, s)
+        nv = synth.normal((B, Hkv, 1, D), 14, s)
+        q = synth.normal((B, Hq, 1, D), 15, s)
+        K.kvc_window_decode_step(out, q.to(dev()), gk, gv, nk.to(dev()), nv.to(dev()),
+                                 torch.from_numpy(sk).to(dev()), W, lengths=Lg, rope=rope_d,
+                                 status=st, windowed=policy)
+        lens = orc.seq_lengths(sk, 1, C, policy, W)
+        if policy == orc.RING:
+            orc.ring_append(wk, wv, synth.bits(nk), synth.bits(nv), lens["past_abs"],
+                            cos.numpy(), sin.numpy())
+        else:
+            orc.window_append(wk, wv, synth.bits(nk), synth.bits(nv), lens, 1, cos.numpy(),
+                              sin.numpy())
+        torch.cuda.synchronize()
+        got_len = lengths_np(Lg)
+        for f in Lg.FIELDS:
+            np.testing.assert_array_equal(got_len[f], lens[f], err_msg=f"{f} step {s}")
+        assert_bytes_equal(gk, wk, f"k step {s}")
+        assert_bytes_equal(gv, wv, f"v step {s}")
+        compacting = policy != orc.RING and bool((lens["evict"] > 0).any())
+        if s % 5 == 4 or (policy == orc.DRIFTING and compacting):
+            if policy == orc.RING:
+                want, _ = orc.ring_attention(synth.bits(q), wk, wv, T, W, cos_cache=cos.numpy(),
+                                             sin_cache=sin.numpy())
+            else:
+                want, _ = orc.gqa_attention(synth.bits(q), wk, wv, lens["cache_total"],
+                                            lens["total_abs"], window=W, cos_cache=cos.numpy(),
+                                            sin_cache=sin.numpy())
+            assert_close(out, want, 2e-2, f"{spec} step {s}")
     assert st.item() == 0
