@@ -160,15 +160,28 @@ class Workload:
     e = 2  # bytes per bf16 element
 
     def e2e_setup(self):
+        """The step's inputs travel as one pinned host buffer and one copy:
+        every device input is re-pointed (in place, so the workload keeps
+        using the same tensor objects) at its slice of one device buffer."""
         torch = self.torch
-        self.h_in = [t.pin_memory() for t in self.host_inputs]
+        offs, n = [], 0
+        for t in self.host_inputs:
+            offs.append(n)
+            n += (t.numel() * t.element_size() + 255) // 256 * 256
+        self.h_pack = torch.empty(n, dtype=torch.uint8).pin_memory()
+        dev = self.device_inputs[0].device
+        self.d_pack = torch.empty(n, dtype=torch.uint8, device=dev)
+        for h, d, o in zip(self.host_inputs, self.device_inputs, offs):
+            nb = h.numel() * h.element_size()
+            self.h_pack[o:o + nb].copy_(h.contiguous().view(-1).view(torch.uint8))
+            d.set_(self.d_pack.untyped_storage(), o // d.element_size(), d.shape, d.stride())
+        self.d_pack.copy_(self.h_pack)
         self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        self.h2d = sum(t.numel() * t.element_size() for t in self.h_in)
+        self.h2d = n
         self.d2h = self.h_out.numel() * self.h_out.element_size()
 
     def e2e_step(self, i):
-        for h, d in zip(self.h_in, self.device_inputs):
-            d.copy_(h, non_blocking=True)
+        self.d_pack.copy_(self.h_pack, non_blocking=True)
         self.step(i)
         self.h_out.copy_(self.out, non_blocking=True)
 
