@@ -218,3 +218,74 @@ def test_fused_window_workloads_full_size(K, orc, spec):
                                             sin_cache=sin.numpy())
             assert_close(out, want, 2e-2, f"{spec} step {s}")
     assert st.item() == 0
+
+
+def test_window_workload_256_steps_against_full_history(K, orc):
+    """The windowed decode workload as stated (64 x 64/8 heads x 64, C = W =
+    128, starting totals U[1, 32768], 256 consecutive one-token steps with
+    in-place compaction) through the fused step, checked against attention
+    over the full history: the cache starts as the rotated last min(T0, C)
+    tokens of a per-row history, every new token is appended to that
+    history, and the attention of the final step and of every 32nd step is
+    compared with the attention over the whole history under the window
+    mask (with the cache bytes against the oracle's compaction on every
+    step)."""
+    w = synth.WINDOW_DECODE
+    B, Hq, Hkv, D, C, W = w.batch, w.q_heads, w.kv_heads, w.head_dim, w.capacity, w.window
+    steps = 256
+    T0 = synth.randint(w.total_lo, w.total_hi + 1, (B,), 21, 1).numpy()
+    T0[:3] = [1, C - 1, C]
+    cos, sin = synth.rope_cache(int(T0.max()) + steps + 1, D, w.theta)
+    cn, sn = cos.numpy(), sin.numpy()
+    # per-row history of the last C tokens before the run (rotated K, V),
+    # stored in the cache at [0, min(T0, C)); the rest of the cache is noise
+    n0 = np.minimum(T0, C)
+    hk = synth.bits(synth.normal((B, Hkv, C, D), 22, 1))
+    hv = synth.bits(synth.normal((B, Hkv, C, D), 22, 2))
+    kc = synth.bits(synth.normal((B, Hkv, C, D), 22, 3)).copy()
+    vc = synth.bits(synth.normal((B, Hkv, C, D), 22, 4)).copy()
+    hist_k = [[None] * 0 for _ in range(B)]
+    hist_v = [[None] * 0 for _ in range(B)]
+    for b in range(B):
+        pos = np.arange(T0[b] - n0[b], T0[b])
+        rk = orc.rope_rows(np.ascontiguousarray(hk[b, :, :n0[b]]),
+                           np.tile(pos, Hkv), cn, sn).reshape(Hkv, n0[b], D)
+        kc[b, :, :n0[b]] = rk
+        vc[b, :, :n0[b]] = hv[b, :, :n0[b]]
+        hist_k[b] = [rk[:, j] for j in range(n0[b])]
+        hist_v[b] = [hv[b, :, j] for j in range(n0[b])]
+    wk, wv = kc.copy(), vc.copy()
+    gk = synth.from_bits(kc, torch.bfloat16).to(dev())
+    gv = synth.from_bits(vc, torch.bfloat16).to(dev())
+    rope_d = (cos.to(dev()), sin.to(dev()))
+    st = status()
+    out = torch.empty(B, Hq, 1, D, dtype=torch.bfloat16, device=dev())
+    for s in range(steps):
+        T = T0 + s + 1
+        sk = (T - 1).astype(np.int32)
+        nk = synth.normal((B, Hkv, 1, D), 23, s)
+        nv = synth.normal((B, Hkv, 1, D), 24, s)
+        q = synth.normal((B, Hq, 1, D), 25, s)
+        K.kvc_window_decode_step(out, q.to(dev()), gk, gv, nk.to(dev()), nv.to(dev()),
+                                 torch.from_numpy(sk).to(dev()), W, rope=rope_d, status=st)
+        lens = orc.seq_lengths(sk, 1, C, orc.WINDOWED, W)
+        orc.window_append(wk, wv, synth.bits(nk), synth.bits(nv), lens, 1, cn, sn)
+        nkr = orc.rope_rows(synth.bits(nk)[:, :, 0], np.repeat(T - 1, Hkv), cn, sn)
+        for b in range(B):
+            hist_k[b].append(nkr[b])
+            hist_v[b].append(synth.bits(nv)[b, :, 0])
+        torch.cuda.synchronize()
+        assert_bytes_equal(gk, wk, f"k step {s}")
+        if s % 32 == 31 or s == steps - 1:
+            # the full history's last W tokens are all a window can see
+            n = np.minimum(W, [len(h) for h in hist_k])
+            fk = np.zeros((B, Hkv, W, D), np.uint16)
+            fv = np.zeros_like(fk)
+            for b in range(B):
+                fk[b, :, :n[b]] = np.stack(hist_k[b][-n[b]:], axis=1)
+                fv[b, :, :n[b]] = np.stack(hist_v[b][-n[b]:], axis=1)
+            want, _ = orc.gqa_attention(synth.bits(q), fk, fv, n.astype(np.int32),
+                                        T.astype(np.int32), window=W, cos_cache=cn,
+                                        sin_cache=sn)
+            assert_close(out, want, 2e-2, f"step {s} against the full history")
+    assert st.item() == 0
