@@ -201,6 +201,31 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// 2-D tiled TMA store from shared memory (bulk-group completion); the
+// coordinates must be inside the tensor (never negative)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int32_t x, int32_t y,
+                                             const void *smem_src)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group"
+                 " [%0, {%1, %2}], [%3];" ::"l"(reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(smem_u32(smem_src))
+                 : "memory");
+}
+__device__ __forceinline__ void tma_store_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// waits until every committed TMA store has finished reading shared memory
+__device__ __forceinline__ void tma_store_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// waits until every committed TMA store has completed
+__device__ __forceinline__ void tma_store_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // 3-D tiled TMA load (see tma_load_2d; x is the innermost coordinate)
 __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map, int32_t x,
                                             int32_t y, int32_t z, uint64_t *bar)

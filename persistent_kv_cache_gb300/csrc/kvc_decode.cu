@@ -674,15 +674,17 @@ decode_combine_kernel(const DecodeArgs a, int D)
 // "Design": rows [E, Lp) move to [0, Lp - E) and the new row goes to Lp - E;
 // Lp, E, L from the windowed formula or from the drifting layout of the PR's
 // CPU commit).  One CTA owns one (batch row, kv head) slice and keeps the new
-// window in shared memory: cp.async brings the old rows in at once (from
-// cache row r + E) while the threads rotate the query and the new row.  When
-// rows were evicted the window is then written back E rows lower (all reads
-// have completed, so the in-place move needs no scratch); otherwise only the
-// rows the window can see are loaded and only the new row is stored.  A ring
-// of C slots ("Stateful decode & KV cache", "Sliding-window ring buffer")
-// never moves: window row r is read from slot (T - L + r) mod C and the new
-// row is stored at slot (T - 1) mod C.  The
-// attention runs from shared memory, so the slice is read once, in one launch.
+// window in shared memory.  One thread brings the old rows in with 64-row TMA
+// boxes (window row r from cache row r + E) while the others rotate the query
+// and the new row.  When rows were evicted, the window goes back E rows lower
+// by TMA stores of its full 64-row tiles (and thread stores of a last partial
+// one), drained only before the merge reuses the shared memory, so they
+// overlap the attention; otherwise only the rows the window can see are
+// loaded and only the new row is stored.  A ring of C slots ("Stateful
+// decode & KV cache", "Sliding-window ring buffer") never moves: its slots
+// are loaded in slot order, the new row replaces slot (T - 1) mod C, and the
+// attention masks the slots by position (the visible ones are at most two
+// runs of slots).
 // --------------------------------------------------------------------------
 struct WindowStepArgs {
     void *out;
@@ -707,8 +709,10 @@ __host__ __device__ constexpr int64_t window_step_max_capacity(int D) { return 3
 
 template <typename T, int D>
 __global__ void __launch_bounds__(128, 4)
-window_step_kernel(const WindowStepArgs a)
+window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_v, const WindowStepArgs a)
 {
+    constexpr int BOXES = D / 64;
     constexpr int KT_BYTES = kTile * D * 2;  // one 64-row K (or V) tile
     constexpr int QS = D + 8;
     constexpr int CPR = D / 8;               // 16-byte chunks per row
@@ -720,6 +724,13 @@ window_step_kernel(const WindowStepArgs a)
     const int ntile_max = (int)((C + kTile - 1) / kTile);
     uint8_t *tiles = smem;  // tile t: K at t * 2 * KT_BYTES, V after it
     T *qs = reinterpret_cast<T *>(smem + (size_t)ntile_max * 2 * KT_BYTES);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + (size_t)ntile_max * 2 * KT_BYTES +
+                                                 16 * QS * 2);
+    // byte offset of row r, 16-byte chunk c of the K (is_v = 0) or V tile
+    auto at = [&](bool is_v, int r, int c) {
+        return tiles + (size_t)(r / kTile) * 2 * KT_BYTES + (is_v ? KT_BYTES : 0) +
+               (c >> 3) * 8192 + kvc::sw128(r % kTile, c & 7);
+    };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x / a.kv_heads, kvh = blockIdx.x % a.kv_heads;
@@ -751,126 +762,199 @@ window_step_kernel(const WindowStepArgs a)
         return;
     }
     const int g = a.group;
-    const int vis0 = (a.window > 0 && L > a.window) ? L - a.window : 0;
-    const int64_t slice = (int64_t)b * a.kv_heads + kvh;
-    T *kc = static_cast<T *>(a.k_cache) + slice * C * D;
-    T *vc = static_cast<T *>(a.v_cache) + slice * C * D;
-    const int ntiles = (L + kTile - 1) / kTile;
-
-    // 1. the old rows, straight from cache row r + E (ring: slot
-    //    (T - L + r) mod C) into the swizzled tiles: all of them when they
-    //    move, else only those the window sees; rows not loaded are zeroed
-    //    (a masked row must still be finite for P.V)
     const bool ring = a.policy == KVC_RING;
     const bool moves = !ring && E > 0;
-    const int ring0 = ring ? (int)((T_ - L) % C) : 0;  // slot of window row 0
-    const int r_load0 = moves ? 0 : vis0;
-    const int nchunks = ntiles * kTile * CPR;
-    for (int idx = threadIdx.x; idx < 2 * nchunks; idx += 128) {
-        const bool is_v = idx >= nchunks;
-        const int w = is_v ? idx - nchunks : idx;
-        const int r = w / CPR, c = w % CPR;  // window row, 16-byte chunk
-        uint8_t *dst = tiles + (size_t)(r / kTile) * 2 * KT_BYTES + (is_v ? KT_BYTES : 0) +
-                       (c >> 3) * 8192 + kvc::sw128(r % kTile, c & 7);
-        if (r >= r_load0 && r < L - 1) {
-            int sr = r + E;
-            if (ring) {
-                sr = ring0 + r;
-                sr -= sr >= C ? (int)C : 0;
+    const int nvis = (a.window > 0 && L > a.window) ? a.window : L;  // visible positions
+    const int vis0 = L - nvis;
+    const int64_t slice = (int64_t)b * a.kv_heads + kvh;
+    const int64_t row0 = slice * C;  // the slice's first row in the tensor maps
+    T *kc = static_cast<T *>(a.k_cache) + row0 * D;
+    T *vc = static_cast<T *>(a.v_cache) + row0 * D;
+
+    // Shared-memory rows: the window row r (windowed / drifting), or the slot
+    // s (ring).  new_r: where the new row goes; [t_lo, t_hi): tiles loaded
+    // from the cache (row r from cache row r + src_off).
+    int new_r, t_lo, t_hi, src_off;
+    if (ring) {
+        new_r = (int)((T_ - 1) % C);
+        const int held = (int)(T_ - 1 < C ? T_ - 1 : C);  // slots holding an old token
+        t_lo = 0;
+        t_hi = (held + kTile - 1) / kTile;
+        src_off = 0;
+    } else {
+        new_r = L - 1;
+        t_lo = moves ? 0 : vis0 / kTile;
+        t_hi = (L - 1 + kTile - 1) / kTile;  // rows [0, L - 1) hold old tokens
+        src_off = E;
+    }
+    const int ntiles = ring ? (int)((C + kTile - 1) / kTile) : (L + kTile - 1) / kTile;
+
+    // 1. one thread starts the TMA loads of the old rows
+    if (threadIdx.x == 0) {
+        kvc::mbar_init(bar, 1);
+        kvc::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        kvc::tma_prefetch_desc(&tmap_k);
+        kvc::tma_prefetch_desc(&tmap_v);
+        const uint32_t bytes = t_hi > t_lo ? (uint32_t)(t_hi - t_lo) * 2u * KT_BYTES : 0u;
+        kvc::mbar_arrive_expect_tx(bar, bytes);
+        for (int t = t_lo; t < t_hi; ++t) {
+            const int32_t y = (int32_t)(row0 + src_off + t * kTile);
+#pragma unroll
+            for (int bx = 0; bx < BOXES; ++bx) {
+                kvc::tma_load_2d(tiles + (size_t)t * 2 * KT_BYTES + bx * 8192, &tmap_k, bx * 64,
+                                 y, bar);
+                kvc::tma_load_2d(tiles + (size_t)t * 2 * KT_BYTES + KT_BYTES + bx * 8192,
+                                 &tmap_v, bx * 64, y, bar);
             }
-            const T *src = (is_v ? vc : kc) + (int64_t)sr * D + c * 8;
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(kvc::smem_u32(dst)),
-                         "l"(src)
-                         : "memory");
-        } else if (r != L - 1) {
-            *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
         }
     }
-    asm volatile("cp.async.commit_group;" ::: "memory");
 
-    // 2. meanwhile: the group's query rows rotated at T - 1, and the new row
-    //    (K rotated at P = T - 1, V as given) placed at window row L - 1
+    // 2. meanwhile: the group's query rows rotated at T - 1 into qs, and the
+    //    new row (K rotated at P = T - 1, V as given) into registers
+    const T *nk = static_cast<const T *>(a.new_k) + slice * D;
+    const T *nv = static_cast<const T *>(a.new_v) + slice * D;
+    const float *cs = a.cos_t ? a.cos_t + (int64_t)P * (D / 2) : nullptr;
+    const float *sn = a.cos_t ? a.sin_t + (int64_t)P * (D / 2) : nullptr;
     {
         const T *qg = static_cast<const T *>(a.q) + ((int64_t)b * a.q_heads + kvh * g) * D;
-        const T *nk = static_cast<const T *>(a.new_k) + slice * D;
-        const T *nv = static_cast<const T *>(a.new_v) + slice * D;
-        const float *cs = a.cos_t ? a.cos_t + (int64_t)P * (D / 2) : nullptr;
-        const float *sn = a.cos_t ? a.sin_t + (int64_t)P * (D / 2) : nullptr;
-        const int rl = L - 1;
-        uint8_t *ktl = tiles + (size_t)(rl / kTile) * 2 * KT_BYTES;
-        for (int idx = threadIdx.x; idx < 18 * (D / 2); idx += 128) {
+        for (int idx = threadIdx.x; idx < 16 * (D / 2); idx += 128) {
             const int h = idx / (D / 2), i = idx % (D / 2);
-            if (h < 16) {
-                float lo = 0.f, hi = 0.f;
-                if (h < g) {
-                    lo = kvc::Elem<T>::to_f32(qg[h * D + i]);
-                    hi = kvc::Elem<T>::to_f32(qg[h * D + i + D / 2]);
-                    if (cs)
-                        kvc::rope_pair(lo, hi, cs[i], sn[i]);
-                }
-                qs[h * QS + i] = kvc::Elem<T>::from_f32(lo);
-                qs[h * QS + i + D / 2] = kvc::Elem<T>::from_f32(hi);
-            } else {
-                // h == 16: K pair (i, i + D/2); h == 17: the same V elements
-                const bool is_v = h == 17;
-                T lo_t, hi_t;
-                if (!is_v) {
-                    float lo = kvc::Elem<T>::to_f32(nk[i]), hi = kvc::Elem<T>::to_f32(nk[i + D / 2]);
-                    if (cs)
-                        kvc::rope_pair(lo, hi, cs[i], sn[i]);
-                    lo_t = kvc::Elem<T>::from_f32(lo);
-                    hi_t = kvc::Elem<T>::from_f32(hi);
-                } else {
-                    lo_t = nv[i];
-                    hi_t = nv[i + D / 2];
-                }
-                uint8_t *tb = ktl + (is_v ? KT_BYTES : 0);
-                const int c_lo = i / 8, c_hi = (i + D / 2) / 8;
-                *reinterpret_cast<T *>(tb + (c_lo >> 3) * 8192 + kvc::sw128(rl % kTile, c_lo & 7) +
-                                       (i % 8) * 2) = lo_t;
-                *reinterpret_cast<T *>(tb + (c_hi >> 3) * 8192 + kvc::sw128(rl % kTile, c_hi & 7) +
-                                       ((i + D / 2) % 8) * 2) = hi_t;
+            float lo = 0.f, hi = 0.f;
+            if (h < g) {
+                lo = kvc::Elem<T>::to_f32(qg[h * D + i]);
+                hi = kvc::Elem<T>::to_f32(qg[h * D + i + D / 2]);
+                if (cs)
+                    kvc::rope_pair(lo, hi, cs[i], sn[i]);
             }
+            qs[h * QS + i] = kvc::Elem<T>::from_f32(lo);
+            qs[h * QS + i + D / 2] = kvc::Elem<T>::from_f32(hi);
         }
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    // the new row: thread i < D / 2 owns the pair (i, i + D/2) of K (i < D/2)
+    // or V (threads D/2 .. D - 1); D <= 128 so every pair has a thread
+    T new_lo{}, new_hi{};
+    const bool row_thread = threadIdx.x < D;
+    const bool row_is_v = threadIdx.x >= D / 2;
+    const int row_i = row_is_v ? threadIdx.x - D / 2 : threadIdx.x;
+    if (row_thread) {
+        if (!row_is_v) {
+            float lo = kvc::Elem<T>::to_f32(nk[row_i]), hi = kvc::Elem<T>::to_f32(nk[row_i + D / 2]);
+            if (cs)
+                kvc::rope_pair(lo, hi, cs[row_i], sn[row_i]);
+            new_lo = kvc::Elem<T>::from_f32(lo);
+            new_hi = kvc::Elem<T>::from_f32(hi);
+        } else {
+            new_lo = nv[row_i];
+            new_hi = nv[row_i + D / 2];
+        }
+    }
+
+    // 3. wait for the old rows; place the new row; zero V wherever a row
+    //    that attention might touch holds no token of the window (0 * stale
+    //    bytes must stay 0)
+    bool ok = kvc::mbar_wait(bar, 0);
+    if (!ok) {
+        if (threadIdx.x == 0)
+            kvc::raise_status(a.status, KVC_DEV_TIMEOUT);
+        kvc::mbar_wait(bar, 0);  // let the copies land before the CTA can exit
+        return;
+    }
+    if (row_thread) {
+        const int c_lo = row_i / 8, c_hi = (row_i + D / 2) / 8;
+        *reinterpret_cast<T *>(at(row_is_v, new_r, c_lo) + (row_i % 8) * 2) = new_lo;
+        *reinterpret_cast<T *>(at(row_is_v, new_r, c_hi) + ((row_i + D / 2) % 8) * 2) = new_hi;
+    }
+    {
+        // rows past the window in its last tile; for a ring, the slots never
+        // written (T <= C) and the slots past C
+        int z0, z1;
+        if (ring) {
+            z0 = T_ < C ? (int)T_ : (int)C;
+            z1 = ntiles * kTile;
+        } else {
+            z0 = L;
+            z1 = ntiles * kTile;
+        }
+        const int n = (z1 - z0) * CPR;
+        for (int idx = threadIdx.x; idx < n; idx += 128) {
+            const int r = z0 + idx / CPR, c = idx % CPR;
+            *reinterpret_cast<uint4 *>(at(true, r, c)) = make_uint4(0, 0, 0, 0);
+        }
+    }
+    kvc::fence_proxy_async_smem();
     __syncthreads();
 
-    // 3. write the window back: every row E lower when rows were evicted,
-    //    otherwise only the new row (at Lp, or a ring's slot (T - 1) mod C).
-    //    All reads of the old rows are complete, so the in-place move needs
-    //    no scratch.
-    {
-        const int r_first = moves ? 0 : L - 1;
+    // 4. write back: the whole window E rows lower when rows moved (full
+    //    64-row tiles by TMA store, a last partial tile by the threads),
+    //    otherwise the new row alone
+    int stored_tiles = 0;
+    if (moves) {
+        stored_tiles = L / kTile;
+        if (threadIdx.x == 0 && stored_tiles > 0) {
+            for (int t = 0; t < stored_tiles; ++t) {
+                const int32_t y = (int32_t)(row0 + t * kTile);
+#pragma unroll
+                for (int bx = 0; bx < BOXES; ++bx) {
+                    kvc::tma_store_2d(&tmap_k, bx * 64, y,
+                                      tiles + (size_t)t * 2 * KT_BYTES + bx * 8192);
+                    kvc::tma_store_2d(&tmap_v, bx * 64, y,
+                                      tiles + (size_t)t * 2 * KT_BYTES + KT_BYTES + bx * 8192);
+                }
+            }
+            kvc::tma_store_commit();
+        }
+        const int r_first = stored_tiles * kTile;
         const int n = (L - r_first) * CPR;
-        const int new_dst = ring ? (int)((T_ - 1) % C) : L - 1;
         for (int idx = threadIdx.x; idx < 2 * n; idx += 128) {
             const bool is_v = idx >= n;
             const int w = is_v ? idx - n : idx;
             const int r = r_first + w / CPR, c = w % CPR;
-            const uint8_t *src = tiles + (size_t)(r / kTile) * 2 * KT_BYTES + (is_v ? KT_BYTES : 0) +
-                                 (c >> 3) * 8192 + kvc::sw128(r % kTile, c & 7);
-            const int dr = r == L - 1 ? new_dst : r;
-            *reinterpret_cast<uint4 *>((is_v ? vc : kc) + (int64_t)dr * D + c * 8) =
-                *reinterpret_cast<const uint4 *>(src);
+            *reinterpret_cast<uint4 *>((is_v ? vc : kc) + (int64_t)r * D + c * 8) =
+                *reinterpret_cast<const uint4 *>(at(is_v, r, c));
         }
+    } else if (row_thread) {
+        T *dst = (row_is_v ? vc : kc) + (int64_t)new_r * D;
+        dst[row_i] = new_lo;
+        dst[row_i + D / 2] = new_hi;
     }
 
-    // 4. attention over the window held in shared memory
+    // 5. attention over the rows the window sees
     GroupAttn<T, D> ga;
     ga.init();
     ga.load_q(qs, QS, lane);
-    for (int t = 0; t < ntiles; ++t) {
-        const int t0 = t * kTile;
-        const int lo = min(16, max(0, vis0 - t0 - 16 * warp));
-        const int hi = min(16, max(0, L - t0 - 16 * warp));
-        const uint32_t kb = kvc::smem_u32(tiles + (size_t)t * 2 * KT_BYTES);
-        if (hi > lo)
-            ga.tile(kb, kb + KT_BYTES, warp, lane, lo, hi, a.scale_log2);
+    // visible rows: [vis0, L) of the window, or for a ring the nvis slots
+    // ending at new_r (one run, or [0, new_r] and [C - rest, C))
+    int lo1 = vis0, hi1 = L, lo2 = 0, hi2 = 0;
+    if (ring) {
+        const int first = new_r - nvis + 1;
+        if (first >= 0) {
+            lo1 = first;
+            hi1 = new_r + 1;
+        } else {
+            lo1 = 0;
+            hi1 = new_r + 1;
+            lo2 = (int)C + first;
+            hi2 = (int)C;
+        }
     }
+    for (int t = 0; t < ntiles; ++t) {
+        const int r0 = t * kTile + 16 * warp;  // this warp's 16 rows of the tile
+        const uint32_t kb = kvc::smem_u32(tiles + (size_t)t * 2 * KT_BYTES);
+        const int l1 = min(16, max(0, lo1 - r0)), h1 = min(16, max(0, hi1 - r0));
+        const int l2 = min(16, max(0, lo2 - r0)), h2 = min(16, max(0, hi2 - r0));
+        if (h1 > l1)
+            ga.tile(kb, kb + KT_BYTES, warp, lane, l1, h1, a.scale_log2);
+        if (h2 > l2)
+            ga.tile(kb, kb + KT_BYTES, warp, lane, l2, h2, a.scale_log2);
+    }
+    if (threadIdx.x == 0 && stored_tiles > 0)
+        kvc::tma_store_wait_read();  // the merge below reuses the tiles' memory
     __syncthreads();
 
-    // 5. merge the four warps and write the group's output rows
+    // 6. merge the four warps and write the group's output rows
     float *cm = reinterpret_cast<float *>(smem);
     float *cl = cm + kConsumers * 16;
     float *co = cl + kConsumers * 16;
@@ -883,6 +967,8 @@ window_step_kernel(const WindowStepArgs a)
         const int64_t qrow = (int64_t)b * a.q_heads + kvh * g + h;
         static_cast<T *>(a.out)[qrow * D + d] = kvc::Elem<T>::from_f32(osum / lsum);
     }
+    if (threadIdx.x == 0 && stored_tiles > 0)
+        kvc::tma_store_wait_all();  // the window's stores complete before the CTA retires
 }
 
 } // namespace
@@ -1390,14 +1476,24 @@ template <typename T, int D>
 kvc_status launch_window_step(const WindowStepArgs &a, int batch, cudaStream_t stream)
 {
     const int64_t ntile_max = (a.capacity + kTile - 1) / kTile;
-    size_t smem = 1024 + (size_t)ntile_max * 2 * kTile * D * 2 + 16 * (D + 8) * 2;
+    size_t smem = 1024 + (size_t)ntile_max * 2 * kTile * D * 2 + 16 * (D + 8) * 2 + 16;
     const size_t merge = 1024 + kConsumers * 16 * (2 + D) * sizeof(float);
     smem = smem > merge ? smem : merge;
+    const CUtensorMapDataType tt = std::is_same<T, __half>::value
+                                       ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint64_t rows = (uint64_t)batch * a.kv_heads * a.capacity;
+    if (rows > (uint64_t)INT32_MAX)
+        return KVC_ERR_SHAPE;
+    CUtensorMap tk, tv;
+    if (!kvc_host::encode_2d_bf16_sw128(&tk, a.k_cache, rows, D, kTile, tt) ||
+        !kvc_host::encode_2d_bf16_sw128(&tv, a.v_cache, rows, D, kTile, tt))
+        return KVC_ERR_CUDA;
     auto kern = window_step_kernel<T, D>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return KVC_ERR_CUDA;
-    kern<<<(unsigned)(batch * a.kv_heads), 128, smem, stream>>>(a);
+    kern<<<(unsigned)(batch * a.kv_heads), 128, smem, stream>>>(tk, tv, a);
     return kvc_host::launch_status();
 }
 
