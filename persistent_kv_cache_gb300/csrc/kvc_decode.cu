@@ -734,6 +734,35 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x / a.kv_heads, kvh = blockIdx.x % a.kv_heads;
+    const int g = a.group;
+    const int64_t slice = (int64_t)b * a.kv_heads + kvh;
+
+    // 0. what does not depend on the lengths is loaded at once, beside
+    //    seqlens_k: the group's query pairs (i, i + D/2) and the new row
+    //    (thread i < D/2 holds a K pair, D/2 <= i < D a V pair)
+    constexpr int QPT = 16 * (D / 2) / 128;  // query pairs per thread
+    T q_lo[QPT], q_hi[QPT];
+    {
+        const T *qg = static_cast<const T *>(a.q) + ((int64_t)b * a.q_heads + kvh * g) * D;
+#pragma unroll
+        for (int j = 0; j < QPT; ++j) {
+            const int idx = threadIdx.x + 128 * j;
+            const int h = idx / (D / 2), i = idx % (D / 2);
+            q_lo[j] = h < g ? qg[h * D + i] : T{};
+            q_hi[j] = h < g ? qg[h * D + i + D / 2] : T{};
+        }
+    }
+    const bool row_thread = threadIdx.x < D;
+    const bool row_is_v = threadIdx.x >= D / 2;
+    const int row_i = row_is_v ? threadIdx.x - D / 2 : threadIdx.x;
+    T new_lo{}, new_hi{};
+    if (row_thread) {
+        const T *src = (row_is_v ? static_cast<const T *>(a.new_v)
+                                 : static_cast<const T *>(a.new_k)) + slice * D;
+        new_lo = src[row_i];
+        new_hi = src[row_i + D / 2];
+    }
+
     const int64_t T_ = (int64_t)a.seqlens_k[b] + 1;
     const bool write_len = kvh == 0 && threadIdx.x == 0 && a.len.cache_total != nullptr;
     if (T_ < 1 || T_ > (int64_t)INT32_MAX) {
@@ -761,12 +790,10 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
             kvc::raise_status(a.status, KVC_DEV_ROPE_RANGE);
         return;
     }
-    const int g = a.group;
     const bool ring = a.policy == KVC_RING;
     const bool moves = !ring && E > 0;
     const int nvis = (a.window > 0 && L > a.window) ? a.window : L;  // visible positions
     const int vis0 = L - nvis;
-    const int64_t slice = (int64_t)b * a.kv_heads + kvh;
     const int64_t row0 = slice * C;  // the slice's first row in the tensor maps
     T *kc = static_cast<T *>(a.k_cache) + row0 * D;
     T *vc = static_cast<T *>(a.v_cache) + row0 * D;
@@ -812,44 +839,25 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
     }
 
-    // 2. meanwhile: the group's query rows rotated at T - 1 into qs, and the
-    //    new row (K rotated at P = T - 1, V as given) into registers
-    const T *nk = static_cast<const T *>(a.new_k) + slice * D;
-    const T *nv = static_cast<const T *>(a.new_v) + slice * D;
+    // 2. meanwhile: the query rows and the new K row rotated at P = T - 1
+    //    (the cos/sin rows are the only loads that needed the lengths)
     const float *cs = a.cos_t ? a.cos_t + (int64_t)P * (D / 2) : nullptr;
     const float *sn = a.cos_t ? a.sin_t + (int64_t)P * (D / 2) : nullptr;
-    {
-        const T *qg = static_cast<const T *>(a.q) + ((int64_t)b * a.q_heads + kvh * g) * D;
-        for (int idx = threadIdx.x; idx < 16 * (D / 2); idx += 128) {
-            const int h = idx / (D / 2), i = idx % (D / 2);
-            float lo = 0.f, hi = 0.f;
-            if (h < g) {
-                lo = kvc::Elem<T>::to_f32(qg[h * D + i]);
-                hi = kvc::Elem<T>::to_f32(qg[h * D + i + D / 2]);
-                if (cs)
-                    kvc::rope_pair(lo, hi, cs[i], sn[i]);
-            }
-            qs[h * QS + i] = kvc::Elem<T>::from_f32(lo);
-            qs[h * QS + i + D / 2] = kvc::Elem<T>::from_f32(hi);
-        }
+#pragma unroll
+    for (int j = 0; j < QPT; ++j) {
+        const int idx = threadIdx.x + 128 * j;
+        const int h = idx / (D / 2), i = idx % (D / 2);
+        float lo = kvc::Elem<T>::to_f32(q_lo[j]), hi = kvc::Elem<T>::to_f32(q_hi[j]);
+        if (cs && h < g)
+            kvc::rope_pair(lo, hi, cs[i], sn[i]);
+        qs[h * QS + i] = kvc::Elem<T>::from_f32(lo);
+        qs[h * QS + i + D / 2] = kvc::Elem<T>::from_f32(hi);
     }
-    // the new row: thread i < D / 2 owns the pair (i, i + D/2) of K (i < D/2)
-    // or V (threads D/2 .. D - 1); D <= 128 so every pair has a thread
-    T new_lo{}, new_hi{};
-    const bool row_thread = threadIdx.x < D;
-    const bool row_is_v = threadIdx.x >= D / 2;
-    const int row_i = row_is_v ? threadIdx.x - D / 2 : threadIdx.x;
-    if (row_thread) {
-        if (!row_is_v) {
-            float lo = kvc::Elem<T>::to_f32(nk[row_i]), hi = kvc::Elem<T>::to_f32(nk[row_i + D / 2]);
-            if (cs)
-                kvc::rope_pair(lo, hi, cs[row_i], sn[row_i]);
-            new_lo = kvc::Elem<T>::from_f32(lo);
-            new_hi = kvc::Elem<T>::from_f32(hi);
-        } else {
-            new_lo = nv[row_i];
-            new_hi = nv[row_i + D / 2];
-        }
+    if (row_thread && !row_is_v && cs) {
+        float lo = kvc::Elem<T>::to_f32(new_lo), hi = kvc::Elem<T>::to_f32(new_hi);
+        kvc::rope_pair(lo, hi, cs[row_i], sn[row_i]);
+        new_lo = kvc::Elem<T>::from_f32(lo);
+        new_hi = kvc::Elem<T>::from_f32(hi);
     }
 
     // 3. wait for the old rows; place the new row; zero V wherever a row
