@@ -452,7 +452,8 @@ kvc_status kvc_window_decode_step(void *out, const void *q, void *k_cache, void 
  *                 results up to floating-point rounding order.
  * Supported: KVC_BF16/KVC_F16 with head_dim in {64, 128, 256} and
  * q_heads / kv_heads in {1, 2, 4, 8, 16} (tcgen05 tensor-core path);
- * KVC_F32 with head_dim <= 256 (no workspace used).  Buffers 16-byte aligned.
+ * KVC_F32 with head_dim <= 256 (no workspace used).  Buffers, the rope
+ * tables included, 16-byte aligned (KVC_ERR_ALIGN).
  */
 kvc_status kvc_gqa_prefill_chunk(void *out, const void *q, const void *k_rows, const void *v_rows,
                                  int64_t rows_per_head, kvc_lengths len, int batch, int q_heads,

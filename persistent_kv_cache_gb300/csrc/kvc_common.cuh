@@ -211,6 +211,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int32_t x, 
                  "r"(x), "r"(y), "r"(smem_u32(smem_src))
                  : "memory");
 }
+// 4-D tiled TMA store (see tma_store_2d)
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, int32_t x, int32_t y,
+                                             int32_t z, int32_t w, const void *smem_src)
+{
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group"
+                 " [%0, {%1, %2, %3, %4}], [%5];" ::"l"(reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(smem_src))
+                 : "memory");
+}
 __device__ __forceinline__ void tma_store_commit()
 {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
@@ -288,6 +297,14 @@ bool encode_2d_bf16_sw128(CUtensorMap *map, const void *base, uint64_t rows, uin
 // lands in shared memory as box_blocks consecutive [box_rows][128 B] blocks
 bool encode_3d_sw128(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                      uint32_t box_rows, uint32_t box_blocks, CUtensorMapDataType type);
+
+// 4-D view of a [heads, rows, cols] tensor of elem_bytes-wide elements as
+// (128-byte column span, rows, cols / span column blocks, heads) with
+// 128-byte swizzle; a box of (span, box_rows, every block, box_heads) lands in
+// shared memory as [box_heads][blocks][box_rows][128 B]
+bool encode_4d_heads_sw128(CUtensorMap *map, const void *base, uint64_t heads, uint64_t rows,
+                           uint64_t cols, uint32_t elem_bytes, uint32_t box_rows,
+                           uint32_t box_heads, CUtensorMapDataType type);
 
 } // namespace kvc_host
 

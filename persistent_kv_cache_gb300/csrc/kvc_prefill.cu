@@ -9,7 +9,8 @@
 // K/V tile is read once for all heads of the group.  Key tiles are 128 rows.
 //
 //   TMEM columns  O [0, D) fp32 | S/P double buffer [D, D + 256)
-//   shared mem    Q tile (128 x D, 128-byte swizzled) | ring of 16 KB slabs
+//   shared mem    Q tile (128 x D, 128-byte swizzled) | ring of K/V slabs;
+//                 the output tile is staged over both at the end
 //   warp 0        allocates tensor memory and issues tcgen05.mma in the order
 //                 S_0, S_1, PV_0, S_2, PV_1, ...:
 //                   S_j = Q K_j^T   A = Q (shared), B = K slabs (K-major)
@@ -23,7 +24,8 @@
 //                 running max is only raised when it grows by more than 2^8,
 //                 exact after the final division), write P_j as 16-bit pairs
 //                 over S_j, rescale its half of O when the max moved, and at
-//                 the end divide by l and store its half of the output row.
+//                 the end divide by l and stage its half of the output row
+//                 in shared memory; one TMA store writes the block's tile.
 //   warp 9        TMA producer: streams the K and V slabs into the ring in
 //                 the order the tensor pipe consumes them (K_0, K_1, V_0,
 //                 K_2, V_1, ...), one 3-D box of up to 32 KB per slot (the
@@ -46,6 +48,7 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = 32 * (1 + kSoftmaxWarps + 1);  // MMA, softmax x 8, TMA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr uint32_t kEpilogueBar = 5;       // named barrier of the softmax warps (1-4: pairs)
 
 // ---------------- tcgen05 helpers (inline PTX) ----------------
 
@@ -204,6 +207,13 @@ __host__ __device__ constexpr uint32_t f16_idesc(uint32_t ab_type, uint32_t b_mn
            ((M >> 4) << 24);
 }
 
+// One lane's share of a query row when a warp's 32 lanes cover the D/2
+// rotation pairs: N 16-bit values (q) and N floats (f) per half row.
+template <int N> struct QuarterRow;
+template <> struct QuarterRow<4> { using q = uint2;          using f = float4; };
+template <> struct QuarterRow<2> { using q = uint32_t;       using f = float2; };
+template <> struct QuarterRow<1> { using q = unsigned short; using f = float; };
+
 struct PrefillArgs {
     void *out;
     const void *q;
@@ -243,6 +253,10 @@ template <int D> struct PrefillSmem {
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;  // tmem addr, abort flag
     static constexpr int RED_OFF = MISC_OFF + 16;        // row max / sum exchange, 4 x 128 floats
     static constexpr int TOTAL = RED_OFF + 4 * kBM * 4;
+    // the epilogue stages the output tile (16-bit, or the fp32 partial of a
+    // KV split) over the Q tile and the ring, which are free by then
+    static constexpr int O_OFF = Q_OFF;
+    static_assert(kBM * D * 4 <= RING_OFF + NSLAB * SLAB, "fp32 output tile must fit");
     // TMEM columns: O [0, D) fp32 | S/P double buffer [D, D + 256)
     static constexpr uint32_t COL_O = 0, COL_S = D;
     static constexpr uint32_t TMEM_COLS = 512;
@@ -295,7 +309,8 @@ __device__ __forceinline__ void slab_group(int g, int ntiles, bool &is_v, int &t
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                  const __grid_constant__ CUtensorMap tmap_v, const PrefillArgs a)
+                  const __grid_constant__ CUtensorMap tmap_v,
+                  const __grid_constant__ CUtensorMap tmap_o, const PrefillArgs a)
 {
     using SM = PrefillSmem<D>;
     constexpr int BOXES = D / 64;
@@ -517,35 +532,66 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         float *red = reinterpret_cast<float *>(smem + SM::RED_OFF);  // [2 tiles][2 halves][128]
         const uint32_t pair_bar = 1 + quad;       // named barrier of the two warps of a quadrant
 
-        // query row: rotate at absolute position P + ii and stage it as 16-bit
-        // in the swizzled Q tile (row m of each 64-column box); each half
-        // takes half of the rotation pairs (i, i + D/2)
+        // query tile: row r is rotated at absolute position P + (its query)
+        // and staged as 16-bit in the swizzled Q tile (row r of each
+        // 64-column box).  The tensor pipe waits on this, so the loads are
+        // coalesced: a warp takes 16 rows, one row at a time, its lanes
+        // spread along D (lane l owns the rotation pairs (c, c + D/2) for
+        // c in [PPL*l, PPL*l + PPL)), and the loads of QRB rows go out
+        // together.
         {
-            const T *qsrc = static_cast<const T *>(a.q) + qrow * D;
-            const float *cs = (a.cos_t && row_valid) ? a.cos_t + (int64_t)(P + ii) * (D / 2) : nullptr;
-            const float *sn = (a.cos_t && row_valid) ? a.sin_t + (int64_t)(P + ii) * (D / 2) : nullptr;
+            using QVec = typename QuarterRow<D / 64>::q;
+            using FVec = typename QuarterRow<D / 64>::f;
+            constexpr int PPL = D / 64;
+            constexpr int ROWS = kBM / kSoftmaxWarps;
+            constexpr int QRB = 8;
             uint8_t *qt = smem + SM::Q_OFF;
+            const int c0 = PPL * lane;
+            const uint32_t off_lo = (uint32_t)(c0 >> 6) * (kBM * 128), sub = (uint32_t)(c0 & 7) * 2;
+            const uint32_t off_hi = (uint32_t)((D / 2 + c0) >> 6) * (kBM * 128);
+            const uint32_t ch_lo = (uint32_t)(c0 & 63) >> 3, ch_hi = (uint32_t)((D / 2 + c0) & 63) >> 3;
 #pragma unroll 1
-            for (int c = half * (D / 32); c < (half + 1) * (D / 32); ++c) {
-                uint4 lo4 = make_uint4(0, 0, 0, 0), hi4 = make_uint4(0, 0, 0, 0);
-                if (row_valid) {
-                    lo4 = *reinterpret_cast<const uint4 *>(qsrc + c * 8);
-                    hi4 = *reinterpret_cast<const uint4 *>(qsrc + D / 2 + c * 8);
-                }
-                if (cs) {
-                    T *lv = reinterpret_cast<T *>(&lo4);
-                    T *hv = reinterpret_cast<T *>(&hi4);
+            for (int rb = 0; rb < ROWS; rb += QRB) {
+                QVec lo[QRB], hi[QRB];
+                FVec cv[QRB], sv[QRB];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        float x = kvc::Elem<T>::to_f32(lv[e]), y = kvc::Elem<T>::to_f32(hv[e]);
-                        kvc::rope_pair(x, y, cs[c * 8 + e], sn[c * 8 + e]);
-                        lv[e] = kvc::Elem<T>::from_f32(x);
-                        hv[e] = kvc::Elem<T>::from_f32(y);
+                for (int u = 0; u < QRB; ++u) {
+                    const int mr = sw * ROWS + rb + u;
+                    const int hr = mr / QB, ir = q0 + (mr - hr * QB);
+                    lo[u] = QVec{};
+                    hi[u] = QVec{};
+                    if (ir < S && hr < g) {
+                        const T *src = static_cast<const T *>(a.q) +
+                                       (((int64_t)b * a.q_heads + kvh * g + hr) * S + ir) * D;
+                        lo[u] = *reinterpret_cast<const QVec *>(src + c0);
+                        hi[u] = *reinterpret_cast<const QVec *>(src + D / 2 + c0);
+                        if (a.cos_t) {
+                            const int64_t o = (int64_t)(P + ir) * (D / 2) + c0;
+                            cv[u] = *reinterpret_cast<const FVec *>(a.cos_t + o);
+                            sv[u] = *reinterpret_cast<const FVec *>(a.sin_t + o);
+                        }
                     }
                 }
-                const int clo = c, chi = D / 16 + c;  // 16-byte chunk index along D
-                *reinterpret_cast<uint4 *>(qt + (clo >> 3) * (kBM * 128) + kvc::sw128(m, clo & 7)) = lo4;
-                *reinterpret_cast<uint4 *>(qt + (chi >> 3) * (kBM * 128) + kvc::sw128(m, chi & 7)) = hi4;
+#pragma unroll
+                for (int u = 0; u < QRB; ++u) {
+                    const int mr = sw * ROWS + rb + u;
+                    const int hr = mr / QB, ir = q0 + (mr - hr * QB);
+                    if (a.cos_t && ir < S && hr < g) {
+                        T *lv = reinterpret_cast<T *>(&lo[u]);
+                        T *hv = reinterpret_cast<T *>(&hi[u]);
+                        const float *cf = reinterpret_cast<const float *>(&cv[u]);
+                        const float *sf = reinterpret_cast<const float *>(&sv[u]);
+#pragma unroll
+                        for (int e = 0; e < PPL; ++e) {
+                            float x = kvc::Elem<T>::to_f32(lv[e]), y = kvc::Elem<T>::to_f32(hv[e]);
+                            kvc::rope_pair(x, y, cf[e], sf[e]);
+                            lv[e] = kvc::Elem<T>::from_f32(x);
+                            hv[e] = kvc::Elem<T>::from_f32(y);
+                        }
+                    }
+                    *reinterpret_cast<QVec *>(qt + off_lo + kvc::sw128(mr, ch_lo) + sub) = lo[u];
+                    *reinterpret_cast<QVec *>(qt + off_hi + kvc::sw128(mr, ch_hi) + sub) = hi[u];
+                }
             }
             kvc::fence_proxy_async_smem();
             __syncwarp();
@@ -680,58 +726,74 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 kvc::mbar_arrive(&p_full[s]);
         }
 
-        // epilogue: combine the two halves' sums, wait for the last PV,
-        // divide by l and store my half of the output row
+        // epilogue: combine the two halves' sums, wait for the last PV, then
+        // stage my half of the row in shared memory, where the Q tile and
+        // the ring were (every MMA that read them has completed once the
+        // last PV has), in the output box's order [head][column block]
+        // [query][128 B] (128-byte swizzled), and one thread stores the tile
+        // with a single TMA store that clips the queries past S.
         // (the buffer of parity ntiles & 1 was last read before the final tile's barrier)
         red[((ntiles & 1) * 2 + half) * kBM + m] = l_run;
         named_bar_sync(pair_bar, 64);
         const float l_tot = l_run + red[((ntiles & 1) * 2 + (half ^ 1)) * kBM + m];
-        if (ok && ntiles > 0 &&
-            wait_or_abort(&o_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_flag,
-                          a.status)) {
+        const bool have_o = ok && wait_or_abort(&o_done[(ntiles - 1) & 1],
+                                                ((ntiles - 1) >> 1) & 1, abort_flag, a.status);
+        const int r_in = m - hh * QB;  // query of this row within the block
+        if (have_o) {
             tc_fence_after();
             if (a.nsplit == 1) {
+                // 16-bit output: a 128-byte row holds 64 columns
                 const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-                T *dst = static_cast<T *>(a.out) + qrow * D;
 #pragma unroll 1
                 for (int cc = half * (D / 2); cc < (half + 1) * (D / 2); cc += 32) {
                     float o[32];
                     tmem_ld32(lane_addr + COL_O + cc, o);
-                    if (row_valid) {
 #pragma unroll
-                        for (int c = 0; c < 32; c += 8) {
-                            uint4 pkt;
-                            T *e = reinterpret_cast<T *>(&pkt);
+                    for (int c = 0; c < 32; c += 8) {
+                        uint4 pkt;
+                        T *e = reinterpret_cast<T *>(&pkt);
 #pragma unroll
-                            for (int u = 0; u < 8; ++u)
-                                e[u] = kvc::Elem<T>::from_f32(o[c + u] * inv);
-                            *reinterpret_cast<uint4 *>(dst + cc + c) = pkt;
-                        }
+                        for (int u = 0; u < 8; ++u)
+                            e[u] = kvc::Elem<T>::from_f32(o[c + u] * inv);
+                        const int col = cc + c;
+                        const uint32_t row = (uint32_t)((hh * (D / 64) + (col >> 6)) * QB + r_in);
+                        *reinterpret_cast<uint4 *>(smem + SM::O_OFF + kvc::sw128(row, (col & 63) >> 3)) = pkt;
                     }
                 }
             } else {
-                // this split's partial: o unnormalised, l, and the reference
-                // max m (log2 units) that o and l are relative to
-                const int64_t pr = split * rows_total + qrow;
-                float *dst = a.ws_o + pr * D;
+                // this split's partial, fp32: o unnormalised (a 128-byte row
+                // holds 32 columns), l, and the reference max m (log2 units)
+                // that o and l are relative to
 #pragma unroll 1
                 for (int cc = half * (D / 2); cc < (half + 1) * (D / 2); cc += 32) {
                     float o[32];
                     tmem_ld32(lane_addr + COL_O + cc, o);
-                    if (row_valid) {
 #pragma unroll
-                        for (int c = 0; c < 32; c += 4)
-                            *reinterpret_cast<float4 *>(dst + cc + c) =
-                                make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+                    for (int c = 0; c < 32; c += 4) {
+                        const int col = cc + c;
+                        const uint32_t row = (uint32_t)((hh * (D / 32) + (col >> 5)) * QB + r_in);
+                        *reinterpret_cast<float4 *>(smem + SM::O_OFF + kvc::sw128(row, (col & 31) >> 2)) =
+                            make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
                     }
                 }
                 if (row_valid && half == 0) {
+                    const int64_t pr = split * rows_total + qrow;
                     a.ws_m[pr] = m_run;
                     a.ws_l[pr] = l_tot;
                 }
             }
         }
         tc_fence_before();
+        kvc::fence_proxy_async_smem();
+        named_bar_sync(kEpilogueBar, 32 * kSoftmaxWarps);
+        if (sw == 0 && lane == 0 && !*abort_flag) {
+            // a failed wait anywhere raised the abort flag: then nothing is stored
+            const int head0 = b * a.q_heads + kvh * g;
+            const int h = a.nsplit == 1 ? head0 : split * a.batch * a.q_heads + head0;
+            kvc::tma_store_4d(&tmap_o, 0, q0, 0, h, smem + SM::O_OFF);
+            kvc::tma_store_commit();
+            kvc::tma_store_wait_all();
+        }
     }
 
     __syncthreads();
@@ -830,7 +892,7 @@ kvc_status launch_prefill_tc(void *out, const void *q, const void *k_rows, const
     const CUtensorMapDataType tt = std::is_same<T, __half>::value
                                        ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    CUtensorMap tk, tv;
+    CUtensorMap tk, tv, to;
     if (!kvc_host::encode_3d_sw128(&tk, k_rows, rows, D, kBN, SM::DB, tt) ||
         !kvc_host::encode_3d_sw128(&tv, v_rows, rows, D, SM::KPS, D / 64, tt))
         return KVC_ERR_CUDA;
@@ -870,9 +932,19 @@ kvc_status launch_prefill_tc(void *out, const void *q, const void *k_rows, const
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return KVC_ERR_CUDA;
+    // the output tile store: [batch * q_heads, S, D] 16-bit, or the fp32
+    // partials [nsplit * batch * q_heads, S, D]; a box is one query block of
+    // every head of a group
+    const bool part = a.nsplit > 1;
+    if (!kvc_host::encode_4d_heads_sw128(
+            &to, part ? static_cast<void *>(a.ws_o) : out,
+            (uint64_t)(part ? a.nsplit : 1) * batch * q_heads, (uint64_t)S, D, part ? 4 : 2,
+            (uint32_t)a.qb_rows, (uint32_t)a.group,
+            part ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : tt))
+        return KVC_ERR_CUDA;
     const int qblocks = (S + a.qb_rows - 1) / a.qb_rows;
     dim3 grid(qblocks * a.nsplit, kv_heads, batch);
-    kern<<<grid, kThreads, smem, stream>>>(tk, tv, a);
+    kern<<<grid, kThreads, smem, stream>>>(tk, tv, to, a);
     if (a.nsplit > 1)
         prefill_combine_kernel<T, D><<<(unsigned)((rows_total + 3) / 4), 128, 0, stream>>>(a);
     return kvc_host::launch_status();
@@ -953,6 +1025,8 @@ KVC_API kvc_status kvc_gqa_prefill_chunk(void *out, const void *q, const void *k
     for (const void *p : {(const void *)out, q, k_rows, v_rows})
         if (!kvc_host::aligned16(p))
             return KVC_ERR_ALIGN;
+    if (rope_cos && (!kvc_host::aligned16(rope_cos) || !kvc_host::aligned16(rope_sin)))
+        return KVC_ERR_ALIGN;
     if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return KVC_ERR_ALIGN;
     if (scale == 0.f)

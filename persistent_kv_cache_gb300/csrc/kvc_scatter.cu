@@ -154,6 +154,26 @@ bool encode_2d_bf16_sw128(CUtensorMap *map, const void *base, uint64_t rows, uin
     return r == CUDA_SUCCESS;
 }
 
+bool encode_4d_heads_sw128(CUtensorMap *map, const void *base, uint64_t heads, uint64_t rows,
+                           uint64_t cols, uint32_t elem_bytes, uint32_t box_rows,
+                           uint32_t box_heads, CUtensorMapDataType type)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn || elem_bytes == 0 || 128 % elem_bytes != 0)
+        return false;
+    const uint64_t span = 128 / elem_bytes;
+    if (cols % span != 0)
+        return false;
+    cuuint64_t dims[4] = {span, rows, cols / span, heads};
+    cuuint64_t strides[3] = {cols * elem_bytes, 128, rows * cols * elem_bytes};
+    cuuint32_t box[4] = {(cuuint32_t)span, box_rows, (cuuint32_t)(cols / span), box_heads};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, type, 4, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 } // namespace kvc_host
 
 KVC_API kvc_status kvc_tensor_scatter(void *present_cache, const void *past_cache,

@@ -180,6 +180,10 @@ def test_prefill_host_checks(kvc):
     assert f(*base, 100, L, 2, 8, 2, 16, 64, 9, 0, 0.0, None, None, 0, *ws) == 3  # dtype
     assert f(*base, 100, L, 2, 8, 2, 16, 64, 1, 0, 0.0, None, None, 0, FAKE + 16, 1 << 20,
              None, None) == 4                                                  # ws alignment
+    assert f(*base, 100, L, 2, 8, 2, 16, 64, 1, 0, 0.0, FAKE * 5 + 4, FAKE * 6, 200,
+             *ws) == 4                                                         # rope alignment
+    assert f(*base, 100, L, 2, 8, 2, 16, 64, 1, 0, 0.0, FAKE * 5, FAKE * 6 + 8, 200,
+             *ws) == 4
     wsz = lib.kvc_gqa_prefill_workspace_size
     assert wsz(8, 16, 8, 2048, 4096 + 2048, 256, 1, 4096) == 0   # a full grid: no split
     assert wsz(2, 8, 2, 64, 4096, 128, 0, 0) == 0                # fp32: never split
