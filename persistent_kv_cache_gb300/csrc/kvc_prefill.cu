@@ -242,8 +242,13 @@ template <int D> struct PrefillSmem {
     static constexpr int DB = SLAB / (kBN * 128);        // 64-column blocks per K slab
     static constexpr int KPS = SLAB / (D * 2);           // keys per V slab
     static constexpr int Q_BYTES = kBM * D * 2;          // D/64 boxes of 128 x 64
-    static constexpr int NSLAB_MAX = (220 * 1024 - Q_BYTES) / SLAB;
-    static constexpr int NSLAB = NSLAB_MAX < 12 ? NSLAB_MAX : 12;  // ring depth
+    // Ring depth: every slot the opt-in shared memory of a CTA (227 KB)
+    // leaves beside the Q tile and the barriers / exchange area (at most
+    // 2.3 KB).
+    static constexpr int SMEM_BUDGET = 227 * 1024;
+    static constexpr int MISC_MAX = (2 * 12 + 8) * 8 + 16 + 4 * kBM * 4;
+    static constexpr int NSLAB_MAX = (SMEM_BUDGET - Q_BYTES - MISC_MAX) / SLAB;
+    static constexpr int NSLAB = NSLAB_MAX < 12 ? NSLAB_MAX : 12;
     static constexpr int Q_OFF = 0;
     static constexpr int RING_OFF = Q_OFF + Q_BYTES;
     static constexpr int BAR_OFF = RING_OFF + NSLAB * SLAB;
@@ -257,6 +262,7 @@ template <int D> struct PrefillSmem {
     // KV split) over the Q tile and the ring, which are free by then
     static constexpr int O_OFF = Q_OFF;
     static_assert(kBM * D * 4 <= RING_OFF + NSLAB * SLAB, "fp32 output tile must fit");
+    static_assert(TOTAL <= SMEM_BUDGET, "layout exceeds the opt-in shared memory");
     // TMEM columns: O [0, D) fp32 | S/P double buffer [D, D + 256)
     static constexpr uint32_t COL_O = 0, COL_S = D;
     static constexpr uint32_t TMEM_COLS = 512;
@@ -451,27 +457,33 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     } else if (warp == 0) {
         // ======================= MMA issuer =======================
         // tensor-pipe order: S_0, S_1, PV_0, S_2, PV_1, ...  S_{j+2} reuses the
-        // TMEM buffer that holds P_j, after PV_j in issue order
+        // TMEM buffer that holds P_j, after PV_j in issue order.
+        // A single thread issues every MMA, so its issue cost is per MMA: the
+        // shared-memory descriptors are built once and stepped by constant
+        // offsets (the start-address field counts 16-byte units and shared
+        // addresses stay below 256 KB, so adding to it never carries out).
         if (lane == 0) {
             bool ok = wait_or_abort(q_full, 0, abort_flag, a.status);
             int q = 0;  // next slab of the ring, in consumption order
+            const uint64_t q_desc = sw128_desc(smem_base + SM::Q_OFF, 16);
+            const uint64_t k_ring = sw128_desc(smem_base + SM::RING_OFF, 16);
+            const uint64_t v_ring = sw128_desc(smem_base + SM::RING_OFF, KPS * 128);
             auto issue_s = [&](int j) -> bool {
-                const uint32_t qa = smem_base + SM::Q_OFF;
+                const uint32_t d_s = tmem + COL_S + (j & 1) * kBN;
                 for (int sl = 0; sl < NST; ++sl, ++q) {
                     const int slot = q % NSLAB;
                     if (!wait_or_abort(&full[slot], (q / NSLAB) & 1, abort_flag, a.status))
                         return false;
                     tc_fence_after();
-                    const uint32_t kb = smem_base + SM::RING_OFF + slot * SM::SLAB;
+                    const uint64_t qd = q_desc + (uint64_t)(sl * DB * (kBM * 128 / 16));
+                    const uint64_t kd = k_ring + (uint64_t)(slot * (SM::SLAB / 16));
 #pragma unroll
                     for (int blk = 0; blk < DB; ++blk) {
-                        const int box = sl * DB + blk;  // 64-column block of D
 #pragma unroll
                         for (int k4 = 0; k4 < 4; ++k4) {
-                            const int kk = box * 4 + k4;
-                            const uint64_t ad = sw128_desc(qa + box * (kBM * 128) + k4 * 32, 16);
-                            const uint64_t bd = sw128_desc(kb + blk * (kBN * 128) + k4 * 32, 16);
-                            tc_mma_ss(tmem + COL_S + (j & 1) * kBN, ad, bd, IDESC_S, kk > 0);
+                            const uint64_t ad = qd + (uint64_t)((blk * (kBM * 128) + k4 * 32) / 16);
+                            const uint64_t bd = kd + (uint64_t)((blk * (kBN * 128) + k4 * 32) / 16);
+                            tc_mma_ss(d_s, ad, bd, IDESC_S, (sl | blk | k4) != 0);
                         }
                     }
                     tc_commit(&empty[slot]);
@@ -495,13 +507,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t vb = smem_base + SM::RING_OFF + slot * SM::SLAB;
+                    const uint64_t vd = v_ring + (uint64_t)(slot * (SM::SLAB / 16));
+                    const uint32_t pa = tmem + COL_S + s * kBN + sl * (KPS / 16) * 8;
 #pragma unroll
                     for (int k2 = 0; k2 < KPS / 16; ++k2) {
-                        const int kk = sl * (KPS / 16) + k2;  // 16-key step within the tile
-                        const uint64_t bd = sw128_desc(vb + k2 * 2048, KPS * 128);
-                        tc_mma_ts(tmem + COL_O, tmem + COL_S + s * kBN + kk * 8, bd, IDESC_O,
-                                  (j > 0 || kk > 0) ? 1u : 0u);
+                        // 16-key step k2 of this slab: P columns (16-bit pairs) and V rows
+                        tc_mma_ts(tmem + COL_O, pa + k2 * 8, vd + (uint64_t)(k2 * (2048 / 16)),
+                                  IDESC_O, (j > 0 || sl > 0 || k2 > 0) ? 1u : 0u);
                     }
                     tc_commit(&empty[slot]);
                 }
@@ -925,6 +937,8 @@ kvc_status launch_prefill_tc(void *out, const void *q, const void *k_rows, const
     int dev = 0, optin = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    // the dynamic window starts 1024-byte aligned after the reserved area;
+    // the kernel checks its layout fits what it was given (KVC_DEV_CAPACITY)
     const size_t smem = std::min<size_t>((size_t)SM::TOTAL + 1024, (size_t)optin);
     if (smem < (size_t)SM::TOTAL)
         return KVC_ERR_UNSUPPORTED;
