@@ -22,6 +22,8 @@ Other workloads (--workload):
   window-prefill  8 x 16/8 heads x 256, C = W = 4096, P ~ U[0, 20000],
                   --chunk S in {64, 512, 2048}; one step = lengths + staging
                   seed/append + tcgen05 chunk attention + copy-back
+  window-prefill-inplace  the same step with the stage held in the cache's
+                  own rows (no seed copy; the copy-back is an in-place shift)
   scatter         TensorScatter circular, (16, 8, 4096, 128) bf16, in place,
                   --chunk S in {1, 16, 64}; one step = one scatter call (the
                   line also reports the per-launch floor of a graph node)
@@ -564,6 +566,55 @@ class WindowPrefill(Workload):
         return "windowed chunked prefill: tcgen05 TFLOP/s (visible), tokens/s", "TFLOP/s"
 
 
+class WindowPrefillInplace(WindowPrefill):
+    """The windowed chunked-prefill step with the stage held in the cache's
+    own rows (kvc_window_append_inplace): the cache lives in rows [0, C) of
+    a buffer of C + S rows per head, the new rows are written after it, the
+    attention runs there, and the copy-back is an in-place shift (no seed
+    copy)."""
+
+    def __init__(self, dev, seed=0, with_kernels=True, chunk=2048):
+        super().__init__(dev, seed=seed, with_kernels=with_kernels, chunk=chunk)
+        import torch
+        w, S, e = self.w, self.S, self.e
+        B, Hkv, C, D = w.batch, w.kv_heads, w.capacity, w.head_dim
+        self.rows_k = torch.empty(B, Hkv, C + S, D, device=dev, dtype=torch.bfloat16)
+        self.rows_v = torch.empty_like(self.rows_k)
+        self.rows_k[:, :, :C] = self.kc
+        self.rows_v[:, :, :C] = self.vc
+        del self.ks, self.vs
+        Lp = np.minimum(self.P, C)
+        E = np.maximum(0, Lp + S - C)
+        L = Lp - E + S
+        # the shift reads and writes L rows of every (K/V, head) where rows evict
+        self.stage_bytes = int(2 * Hkv * D * e * int((2 * L * (E > 0)).sum()))
+        self.bytes_per_step = self.stage_bytes + self.kernel_bytes + 2 * 2 * B * Hkv * S * D * e
+        if with_kernels:
+            self.launches_per_step = 4 + (1 if self.pws is not None else 0)
+
+    def step(self, i):
+        K, w = self.K, self.w
+        K.kvc_seq_lengths(self.sk, self.S, w.capacity, 1, local_window_size=w.window, out=self.L,
+                          status=self.st)
+        K.kvc_window_append_inplace(self.rows_k, self.rows_v, self.nk, self.nv, self.L,
+                                    w.capacity, 1, K.KVC_APPEND, rope=self.rope, status=self.st)
+        self.kernel(i)
+        K.kvc_window_append_inplace(self.rows_k, self.rows_v, None, None, self.L, w.capacity, 1,
+                                    K.KVC_COPY_BACK, new_tokens=self.S, rope=self.rope,
+                                    status=self.st)
+
+    def kernel(self, i):
+        self.K.kvc_gqa_prefill_chunk(self.out, self.q, self.rows_k, self.rows_v, self.L,
+                                     local_window_size=self.w.window, rope=self.rope,
+                                     status=self.st, workspace=self.pws)
+
+    def config(self):
+        c = super().config()
+        c["workload"] = self.w.name + "-inplace-stage"
+        c["l2"] = "cache + stage rows ~0.6 GB per step > L2"
+        return c
+
+
 class Scatter(Workload):
     """TensorScatter circular on one (16, 8, 4096, 128) bf16 cache: in place,
     or (functional) into a separate present cache."""
@@ -772,6 +823,7 @@ WORKLOADS = {"contig-decode": ContigDecode, "contig-decode-unfused": ContigDecod
              "window-decode-unfused": WindowDecodeUnfused,
              "window-decode-drift": WindowDecodeDrift, "window-decode-ring": WindowDecodeRing,
              "window-decode-hot": WindowDecodeHot, "window-prefill": WindowPrefill,
+             "window-prefill-inplace": WindowPrefillInplace,
              "scatter-functional": ScatterFunctional,
              "scatter": Scatter}
 

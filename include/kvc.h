@@ -10,6 +10,7 @@
  *                          staging seed / copy-back (windowed, several tokens)
  *     kvc_gqa_decode       one-token GQA attention over the cache
  *     kvc_gqa_decode_ring  the same over a ring of C slots (circular addressing)
+ *     kvc_window_append_inplace  the staging step with the stage in the cache's rows
  *     kvc_paged_append, kvc_gqa_decode_paged  append and decode on a paged cache
  *     kvc_decode_step      lengths + append + decode in one launch (contiguous
  *                          cache or ring)
@@ -67,7 +68,7 @@
 extern "C" {
 #endif
 
-#define KVC_ABI_VERSION 3
+#define KVC_ABI_VERSION 4
 
 typedef enum {
     KVC_OK = 0,
@@ -218,6 +219,46 @@ kvc_status kvc_window_append(void *k_cache, void *v_cache, const void *new_k, co
                              int dtype, int windowed, int phase, const float *rope_cos,
                              const float *rope_sin, int64_t rope_max_pos, int32_t *dev_status,
                              void *stream);
+
+/*
+ * kvc_window_append_inplace -- the C + S staging step of a windowed cache
+ * with the stage held in the cache's own rows ("GQA support
+ * sliding_window_cache", "Design": a step with S new tokens attends over the
+ * cached rows and the new ones, then keeps the last positions; here the stage
+ * is not a second buffer).  The cache lives in rows [0, Lp) of a buffer with
+ * rows_per_head >= capacity + new_tokens rows per head, so the rows a stage
+ * would hold are already in place and no seed copy is made.
+ *
+ * k_rows, v_rows  device [batch, kv_heads, rows_per_head, head_dim]; rows
+ *                 [0, Lp) hold the cache (Lp = len.cache_past).  Other calls
+ *                 that read this cache take rows_per_head as their row pitch
+ *                 (their `capacity` argument), while kvc_seq_lengths takes the
+ *                 cache's capacity C.
+ * new_k, new_v    device [batch, kv_heads, new_tokens, head_dim].
+ * len             outputs of kvc_seq_lengths for the same S and C.
+ * windowed        KVC_WINDOWED or KVC_DRIFTING.
+ * phase = KVC_APPEND:     rows [Lp, Lp + S) <- the new rows (K rotated at
+ *                         P + i, as kvc_window_append).  Attention then runs
+ *                         on these rows (kvc_gqa_prefill_chunk with this
+ *                         rows_per_head).
+ * phase = KVC_COPY_BACK:  rows [0, L) <- rows [E, Lp + S), moved in place
+ *                         (one CTA per (batch, kv head, K/V) walks the range
+ *                         in ascending chunks, so every row is read before it
+ *                         is overwritten).  Rows [0, L) are then byte for byte
+ *                         what kvc_window_append's staged pair leaves in a
+ *                         cache of `capacity` rows; rows past L are scratch.
+ * A row rejected by kvc_seq_lengths (lengths -1) or for its RoPE range is left
+ * untouched by both phases (KVC_DEV_ROPE_RANGE as kvc_window_append).
+ * head_dim * element size a multiple of 16 bytes (KVC_ERR_UNSUPPORTED);
+ * buffers 16-byte aligned; rows_per_head < capacity + new_tokens ->
+ * KVC_ERR_CAPACITY.
+ */
+kvc_status kvc_window_append_inplace(void *k_rows, void *v_rows, const void *new_k,
+                                     const void *new_v, kvc_lengths len, int batch, int kv_heads,
+                                     int new_tokens, int64_t capacity, int64_t rows_per_head,
+                                     int head_dim, int dtype, int windowed, int phase,
+                                     const float *rope_cos, const float *rope_sin,
+                                     int64_t rope_max_pos, int32_t *dev_status, void *stream);
 
 /*
  * kvc_gqa_decode -- one-token grouped-query attention over the cache after

@@ -22,6 +22,9 @@
 //                        copy-back), 16-byte vectors
 //   compact_kernel       windowed S == 1: in-place E-row left shift of the
 //                        resident rows in ascending tiles, then the new row
+//   shift_rows_kernel    the copy-back of a stage held in the cache's own rows
+//                        (kvc_window_append_inplace): an in-place E-row left
+//                        shift of a whole slice through bulk copies
 #include "kvc_common.cuh"
 
 namespace {
@@ -278,6 +281,88 @@ compact_kernel(T *__restrict__ k_cache, T *__restrict__ v_cache, const T *__rest
     }
 }
 
+// In-place move of rows [E, E + L) of a (b, head) slice to rows [0, L): the
+// copy-back of kvc_window_append_inplace.  One CTA per (b, head, K/V); its
+// first thread streams the slice's contiguous byte range through a ring of
+// shared-memory chunks with 1-D bulk copies: chunk c comes from source bytes
+// E * row_bytes + [c CH, (c + 1) CH) and goes to [c CH, (c + 1) CH).  The move
+// is downwards, so chunk c's store overwrites only bytes that chunks <= c
+// read, and it is issued after those loads have landed; every later load
+// reads above every byte stored so far.  No second buffer is needed.
+constexpr int kShiftSlots = 6;
+constexpr int kShiftChunk = 32768;
+constexpr int kShiftSmem = kShiftSlots * kShiftChunk + kShiftSlots * 8 + 128;
+
+__global__ void __launch_bounds__(32)
+shift_rows_kernel(char *__restrict__ k_rows, char *__restrict__ v_rows, kvc_lengths len,
+                  int kv_heads, int64_t row_bytes, int64_t rows_per_head, int S,
+                  int64_t rope_limit_rows, int32_t *status)
+{
+    extern __shared__ uint8_t shift_smem_raw[];
+    if (threadIdx.x != 0)
+        return;
+    const int slice = blockIdx.x;
+    const int b = slice / kv_heads;
+    const bool is_k = blockIdx.y == 0;
+    const int L = len.cache_total[b];
+    if (L < 0)
+        return;
+    // a row rejected for its RoPE range had nothing appended: nothing moves
+    if (rope_limit_rows >= 0 && (int64_t)len.past_abs[b] + S > rope_limit_rows)
+        return;
+    const int64_t E = len.evict[b];
+    const int64_t Lp = len.cache_past[b];
+    if (E < 0 || Lp < 0 || Lp + S > rows_per_head || E + L != Lp + S) {
+        if (is_k && slice % kv_heads == 0)
+            kvc::raise_status(status, KVC_DEV_CAPACITY);
+        return;
+    }
+    if (E == 0 || L == 0)
+        return;  // the rows are already in place
+    uint8_t *ring = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(shift_smem_raw) + 127) & ~uintptr_t(127));
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + kShiftSlots * kShiftChunk);
+    for (int i = 0; i < kShiftSlots; ++i)
+        kvc::mbar_init(&full[i], 1);
+    kvc::fence_mbar_init();
+    char *dst = (is_k ? k_rows : v_rows) + (int64_t)slice * rows_per_head * row_bytes;
+    const char *src = dst + E * row_bytes;
+    const int64_t n = (int64_t)L * row_bytes;
+    const int64_t nchunks = (n + kShiftChunk - 1) / kShiftChunk;
+    auto chunk_bytes = [&](int64_t c) -> uint32_t {
+        const int64_t rest = n - c * kShiftChunk;
+        return (uint32_t)(rest < kShiftChunk ? rest : kShiftChunk);
+    };
+    auto load = [&](int64_t c) {
+        const int slot = (int)(c % kShiftSlots);
+        kvc::mbar_arrive_expect_tx(&full[slot], chunk_bytes(c));
+        kvc::bulk_load(ring + slot * kShiftChunk, src + c * kShiftChunk, chunk_bytes(c),
+                       &full[slot]);
+    };
+    const int64_t lead = nchunks < kShiftSlots ? nchunks : kShiftSlots;
+    for (int64_t c = 0; c < lead; ++c)
+        load(c);
+    int64_t issued = lead;
+    for (int64_t c = 0; c < nchunks; ++c) {
+        const int slot = (int)(c % kShiftSlots);
+        if (!kvc::mbar_wait(&full[slot], (uint32_t)(c / kShiftSlots) & 1u)) {
+            // a load that never lands: record it, let the other loads in
+            // flight land, and leave the slice as it is from chunk c on
+            kvc::raise_status(status, KVC_DEV_TIMEOUT);
+            for (int64_t d = c + 1; d < issued; ++d)
+                kvc::mbar_wait(&full[d % kShiftSlots], (uint32_t)(d / kShiftSlots) & 1u);
+            break;
+        }
+        kvc::bulk_store(dst + c * kShiftChunk, ring + slot * kShiftChunk, chunk_bytes(c));
+        kvc::tma_store_commit();
+        if (issued < nchunks) {
+            kvc::tma_store_wait_read();  // the slot's bytes have left shared memory
+            load(issued++);
+        }
+    }
+    kvc::tma_store_wait_all();
+}
+
 template <typename T>
 kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const void *new_v,
                         void *k_stage, void *v_stage, const kvc_lengths &len, int batch,
@@ -354,6 +439,36 @@ kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const v
     return kvc_host::launch_status();
 }
 
+// new rows at [Lp, Lp + S) of a buffer with rows_per_head rows per head
+template <typename T>
+kvc_status append_stage_rows(void *k_rows, void *v_rows, const void *new_k, const void *new_v,
+                             const kvc_lengths &len, int batch, int kv_heads, int S,
+                             int64_t rows_per_head, int D, const float *cos_t, const float *sin_t,
+                             int64_t rope_max_pos, int32_t *status, cudaStream_t stream)
+{
+    constexpr int VEC = 16 / sizeof(T);
+    const bool vec_ok = (D / 2) % VEC == 0;
+    const int pairs = vec_ok ? D / (2 * VEC) : D / 2;
+    const int64_t work = (int64_t)S * pairs;
+    int gx = (int)((work + 127) / 128);
+    gx = gx < 1 ? 1 : (gx > 64 ? 64 : gx);
+    dim3 grid(gx, batch * kv_heads, 2);
+    T *kd = static_cast<T *>(k_rows);
+    T *vd = static_cast<T *>(v_rows);
+    const T *nk = static_cast<const T *>(new_k);
+    const T *nv = static_cast<const T *>(new_v);
+    const PageTable none{nullptr, 0, 0, 0};
+    if (vec_ok)
+        new_rows_kernel<T, VEC><<<grid, 128, 0, stream>>>(kd, vd, nk, nv, len, kv_heads, S, D,
+                                                          rows_per_head, 1, cos_t, sin_t,
+                                                          rope_max_pos, status, none);
+    else
+        new_rows_kernel<T, 1><<<grid, 128, 0, stream>>>(kd, vd, nk, nv, len, kv_heads, S, D,
+                                                        rows_per_head, 1, cos_t, sin_t,
+                                                        rope_max_pos, status, none);
+    return kvc_host::launch_status();
+}
+
 template <typename T>
 kvc_status paged_append_typed(void *k_pool, void *v_pool, const void *new_k, const void *new_v,
                               const kvc_lengths &len, int batch, int kv_heads, int S, int D,
@@ -384,6 +499,78 @@ kvc_status paged_append_typed(void *k_pool, void *v_pool, const void *new_k, con
 }
 
 } // namespace
+
+KVC_API kvc_status kvc_window_append_inplace(void *k_rows, void *v_rows, const void *new_k,
+                                             const void *new_v, kvc_lengths len, int batch,
+                                             int kv_heads, int new_tokens, int64_t capacity,
+                                             int64_t rows_per_head, int head_dim, int dtype,
+                                             int windowed, int phase, const float *rope_cos,
+                                             const float *rope_sin, int64_t rope_max_pos,
+                                             int32_t *dev_status, void *stream_)
+{
+    const int eb = kvc_host::elem_bytes_of(dtype);
+    if (eb == 0)
+        return KVC_ERR_DTYPE;
+    if (batch < 0 || kv_heads < 1 || new_tokens < 1 || head_dim < 2 || head_dim > 1024 ||
+        (head_dim & 1))
+        return KVC_ERR_SHAPE;
+    if (capacity < 1 || capacity > (int64_t)INT32_MAX || rows_per_head < capacity + new_tokens ||
+        rows_per_head > (int64_t)INT32_MAX)
+        return KVC_ERR_CAPACITY;
+    if (windowed != KVC_WINDOWED && windowed != KVC_DRIFTING)
+        return KVC_ERR_UNSUPPORTED;
+    if (phase != KVC_APPEND && phase != KVC_COPY_BACK)
+        return KVC_ERR_UNSUPPORTED;
+    if (((int64_t)head_dim * eb) % 16 != 0)
+        return KVC_ERR_UNSUPPORTED;
+    if ((rope_cos == nullptr) != (rope_sin == nullptr))
+        return KVC_ERR_NULL;
+    if (rope_cos && rope_max_pos < 1)
+        return KVC_ERR_SHAPE;
+    if (batch == 0)
+        return KVC_OK;
+    if (!k_rows || !v_rows || !kvc_host::lengths_ok(len))
+        return KVC_ERR_NULL;
+    if (phase == KVC_APPEND && (!new_k || !new_v))
+        return KVC_ERR_NULL;
+    const size_t rows_bytes = (size_t)batch * kv_heads * rows_per_head * head_dim * eb;
+    if (kvc_host::overlaps(k_rows, rows_bytes, v_rows, rows_bytes))
+        return KVC_ERR_SHAPE;
+    for (const void *p : {(const void *)k_rows, (const void *)v_rows,
+                          phase == KVC_APPEND ? new_k : nullptr,
+                          phase == KVC_APPEND ? new_v : nullptr})
+        if (p && !kvc_host::aligned16(p))
+            return KVC_ERR_ALIGN;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const int slices = batch * kv_heads;
+    if (phase == KVC_APPEND) {
+        // the stage append with the cache's own rows as the stage: rows
+        // [Lp, Lp + S) of a buffer of rows_per_head rows
+        switch (dtype) {
+        case KVC_F32:
+            return append_stage_rows<float>(k_rows, v_rows, new_k, new_v, len, batch, kv_heads,
+                                            new_tokens, rows_per_head, head_dim, rope_cos,
+                                            rope_sin, rope_max_pos, dev_status, stream);
+        case KVC_BF16:
+            return append_stage_rows<__nv_bfloat16>(k_rows, v_rows, new_k, new_v, len, batch,
+                                                    kv_heads, new_tokens, rows_per_head,
+                                                    head_dim, rope_cos, rope_sin, rope_max_pos,
+                                                    dev_status, stream);
+        default:
+            return append_stage_rows<__half>(k_rows, v_rows, new_k, new_v, len, batch, kv_heads,
+                                             new_tokens, rows_per_head, head_dim, rope_cos,
+                                             rope_sin, rope_max_pos, dev_status, stream);
+        }
+    }
+    if (cudaFuncSetAttribute(shift_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kShiftSmem) != cudaSuccess)
+        return KVC_ERR_CUDA;
+    shift_rows_kernel<<<dim3(slices, 2), 32, kShiftSmem, stream>>>(
+        static_cast<char *>(k_rows), static_cast<char *>(v_rows), len, kv_heads,
+        (int64_t)head_dim * eb, rows_per_head, new_tokens, rope_cos ? rope_max_pos : -1,
+        dev_status);
+    return kvc_host::launch_status();
+}
 
 KVC_API kvc_status kvc_seq_lengths(const int32_t *seqlens_k, int batch, int new_tokens,
                                    int64_t capacity, int windowed, int local_window_size,

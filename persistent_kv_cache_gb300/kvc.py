@@ -35,7 +35,7 @@ KVC_DEV_TIMEOUT = 16
 EXPORTS = ("kvc_tensor_scatter", "kvc_seq_lengths", "kvc_window_append", "kvc_gqa_decode",
            "kvc_gqa_decode_workspace_size", "kvc_gqa_decode_noalloc", "kvc_gqa_decode_ring",
            "kvc_decode_step", "kvc_decode_step_workspace_size", "kvc_window_decode_step",
-           "kvc_paged_append", "kvc_gqa_decode_paged",
+           "kvc_paged_append", "kvc_gqa_decode_paged", "kvc_window_append_inplace",
            "kvc_gqa_prefill_chunk", "kvc_gqa_prefill_workspace_size", "kvc_status_string",
            "kvc_abi_version")
 KVC_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
@@ -93,6 +93,8 @@ def library() -> ctypes.CDLL:
             "kvc_tensor_scatter": [P, P, P, P, I, P, I64, I, I, I, P, P],
             "kvc_seq_lengths": [P, I, I, I64, I, I, L, P, P],
             "kvc_window_append": [P, P, P, P, P, P, L, I, I, I, I64, I, I, I, I, P, P, I64, P, P],
+            "kvc_window_append_inplace": [P, P, P, P, L, I, I, I, I64, I64, I, I, I, I, P, P, I64,
+                                          P, P],
             "kvc_gqa_decode": [P, P, P, P, L, I, I, I, I64, I, I, I, F, P, P, I64, P, SZ, P, P],
             "kvc_gqa_decode_ring": [P, P, P, P, L, I, I, I, I64, I, I, I, F, P, P, I64, P, SZ, P,
                                     P],
@@ -178,6 +180,20 @@ def kvc_window_append(k_cache, v_cache, new_k, new_v, lengths, windowed, phase=K
         _ptr(k_cache), _ptr(v_cache), _ptr(new_k), _ptr(new_v), _ptr(k_stage), _ptr(v_stage),
         lengths.c(), B, Hkv, S, C, D, _dtype_code(k_cache), int(windowed), phase, cs, sn, rmax,
         _ptr(status), _stream(stream)))
+
+
+def kvc_window_append_inplace(k_rows, v_rows, new_k, new_v, lengths, capacity, windowed,
+                              phase=KVC_APPEND, new_tokens=None, rope=None, status=None,
+                              stream=None):
+    """k_rows/v_rows: [B, Hkv, rows_per_head, D] with rows_per_head >= capacity + S; the
+    cache lives in rows [0, Lp).  new_tokens is needed when new_k is None (KVC_COPY_BACK)."""
+    B, Hkv, R, D = k_rows.shape
+    S = new_k.shape[2] if new_k is not None else int(new_tokens)
+    cs, sn, rmax = _rope(rope)
+    _check("kvc_window_append_inplace", library().kvc_window_append_inplace(
+        _ptr(k_rows), _ptr(v_rows), _ptr(new_k), _ptr(new_v), lengths.c(), B, Hkv, S, capacity, R,
+        D, _dtype_code(k_rows), int(windowed), phase, cs, sn, rmax, _ptr(status),
+        _stream(stream)))
 
 
 def kvc_gqa_decode_workspace_size(batch, q_heads, kv_heads, capacity, head_dim, dtype):

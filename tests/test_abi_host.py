@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(kvc):
 
 
 def test_version_and_strings(kvc):
-    assert kvc.kvc_abi_version() == 3
+    assert kvc.kvc_abi_version() == 4
     assert kvc.kvc_status_string(0) == "ok"
     assert "window" in kvc.kvc_status_string(7)
 
@@ -211,3 +211,24 @@ def test_window_step_host_checks(kvc):
     half = kvc.KvcLengths(FAKE, None, None, None, None)
     assert f(*base, half, 2, 8, 2, 128, 64, 1, 2, 128, 0.0, None, None, 0, None, None) == 1
     assert f(*base, none, 0, 8, 2, 128, 64, 1, 2, 128, 0.0, None, None, 0, None, None) == 0
+
+
+def test_append_inplace_host_checks(kvc):
+    lib = kvc.library()
+    f = lib.kvc_window_append_inplace
+    L = _lengths(kvc)
+    far = [FAKE, 1 << 32, FAKE * 3, FAKE * 4, L]   # k rows, v rows far apart, new k, new v
+    # (..., batch, kv_heads, S, capacity, rows_per_head, head_dim, dtype, policy, phase, cos, sin,
+    #  rope_max, status, stream)
+    ok = [2, 2, 16, 128, 144, 64, 1, 1, 0, None, None, 0, None, None]
+    assert f(*far, *ok[:4], 143, *ok[5:]) == 6                      # rows_per_head < C + S
+    assert f(*far, *ok[:7], 0, *ok[8:]) == 5                        # contiguous: no stage
+    assert f(*far, *ok[:7], 3, *ok[8:]) == 5                        # ring: nothing moves
+    assert f(*far, *ok[:8], 2, *ok[9:]) == 5                        # unknown phase
+    assert f(*far, *ok[:5], 4, *ok[6:]) == 5                        # 8-byte rows: no bulk copies
+    assert f(*far, *ok[:6], 7, *ok[7:]) == 3                        # dtype
+    assert f(far[0], far[1], None, None, L, *ok) == 1               # append without new rows
+    assert f(FAKE + 8, *far[1:], *ok) == 4                          # alignment
+    assert f(FAKE, FAKE + 16, FAKE * 3, FAKE * 4, L, *ok) == 2      # K and V rows overlap
+    assert f(*far, *ok[:9], FAKE, None, 16, None, None) == 1        # half a rope table
+    assert f(*far, 0, *ok[1:]) == 0                                 # empty batch
