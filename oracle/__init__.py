@@ -30,6 +30,15 @@ patterns) and returns numpy arrays; each one cites the page it restates:
   time); attention lists the ring's slots in position order and is then the
   plain attention above.
 
+* ``quantize_affine``, ``dequantize_affine``, ``quantize_page``,
+  ``paged_attention_q`` -- "Persistent input/output feedback", "Optional
+  heterogeneous paged KV" (selected-block quantization: affine codes with a
+  scale and zero point per K or V block, ties to even, saturation to the
+  code range, reconstruction (code - zero point) * scale) and the roadmap's
+  "Phase 3: cache quantization and fusion" (cold pages quantized to INT8):
+  attention over a paged cache whose pages are 16-bit or INT8 is the plain
+  attention above over the reconstructed rows.
+
 Pins: every function is checked in ``tests/test_oracle_*.py`` against the
 pages' worked examples, closed forms, brute-force simulations and library
 routines (see the docstrings there).  No function here is "parity unpinned".
@@ -326,3 +335,83 @@ def paged_attention(q, k_pool, v_pool, block_table, page_size, n_rows, total_abs
     v = paged_rows(v_pool, block_table, n_rows, page_size)
     return gqa_attention(q, k, v, np.asarray(n_rows, np.int32), np.asarray(total_abs, np.int32),
                          window=window, scale=scale, cos_cache=cos_cache, sin_cache=sin_cache)
+
+
+# ---------------------------------------------------------------------------
+# affine page quantization ("Persistent input/output feedback", "Optional
+# heterogeneous paged KV": selected-block quantization; roadmap "Phase 3")
+# ---------------------------------------------------------------------------
+
+PAGE_QUANT = 0x40000000  # block-table flag: the entry names a page of the int8 pools
+
+
+def to_f32(a):
+    """float32 values of 16-bit bit patterns (uint16 = bf16), float16 or float32."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32)
+    return a.astype(np.float32)
+
+
+def quantize_affine(x, scale, zero_point, unsigned=False):
+    """Affine codes of float32 values: x / scale in float32, rounded to the
+    nearest integer with ties to even, plus the zero point, saturated to the
+    code range (INT8 [-128, 127], UINT8 [0, 255]).  Returns int32 codes."""
+    t = np.asarray(x, dtype=np.float32) / np.float32(scale)
+    r = np.rint(t).astype(np.float64)          # integral (or +-inf): ties to even
+    lo, hi = (0, 255) if unsigned else (-128, 127)
+    return np.clip(r + zero_point, lo, hi).astype(np.int32)
+
+
+def dequantize_affine(codes, scale, zero_point):
+    """Reconstruction (code - zero point) * scale in float32."""
+    return ((np.asarray(codes, dtype=np.float32) - np.float32(zero_point)) *
+            np.float32(scale)).astype(np.float32)
+
+
+def quantize_page(page, scale, zero_point, unsigned=False):
+    """One page (any shape) of 16-bit bits or float32 values -> (stored int8
+    bytes, stored zero point).  The stored byte is the code minus a bias (0
+    for INT8, 128 for UINT8) and the stored zero point is zero_point minus the
+    same bias, so (stored - stored zero point) * scale is the reconstruction
+    for either code type."""
+    codes = quantize_affine(to_f32(page), scale, zero_point, unsigned)
+    bias = 128 if unsigned else 0
+    return (codes - bias).astype(np.int8), int(zero_point) - bias
+
+
+def paged_rows_q(pool, qpool, qparams, which, block_table, n_rows, page_size):
+    """float32 logical rows [B, Hkv, max(n_rows), D] of a paged cache whose
+    table entries name either a page of the 16-bit pool or (flag PAGE_QUANT)
+    a page of the int8 pool, reconstructed with that page's scale and stored
+    zero point (qparams[page] = (k_scale, k_zp, v_scale, v_zp); which = 0 for
+    K, 1 for V)."""
+    bt = np.asarray(block_table)
+    B = bt.shape[0]
+    _, Hkv, P, D = pool.shape
+    assert P == page_size
+    n = np.asarray(n_rows, dtype=np.int64)
+    R = int(n.max()) if B else 0
+    out = np.zeros((B, Hkv, max(R, 1), D), dtype=np.float32)
+    for b in range(B):
+        for r in range(int(n[b])):
+            e = int(bt[b, r // P])
+            if e & PAGE_QUANT:
+                page = e & (PAGE_QUANT - 1)
+                sc, zp = qparams[page][2 * which], qparams[page][2 * which + 1]
+                out[b, :, r] = dequantize_affine(qpool[page, :, r % P], sc, zp)
+            else:
+                out[b, :, r] = to_f32(pool[e, :, r % P])
+    return out
+
+
+def paged_attention_q(q, k_pool, v_pool, qk_pool, qv_pool, qparams, block_table, page_size,
+                      n_rows, total_abs, window=0, scale=None, cos_cache=None, sin_cache=None):
+    """Attention of q [B, Hq, S, D] (16-bit bits or float32) over a paged
+    cache of 16-bit and int8 pages, in float32 over the reconstructed rows.
+    Returns (out float32, flags)."""
+    k = paged_rows_q(k_pool, qk_pool, qparams, 0, block_table, n_rows, page_size)
+    v = paged_rows_q(v_pool, qv_pool, qparams, 1, block_table, n_rows, page_size)
+    return gqa_attention(to_f32(q), k, v, np.asarray(n_rows, np.int32),
+                         np.asarray(total_abs, np.int32), window=window, scale=scale,
+                         cos_cache=cos_cache, sin_cache=sin_cache)
