@@ -32,6 +32,8 @@ Other workloads (--workload):
   window-decode-hot   window-decode on one cache (16.8 MB, L2-resident)
   paged-decode    the contiguous decode workload held in 64-row pages of a
                   shuffled page pool (lengths + paged append + paged decode)
+  paged-decode-int8  the same with every full page below a row's newest one
+                  quantized to int8 (lengths + append + mixed-page decode)
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--workload ...] [--chunk S] [--profile]
@@ -800,6 +802,105 @@ class PagedDecode(ContigDecode):
         return dt, nbytes
 
 
+class PagedDecodeQ8(PagedDecode):
+    """The paged decode workload with every full page below a row's newest
+    one held as int8 (affine, scale 0.04, zero point 0 for K and V; the
+    newest page, where the step appends, stays 16-bit): one step =
+    kvc_seq_lengths + kvc_paged_append + kvc_gqa_decode_paged_q (+ merge)."""
+    k_scale = v_scale = 0.04
+
+    def __init__(self, dev, seed=0, with_kernels=True, chunk=None):
+        import torch
+        super().__init__(dev, seed=seed, with_kernels=with_kernels, chunk=chunk)
+        self.roofline_kernel = "kvc_gqa_decode_paged_q (split + merge launches)"
+        self.traffic_key = ("kvc_decode.cu", "decode_split_kernel_paged_q")
+        w, P, e = self.w, self.page_size, self.e
+        B, Hq, Hkv, D = w.batch, w.q_heads, w.kv_heads, w.head_dim
+        # the rows of each sequence that live in int8 pages (all pages before
+        # the one holding row T - 1, which the step appends to)
+        full = (self.T - 1) // P
+        self.q8_rows = full * P
+        n16 = self.T - self.q8_rows
+        self.kernel_bytes = (int(self.q8_rows.sum()) * Hkv * D * 2
+                             + int(n16.sum()) * Hkv * D * 2 * e + 2 * B * Hq * D * e)
+        self.bytes_per_step = self.kernel_bytes + self.append_bytes
+        src, dst = [], []
+        self.qtab_host = self.table_host.copy()
+        for b in range(B):
+            for j in range(int(full[b])):
+                src.append(int(self.table_host[b, j]))
+                self.qtab_host[b, j] = 0x40000000 | len(dst)
+                dst.append(len(dst))
+        self.n_q_pages = max(1, len(dst))
+        if not with_kernels:
+            return
+        K = self.K
+        self.qk = torch.empty(self.n_q_pages, Hkv, P, D, dtype=torch.int8, device=dev)
+        self.qv = torch.empty_like(self.qk)
+        self.qp = torch.zeros(self.n_q_pages, 4, dtype=torch.float32, device=dev)
+        if src:
+            K.kvc_quantize_pages(self.kc, self.vc, self.qk, self.qv,
+                                 torch.tensor(src, dtype=torch.int32, device=dev),
+                                 torch.tensor(dst, dtype=torch.int32, device=dev), self.qp,
+                                 self.k_scale, 0, False, self.v_scale, 0, False, status=self.st)
+        self.qtable = torch.from_numpy(self.qtab_host).to(dev)
+        torch.cuda.synchronize()
+
+    def kernel(self, i):
+        self.K.kvc_gqa_decode_paged_q(self.out, self.q, self.kc, self.vc, self.qk, self.qv,
+                                      self.qp, self.qtable, self.L, rope=self.rope,
+                                      workspace=self.ws, status=self.st)
+
+    def config(self):
+        c = super().config()
+        c.update({"workload": self.w.name + "-paged64-int8",
+                  "int8_pages": int(self.n_q_pages), "int8_scale": self.k_scale,
+                  "int8_rows_fraction": float(self.q8_rows.sum() / self.T.sum())})
+        return c
+
+    def oracle_sample(self, rows):
+        """The oracle's append + attention over the sampled rows, with their
+        int8 pages quantized by the oracle from the same 16-bit pages (once,
+        before the timed part: quantizing is not part of a step)."""
+        import oracle
+        from persistent_kv_cache_gb300 import synth
+        w = self.w
+        rows = list(rows)[:2]
+        P = self.page_size
+        kp = synth.bits(self.kc.cpu()).copy()
+        vp = synth.bits(self.vc.cpu()).copy()
+        tab16 = self.table_host[rows]
+        T = self.T[rows]
+        full = (T - 1) // P
+        n_q = max(1, int(full.sum()))
+        qk = np.zeros((n_q, w.kv_heads, P, w.head_dim), np.int8)
+        qv = np.zeros_like(qk)
+        qp = np.zeros((n_q, 4), np.float32)
+        tab = tab16.copy()
+        n = 0
+        for i in range(len(rows)):
+            for j in range(int(full[i])):
+                qk[n], zk = oracle.quantize_page(kp[tab16[i, j]], self.k_scale, 0)
+                qv[n], zv = oracle.quantize_page(vp[tab16[i, j]], self.v_scale, 0)
+                qp[n] = (self.k_scale, zk, self.v_scale, zv)
+                tab[i, j] = oracle.PAGE_QUANT | n
+                n += 1
+        nk, nv = synth.bits(self.nk_host[rows]), synth.bits(self.nv_host[rows])
+        q = synth.bits(self.q_host[rows])
+        cos, sin = (t.cpu().numpy() for t in self.rope)
+        t0 = time.perf_counter()
+        oracle.paged_append(kp, vp, tab16, P, nk, nv, T - 1, cos, sin)
+        oracle.paged_attention_q(q, kp, vp, qk, qv, qp, tab, P, T, T, cos_cache=cos,
+                                 sin_cache=sin)
+        dt = time.perf_counter() - t0
+        q8 = self.q8_rows[rows]
+        nbytes = (int(q8.sum()) * w.kv_heads * w.head_dim * 2
+                  + int((T - q8).sum()) * w.kv_heads * w.head_dim * 2 * self.e
+                  + 2 * len(rows) * w.q_heads * w.head_dim * self.e
+                  + 2 * 2 * len(rows) * w.kv_heads * w.head_dim * self.e)
+        return dt, nbytes
+
+
 def torch_index(a):
     import torch
     return torch.from_numpy(np.asarray(a, dtype=np.int64))
@@ -824,6 +925,7 @@ WORKLOADS = {"contig-decode": ContigDecode, "contig-decode-unfused": ContigDecod
              "window-decode-drift": WindowDecodeDrift, "window-decode-ring": WindowDecodeRing,
              "window-decode-hot": WindowDecodeHot, "window-prefill": WindowPrefill,
              "window-prefill-inplace": WindowPrefillInplace,
+             "paged-decode-int8": PagedDecodeQ8,
              "scatter-functional": ScatterFunctional,
              "scatter": Scatter}
 

@@ -12,6 +12,8 @@
  *     kvc_gqa_decode_ring  the same over a ring of C slots (circular addressing)
  *     kvc_window_append_inplace  the staging step with the stage in the cache's rows
  *     kvc_paged_append, kvc_gqa_decode_paged  append and decode on a paged cache
+ *     kvc_quantize_pages, kvc_gqa_decode_paged_q  int8 pages and decode over
+ *                          a cache of 16-bit and int8 pages
  *     kvc_decode_step      lengths + append + decode in one launch (contiguous
  *                          cache or ring)
  *     kvc_window_decode_step  the same for a windowed cache (small windows)
@@ -68,7 +70,7 @@
 extern "C" {
 #endif
 
-#define KVC_ABI_VERSION 4
+#define KVC_ABI_VERSION 5
 
 typedef enum {
     KVC_OK = 0,
@@ -393,6 +395,77 @@ kvc_status kvc_gqa_decode_paged(void *out, const void *q, const void *k_pool,
                                 int local_window_size, float scale, const float *rope_cos,
                                 const float *rope_sin, int64_t rope_max_pos, void *workspace,
                                 size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * Quantized pages ("Persistent input/output feedback", "Optional
+ * heterogeneous paged KV": selected-block affine quantization; "Persistent
+ * KV Cache and Decode Performance Roadmap", "Phase 3": cold pages to INT8,
+ * recent tokens kept in the native type).  Int8 pages live in pools
+ * qk_pool, qv_pool [n_qpool_pages, kv_heads, page_size, head_dim] (int8); a
+ * block-table entry with KVC_PAGE_QUANT set names page
+ * (entry & ~KVC_PAGE_QUANT) of these pools.  qparams is device float
+ * [n_qpool_pages][4] = (k_scale, k_zp, v_scale, v_zp) per int8 page, so that
+ * a stored byte s reconstructs as (s - zp) * scale.
+ *
+ * Payload order (the MMA fragment order of the decode): the page_size rows of
+ * a (page, kv head) are cut into groups of 16; group G is 16 * head_dim
+ * bytes at G * 16 * head_dim.  Within a group, with D = head_dim:
+ *   K element (row j, column d):  nb = j / 8, g = j % 8, kk = d / 16,
+ *     dd = d % 16, lane = 4 g + (dd % 8) / 2,
+ *     f = (nb * D / 16 + kk) * 4 + 2 (dd / 8) + dd % 2
+ *   V element (row j, column c):  nn = c / 16, cc = c % 16,
+ *     lane = 4 (cc % 8) + (j % 8) / 2, f = (nn * 2 + cc / 8) * 4 + 2 (j / 8) + j % 2
+ *   byte = (f / 16) * 512 + lane * 16 + f % 16
+ * (lane l's D / 2 bytes are the B fragments of its mma.m16n8k16 steps,
+ * stored as 16-byte pieces interleaved across the 32 lanes).
+ */
+#define KVC_PAGE_QUANT 0x40000000
+
+/*
+ * kvc_quantize_pages -- page src_pages[i] of the 16-bit pools (every row and
+ * KV head) becomes int8 page dst_pages[i], for i < n_pages:
+ *     code = saturate(round_half_even(x / scale) + zero_point)
+ * with x / scale in float32, saturated to [-128, 127] (INT8) or [0, 255]
+ * (UINT8: *_unsigned != 0); the stored byte is code - bias (bias 0 for INT8,
+ * 128 for UINT8) and qparams[dst] = (k_scale, k_zero_point - k_bias, v_scale,
+ * v_zero_point - v_bias).  K and V may use different formats.
+ * k_pool, v_pool     device [n_pool_pages, kv_heads, page_size, head_dim],
+ *                    KVC_BF16 or KVC_F16.
+ * src_pages, dst_pages  device int32 [n_pages]; a pair with an id outside its
+ *                    pool sets KVC_DEV_INDEX_OOB and is skipped.  Destinations
+ *                    must be distinct.  The block table is not touched: the
+ *                    caller points its entries at (dst | KVC_PAGE_QUANT).
+ * Scales positive and finite, zero points inside the code range
+ * (KVC_ERR_SHAPE otherwise); page_size a multiple of 16; head_dim a multiple
+ * of 32.
+ */
+kvc_status kvc_quantize_pages(const void *k_pool, const void *v_pool, void *qk_pool,
+                              void *qv_pool, const int32_t *src_pages, const int32_t *dst_pages,
+                              int n_pages, int64_t n_pool_pages, int64_t n_qpool_pages,
+                              int page_size, int kv_heads, int head_dim, int dtype, float k_scale,
+                              int k_zero_point, int k_unsigned, float v_scale, int v_zero_point,
+                              int v_unsigned, float *qparams, int32_t *dev_status, void *stream);
+
+/*
+ * kvc_gqa_decode_paged_q -- kvc_gqa_decode_paged over a cache whose pages are
+ * 16-bit (entries naming the k_pool / v_pool pages) or int8 (entries with
+ * KVC_PAGE_QUANT).  An int8 tile is read at half the bytes and its
+ * reconstruction (s - zp) * scale enters the attention with the page's
+ * scale applied in float32 after the products: scores = k_scale * q . (s - zp),
+ * values = v_scale * sum p (s - zp).  An entry outside its pool sets
+ * KVC_DEV_INDEX_OOB (that row's output is undefined).  Same arguments and
+ * limits as kvc_gqa_decode_paged plus the int8 pools, qparams (16-byte
+ * aligned) and n_qpool_pages.
+ */
+kvc_status kvc_gqa_decode_paged_q(void *out, const void *q, const void *k_pool,
+                                  const void *v_pool, const void *qk_pool, const void *qv_pool,
+                                  const float *qparams, int64_t n_qpool_pages,
+                                  const int32_t *block_table, int max_pages, int64_t n_pool_pages,
+                                  int page_size, kvc_lengths len, int batch, int q_heads,
+                                  int kv_heads, int head_dim, int dtype, int local_window_size,
+                                  float scale, const float *rope_cos, const float *rope_sin,
+                                  int64_t rope_max_pos, void *workspace, size_t workspace_bytes,
+                                  int32_t *dev_status, void *stream);
 
 /*
  * kvc_decode_step -- one fused one-token step on a contiguous cache or a

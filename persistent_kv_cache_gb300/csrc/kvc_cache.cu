@@ -22,9 +22,14 @@
 //                        copy-back), 16-byte vectors
 //   compact_kernel       windowed S == 1: in-place E-row left shift of the
 //                        resident rows in ascending tiles, then the new row
+//   quantize_pages_kernel  affine int8 quantization of selected cache pages
+//                        ("Persistent input/output feedback", "Optional
+//                        heterogeneous paged KV": selected-block quantization)
 //   shift_rows_kernel    the copy-back of a stage held in the cache's own rows
 //                        (kvc_window_append_inplace): an in-place E-row left
 //                        shift of a whole slice through bulk copies
+#include <cmath>
+
 #include "kvc_common.cuh"
 
 namespace {
@@ -363,6 +368,78 @@ shift_rows_kernel(char *__restrict__ k_rows, char *__restrict__ v_rows, kvc_leng
     kvc::tma_store_wait_all();
 }
 
+// Page src[i] of a 16-bit pool -> int8 page dst[i], one CTA per (i, kv head,
+// K/V): code = saturate(rint(x / scale) + zp) with x / scale rounded once in
+// float32 and rint rounding ties to even, stored as code - bias (bias 128 for
+// UINT8, so that one int8 payload serves both code types), in the fragment
+// order of include/kvc.h (q8_k_pos / q8_v_pos below): the decode's lanes then
+// load their MMA operand bytes with 16-byte loads and no shuffling.
+
+// byte of element (row j, column d) within a 16-row group of a K payload
+__device__ __forceinline__ int q8_k_pos(int j, int d, int D)
+{
+    const int nb = j >> 3, g = j & 7, kk = d >> 4, dd = d & 15;
+    const int lane = 4 * g + ((dd & 7) >> 1);
+    const int fb = (nb * (D >> 4) + kk) * 4 + 2 * (dd >> 3) + (dd & 1);
+    return (fb >> 4) * 512 + lane * 16 + (fb & 15);
+}
+
+// byte of element (row j, column c) within a 16-row group of a V payload
+__device__ __forceinline__ int q8_v_pos(int j, int c, int D)
+{
+    const int nn = c >> 4, cc = c & 15;
+    const int lane = 4 * (cc & 7) + ((j & 7) >> 1);
+    const int fb = (nn * 2 + (cc >> 3)) * 4 + 2 * (j >> 3) + (j & 1);
+    return (fb >> 4) * 512 + lane * 16 + (fb & 15);
+}
+struct QuantSpec {
+    float scale;
+    int zp, lo, hi, bias;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+quantize_pages_kernel(const T *__restrict__ k_pool, const T *__restrict__ v_pool,
+                      int8_t *__restrict__ qk_pool, int8_t *__restrict__ qv_pool,
+                      const int32_t *__restrict__ src_pages, const int32_t *__restrict__ dst_pages,
+                      int64_t n_pool_pages, int64_t n_q_pages, int kv_heads, int D, int64_t slab,
+                      QuantSpec kq, QuantSpec vq, float *__restrict__ qparams, int32_t *status)
+{
+    const int i = blockIdx.x, h = blockIdx.y;
+    const bool is_k = blockIdx.z == 0;
+    const int src = src_pages[i], dst = dst_pages[i];
+    if (src < 0 || (int64_t)src >= n_pool_pages || dst < 0 || (int64_t)dst >= n_q_pages) {
+        if (threadIdx.x == 0 && h == 0 && is_k)
+            kvc::raise_status(status, KVC_DEV_INDEX_OOB);
+        return;
+    }
+    const QuantSpec q = is_k ? kq : vq;
+    if (threadIdx.x == 0 && h == 0) {
+        qparams[(int64_t)dst * 4 + (is_k ? 0 : 2)] = q.scale;
+        qparams[(int64_t)dst * 4 + (is_k ? 1 : 3)] = (float)(q.zp - q.bias);
+    }
+    // slab = page_size * head_dim elements of one (page, head), a multiple of 8
+    const int64_t so = ((int64_t)src * kv_heads + h) * slab;
+    const int64_t dof = ((int64_t)dst * kv_heads + h) * slab;
+    const uint4 *in = reinterpret_cast<const uint4 *>((is_k ? k_pool : v_pool) + so);
+    int8_t *out = (is_k ? qk_pool : qv_pool) + dof;
+    const float lo = (float)q.lo, hi = (float)q.hi, zp = (float)q.zp;
+    const int cpr = D / 8;  // 8-element chunks per row
+    for (int64_t c = threadIdx.x; c < slab / 8; c += blockDim.x) {
+        const uint4 x = in[c];
+        const T *e = reinterpret_cast<const T *>(&x);
+        const int row = (int)(c / cpr), d0 = (int)(c % cpr) * 8;
+        int8_t *grp = out + (int64_t)(row >> 4) * 16 * D;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float t = __fdiv_rn(kvc::Elem<T>::to_f32(e[k]), q.scale);
+            const float code = fminf(fmaxf(rintf(t) + zp, lo), hi);
+            grp[is_k ? q8_k_pos(row & 15, d0 + k, D) : q8_v_pos(row & 15, d0 + k, D)] =
+                (int8_t)((int)code - q.bias);
+        }
+    }
+}
+
 template <typename T>
 kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const void *new_v,
                         void *k_stage, void *v_stage, const kvc_lengths &len, int batch,
@@ -499,6 +576,63 @@ kvc_status paged_append_typed(void *k_pool, void *v_pool, const void *new_k, con
 }
 
 } // namespace
+
+KVC_API kvc_status kvc_quantize_pages(const void *k_pool, const void *v_pool, void *qk_pool,
+                                      void *qv_pool, const int32_t *src_pages,
+                                      const int32_t *dst_pages, int n_pages,
+                                      int64_t n_pool_pages, int64_t n_qpool_pages, int page_size,
+                                      int kv_heads, int head_dim, int dtype, float k_scale,
+                                      int k_zero_point, int k_unsigned, float v_scale,
+                                      int v_zero_point, int v_unsigned, float *qparams,
+                                      int32_t *dev_status, void *stream_)
+{
+    if (dtype != KVC_BF16 && dtype != KVC_F16)
+        return kvc_host::elem_bytes_of(dtype) ? KVC_ERR_UNSUPPORTED : KVC_ERR_DTYPE;
+    // the payload's fragment order works in 16-row groups and 32-column blocks
+    if (n_pages < 0 || kv_heads < 1 || page_size < 16 || page_size % 16 != 0 || head_dim < 32 ||
+        head_dim % 32 != 0 || n_pool_pages < 1 || n_qpool_pages < 1)
+        return KVC_ERR_SHAPE;
+    if (n_pages > 65535 || kv_heads > 65535)
+        return KVC_ERR_SHAPE;
+    auto spec = [](float scale, int zp, int uns, QuantSpec &q) {
+        if (!(scale > 0.f) || !std::isfinite(scale))
+            return false;
+        q.scale = scale;
+        q.zp = zp;
+        q.lo = uns ? 0 : -128;
+        q.hi = uns ? 255 : 127;
+        q.bias = uns ? 128 : 0;
+        return zp >= q.lo && zp <= q.hi;
+    };
+    QuantSpec kq, vq;
+    if (!spec(k_scale, k_zero_point, k_unsigned, kq) || !spec(v_scale, v_zero_point, v_unsigned, vq))
+        return KVC_ERR_SHAPE;
+    if (n_pages == 0)
+        return KVC_OK;
+    if (!k_pool || !v_pool || !qk_pool || !qv_pool || !src_pages || !dst_pages || !qparams)
+        return KVC_ERR_NULL;
+    for (const void *p : {k_pool, v_pool, (const void *)qk_pool, (const void *)qv_pool,
+                          (const void *)qparams})
+        if (!kvc_host::aligned16(p))
+            return KVC_ERR_ALIGN;
+    const int64_t slab = (int64_t)page_size * head_dim;
+    const size_t qb = (size_t)n_qpool_pages * kv_heads * slab;
+    if (kvc_host::overlaps(qk_pool, qb, qv_pool, qb))
+        return KVC_ERR_SHAPE;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const dim3 grid(n_pages, kv_heads, 2);
+    if (dtype == KVC_BF16)
+        quantize_pages_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(k_pool), static_cast<const __nv_bfloat16 *>(v_pool),
+            static_cast<int8_t *>(qk_pool), static_cast<int8_t *>(qv_pool), src_pages, dst_pages,
+            n_pool_pages, n_qpool_pages, kv_heads, head_dim, slab, kq, vq, qparams, dev_status);
+    else
+        quantize_pages_kernel<__half><<<grid, 256, 0, stream>>>(
+            static_cast<const __half *>(k_pool), static_cast<const __half *>(v_pool),
+            static_cast<int8_t *>(qk_pool), static_cast<int8_t *>(qv_pool), src_pages, dst_pages,
+            n_pool_pages, n_qpool_pages, kv_heads, head_dim, slab, kq, vq, qparams, dev_status);
+    return kvc_host::launch_status();
+}
 
 KVC_API kvc_status kvc_window_append_inplace(void *k_rows, void *v_rows, const void *new_k,
                                              const void *new_v, kvc_lengths len, int batch,

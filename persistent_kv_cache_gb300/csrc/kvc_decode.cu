@@ -105,6 +105,18 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// s - zp for the four signed bytes of w, exactly, as floats: byte b + 128 goes
+// into the low mantissa byte of 2^23 (0x4B000000), so the float is
+// 2^23 + 128 + b, and off = 2^23 + 128 + zp leaves b - zp (|b - zp| <= 255).
+__device__ __forceinline__ void s8x4_minus(uint32_t w, float off, float (&f)[4])
+{
+    const uint32_t u = w ^ 0x80808080u;
+    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - off;
+    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - off;
+    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)) - off;
+    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - off;
+}
+
 // Attention state of one consumer warp over 64-row K/V tiles held in shared
 // memory (128-byte swizzled boxes of 64 columns, 8 KB per box): the GQA
 // group's query heads are the M = 16 rows of mma.sync m16n8k16, the warp
@@ -137,6 +149,62 @@ template <typename T, int D> struct GroupAttn {
             qa[kk][3] =
                 *reinterpret_cast<const uint32_t *>(&qs[(row + 8) * QS + kk * 16 + 8 + col]);
         }
+    }
+
+    // Online-softmax update with raw scores sc of this warp's 16 keys (the
+    // same steps as in tile()): mask keys outside [lo, hi), raise m, rescale
+    // l and o, and pack P (times vscale) as the A fragment of the PV MMAs.
+    __device__ __forceinline__ void softmax_step(float (&sc)[2][4], int lane, int lo, int hi,
+                                                 float scale_log2, float vscale, uint32_t (&pa)[4])
+    {
+        float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int col = 8 * j + 2 * (lane & 3) + (e & 1);
+                float v = sc[j][e] * scale_log2;
+                v = (col >= lo && col < hi) ? v : -INFINITY;
+                sc[j][e] = v;
+                if (e < 2)
+                    mx_lo = fmaxf(mx_lo, v);
+                else
+                    mx_hi = fmaxf(mx_hi, v);
+            }
+        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+        const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+        // a row with nothing visible yet keeps m = -inf and contributes 0
+        const float ref_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
+        const float ref_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
+        const float al_lo = exp2f(m_lo - ref_lo), al_hi = exp2f(m_hi - ref_hi);
+        m_lo = mn_lo;
+        m_hi = mn_hi;
+        float ps_lo = 0.f, ps_hi = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            sc[j][0] = exp2f(sc[j][0] - ref_lo);
+            sc[j][1] = exp2f(sc[j][1] - ref_lo);
+            sc[j][2] = exp2f(sc[j][2] - ref_hi);
+            sc[j][3] = exp2f(sc[j][3] - ref_hi);
+            ps_lo += sc[j][0] + sc[j][1];
+            ps_hi += sc[j][2] + sc[j][3];
+        }
+        l_lo = l_lo * al_lo + ps_lo;
+        l_hi = l_hi * al_hi + ps_hi;
+#pragma unroll
+        for (int n = 0; n < NB; ++n) {
+            o[n][0] *= al_lo;
+            o[n][1] *= al_lo;
+            o[n][2] *= al_hi;
+            o[n][3] *= al_hi;
+        }
+        pa[0] = Mma<T>::pack(sc[0][0] * vscale, sc[0][1] * vscale);
+        pa[1] = Mma<T>::pack(sc[0][2] * vscale, sc[0][3] * vscale);
+        pa[2] = Mma<T>::pack(sc[1][0] * vscale, sc[1][1] * vscale);
+        pa[3] = Mma<T>::pack(sc[1][2] * vscale, sc[1][3] * vscale);
     }
 
     // One tile: rows [lo, hi) of this warp's 16 rows are visible (the caller
@@ -215,6 +283,52 @@ template <typename T, int D> struct GroupAttn {
         }
     }
 
+    // One tile of an int8 page: kq / vq = this warp's 16-row group of the K
+    // and V payloads in fragment order (kvc_quantize_pages): the lane's
+    // D / 2 bytes of each are the exact B fragments of its QK and PV MMAs,
+    // as 16-byte pieces interleaved across the warp (piece i of lane l at
+    // i * 512 + l * 16).  They become the integers s - zp in registers
+    // (koff / voff = 2^23 + 128 + zp); the scores take the page's K scale
+    // (folded into scale_log2) and the probabilities its V scale.  Every
+    // converted value is finite, and P is 0 past `hi`, so the rows past the
+    // split end need no zeroing.
+    __device__ __forceinline__ void tile_q8(const uint8_t *kq, const uint8_t *vq, int lane, int lo,
+                                            int hi, float scale_log2, float vscale, float koff,
+                                            float voff)
+    {
+        constexpr int NU = D / 32;  // 16-byte pieces of a lane's fragment bytes
+        uint4 kf[NU];
+#pragma unroll
+        for (int i = 0; i < NU; ++i)
+            kf[i] = *reinterpret_cast<const uint4 *>(kq + i * 512 + lane * 16);
+        const uint32_t *kw = reinterpret_cast<const uint32_t *>(kf);
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb) {
+                float f[4];
+                s8x4_minus(kw[nb * (D / 16) + kk], koff, f);
+                Mma<T>::run(sc[nb], qa[kk], Mma<T>::pack(f[0], f[1]), Mma<T>::pack(f[2], f[3]));
+            }
+        uint32_t pa[4];
+        softmax_step(sc, lane, lo, hi, scale_log2, vscale, pa);
+        uint4 vf[NU];
+#pragma unroll
+        for (int i = 0; i < NU; ++i)
+            vf[i] = *reinterpret_cast<const uint4 *>(vq + i * 512 + lane * 16);
+        const uint32_t *vw = reinterpret_cast<const uint32_t *>(vf);
+#pragma unroll
+        for (int nn = 0; nn < D / 16; ++nn)
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb) {
+                float f[4];
+                s8x4_minus(vw[nn * 2 + nb], voff, f);
+                Mma<T>::run(o[2 * nn + nb], pa, Mma<T>::pack(f[0], f[1]),
+                            Mma<T>::pack(f[2], f[3]));
+            }
+    }
+
     // finish l across the quad and publish (m, l, o) of heads < g for the
     // 4-warp merge: cm/cl [4][16], co [4][rows][D] (rows >= g)
     __device__ __forceinline__ void publish(float *cm, float *cl, float *co, int warp, int lane,
@@ -290,18 +404,24 @@ struct DecodeArgs {
     const int32_t *block_table;
     int max_pages, page_size;
     int64_t n_pool_pages;
+    // int8 pages (kvc_gqa_decode_paged_q): a table entry with KVC_PAGE_QUANT
+    // names page (entry & ~KVC_PAGE_QUANT) of these pools, read as
+    // (stored - zp) * scale with qparams[page] = (k_scale, k_zp, v_scale, v_zp)
+    const int8_t *qk_pool, *qv_pool;
+    const float *qparams;
+    int64_t n_q_pages;
 };
 
 // what the split kernel reads: the lengths arrays over a cache or a ring
 // (plain), seqlens_k with the append fused in (fused), or a paged cache
-enum : int { kPlain = 0, kFused = 1, kPaged = 2 };
+enum : int { kPlain = 0, kFused = 1, kPaged = 2, kPagedQ = 3 };
 
 // First logical row a split count starts from: the window's first visible
 // row, rounded down to a tile for a paged cache so that no tile straddles a
 // page (the rows below the window are masked).
 template <int MODE> __device__ __forceinline__ int split_origin(int vis0)
 {
-    return MODE == kPaged ? vis0 & ~(kTile - 1) : vis0;
+    return MODE >= kPaged ? vis0 & ~(kTile - 1) : vis0;
 }
 
 // (L, T) of batch row b: from the lengths arrays, or in the fused step from
@@ -372,14 +492,24 @@ __device__ __forceinline__ void row_check(const DecodeArgs &a, int b)
     }
 }
 
+// does entry e of a kPagedQ table name a valid int8 page?
+__device__ __forceinline__ bool int8_page(int e, const DecodeArgs &a)
+{
+    return e >= 0 && (e & KVC_PAGE_QUANT) && (int64_t)(e & ~KVC_PAGE_QUANT) < a.n_q_pages;
+}
+
 // One CTA per (split, kv head, batch row) for kvc_gqa_decode,
 // kvc_gqa_decode_ring and the fused kvc_decode_step; the split partials go
 // to decode_combine_kernel.  kFused: lengths from seqlens_k, and the CTA
 // holding the newest position places the new K/V row in its tile on chip
 // and stores it to the cache.  kPaged: tiles of 64 logical rows, each inside
-// one page; the producer warp reads the split's page ids at once.
+// one page; the producer warp reads the split's page ids at once.  kPagedQ:
+// the same over 16-bit and int8 pages (an int8 tile arrives by two 1-D bulk
+// copies at half the bytes and is expanded on chip before its MMAs).
+// (kPagedQ: at most as many registers as the CTAs its shared memory lets
+// share an SM can hold -- two at head_dim 128, three at 64)
 template <typename T, int D, int MODE>
-__global__ void __launch_bounds__(160)
+__global__ void __launch_bounds__(160, MODE == kPagedQ ? (D >= 128 ? 2 : 3) : 0)
 decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a)
 {
@@ -393,10 +523,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
+    // kPagedQ: the stage memory is a ring of NBAR slots of KT_BYTES; an int8
+    // tile (K and V payloads) takes one slot, a 16-bit tile two (K, V)
+    constexpr int NBAR = MODE == kPagedQ ? 2 * NS : NS;
     T *qs = reinterpret_cast<T *>(smem + NS * STAGE_BYTES);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * STAGE_BYTES + 16 * QS * 2);
-    uint64_t *empty = full + NS;
-    int *abort_flag = reinterpret_cast<int *>(empty + NS);
+    uint64_t *empty = full + NBAR;
+    int *abort_flag = reinterpret_cast<int *>(empty + NBAR);
     int *page_ids = abort_flag + 4;  // [32] paged: the split's pages
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -421,7 +554,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         q0 -= C;
     const int cnt_a = min(cnt, C - q0);
     // rows of tile t below the window (a paged cache's first tile only)
-    auto tile_lo = [&](int t) { return MODE == kPaged ? max(0, vis0 - (q0 + t * kTile)) : 0; };
+    auto tile_lo = [&](int t) { return MODE >= kPaged ? max(0, vis0 - (q0 + t * kTile)) : 0; };
     const int nt_a = (cnt_a + kTile - 1) / kTile;
     const int ntiles = nt_a + (cnt - cnt_a + kTile - 1) / kTile;
     // first slot and number of valid rows of tile t
@@ -433,7 +566,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int64_t row_base = ((int64_t)b * a.kv_heads + kvh) * a.capacity;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < NBAR; ++s) {
             kvc::mbar_init(&full[s], 1);
             kvc::mbar_init(&empty[s], kConsumers);
         }
@@ -445,13 +578,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     if (warp == kConsumers) {
         // ---------------- producer ----------------
         int page0 = 0;
-        if constexpr (MODE == kPaged) {
+        if constexpr (MODE >= kPaged) {
             // the pages this split touches, one lane each (at most 32)
             page0 = q0 / a.page_size;
             const int npages = (q0 + cnt - 1) / a.page_size - page0 + 1;
             if (lane < npages) {
                 int id = a.block_table[(int64_t)b * a.max_pages + page0 + lane];
-                if (id < 0 || (int64_t)id >= a.n_pool_pages) {
+                const bool q8 = MODE == kPagedQ && int8_page(id, a);
+                if (!q8 && (id < 0 || (int64_t)id >= a.n_pool_pages)) {
                     kvc::raise_status(a.status, KVC_DEV_INDEX_OOB);
                     id = 0;  // read a page that exists; the row's result is void
                 }
@@ -459,7 +593,50 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
             }
             __syncwarp();
         }
-        if (lane == 0) {
+        if (MODE == kPagedQ && lane == 0) {
+            kvc::tma_prefetch_desc(&tmap_k);
+            kvc::tma_prefetch_desc(&tmap_v);
+            int pos = 0;  // ring position of the next tile's first slot
+            for (int t = 0; t < ntiles; ++t) {
+                const int r = q0 + t * kTile;  // logical row, a multiple of 64
+                const int id = page_ids[r / a.page_size - page0];
+                const bool q8 = int8_page(id, a);
+                const int need = q8 ? 1 : 2;
+                bool stop = false;
+                for (int u = 0; u < need && !stop; ++u) {
+                    const int p = pos + u;
+                    if (p >= NBAR && !kvc::mbar_wait(&empty[p % NBAR], ((p / NBAR) - 1) & 1)) {
+                        kvc::raise_status(a.status, KVC_DEV_TIMEOUT);
+                        stop = true;
+                    }
+                }
+                if (stop || *reinterpret_cast<volatile int *>(abort_flag))
+                    break;
+                const int s0 = pos % NBAR, s1 = (pos + 1) % NBAR;
+                uint8_t *b0 = stages + s0 * KT_BYTES;
+                if (q8) {
+                    // the tile's 64 rows of K and of V payload, contiguous in the page
+                    const int64_t off =
+                        (((int64_t)(id & ~KVC_PAGE_QUANT) * a.kv_heads + kvh) * a.page_size +
+                         r % a.page_size) * D;
+                    kvc::mbar_arrive_expect_tx(&full[s0], 2 * kTile * D);
+                    kvc::bulk_load(b0, a.qk_pool + off, kTile * D, &full[s0]);
+                    kvc::bulk_load(b0 + kTile * D, a.qv_pool + off, kTile * D, &full[s0]);
+                } else {
+                    uint8_t *b1 = stages + s1 * KT_BYTES;
+                    const int32_t y = (int32_t)(((int64_t)id * a.kv_heads + kvh) * a.page_size +
+                                                r % a.page_size);
+                    kvc::mbar_arrive_expect_tx(&full[s0], KT_BYTES);
+                    kvc::mbar_arrive_expect_tx(&full[s1], KT_BYTES);
+#pragma unroll
+                    for (int bx = 0; bx < BOXES; ++bx) {
+                        kvc::tma_load_2d(b0 + bx * 8192, &tmap_k, bx * 64, y, &full[s0]);
+                        kvc::tma_load_2d(b1 + bx * 8192, &tmap_v, bx * 64, y, &full[s1]);
+                    }
+                }
+                pos += need;
+            }
+        } else if (lane == 0) {
             kvc::tma_prefetch_desc(&tmap_k);
             kvc::tma_prefetch_desc(&tmap_v);
             for (int t = 0; t < ntiles; ++t) {
@@ -472,15 +649,16 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     break;
                 uint8_t *kb = stages + s * STAGE_BYTES;
                 uint8_t *vb = kb + KT_BYTES;
-                kvc::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-                int32_t y;
-                if constexpr (MODE == kPaged) {
+                int32_t y = 0;
+                if constexpr (MODE >= kPaged) {
                     const int r = q0 + t * kTile;  // logical row, a multiple of 64
-                    const int64_t page = page_ids[r / a.page_size - page0];
-                    y = (int32_t)((page * a.kv_heads + kvh) * a.page_size + r % a.page_size);
+                    const int id = page_ids[r / a.page_size - page0];
+                    y = (int32_t)(((int64_t)id * a.kv_heads + kvh) * a.page_size +
+                                  r % a.page_size);
                 } else {
                     y = (int32_t)(row_base + tile_start(t));
                 }
+                kvc::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
 #pragma unroll
                 for (int bx = 0; bx < BOXES; ++bx) {
                     kvc::tma_load_2d(kb + bx * 8192, &tmap_k, bx * 64, y, &full[s]);
@@ -516,8 +694,81 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     ga.init();
     ga.load_q(qs, QS, lane);
     bool timed_out = false;
+    // kPagedQ: lane l holds the split's l-th table entry and, for an int8
+    // page, its (k_scale, k_zp, v_scale, v_zp); a tile takes them by shuffle
+    int my_e = 0;
+    float my_p[4] = {1.f, 0.f, 1.f, 0.f};
+    if constexpr (MODE == kPagedQ) {
+        const int pg0 = q0 / a.page_size;
+        if (lane < (q0 + cnt - 1) / a.page_size - pg0 + 1) {
+            my_e = a.block_table[(int64_t)b * a.max_pages + pg0 + lane];
+            if (int8_page(my_e, a)) {
+                const float4 pr = *reinterpret_cast<const float4 *>(
+                    a.qparams + 4 * (int64_t)(my_e & ~KVC_PAGE_QUANT));
+                my_p[0] = pr.x;
+                my_p[1] = pr.y;
+                my_p[2] = pr.z;
+                my_p[3] = pr.w;
+            } else {
+                my_e = 0;
+            }
+        }
+    }
 
-    for (int t = 0; t < ntiles; ++t) {
+    int pos = 0;  // kPagedQ: ring position of the tile's first slot
+    for (int t = 0; MODE == kPagedQ && t < ntiles; ++t) {
+        const int pi = (q0 + t * kTile) / a.page_size - q0 / a.page_size;
+        const bool q8 = (__shfl_sync(0xffffffffu, my_e, pi) & KVC_PAGE_QUANT) != 0;
+        const int s0 = pos % NBAR, s1 = (pos + 1) % NBAR;
+        if (!kvc::mbar_wait(&full[s0], (uint32_t)(pos / NBAR) & 1u) ||
+            (!q8 && !kvc::mbar_wait(&full[s1], (uint32_t)((pos + 1) / NBAR) & 1u))) {
+            timed_out = true;
+            break;
+        }
+        const int rows_t = tile_rows(t);
+        const int my_valid = min(16, max(0, rows_t - 16 * warp));
+        const int my_lo = min(16, max(0, tile_lo(t) - 16 * warp));
+        bool wrote = false;
+        if (q8) {
+            const float ks = __shfl_sync(0xffffffffu, my_p[0], pi);
+            const float kz = __shfl_sync(0xffffffffu, my_p[1], pi);
+            const float vs = __shfl_sync(0xffffffffu, my_p[2], pi);
+            const float vz = __shfl_sync(0xffffffffu, my_p[3], pi);
+            if (my_lo < my_valid) {
+                const uint8_t *base = stages + s0 * KT_BYTES;
+                ga.tile_q8(base + warp * 16 * D, base + kTile * D + warp * 16 * D, lane, my_lo,
+                           my_valid, a.scale_log2 * ks, vs, 8388608.f + 128.f + kz,
+                           8388608.f + 128.f + vz);
+            }
+        } else if (my_valid > 0) {
+            if (my_valid < 16) {
+                // rows past the split end: zero V so that 0 * garbage stays 0
+                uint8_t *vgen = stages + s1 * KT_BYTES;
+                for (int idx = lane; idx < (16 - my_valid) * BOXES * 8; idx += 32) {
+                    const int rr = 16 * warp + my_valid + idx / (BOXES * 8);
+                    const int bx = (idx / 8) % BOXES, c = idx % 8;
+                    *reinterpret_cast<uint4 *>(vgen + bx * 8192 + rr * 128 + c * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+                wrote = true;
+            }
+            if (my_lo < my_valid)
+                ga.tile(kvc::smem_u32(stages + s0 * KT_BYTES), kvc::smem_u32(stages + s1 * KT_BYTES),
+                        warp, lane, my_lo, my_valid, a.scale_log2);
+        }
+        if (wrote)
+            kvc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            kvc::mbar_arrive(&empty[s0]);
+            if (!q8)
+                kvc::mbar_arrive(&empty[s1]);
+        }
+        pos += q8 ? 1 : 2;
+    }
+
+    for (int t = 0; MODE != kPagedQ && t < ntiles; ++t) {
         const int s = t % NS, k = t / NS;
         if (!kvc::mbar_wait(&full[s], k & 1)) {
             timed_out = true;
@@ -1113,6 +1364,9 @@ struct PagedExtra {
     const int32_t *block_table;
     int max_pages, page_size;
     int64_t n_pool_pages;
+    const int8_t *qk_pool, *qv_pool;  // int8 pages (kvc_gqa_decode_paged_q), else NULL
+    const float *qparams;
+    int64_t n_q_pages;
 };
 
 // inputs of the fused step (kvc_decode_step) on top of the decode's own
@@ -1158,7 +1412,11 @@ kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const 
     a.sin_t = sin_t;
     a.rope_max_pos = rope_max_pos;
     a.split_rows = decode_split_rows(C);
-    a.max_splits = (int)decode_max_splits(C);
+    // int8 pages: twice the rows per split (the same bytes per CTA as a
+    // 16-bit split; fewer CTAs, so less of their fixed start and merge cost)
+    if (px && px->qk_pool && C >= 4096)
+        a.split_rows *= 2;
+    a.max_splits = (int)((C + a.split_rows - 1) / a.split_rows);
     const int64_t np = (int64_t)batch * q_heads * a.max_splits;
     a.ws_o = static_cast<float *>(workspace);
     a.ws_m = a.ws_o + np * D;
@@ -1179,13 +1437,18 @@ kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const 
         a.max_pages = px->max_pages;
         a.page_size = px->page_size;
         a.n_pool_pages = px->n_pool_pages;
+        a.qk_pool = px->qk_pool;
+        a.qv_pool = px->qv_pool;
+        a.qparams = px->qparams;
+        a.n_q_pages = px->n_q_pages;
     }
     constexpr int NS = decode_stages(D);
     const size_t smem = 1024 + (size_t)NS * 2 * kTile * D * 2 + 16 * (D + 8) * 2 +
-                        2 * NS * sizeof(uint64_t) + 16 + 32 * sizeof(int);
-    auto kern = fx   ? decode_split_kernel<T, D, kFused>
-                : px ? decode_split_kernel<T, D, kPaged>
-                     : decode_split_kernel<T, D, kPlain>;
+                        4 * NS * sizeof(uint64_t) + 16 + 32 * sizeof(int);
+    auto kern = fx                 ? decode_split_kernel<T, D, kFused>
+                : px && px->qk_pool ? decode_split_kernel<T, D, kPagedQ>
+                : px               ? decode_split_kernel<T, D, kPaged>
+                                   : decode_split_kernel<T, D, kPlain>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return KVC_ERR_CUDA;
@@ -1316,15 +1579,16 @@ KVC_API kvc_status kvc_gqa_decode_ring(void *out, const void *q, const void *k_c
                         rope_max_pos, workspace, workspace_bytes, 1, dev_status, stream);
 }
 
-KVC_API kvc_status kvc_gqa_decode_paged(void *out, const void *q, const void *k_pool,
-                                        const void *v_pool, const int32_t *block_table,
-                                        int max_pages, int64_t n_pool_pages, int page_size,
-                                        kvc_lengths len, int batch, int q_heads, int kv_heads,
-                                        int head_dim, int dtype, int local_window_size,
-                                        float scale, const float *rope_cos,
-                                        const float *rope_sin, int64_t rope_max_pos,
-                                        void *workspace, size_t workspace_bytes,
-                                        int32_t *dev_status, void *stream)
+namespace {
+
+kvc_status paged_decode_entry(void *out, const void *q, const void *k_pool, const void *v_pool,
+                              const int8_t *qk_pool, const int8_t *qv_pool, const float *qparams,
+                              int64_t n_q_pages, const int32_t *block_table, int max_pages,
+                              int64_t n_pool_pages, int page_size, kvc_lengths len, int batch,
+                              int q_heads, int kv_heads, int head_dim, int dtype,
+                              int local_window_size, float scale, const float *rope_cos,
+                              const float *rope_sin, int64_t rope_max_pos, void *workspace,
+                              size_t workspace_bytes, int32_t *dev_status, void *stream)
 {
     if (dtype != KVC_BF16 && dtype != KVC_F16)
         return dtype == KVC_F32 ? KVC_ERR_UNSUPPORTED : KVC_ERR_DTYPE;
@@ -1361,7 +1625,8 @@ KVC_API kvc_status kvc_gqa_decode_paged(void *out, const void *q, const void *k_
         return KVC_ERR_ALIGN;
     if (scale == 0.f)
         scale = 1.0f / sqrtf((float)head_dim);
-    const PagedExtra px{block_table, max_pages, page_size, n_pool_pages};
+    const PagedExtra px{block_table, max_pages, page_size, n_pool_pages, qk_pool, qv_pool, qparams,
+                        n_q_pages};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dtype == KVC_BF16)
         return head_dim == 64
@@ -1383,6 +1648,57 @@ KVC_API kvc_status kvc_gqa_decode_paged(void *out, const void *q, const void *k_
                                               kv_heads, capacity, local_window_size, scale,
                                               rope_cos, rope_sin, rope_max_pos, workspace, 0,
                                               dev_status, st, nullptr, &px);
+}
+
+} // namespace
+
+KVC_API kvc_status kvc_gqa_decode_paged(void *out, const void *q, const void *k_pool,
+                                        const void *v_pool, const int32_t *block_table,
+                                        int max_pages, int64_t n_pool_pages, int page_size,
+                                        kvc_lengths len, int batch, int q_heads, int kv_heads,
+                                        int head_dim, int dtype, int local_window_size,
+                                        float scale, const float *rope_cos,
+                                        const float *rope_sin, int64_t rope_max_pos,
+                                        void *workspace, size_t workspace_bytes,
+                                        int32_t *dev_status, void *stream)
+{
+    return paged_decode_entry(out, q, k_pool, v_pool, nullptr, nullptr, nullptr, 0, block_table,
+                              max_pages, n_pool_pages, page_size, len, batch, q_heads, kv_heads,
+                              head_dim, dtype, local_window_size, scale, rope_cos, rope_sin,
+                              rope_max_pos, workspace, workspace_bytes, dev_status, stream);
+}
+
+KVC_API kvc_status kvc_gqa_decode_paged_q(void *out, const void *q, const void *k_pool,
+                                          const void *v_pool, const void *qk_pool,
+                                          const void *qv_pool, const float *qparams,
+                                          int64_t n_qpool_pages, const int32_t *block_table,
+                                          int max_pages, int64_t n_pool_pages, int page_size,
+                                          kvc_lengths len, int batch, int q_heads, int kv_heads,
+                                          int head_dim, int dtype, int local_window_size,
+                                          float scale, const float *rope_cos,
+                                          const float *rope_sin, int64_t rope_max_pos,
+                                          void *workspace, size_t workspace_bytes,
+                                          int32_t *dev_status, void *stream)
+{
+    if (n_qpool_pages < 1 || n_qpool_pages * kv_heads * (int64_t)page_size * head_dim >
+                                 ((int64_t)1 << 40))
+        return KVC_ERR_SHAPE;
+    if (batch > 0) {
+        if (!qk_pool || !qv_pool || !qparams)
+            return KVC_ERR_NULL;
+        for (const void *p : {qk_pool, qv_pool, (const void *)qparams})
+            if (!kvc_host::aligned16(p))
+                return KVC_ERR_ALIGN;
+        const size_t qb = (size_t)n_qpool_pages * kv_heads * page_size * head_dim;
+        if (kvc_host::overlaps(qk_pool, qb, qv_pool, qb))
+            return KVC_ERR_SHAPE;
+    }
+    return paged_decode_entry(out, q, k_pool, v_pool, static_cast<const int8_t *>(qk_pool),
+                              static_cast<const int8_t *>(qv_pool), qparams, n_qpool_pages,
+                              block_table, max_pages, n_pool_pages, page_size, len, batch,
+                              q_heads, kv_heads, head_dim, dtype, local_window_size, scale,
+                              rope_cos, rope_sin, rope_max_pos, workspace, workspace_bytes,
+                              dev_status, stream);
 }
 
 // --------------------------------------------------------------------------

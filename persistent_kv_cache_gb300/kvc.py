@@ -36,9 +36,11 @@ EXPORTS = ("kvc_tensor_scatter", "kvc_seq_lengths", "kvc_window_append", "kvc_gq
            "kvc_gqa_decode_workspace_size", "kvc_gqa_decode_noalloc", "kvc_gqa_decode_ring",
            "kvc_decode_step", "kvc_decode_step_workspace_size", "kvc_window_decode_step",
            "kvc_paged_append", "kvc_gqa_decode_paged", "kvc_window_append_inplace",
+           "kvc_quantize_pages", "kvc_gqa_decode_paged_q",
            "kvc_gqa_prefill_chunk", "kvc_gqa_prefill_workspace_size", "kvc_status_string",
            "kvc_abi_version")
 KVC_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
+KVC_PAGE_QUANT = 0x40000000  # block-table flag: the entry names an int8 page
 
 
 class KvcLibraryMissing(RuntimeError):
@@ -102,6 +104,10 @@ def library() -> ctypes.CDLL:
             "kvc_paged_append": [P, P, P, P, P, I, I64, I, L, I, I, I, I, I, P, P, I64, P, P],
             "kvc_gqa_decode_paged": [P, P, P, P, P, I, I64, I, L, I, I, I, I, I, I, F, P, P, I64,
                                      P, SZ, P, P],
+            "kvc_quantize_pages": [P, P, P, P, P, P, I, I64, I64, I, I, I, I, F, I, I, F, I, I, P,
+                                   P, P],
+            "kvc_gqa_decode_paged_q": [P, P, P, P, P, P, P, I64, P, I, I64, I, L, I, I, I, I, I, I,
+                                       F, P, P, I64, P, SZ, P, P],
             "kvc_decode_step": [P, P, P, P, P, P, P, L, I, I, I, I64, I, I, I, I, F, P, P, I64, P,
                                 SZ, P, P],
             "kvc_decode_step_workspace_size": [I, I, I, I64, I, I],
@@ -246,6 +252,42 @@ def kvc_paged_append(k_pool, v_pool, new_k, new_v, block_table, lengths, rope=No
         _ptr(k_pool), _ptr(v_pool), _ptr(new_k), _ptr(new_v), _ptr(block_table),
         block_table.shape[1], n_pages, ps, lengths.c(), B, Hkv, S, D, _dtype_code(k_pool), cs,
         sn, rmax, _ptr(status), _stream(stream)))
+
+
+def kvc_quantize_pages(k_pool, v_pool, qk_pool, qv_pool, src_pages, dst_pages, qparams, k_scale,
+                       k_zero_point=0, k_unsigned=False, v_scale=None, v_zero_point=None,
+                       v_unsigned=None, status=None, stream=None):
+    """Int8 pages dst_pages[i] <- 16-bit pages src_pages[i] (include/kvc.h); V takes K's
+    format unless given its own."""
+    n_pool, Hkv, ps, D = k_pool.shape
+    v_scale = k_scale if v_scale is None else v_scale
+    v_zero_point = k_zero_point if v_zero_point is None else v_zero_point
+    v_unsigned = k_unsigned if v_unsigned is None else v_unsigned
+    _check("kvc_quantize_pages", library().kvc_quantize_pages(
+        _ptr(k_pool), _ptr(v_pool), _ptr(qk_pool), _ptr(qv_pool), _ptr(src_pages),
+        _ptr(dst_pages), src_pages.numel(), n_pool, qk_pool.shape[0], ps, Hkv, D,
+        _dtype_code(k_pool), float(k_scale), int(k_zero_point), int(bool(k_unsigned)),
+        float(v_scale), int(v_zero_point), int(bool(v_unsigned)), _ptr(qparams), _ptr(status),
+        _stream(stream)))
+
+
+def kvc_gqa_decode_paged_q(out, q, k_pool, v_pool, qk_pool, qv_pool, qparams, block_table,
+                           lengths, local_window_size=0, scale=0.0, rope=None, workspace=None,
+                           status=None, stream=None):
+    """kvc_gqa_decode_paged over 16-bit and int8 pages (include/kvc.h)."""
+    B, Hq, _, D = q.shape
+    n_pages, Hkv, ps, _ = k_pool.shape
+    max_pages = block_table.shape[1]
+    if workspace is None:
+        n = kvc_gqa_decode_workspace_size(B, Hq, Hkv, max_pages * ps, D, _dtype_code(q))
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    cs, sn, rmax = _rope(rope)
+    _check("kvc_gqa_decode_paged_q", library().kvc_gqa_decode_paged_q(
+        _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(qk_pool), _ptr(qv_pool),
+        _ptr(qparams), qk_pool.shape[0], _ptr(block_table), max_pages, n_pages, ps, lengths.c(),
+        B, Hq, Hkv, D, _dtype_code(q), local_window_size, scale, cs, sn, rmax, _ptr(workspace),
+        workspace.numel(), _ptr(status), _stream(stream)))
+    return out
 
 
 def kvc_gqa_decode_paged(out, q, k_pool, v_pool, block_table, lengths, local_window_size=0,

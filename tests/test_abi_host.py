@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(kvc):
 
 
 def test_version_and_strings(kvc):
-    assert kvc.kvc_abi_version() == 4
+    assert kvc.kvc_abi_version() == 5
     assert kvc.kvc_status_string(0) == "ok"
     assert "window" in kvc.kvc_status_string(7)
 
@@ -232,3 +232,40 @@ def test_append_inplace_host_checks(kvc):
     assert f(FAKE, FAKE + 16, FAKE * 3, FAKE * 4, L, *ok) == 2      # K and V rows overlap
     assert f(*far, *ok[:9], FAKE, None, 16, None, None) == 1        # half a rope table
     assert f(*far, 0, *ok[1:]) == 0                                 # empty batch
+
+
+def test_quantize_pages_host_checks(kvc):
+    lib = kvc.library()
+    f = lib.kvc_quantize_pages
+    # (k, v, qk, qv, src, dst, n, n_pool, n_q, page, kv_heads, D, dtype, k_scale, k_zp, k_uns,
+    #  v_scale, v_zp, v_uns, qparams, status, stream)
+    ptr = [FAKE, 1 << 32, 2 << 32, 3 << 32, FAKE * 5, FAKE * 6]
+    ok = [4, 8, 8, 64, 2, 128, 1, 0.01, 0, 0, 0.01, 128, 1, FAKE * 7, None, None]
+    assert f(*ptr, *ok[:6], 0, *ok[7:]) == 5                        # fp32 pools
+    assert f(*ptr, *ok[:6], 9, *ok[7:]) == 3                        # unknown dtype
+    assert f(*ptr, *ok[:5], 12, *ok[6:]) == 2                       # head_dim not a multiple of 8
+    assert f(*ptr, *ok[:7], 0.0, *ok[8:]) == 2                      # scale 0
+    assert f(*ptr, *ok[:7], float("nan"), *ok[8:]) == 2             # scale NaN
+    assert f(*ptr, *ok[:7], float("inf"), *ok[8:]) == 2
+    assert f(*ptr, *ok[:8], 200, *ok[9:]) == 2                      # INT8 zero point 200
+    assert f(*ptr, *ok[:11], -1, *ok[12:]) == 2                     # UINT8 zero point -1
+    assert f(*ptr, 0, *ok[1:]) == 0                                 # nothing to convert
+    assert f(None, *ptr[1:], *ok) == 1
+    assert f(FAKE + 8, *ptr[1:], *ok) == 4                          # alignment
+    assert f(*ptr[:2], FAKE * 9, FAKE * 9 + 16, *ptr[4:], *ok) == 2  # int8 pools overlap
+
+
+def test_decode_paged_q_host_checks(kvc):
+    lib = kvc.library()
+    f = lib.kvc_gqa_decode_paged_q
+    L = _lengths(kvc)
+    # (out, q, k, v, qk, qv, qparams, n_q, table, max_pages, n_pool, page, len, B, Hq, Hkv, D,
+    #  dtype, W, scale, cos, sin, rope_max, ws, ws_bytes, status, stream)
+    pools = [FAKE, FAKE * 2, FAKE * 3, 1 << 32, 2 << 32, 3 << 32, FAKE * 4]
+    tail = [FAKE * 5, 8, 64, 64, L, 2, 8, 2, 128, 1, 0, 0.0, None, None, 0, FAKE, 1 << 24, None,
+            None]
+    assert f(*pools, 0, *tail) == 2                                  # no int8 pages
+    assert f(*pools[:4], None, *pools[5:], 8, *tail) == 1            # int8 pool missing
+    assert f(*pools[:6], FAKE * 4 + 4, 8, *tail) == 4                # qparams alignment
+    assert f(*pools[:4], 4 << 32, (4 << 32) + 16, pools[6], 8, *tail) == 2  # int8 pools overlap
+    assert f(*pools, 8, *tail[:3], 48, *tail[4:]) == 2               # page not a multiple of 64
