@@ -184,6 +184,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
     }
 }
 
+// programmatic dependent launch: the next kernel of the stream, if launched
+// with programmatic serialisation, may be scheduled once every CTA of this
+// grid has signalled (or exited); a kernel so launched waits, before reading
+// what the kernels before it wrote, until they have completed and their
+// writes are visible (without the launch attribute both are no-ops)
+__device__ __forceinline__ void grid_dep_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// asks L2 for `bytes` (a multiple of 16) at a 16-byte aligned global address;
+// the copy lands nowhere else and nothing waits for it
+__device__ __forceinline__ void prefetch_l2(const void *gsrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                     reinterpret_cast<uint64_t>(gsrc)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

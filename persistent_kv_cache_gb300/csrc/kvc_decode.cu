@@ -925,17 +925,20 @@ decode_combine_kernel(const DecodeArgs a, int D)
 // "Design": rows [E, Lp) move to [0, Lp - E) and the new row goes to Lp - E;
 // Lp, E, L from the windowed formula or from the drifting layout of the PR's
 // CPU commit).  One CTA owns one (batch row, kv head) slice and keeps the new
-// window in shared memory.  One thread brings the old rows in with 64-row TMA
-// boxes (window row r from cache row r + E) while the others rotate the query
-// and the new row.  When rows were evicted, the window goes back E rows lower
-// by TMA stores of its full 64-row tiles (and thread stores of a last partial
-// one), drained only before the merge reuses the shared memory, so they
-// overlap the attention; otherwise only the rows the window can see are
-// loaded and only the new row is stored.  A ring of C slots ("Stateful
-// decode & KV cache", "Sliding-window ring buffer") never moves: its slots
-// are loaded in slot order, the new row replaces slot (T - 1) mod C, and the
-// attention masks the slots by position (the visible ones are at most two
-// runs of slots).
+// window in shared memory.  The step is bound by latency, not bandwidth, so
+// the slice's rows are asked of L2 at entry, before seqlens_k has arrived;
+// once it has, one thread brings the old rows in with 64-row TMA boxes
+// (window row r from cache row r + E), one mbarrier per tile, while the
+// others rotate the query and the new row.  The tiles are then taken in
+// order as they land: the new row and the zeroed rows are placed in theirs,
+// a tile goes back E rows lower by TMA store as soon as it is final (the
+// stores of tile t only overwrite cache rows that tiles <= t were loaded
+// from), and the warps run its attention.  A last partial tile goes back by
+// thread stores; without an eviction only the new row is stored.  A ring of
+// C slots ("Stateful decode & KV cache", "Sliding-window ring buffer") never
+// moves: its slots are loaded in slot order, the new row replaces slot
+// (T - 1) mod C, and the attention masks the slots by position (the visible
+// ones are at most two runs of slots).
 // --------------------------------------------------------------------------
 struct WindowStepArgs {
     void *out;
@@ -976,7 +979,7 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
     uint8_t *tiles = smem;  // tile t: K at t * 2 * KT_BYTES, V after it
     T *qs = reinterpret_cast<T *>(smem + (size_t)ntile_max * 2 * KT_BYTES);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + (size_t)ntile_max * 2 * KT_BYTES +
-                                                 16 * QS * 2);
+                                                 16 * QS * 2);  // [ntile_max]
     // byte offset of row r, 16-byte chunk c of the K (is_v = 0) or V tile
     auto at = [&](bool is_v, int r, int c) {
         return tiles + (size_t)(r / kTile) * 2 * KT_BYTES + (is_v ? KT_BYTES : 0) +
@@ -987,6 +990,28 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int b = blockIdx.x / a.kv_heads, kvh = blockIdx.x % a.kv_heads;
     const int g = a.group;
     const int64_t slice = (int64_t)b * a.kv_heads + kvh;
+
+    // the slice's rows are asked of L2 at once when the step loads all of
+    // them but the ones past its length: with C - W < 64 the first visible
+    // row is always in tile 0, so every step loads tiles 0 .. its last one
+    if (threadIdx.x == 0) {
+        if (C - a.window < kTile) {
+            const uint32_t sb = (uint32_t)(C * D * sizeof(T));
+            kvc::prefetch_l2(static_cast<const T *>(a.k_cache) + slice * C * D, sb);
+            kvc::prefetch_l2(static_cast<const T *>(a.v_cache) + slice * C * D, sb);
+        }
+        for (int t = 0; t < ntile_max; ++t)
+            kvc::mbar_init(&bar[t], 1);
+        kvc::fence_mbar_init();
+        kvc::tma_prefetch_desc(&tmap_k);
+        kvc::tma_prefetch_desc(&tmap_v);
+    }
+    // the L2 requests above are hints and read nothing into the CTA; all
+    // else waits for the kernels before this one (launched with
+    // programmatic serialisation, the next step's kernel can meanwhile be
+    // scheduled and ask L2 for its own rows)
+    kvc::grid_dep_launch();
+    kvc::grid_dep_wait();
 
     // 0. what does not depend on the lengths is loaded at once, beside
     //    seqlens_k: the group's query pairs (i, i + D/2) and the new row
@@ -1067,25 +1092,17 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
     const int ntiles = ring ? (int)((C + kTile - 1) / kTile) : (L + kTile - 1) / kTile;
 
-    // 1. one thread starts the TMA loads of the old rows
+    // 1. one thread starts the TMA loads of the old rows, one barrier a tile
     if (threadIdx.x == 0) {
-        kvc::mbar_init(bar, 1);
-        kvc::fence_mbar_init();
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        kvc::tma_prefetch_desc(&tmap_k);
-        kvc::tma_prefetch_desc(&tmap_v);
-        const uint32_t bytes = t_hi > t_lo ? (uint32_t)(t_hi - t_lo) * 2u * KT_BYTES : 0u;
-        kvc::mbar_arrive_expect_tx(bar, bytes);
         for (int t = t_lo; t < t_hi; ++t) {
             const int32_t y = (int32_t)(row0 + src_off + t * kTile);
+            kvc::mbar_arrive_expect_tx(&bar[t], 2u * KT_BYTES);
 #pragma unroll
             for (int bx = 0; bx < BOXES; ++bx) {
                 kvc::tma_load_2d(tiles + (size_t)t * 2 * KT_BYTES + bx * 8192, &tmap_k, bx * 64,
-                                 y, bar);
+                                 y, &bar[t]);
                 kvc::tma_load_2d(tiles + (size_t)t * 2 * KT_BYTES + KT_BYTES + bx * 8192,
-                                 &tmap_v, bx * 64, y, bar);
+                                 &tmap_v, bx * 64, y, &bar[t]);
             }
         }
     }
@@ -1111,79 +1128,22 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
         new_hi = kvc::Elem<T>::from_f32(hi);
     }
 
-    // 3. wait for the old rows; place the new row; zero V wherever a row
-    //    that attention might touch holds no token of the window (0 * stale
-    //    bytes must stay 0)
-    bool ok = kvc::mbar_wait(bar, 0);
-    if (!ok) {
-        if (threadIdx.x == 0)
-            kvc::raise_status(a.status, KVC_DEV_TIMEOUT);
-        kvc::mbar_wait(bar, 0);  // let the copies land before the CTA can exit
-        return;
-    }
-    if (row_thread) {
-        const int c_lo = row_i / 8, c_hi = (row_i + D / 2) / 8;
-        *reinterpret_cast<T *>(at(row_is_v, new_r, c_lo) + (row_i % 8) * 2) = new_lo;
-        *reinterpret_cast<T *>(at(row_is_v, new_r, c_hi) + ((row_i + D / 2) % 8) * 2) = new_hi;
-    }
-    {
-        // rows past the window in its last tile; for a ring, the slots never
-        // written (T <= C) and the slots past C
-        int z0, z1;
-        if (ring) {
-            z0 = T_ < C ? (int)T_ : (int)C;
-            z1 = ntiles * kTile;
-        } else {
-            z0 = L;
-            z1 = ntiles * kTile;
-        }
-        const int n = (z1 - z0) * CPR;
-        for (int idx = threadIdx.x; idx < n; idx += 128) {
-            const int r = z0 + idx / CPR, c = idx % CPR;
-            *reinterpret_cast<uint4 *>(at(true, r, c)) = make_uint4(0, 0, 0, 0);
-        }
-    }
-    kvc::fence_proxy_async_smem();
-    __syncthreads();
-
-    // 4. write back: the whole window E rows lower when rows moved (full
-    //    64-row tiles by TMA store, a last partial tile by the threads),
-    //    otherwise the new row alone
-    int stored_tiles = 0;
-    if (moves) {
-        stored_tiles = L / kTile;
-        if (threadIdx.x == 0 && stored_tiles > 0) {
-            for (int t = 0; t < stored_tiles; ++t) {
-                const int32_t y = (int32_t)(row0 + t * kTile);
-#pragma unroll
-                for (int bx = 0; bx < BOXES; ++bx) {
-                    kvc::tma_store_2d(&tmap_k, bx * 64, y,
-                                      tiles + (size_t)t * 2 * KT_BYTES + bx * 8192);
-                    kvc::tma_store_2d(&tmap_v, bx * 64, y,
-                                      tiles + (size_t)t * 2 * KT_BYTES + KT_BYTES + bx * 8192);
-                }
-            }
-            kvc::tma_store_commit();
-        }
-        const int r_first = stored_tiles * kTile;
-        const int n = (L - r_first) * CPR;
-        for (int idx = threadIdx.x; idx < 2 * n; idx += 128) {
-            const bool is_v = idx >= n;
-            const int w = is_v ? idx - n : idx;
-            const int r = r_first + w / CPR, c = w % CPR;
-            *reinterpret_cast<uint4 *>((is_v ? vc : kc) + (int64_t)r * D + c * 8) =
-                *reinterpret_cast<const uint4 *>(at(is_v, r, c));
-        }
-    } else if (row_thread) {
+    // the new row goes to shared memory and, without an eviction, straight
+    // to its cache row (a load of that row, if any, is overwritten below)
+    if (!moves && row_thread) {
         T *dst = (row_is_v ? vc : kc) + (int64_t)new_r * D;
         dst[row_i] = new_lo;
         dst[row_i + D / 2] = new_hi;
     }
 
-    // 5. attention over the rows the window sees
-    GroupAttn<T, D> ga;
-    ga.init();
-    ga.load_q(qs, QS, lane);
+    // rows whose V is zeroed: wherever attention might touch a row that
+    // holds no token of the window (0 * stale bytes must stay 0) -- rows past
+    // the window in its last tile; for a ring, the slots never written
+    // (T <= C) and the slots past C
+    const int z0 = ring ? (T_ < C ? (int)T_ : (int)C) : L;
+    const int z1 = ntiles * kTile;
+    const int stored_tiles = moves ? L / kTile : 0;  // full tiles stored by TMA
+
     // visible rows: [vis0, L) of the window, or for a ring the nvis slots
     // ending at new_r (one run, or [0, new_r] and [C - rest, C))
     int lo1 = vis0, hi1 = L, lo2 = 0, hi2 = 0;
@@ -1199,19 +1159,80 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
             hi2 = (int)C;
         }
     }
+
+    // 3-5. the tiles in order: wait for the tile, place what belongs in it,
+    //      store it back when rows moved, run its attention
+    __syncthreads();  // the barriers' initialisation is visible to all threads
+    GroupAttn<T, D> ga;
+    ga.init();
+    ga.load_q(qs, QS, lane);
+    // (a wait that runs out marks this thread; the loop goes on, skipping
+    // the work, so that every thread meets the same barriers)
+    bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
-        const int r0 = t * kTile + 16 * warp;  // this warp's 16 rows of the tile
+        if (t >= t_lo && t < t_hi && !kvc::mbar_wait(&bar[t], 0))
+            ok = false;
+        const int r_lo = t * kTile, r_hi = r_lo + kTile;
+        const bool has_new = new_r >= r_lo && new_r < r_hi;
+        const int zl = max(z0, r_lo), zh = min(z1, r_hi);
+        if (has_new || zh > zl) {
+            if (has_new && row_thread) {
+                const int c_lo = row_i / 8, c_hi = (row_i + D / 2) / 8;
+                *reinterpret_cast<T *>(at(row_is_v, new_r, c_lo) + (row_i % 8) * 2) = new_lo;
+                *reinterpret_cast<T *>(at(row_is_v, new_r, c_hi) + ((row_i + D / 2) % 8) * 2) =
+                    new_hi;
+            }
+            for (int idx = threadIdx.x; idx < (zh - zl) * CPR; idx += 128)
+                *reinterpret_cast<uint4 *>(at(true, zl + idx / CPR, idx % CPR)) =
+                    make_uint4(0, 0, 0, 0);
+            kvc::fence_proxy_async_smem();
+            __syncthreads();
+        }
+        if (t < stored_tiles) {
+            if (threadIdx.x == 0 && ok) {
+                const int32_t y = (int32_t)(row0 + r_lo);
+#pragma unroll
+                for (int bx = 0; bx < BOXES; ++bx) {
+                    kvc::tma_store_2d(&tmap_k, bx * 64, y,
+                                      tiles + (size_t)t * 2 * KT_BYTES + bx * 8192);
+                    kvc::tma_store_2d(&tmap_v, bx * 64, y,
+                                      tiles + (size_t)t * 2 * KT_BYTES + KT_BYTES + bx * 8192);
+                }
+                kvc::tma_store_commit();
+            }
+        } else if (moves && r_lo < L && ok) {
+            // the last, partial tile: rows [r_lo, L) by the threads (its
+            // final contents were made visible by the barrier above)
+            const int n = (L - r_lo) * CPR;
+            for (int idx = threadIdx.x; idx < 2 * n; idx += 128) {
+                const bool is_v = idx >= n;
+                const int w = is_v ? idx - n : idx;
+                const int r = r_lo + w / CPR, c = w % CPR;
+                *reinterpret_cast<uint4 *>((is_v ? vc : kc) + (int64_t)r * D + c * 8) =
+                    *reinterpret_cast<const uint4 *>(at(is_v, r, c));
+            }
+        }
+        const int r0 = r_lo + 16 * warp;  // this warp's 16 rows of the tile
         const uint32_t kb = kvc::smem_u32(tiles + (size_t)t * 2 * KT_BYTES);
         const int l1 = min(16, max(0, lo1 - r0)), h1 = min(16, max(0, hi1 - r0));
         const int l2 = min(16, max(0, lo2 - r0)), h2 = min(16, max(0, hi2 - r0));
-        if (h1 > l1)
+        if (ok && h1 > l1)
             ga.tile(kb, kb + KT_BYTES, warp, lane, l1, h1, a.scale_log2);
-        if (h2 > l2)
+        if (ok && h2 > l2)
             ga.tile(kb, kb + KT_BYTES, warp, lane, l2, h2, a.scale_log2);
     }
     if (threadIdx.x == 0 && stored_tiles > 0)
         kvc::tma_store_wait_read();  // the merge below reuses the tiles' memory
-    __syncthreads();
+    if (!__syncthreads_and(ok)) {
+        // a tile that never landed: report it, let every copy in flight land
+        // (each wait bounded) and leave the output unwritten
+        if (threadIdx.x == 0) {
+            kvc::raise_status(a.status, KVC_DEV_TIMEOUT);
+            for (int t = t_lo; t < t_hi; ++t)
+                kvc::mbar_wait(&bar[t], 0);
+        }
+        return;
+    }
 
     // 6. merge the four warps and write the group's output rows
     float *cm = reinterpret_cast<float *>(smem);
@@ -1226,8 +1247,6 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
         const int64_t qrow = (int64_t)b * a.q_heads + kvh * g + h;
         static_cast<T *>(a.out)[qrow * D + d] = kvc::Elem<T>::from_f32(osum / lsum);
     }
-    if (threadIdx.x == 0 && stored_tiles > 0)
-        kvc::tma_store_wait_all();  // the window's stores complete before the CTA retires
 }
 
 } // namespace
@@ -1800,7 +1819,7 @@ template <typename T, int D>
 kvc_status launch_window_step(const WindowStepArgs &a, int batch, cudaStream_t stream)
 {
     const int64_t ntile_max = (a.capacity + kTile - 1) / kTile;
-    size_t smem = 1024 + (size_t)ntile_max * 2 * kTile * D * 2 + 16 * (D + 8) * 2 + 16;
+    size_t smem = 1024 + (size_t)ntile_max * 2 * kTile * D * 2 + 16 * (D + 8) * 2 + 8 * ntile_max;
     const size_t merge = 1024 + kConsumers * 16 * (2 + D) * sizeof(float);
     smem = smem > merge ? smem : merge;
     const CUtensorMapDataType tt = std::is_same<T, __half>::value
@@ -1817,7 +1836,18 @@ kvc_status launch_window_step(const WindowStepArgs &a, int batch, cudaStream_t s
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return KVC_ERR_CUDA;
-    kern<<<(unsigned)(batch * a.kv_heads), 128, smem, stream>>>(tk, tv, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(batch * a.kv_heads));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tk, tv, a) != cudaSuccess)
+        return KVC_ERR_CUDA;
     return kvc_host::launch_status();
 }
 
