@@ -1032,6 +1032,20 @@ def run_ours(args):
                 "issued_tflops": wl.issued_flops / (kern_ms / 1e3) / 1e12,
                 "algorithmic_flops_per_launch": wl.flops}
         extra = {"stage_and_cache_gbs": wl.bytes_per_step * args.steps / sec / 1e9}
+        # a chunk whose flops per algorithmic byte sit below the ridge point
+        # of the two measured peaks is bound by HBM, not by the tensor pipe:
+        # the roofline is then the bytes' (the tensor figures stay beside it)
+        ai = wl.flops / wl.kernel_bytes
+        ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+        if ai < ridge:
+            gbs = wl.kernel_bytes / (kern_ms / 1e3) / 1e9
+            roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": gbs / peaks["hbm_gbs"], "peak_kind": peak_kind,
+                    "algorithmic_bytes_per_launch": wl.kernel_bytes,
+                    "flops_per_byte": ai, "ridge_flops_per_byte": ridge,
+                    "tensor_achieved_tflops": achieved, "tensor_frac": achieved / peak,
+                    "tensor_peak_kind": f"{peak_kind} bf16 burst",
+                    "algorithmic_flops_per_launch": wl.flops}
     else:
         value = wl.bytes_per_step * args.steps * world / sec / 1e9
         e2e_value = wl.bytes_per_step * args.steps * world / e2e_s / 1e9

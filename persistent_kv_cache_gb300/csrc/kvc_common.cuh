@@ -291,6 +291,17 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// 4-D tiled TMA load (see tma_load_2d; x is the innermost coordinate)
+__device__ __forceinline__ void tma_load_4d(void *smem_dst, const CUtensorMap *map, int32_t x,
+                                            int32_t y, int32_t z, int32_t w, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // byte offset of 16-byte chunk `c` (0..7) of row `r` inside a box written by
 // TMA with 128-byte swizzle (rows of 128 bytes, 1024-byte aligned box)
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c)
@@ -350,6 +361,13 @@ bool encode_3d_sw128(CUtensorMap *map, const void *base, uint64_t rows, uint64_t
 bool encode_4d_heads_sw128(CUtensorMap *map, const void *base, uint64_t heads, uint64_t rows,
                            uint64_t cols, uint32_t elem_bytes, uint32_t box_rows,
                            uint32_t box_heads, CUtensorMapDataType type);
+
+// the same tensor as (span, rows, heads, column blocks): a box of (span,
+// box_rows, box_heads, every block) lands as [blocks][box_heads][box_rows]
+// [128 B], i.e. column block by column block, the heads' rows stacked
+bool encode_4d_blocks_sw128(CUtensorMap *map, const void *base, uint64_t heads, uint64_t rows,
+                            uint64_t cols, uint32_t elem_bytes, uint32_t box_rows,
+                            uint32_t box_heads, CUtensorMapDataType type);
 
 } // namespace kvc_host
 

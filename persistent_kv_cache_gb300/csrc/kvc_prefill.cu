@@ -11,14 +11,17 @@
 //   TMEM columns  O [0, D) fp32 | S/P double buffer [D, D + 256)
 //   shared mem    Q tile (128 x D, 128-byte swizzled) | ring of K/V slabs;
 //                 the output tile is staged over both at the end
+//   entry         one thread loads the raw query tile with a single 4-D TMA
+//                 load straight into the MMA's layout (column block by
+//                 column block, the group's heads' rows stacked)
 //   warp 0        allocates tensor memory and issues tcgen05.mma in the order
 //                 S_0, S_1, PV_0, S_2, PV_1, ...:
 //                   S_j = Q K_j^T   A = Q (shared), B = K slabs (K-major)
 //                   O  += P_j V_j   A = P_j in TMEM, B = V slabs (MN-major)
 //                 so the next scores are always queued behind the current PV
 //   warps 1-8     two threads per row (= TMEM lane), each owning half of the
-//                 score columns and half of O: rotate the query row into the
-//                 Q tile, then per tile read its S_j half, mask only tiles the
+//                 score columns and half of O: rotate the query rows in
+//                 place in the Q tile, then per tile read its S_j half, mask only tiles the
 //                 window or diagonal cuts, exchange the row max with the
 //                 partner thread, online softmax in the log2 domain (the
 //                 running max is only raised when it grows by more than 2^8,
@@ -274,15 +277,15 @@ template <int D> struct PrefillSmem {
     // leaves beside the Q tile and the barriers / exchange area (at most
     // 2.3 KB).
     static constexpr int SMEM_BUDGET = 227 * 1024;
-    static constexpr int MISC_MAX = (2 * 12 + 8) * 8 + 16 + 4 * kBM * 4;
+    static constexpr int MISC_MAX = (2 * 12 + 9) * 8 + 16 + 4 * kBM * 4;
     static constexpr int NSLAB_MAX = (SMEM_BUDGET - Q_BYTES - MISC_MAX) / SLAB;
     static constexpr int NSLAB = NSLAB_MAX < 12 ? NSLAB_MAX : 12;
     static constexpr int Q_OFF = 0;
     static constexpr int RING_OFF = Q_OFF + Q_BYTES;
     static constexpr int BAR_OFF = RING_OFF + NSLAB * SLAB;
     // barriers: full[NSLAB], empty[NSLAB], s_full[2], p_full[2], o_done[2],
-    //           q_full, drain
-    static constexpr int NBAR = 2 * NSLAB + 8;
+    //           q_full, drain, q_tma
+    static constexpr int NBAR = 2 * NSLAB + 9;
     static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;  // tmem addr, abort flag
     static constexpr int RED_OFF = MISC_OFF + 16;        // row max / sum exchange, 4 x 128 floats
     static constexpr int TOTAL = RED_OFF + 4 * kBM * 4;
@@ -342,7 +345,8 @@ __device__ __forceinline__ void slab_group(int g, int ntiles, bool &is_v, int &t
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                  const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v,
                   const __grid_constant__ CUtensorMap tmap_o, const PrefillArgs a)
 {
@@ -371,7 +375,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + SM::BAR_OFF);
     uint64_t *full = bars, *empty = bars + NSLAB, *s_full = bars + 2 * NSLAB,
              *p_full = s_full + 2, *o_done = s_full + 4, *q_full = s_full + 6,
-             *drain = s_full + 7;
+             *drain = s_full + 7, *q_tma = s_full + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SM::MISC_OFF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM::MISC_OFF + 4);
 
@@ -379,26 +383,54 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int qblk = blockIdx.x / a.nsplit, split = blockIdx.x % a.nsplit;
     const int kvh = blockIdx.y, b = blockIdx.z;
     const int g = a.group, QB = a.qb_rows, S = a.S;
+    const int q0 = qblk * QB;
+    if (q0 >= S)
+        return;
+
+    // The raw query tile needs no lengths: one TMA load issued at entry
+    // brings it in the MMA's layout (block of 64 columns by block, row
+    // m = head * QB + query; rows past S are zero-filled) while the lengths
+    // arrive; a CTA that leaves before its pipeline starts lets it land.
+    if (threadIdx.x == 0) {
+        kvc::mbar_init(q_tma, 1);
+        kvc::fence_mbar_init();
+        kvc::tma_prefetch_desc(&tmap_q);
+        kvc::mbar_arrive_expect_tx(q_tma, SM::Q_BYTES);
+        kvc::tma_load_4d(smem + SM::Q_OFF, &tmap_q, 0, q0, b * a.q_heads + kvh * g, 0, q_tma);
+    }
+    auto leave = [&]() {
+        if (threadIdx.x == 0)
+            kvc::mbar_wait(q_tma, 0);
+    };
 
     // ---- per batch row geometry (uniform over the CTA) ----
     const int L = a.len.cache_total[b];
-    if (L < 0)
+    if (L < 0) {
+        leave();
         return;
+    }
     const int Lp = a.len.cache_past[b];
     const int P = a.len.past_abs[b];
     if (Lp < 0 || (int64_t)Lp + S > a.rows_per_head) {
         if (threadIdx.x == 0 && qblk == 0 && kvh == 0)
             kvc::raise_status(a.status, KVC_DEV_CAPACITY);
+        leave();
         return;
     }
     if (a.cos_t && (int64_t)P + S > a.rope_max_pos) {
         if (threadIdx.x == 0 && qblk == 0 && kvh == 0)
             kvc::raise_status(a.status, KVC_DEV_ROPE_RANGE);
+        leave();
         return;
     }
-    const int q0 = qblk * QB;
-    if (q0 >= S)
-        return;
+    // the rotation rows of the block's queries are asked of L2 at once: the
+    // softmax warps read them right after, behind the start of the K/V stream
+    if (threadIdx.x == 0 && a.cos_t) {
+        const int64_t o = (int64_t)(P + q0) * (D / 2);
+        const uint32_t nb = (uint32_t)(min(QB, S - q0) * (D / 2) * sizeof(float));
+        kvc::prefetch_l2(a.cos_t + o, nb);
+        kvc::prefetch_l2(a.sin_t + o, nb);
+    }
     const int q_last = min(S - 1, q0 + QB - 1);
     const int hi = Lp + q_last;  // last visible row of the block
     int lo = 0;
@@ -419,6 +451,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 a.ws_l[split * rows_total + qrow] = 0.f;
             }
         }
+        leave();
         return;
     }
     lo += t0 * kBN;
@@ -572,53 +605,44 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         float *red = reinterpret_cast<float *>(smem + SM::RED_OFF);  // [2 tiles][2 halves][128]
         const uint32_t pair_bar = 1 + quad;       // named barrier of the two warps of a quadrant
 
-        // query tile: row r is rotated at absolute position P + (its query)
-        // and staged as 16-bit in the swizzled Q tile (row r of each
-        // 64-column box).  The tensor pipe waits on this, so the loads are
-        // coalesced: a warp takes 16 rows, one row at a time, its lanes
-        // spread along D (lane l owns the rotation pairs (c, c + D/2) for
-        // c in [PPL*l, PPL*l + PPL)), and the loads of QRB rows go out
-        // together.
+        // query tile: the raw rows landed by TMA; each warp rotates its 16
+        // rows in place at absolute position P + (the row's query), its lanes
+        // spread along D (lane l owns the rotation pairs (c, c + D/2) for c
+        // in [PPL*l, PPL*l + PPL)), the cos/sin loads of all 16 rows issued
+        // together.  Rows past S stay zero.  The tensor pipe waits on this.
         {
-            using QVec = typename QuarterRow<D / 64>::q;
-            using FVec = typename QuarterRow<D / 64>::f;
-            constexpr int PPL = D / 64;
-            constexpr int ROWS = kBM / kSoftmaxWarps;
-            constexpr int QRB = 8;
-            uint8_t *qt = smem + SM::Q_OFF;
-            const int c0 = PPL * lane;
-            const uint32_t off_lo = (uint32_t)(c0 >> 6) * (kBM * 128), sub = (uint32_t)(c0 & 7) * 2;
-            const uint32_t off_hi = (uint32_t)((D / 2 + c0) >> 6) * (kBM * 128);
-            const uint32_t ch_lo = (uint32_t)(c0 & 63) >> 3, ch_hi = (uint32_t)((D / 2 + c0) & 63) >> 3;
-#pragma unroll 1
-            for (int rb = 0; rb < ROWS; rb += QRB) {
-                QVec lo[QRB], hi[QRB];
-                FVec cv[QRB], sv[QRB];
+            const bool q_ok = wait_or_abort(q_tma, 0, abort_flag, a.status);
+            if (q_ok && a.cos_t) {
+                using QVec = typename QuarterRow<D / 64>::q;
+                using FVec = typename QuarterRow<D / 64>::f;
+                constexpr int PPL = D / 64;
+                constexpr int ROWS = kBM / kSoftmaxWarps;
+                uint8_t *qt = smem + SM::Q_OFF;
+                const int c0 = PPL * lane;
+                const uint32_t off_lo = (uint32_t)(c0 >> 6) * (kBM * 128), sub = (uint32_t)(c0 & 7) * 2;
+                const uint32_t off_hi = (uint32_t)((D / 2 + c0) >> 6) * (kBM * 128);
+                const uint32_t ch_lo = (uint32_t)(c0 & 63) >> 3, ch_hi = (uint32_t)((D / 2 + c0) & 63) >> 3;
+                FVec cv[ROWS], sv[ROWS];
 #pragma unroll
-                for (int u = 0; u < QRB; ++u) {
-                    const int mr = sw * ROWS + rb + u;
-                    const int hr = mr / QB, ir = q0 + (mr - hr * QB);
-                    lo[u] = QVec{};
-                    hi[u] = QVec{};
-                    if (ir < S && hr < g) {
-                        const T *src = static_cast<const T *>(a.q) +
-                                       (((int64_t)b * a.q_heads + kvh * g + hr) * S + ir) * D;
-                        lo[u] = *reinterpret_cast<const QVec *>(src + c0);
-                        hi[u] = *reinterpret_cast<const QVec *>(src + D / 2 + c0);
-                        if (a.cos_t) {
-                            const int64_t o = (int64_t)(P + ir) * (D / 2) + c0;
-                            cv[u] = *reinterpret_cast<const FVec *>(a.cos_t + o);
-                            sv[u] = *reinterpret_cast<const FVec *>(a.sin_t + o);
-                        }
+                for (int u = 0; u < ROWS; ++u) {
+                    const int mr = sw * ROWS + u;
+                    const int ir = q0 + (mr - (mr / QB) * QB);
+                    if (ir < S) {
+                        const int64_t o = (int64_t)(P + ir) * (D / 2) + c0;
+                        cv[u] = *reinterpret_cast<const FVec *>(a.cos_t + o);
+                        sv[u] = *reinterpret_cast<const FVec *>(a.sin_t + o);
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < QRB; ++u) {
-                    const int mr = sw * ROWS + rb + u;
-                    const int hr = mr / QB, ir = q0 + (mr - hr * QB);
-                    if (a.cos_t && ir < S && hr < g) {
-                        T *lv = reinterpret_cast<T *>(&lo[u]);
-                        T *hv = reinterpret_cast<T *>(&hi[u]);
+                for (int u = 0; u < ROWS; ++u) {
+                    const int mr = sw * ROWS + u;
+                    const int ir = q0 + (mr - (mr / QB) * QB);
+                    if (ir < S) {
+                        QVec *plo = reinterpret_cast<QVec *>(qt + off_lo + kvc::sw128(mr, ch_lo) + sub);
+                        QVec *phi = reinterpret_cast<QVec *>(qt + off_hi + kvc::sw128(mr, ch_hi) + sub);
+                        QVec lo = *plo, hi = *phi;
+                        T *lv = reinterpret_cast<T *>(&lo);
+                        T *hv = reinterpret_cast<T *>(&hi);
                         const float *cf = reinterpret_cast<const float *>(&cv[u]);
                         const float *sf = reinterpret_cast<const float *>(&sv[u]);
 #pragma unroll
@@ -628,9 +652,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             lv[e] = kvc::Elem<T>::from_f32(x);
                             hv[e] = kvc::Elem<T>::from_f32(y);
                         }
+                        *plo = lo;
+                        *phi = hi;
                     }
-                    *reinterpret_cast<QVec *>(qt + off_lo + kvc::sw128(mr, ch_lo) + sub) = lo[u];
-                    *reinterpret_cast<QVec *>(qt + off_hi + kvc::sw128(mr, ch_hi) + sub) = hi[u];
                 }
             }
             kvc::fence_proxy_async_smem();
@@ -822,7 +846,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const int h = a.nsplit == 1 ? head0 : split * a.batch * a.q_heads + head0;
             kvc::tma_store_4d(&tmap_o, 0, q0, 0, h, smem + SM::O_OFF);
             kvc::tma_store_commit();
-            kvc::tma_store_wait_all();
+            kvc::tma_store_wait_read();  // the CTA may leave once the tile has been read
         }
     }
 
@@ -831,6 +855,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
         tc_fence_after();
         tmem_dealloc(tmem, SM::TMEM_COLS);
     }
+    if (threadIdx.x == 0 && *abort_flag)
+        kvc::mbar_wait(q_tma, 0);  // a query tile still in flight lands before the CTA leaves
 }
 
 // Merges the KV splits' partials of every query row (one warp per row): the
@@ -922,9 +948,12 @@ kvc_status launch_prefill_tc(void *out, const void *q, const void *k_rows, const
     const CUtensorMapDataType tt = std::is_same<T, __half>::value
                                        ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    CUtensorMap tk, tv, to;
+    CUtensorMap tq, tk, tv, to;
     if (!kvc_host::encode_3d_sw128(&tk, k_rows, rows, D, kBN, SM::DB, tt) ||
-        !kvc_host::encode_3d_sw128(&tv, v_rows, rows, D, SM::KPS, D / 64, tt))
+        !kvc_host::encode_3d_sw128(&tv, v_rows, rows, D, SM::KPS, D / 64, tt) ||
+        !kvc_host::encode_4d_blocks_sw128(&tq, q, (uint64_t)batch * q_heads, (uint64_t)S, D,
+                                          sizeof(T), (uint32_t)(kBM / (q_heads / kv_heads)),
+                                          (uint32_t)(q_heads / kv_heads), tt))
         return KVC_ERR_CUDA;
     PrefillArgs a;
     a.out = out;
@@ -976,7 +1005,7 @@ kvc_status launch_prefill_tc(void *out, const void *q, const void *k_rows, const
         return KVC_ERR_CUDA;
     const int qblocks = (S + a.qb_rows - 1) / a.qb_rows;
     dim3 grid(qblocks * a.nsplit, kv_heads, batch);
-    kern<<<grid, kThreads, smem, stream>>>(tk, tv, to, a);
+    kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, a);
     if (a.nsplit > 1)
         prefill_combine_kernel<T, D><<<(unsigned)((rows_total + 3) / 4), 128, 0, stream>>>(a);
     return kvc_host::launch_status();

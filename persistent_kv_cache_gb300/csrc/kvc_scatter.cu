@@ -3,8 +3,9 @@
 // helpers (status strings, SM count, tensor-map encoding).
 //
 // In place (present == past) only the S updated rows of every prefix move:
-// one warp copies one trailing slice ("row") with the widest vector the
-// alignment allows.  The functional form first copies past -> present with a
+// one thread copies one vector (the widest the alignment allows) of one
+// trailing slice ("row"), its update load issued before the index load so
+// that the two latencies overlap.  The functional form first copies past -> present with a
 // bandwidth-bound vector copy, then runs the same in-place scatter on present.
 #include <cudaTypedefs.h>
 
@@ -21,11 +22,11 @@ scatter_rows_kernel(char *__restrict__ present, const char *__restrict__ update,
                     int64_t prefixes_per_batch, int64_t max_seq, int64_t seq_len,
                     int64_t row_vecs, int circular, int32_t *status)
 {
-    const int lane = threadIdx.x & 31;
-    const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    const int64_t n_rows = n_prefix * seq_len;
-    for (int64_t row = warp; row < n_rows; row += n_warps) {
+    const int64_t n_vec = n_prefix * seq_len * row_vecs;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec; i += stride) {
+        const V v = reinterpret_cast<const V *>(update)[i];
+        const int64_t row = i / row_vecs, c = i - row * row_vecs;
         const int64_t p = row / seq_len;
         const int64_t s = row - p * seq_len;
         const int64_t b = p / prefixes_per_batch;
@@ -36,14 +37,11 @@ scatter_rows_kernel(char *__restrict__ present, const char *__restrict__ update,
             if (idx < 0)
                 idx += max_seq;
         } else if (wi < 0 || wi + seq_len > max_seq) {
-            if (lane == 0 && s == 0 && p == b * prefixes_per_batch)
+            if (s == 0 && c == 0 && p == b * prefixes_per_batch)
                 kvc::raise_status(status, KVC_DEV_INDEX_OOB);
             continue;
         }
-        V *dst = reinterpret_cast<V *>(present) + (p * max_seq + idx) * row_vecs;
-        const V *src = reinterpret_cast<const V *>(update) + row * row_vecs;
-        for (int64_t c = lane; c < row_vecs; c += 32)
-            dst[c] = src[c];
+        reinterpret_cast<V *>(present)[(p * max_seq + idx) * row_vecs + c] = v;
     }
 }
 
@@ -77,8 +75,7 @@ void launch_scatter(char *present, const char *update, const int64_t *wi, int64_
                     int32_t *status, cudaStream_t stream)
 {
     const int64_t rows = n_prefix * S;
-    const int64_t warps_needed = rows;
-    int64_t blocks = (warps_needed + 7) / 8;
+    int64_t blocks = (rows * (slice_bytes / (int64_t)sizeof(V)) + 255) / 256;
     const int64_t cap = (int64_t)kvc_host::sm_count() * 16;
     if (blocks > cap)
         blocks = cap;
@@ -167,6 +164,26 @@ bool encode_4d_heads_sw128(CUtensorMap *map, const void *base, uint64_t heads, u
     cuuint64_t dims[4] = {span, rows, cols / span, heads};
     cuuint64_t strides[3] = {cols * elem_bytes, 128, rows * cols * elem_bytes};
     cuuint32_t box[4] = {(cuuint32_t)span, box_rows, (cuuint32_t)(cols / span), box_heads};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, type, 4, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool encode_4d_blocks_sw128(CUtensorMap *map, const void *base, uint64_t heads, uint64_t rows,
+                            uint64_t cols, uint32_t elem_bytes, uint32_t box_rows,
+                            uint32_t box_heads, CUtensorMapDataType type)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn || elem_bytes == 0 || 128 % elem_bytes != 0)
+        return false;
+    const uint64_t span = 128 / elem_bytes;
+    if (cols % span != 0)
+        return false;
+    cuuint64_t dims[4] = {span, rows, heads, cols / span};
+    cuuint64_t strides[3] = {cols * elem_bytes, rows * cols * elem_bytes, 128};
+    cuuint32_t box[4] = {(cuuint32_t)span, box_rows, box_heads, (cuuint32_t)(cols / span)};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(map, type, 4, const_cast<void *>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
