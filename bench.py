@@ -455,7 +455,6 @@ class WindowDecode(Workload):
 class WindowPrefill(Workload):
     """Windowed chunked prefill through the C + S staging cache."""
     roofline_kernel = "kvc_gqa_prefill_chunk (tcgen05)"
-    traffic_key = ("kvc_prefill.cu", "prefill_tc_kernel")
     bound = "tensor"
 
     def __init__(self, dev, seed=0, with_kernels=True, chunk=2048):
@@ -465,6 +464,8 @@ class WindowPrefill(Workload):
         self.torch = torch
         w = self.w = synth.WINDOW_PREFILL
         S = self.S = int(chunk or 2048)
+        # the kernel's DRAM traffic depends on the chunk (grid and reuse)
+        self.traffic_key = ("kvc_prefill.cu", f"prefill_tc_kernel@chunk{S}")
         B, Hq, Hkv, D, C, W = w.batch, w.q_heads, w.kv_heads, w.head_dim, w.capacity, w.window
         g = torch.Generator(device=dev)
         g.manual_seed(seed)
