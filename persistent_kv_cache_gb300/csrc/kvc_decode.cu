@@ -869,6 +869,68 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
 }
 
+// The same merge when a row has at most kFastSplits partials (capacity up
+// to 8192 rows): the partials sit in L2 right after the split kernel, so the
+// merge is a chain of round trips, not bytes.  Every thread loads all
+// max_splits (m, l) pairs and its columns' partials at once, before the
+// row's split count (which needs the lengths) is known; partials past that
+// count are stale workspace and are dropped by selection, never multiplied
+// in, so whatever they hold cannot reach the output.  D <= 128 * kFastCols.
+constexpr int kFastSplits = 16, kFastCols = 2;
+template <typename T, int MODE>
+__global__ void __launch_bounds__(128)
+decode_combine_fast_kernel(const DecodeArgs a, int D)
+{
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int MS = a.max_splits;
+    const int64_t qrow = (int64_t)b * a.q_heads + h;
+    const int64_t p0 = qrow * MS;
+    float m[kFastSplits], l[kFastSplits], o[kFastSplits][kFastCols];
+#pragma unroll
+    for (int j = 0; j < kFastSplits; ++j) {
+        m[j] = -INFINITY;
+        l[j] = 0.f;
+        if (j < MS) {
+            m[j] = a.ws_m[p0 + j];
+            l[j] = a.ws_l[p0 + j];
+        }
+#pragma unroll
+        for (int c = 0; c < kFastCols; ++c) {
+            const int d = threadIdx.x + 128 * c;
+            o[j][c] = (j < MS && d < D) ? a.ws_o[(p0 + j) * D + d] : 0.f;
+        }
+    }
+    int L, tot;
+    const int nsplit = row_splits<MODE>(a, b, L, tot);
+    if (nsplit <= 1)
+        return;
+    float mstar = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kFastSplits; ++j)
+        mstar = j < nsplit ? fmaxf(mstar, m[j]) : mstar;
+    float lsum = 0.f, acc[kFastCols];
+#pragma unroll
+    for (int c = 0; c < kFastCols; ++c)
+        acc[c] = 0.f;
+#pragma unroll
+    for (int j = 0; j < kFastSplits; ++j) {
+        if (j < nsplit) {
+            const float w = exp2f(m[j] - mstar);
+            lsum += l[j] * w;
+#pragma unroll
+            for (int c = 0; c < kFastCols; ++c)
+                acc[c] += o[j][c] * w;
+        }
+    }
+    const float inv_l = 1.f / lsum;
+#pragma unroll
+    for (int c = 0; c < kFastCols; ++c) {
+        const int d = threadIdx.x + 128 * c;
+        if (d < D)
+            static_cast<T *>(a.out)[qrow * D + d] = kvc::Elem<T>::from_f32(acc[c] * inv_l);
+    }
+}
+
 // merges the per-split partials of rows that used more than one split: the
 // splits' m and l are read in parallel into shared memory, the weights
 // 2^(m_j - max m) computed once, and each output column sums its partials
@@ -1476,10 +1538,17 @@ kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const 
     if (a.max_splits > 1) {
         dim3 g2(q_heads, batch);
         const size_t cs = 3 * a.max_splits * sizeof(float);
-        if (fx)
+        const bool fast = a.max_splits <= kFastSplits && D <= 128 * kFastCols;
+        if (fx && fast)
+            decode_combine_fast_kernel<T, kFused><<<g2, 128, 0, stream>>>(a, D);
+        else if (fx)
             decode_combine_kernel<T, kFused><<<g2, 128, cs, stream>>>(a, D);
+        else if (px && fast)
+            decode_combine_fast_kernel<T, kPaged><<<g2, 128, 0, stream>>>(a, D);
         else if (px)
             decode_combine_kernel<T, kPaged><<<g2, 128, cs, stream>>>(a, D);
+        else if (fast)
+            decode_combine_fast_kernel<T, kPlain><<<g2, 128, 0, stream>>>(a, D);
         else
             decode_combine_kernel<T, kPlain><<<g2, 128, cs, stream>>>(a, D);
     }
