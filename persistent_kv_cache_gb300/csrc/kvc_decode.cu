@@ -531,6 +531,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     uint64_t *empty = full + NBAR;
     int *abort_flag = reinterpret_cast<int *>(empty + NBAR);
     int *page_ids = abort_flag + 4;  // [32] paged: the split's pages
+    // kFused: the new row, K rotated at its position then V ([2][D])
+    T *newrow = reinterpret_cast<T *>(page_ids + 32);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -688,6 +690,35 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
             qs[h * QS + i] = kvc::Elem<T>::from_f32(lo);
             qs[h * QS + i + D / 2] = kvc::Elem<T>::from_f32(hi);
         }
+        if constexpr (MODE == kFused) {
+            // the CTA whose split ends at the newest position (tot - 1) appends
+            // it: while the first tiles are in flight, the new K row is rotated
+            // there and both rows are stored to the cache and kept here for the
+            // last tile, whose TMA copy of that row predates them
+            if (split == nsplit - 1 && threadIdx.x < D / 2) {
+                const int i = threadIdx.x;
+                const int64_t slice = (int64_t)b * a.kv_heads + kvh;
+                const int64_t dst_row = a.ring ? (int64_t)(tot - 1) % a.capacity : (int64_t)tot - 1;
+                const T *nk = static_cast<const T *>(a.new_k) + slice * D;
+                const T *nv = static_cast<const T *>(a.new_v) + slice * D;
+                T *kc = static_cast<T *>(a.k_cache) + (slice * a.capacity + dst_row) * D;
+                T *vc = static_cast<T *>(a.v_cache) + (slice * a.capacity + dst_row) * D;
+                float lo = kvc::Elem<T>::to_f32(nk[i]), hi = kvc::Elem<T>::to_f32(nk[i + D / 2]);
+                if (a.cos_t)
+                    kvc::rope_pair(lo, hi, a.cos_t[(int64_t)(tot - 1) * (D / 2) + i],
+                                   a.sin_t[(int64_t)(tot - 1) * (D / 2) + i]);
+                const T klo = kvc::Elem<T>::from_f32(lo), khi = kvc::Elem<T>::from_f32(hi);
+                const T vlo = nv[i], vhi = nv[i + D / 2];
+                kc[i] = klo;
+                kc[i + D / 2] = khi;
+                vc[i] = vlo;
+                vc[i + D / 2] = vhi;
+                newrow[i] = klo;
+                newrow[i + D / 2] = khi;
+                newrow[D + i] = vlo;
+                newrow[D + i + D / 2] = vhi;
+            }
+        }
     }
     consumer_sync();
     GroupAttn<T, D> ga;
@@ -782,28 +813,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         if (MODE == kFused && split == nsplit - 1 && t == ntiles - 1 && my_valid > 0 &&
             16 * warp + my_valid == rows_t) {
             // this warp owns the newest row (position tot - 1): place the new
-            // K (rotated there) and V row in the tile and store it to the cache
+            // K (rotated there) and V row, appended at the start, in the tile
             const int rr = rows_t - 1;
-            const int64_t slice = (int64_t)b * a.kv_heads + kvh;
-            const int64_t dst_row = a.ring ? (int64_t)(tot - 1) % a.capacity : (int64_t)tot - 1;
-            const T *nk = static_cast<const T *>(a.new_k) + slice * D;
-            const T *nv = static_cast<const T *>(a.new_v) + slice * D;
-            T *kc = static_cast<T *>(a.k_cache) + (slice * a.capacity + dst_row) * D;
-            T *vc = static_cast<T *>(a.v_cache) + (slice * a.capacity + dst_row) * D;
-            const float *cs = a.cos_t ? a.cos_t + (int64_t)(tot - 1) * (D / 2) : nullptr;
-            const float *sn = a.cos_t ? a.sin_t + (int64_t)(tot - 1) * (D / 2) : nullptr;
             uint8_t *kgen = stages + s * STAGE_BYTES;
             uint8_t *vgen = kgen + KT_BYTES;
             for (int i = lane; i < D / 2; i += 32) {
-                float lo = kvc::Elem<T>::to_f32(nk[i]), hi = kvc::Elem<T>::to_f32(nk[i + D / 2]);
-                if (cs)
-                    kvc::rope_pair(lo, hi, cs[i], sn[i]);
-                const T klo = kvc::Elem<T>::from_f32(lo), khi = kvc::Elem<T>::from_f32(hi);
-                const T vlo = nv[i], vhi = nv[i + D / 2];
-                kc[i] = klo;
-                kc[i + D / 2] = khi;
-                vc[i] = vlo;
-                vc[i + D / 2] = vhi;
+                const T klo = newrow[i], khi = newrow[i + D / 2];
+                const T vlo = newrow[D + i], vhi = newrow[D + i + D / 2];
                 const int c0 = i, c1 = i + D / 2;
                 const int o0 = (c0 >> 6) * 8192 + kvc::sw128(rr, (c0 & 63) >> 3) + (c0 & 7) * 2;
                 const int o1 = (c1 >> 6) * 8192 + kvc::sw128(rr, (c1 & 63) >> 3) + (c1 & 7) * 2;
@@ -1524,8 +1540,9 @@ kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const 
         a.n_q_pages = px->n_q_pages;
     }
     constexpr int NS = decode_stages(D);
+    // (+ the fused step's new K and V row)
     const size_t smem = 1024 + (size_t)NS * 2 * kTile * D * 2 + 16 * (D + 8) * 2 +
-                        4 * NS * sizeof(uint64_t) + 16 + 32 * sizeof(int);
+                        4 * NS * sizeof(uint64_t) + 16 + 32 * sizeof(int) + 2 * D * sizeof(T);
     auto kern = fx                 ? decode_split_kernel<T, D, kFused>
                 : px && px->qk_pool ? decode_split_kernel<T, D, kPagedQ>
                 : px               ? decode_split_kernel<T, D, kPaged>
