@@ -331,8 +331,10 @@ class WindowDecode(Workload):
     def __init__(self, dev, seed=0, with_kernels=True, chunk=None, max_steps=4096):
         self.roofline_kernel = ("kvc_window_decode_step (fused step)" if self.fused
                                 else "kvc_gqa_decode (window decode)")
-        self.traffic_key = ("kvc_decode.cu",
-                            "window_step_kernel" if self.fused else "decode_split_kernel_window")
+        # the kernel's DRAM traffic depends on the layout and on the replicas
+        layout = self.spec.lower() + ("_hot" if self.replicas == 1 else "")
+        self.traffic_key = ("kvc_decode.cu", ("window_step_kernel@" if self.fused
+                                              else "decode_split_kernel_window@") + layout)
         import torch
 
         from persistent_kv_cache_gb300 import synth
