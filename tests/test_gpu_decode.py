@@ -3,7 +3,8 @@ against the oracle: max-abs error <= 2e-2 for bf16/fp16 and <= 1e-4 for fp32.
 
 Covers the tiny fp32 scatter-then-decode workload, ragged lengths over
 several TMA tiles and splits with partial tails, GQA groups 1..16, window
-masks narrower than the resident rows, the contiguous bf16 workload at full
+masks narrower than the resident rows, capacities whose rows need more
+splits than the merge's fast path takes, the contiguous bf16 workload at full
 size (32 x 32/8 heads x 128, capacity 8192, lengths U[512, 8192]; cache bytes
 checked everywhere, attention sampled on several batch rows), the windowed
 ring decode (64 x 64/8 x 64, C = W = 128) over consecutive one-token steps,
@@ -117,6 +118,16 @@ def test_multi_split_with_window(K, orc, g):
     for window in (0, 700, 64, 1):
         _decode_case(K, orc, torch.bfloat16, len(T), 2 * g, 2, 128, 4096, T, window, 0, True,
                      20 + window)
+
+
+def test_more_splits_than_the_fast_merge(K, orc):
+    """capacity 12288 (512-row splits, up to 24 a row): the merge takes its
+    general path; rows with one split, 16, 17 and 24, with and without a
+    window."""
+    T = [1, 512, 8192, 8193, 9000, 12288]
+    for window in (0, 5000):
+        _decode_case(K, orc, torch.bfloat16, len(T), 8, 2, 128, 12288, T, window, 0, True,
+                     40 + window)
 
 
 def test_windowed_cache_decode(K, orc):

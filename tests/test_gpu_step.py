@@ -97,6 +97,9 @@ def test_contiguous_workload_full_size(K, orc):
     (True, torch.bfloat16, 128, 4, 4096, 0),
     (True, torch.bfloat16, 64, 16, 4096, 3000),
     (True, torch.float16, 128, 2, 300, 300),
+    # capacity 12288: up to 24 splits a row, past the merge's 16-split fast path
+    (False, torch.bfloat16, 128, 4, 12288, 0),
+    (True, torch.bfloat16, 128, 4, 12288, 5000),
 ])
 def test_consecutive_steps_and_graph(K, orc, ring, dtype, D, g, C, W):
     B, Hkv = 5, 2
