@@ -58,6 +58,10 @@ METRIC = "KV append+GQA decode: achieved HBM GB/s (% of peak), decode steps/s"
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# nominal GB300 figures: HBM3e bandwidth and dense bf16 tensor throughput
+NOMINAL_GBS, NOMINAL_TFLOPS = 7900.0, 2250.0
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -1058,6 +1062,9 @@ def run_ours(args):
                 "frac": achieved / peak, "peak_kind": peak_kind,
                 "algorithmic_bytes_per_launch": wl.kernel_bytes}
         extra = {"pct_of_peak": 100.0 * value / peak}
+    # the same fraction against the part's nominal figure (context only)
+    roof["frac_of_nominal"] = roof["achieved"] / (NOMINAL_TFLOPS if roof["unit"] == "TFLOP/s"
+                                                  else NOMINAL_GBS)
     roof.update({"kernel": wl.roofline_kernel, "traffic": kernel_traffic(wl.traffic_key),
                  "avg_launch_ms": kern_ms})
     cpu = None
