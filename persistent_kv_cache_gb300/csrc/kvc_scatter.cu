@@ -9,6 +9,7 @@
 // bandwidth-bound vector copy, then runs the same in-place scatter on present.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "kvc_common.cuh"
@@ -90,18 +91,22 @@ void launch_scatter(char *present, const char *update, const int64_t *wi, int64_
 
 namespace kvc_host {
 
+// SM count of the current device, looked up once per device; host threads
+// may call the library concurrently, so the cache is atomic
 int sm_count()
 {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-        return 148;
-    if (cached[dev] == 0) {
-        int n = 0;
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = n > 0 ? n : 148;
+        return 152;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            n <= 0)
+            n = 152;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
