@@ -133,7 +133,17 @@ def library() -> ctypes.CDLL:
 
 
 def _ptr(t):
-    return None if t is None else t.data_ptr()
+    """Device address of a tensor the library reads or writes as a dense
+    array: it must live on a CUDA device and be contiguous (a strided view
+    would be read in the wrong order, or past its storage)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"expected a contiguous tensor, got shape {tuple(t.shape)} "
+                         f"with strides {t.stride()}")
+    return t.data_ptr()
 
 
 def _stream(stream):
@@ -155,7 +165,9 @@ def _rope(rope):
     if rope is None:
         return None, None, 0
     cos, sin = rope
-    return cos.data_ptr(), sin.data_ptr(), cos.shape[0]
+    if cos.dtype != torch.float32 or sin.dtype != torch.float32 or cos.shape != sin.shape:
+        raise ValueError("rope: cos and sin are float32 tables of the same shape [max_pos, D/2]")
+    return _ptr(cos), _ptr(sin), cos.shape[0]
 
 
 def kvc_tensor_scatter(present, past, update, write_indices=None, axis=-2, mode=KVC_LINEAR,

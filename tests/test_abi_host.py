@@ -33,6 +33,17 @@ def test_every_declared_symbol_is_exported(kvc):
     assert set(kvc.EXPORTS) <= set(names)
 
 
+def test_binding_rejects_host_tensors(kvc):
+    """The binding passes device addresses only: a tensor in host memory is
+    refused before anything reaches the library."""
+    import torch
+    x = torch.zeros(2, 2, 16, 8)
+    with pytest.raises(ValueError, match="CUDA"):
+        kvc.kvc_tensor_scatter(x, x, x[:, :, :1].contiguous())
+    with pytest.raises(ValueError, match="CUDA"):
+        kvc.kvc_seq_lengths(torch.zeros(2, dtype=torch.int32), 1, 16, 0)
+
+
 def test_version_and_strings(kvc):
     assert kvc.kvc_abi_version() == 5
     assert kvc.kvc_status_string(0) == "ok"

@@ -89,6 +89,15 @@ def test_absent_write_indices(K, orc):
     assert_bytes_equal(t, want)
 
 
+def test_strided_views_are_refused(K):
+    """A non-contiguous view would be read as if it were dense: refused."""
+    t = torch.zeros(2, 3, 16, 8, device=dev())
+    upd = torch.zeros(2, 3, 1, 16, device=dev())[..., ::2]  # [2, 3, 1, 8], stride 2
+    assert not upd.is_contiguous()
+    with pytest.raises(ValueError, match="contiguous"):
+        K.kvc_tensor_scatter(t, t, upd)
+
+
 def test_unaligned_rows(K, orc):
     """Trailing slices of 3 bytes take the byte path."""
     rng = np.random.default_rng(6)
