@@ -1049,6 +1049,18 @@ def run_ours(args):
         k1.record()
         torch.cuda.synchronize()
         kern_ms = k0.elapsed_time(k1) / args.steps
+        # outside the timed region: the spread of the step time over ten more
+        # replays of the same K-step graph (median and 10th percentile)
+        reps = []
+        for _ in range(10):
+            start.record()
+            step_graph.replay()
+            end.record()
+            torch.cuda.synchronize()
+            reps.append(start.elapsed_time(end) / args.steps)
+        reps.sort()
+        replay_stats = {"replays": len(reps), "median_ms_per_step": reps[len(reps) // 2],
+                        "p10_ms_per_step": reps[len(reps) // 10]}
         wl.e2e_setup()
         for _ in range(args.warmup):
             wl.e2e_step(i)
@@ -1136,6 +1148,7 @@ def run_ours(args):
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": wl.h2d,
                 "d2h_bytes_per_step": wl.d2h, "steps_per_s": args.steps * world / e2e_s},
         "roofline": roof,
+        "replay_stats": replay_stats,
         "cpu_baseline": cpu,
         "gpu_launches": wl.launches_per_step * args.steps,
         "clocks": clocks.summary(),
