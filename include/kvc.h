@@ -474,10 +474,11 @@ kvc_status kvc_gqa_decode_paged_q(void *out, const void *q, const void *k_pool,
  * the attention in one launch ("Persistent KV Cache and Decode Performance
  * Roadmap", Phase 1; "GQA support sliding_window_cache", "Design";
  * "Stateful decode & KV cache", "Sliding-window ring buffer").  The CTA that
- * holds the newest position places the new K (rotated at T - 1) and V row
- * into its tile on chip and stores it to the cache (row T - 1, or slot
- * (T - 1) mod C).  Rows long enough for several splits are merged by a
- * second launch, as in kvc_gqa_decode.
+ * holds the newest position rotates the new K row at T - 1 and stores it and
+ * the V row to the cache (row T - 1, or slot (T - 1) mod C) while its first
+ * tiles are in flight, then places both in its last tile on chip.  Rows long
+ * enough for several splits are merged by a second launch, as in
+ * kvc_gqa_decode.
  *
  * out, q          device [batch, q_heads, 1, head_dim].
  * k_cache/v_cache device [batch, kv_heads, capacity, head_dim], updated in place.
