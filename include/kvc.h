@@ -78,7 +78,7 @@ typedef enum {
     KVC_ERR_SHAPE = 2,       /* a size is out of range or buffers overlap badly  */
     KVC_ERR_DTYPE = 3,       /* element type not supported by this entry point   */
     KVC_ERR_ALIGN = 4,       /* a buffer is not 16-byte aligned where required   */
-    KVC_ERR_UNSUPPORTED = 5, /* a valid combination this build does not cover    */
+    KVC_ERR_UNSUPPORTED = 5, /* a valid combination the library does not cover   */
     KVC_ERR_CAPACITY = 6,    /* capacity < 1 or too small for the request        */
     KVC_ERR_WINDOW = 7,      /* windowed cache needs 0 < local_window_size <= C  */
     KVC_ERR_WORKSPACE = 8,   /* workspace NULL or smaller than required          */

@@ -293,7 +293,7 @@ KVC_API const char *kvc_status_string(kvc_status s)
     case KVC_ERR_SHAPE: return "size out of range or overlapping buffers";
     case KVC_ERR_DTYPE: return "element type not supported";
     case KVC_ERR_ALIGN: return "buffer not 16-byte aligned";
-    case KVC_ERR_UNSUPPORTED: return "combination not supported by this build";
+    case KVC_ERR_UNSUPPORTED: return "combination not supported by the library";
     case KVC_ERR_CAPACITY: return "capacity out of range";
     case KVC_ERR_WINDOW: return "windowed cache needs 0 < local_window_size <= capacity";
     case KVC_ERR_WORKSPACE: return "workspace missing or too small";
