@@ -644,8 +644,10 @@ class Scatter(Workload):
         self.torch = torch
         self.roofline_kernel = ("kvc_tensor_scatter (in place)" if self.in_place
                                 else "kvc_tensor_scatter (functional: cache copy + scatter)")
+        # DRAM traffic per call depends on the number of update rows
         self.traffic_key = ("kvc_scatter.cu",
-                            "scatter_rows_kernel" if self.in_place else "scatter_functional")
+                            ("scatter_rows_kernel" if self.in_place else "scatter_functional")
+                            + f"@chunk{int(chunk or 64)}")
         w = self.w = synth.SCATTER
         S = self.S = int(chunk or 64)
         shape = (w.batch, w.heads, w.max_seq, w.head_dim)
