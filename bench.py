@@ -643,7 +643,7 @@ class Scatter(Workload):
         from persistent_kv_cache_gb300 import synth
         self.torch = torch
         self.roofline_kernel = ("kvc_tensor_scatter (in place)" if self.in_place
-                                else "kvc_tensor_scatter (functional: cache copy + scatter)")
+                                else "kvc_tensor_scatter (functional: one-pass scatter_copy_kernel)")
         # DRAM traffic per call depends on the number of update rows
         self.traffic_key = ("kvc_scatter.cu",
                             ("scatter_rows_kernel" if self.in_place else "scatter_functional")

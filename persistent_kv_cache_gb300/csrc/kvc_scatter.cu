@@ -5,8 +5,9 @@
 // In place (present == past) only the S updated rows of every prefix move:
 // one thread copies one vector (the widest the alignment allows) of one
 // trailing slice ("row"), its update load issued before the index load so
-// that the two latencies overlap.  The functional form first copies past -> present with a
-// bandwidth-bound vector copy, then runs the same in-place scatter on present.
+// that the two latencies overlap.  The functional form writes every vector of
+// present once in a single bandwidth-bound pass, each from the update or from
+// past; with no update rows it is a plain vector copy.
 #include <cudaTypedefs.h>
 
 #include <atomic>
@@ -44,6 +45,88 @@ scatter_rows_kernel(char *__restrict__ present, const char *__restrict__ update,
         }
         reinterpret_cast<V *>(present)[(p * max_seq + idx) * row_vecs + c] = v;
     }
+}
+
+// Functional TensorScatter in one pass: every vector of present is written
+// once, from the update when its row is one of the S rows written into its
+// prefix, else from past.  A prefix holds span = max_seq * row_vecs vectors;
+// its written rows start at vector base = (first written row) * row_vecs and
+// run on, modulo span in circular mode, so a vector's distance from base
+// (taken modulo span) is at once the test (< S * row_vecs) and its offset in
+// the prefix's block of the update: no division per vector.  Linear mode with
+// an index out of range leaves that batch row equal to past and raises
+// KVC_DEV_INDEX_OOB, as the in-place form does.
+// the source of present's vector k in a prefix: the update when k lies in the
+// written range (offset from base, modulo span, below n_upd), else past
+template <typename V>
+__device__ __forceinline__ const V *pick_source(const V *src, const V *upd, int64_t k,
+                                                int64_t base, int64_t span, int64_t n_upd)
+{
+    int64_t off = k - base;
+    if (off < 0)
+        off += span;
+    return off < n_upd ? upd + off : src + k;
+}
+
+template <typename V>
+__global__ void __launch_bounds__(256, 6)
+scatter_copy_kernel(V *__restrict__ present, const V *__restrict__ past,
+                    const V *__restrict__ update, const int64_t *__restrict__ write_indices,
+                    int64_t n_prefix, int64_t prefixes_per_batch, int64_t max_seq,
+                    int64_t seq_len, int64_t row_vecs, int circular, int32_t *status)
+{
+    // one contiguous tile of 4 x 256 vectors of one prefix per block: each
+    // warp reads and writes 32 consecutive vectors per access, four in flight
+    const int64_t span = max_seq * row_vecs, upd_vecs = seq_len * row_vecs;
+    const int64_t k0 = (int64_t)blockIdx.x * 1024 + threadIdx.x;
+    for (int64_t p = blockIdx.y; p < n_prefix; p += gridDim.y) {
+        const int64_t b = p / prefixes_per_batch;
+        const int64_t wi = write_indices ? write_indices[b] : 0;
+        int64_t base = 0, n_upd = upd_vecs;
+        if (circular) {
+            int64_t lo = wi % max_seq;
+            if (lo < 0)
+                lo += max_seq;
+            base = lo * row_vecs;
+        } else if (wi < 0 || wi + seq_len > max_seq) {
+            n_upd = 0;
+            if (blockIdx.x == 0 && threadIdx.x == 0 && p == b * prefixes_per_batch)
+                kvc::raise_status(status, KVC_DEV_INDEX_OOB);
+        } else {
+            base = wi * row_vecs;
+        }
+        const V *src = past + p * span;
+        const V *upd = update + p * upd_vecs;
+        V *dst = present + p * span;
+        V v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t k = k0 + j * 256;
+            if (k < span)
+                v[j] = *pick_source(src, upd, k, base, span, n_upd);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t k = k0 + j * 256;
+            if (k < span)
+                dst[k] = v[j];
+        }
+    }
+}
+
+template <typename V>
+void launch_scatter_copy(char *present, const char *past, const char *update, const int64_t *wi,
+                         int64_t n_prefix, int64_t ppb, int64_t max_seq, int64_t S,
+                         int64_t slice_bytes, int circular, int32_t *status, cudaStream_t stream)
+{
+    // x: the 1024-vector tiles of one prefix; y: prefixes (looped past 65535)
+    const int64_t row_vecs = slice_bytes / (int64_t)sizeof(V);
+    const int64_t gx = (max_seq * row_vecs + 1023) / 1024;
+    const int64_t gy = n_prefix < 65535 ? n_prefix : 65535;
+    scatter_copy_kernel<V><<<dim3((unsigned)gx, (unsigned)gy), 256, 0, stream>>>(
+        reinterpret_cast<V *>(present), reinterpret_cast<const V *>(past),
+        reinterpret_cast<const V *>(update), wi, n_prefix, ppb, max_seq, S, row_vecs, circular,
+        status);
 }
 
 // dst[i] = src[i] for i < n (16-byte vectors, four in flight per thread)
@@ -242,6 +325,33 @@ KVC_API kvc_status kvc_tensor_scatter(void *present_cache, const void *past_cach
     if (n_elems == 0)
         return KVC_OK;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const int64_t ppb = n_prefix / cache_shape[0];
+    const int circ = mode == KVC_CIRCULAR;
+
+    if (!in_place && update_seq_len > 0) {
+        // copy and scatter in one pass, the widest vector every pointer allows
+        char *dst = static_cast<char *>(present_cache);
+        const char *src = static_cast<const char *>(past_cache);
+        const char *upd = static_cast<const char *>(update);
+        const uintptr_t a = reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src) |
+                            reinterpret_cast<uintptr_t>(upd);
+        if (slice % 16 == 0 && (a & 15u) == 0)
+            launch_scatter_copy<uint4>(dst, src, upd, write_indices, n_prefix, ppb, max_seq,
+                                       update_seq_len, slice, circ, dev_status, stream);
+        else if (slice % 8 == 0 && (a & 7u) == 0)
+            launch_scatter_copy<uint2>(dst, src, upd, write_indices, n_prefix, ppb, max_seq,
+                                       update_seq_len, slice, circ, dev_status, stream);
+        else if (slice % 4 == 0 && (a & 3u) == 0)
+            launch_scatter_copy<uint32_t>(dst, src, upd, write_indices, n_prefix, ppb, max_seq,
+                                          update_seq_len, slice, circ, dev_status, stream);
+        else if (slice % 2 == 0 && (a & 1u) == 0)
+            launch_scatter_copy<uint16_t>(dst, src, upd, write_indices, n_prefix, ppb, max_seq,
+                                          update_seq_len, slice, circ, dev_status, stream);
+        else
+            launch_scatter_copy<uint8_t>(dst, src, upd, write_indices, n_prefix, ppb, max_seq,
+                                         update_seq_len, slice, circ, dev_status, stream);
+        return kvc_host::launch_status();
+    }
 
     if (!in_place) {
         char *dst = static_cast<char *>(present_cache);
@@ -262,11 +372,9 @@ KVC_API kvc_status kvc_tensor_scatter(void *present_cache, const void *past_cach
     if (update_seq_len == 0)
         return kvc_host::launch_status();
 
-    const int64_t ppb = n_prefix / cache_shape[0];
     char *present = static_cast<char *>(present_cache);
     const char *upd = static_cast<const char *>(update);
     const uintptr_t a = reinterpret_cast<uintptr_t>(present) | reinterpret_cast<uintptr_t>(upd);
-    const int circ = mode == KVC_CIRCULAR;
     if (slice % 16 == 0 && (a & 15u) == 0)
         launch_scatter<uint4>(present, upd, write_indices, n_prefix, ppb, max_seq,
                               update_seq_len, slice, circ, dev_status, stream);

@@ -161,3 +161,39 @@ def test_linear_out_of_range_leaves_row(K, orc):
     K.kvc_tensor_scatter(t, t, upd.to(dev()), wi.to(dev()), status=st)
     assert_bytes_equal(t, want)
     assert st.item() == K.KVC_DEV_INDEX_OOB
+
+
+@pytest.mark.parametrize("case", ["bytes3", "full_ring", "linear_oob", "no_indices",
+                                  "many_prefixes", "long_prefix"])
+def test_functional_edges(K, orc, case):
+    """The one-pass functional form (present != past) on the shapes that
+    steer its vector width, its grid and its index arithmetic."""
+    rng = np.random.default_rng(sum(map(ord, case)))
+    npdt, shape, S, mode, wi = {
+        # 3-byte rows: the byte-wide path
+        "bytes3": (np.uint8, (2, 5, 7, 3), 4, 1, np.array([5, -2])),
+        # every row rewritten, indices negative and beyond max_seq
+        "full_ring": (np.float32, (3, 2, 9, 4), 9, 1, np.array([-4, 13, 0])),
+        # batch row 0 out of range: it must come out equal to past
+        "linear_oob": (np.float16, (2, 3, 8, 8), 3, 0, np.array([6, 2])),
+        "no_indices": (np.float32, (3, 4, 9, 6), 2, 0, None),
+        # more prefixes than one grid dimension holds
+        "many_prefixes": (np.uint8, (2, 35000, 3, 16), 2, 1, np.array([1, 5])),
+        # a single long prefix spread over many blocks, 16-byte rows
+        "long_prefix": (np.float16, (1, 1, 20011, 8), 37, 1, np.array([20000])),
+    }[case]
+    ush = list(shape)
+    ush[2] = S
+    past = rng.integers(0, 250, size=shape).astype(npdt)
+    upd = rng.integers(0, 250, size=ush).astype(npdt)
+    want, flags = orc.tensor_scatter(past, upd, wi, axis=2, mode=mode)
+    tp = torch.from_numpy(past).to(dev())
+    out = torch.full_like(tp, 77)
+    st = status()
+    K.kvc_tensor_scatter(out, tp, torch.from_numpy(upd).to(dev()),
+                         None if wi is None else torch.from_numpy(wi).to(dev()), axis=2,
+                         mode=K.KVC_CIRCULAR if mode else K.KVC_LINEAR, status=st)
+    assert_bytes_equal(out, want, case)
+    assert_bytes_equal(tp, past, case + ": past untouched")
+    assert bool(st.item() & K.KVC_DEV_INDEX_OOB) == bool(flags.any())
+    assert (case == "linear_oob") == bool(flags.any())
