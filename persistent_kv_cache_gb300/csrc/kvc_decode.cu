@@ -124,9 +124,27 @@ __device__ __forceinline__ void s8x4_minus(uint32_t w, float off, float (&f)[4])
 // softmax in the log2 domain.  Thread t holds heads t/4 and t/4 + 8.
 template <typename T, int D> struct GroupAttn {
     static constexpr int NB = D / 8;  // 8-column blocks of the output
-    uint32_t qa[D / 16][4];
+    // the query's A fragments stay in registers up to head_dim 128; at 256
+    // the output alone takes 128 registers a thread, so the fragments are
+    // read from the staged rows (one ldmatrix per 16 columns) instead
+    static constexpr bool QREG = D <= 128;
+    uint32_t qa[QREG ? D / 16 : 1][4];
+    uint32_t q_addr;  // !QREG: this lane's ldmatrix row address in the staged rows
     float o[NB][4];
     float m_lo, m_hi, l_lo, l_hi;
+
+    // A fragment of query columns [16 kk, 16 kk + 16)
+    __device__ __forceinline__ void q_frag(int kk, uint32_t (&a)[4]) const
+    {
+        if constexpr (QREG) {
+            a[0] = qa[kk][0];
+            a[1] = qa[kk][1];
+            a[2] = qa[kk][2];
+            a[3] = qa[kk][3];
+        } else {
+            ldsm_x4(q_addr + kk * 32, a[0], a[1], a[2], a[3]);
+        }
+    }
 
     __device__ __forceinline__ void init()
     {
@@ -137,9 +155,17 @@ template <typename T, int D> struct GroupAttn {
         l_lo = l_hi = 0.f;
     }
 
-    // A fragments of the rotated query rows staged as qs[16][QS]
+    // A fragments of the rotated query rows staged as qs[16][QS] (at D > 128
+    // the rows must stay in place while the tiles are attended)
     __device__ __forceinline__ void load_q(const T *qs, int QS, int lane)
     {
+        if constexpr (!QREG) {
+            // ldmatrix x4: lanes 8m..8m+7 address the rows of matrix m =
+            // (rows 0-7 | 8-15) x (columns 0-7 | 8-15) of a 16-column block
+            const int r = (lane & 7) + ((lane >> 3) & 1) * 8, c = (lane >> 4) * 8;
+            q_addr = kvc::smem_u32(qs + r * QS + c);
+            return;
+        }
         const int row = lane >> 2, col = (lane & 3) * 2;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -218,10 +244,11 @@ template <typename T, int D> struct GroupAttn {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const int cidx = 2 * kk + (mat & 1);
-            uint32_t r_0, r_1, r_2, r_3;
+            uint32_t r_0, r_1, r_2, r_3, a[4];
+            q_frag(kk, a);
             ldsm_x4(kb + (cidx >> 3) * 8192 + kvc::sw128(krow, cidx & 7), r_0, r_1, r_2, r_3);
-            Mma<T>::run(sc[0], qa[kk], r_0, r_1);
-            Mma<T>::run(sc[1], qa[kk], r_2, r_3);
+            Mma<T>::run(sc[0], a, r_0, r_1);
+            Mma<T>::run(sc[1], a, r_2, r_3);
         }
         float mx_lo = -INFINITY, mx_hi = -INFINITY;
 #pragma unroll
@@ -297,36 +324,52 @@ template <typename T, int D> struct GroupAttn {
                                             float voff)
     {
         constexpr int NU = D / 32;  // 16-byte pieces of a lane's fragment bytes
-        uint4 kf[NU];
-#pragma unroll
-        for (int i = 0; i < NU; ++i)
-            kf[i] = *reinterpret_cast<const uint4 *>(kq + i * 512 + lane * 16);
-        const uint32_t *kw = reinterpret_cast<const uint32_t *>(kf);
+        // (at D > 128 the pieces are loaded and used in two halves, to keep
+        // the registers for the output)
+        constexpr int HALVES = D > 128 ? 2 : 1;
+        constexpr int NH = NU / HALVES;
         float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
+        for (int hh = 0; hh < HALVES; ++hh) {
+            // K words: nb * (D / 16) + kk; half hh holds nb = hh when halved
+            uint4 kf[NH];
 #pragma unroll
-            for (int nb = 0; nb < 2; ++nb) {
-                float f[4];
-                s8x4_minus(kw[nb * (D / 16) + kk], koff, f);
-                Mma<T>::run(sc[nb], qa[kk], Mma<T>::pack(f[0], f[1]), Mma<T>::pack(f[2], f[3]));
-            }
+            for (int i = 0; i < NH; ++i)
+                kf[i] = *reinterpret_cast<const uint4 *>(kq + (hh * NH + i) * 512 + lane * 16);
+            const uint32_t *kw = reinterpret_cast<const uint32_t *>(kf);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+                for (int nb = 0; nb < 2 / HALVES; ++nb) {
+                    const int nbg = HALVES == 2 ? hh : nb;
+                    uint32_t a[4];
+                    q_frag(kk, a);
+                    float f[4];
+                    s8x4_minus(kw[nb * (D / 16) + kk], koff, f);
+                    Mma<T>::run(sc[nbg], a, Mma<T>::pack(f[0], f[1]), Mma<T>::pack(f[2], f[3]));
+                }
+        }
         uint32_t pa[4];
         softmax_step(sc, lane, lo, hi, scale_log2, vscale, pa);
-        uint4 vf[NU];
 #pragma unroll
-        for (int i = 0; i < NU; ++i)
-            vf[i] = *reinterpret_cast<const uint4 *>(vq + i * 512 + lane * 16);
-        const uint32_t *vw = reinterpret_cast<const uint32_t *>(vf);
+        for (int hh = 0; hh < HALVES; ++hh) {
+            // V words: nn * 2 + nb; half hh holds nn in [hh D / 32, (hh + 1) D / 32)
+            uint4 vf[NH];
 #pragma unroll
-        for (int nn = 0; nn < D / 16; ++nn)
+            for (int i = 0; i < NH; ++i)
+                vf[i] = *reinterpret_cast<const uint4 *>(vq + (hh * NH + i) * 512 + lane * 16);
+            const uint32_t *vw = reinterpret_cast<const uint32_t *>(vf);
 #pragma unroll
-            for (int nb = 0; nb < 2; ++nb) {
-                float f[4];
-                s8x4_minus(vw[nn * 2 + nb], voff, f);
-                Mma<T>::run(o[2 * nn + nb], pa, Mma<T>::pack(f[0], f[1]),
-                            Mma<T>::pack(f[2], f[3]));
-            }
+            for (int n2 = 0; n2 < D / 16 / HALVES; ++n2)
+#pragma unroll
+                for (int nb = 0; nb < 2; ++nb) {
+                    const int nn = hh * (D / 16 / HALVES) + n2;
+                    float f[4];
+                    s8x4_minus(vw[n2 * 2 + nb], voff, f);
+                    Mma<T>::run(o[2 * nn + nb], pa, Mma<T>::pack(f[0], f[1]),
+                                Mma<T>::pack(f[2], f[3]));
+                }
+        }
     }
 
     // finish l across the quad and publish (m, l, o) of heads < g for the
@@ -498,6 +541,33 @@ __device__ __forceinline__ bool int8_page(int e, const DecodeArgs &a)
     return e >= 0 && (e & KVC_PAGE_QUANT) && (int64_t)(e & ~KVC_PAGE_QUANT) < a.n_q_pages;
 }
 
+// Shared memory of the split kernel.  The tiles arrive in a ring: NS stages
+// of one K and one V tile each (16-bit pages up to head_dim 128), or ring
+// slots of one 64-row tile of K or of V each, a 16-bit tile taking two slots
+// and an int8 tile (its K and V payloads, half the bytes) one.  Slots serve
+// int8 pages, and head_dim 256, where a 64-row tile is 32 KB and three slots
+// (96 KB) let two CTAs share an SM.
+template <int D, int MODE> __host__ __device__ constexpr bool decode_uses_slots()
+{
+    return MODE == kPagedQ || D >= 256;
+}
+template <int D, int MODE> __host__ __device__ constexpr int decode_ring_slots()
+{
+    return D >= 256 ? 3 : MODE == kPagedQ ? 2 * decode_stages(D) : decode_stages(D);
+}
+template <int D, int MODE> __host__ __device__ constexpr int decode_slot_bytes()
+{
+    return decode_uses_slots<D, MODE>() ? kTile * D * 2 : 2 * kTile * D * 2;
+}
+// bytes after the 1024-byte alignment pad: ring, staged query rows [16][D + 8],
+// full/empty barriers, abort flag (+pad), the split's page ids [32], and the
+// fused step's new K and V row
+template <int D, int MODE> __host__ __device__ constexpr int decode_smem_bytes()
+{
+    return decode_ring_slots<D, MODE>() * decode_slot_bytes<D, MODE>() + 16 * (D + 8) * 2 +
+           2 * decode_ring_slots<D, MODE>() * 8 + 16 + 32 * 4 + 2 * D * 2;
+}
+
 // One CTA per (split, kv head, batch row) for kvc_gqa_decode,
 // kvc_gqa_decode_ring and the fused kvc_decode_step; the split partials go
 // to decode_combine_kernel.  kFused: lengths from seqlens_k, and the CTA
@@ -506,28 +576,27 @@ __device__ __forceinline__ bool int8_page(int e, const DecodeArgs &a)
 // one page; the producer warp reads the split's page ids at once.  kPagedQ:
 // the same over 16-bit and int8 pages (an int8 tile arrives by two 1-D bulk
 // copies at half the bytes and is expanded on chip before its MMAs).
-// (kPagedQ: at most as many registers as the CTAs its shared memory lets
-// share an SM can hold -- two at head_dim 128, three at 64)
+// (kPagedQ and head_dim 256: at most as many registers as the CTAs the
+// shared memory lets share an SM can hold -- two at head_dim 128 and 256,
+// three at 64)
 template <typename T, int D, int MODE>
-__global__ void __launch_bounds__(160, MODE == kPagedQ ? (D >= 128 ? 2 : 3) : 0)
+__global__ void __launch_bounds__(160, (MODE == kPagedQ || D >= 256) ? (D >= 128 ? 2 : 3) : 0)
 decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a)
 {
-    constexpr int NS = decode_stages(D);
+    constexpr bool SLOTS = decode_uses_slots<D, MODE>();
+    constexpr int NBAR = decode_ring_slots<D, MODE>();
+    constexpr int SLOT_BYTES = decode_slot_bytes<D, MODE>();
     constexpr int BOXES = D / 64;
     constexpr int KT_BYTES = kTile * D * 2;  // one K (or V) tile
-    constexpr int STAGE_BYTES = 2 * KT_BYTES;
     constexpr int QS = D + 8;                // padded Q row (elements)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
-    // kPagedQ: the stage memory is a ring of NBAR slots of KT_BYTES; an int8
-    // tile (K and V payloads) takes one slot, a 16-bit tile two (K, V)
-    constexpr int NBAR = MODE == kPagedQ ? 2 * NS : NS;
-    T *qs = reinterpret_cast<T *>(smem + NS * STAGE_BYTES);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * STAGE_BYTES + 16 * QS * 2);
+    T *qs = reinterpret_cast<T *>(smem + NBAR * SLOT_BYTES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NBAR * SLOT_BYTES + 16 * QS * 2);
     uint64_t *empty = full + NBAR;
     int *abort_flag = reinterpret_cast<int *>(empty + NBAR);
     int *page_ids = abort_flag + 4;  // [32] paged: the split's pages
@@ -595,76 +664,77 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
             }
             __syncwarp();
         }
-        if (MODE == kPagedQ && lane == 0) {
+        if (lane == 0) {
             kvc::tma_prefetch_desc(&tmap_k);
             kvc::tma_prefetch_desc(&tmap_v);
-            int pos = 0;  // ring position of the next tile's first slot
+            int pos = 0;  // slots: ring position of the next tile's first slot
             for (int t = 0; t < ntiles; ++t) {
-                const int r = q0 + t * kTile;  // logical row, a multiple of 64
-                const int id = page_ids[r / a.page_size - page0];
-                const bool q8 = int8_page(id, a);
-                const int need = q8 ? 1 : 2;
-                bool stop = false;
-                for (int u = 0; u < need && !stop; ++u) {
-                    const int p = pos + u;
-                    if (p >= NBAR && !kvc::mbar_wait(&empty[p % NBAR], ((p / NBAR) - 1) & 1)) {
-                        kvc::raise_status(a.status, KVC_DEV_TIMEOUT);
-                        stop = true;
-                    }
-                }
-                if (stop || *reinterpret_cast<volatile int *>(abort_flag))
-                    break;
-                const int s0 = pos % NBAR, s1 = (pos + 1) % NBAR;
-                uint8_t *b0 = stages + s0 * KT_BYTES;
-                if (q8) {
-                    // the tile's 64 rows of K and of V payload, contiguous in the page
-                    const int64_t off =
-                        (((int64_t)(id & ~KVC_PAGE_QUANT) * a.kv_heads + kvh) * a.page_size +
-                         r % a.page_size) * D;
-                    kvc::mbar_arrive_expect_tx(&full[s0], 2 * kTile * D);
-                    kvc::bulk_load(b0, a.qk_pool + off, kTile * D, &full[s0]);
-                    kvc::bulk_load(b0 + kTile * D, a.qv_pool + off, kTile * D, &full[s0]);
-                } else {
-                    uint8_t *b1 = stages + s1 * KT_BYTES;
-                    const int32_t y = (int32_t)(((int64_t)id * a.kv_heads + kvh) * a.page_size +
-                                                r % a.page_size);
-                    kvc::mbar_arrive_expect_tx(&full[s0], KT_BYTES);
-                    kvc::mbar_arrive_expect_tx(&full[s1], KT_BYTES);
-#pragma unroll
-                    for (int bx = 0; bx < BOXES; ++bx) {
-                        kvc::tma_load_2d(b0 + bx * 8192, &tmap_k, bx * 64, y, &full[s0]);
-                        kvc::tma_load_2d(b1 + bx * 8192, &tmap_v, bx * 64, y, &full[s1]);
-                    }
-                }
-                pos += need;
-            }
-        } else if (lane == 0) {
-            kvc::tma_prefetch_desc(&tmap_k);
-            kvc::tma_prefetch_desc(&tmap_v);
-            for (int t = 0; t < ntiles; ++t) {
-                const int s = t % NS, k = t / NS;
-                if (t >= NS && !kvc::mbar_wait(&empty[s], (k - 1) & 1)) {
-                    kvc::raise_status(a.status, KVC_DEV_TIMEOUT);
-                    break;
-                }
-                if (*reinterpret_cast<volatile int *>(abort_flag))
-                    break;
-                uint8_t *kb = stages + s * STAGE_BYTES;
-                uint8_t *vb = kb + KT_BYTES;
+                // the tile's first row in the tensor maps, and whether it is int8
                 int32_t y = 0;
+                bool q8 = false;
+                int64_t q8off = 0;
                 if constexpr (MODE >= kPaged) {
                     const int r = q0 + t * kTile;  // logical row, a multiple of 64
                     const int id = page_ids[r / a.page_size - page0];
-                    y = (int32_t)(((int64_t)id * a.kv_heads + kvh) * a.page_size +
-                                  r % a.page_size);
+                    if constexpr (MODE == kPagedQ)
+                        q8 = int8_page(id, a);
+                    if (q8)
+                        q8off = (((int64_t)(id & ~KVC_PAGE_QUANT) * a.kv_heads + kvh) *
+                                     a.page_size + r % a.page_size) * D;
+                    else
+                        y = (int32_t)(((int64_t)id * a.kv_heads + kvh) * a.page_size +
+                                      r % a.page_size);
                 } else {
                     y = (int32_t)(row_base + tile_start(t));
                 }
-                kvc::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+                if constexpr (SLOTS) {
+                    const int need = q8 ? 1 : 2;
+                    bool stop = false;
+                    for (int u = 0; u < need && !stop; ++u) {
+                        const int p = pos + u;
+                        if (p >= NBAR &&
+                            !kvc::mbar_wait(&empty[p % NBAR], ((p / NBAR) - 1) & 1)) {
+                            kvc::raise_status(a.status, KVC_DEV_TIMEOUT);
+                            stop = true;
+                        }
+                    }
+                    if (stop || *reinterpret_cast<volatile int *>(abort_flag))
+                        break;
+                    const int s0 = pos % NBAR, s1 = (pos + 1) % NBAR;
+                    uint8_t *b0 = stages + s0 * SLOT_BYTES;
+                    if (q8) {
+                        // the tile's 64 rows of K and of V payload, contiguous in the page
+                        kvc::mbar_arrive_expect_tx(&full[s0], 2 * kTile * D);
+                        kvc::bulk_load(b0, a.qk_pool + q8off, kTile * D, &full[s0]);
+                        kvc::bulk_load(b0 + kTile * D, a.qv_pool + q8off, kTile * D, &full[s0]);
+                    } else {
+                        uint8_t *b1 = stages + s1 * SLOT_BYTES;
+                        kvc::mbar_arrive_expect_tx(&full[s0], KT_BYTES);
 #pragma unroll
-                for (int bx = 0; bx < BOXES; ++bx) {
-                    kvc::tma_load_2d(kb + bx * 8192, &tmap_k, bx * 64, y, &full[s]);
-                    kvc::tma_load_2d(vb + bx * 8192, &tmap_v, bx * 64, y, &full[s]);
+                        for (int bx = 0; bx < BOXES; ++bx)
+                            kvc::tma_load_2d(b0 + bx * 8192, &tmap_k, bx * 64, y, &full[s0]);
+                        kvc::mbar_arrive_expect_tx(&full[s1], KT_BYTES);
+#pragma unroll
+                        for (int bx = 0; bx < BOXES; ++bx)
+                            kvc::tma_load_2d(b1 + bx * 8192, &tmap_v, bx * 64, y, &full[s1]);
+                    }
+                    pos += need;
+                } else {
+                    const int s = t % NBAR, k = t / NBAR;
+                    if (t >= NBAR && !kvc::mbar_wait(&empty[s], (k - 1) & 1)) {
+                        kvc::raise_status(a.status, KVC_DEV_TIMEOUT);
+                        break;
+                    }
+                    if (*reinterpret_cast<volatile int *>(abort_flag))
+                        break;
+                    uint8_t *kb = stages + s * SLOT_BYTES;
+                    uint8_t *vb = kb + KT_BYTES;
+                    kvc::mbar_arrive_expect_tx(&full[s], SLOT_BYTES);
+#pragma unroll
+                    for (int bx = 0; bx < BOXES; ++bx) {
+                        kvc::tma_load_2d(kb + bx * 8192, &tmap_k, bx * 64, y, &full[s]);
+                        kvc::tma_load_2d(vb + bx * 8192, &tmap_v, bx * 64, y, &full[s]);
+                    }
                 }
             }
         }
@@ -746,77 +816,45 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
     }
 
-    int pos = 0;  // kPagedQ: ring position of the tile's first slot
-    for (int t = 0; MODE == kPagedQ && t < ntiles; ++t) {
-        const int pi = (q0 + t * kTile) / a.page_size - q0 / a.page_size;
-        const bool q8 = (__shfl_sync(0xffffffffu, my_e, pi) & KVC_PAGE_QUANT) != 0;
-        const int s0 = pos % NBAR, s1 = (pos + 1) % NBAR;
-        if (!kvc::mbar_wait(&full[s0], (uint32_t)(pos / NBAR) & 1u) ||
-            (!q8 && !kvc::mbar_wait(&full[s1], (uint32_t)((pos + 1) / NBAR) & 1u))) {
-            timed_out = true;
-            break;
+    int pos = 0;  // slots: ring position of the tile's first slot
+    for (int t = 0; t < ntiles; ++t) {
+        bool q8 = false;
+        int pi = 0;  // kPagedQ: the tile's page among the split's
+        if constexpr (MODE == kPagedQ) {
+            pi = (q0 + t * kTile) / a.page_size - q0 / a.page_size;
+            q8 = (__shfl_sync(0xffffffffu, my_e, pi) & KVC_PAGE_QUANT) != 0;
+        }
+        // the tile's K and V (16-bit), or its int8 K and V payloads (kgen)
+        uint8_t *kgen, *vgen;
+        int s0, s1;
+        if constexpr (SLOTS) {
+            s0 = pos % NBAR;
+            s1 = (pos + 1) % NBAR;
+            kgen = stages + s0 * SLOT_BYTES;
+            vgen = stages + s1 * SLOT_BYTES;
+            if (!kvc::mbar_wait(&full[s0], (uint32_t)(pos / NBAR) & 1u) ||
+                (!q8 && !kvc::mbar_wait(&full[s1], (uint32_t)((pos + 1) / NBAR) & 1u))) {
+                timed_out = true;
+                break;
+            }
+        } else {
+            s0 = s1 = t % NBAR;
+            kgen = stages + s0 * SLOT_BYTES;
+            vgen = kgen + KT_BYTES;
+            if (!kvc::mbar_wait(&full[s0], (uint32_t)(t / NBAR) & 1u)) {
+                timed_out = true;
+                break;
+            }
         }
         const int rows_t = tile_rows(t);
         const int my_valid = min(16, max(0, rows_t - 16 * warp));
         const int my_lo = min(16, max(0, tile_lo(t) - 16 * warp));
         bool wrote = false;
-        if (q8) {
-            const float ks = __shfl_sync(0xffffffffu, my_p[0], pi);
-            const float kz = __shfl_sync(0xffffffffu, my_p[1], pi);
-            const float vs = __shfl_sync(0xffffffffu, my_p[2], pi);
-            const float vz = __shfl_sync(0xffffffffu, my_p[3], pi);
-            if (my_lo < my_valid) {
-                const uint8_t *base = stages + s0 * KT_BYTES;
-                ga.tile_q8(base + warp * 16 * D, base + kTile * D + warp * 16 * D, lane, my_lo,
-                           my_valid, a.scale_log2 * ks, vs, 8388608.f + 128.f + kz,
-                           8388608.f + 128.f + vz);
-            }
-        } else if (my_valid > 0) {
-            if (my_valid < 16) {
-                // rows past the split end: zero V so that 0 * garbage stays 0
-                uint8_t *vgen = stages + s1 * KT_BYTES;
-                for (int idx = lane; idx < (16 - my_valid) * BOXES * 8; idx += 32) {
-                    const int rr = 16 * warp + my_valid + idx / (BOXES * 8);
-                    const int bx = (idx / 8) % BOXES, c = idx % 8;
-                    *reinterpret_cast<uint4 *>(vgen + bx * 8192 + rr * 128 + c * 16) =
-                        make_uint4(0, 0, 0, 0);
-                }
-                __syncwarp();
-                wrote = true;
-            }
-            if (my_lo < my_valid)
-                ga.tile(kvc::smem_u32(stages + s0 * KT_BYTES), kvc::smem_u32(stages + s1 * KT_BYTES),
-                        warp, lane, my_lo, my_valid, a.scale_log2);
-        }
-        if (wrote)
-            kvc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            kvc::mbar_arrive(&empty[s0]);
-            if (!q8)
-                kvc::mbar_arrive(&empty[s1]);
-        }
-        pos += q8 ? 1 : 2;
-    }
-
-    for (int t = 0; MODE != kPagedQ && t < ntiles; ++t) {
-        const int s = t % NS, k = t / NS;
-        if (!kvc::mbar_wait(&full[s], k & 1)) {
-            timed_out = true;
-            break;
-        }
-        const uint32_t kb = kvc::smem_u32(stages + s * STAGE_BYTES);
-        const uint32_t vb = kb + KT_BYTES;
-        const int rows_t = tile_rows(t);
-        const int my_valid = min(16, max(0, rows_t - 16 * warp));
-        bool patched = false;
         if (MODE == kFused && split == nsplit - 1 && t == ntiles - 1 && my_valid > 0 &&
             16 * warp + my_valid == rows_t) {
             // this warp owns the newest row (position tot - 1): place the new
             // K (rotated there) and V row, appended at the start, in the tile
             const int rr = rows_t - 1;
-            uint8_t *kgen = stages + s * STAGE_BYTES;
-            uint8_t *vgen = kgen + KT_BYTES;
             for (int i = lane; i < D / 2; i += 32) {
                 const T klo = newrow[i], khi = newrow[i + D / 2];
                 const T vlo = newrow[D + i], vhi = newrow[D + i + D / 2];
@@ -828,13 +866,21 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 *reinterpret_cast<T *>(vgen + o0) = vlo;
                 *reinterpret_cast<T *>(vgen + o1) = vhi;
             }
-            patched = true;
+            wrote = true;
             __syncwarp();
         }
-        if (my_valid > 0) {
+        if (q8) {
+            const float ks = __shfl_sync(0xffffffffu, my_p[0], pi);
+            const float kz = __shfl_sync(0xffffffffu, my_p[1], pi);
+            const float vs = __shfl_sync(0xffffffffu, my_p[2], pi);
+            const float vz = __shfl_sync(0xffffffffu, my_p[3], pi);
+            if (my_lo < my_valid)
+                ga.tile_q8(kgen + warp * 16 * D, kgen + kTile * D + warp * 16 * D, lane, my_lo,
+                           my_valid, a.scale_log2 * ks, vs, 8388608.f + 128.f + kz,
+                           8388608.f + 128.f + vz);
+        } else if (my_valid > 0) {
             if (my_valid < 16) {
                 // rows past the split end: zero V so that 0 * garbage stays 0
-                uint8_t *vgen = stages + s * STAGE_BYTES + KT_BYTES;
                 for (int idx = lane; idx < (16 - my_valid) * BOXES * 8; idx += 32) {
                     const int rr = 16 * warp + my_valid + idx / (BOXES * 8);
                     const int bx = (idx / 8) % BOXES, c = idx % 8;
@@ -842,16 +888,21 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         make_uint4(0, 0, 0, 0);
                 }
                 __syncwarp();
+                wrote = true;
             }
-            const int my_lo = min(16, max(0, tile_lo(t) - 16 * warp));
             if (my_lo < my_valid)
-                ga.tile(kb, vb, warp, lane, my_lo, my_valid, a.scale_log2);
+                ga.tile(kvc::smem_u32(kgen), kvc::smem_u32(vgen), warp, lane, my_lo, my_valid,
+                        a.scale_log2);
         }
-        if ((my_valid > 0 && my_valid < 16) || patched)
+        if (wrote)
             kvc::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0)
-            kvc::mbar_arrive(&empty[s]);
+        if (lane == 0) {
+            kvc::mbar_arrive(&empty[s0]);
+            if (SLOTS && !q8)
+                kvc::mbar_arrive(&empty[s1]);
+        }
+        pos += q8 ? 1 : 2;
     }
     if (timed_out) {
         if (lane == 0) {
@@ -1040,7 +1091,7 @@ struct WindowStepArgs {
 __host__ __device__ constexpr int64_t window_step_max_capacity(int D) { return 32768 / D; }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(128, 4)
+__global__ void __launch_bounds__(128, D >= 256 ? 2 : 4)
 window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const WindowStepArgs a)
 {
@@ -1106,15 +1157,25 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
             q_hi[j] = h < g ? qg[h * D + i + D / 2] : T{};
         }
     }
-    const bool row_thread = threadIdx.x < D;
-    const bool row_is_v = threadIdx.x >= D / 2;
-    const int row_i = row_is_v ? threadIdx.x - D / 2 : threadIdx.x;
-    T new_lo{}, new_hi{};
-    if (row_thread) {
-        const T *src = (row_is_v ? static_cast<const T *>(a.new_v)
-                                 : static_cast<const T *>(a.new_k)) + slice * D;
-        new_lo = src[row_i];
-        new_hi = src[row_i + D / 2];
+    // the new row's pairs: item x < D / 2 is K pair x, item D / 2 + i is V
+    // pair i; thread t holds items t and t + 128 (the second only at D = 256)
+    constexpr int RPT = D > 128 ? 2 : 1;
+    bool row_thread[RPT], row_is_v[RPT];
+    int row_i[RPT];
+    T new_lo[RPT], new_hi[RPT];
+#pragma unroll
+    for (int u = 0; u < RPT; ++u) {
+        const int x = threadIdx.x + 128 * u;
+        row_thread[u] = x < D;
+        row_is_v[u] = x >= D / 2;
+        row_i[u] = row_is_v[u] ? x - D / 2 : x;
+        new_lo[u] = new_hi[u] = T{};
+        if (row_thread[u]) {
+            const T *src = (row_is_v[u] ? static_cast<const T *>(a.new_v)
+                                        : static_cast<const T *>(a.new_k)) + slice * D;
+            new_lo[u] = src[row_i[u]];
+            new_hi[u] = src[row_i[u] + D / 2];
+        }
     }
 
     const int64_t T_ = (int64_t)a.seqlens_k[b] + 1;
@@ -1199,19 +1260,25 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
         qs[h * QS + i] = kvc::Elem<T>::from_f32(lo);
         qs[h * QS + i + D / 2] = kvc::Elem<T>::from_f32(hi);
     }
-    if (row_thread && !row_is_v && cs) {
-        float lo = kvc::Elem<T>::to_f32(new_lo), hi = kvc::Elem<T>::to_f32(new_hi);
-        kvc::rope_pair(lo, hi, cs[row_i], sn[row_i]);
-        new_lo = kvc::Elem<T>::from_f32(lo);
-        new_hi = kvc::Elem<T>::from_f32(hi);
+#pragma unroll
+    for (int u = 0; u < RPT; ++u) {
+        if (row_thread[u] && !row_is_v[u] && cs) {
+            float lo = kvc::Elem<T>::to_f32(new_lo[u]), hi = kvc::Elem<T>::to_f32(new_hi[u]);
+            kvc::rope_pair(lo, hi, cs[row_i[u]], sn[row_i[u]]);
+            new_lo[u] = kvc::Elem<T>::from_f32(lo);
+            new_hi[u] = kvc::Elem<T>::from_f32(hi);
+        }
     }
 
     // the new row goes to shared memory and, without an eviction, straight
     // to its cache row (a load of that row, if any, is overwritten below)
-    if (!moves && row_thread) {
-        T *dst = (row_is_v ? vc : kc) + (int64_t)new_r * D;
-        dst[row_i] = new_lo;
-        dst[row_i + D / 2] = new_hi;
+#pragma unroll
+    for (int u = 0; u < RPT; ++u) {
+        if (!moves && row_thread[u]) {
+            T *dst = (row_is_v[u] ? vc : kc) + (int64_t)new_r * D;
+            dst[row_i[u]] = new_lo[u];
+            dst[row_i[u] + D / 2] = new_hi[u];
+        }
     }
 
     // rows whose V is zeroed: wherever attention might touch a row that
@@ -1254,11 +1321,16 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
         const bool has_new = new_r >= r_lo && new_r < r_hi;
         const int zl = max(z0, r_lo), zh = min(z1, r_hi);
         if (has_new || zh > zl) {
-            if (has_new && row_thread) {
-                const int c_lo = row_i / 8, c_hi = (row_i + D / 2) / 8;
-                *reinterpret_cast<T *>(at(row_is_v, new_r, c_lo) + (row_i % 8) * 2) = new_lo;
-                *reinterpret_cast<T *>(at(row_is_v, new_r, c_hi) + ((row_i + D / 2) % 8) * 2) =
-                    new_hi;
+#pragma unroll
+            for (int u = 0; u < RPT; ++u) {
+                if (has_new && row_thread[u]) {
+                    const int ri = row_i[u];
+                    const int c_lo = ri / 8, c_hi = (ri + D / 2) / 8;
+                    *reinterpret_cast<T *>(at(row_is_v[u], new_r, c_lo) + (ri % 8) * 2) =
+                        new_lo[u];
+                    *reinterpret_cast<T *>(at(row_is_v[u], new_r, c_hi) +
+                                           ((ri + D / 2) % 8) * 2) = new_hi[u];
+                }
             }
             for (int idx = threadIdx.x; idx < (zh - zl) * CPR; idx += 128)
                 *reinterpret_cast<uint4 *>(at(true, zl + idx / CPR, idx % CPR)) =
@@ -1539,10 +1611,9 @@ kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const 
         a.qparams = px->qparams;
         a.n_q_pages = px->n_q_pages;
     }
-    constexpr int NS = decode_stages(D);
-    // (+ the fused step's new K and V row)
-    const size_t smem = 1024 + (size_t)NS * 2 * kTile * D * 2 + 16 * (D + 8) * 2 +
-                        4 * NS * sizeof(uint64_t) + 16 + 32 * sizeof(int) + 2 * D * sizeof(T);
+    const bool q8 = px && px->qk_pool;
+    const size_t smem = 1024 + (size_t)(q8 ? decode_smem_bytes<D, kPagedQ>()
+                                           : decode_smem_bytes<D, kPlain>());
     auto kern = fx                 ? decode_split_kernel<T, D, kFused>
                 : px && px->qk_pool ? decode_split_kernel<T, D, kPagedQ>
                 : px               ? decode_split_kernel<T, D, kPaged>
@@ -1572,18 +1643,31 @@ kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const 
     return kvc_host::launch_status();
 }
 
-template <typename T>
-kvc_status dispatch_decode16(int D, void *out, const void *q, const void *k, const void *v,
-                             const kvc_lengths &len, int B, int Hq, int Hkv, int64_t C, int W,
-                             float scale, const float *cs, const float *sn, int64_t rmax,
-                             void *ws, int ring, int32_t *st, cudaStream_t stream)
+// the 16-bit tensor-core kernels: element type and head dimension as
+// template arguments
+template <typename T_, int D_> struct Dim16 {
+    using T = T_;
+    static constexpr int D = D_;
+};
+inline bool dim16_ok(int D) { return D == 64 || D == 128 || D == 256; }
+
+template <typename F> kvc_status with_dim16(int dtype, int D, F &&f)
 {
-    if (D == 64)
-        return launch_decode16<T, 64>(out, q, k, v, len, B, Hq, Hkv, C, W, scale, cs, sn, rmax,
-                                      ws, ring, st, stream);
-    if (D == 128)
-        return launch_decode16<T, 128>(out, q, k, v, len, B, Hq, Hkv, C, W, scale, cs, sn, rmax,
-                                       ws, ring, st, stream);
+    if (dtype == KVC_BF16) {
+        if (D == 64)
+            return f(Dim16<__nv_bfloat16, 64>{});
+        if (D == 128)
+            return f(Dim16<__nv_bfloat16, 128>{});
+        if (D == 256)
+            return f(Dim16<__nv_bfloat16, 256>{});
+    } else if (dtype == KVC_F16) {
+        if (D == 64)
+            return f(Dim16<__half, 64>{});
+        if (D == 128)
+            return f(Dim16<__half, 128>{});
+        if (D == 256)
+            return f(Dim16<__half, 256>{});
+    }
     return KVC_ERR_UNSUPPORTED;
 }
 
@@ -1625,7 +1709,7 @@ kvc_status decode_entry(void *out, const void *q, const void *k_cache, const voi
     if (rope_cos && rope_max_pos < 1)
         return KVC_ERR_SHAPE;
     const int g = q_heads / kv_heads;
-    if (dtype == KVC_F32 ? head_dim > 256 : ((head_dim != 64 && head_dim != 128) || g > 16))
+    if (dtype == KVC_F32 ? head_dim > 256 : (!dim16_ok(head_dim) || g > 16))
         return KVC_ERR_UNSUPPORTED;
     if (batch == 0)
         return KVC_OK;
@@ -1647,14 +1731,12 @@ kvc_status decode_entry(void *out, const void *q, const void *k_cache, const voi
         return kvc_f32::launch(out, q, k_cache, v_cache, capacity, len, batch, q_heads, kv_heads,
                                1, head_dim, local_window_size, scale, rope_cos, rope_sin,
                                rope_max_pos, ring ? 2 : 0, dev_status, stream);
-    if (dtype == KVC_BF16)
-        return dispatch_decode16<__nv_bfloat16>(head_dim, out, q, k_cache, v_cache, len, batch,
-                                                q_heads, kv_heads, capacity, local_window_size,
-                                                scale, rope_cos, rope_sin, rope_max_pos,
-                                                workspace, ring, dev_status, stream);
-    return dispatch_decode16<__half>(head_dim, out, q, k_cache, v_cache, len, batch, q_heads,
-                                     kv_heads, capacity, local_window_size, scale, rope_cos,
-                                     rope_sin, rope_max_pos, workspace, ring, dev_status, stream);
+    return with_dim16(dtype, head_dim, [&](auto td) {
+        using TD = decltype(td);
+        return launch_decode16<typename TD::T, TD::D>(
+            out, q, k_cache, v_cache, len, batch, q_heads, kv_heads, capacity, local_window_size,
+            scale, rope_cos, rope_sin, rope_max_pos, workspace, ring, dev_status, stream);
+    });
 }
 
 } // namespace
@@ -1699,7 +1781,7 @@ kvc_status paged_decode_entry(void *out, const void *q, const void *k_pool, cons
         return dtype == KVC_F32 ? KVC_ERR_UNSUPPORTED : KVC_ERR_DTYPE;
     if (batch < 0 || q_heads < 1 || kv_heads < 1 || q_heads % kv_heads != 0)
         return KVC_ERR_SHAPE;
-    if ((head_dim != 64 && head_dim != 128) || q_heads / kv_heads > 16)
+    if (!dim16_ok(head_dim) || q_heads / kv_heads > 16)
         return KVC_ERR_UNSUPPORTED;
     // pages hold whole 64-row tiles
     if (page_size < kTile || page_size % kTile != 0 || max_pages < 1 || n_pool_pages < 1)
@@ -1733,26 +1815,12 @@ kvc_status paged_decode_entry(void *out, const void *q, const void *k_pool, cons
     const PagedExtra px{block_table, max_pages, page_size, n_pool_pages, qk_pool, qv_pool, qparams,
                         n_q_pages};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (dtype == KVC_BF16)
-        return head_dim == 64
-                   ? launch_decode16<__nv_bfloat16, 64>(out, q, k_pool, v_pool, len, batch, q_heads,
-                                                        kv_heads, capacity, local_window_size,
-                                                        scale, rope_cos, rope_sin, rope_max_pos,
-                                                        workspace, 0, dev_status, st, nullptr,
-                                                        &px)
-                   : launch_decode16<__nv_bfloat16, 128>(
-                         out, q, k_pool, v_pool, len, batch, q_heads, kv_heads, capacity,
-                         local_window_size, scale, rope_cos, rope_sin, rope_max_pos, workspace, 0,
-                         dev_status, st, nullptr, &px);
-    return head_dim == 64
-               ? launch_decode16<__half, 64>(out, q, k_pool, v_pool, len, batch, q_heads, kv_heads,
-                                             capacity, local_window_size, scale, rope_cos,
-                                             rope_sin, rope_max_pos, workspace, 0, dev_status, st,
-                                             nullptr, &px)
-               : launch_decode16<__half, 128>(out, q, k_pool, v_pool, len, batch, q_heads,
-                                              kv_heads, capacity, local_window_size, scale,
-                                              rope_cos, rope_sin, rope_max_pos, workspace, 0,
-                                              dev_status, st, nullptr, &px);
+    return with_dim16(dtype, head_dim, [&](auto td) {
+        using TD = decltype(td);
+        return launch_decode16<typename TD::T, TD::D>(
+            out, q, k_pool, v_pool, len, batch, q_heads, kv_heads, capacity, local_window_size,
+            scale, rope_cos, rope_sin, rope_max_pos, workspace, 0, dev_status, st, nullptr, &px);
+    });
 }
 
 } // namespace
@@ -1843,8 +1911,7 @@ KVC_API kvc_status kvc_decode_step(void *out, const void *q, void *k_cache, void
     const int g = q_heads / kv_heads;
     // the merge keeps 3 x 16 x splits floats next to the 4-warp partials in
     // the stage buffers: at most 128 splits (capacity 65536)
-    if (dtype == KVC_F32 || (head_dim != 64 && head_dim != 128) || g > 16 ||
-        decode_max_splits(capacity) > 128)
+    if (dtype == KVC_F32 || !dim16_ok(head_dim) || g > 16 || decode_max_splits(capacity) > 128)
         return KVC_ERR_UNSUPPORTED;
     const bool some_len = len.past_abs || len.total_abs || len.cache_past || len.cache_total ||
                           len.evict;
@@ -1878,25 +1945,12 @@ KVC_API kvc_status kvc_decode_step(void *out, const void *q, void *k_cache, void
     const kvc_lengths l = some_len ? len : kvc_lengths{nullptr, nullptr, nullptr, nullptr, nullptr};
     const int ring = windowed == KVC_RING;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (dtype == KVC_BF16)
-        return head_dim == 64
-                   ? launch_decode16<__nv_bfloat16, 64>(out, q, k_cache, v_cache, l, batch, q_heads,
-                                                        kv_heads, capacity, local_window_size,
-                                                        scale, rope_cos, rope_sin, rope_max_pos,
-                                                        workspace, ring, dev_status, st, &fx)
-                   : launch_decode16<__nv_bfloat16, 128>(
-                         out, q, k_cache, v_cache, l, batch, q_heads, kv_heads, capacity,
-                         local_window_size, scale, rope_cos, rope_sin, rope_max_pos, workspace,
-                         ring, dev_status, st, &fx);
-    return head_dim == 64
-               ? launch_decode16<__half, 64>(out, q, k_cache, v_cache, l, batch, q_heads,
-                                             kv_heads, capacity, local_window_size, scale,
-                                             rope_cos, rope_sin, rope_max_pos, workspace, ring,
-                                             dev_status, st, &fx)
-               : launch_decode16<__half, 128>(out, q, k_cache, v_cache, l, batch, q_heads,
-                                              kv_heads, capacity, local_window_size, scale,
-                                              rope_cos, rope_sin, rope_max_pos, workspace, ring,
-                                              dev_status, st, &fx);
+    return with_dim16(dtype, head_dim, [&](auto td) {
+        using TD = decltype(td);
+        return launch_decode16<typename TD::T, TD::D>(
+            out, q, k_cache, v_cache, l, batch, q_heads, kv_heads, capacity, local_window_size,
+            scale, rope_cos, rope_sin, rope_max_pos, workspace, ring, dev_status, st, &fx);
+    });
 }
 
 namespace {
@@ -1964,7 +2018,7 @@ KVC_API kvc_status kvc_window_decode_step(void *out, const void *q, void *k_cach
     if (rope_cos && rope_max_pos < 1)
         return KVC_ERR_SHAPE;
     const int g = q_heads / kv_heads;
-    if (dtype == KVC_F32 || (head_dim != 64 && head_dim != 128) || g > 16 ||
+    if (dtype == KVC_F32 || !dim16_ok(head_dim) || g > 16 ||
         capacity > window_step_max_capacity(head_dim))
         return KVC_ERR_UNSUPPORTED;
     const bool some_len = len.past_abs || len.total_abs || len.cache_past || len.cache_total ||
@@ -2005,11 +2059,10 @@ KVC_API kvc_status kvc_window_decode_step(void *out, const void *q, void *k_cach
     a.rope_max_pos = rope_max_pos;
     a.status = dev_status;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (dtype == KVC_BF16)
-        return head_dim == 64 ? launch_window_step<__nv_bfloat16, 64>(a, batch, st)
-                              : launch_window_step<__nv_bfloat16, 128>(a, batch, st);
-    return head_dim == 64 ? launch_window_step<__half, 64>(a, batch, st)
-                          : launch_window_step<__half, 128>(a, batch, st);
+    return with_dim16(dtype, head_dim, [&](auto td) {
+        using TD = decltype(td);
+        return launch_window_step<typename TD::T, TD::D>(a, batch, st);
+    });
 }
 
 // --------------------------------------------------------------------------

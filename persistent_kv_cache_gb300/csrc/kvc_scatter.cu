@@ -47,15 +47,6 @@ scatter_rows_kernel(char *__restrict__ present, const char *__restrict__ update,
     }
 }
 
-// Functional TensorScatter in one pass: every vector of present is written
-// once, from the update when its row is one of the S rows written into its
-// prefix, else from past.  A prefix holds span = max_seq * row_vecs vectors;
-// its written rows start at vector base = (first written row) * row_vecs and
-// run on, modulo span in circular mode, so a vector's distance from base
-// (taken modulo span) is at once the test (< S * row_vecs) and its offset in
-// the prefix's block of the update: no division per vector.  Linear mode with
-// an index out of range leaves that batch row equal to past and raises
-// KVC_DEV_INDEX_OOB, as the in-place form does.
 // the source of present's vector k in a prefix: the update when k lies in the
 // written range (offset from base, modulo span, below n_upd), else past
 template <typename V>
@@ -68,6 +59,19 @@ __device__ __forceinline__ const V *pick_source(const V *src, const V *upd, int6
     return off < n_upd ? upd + off : src + k;
 }
 
+// Functional TensorScatter in one pass: every vector of present is written
+// once, from the update when its row is one of the S rows written into its
+// prefix, else from past.  A prefix holds span = max_seq * row_vecs vectors;
+// its written rows start at vector base = (first written row) * row_vecs and
+// run on, modulo span in circular mode, so a vector's distance from base
+// (taken modulo span) is at once the test (< S * row_vecs) and its offset in
+// the prefix's block of the update: no division per vector.  Linear mode with
+// an index out of range leaves that batch row equal to past and raises
+// KVC_DEV_INDEX_OOB, as the in-place form does.  A block covers one tile of
+// kCopyTile vectors of one prefix, so the host sends prefixes shorter than a
+// tile to the copy + in-place scatter pair instead.
+constexpr int64_t kCopyTile = 1024;
+
 template <typename V>
 __global__ void __launch_bounds__(256, 6)
 scatter_copy_kernel(V *__restrict__ present, const V *__restrict__ past,
@@ -78,7 +82,7 @@ scatter_copy_kernel(V *__restrict__ present, const V *__restrict__ past,
     // one contiguous tile of 4 x 256 vectors of one prefix per block: each
     // warp reads and writes 32 consecutive vectors per access, four in flight
     const int64_t span = max_seq * row_vecs, upd_vecs = seq_len * row_vecs;
-    const int64_t k0 = (int64_t)blockIdx.x * 1024 + threadIdx.x;
+    const int64_t k0 = (int64_t)blockIdx.x * kCopyTile + threadIdx.x;
     for (int64_t p = blockIdx.y; p < n_prefix; p += gridDim.y) {
         const int64_t b = p / prefixes_per_batch;
         const int64_t wi = write_indices ? write_indices[b] : 0;
@@ -121,7 +125,7 @@ void launch_scatter_copy(char *present, const char *past, const char *update, co
 {
     // x: the 1024-vector tiles of one prefix; y: prefixes (looped past 65535)
     const int64_t row_vecs = slice_bytes / (int64_t)sizeof(V);
-    const int64_t gx = (max_seq * row_vecs + 1023) / 1024;
+    const int64_t gx = (max_seq * row_vecs + kCopyTile - 1) / kCopyTile;
     const int64_t gy = n_prefix < 65535 ? n_prefix : 65535;
     scatter_copy_kernel<V><<<dim3((unsigned)gx, (unsigned)gy), 256, 0, stream>>>(
         reinterpret_cast<V *>(present), reinterpret_cast<const V *>(past),
@@ -328,13 +332,22 @@ KVC_API kvc_status kvc_tensor_scatter(void *present_cache, const void *past_cach
     const int64_t ppb = n_prefix / cache_shape[0];
     const int circ = mode == KVC_CIRCULAR;
 
-    if (!in_place && update_seq_len > 0) {
-        // copy and scatter in one pass, the widest vector every pointer allows
+    const char *upd_c = static_cast<const char *>(update);
+    const uintptr_t a_all = reinterpret_cast<uintptr_t>(present_cache) |
+                            reinterpret_cast<uintptr_t>(past_cache) |
+                            reinterpret_cast<uintptr_t>(upd_c);
+    // vector width of the one-pass form (the widest every pointer allows)
+    const int64_t vw = (slice % 16 == 0 && (a_all & 15u) == 0)  ? 16
+                       : (slice % 8 == 0 && (a_all & 7u) == 0) ? 8
+                       : (slice % 4 == 0 && (a_all & 3u) == 0) ? 4
+                       : (slice % 2 == 0 && (a_all & 1u) == 0) ? 2
+                                                                : 1;
+    if (!in_place && update_seq_len > 0 && max_seq * slice >= kCopyTile * vw) {
+        // copy and scatter in one pass: each prefix fills at least one tile
         char *dst = static_cast<char *>(present_cache);
         const char *src = static_cast<const char *>(past_cache);
-        const char *upd = static_cast<const char *>(update);
-        const uintptr_t a = reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src) |
-                            reinterpret_cast<uintptr_t>(upd);
+        const char *upd = upd_c;
+        const uintptr_t a = a_all;
         if (slice % 16 == 0 && (a & 15u) == 0)
             launch_scatter_copy<uint4>(dst, src, upd, write_indices, n_prefix, ppb, max_seq,
                                        update_seq_len, slice, circ, dev_status, stream);

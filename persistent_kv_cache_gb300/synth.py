@@ -134,3 +134,9 @@ WINDOW_PREFILL = DecodeWorkload("window-prefill-bf16-b8-h16kv8-d256-w4096", batc
                                 q_heads=16, kv_heads=8, head_dim=256, capacity=4096,
                                 window=4096, windowed=True, total_lo=0, total_hi=20000,
                                 new_tokens=(64, 512, 2048))
+# one-token decode on the windowed-prefill workload's heads (16 / 8, head_dim
+# 256) held as a ring of C = W = 4096 slots, past lengths as the prefill's
+WINDOW_DECODE_256 = DecodeWorkload("window-decode-ring-bf16-b8-h16kv8-d256-c4096-w4096",
+                                   batch=8, q_heads=16, kv_heads=8, head_dim=256,
+                                   capacity=4096, window=4096, windowed=True, total_lo=1,
+                                   total_hi=20000, extra={"policy": 3})

@@ -121,6 +121,9 @@ def test_decode_host_checks(kvc):
     bad = [FAKE + 8] + base[1:]
     assert f(*bad, 2, 8, 2, 64, 128, 1, 0, 0.0, None, None, 0, FAKE, 256, None, None) == 4
     assert lib.kvc_gqa_decode_workspace_size(2, 8, 2, 128, 64, 1) == 256
+    # head_dim 256 is a supported 16-bit size: a missing workspace is the error
+    assert f(*base, 2, 16, 8, 8192, 256, 1, 0, 0.0, None, None, 0, None, 0, None, None) == 8
+    assert f(*base, 2, 16, 8, 8192, 256, 2, 0, 0.0, None, None, 0, None, 0, None, None) == 8
 
 
 def test_decode_ring_host_checks(kvc):

@@ -102,7 +102,7 @@ def _decode_case(K, orc, dtype, B, Hq, Hkv, D, C, T, window, windowed, rope, see
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("g", [1, 4, 8])
 def test_contiguous_ragged(K, orc, dtype, D, g):
     Hkv = 2
@@ -118,6 +118,18 @@ def test_multi_split_with_window(K, orc, g):
     for window in (0, 700, 64, 1):
         _decode_case(K, orc, torch.bfloat16, len(T), 2 * g, 2, 128, 4096, T, window, 0, True,
                      20 + window)
+
+
+@pytest.mark.parametrize("g", [1, 2, 16])
+def test_head_dim_256_multi_split(K, orc, g):
+    """head_dim 256 (tiles in a ring of three 32 KB slots, the query's
+    fragments read from shared memory): 512-row splits merged by the
+    combine pass, windows cutting rows at unaligned places."""
+    T = [1, 63, 64, 65, 511, 513, 2048, 4096]
+    for window in (0, 4096, 700, 1):
+        for dtype in (torch.bfloat16, torch.float16):
+            _decode_case(K, orc, dtype, len(T), 2 * g, 2, 256, 4096, T, window, 0, True,
+                         50 + window + g)
 
 
 def test_more_splits_than_the_fast_merge(K, orc):

@@ -83,7 +83,7 @@ def _one_token_run(K, orc, fused, B, g, Hkv, D, C, W, T0, steps, seed):
 
 
 @pytest.mark.parametrize("fused", [False, True])
-@pytest.mark.parametrize("D,g", [(64, 8), (128, 4)])
+@pytest.mark.parametrize("D,g", [(64, 8), (128, 4), (256, 2)])
 def test_drift_one_token_steps(K, orc, fused, D, g):
     W = 120
     C = W + 8

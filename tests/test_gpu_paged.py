@@ -93,7 +93,9 @@ def test_paged_workload_full_size(K, orc):
 @pytest.mark.parametrize("P,D,g,W,dtype", [(64, 128, 4, 700, torch.bfloat16),
                                            (128, 64, 8, 100, torch.float16),
                                            (256, 128, 2, 0, torch.bfloat16),
-                                           (64, 64, 16, 1, torch.bfloat16)])
+                                           (64, 64, 16, 1, torch.bfloat16),
+                                           (64, 256, 2, 1000, torch.bfloat16),
+                                           (128, 256, 4, 0, torch.float16)])
 def test_paged_steps(K, orc, P, D, g, W, dtype):
     """Chunks then one-token steps, window boundaries off the tiles."""
     B, Hkv = 4, 2

@@ -160,7 +160,7 @@ def _quantize_table(K, table, n_rows, P, kp_d, vp_d, qk, qv, qp, ks, kz, ku, vs,
     return new
 
 
-@pytest.mark.parametrize("D,zp,uns", [(128, 0, False), (64, 128, True)])
+@pytest.mark.parametrize("D,zp,uns", [(128, 0, False), (64, 128, True), (256, 3, False)])
 def test_grid_values_equal_16bit_decode(K, D, zp, uns):
     """Every value k * 2^-5 (|k| <= 100): the int8 pages reconstruct exactly
     and the int8 decode equals the 16-bit paged decode bit for bit."""
@@ -226,7 +226,9 @@ def test_full_size_int8_cold_pages(K, orc):
 @pytest.mark.parametrize("P,D,g,W,dtype,uns", [(64, 128, 4, 700, torch.bfloat16, False),
                                                (128, 64, 8, 100, torch.float16, True),
                                                (256, 128, 2, 0, torch.bfloat16, True),
-                                               (64, 64, 16, 1, torch.bfloat16, False)])
+                                               (64, 64, 16, 1, torch.bfloat16, False),
+                                               (64, 256, 2, 1000, torch.bfloat16, False),
+                                               (128, 256, 8, 0, torch.float16, True)])
 def test_mixed_tables(K, orc, P, D, g, W, dtype, uns):
     B, Hkv, max_pages = 4, 2, 12
     Hq = Hkv * g

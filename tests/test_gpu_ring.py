@@ -73,7 +73,8 @@ def _steps(K, orc, fused, B, g, Hkv, D, C, W, T0, steps, seed):
 
 
 @pytest.mark.parametrize("fused", [False, True])
-@pytest.mark.parametrize("D,g,C,W", [(64, 8, 128, 128), (128, 4, 128, 100), (64, 16, 96, 40)])
+@pytest.mark.parametrize("D,g,C,W", [(64, 8, 128, 128), (128, 4, 128, 100), (64, 16, 96, 40),
+                                     (256, 2, 128, 128), (256, 8, 64, 50)])
 def test_ring_one_token_steps(K, orc, fused, D, g, C, W):
     T0 = [1, C - 2, C, C + 1, 700, 30001]
     _steps(K, orc, fused, len(T0), g, 2, D, C, W, T0, 5, 110 + D + C + fused)

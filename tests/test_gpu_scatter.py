@@ -164,10 +164,14 @@ def test_linear_out_of_range_leaves_row(K, orc):
 
 
 @pytest.mark.parametrize("case", ["bytes3", "full_ring", "linear_oob", "no_indices",
-                                  "many_prefixes", "long_prefix"])
+                                  "many_prefixes", "long_prefix", "wide8_long", "wide4_long",
+                                  "wide2_long", "wide1_long", "linear_oob_long"])
 def test_functional_edges(K, orc, case):
-    """The one-pass functional form (present != past) on the shapes that
-    steer its vector width, its grid and its index arithmetic."""
+    """The functional form (present != past) on the shapes that steer its
+    path, vector width, grid and index arithmetic: prefixes shorter than one
+    16 KB tile of the one-pass kernel take the copy + in-place scatter pair
+    (the first five cases); longer ones take the one-pass kernel at 16-, 8-,
+    4-, 2- and 1-byte vectors, each with a write that wraps the ring."""
     rng = np.random.default_rng(sum(map(ord, case)))
     npdt, shape, S, mode, wi = {
         # 3-byte rows: the byte-wide path
@@ -181,6 +185,13 @@ def test_functional_edges(K, orc, case):
         "many_prefixes": (np.uint8, (2, 35000, 3, 16), 2, 1, np.array([1, 5])),
         # a single long prefix spread over many blocks, 16-byte rows
         "long_prefix": (np.float16, (1, 1, 20011, 8), 37, 1, np.array([20000])),
+        # one-pass kernel at the narrower vector widths (8-, 4-, 6- and 3-byte rows)
+        "wide8_long": (np.float16, (2, 3, 4100, 4), 9, 1, np.array([4095, -3])),
+        "wide4_long": (np.float16, (2, 3, 4099, 2), 5, 1, np.array([4097, 7])),
+        "wide2_long": (np.float16, (2, 2, 3001, 3), 4, 1, np.array([2999, 3000])),
+        "wide1_long": (np.uint8, (2, 2, 1500, 3), 6, 1, np.array([1497, -1])),
+        # batch row 0 out of range in the one-pass kernel
+        "linear_oob_long": (np.float16, (2, 2, 5000, 8), 11, 0, np.array([4990, 10])),
     }[case]
     ush = list(shape)
     ush[2] = S
@@ -196,4 +207,4 @@ def test_functional_edges(K, orc, case):
     assert_bytes_equal(out, want, case)
     assert_bytes_equal(tp, past, case + ": past untouched")
     assert bool(st.item() & K.KVC_DEV_INDEX_OOB) == bool(flags.any())
-    assert (case == "linear_oob") == bool(flags.any())
+    assert case.startswith("linear_oob") == bool(flags.any())

@@ -100,6 +100,10 @@ def test_contiguous_workload_full_size(K, orc):
     # capacity 12288: up to 24 splits a row, past the merge's 16-split fast path
     (False, torch.bfloat16, 128, 4, 12288, 0),
     (True, torch.bfloat16, 128, 4, 12288, 5000),
+    # head_dim 256 (three 32 KB ring slots a CTA)
+    (False, torch.bfloat16, 256, 2, 4096, 0),
+    (True, torch.float16, 256, 2, 4096, 4096),
+    (True, torch.bfloat16, 256, 8, 300, 130),
 ])
 def test_consecutive_steps_and_graph(K, orc, ring, dtype, D, g, C, W):
     B, Hkv = 5, 2
