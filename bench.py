@@ -34,9 +34,24 @@ Other workloads (--workload):
                   shuffled page pool (lengths + paged append + paged decode)
   paged-decode-int8  the same with every full page below a row's newest one
                   quantized to int8 (lengths + append + mixed-page decode)
+  ring-decode-d256  one-token decode at head_dim 256: 8 x 16/8 heads held as
+                  a ring of C = W = 4096 slots, T ~ U[1, 20000] (one
+                  kvc_decode_step + merge)
+  window-decode-d256  the same heads kept compacted (C = W = 4096): lengths +
+                  in-place compaction by one row (cluster kernel) + split
+                  decode + merge; the roofline kernel is the compaction
+
+The default one-GPU run also times window-prefill at S = 2048 and S = 64,
+window-decode, scatter-functional (S = 64), ring-decode-d256 and
+window-decode-d256, each as an
+entry of the line's "secondary" list with its own roofline, clocks and CPU
+baseline (--no-secondary leaves them out).  Before each timed region the
+step graph is replayed for --soak seconds (default 1) so that the clock
+record covers the GPU under that load.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--workload ...] [--chunk S] [--profile]
+                       [--workload ...] [--chunk S] [--profile] [--soak SEC]
+                       [--secondary | --no-secondary]
 Prints one JSON line (rank 0).
 """
 from __future__ import annotations
@@ -123,12 +138,15 @@ class ClockSampler:
             except ValueError:
                 continue
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        busy = [r for r in rows if r[2] > 0] or rows
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0,
+                    "samples_under_load": 0}
+        loaded = [r for r in rows if r[2] > 0]
+        busy = loaded or rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in busy for i, v in enumerate(r[3]) if v == "Active"})
         return {"sm_mhz": float(np.median([r[0] for r in busy])), "sm_max_mhz": busy[0][1],
-                "reasons": reasons, "samples": len(busy)}
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded),
+                "sm_mhz_min_under_load": min(r[0] for r in busy)}
 
 
 # --------------------------------------------------------------------------
@@ -940,7 +958,165 @@ class WindowDecodeRing(WindowDecode):
     spec = "WINDOW_DECODE_RING"
 
 
+class RingDecode256(Workload):
+    """One-token decode at head_dim 256: the windowed-prefill workload's heads
+    (8 x 16/8 heads, W = 4096) as a ring of C = 4096 slots, past lengths
+    U[1, 20000]; one step = one kvc_decode_step (lengths, RoPE append of the
+    new row, split decode) plus the split merge."""
+    bound = "hbm"
+    roofline_kernel = "kvc_decode_step, ring, head_dim 256 (split + merge)"
+    traffic_key = ("kvc_decode.cu", "decode_split_kernel_fused@ring_d256")
+
+    def __init__(self, dev, seed=0, with_kernels=True, chunk=None):
+        import torch
+
+        from persistent_kv_cache_gb300 import synth
+        self.torch = torch
+        w = self.w = synth.WINDOW_DECODE_256
+        B, Hq, Hkv, D, C, W = w.batch, w.q_heads, w.kv_heads, w.head_dim, w.capacity, w.window
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        bf = torch.bfloat16
+        self.kc = torch.randn(B, Hkv, C, D, generator=g, device=dev, dtype=bf)
+        self.vc = torch.randn(B, Hkv, C, D, generator=g, device=dev, dtype=bf)
+        self.T = synth.randint(w.total_lo, w.total_hi + 1, (B,), seed, 256).numpy()
+        sk_host = torch.from_numpy((self.T - 1).astype(np.int32))
+        self.q_host = synth.normal((B, Hq, 1, D), seed, 5)
+        self.nk_host = synth.normal((B, Hkv, 1, D), seed, 3)
+        self.nv_host = synth.normal((B, Hkv, 1, D), seed, 4)
+        self.host_inputs = [sk_host, self.q_host, self.nk_host, self.nv_host]
+        self.device_inputs = [t.to(dev) for t in self.host_inputs]
+        self.sk, self.q, self.nk, self.nv = self.device_inputs
+        cos, sin = synth.rope_cache(int(self.T.max()) + 1, D, w.theta)
+        self.rope = (cos.to(dev), sin.to(dev))
+        e = self.e
+        # the visible rows (the newest min(T, C, W) positions) of K and V,
+        # q read, out written, the new K/V row read and written
+        vis = np.minimum(np.minimum(self.T, C), W)
+        self.bytes_per_step = (int(vis.sum()) * Hkv * D * 2 * e + 2 * B * Hq * D * e
+                               + 2 * 2 * B * Hkv * D * e)
+        self.kernel_bytes = self.bytes_per_step
+        self.tokens_per_step = B
+        if not with_kernels:
+            return
+        from persistent_kv_cache_gb300 import kvc as K
+        self.K = K
+        self.out = torch.empty(B, Hq, 1, D, dtype=bf, device=dev)
+        self.L = K.Lengths(B, dev)
+        self.st = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.ws = K.decode_step_workspace(self.out, self.kc)
+        merge = 1 if K.kvc_gqa_decode_workspace_size(B, Hq, Hkv, C, D, K.KVC_BF16) > 256 else 0
+        self.launches_per_step = 1 + merge
+
+    def step(self, i):
+        self.K.kvc_decode_step(self.out, self.q, self.kc, self.vc, self.nk, self.nv, self.sk,
+                               self.w.window, lengths=self.L, rope=self.rope, workspace=self.ws,
+                               status=self.st, windowed=self.K.KVC_RING)
+
+    def kernel(self, i):
+        self.step(i)
+
+    def config(self):
+        w = self.w
+        return {"workload": w.name, "batch": w.batch, "q_heads": w.q_heads,
+                "kv_heads": w.kv_heads, "head_dim": w.head_dim, "capacity": w.capacity,
+                "window": w.window, "layout": "ring", "total_len": f"U[{w.total_lo},{w.total_hi}]",
+                "rope_theta": w.theta, "new_tokens": 1, "fused_step": True,
+                "l2": "inputs larger than L2 (~268 MB of K/V read per step)",
+                "bytes_per_step": self.bytes_per_step}
+
+    def oracle_sample(self, rows, sync=None):
+        import oracle
+        from persistent_kv_cache_gb300 import synth
+        w = self.w
+        rows = list(rows)
+        kc = synth.bits(self.kc[rows].cpu()).copy()
+        vc = synth.bits(self.vc[rows].cpu()).copy()
+        cos, sin = (t.cpu().numpy() for t in self.rope)
+        T = self.T[rows]
+        if sync is not None:
+            sync()  # the threads of a parallel sample start together
+        t0 = time.perf_counter()
+        oracle.ring_append(kc, vc, synth.bits(self.nk_host[rows]), synth.bits(self.nv_host[rows]),
+                           T - 1, cos, sin)
+        oracle.ring_attention(synth.bits(self.q_host[rows]), kc, vc, T, w.window, cos_cache=cos,
+                              sin_cache=sin)
+        dt = time.perf_counter() - t0
+        return dt, self.bytes_per_step * len(rows) / w.batch
+
+    def metric(self):
+        return "ring decode, head_dim 256: achieved HBM GB/s, decode steps/s", "GB/s"
+
+
+class WindowDecode256(RingDecode256):
+    """One-token steps on the windowed-prefill workload's cache kept
+    compacted (C = W = 4096, head_dim 256, 8 x 16/8 heads, past lengths
+    U[1, 20000]): lengths, the in-place compaction of the whole window by one
+    row plus the RoPE append (a cluster of eight CTAs per slice), then the
+    split decode and merge.  The roofline kernel is the compaction."""
+    roofline_kernel = "kvc_window_append, S = 1 (cluster compaction)"
+    traffic_key = ("kvc_cache.cu", "compact_cluster_kernel@window_d256")
+
+    def __init__(self, dev, seed=0, with_kernels=True, chunk=None):
+        super().__init__(dev, seed=seed, with_kernels=with_kernels, chunk=chunk)
+        w, e = self.w, self.e
+        B, Hq, Hkv, D, C = w.batch, w.q_heads, w.kv_heads, w.head_dim, w.capacity
+        Lp, E, L = _cache_lengths(1, self.T, 1, C, w.window)
+        row = Hkv * D * 2 * e
+        # compaction: the Lp - E surviving rows read and written where rows
+        # evict, the new row read and written; decode: the L visible rows,
+        # q read and out written
+        self.kernel_bytes = int((2 * (Lp - E) * (E > 0)).sum()) * row + 2 * B * row
+        self.bytes_per_step = self.kernel_bytes + int(L.sum()) * row + 2 * B * Hq * D * e
+        if with_kernels:
+            self.ws = self.K.decode_workspace(self.out, self.kc)
+            self.launches_per_step = 3 + (1 if self.ws.numel() > 256 else 0)
+
+    def step(self, i):
+        K, w = self.K, self.w
+        K.kvc_seq_lengths(self.sk, 1, w.capacity, K.KVC_WINDOWED, local_window_size=w.window,
+                          out=self.L, status=self.st)
+        self.kernel(i)
+        K.kvc_gqa_decode(self.out, self.q, self.kc, self.vc, self.L, local_window_size=w.window,
+                         rope=self.rope, workspace=self.ws, status=self.st)
+
+    def kernel(self, i):
+        self.K.kvc_window_append(self.kc, self.vc, self.nk, self.nv, self.L, self.K.KVC_WINDOWED,
+                                 rope=self.rope, status=self.st)
+
+    def config(self):
+        c = super().config()
+        c.update({"workload": "window-decode-bf16-b8-h16kv8-d256-c4096-w4096",
+                  "layout": "compact every step", "fused_step": False,
+                  "l2": "~805 MB moved and read per step > L2"})
+        return c
+
+    def oracle_sample(self, rows, sync=None):
+        import oracle
+        from persistent_kv_cache_gb300 import synth
+        w = self.w
+        rows = list(rows)
+        kc = synth.bits(self.kc[rows].cpu()).copy()
+        vc = synth.bits(self.vc[rows].cpu()).copy()
+        cos, sin = (t.cpu().numpy() for t in self.rope)
+        sk = (self.T[rows] - 1).astype(np.int32)
+        if sync is not None:
+            sync()  # the threads of a parallel sample start together
+        t0 = time.perf_counter()
+        lens = oracle.seq_lengths(sk, 1, w.capacity, 1, w.window)
+        oracle.window_append(kc, vc, synth.bits(self.nk_host[rows]),
+                             synth.bits(self.nv_host[rows]), lens, 1, cos, sin)
+        oracle.gqa_attention(synth.bits(self.q_host[rows]), kc, vc, lens["cache_total"],
+                             lens["total_abs"], window=w.window, cos_cache=cos, sin_cache=sin)
+        dt = time.perf_counter() - t0
+        return dt, self.bytes_per_step * len(rows) / w.batch
+
+    def metric(self):
+        return "window decode, head_dim 256, C = W = 4096: achieved HBM GB/s, steps/s", "GB/s"
+
+
 WORKLOADS = {"contig-decode": ContigDecode, "contig-decode-unfused": ContigDecodeUnfused,
+             "ring-decode-d256": RingDecode256, "window-decode-d256": WindowDecode256,
              "paged-decode": PagedDecode,
              "window-decode": WindowDecode,
              "window-decode-unfused": WindowDecodeUnfused,
@@ -998,33 +1174,38 @@ def kernel_traffic(key):
         return None
 
 
-def run_ours(args):
-    import torch
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    n_steps = args.warmup * 2 + args.steps * 3 + 8
-    kw = {"chunk": args.chunk}
-    if args.workload in ("window-decode", "window-decode-unfused", "window-decode-drift",
-                         "window-decode-ring", "window-decode-hot", "scatter",
-                         "scatter-functional"):
-        kw["max_steps"] = n_steps
-    wl = WORKLOADS[args.workload](dev, seed=rank, **kw)
-    peaks, peak_kind = load_peaks()
+# workloads whose per-step inputs are drawn for a fixed number of steps
+_MAX_STEPS = ("window-decode", "window-decode-unfused", "window-decode-drift",
+              "window-decode-ring", "window-decode-hot", "scatter", "scatter-functional")
 
+# what the default one-GPU run also times, each as an entry of the line's
+# "secondary" list: (workload, chunk)
+SECONDARY = (("window-prefill", 2048), ("window-prefill", 64), ("window-decode", None),
+             ("scatter-functional", 64), ("ring-decode-d256", None),
+             ("window-decode-d256", None))
+
+
+def make_workload(name, dev, seed, chunk, n_steps):
+    kw = {"chunk": chunk}
+    if name in _MAX_STEPS:
+        kw["max_steps"] = n_steps
+    return WORKLOADS[name](dev, seed=seed, **kw)
+
+
+def time_workload(wl, args, world, dev, soak_s):
+    """W eager warm-up steps; the K timed steps captured once as a CUDA graph
+    (no host work in the timed region); the graph replayed for at least
+    `soak_s` seconds so that the clock sampler sees the GPU under this load;
+    then the K steps timed once (CUDA events, barrier and synchronize on both
+    sides), the roofline kernel's K launches timed from a second graph, ten
+    more replays for the spread, and the end-to-end pass."""
+    import torch
     with ClockSampler(dev) as clocks:
         i = 0
         for _ in range(args.warmup):
             wl.step(i)
             i += 1
         torch.cuda.synchronize()
-        # the K timed steps are captured once as a CUDA graph (no host work in
-        # the timed region) and replayed; a second graph holds only the
-        # roofline kernel's K launches, timed the same way
         step_graph, kern_graph = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.graph(step_graph):
             for k in range(args.steps):
@@ -1036,6 +1217,15 @@ def run_ours(args):
         step_graph.replay()
         kern_graph.replay()
         torch.cuda.synchronize()
+        t_soak = time.perf_counter()
+        soak_replays = 0
+        while time.perf_counter() - t_soak < soak_s:
+            step_graph.replay()
+            soak_replays += 1
+            if soak_replays % 4 == 0:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        soak_wall = time.perf_counter() - t_soak
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
@@ -1062,7 +1252,9 @@ def run_ours(args):
             reps.append(start.elapsed_time(end) / args.steps)
         reps.sort()
         replay_stats = {"replays": len(reps), "median_ms_per_step": reps[len(reps) // 2],
-                        "p10_ms_per_step": reps[len(reps) // 10]}
+                        "p10_ms_per_step": reps[len(reps) // 10],
+                        "soak_replays_before_timing": soak_replays, "soak_s": soak_wall}
+        del step_graph, kern_graph
         wl.e2e_setup()
         for _ in range(args.warmup):
             wl.e2e_step(i)
@@ -1077,14 +1269,13 @@ def run_ours(args):
         e2e_s = time.perf_counter() - t0
         barrier(world)
         measured = wl.extra_measure() if hasattr(wl, "extra_measure") else {}
-    status = int(wl.st.item())
-    ms = max_over_ranks(ms, world, dev)
-    e2e_s = max_over_ranks(e2e_s, world, dev)
-    if rank != 0:
-        return
+    return {"ms": ms, "kern_ms": kern_ms, "replay_stats": replay_stats, "e2e_s": e2e_s,
+            "measured": measured, "clocks": clocks.summary(), "status": int(wl.st.item())}
 
+
+def roofline_of(wl, args, world, ms, kern_ms, e2e_s, peaks, peak_kind):
+    """(value, e2e value, roofline object, extra keys) of one timed workload."""
     sec = ms / 1e3
-    metric, unit = wl.metric()
     if wl.bound == "tensor":
         value = wl.flops * args.steps * world / sec / 1e12
         e2e_value = wl.flops * args.steps * world / e2e_s / 1e12
@@ -1124,38 +1315,100 @@ def run_ours(args):
                                                   else NOMINAL_GBS)
     roof.update({"kernel": wl.roofline_kernel, "traffic": kernel_traffic(wl.traffic_key),
                  "avg_launch_ms": kern_ms})
-    cpu = None
-    if world == 1:
-        # bounded samples: the oracle over the batch rows (at most 32), on
-        # every host core (rows dealt over threads) for about 5 s of wall
-        # time, and on one thread for about 10 s
-        rows = range(min(wl.w.batch, 32))
-        scale = 1e12 if wl.bound == "tensor" else 1e9
-        pw, pa, preps, pn = oracle_threads(wl, rows, host_cores(), 5.0, 15.0)
-        sw, sa, sreps, _ = oracle_threads(wl, rows, 1, 10.0, 30.0)
-        cpu = {"value": pa / pw / scale, "unit": unit, "cores": pn, "kind": "oracle",
-               "sample": f"{type(wl).__name__}.oracle_sample over {len(rows)} batch rows "
-                         f"dealt over {pn} threads, {preps} repetitions, {pw:.1f} s wall; "
-                         f"the C oracle as written",
-               "single_thread": {"value": sa / sw / scale, "cores": 1,
-                                 "sample": f"the same rows on one thread, {sreps} "
-                                           f"repetitions, {sw:.1f} s"}}
+    return value, e2e_value, roof, extra
+
+
+def cpu_baseline_of(wl, parallel=(5.0, 15.0), single=(10.0, 30.0)):
+    """Bounded samples of the oracle over the workload's batch rows (at most
+    32): on every host core (rows dealt over threads), and, when `single` is
+    given, on one thread."""
+    unit = wl.metric()[1]
+    rows = range(min(wl.w.batch, 32))
+    scale = 1e12 if wl.bound == "tensor" else 1e9
+    pw, pa, preps, pn = oracle_threads(wl, rows, host_cores(), *parallel)
+    cpu = {"value": pa / pw / scale, "unit": unit, "cores": pn, "kind": "oracle",
+           "sample": f"{type(wl).__name__}.oracle_sample over {len(rows)} batch rows "
+                     f"dealt over {pn} threads, {preps} repetitions, {pw:.1f} s wall; "
+                     f"the C oracle as written"}
+    if single is not None:
+        sw, sa, sreps, _ = oracle_threads(wl, rows, 1, *single)
+        cpu["single_thread"] = {"value": sa / sw / scale, "cores": 1,
+                                "sample": f"the same rows on one thread, {sreps} "
+                                          f"repetitions, {sw:.1f} s"}
+    return cpu
+
+
+def secondary_entry(name, chunk, args, dev, peaks, peak_kind):
+    """One more workload timed the same way as the main line (one GPU)."""
+    import torch
+    n_steps = args.warmup * 2 + args.steps * 3 + 8
+    wl = make_workload(name, dev, 0, chunk, n_steps)
+    r = time_workload(wl, args, 1, dev, args.soak)
+    value, e2e_value, roof, extra = roofline_of(wl, args, 1, r["ms"], r["kern_ms"], r["e2e_s"],
+                                                peaks, peak_kind)
+    metric, unit = wl.metric()
+    sec = r["ms"] / 1e3
+    entry = {"workload": name, "chunk": chunk, "metric": metric, "value": value, "unit": unit,
+             "ms_per_step": r["ms"] / args.steps, "steps": args.steps,
+             "higher_is_better": True, "config": wl.config(), **extra, **r["measured"],
+             "steps_per_s": args.steps / sec,
+             "tokens_per_s": wl.tokens_per_step * args.steps / sec,
+             "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": wl.h2d,
+                     "d2h_bytes_per_step": wl.d2h, "steps_per_s": args.steps / r["e2e_s"]},
+             "roofline": roof, "replay_stats": r["replay_stats"],
+             "cpu_baseline": cpu_baseline_of(wl, parallel=(2.0, 6.0), single=None),
+             "gpu_launches": wl.launches_per_step * args.steps, "clocks": r["clocks"],
+             "device_status": r["status"]}
+    del wl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    n_steps = args.warmup * 2 + args.steps * 3 + 8
+    wl = make_workload(args.workload, dev, rank, args.chunk, n_steps)
+    peaks, peak_kind = load_peaks()
+    r = time_workload(wl, args, world, dev, args.soak)
+    ms = max_over_ranks(r["ms"], world, dev)
+    e2e_s = max_over_ranks(r["e2e_s"], world, dev)
+    if rank != 0:
+        return
+
+    sec = ms / 1e3
+    metric, unit = wl.metric()
+    value, e2e_value, roof, extra = roofline_of(wl, args, world, ms, r["kern_ms"], e2e_s, peaks,
+                                                peak_kind)
+    cpu = cpu_baseline_of(wl) if world == 1 else None
     line = {
         "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": wl.config(), **extra, **measured,
+        "config": wl.config(), **extra, **r["measured"],
         "steps_per_s": args.steps * world / sec,
         "tokens_per_s": wl.tokens_per_step * args.steps * world / sec,
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": wl.h2d,
                 "d2h_bytes_per_step": wl.d2h, "steps_per_s": args.steps * world / e2e_s},
         "roofline": roof,
-        "replay_stats": replay_stats,
+        "replay_stats": r["replay_stats"],
         "cpu_baseline": cpu,
         "gpu_launches": wl.launches_per_step * args.steps,
-        "clocks": clocks.summary(),
-        "device_status": status,
+        "clocks": r["clocks"],
+        "device_status": r["status"],
     }
+    if world == 1 and args.secondary:
+        del wl
+        torch.cuda.empty_cache()
+        line["secondary"] = [secondary_entry(n, c, args, dev, peaks, peak_kind)
+                             for n, c in SECONDARY if (n, c) != (args.workload, args.chunk)]
     print(json.dumps(line), flush=True)
 
 
@@ -1221,7 +1474,15 @@ def main():
                     help="new tokens per step (window-prefill: 64/512/2048; scatter: 1/16/64)")
     ap.add_argument("--profile", action="store_true",
                     help="device steps only (the command run under ncu)")
+    ap.add_argument("--soak", type=float, default=1.0,
+                    help="seconds of replays of the step graph before the timed region, so "
+                         "that the clock record covers the GPU under this load")
+    ap.add_argument("--secondary", dest="secondary", action="store_true", default=None,
+                    help="also time the other workloads (default on the one-GPU default run)")
+    ap.add_argument("--no-secondary", dest="secondary", action="store_false")
     args = ap.parse_args()
+    if args.secondary is None:
+        args.secondary = args.workload == "contig-decode" and args.chunk is None
     if args.profile:
         from persistent_kv_cache_gb300 import build as B
         B.build()

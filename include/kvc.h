@@ -16,7 +16,7 @@
  *                          a cache of 16-bit and int8 pages
  *     kvc_decode_step      lengths + append + decode in one launch (contiguous
  *                          cache or ring)
- *     kvc_window_decode_step  the same for a windowed cache (small windows)
+ *     kvc_window_decode_step  the same for a windowed cache
  *     kvc_gqa_prefill_chunk  multi-token GQA attention over staged rows
  *     kvc_tensor_scatter   the ONNX TensorScatter cache update (linear/circular)
  *
@@ -70,7 +70,7 @@
 extern "C" {
 #endif
 
-#define KVC_ABI_VERSION 5
+#define KVC_ABI_VERSION 6
 
 typedef enum {
     KVC_OK = 0,
@@ -279,7 +279,7 @@ kvc_status kvc_window_append_inplace(void *k_rows, void *v_rows, const void *new
  * scale         0 -> 1/sqrt(head_dim).
  * workspace     device scratch of kvc_gqa_decode_workspace_size(...) bytes
  *               (holds per-split partial (m, l, o)); 256-byte aligned.
- * Supported: KVC_BF16/KVC_F16 with head_dim in {64, 128} and
+ * Supported: KVC_BF16/KVC_F16 with head_dim in {64, 128, 256} and
  * q_heads / kv_heads <= 16 (tensor-core path); KVC_F32 with head_dim <= 256.
  * All buffers 16-byte aligned (KVC_ERR_ALIGN).
  */
@@ -386,7 +386,7 @@ kvc_status kvc_paged_append(void *k_pool, void *v_pool, const void *new_k, const
  * outside the pool sets KVC_DEV_INDEX_OOB; that row's output is then
  * undefined.  Workspace: kvc_gqa_decode_workspace_size(batch, q_heads,
  * kv_heads, max_pages * page_size, head_dim, dtype).  Supported:
- * KVC_BF16/KVC_F16, head_dim in {64, 128}, q_heads / kv_heads <= 16.
+ * KVC_BF16/KVC_F16, head_dim in {64, 128, 256}, q_heads / kv_heads <= 16.
  */
 kvc_status kvc_gqa_decode_paged(void *out, const void *q, const void *k_pool,
                                 const void *v_pool, const int32_t *block_table, int max_pages,
@@ -491,8 +491,8 @@ kvc_status kvc_gqa_decode_paged_q(void *out, const void *q, const void *k_pool,
  * local_window_size, scale, rope_*: as kvc_gqa_decode.
  * workspace       device, kvc_decode_step_workspace_size(...) bytes (the same
  *                 as kvc_gqa_decode_workspace_size), 256-byte aligned.
- * Supported: KVC_BF16/KVC_F16, head_dim in {64, 128}, q_heads / kv_heads <=
- * 16 (KVC_ERR_UNSUPPORTED otherwise).
+ * Supported: KVC_BF16/KVC_F16, head_dim in {64, 128, 256}, q_heads / kv_heads
+ * <= 16 (KVC_ERR_UNSUPPORTED otherwise).
  * Device errors as kvc_seq_lengths / kvc_window_append / kvc_gqa_decode.
  */
 kvc_status kvc_decode_step(void *out, const void *q, void *k_cache, void *v_cache,
@@ -508,17 +508,22 @@ size_t kvc_decode_step_workspace_size(int batch, int q_heads, int kv_heads, int6
                                       int head_dim, int dtype);
 
 /*
- * kvc_window_decode_step -- one fused one-token step on a windowed cache:
- * kvc_seq_lengths + kvc_window_append (S = 1) + kvc_gqa_decode in a single
- * launch, with the same results ("GQA support sliding_window_cache",
- * "Design": rows [E, Lp) move to [0, Lp - E), the new row goes to Lp - E;
- * attention over the window that results).  One CTA owns a (batch row, kv
- * head) slice and reads it once: the resident rows are loaded into shared
- * memory (when nothing is evicted, only those the window can see), written
- * back E rows lower when rows were evicted (else only the new row is
- * stored), and attended over from there.  For small windows:
- * capacity * head_dim <= 32768 (C <= 512 at D = 64, C <= 256 at D = 128),
- * else KVC_ERR_UNSUPPORTED.
+ * kvc_window_decode_step -- one one-token step on a windowed cache:
+ * kvc_seq_lengths + kvc_window_append (S = 1) + kvc_gqa_decode with the same
+ * results ("GQA support sliding_window_cache", "Design": rows [E, Lp) move
+ * to [0, Lp - E), the new row goes to Lp - E; attention over the window that
+ * results).
+ *   Small windows, capacity * head_dim <= 32768 (C <= 512 at D = 64, 256 at
+ *   D = 128, 128 at D = 256): a single launch.  One CTA owns a (batch row, kv
+ *   head) slice and reads it once: the resident rows are loaded into shared
+ *   memory (when nothing is evicted, only those the window can see), written
+ *   back E rows lower when rows were evicted (else only the new row is
+ *   stored), and attended over from there.  No workspace is used.
+ *   Larger windows: a ring runs as kvc_decode_step(KVC_RING); a windowed or
+ *   drifting cache runs as kvc_seq_lengths, kvc_window_append (the in-place
+ *   compaction of large slices runs as a cluster of CTAs per slice) and
+ *   kvc_gqa_decode.  The workspace holds the split partials, and the lengths
+ *   when `len` is all NULL.
  *
  * out, q          device [batch, q_heads, 1, head_dim].
  * k_cache/v_cache device [batch, kv_heads, capacity, head_dim], updated in place.
@@ -530,8 +535,10 @@ size_t kvc_decode_step_workspace_size(int batch, int q_heads, int kv_heads, int6
  *                 KVC_ERR_UNSUPPORTED).  For a ring the new row goes to slot
  *                 (T - 1) mod C, nothing else is written, and attention
  *                 reads the slots as kvc_gqa_decode_ring does.
+ * workspace       device, kvc_window_decode_step_workspace_size(...) bytes,
+ *                 256-byte aligned (0 bytes, NULL allowed, for small windows).
  * Requires 0 < local_window_size <= capacity (KVC_ERR_WINDOW).  Supported:
- * KVC_BF16/KVC_F16, head_dim in {64, 128}, q_heads / kv_heads <= 16.
+ * KVC_BF16/KVC_F16, head_dim in {64, 128, 256}, q_heads / kv_heads <= 16.
  * Device errors as kvc_seq_lengths / kvc_window_append / kvc_gqa_decode.
  */
 kvc_status kvc_window_decode_step(void *out, const void *q, void *k_cache, void *v_cache,
@@ -539,8 +546,13 @@ kvc_status kvc_window_decode_step(void *out, const void *q, void *k_cache, void 
                                   kvc_lengths len, int batch, int q_heads, int kv_heads,
                                   int64_t capacity, int head_dim, int dtype, int windowed,
                                   int local_window_size, float scale, const float *rope_cos,
-                                  const float *rope_sin, int64_t rope_max_pos,
-                                  int32_t *dev_status, void *stream);
+                                  const float *rope_sin, int64_t rope_max_pos, void *workspace,
+                                  size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/* Bytes of workspace kvc_window_decode_step needs for these sizes (0 for a
+ * window held on chip, or on bad sizes). */
+size_t kvc_window_decode_step_workspace_size(int batch, int q_heads, int kv_heads,
+                                             int64_t capacity, int head_dim, int dtype);
 
 /*
  * kvc_gqa_prefill_chunk -- attention of an S-token chunk over staged rows

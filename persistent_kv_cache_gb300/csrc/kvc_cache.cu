@@ -286,6 +286,164 @@ compact_kernel(T *__restrict__ k_cache, T *__restrict__ v_cache, const T *__rest
     }
 }
 
+// Windowed S == 1 for large slices, in place, by a thread-block cluster of CL
+// CTAs per (b, head, K/V).  The move is one downward memmove of
+// N = (Lp - E) * row_bytes bytes by S = E * row_bytes.  CTA c owns destination
+// bytes [lo, hi) (a 16-byte multiple Q = ceil(N / CL) each) and reads sources
+// [lo + S, hi + S).  Sources at or above hi are destinations of later CTAs:
+// each CTA copies that part of its sources (min(S, hi - lo) bytes) into
+// shared memory first, then the cluster meets at its hardware barrier; after
+// it no CTA can overwrite bytes another has yet to read, and each CTA streams
+// its own range downwards in ascending pieces (one thread, 1-D bulk copies
+// through a ring of shared-memory slots: a piece's store overwrites only
+// bytes that it or earlier pieces read, and is issued after their loads
+// landed), the saved bytes going out last.  A shift longer than the save
+// buffer (a drifting cache with a large gap) is moved by the cluster's first
+// CTA alone, which is safe by the same ascending order.  The last CTA writes
+// the new row (K rotated at P) at row Lp - E after the barrier, once the
+// bytes it replaces have been saved.
+constexpr int kCompactSlots = 4;
+constexpr int kCompactPiece = 16384;
+constexpr int kCompactSave = 16384;
+constexpr int kCompactSmem = kCompactSlots * kCompactPiece + kCompactSave + 8 * (kCompactSlots + 1) + 128;
+// slices of at least this many bytes take the cluster kernel, one CTA per
+// kCompactClusterBytes of slice (at most 8, the portable cluster size)
+constexpr int64_t kCompactClusterMin = 65536;
+constexpr int64_t kCompactClusterBytes = 262144;
+
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <typename T>
+__global__ void __launch_bounds__(32)
+compact_cluster_kernel(T *__restrict__ k_cache, T *__restrict__ v_cache,
+                       const T *__restrict__ new_k, const T *__restrict__ new_v,
+                       kvc_lengths len, int kv_heads, int D, int64_t C,
+                       const float *__restrict__ cos_t, const float *__restrict__ sin_t,
+                       int64_t rope_max_pos, int32_t *status)
+{
+    extern __shared__ uint8_t compact_smem_raw[];
+    const int CL = (int)gridDim.x;  // the cluster spans blockIdx.x
+    const int c = (int)blockIdx.x;
+    const int slice = blockIdx.y;
+    const int b = slice / kv_heads;
+    const bool is_k = blockIdx.z == 0;
+    const bool lead = c == 0 && is_k && slice % kv_heads == 0 && threadIdx.x == 0;
+    // every CTA of the cluster takes the same early exits (they depend on the
+    // batch row only), so none is left waiting at the barrier below
+    const int L = len.cache_total[b];
+    if (L < 0)
+        return;
+    const int P = len.past_abs[b];
+    if (cos_t != nullptr && (int64_t)P + 1 > rope_max_pos) {
+        if (lead)
+            kvc::raise_status(status, KVC_DEV_ROPE_RANGE);
+        return;
+    }
+    const int Lp = len.cache_past[b];
+    const int E = len.evict[b];
+    if (Lp < 0 || Lp > C || E < 0 || E > Lp || Lp - E + 1 > C) {
+        if (lead)
+            kvc::raise_status(status, KVC_DEV_CAPACITY);
+        return;
+    }
+    uint8_t *ring = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(compact_smem_raw) + 127) & ~uintptr_t(127));
+    uint8_t *save = ring + kCompactSlots * kCompactPiece;
+    uint64_t *full = reinterpret_cast<uint64_t *>(save + kCompactSave);  // [slots + 1]
+    const int64_t rb = (int64_t)D * sizeof(T);
+    char *base = reinterpret_cast<char *>((is_k ? k_cache : v_cache) + (int64_t)slice * C * D);
+    const int64_t N = (int64_t)(Lp - E) * rb, S = (int64_t)E * rb;
+    // this CTA's destination range; the whole range for the first CTA when
+    // the shift is longer than the save buffer
+    const bool solo = S > kCompactSave;
+    const int64_t Q = ((N + CL - 1) / CL + 15) / 16 * 16;
+    int64_t lo = solo ? (c == 0 ? 0 : N) : (int64_t)c * Q;
+    int64_t hi = solo ? N : lo + Q;
+    lo = lo < N ? lo : N;
+    hi = hi < N ? hi : N;
+    const int64_t keep = solo ? 0 : (S < hi - lo ? S : hi - lo);  // saved source bytes
+    const int64_t n_ring = hi - lo - keep;  // bytes streamed through the ring
+    const int64_t npieces = E > 0 ? (n_ring + kCompactPiece - 1) / kCompactPiece : 0;
+    auto piece_bytes = [&](int64_t p) -> uint32_t {
+        const int64_t rest = n_ring - p * kCompactPiece;
+        return (uint32_t)(rest < kCompactPiece ? rest : kCompactPiece);
+    };
+    auto load = [&](int64_t p) {
+        const int slot = (int)(p % kCompactSlots);
+        kvc::mbar_arrive_expect_tx(&full[slot], piece_bytes(p));
+        kvc::bulk_load(ring + slot * kCompactPiece, base + lo + S + p * kCompactPiece,
+                       piece_bytes(p), &full[slot]);
+    };
+    bool ok = true;
+    int64_t issued = 0;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i <= kCompactSlots; ++i)
+            kvc::mbar_init(&full[i], 1);
+        kvc::fence_mbar_init();
+        if (E > 0 && keep > 0) {
+            kvc::mbar_arrive_expect_tx(&full[kCompactSlots], (uint32_t)keep);
+            kvc::bulk_load(save, base + hi + S - keep, (uint32_t)keep, &full[kCompactSlots]);
+        }
+        // the ring's first loads read this CTA's own range: nothing writes
+        // there before the barrier, so they may start now
+        for (; issued < npieces && issued < kCompactSlots; ++issued)
+            load(issued);
+        if (E > 0 && keep > 0 && !kvc::mbar_wait(&full[kCompactSlots], 0))
+            ok = false;
+    }
+    __syncwarp();
+    cluster_sync_all();
+    if (threadIdx.x == 0) {
+        for (int64_t p = 0; p < npieces; ++p) {
+            const int slot = (int)(p % kCompactSlots);
+            if (!ok || !kvc::mbar_wait(&full[slot], (uint32_t)(p / kCompactSlots) & 1u)) {
+                ok = false;
+                break;
+            }
+            kvc::bulk_store(base + lo + p * kCompactPiece, ring + slot * kCompactPiece,
+                            piece_bytes(p));
+            kvc::tma_store_commit();
+            if (issued < npieces) {
+                kvc::tma_store_wait_read();  // the slot's bytes have left shared memory
+                load(issued++);
+            }
+        }
+        if (ok && keep > 0) {
+            kvc::bulk_store(base + hi - keep, save, (uint32_t)keep);
+            kvc::tma_store_commit();
+        }
+        if (!ok) {
+            // a load that never landed: report it and let the others land
+            kvc::raise_status(status, KVC_DEV_TIMEOUT);
+            for (int64_t p = 0; p < issued; ++p)
+                kvc::mbar_wait(&full[p % kCompactSlots], (uint32_t)(p / kCompactSlots) & 1u);
+        }
+        kvc::tma_store_wait_all();
+    }
+    __syncwarp();
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    // the new row, by the last CTA: its old bytes were saved (or, when the
+    // first CTA moved everything alone, read by it) before they are replaced
+    const int writer = solo ? 0 : CL - 1;
+    if (c != writer || !ok)
+        return;
+    const bool rotate = is_k && cos_t != nullptr;
+    T *dst = reinterpret_cast<T *>(base) + (int64_t)(Lp - E) * D;
+    const T *src = (is_k ? new_k : new_v) + (int64_t)slice * D;
+    for (int j = threadIdx.x; j < D / 2; j += 32) {
+        float lo_v = kvc::Elem<T>::to_f32(src[j]), hi_v = kvc::Elem<T>::to_f32(src[j + D / 2]);
+        if (rotate)
+            kvc::rope_pair(lo_v, hi_v, cos_t[(int64_t)P * (D / 2) + j],
+                           sin_t[(int64_t)P * (D / 2) + j]);
+        dst[j] = kvc::Elem<T>::from_f32(lo_v);
+        dst[j + D / 2] = kvc::Elem<T>::from_f32(hi_v);
+    }
+}
+
 // In-place move of rows [E, E + L) of a (b, head) slice to rows [0, L): the
 // copy-back of kvc_window_append_inplace.  One CTA per (b, head, K/V); its
 // first thread streams the slice's contiguous byte range through a ring of
@@ -497,12 +655,37 @@ kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const v
     } else if (S == 1) {
         if (phase != KVC_APPEND)
             return KVC_ERR_UNSUPPORTED;
-        dim3 grid(slices, 2);
-        if (vec_ok && (D * sizeof(T)) % 16 == 0)
-            compact_kernel<T, VEC><<<grid, 256, 0, stream>>>(kc, vc, nk, nv, len, kv_heads, D, C,
-                                                             cos_t, sin_t, rope_max_pos, status);
-        else
+        if (!vec_ok || (D * sizeof(T)) % 16 != 0)
             return KVC_ERR_UNSUPPORTED;
+        const int64_t slice_bytes = C * D * (int64_t)sizeof(T);
+        if (slice_bytes < kCompactClusterMin) {
+            // small slices: one CTA per (b, head, K/V), register tiles
+            compact_kernel<T, VEC><<<dim3(slices, 2), 256, 0, stream>>>(
+                kc, vc, nk, nv, len, kv_heads, D, C, cos_t, sin_t, rope_max_pos, status);
+        } else {
+            // large slices: a cluster of up to 8 CTAs per (b, head, K/V)
+            int cl = (int)((slice_bytes + kCompactClusterBytes - 1) / kCompactClusterBytes);
+            cl = cl < 1 ? 1 : (cl > 8 ? 8 : cl);
+            auto kern = compact_cluster_kernel<T>;
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kCompactSmem) != cudaSuccess)
+                return KVC_ERR_CUDA;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(cl, slices, 2);
+            cfg.blockDim = dim3(32);
+            cfg.dynamicSmemBytes = kCompactSmem;
+            cfg.stream = stream;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = cl;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaLaunchKernelEx(&cfg, kern, kc, vc, nk, nv, len, kv_heads, D, C, cos_t, sin_t,
+                                   rope_max_pos, status) != cudaSuccess)
+                return KVC_ERR_CUDA;
+        }
     } else if (phase == KVC_APPEND) {
         launch_copy(static_cast<char *>(k_stage), static_cast<char *>(v_stage),
                     reinterpret_cast<const char *>(kc), reinterpret_cast<const char *>(vc), C + S,

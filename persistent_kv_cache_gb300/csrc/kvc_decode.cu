@@ -559,13 +559,26 @@ template <int D, int MODE> __host__ __device__ constexpr int decode_slot_bytes()
 {
     return decode_uses_slots<D, MODE>() ? kTile * D * 2 : 2 * kTile * D * 2;
 }
+// At head_dim 256 the output accumulator alone takes 128 registers a
+// thread: the split kernel then runs without a producer warp (four consumer
+// warps, two CTAs an SM, so that a thread may hold up to 255 registers), and
+// the warp that releases a ring slot last issues that slot's next load.
+template <int D, int MODE> __host__ __device__ constexpr bool decode_no_producer()
+{
+    return D >= 256 && MODE != kPagedQ;
+}
+template <int D, int MODE> __host__ __device__ constexpr int decode_threads()
+{
+    return decode_no_producer<D, MODE>() ? 128 : 160;
+}
 // bytes after the 1024-byte alignment pad: ring, staged query rows [16][D + 8],
-// full/empty barriers, abort flag (+pad), the split's page ids [32], and the
-// fused step's new K and V row
+// full/empty barriers, abort flag (+pad), the split's page ids [32], the
+// fused step's new K and V row, and the slots' release counters
 template <int D, int MODE> __host__ __device__ constexpr int decode_smem_bytes()
 {
     return decode_ring_slots<D, MODE>() * decode_slot_bytes<D, MODE>() + 16 * (D + 8) * 2 +
-           2 * decode_ring_slots<D, MODE>() * 8 + 16 + 32 * 4 + 2 * D * 2;
+           2 * decode_ring_slots<D, MODE>() * 8 + 16 + 32 * 4 + 2 * D * 2 +
+           4 * decode_ring_slots<D, MODE>();
 }
 
 // One CTA per (split, kv head, batch row) for kvc_gqa_decode,
@@ -580,11 +593,13 @@ template <int D, int MODE> __host__ __device__ constexpr int decode_smem_bytes()
 // shared memory lets share an SM can hold -- two at head_dim 128 and 256,
 // three at 64)
 template <typename T, int D, int MODE>
-__global__ void __launch_bounds__(160, (MODE == kPagedQ || D >= 256) ? (D >= 128 ? 2 : 3) : 0)
+__global__ void __launch_bounds__(decode_threads<D, MODE>(),
+                                  (MODE == kPagedQ || D >= 256) ? (D >= 128 ? 2 : 3) : 0)
 decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a)
 {
     constexpr bool SLOTS = decode_uses_slots<D, MODE>();
+    constexpr bool NOPROD = decode_no_producer<D, MODE>();
     constexpr int NBAR = decode_ring_slots<D, MODE>();
     constexpr int SLOT_BYTES = decode_slot_bytes<D, MODE>();
     constexpr int BOXES = D / 64;
@@ -602,6 +617,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     int *page_ids = abort_flag + 4;  // [32] paged: the split's pages
     // kFused: the new row, K rotated at its position then V ([2][D])
     T *newrow = reinterpret_cast<T *>(page_ids + 32);
+    // NOPROD: how many warps have released each slot in its current round
+    int *released = reinterpret_cast<int *>(newrow + 2 * D);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -640,13 +657,76 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         for (int s = 0; s < NBAR; ++s) {
             kvc::mbar_init(&full[s], 1);
             kvc::mbar_init(&empty[s], kConsumers);
+            released[s] = 0;
         }
         *abort_flag = 0;
         kvc::fence_mbar_init();
     }
+    if constexpr (MODE >= kPaged && NOPROD) {
+        // the pages this split touches, one lane of the first warp each
+        if (warp == 0) {
+            const int page0 = q0 / a.page_size;
+            const int npages = (q0 + cnt - 1) / a.page_size - page0 + 1;
+            if (lane < npages) {
+                int id = a.block_table[(int64_t)b * a.max_pages + page0 + lane];
+                if (id < 0 || (int64_t)id >= a.n_pool_pages) {
+                    kvc::raise_status(a.status, KVC_DEV_INDEX_OOB);
+                    id = 0;  // read a page that exists; the row's result is void
+                }
+                page_ids[lane] = id;
+            }
+        }
+    }
     __syncthreads();
 
-    if (warp == kConsumers) {
+    // NOPROD: load j of the split fills slot j % NBAR: K (j even) or V (j odd)
+    // of tile j / 2; the first NBAR are issued here, each later one by the
+    // warp that releases its slot last
+    const int n_loads = 2 * ntiles;
+    auto issue_load = [&](int j) {
+        const int t = j >> 1;
+        int32_t y;
+        if constexpr (MODE >= kPaged) {
+            const int r = q0 + t * kTile;  // logical row, a multiple of 64
+            const int id = page_ids[r / a.page_size - q0 / a.page_size];
+            y = (int32_t)(((int64_t)id * a.kv_heads + kvh) * a.page_size + r % a.page_size);
+        } else {
+            y = (int32_t)(row_base + tile_start(t));
+        }
+        const int sl = j % NBAR;
+        uint8_t *dst = stages + sl * SLOT_BYTES;
+        const CUtensorMap *map = (j & 1) ? &tmap_v : &tmap_k;
+        kvc::mbar_arrive_expect_tx(&full[sl], KT_BYTES);
+#pragma unroll
+        for (int bx = 0; bx < BOXES; ++bx)
+            kvc::tma_load_2d(dst + bx * 8192, map, bx * 64, y, &full[sl]);
+    };
+    if constexpr (NOPROD) {
+        if (threadIdx.x == 0) {
+            kvc::tma_prefetch_desc(&tmap_k);
+            kvc::tma_prefetch_desc(&tmap_v);
+            for (int j = 0; j < NBAR && j < n_loads; ++j)
+                issue_load(j);
+        }
+    }
+    // NOPROD: this warp is done with load j's slot; the last of the four to
+    // say so issues load j + NBAR into it (the fences order every warp's use
+    // of the slot, and any bytes it wrote there, before the copy overwrites it)
+    auto release_slot = [&](int j) {
+        if (lane == 0) {
+            const int sl = j % NBAR;
+            __threadfence_block();
+            if (atomicAdd(&released[sl], 1) == kConsumers - 1) {
+                released[sl] = 0;
+                __threadfence_block();
+                kvc::fence_proxy_async_smem();
+                if (j + NBAR < n_loads && !*reinterpret_cast<volatile int *>(abort_flag))
+                    issue_load(j + NBAR);
+            }
+        }
+    };
+
+    if (!NOPROD && warp == kConsumers) {
         // ---------------- producer ----------------
         int page0 = 0;
         if constexpr (MODE >= kPaged) {
@@ -897,7 +977,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         if (wrote)
             kvc::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
+        if constexpr (NOPROD) {
+            release_slot(pos);
+            release_slot(pos + 1);
+        } else if (lane == 0) {
             kvc::mbar_arrive(&empty[s0]);
             if (SLOTS && !q8)
                 kvc::mbar_arrive(&empty[s1]);
@@ -1087,8 +1170,12 @@ struct WindowStepArgs {
 };
 
 // largest capacity whose whole window (K and V) the fused step keeps in
-// shared memory
-__host__ __device__ constexpr int64_t window_step_max_capacity(int D) { return 32768 / D; }
+// shared memory: capacity * head_dim at most kWindowStepMaxElems
+constexpr int64_t kWindowStepMaxElems = 32768;
+__host__ __device__ constexpr int64_t window_step_max_capacity(int D)
+{
+    return kWindowStepMaxElems / D;
+}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(128, D >= 256 ? 2 : 4)
@@ -1614,6 +1701,7 @@ kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const 
     const bool q8 = px && px->qk_pool;
     const size_t smem = 1024 + (size_t)(q8 ? decode_smem_bytes<D, kPagedQ>()
                                            : decode_smem_bytes<D, kPlain>());
+    const int threads = q8 ? decode_threads<D, kPagedQ>() : decode_threads<D, kPlain>();
     auto kern = fx                 ? decode_split_kernel<T, D, kFused>
                 : px && px->qk_pool ? decode_split_kernel<T, D, kPagedQ>
                 : px               ? decode_split_kernel<T, D, kPaged>
@@ -1622,7 +1710,7 @@ kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const 
         cudaSuccess)
         return KVC_ERR_CUDA;
     const dim3 grid(a.max_splits, kv_heads, batch);
-    kern<<<grid, 160, smem, stream>>>(tk, tv, a);
+    kern<<<grid, threads, smem, stream>>>(tk, tv, a);
     if (a.max_splits > 1) {
         dim3 g2(q_heads, batch);
         const size_t cs = 3 * a.max_splits * sizeof(float);
@@ -1993,6 +2081,25 @@ kvc_status launch_window_step(const WindowStepArgs &a, int batch, cudaStream_t s
 
 } // namespace
 
+namespace {
+
+// the large-window step's workspace: the five length arrays (when the caller
+// passes none), then the decode's split partials, each 256-byte aligned
+inline size_t window_step_len_bytes(int batch) { return ((size_t)5 * batch * 4 + 255) / 256 * 256; }
+
+} // namespace
+
+KVC_API size_t kvc_window_decode_step_workspace_size(int batch, int q_heads, int kv_heads,
+                                                     int64_t capacity, int head_dim, int dtype)
+{
+    if (batch < 0 || q_heads < 1 || kv_heads < 1 || capacity < 1 || head_dim < 1)
+        return 0;
+    if (capacity * head_dim <= kWindowStepMaxElems)
+        return 0;  // the one-launch step keeps everything on chip
+    return window_step_len_bytes(batch) +
+           kvc_gqa_decode_workspace_size(batch, q_heads, kv_heads, capacity, head_dim, dtype);
+}
+
 KVC_API kvc_status kvc_window_decode_step(void *out, const void *q, void *k_cache, void *v_cache,
                                           const void *new_k, const void *new_v,
                                           const int32_t *seqlens_k, kvc_lengths len, int batch,
@@ -2000,7 +2107,8 @@ KVC_API kvc_status kvc_window_decode_step(void *out, const void *q, void *k_cach
                                           int head_dim, int dtype, int windowed,
                                           int local_window_size, float scale,
                                           const float *rope_cos, const float *rope_sin,
-                                          int64_t rope_max_pos, int32_t *dev_status,
+                                          int64_t rope_max_pos, void *workspace,
+                                          size_t workspace_bytes, int32_t *dev_status,
                                           void *stream)
 {
     if (kvc_host::elem_bytes_of(dtype) == 0)
@@ -2018,15 +2126,51 @@ KVC_API kvc_status kvc_window_decode_step(void *out, const void *q, void *k_cach
     if (rope_cos && rope_max_pos < 1)
         return KVC_ERR_SHAPE;
     const int g = q_heads / kv_heads;
-    if (dtype == KVC_F32 || !dim16_ok(head_dim) || g > 16 ||
-        capacity > window_step_max_capacity(head_dim))
+    if (dtype == KVC_F32 || !dim16_ok(head_dim) || g > 16)
         return KVC_ERR_UNSUPPORTED;
     const bool some_len = len.past_abs || len.total_abs || len.cache_past || len.cache_total ||
                           len.evict;
     if (some_len && !kvc_host::lengths_ok(len))
         return KVC_ERR_NULL;
+    const bool large = capacity > window_step_max_capacity(head_dim);
+    if (large && windowed == KVC_RING && decode_max_splits(capacity) > 128)
+        return KVC_ERR_UNSUPPORTED;
     if (batch == 0)
         return KVC_OK;
+    if (large) {
+        // A window too large to hold on chip: the ring runs as the fused
+        // split step (nothing moves); a windowed or drifting cache runs
+        // lengths, the in-place compaction + append, and the split decode.
+        const size_t need = kvc_window_decode_step_workspace_size(batch, q_heads, kv_heads,
+                                                                  capacity, head_dim, dtype);
+        if (!workspace || workspace_bytes < need)
+            return KVC_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+            return KVC_ERR_ALIGN;
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
+        const size_t lb = window_step_len_bytes(batch);
+        if (windowed == KVC_RING)
+            return kvc_decode_step(out, q, k_cache, v_cache, new_k, new_v, seqlens_k, len, batch,
+                                   q_heads, kv_heads, capacity, head_dim, dtype, KVC_RING,
+                                   local_window_size, scale, rope_cos, rope_sin, rope_max_pos,
+                                   ws + lb, workspace_bytes - lb, dev_status, stream);
+        kvc_lengths l = len;
+        if (!some_len) {
+            int32_t *w32 = reinterpret_cast<int32_t *>(ws);
+            l = kvc_lengths{w32, w32 + batch, w32 + 2 * batch, w32 + 3 * batch, w32 + 4 * batch};
+        }
+        kvc_status st = kvc_seq_lengths(seqlens_k, batch, 1, capacity, windowed,
+                                        local_window_size, l, dev_status, stream);
+        if (st == KVC_OK)
+            st = kvc_window_append(k_cache, v_cache, new_k, new_v, nullptr, nullptr, l, batch,
+                                   kv_heads, 1, capacity, head_dim, dtype, windowed, KVC_APPEND,
+                                   rope_cos, rope_sin, rope_max_pos, dev_status, stream);
+        if (st == KVC_OK)
+            st = kvc_gqa_decode(out, q, k_cache, v_cache, l, batch, q_heads, kv_heads, capacity,
+                                head_dim, dtype, local_window_size, scale, rope_cos, rope_sin,
+                                rope_max_pos, ws + lb, workspace_bytes - lb, dev_status, stream);
+        return st;
+    }
     if (!out || !q || !k_cache || !v_cache || !new_k || !new_v || !seqlens_k)
         return KVC_ERR_NULL;
     for (const void *p : {(const void *)out, q, (const void *)k_cache, (const void *)v_cache, new_k,

@@ -35,6 +35,7 @@ KVC_DEV_TIMEOUT = 16
 EXPORTS = ("kvc_tensor_scatter", "kvc_seq_lengths", "kvc_window_append", "kvc_gqa_decode",
            "kvc_gqa_decode_workspace_size", "kvc_gqa_decode_noalloc", "kvc_gqa_decode_ring",
            "kvc_decode_step", "kvc_decode_step_workspace_size", "kvc_window_decode_step",
+           "kvc_window_decode_step_workspace_size",
            "kvc_paged_append", "kvc_gqa_decode_paged", "kvc_window_append_inplace",
            "kvc_quantize_pages", "kvc_gqa_decode_paged_q",
            "kvc_gqa_prefill_chunk", "kvc_gqa_prefill_workspace_size", "kvc_status_string",
@@ -113,7 +114,8 @@ def library() -> ctypes.CDLL:
             "kvc_decode_step_workspace_size": [I, I, I, I64, I, I],
             "kvc_gqa_decode_noalloc": [P, P, P, P, L, I, I, I, I64, I, I, I, F, P, P, I64, P, P],
             "kvc_window_decode_step": [P, P, P, P, P, P, P, L, I, I, I, I64, I, I, I, I, F, P, P,
-                                       I64, P, P],
+                                       I64, P, SZ, P, P],
+            "kvc_window_decode_step_workspace_size": [I, I, I, I64, I, I],
             "kvc_gqa_prefill_chunk": [P, P, P, P, I64, L, I, I, I, I, I, I, I, F, P, P, I64, P, SZ,
                                       P, P],
             "kvc_gqa_prefill_workspace_size": [I, I, I, I, I64, I, I, I],
@@ -126,6 +128,7 @@ def library() -> ctypes.CDLL:
             fn.restype = I
         lib.kvc_gqa_decode_workspace_size.restype = SZ
         lib.kvc_decode_step_workspace_size.restype = SZ
+        lib.kvc_window_decode_step_workspace_size.restype = SZ
         lib.kvc_gqa_prefill_workspace_size.restype = SZ
         lib.kvc_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -357,20 +360,32 @@ def kvc_decode_step(out, q, k_cache, v_cache, new_k, new_v, seqlens_k, local_win
     return out
 
 
+def window_step_workspace(q, k_cache):
+    """Workspace for kvc_window_decode_step (None for a window held on chip)."""
+    B, Hq, _, D = q.shape
+    n = library().kvc_window_decode_step_workspace_size(B, Hq, k_cache.shape[1],
+                                                        k_cache.shape[2], D, _dtype_code(q))
+    return torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+
+
 def kvc_window_decode_step(out, q, k_cache, v_cache, new_k, new_v, seqlens_k, local_window_size,
                            lengths=None, scale=0.0, rope=None, status=None, stream=None,
-                           windowed=None):
-    """Fused lengths + windowed one-token append + GQA decode (include/kvc.h).
-    ``windowed``: KVC_WINDOWED (default), KVC_DRIFTING or KVC_RING."""
+                           windowed=None, workspace="auto"):
+    """Lengths + windowed one-token append + GQA decode (include/kvc.h).
+    ``windowed``: KVC_WINDOWED (default), KVC_DRIFTING or KVC_RING;
+    ``workspace``: "auto" allocates what the call needs (large windows only)."""
     windowed = KVC_WINDOWED if windowed is None else int(windowed)
     B, Hq, _, D = q.shape
     _, Hkv, C, _ = k_cache.shape
+    if isinstance(workspace, str):
+        workspace = window_step_workspace(q, k_cache)
     cs, sn, rmax = _rope(rope)
     lc = lengths.c() if lengths is not None else KvcLengths(None, None, None, None, None)
     _check("kvc_window_decode_step", library().kvc_window_decode_step(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(new_k), _ptr(new_v),
         _ptr(seqlens_k), lc, B, Hq, Hkv, C, D, _dtype_code(q), windowed, local_window_size,
-        scale, cs, sn, rmax, _ptr(status), _stream(stream)))
+        scale, cs, sn, rmax, _ptr(workspace), 0 if workspace is None else workspace.numel(),
+        _ptr(status), _stream(stream)))
     return out
 
 

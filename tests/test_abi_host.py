@@ -45,7 +45,7 @@ def test_binding_rejects_host_tensors(kvc):
 
 
 def test_version_and_strings(kvc):
-    assert kvc.kvc_abi_version() == 5
+    assert kvc.kvc_abi_version() == 6
     assert kvc.kvc_status_string(0) == "ok"
     assert "window" in kvc.kvc_status_string(7)
 
@@ -213,18 +213,30 @@ def test_binding_requires_library(monkeypatch, kvc):
 def test_window_step_host_checks(kvc):
     lib = kvc.library()
     f = lib.kvc_window_decode_step
+    wsz = lib.kvc_window_decode_step_workspace_size
     none = kvc.KvcLengths(None, None, None, None, None)
     base = [FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, FAKE * 7]
+    nows = [None, 0, None, None]   # workspace, bytes, dev_status, stream
     for pol in (1, 2):
-        assert f(*base, none, 2, 8, 2, 128, 64, 1, pol, 129, 0.0, None, None, 0, None, None) == 7
-        assert f(*base, none, 2, 8, 2, 128, 64, 1, pol, 0, 0.0, None, None, 0, None, None) == 7
-    assert f(*base, none, 2, 8, 2, 128, 64, 1, 0, 128, 0.0, None, None, 0, None, None) == 5  # contig
-    assert f(*base, none, 2, 8, 2, 128, 64, 1, 4, 128, 0.0, None, None, 0, None, None) == 5  # policy
-    assert f(*base, none, 2, 8, 2, 128, 64, 0, 1, 128, 0.0, None, None, 0, None, None) == 5  # fp32
-    assert f(*base, none, 2, 8, 2, 128, 96, 1, 1, 128, 0.0, None, None, 0, None, None) == 5  # D
+        assert f(*base, none, 2, 8, 2, 128, 64, 1, pol, 129, 0.0, None, None, 0, *nows) == 7
+        assert f(*base, none, 2, 8, 2, 128, 64, 1, pol, 0, 0.0, None, None, 0, *nows) == 7
+    assert f(*base, none, 2, 8, 2, 128, 64, 1, 0, 128, 0.0, None, None, 0, *nows) == 5  # contig
+    assert f(*base, none, 2, 8, 2, 128, 64, 1, 4, 128, 0.0, None, None, 0, *nows) == 5  # policy
+    assert f(*base, none, 2, 8, 2, 128, 64, 0, 1, 128, 0.0, None, None, 0, *nows) == 5  # fp32
+    assert f(*base, none, 2, 8, 2, 128, 96, 1, 1, 128, 0.0, None, None, 0, *nows) == 5  # D
     half = kvc.KvcLengths(FAKE, None, None, None, None)
-    assert f(*base, half, 2, 8, 2, 128, 64, 1, 2, 128, 0.0, None, None, 0, None, None) == 1
-    assert f(*base, none, 0, 8, 2, 128, 64, 1, 2, 128, 0.0, None, None, 0, None, None) == 0
+    assert f(*base, half, 2, 8, 2, 128, 64, 1, 2, 128, 0.0, None, None, 0, *nows) == 1
+    assert f(*base, none, 0, 8, 2, 128, 64, 1, 2, 128, 0.0, None, None, 0, *nows) == 0
+    # a window held on chip needs no workspace; a larger one needs the
+    # lengths (5 x batch int32, 256-byte rounded) and the split partials
+    assert wsz(2, 8, 2, 512, 64, 1) == 0 and wsz(2, 8, 2, 128, 256, 1) == 0
+    assert wsz(2, 8, 2, 1024, 64, 1) == 256 + 256
+    assert wsz(8, 16, 8, 4096, 256, 1) == 256 + 8 * 16 * 8 * (256 + 2) * 4
+    for pol in (1, 2, 3):
+        assert f(*base, none, 8, 16, 8, 4096, 256, 1, pol, 4096, 0.0, None, None, 0,
+                 *nows) == 8
+        assert f(*base, none, 8, 16, 8, 4096, 256, 1, pol, 4096, 0.0, None, None, 0,
+                 FAKE + 16, 1 << 24, None, None) == 4
 
 
 def test_append_inplace_host_checks(kvc):

@@ -157,3 +157,57 @@ def test_fused_step_head_dim_256(K, orc, ring):
         assert_bytes_equal(gv, wv, f"v cache step {s}")
         assert_close(out, want, 2e-2, f"{'ring' if ring else 'contiguous'} step {s}")
     assert st.item() == 0
+
+
+@pytest.mark.parametrize("policy,D,g,C,W,own_len", [
+    (1, 256, 2, 4096, 4096, True),     # the windowed-prefill workload's cache, compact every step
+    (2, 256, 2, 4160, 4096, False),    # drifting, 65-row blocks
+    (3, 256, 2, 4096, 4096, True),     # ring
+    (1, 128, 4, 1024, 1000, False),
+    (2, 64, 8, 2048, 2000, True),
+])
+def test_large_window_step(K, orc, policy, D, g, C, W, own_len):
+    """kvc_window_decode_step above the on-chip limit (capacity * head_dim >
+    32768): lengths, compaction and split decode for a windowed or drifting
+    cache, the fused split step for a ring; lengths kept by the caller or in
+    the call's workspace."""
+    B, Hkv = 6, 2
+    Hq = Hkv * g
+    seed = 500 + policy + D
+    T0 = np.array([1, C - 2, C, C + 1, 9000, 20000], dtype=np.int64)
+    steps = 4 if policy != 2 else C - W + 3   # a drifting run passes a compaction
+    steps = min(steps, 8)
+    cos, sin = synth.rope_cache(int(T0.max()) + steps + 1, D)
+    rope_d = (cos.to(dev()), sin.to(dev()))
+    cn, sn = cos.numpy(), sin.numpy()
+    kc = synth.normal((B, Hkv, C, D), seed, 1)
+    vc = synth.normal((B, Hkv, C, D), seed, 2)
+    wk, wv = synth.bits(kc).copy(), synth.bits(vc).copy()
+    gk, gv = kc.to(dev()), vc.to(dev())
+    st = status()
+    Lg = K.Lengths(B, dev()) if own_len else None
+    out = torch.full((B, Hq, 1, D), float("nan"), dtype=torch.bfloat16, device=dev())
+    for s in range(steps):
+        T = T0 + s
+        sk = (T - 1).astype(np.int32)
+        nk = synth.normal((B, Hkv, 1, D), seed, 10 + s)
+        nv = synth.normal((B, Hkv, 1, D), seed, 20 + s)
+        q = synth.normal((B, Hq, 1, D), seed, 30 + s)
+        K.kvc_window_decode_step(out, q.to(dev()), gk, gv, nk.to(dev()), nv.to(dev()),
+                                 torch.from_numpy(sk).to(dev()), W, lengths=Lg, rope=rope_d,
+                                 status=st, windowed=policy)
+        lens = orc.seq_lengths(sk, 1, C, policy, W)
+        if policy == 3:
+            orc.ring_append(wk, wv, synth.bits(nk), synth.bits(nv), T - 1, cn, sn)
+            want, _ = orc.ring_attention(synth.bits(q), wk, wv, T, W, cos_cache=cn, sin_cache=sn)
+        else:
+            orc.window_append(wk, wv, synth.bits(nk), synth.bits(nv), lens, policy, cn, sn)
+            want, _ = orc.gqa_attention(synth.bits(q), wk, wv, lens["cache_total"],
+                                        lens["total_abs"], window=W, cos_cache=cn, sin_cache=sn)
+        torch.cuda.synchronize()
+        if Lg is not None:
+            _check_lengths(Lg, lens, f"step {s}")
+        assert_bytes_equal(gk, wk, f"k cache step {s}")
+        assert_bytes_equal(gv, wv, f"v cache step {s}")
+        assert_close(out, want, 2e-2, f"policy {policy} step {s}")
+    assert st.item() == 0
