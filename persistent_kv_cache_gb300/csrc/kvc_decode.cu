@@ -44,15 +44,16 @@ __host__ __device__ constexpr int decode_stages(int D) { return D >= 128 ? 3 : 4
 
 // rows handled by one CTA (a multiple of the tile); shared by the kernel launch
 // and the workspace size so both agree
-inline int64_t decode_split_rows(int64_t C)
+constexpr int64_t kSplitRowsD256 = 512;
+inline int64_t decode_split_rows(int64_t C, int D)
 {
     if (C >= 2048)
-        return 512;
+        return D >= 256 ? kSplitRowsD256 : 512;
     return (C + kTile - 1) / kTile * kTile;
 }
-inline int64_t decode_max_splits(int64_t C)
+inline int64_t decode_max_splits(int64_t C, int D)
 {
-    const int64_t sr = decode_split_rows(C);
+    const int64_t sr = decode_split_rows(C, D);
     return (C + sr - 1) / sr;
 }
 
@@ -1667,7 +1668,7 @@ kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const 
     a.cos_t = cos_t;
     a.sin_t = sin_t;
     a.rope_max_pos = rope_max_pos;
-    a.split_rows = decode_split_rows(C);
+    a.split_rows = decode_split_rows(C, D);
     // int8 pages: twice the rows per split (the same bytes per CTA as a
     // 16-bit split; fewer CTAs, so less of their fixed start and merge cost)
     if (px && px->qk_pool && C >= 4096)
@@ -1768,7 +1769,7 @@ KVC_API size_t kvc_gqa_decode_workspace_size(int batch, int q_heads, int kv_head
         return 0;
     if (dtype == KVC_F32)
         return 256;  // the CUDA-core path keeps everything on chip
-    const int64_t ns = decode_max_splits(capacity);
+    const int64_t ns = decode_max_splits(capacity, head_dim);
     if (ns <= 1)
         return 256;
     const int64_t np = (int64_t)batch * q_heads * ns;
@@ -1999,7 +2000,8 @@ KVC_API kvc_status kvc_decode_step(void *out, const void *q, void *k_cache, void
     const int g = q_heads / kv_heads;
     // the merge keeps 3 x 16 x splits floats next to the 4-warp partials in
     // the stage buffers: at most 128 splits (capacity 65536)
-    if (dtype == KVC_F32 || !dim16_ok(head_dim) || g > 16 || decode_max_splits(capacity) > 128)
+    if (dtype == KVC_F32 || !dim16_ok(head_dim) || g > 16 ||
+        decode_max_splits(capacity, head_dim) > 128)
         return KVC_ERR_UNSUPPORTED;
     const bool some_len = len.past_abs || len.total_abs || len.cache_past || len.cache_total ||
                           len.evict;
@@ -2133,7 +2135,7 @@ KVC_API kvc_status kvc_window_decode_step(void *out, const void *q, void *k_cach
     if (some_len && !kvc_host::lengths_ok(len))
         return KVC_ERR_NULL;
     const bool large = capacity > window_step_max_capacity(head_dim);
-    if (large && windowed == KVC_RING && decode_max_splits(capacity) > 128)
+    if (large && windowed == KVC_RING && decode_max_splits(capacity, head_dim) > 128)
         return KVC_ERR_UNSUPPORTED;
     if (batch == 0)
         return KVC_OK;

@@ -150,14 +150,14 @@ def test_windowed_cache_decode(K, orc):
 
 def test_contiguous_workload_full_size(K, orc):
     """32 x 32/8 heads x 128, capacity 8192, T ~ U[512, 8192] (bf16); the
-    appended row of every (b, head) and the attention of six batch rows are
-    checked against the oracle; every other cache byte must be unchanged."""
+    appended row of every (b, head) and the attention of every batch row and
+    head are checked against the oracle; every other cache byte must be
+    unchanged."""
     w = synth.CONTIG_DECODE
     T = synth.randint(w.total_lo, w.total_hi + 1, (w.batch,), 0, 77).numpy()
     T[0], T[1] = w.total_lo, w.total_hi
     err = _decode_case(K, orc, torch.bfloat16, w.batch, w.q_heads, w.kv_heads, w.head_dim,
-                       w.capacity, T, 0, 0, True, 40, check_rows=[0, 1, 5, 12, 23, 31],
-                       untouched_check=True)
+                       w.capacity, T, 0, 0, True, 40, untouched_check=True)
     assert err < 2e-2
 
 

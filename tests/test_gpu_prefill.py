@@ -213,7 +213,11 @@ def test_window_prefill_workload_full_size(K, orc, S):
     P = synth.randint(w.total_lo, w.total_hi + 1, (w.batch,), 0, S).numpy()
     P[0], P[1] = 0, w.capacity - S // 2  # from zero, and a chunk that starts evicting
     rng = np.random.default_rng(S)
-    sample = sorted({0, S - 1, S // 2, *rng.integers(0, S, size=3).tolist()})
+    # the chunk's ends and middle, the edges of the 64-query blocks (the
+    # group of two heads fills the 128-row tile with 64 queries) and three
+    # queries at random
+    edges = {0, 63, 64, 127, 128, S // 2 - 1, S // 2, S - 1}
+    sample = sorted({i for i in edges if i < S} | set(rng.integers(0, S, size=3).tolist()))
     err = _chunk_case(K, orc, torch.bfloat16, w.batch, w.q_heads, w.kv_heads, w.head_dim,
                       w.capacity, S, P, w.window, 1, True, 600 + S, sample=sample)
     assert err <= 2e-2

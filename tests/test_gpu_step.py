@@ -79,7 +79,7 @@ def test_contiguous_workload_full_size(K, orc):
     assert st.item() == 0
     assert torch.equal(gk, k2) and torch.equal(gv, v2)
     assert (out.float() - o2.float()).abs().max().item() <= 2e-2
-    rows = [0, 1, 2, 17, 31]
+    rows = list(range(B))   # every batch row and head
     wk, wv = synth.bits(kc).copy(), synth.bits(vc).copy()
     lens, want = _oracle_step(orc, False, wk, wv, nk, nv, q, T, C, 0, cos.numpy(), sin.numpy(),
                               rows)
