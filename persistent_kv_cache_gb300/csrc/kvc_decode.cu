@@ -44,7 +44,7 @@ __host__ __device__ constexpr int decode_stages(int D) { return D >= 128 ? 3 : 4
 
 // rows handled by one CTA (a multiple of the tile); shared by the kernel launch
 // and the workspace size so both agree
-constexpr int64_t kSplitRowsD256 = 512;
+constexpr int64_t kSplitRowsD256 = 1024;
 inline int64_t decode_split_rows(int64_t C, int D)
 {
     if (C >= 2048)
@@ -123,12 +123,13 @@ __device__ __forceinline__ void s8x4_minus(uint32_t w, float off, float (&f)[4])
 // group's query heads are the M = 16 rows of mma.sync m16n8k16, the warp
 // owns rows [16 w, 16 w + 16) of every tile, and (m, l, o) follow the online
 // softmax in the log2 domain.  Thread t holds heads t/4 and t/4 + 8.
-template <typename T, int D> struct GroupAttn {
+template <typename T, int D, bool QREG_ = (D <= 128), bool SHORTCUTS = false>
+struct GroupAttn {
     static constexpr int NB = D / 8;  // 8-column blocks of the output
     // the query's A fragments stay in registers up to head_dim 128; at 256
     // the output alone takes 128 registers a thread, so the fragments are
     // read from the staged rows (one ldmatrix per 16 columns) instead
-    static constexpr bool QREG = D <= 128;
+    static constexpr bool QREG = QREG_;
     uint32_t qa[QREG ? D / 16 : 1][4];
     uint32_t q_addr;  // !QREG: this lane's ldmatrix row address in the staged rows
     float o[NB][4];
@@ -178,6 +179,25 @@ template <typename T, int D> struct GroupAttn {
         }
     }
 
+    // o *= alpha per head row.  SHORTCUTS (the split kernel): skipped when
+    // every factor of the warp is exactly 1 (the running max did not move),
+    // which leaves o bit for bit as the multiplication would, and the key
+    // mask is skipped on tiles whose 16 keys are all visible -- fewer
+    // instructions where the consumer warps' work is the limit; the
+    // latency-bound window step measured faster without them
+    __device__ __forceinline__ void rescale(float al_lo, float al_hi)
+    {
+        if (SHORTCUTS && !__any_sync(0xffffffffu, al_lo != 1.f || al_hi != 1.f))
+            return;
+#pragma unroll
+        for (int n = 0; n < NB; ++n) {
+            o[n][0] *= al_lo;
+            o[n][1] *= al_lo;
+            o[n][2] *= al_hi;
+            o[n][3] *= al_hi;
+        }
+    }
+
     // Online-softmax update with raw scores sc of this warp's 16 keys (the
     // same steps as in tile()): mask keys outside [lo, hi), raise m, rescale
     // l and o, and pack P (times vscale) as the A fragment of the PV MMAs.
@@ -185,13 +205,15 @@ template <typename T, int D> struct GroupAttn {
                                                  float scale_log2, float vscale, uint32_t (&pa)[4])
     {
         float mx_lo = -INFINITY, mx_hi = -INFINITY;
+        const bool whole = SHORTCUTS && lo == 0 && hi == 16;  // every key visible
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int col = 8 * j + 2 * (lane & 3) + (e & 1);
                 float v = sc[j][e] * scale_log2;
-                v = (col >= lo && col < hi) ? v : -INFINITY;
+                if (!whole)
+                    v = (col >= lo && col < hi) ? v : -INFINITY;
                 sc[j][e] = v;
                 if (e < 2)
                     mx_lo = fmaxf(mx_lo, v);
@@ -221,13 +243,7 @@ template <typename T, int D> struct GroupAttn {
         }
         l_lo = l_lo * al_lo + ps_lo;
         l_hi = l_hi * al_hi + ps_hi;
-#pragma unroll
-        for (int n = 0; n < NB; ++n) {
-            o[n][0] *= al_lo;
-            o[n][1] *= al_lo;
-            o[n][2] *= al_hi;
-            o[n][3] *= al_hi;
-        }
+        rescale(al_lo, al_hi);
         pa[0] = Mma<T>::pack(sc[0][0] * vscale, sc[0][1] * vscale);
         pa[1] = Mma<T>::pack(sc[0][2] * vscale, sc[0][3] * vscale);
         pa[2] = Mma<T>::pack(sc[1][0] * vscale, sc[1][1] * vscale);
@@ -245,20 +261,28 @@ template <typename T, int D> struct GroupAttn {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const int cidx = 2 * kk + (mat & 1);
-            uint32_t r_0, r_1, r_2, r_3, a[4];
-            q_frag(kk, a);
+            uint32_t r_0, r_1, r_2, r_3;
             ldsm_x4(kb + (cidx >> 3) * 8192 + kvc::sw128(krow, cidx & 7), r_0, r_1, r_2, r_3);
-            Mma<T>::run(sc[0], a, r_0, r_1);
-            Mma<T>::run(sc[1], a, r_2, r_3);
+            if constexpr (QREG) {
+                Mma<T>::run(sc[0], qa[kk], r_0, r_1);
+                Mma<T>::run(sc[1], qa[kk], r_2, r_3);
+            } else {
+                uint32_t a[4];
+                q_frag(kk, a);
+                Mma<T>::run(sc[0], a, r_0, r_1);
+                Mma<T>::run(sc[1], a, r_2, r_3);
+            }
         }
         float mx_lo = -INFINITY, mx_hi = -INFINITY;
+        const bool whole = SHORTCUTS && lo == 0 && hi == 16;  // every key visible
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int col = 8 * j + 2 * (lane & 3) + (e & 1);
                 float v = sc[j][e] * scale_log2;
-                v = (col >= lo && col < hi) ? v : -INFINITY;
+                if (!whole)
+                    v = (col >= lo && col < hi) ? v : -INFINITY;
                 sc[j][e] = v;
                 if (e < 2)
                     mx_lo = fmaxf(mx_lo, v);
@@ -288,13 +312,7 @@ template <typename T, int D> struct GroupAttn {
         }
         l_lo = l_lo * al_lo + ps_lo;
         l_hi = l_hi * al_hi + ps_hi;
-#pragma unroll
-        for (int n = 0; n < NB; ++n) {
-            o[n][0] *= al_lo;
-            o[n][1] *= al_lo;
-            o[n][2] *= al_hi;
-            o[n][3] *= al_hi;
-        }
+        rescale(al_lo, al_hi);
         uint32_t pa[4];
         pa[0] = Mma<T>::pack(sc[0][0], sc[0][1]);
         pa[1] = Mma<T>::pack(sc[0][2], sc[0][3]);
@@ -403,25 +421,48 @@ template <typename T, int D> struct GroupAttn {
     }
 };
 
-// merged (unnormalised o, l, reference max) of head h, column d over the
-// four warps' published partials
-__device__ __forceinline__ void merge4(const float *cm, const float *cl, const float *co, int D,
-                                       int rows, int h, int d, float &mstar, float &lsum,
-                                       float &osum)
+// merged (unnormalised o, l, reference max) of head h, columns [d, d + 4)
+// over the four warps' published partials (cm/cl [4][16], co [4][rows][D];
+// d a multiple of 4): one round of shared-memory loads, the partials of the
+// four columns read as one float4 per warp
+struct Merged4 {
+    float mstar, lsum, o[4];
+};
+__device__ __forceinline__ Merged4 merge4(const float *cm, const float *cl, const float *co,
+                                          int D, int rows, int h, int d)
 {
-    mstar = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumers; ++w)
-        mstar = fmaxf(mstar, cm[w * 16 + h]);
-    const float ref = mstar == -INFINITY ? 0.f : mstar;
-    lsum = 0.f;
-    osum = 0.f;
+    Merged4 r;
+    float mw[kConsumers];
+    r.mstar = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kConsumers; ++w) {
-        const float f = exp2f(cm[w * 16 + h] - ref);
-        lsum += cl[w * 16 + h] * f;
-        osum += co[(w * rows + h) * D + d] * f;
+        mw[w] = cm[w * 16 + h];
+        r.mstar = fmaxf(r.mstar, mw[w]);
     }
+    const float ref = r.mstar == -INFINITY ? 0.f : r.mstar;
+    r.lsum = 0.f;
+    r.o[0] = r.o[1] = r.o[2] = r.o[3] = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumers; ++w) {
+        const float f = exp2f(mw[w] - ref);
+        r.lsum += cl[w * 16 + h] * f;
+        const float4 v = *reinterpret_cast<const float4 *>(co + (w * rows + h) * D + d);
+        r.o[0] += v.x * f;
+        r.o[1] += v.y * f;
+        r.o[2] += v.z * f;
+        r.o[3] += v.w * f;
+    }
+    return r;
+}
+
+// out[0, 4) = o[0, 4) / l, rounded to T, as one 8-byte store
+template <typename T>
+__device__ __forceinline__ void store_out4(T *out, const Merged4 &r)
+{
+    uint2 v;
+    v.x = Mma<T>::pack(r.o[0] / r.lsum, r.o[1] / r.lsum);
+    v.y = Mma<T>::pack(r.o[2] / r.lsum, r.o[3] / r.lsum);
+    *reinterpret_cast<uint2 *>(out) = v;
 }
 
 struct DecodeArgs {
@@ -554,7 +595,7 @@ template <int D, int MODE> __host__ __device__ constexpr bool decode_uses_slots(
 }
 template <int D, int MODE> __host__ __device__ constexpr int decode_ring_slots()
 {
-    return D >= 256 ? 3 : MODE == kPagedQ ? 2 * decode_stages(D) : decode_stages(D);
+    return D >= 256 ? 3 : MODE == kPagedQ ? (D == 128 ? 4 : 2 * decode_stages(D)) : decode_stages(D);
 }
 template <int D, int MODE> __host__ __device__ constexpr int decode_slot_bytes()
 {
@@ -564,9 +605,18 @@ template <int D, int MODE> __host__ __device__ constexpr int decode_slot_bytes()
 // thread: the split kernel then runs without a producer warp (four consumer
 // warps, two CTAs an SM, so that a thread may hold up to 255 registers), and
 // the warp that releases a ring slot last issues that slot's next load.
+// (Over int8 pages, where the consumer warps' conversion work is the limit,
+// the same scheme measured slower: the issuing lane stalls its warp.)
 template <int D, int MODE> __host__ __device__ constexpr bool decode_no_producer()
 {
     return D >= 256 && MODE != kPagedQ;
+}
+// the query's MMA fragments are held in registers, else read from shared
+// memory at every tile (head_dim 256; int8 pages, whose conversion work
+// wants the registers for a third CTA an SM)
+template <int D, int MODE> __host__ __device__ constexpr bool decode_q_in_registers()
+{
+    return D <= 128 && MODE != kPagedQ;
 }
 template <int D, int MODE> __host__ __device__ constexpr int decode_threads()
 {
@@ -591,11 +641,11 @@ template <int D, int MODE> __host__ __device__ constexpr int decode_smem_bytes()
 // the same over 16-bit and int8 pages (an int8 tile arrives by two 1-D bulk
 // copies at half the bytes and is expanded on chip before its MMAs).
 // (kPagedQ and head_dim 256: at most as many registers as the CTAs the
-// shared memory lets share an SM can hold -- two at head_dim 128 and 256,
-// three at 64)
+// shared memory lets share an SM can hold -- two at head_dim 256, three
+// over int8 pages at head_dim 64 and 128)
 template <typename T, int D, int MODE>
 __global__ void __launch_bounds__(decode_threads<D, MODE>(),
-                                  (MODE == kPagedQ || D >= 256) ? (D >= 128 ? 2 : 3) : 0)
+                                  (MODE == kPagedQ || D >= 256) ? (D >= 256 ? 2 : 3) : 0)
 decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const DecodeArgs a)
 {
@@ -872,7 +922,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
     }
     consumer_sync();
-    GroupAttn<T, D> ga;
+    GroupAttn<T, D, decode_q_in_registers<D, MODE>(), true> ga;
     ga.init();
     ga.load_q(qs, QS, lane);
     bool timed_out = false;
@@ -1002,19 +1052,19 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     ga.publish(cm, cl, co, warp, lane, g, 16);
     consumer_sync();
     const int hq0 = kvh * g;
-    for (int idx = threadIdx.x; idx < g * D; idx += 128) {
-        const int h = idx / D, d = idx % D;
-        float mstar, lsum, osum;
-        merge4(cm, cl, co, D, 16, h, d, mstar, lsum, osum);
+    for (int idx = threadIdx.x; idx < g * (D / 4); idx += 128) {
+        const int h = idx / (D / 4), d = (idx % (D / 4)) * 4;
+        const Merged4 r = merge4(cm, cl, co, D, 16, h, d);
         const int64_t qrow = (int64_t)b * a.q_heads + hq0 + h;
         if (nsplit == 1) {
-            static_cast<T *>(a.out)[qrow * D + d] = kvc::Elem<T>::from_f32(osum / lsum);
+            store_out4(static_cast<T *>(a.out) + qrow * D + d, r);
         } else {
             const int64_t pr = qrow * a.max_splits + split;
-            a.ws_o[pr * D + d] = osum;
+            *reinterpret_cast<float4 *>(a.ws_o + pr * D + d) =
+                make_float4(r.o[0], r.o[1], r.o[2], r.o[3]);
             if (d == 0) {
-                a.ws_m[pr] = mstar;
-                a.ws_l[pr] = lsum;
+                a.ws_m[pr] = r.mstar;
+                a.ws_l[pr] = r.lsum;
             }
         }
     }
@@ -1147,7 +1197,9 @@ decode_combine_kernel(const DecodeArgs a, int D)
 // a tile goes back E rows lower by TMA store as soon as it is final (the
 // stores of tile t only overwrite cache rows that tiles <= t were loaded
 // from), and the warps run its attention.  A last partial tile goes back by
-// thread stores; without an eviction only the new row is stored.  A ring of
+// thread stores; without an eviction only the visible rows are loaded (from
+// the first visible row on, so a drifting cache with C > W reads W rows, not
+// its whole resident length) and only the new row is stored.  A ring of
 // C slots ("Stateful decode & KV cache", "Sliding-window ring buffer") never
 // moves: its slots are loaded in slot order, the new row replaces slot
 // (T - 1) mod C, and the attention masks the slots by position (the visible
@@ -1208,9 +1260,8 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int g = a.group;
     const int64_t slice = (int64_t)b * a.kv_heads + kvh;
 
-    // the slice's rows are asked of L2 at once when the step loads all of
-    // them but the ones past its length: with C - W < 64 the first visible
-    // row is always in tile 0, so every step loads tiles 0 .. its last one
+    // the whole slice is asked of L2 at once when every step reads nearly
+    // all of it (C - W < 64: at most C - W of its rows go unread)
     if (threadIdx.x == 0) {
         if (C - a.window < kTile) {
             const uint32_t sb = (uint32_t)(C * D * sizeof(T));
@@ -1301,23 +1352,32 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
     T *kc = static_cast<T *>(a.k_cache) + row0 * D;
     T *vc = static_cast<T *>(a.v_cache) + row0 * D;
 
-    // Shared-memory rows: the window row r (windowed / drifting), or the slot
-    // s (ring).  new_r: where the new row goes; [t_lo, t_hi): tiles loaded
-    // from the cache (row r from cache row r + src_off).
-    int new_r, t_lo, t_hi, src_off;
+    // Shared-memory rows: the slot s (ring); the window row r when rows move
+    // (loaded from cache row r + E); otherwise only the visible rows, shared
+    // row r holding window (and cache) row win0 + r, win0 = vis0 -- at any
+    // row, since a TMA box may start at any row.  new_r: the new row's
+    // shared row; [t_lo, t_hi): tiles loaded from the cache (shared row r
+    // from cache row r + src_off).
+    int new_r, t_lo, t_hi, src_off, win0 = 0;
     if (ring) {
         new_r = (int)((T_ - 1) % C);
         const int held = (int)(T_ - 1 < C ? T_ - 1 : C);  // slots holding an old token
         t_lo = 0;
         t_hi = (held + kTile - 1) / kTile;
         src_off = 0;
-    } else {
+    } else if (moves) {
         new_r = L - 1;
-        t_lo = moves ? 0 : vis0 / kTile;
+        t_lo = 0;
         t_hi = (L - 1 + kTile - 1) / kTile;  // rows [0, L - 1) hold old tokens
         src_off = E;
+    } else {
+        win0 = vis0;
+        new_r = L - 1 - win0;
+        t_lo = 0;
+        t_hi = (L - 1 - win0 + kTile - 1) / kTile;
+        src_off = win0;
     }
-    const int ntiles = ring ? (int)((C + kTile - 1) / kTile) : (L + kTile - 1) / kTile;
+    const int ntiles = ring ? (int)((C + kTile - 1) / kTile) : (L - win0 + kTile - 1) / kTile;
 
     // 1. one thread starts the TMA loads of the old rows, one barrier a tile
     if (threadIdx.x == 0) {
@@ -1363,7 +1423,7 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
     for (int u = 0; u < RPT; ++u) {
         if (!moves && row_thread[u]) {
-            T *dst = (row_is_v[u] ? vc : kc) + (int64_t)new_r * D;
+            T *dst = (row_is_v[u] ? vc : kc) + (int64_t)(new_r + win0) * D;
             dst[row_i[u]] = new_lo[u];
             dst[row_i[u] + D / 2] = new_hi[u];
         }
@@ -1373,13 +1433,14 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // holds no token of the window (0 * stale bytes must stay 0) -- rows past
     // the window in its last tile; for a ring, the slots never written
     // (T <= C) and the slots past C
-    const int z0 = ring ? (T_ < C ? (int)T_ : (int)C) : L;
+    const int z0 = ring ? (T_ < C ? (int)T_ : (int)C) : L - win0;
     const int z1 = ntiles * kTile;
     const int stored_tiles = moves ? L / kTile : 0;  // full tiles stored by TMA
 
-    // visible rows: [vis0, L) of the window, or for a ring the nvis slots
-    // ending at new_r (one run, or [0, new_r] and [C - rest, C))
-    int lo1 = vis0, hi1 = L, lo2 = 0, hi2 = 0;
+    // visible rows: window rows [vis0, L) (shared rows from vis0 - win0), or
+    // for a ring the nvis slots ending at new_r (one run, or [0, new_r] and
+    // [C - rest, C))
+    int lo1 = vis0 - win0, hi1 = L - win0, lo2 = 0, hi2 = 0;
     if (ring) {
         const int first = new_r - nvis + 1;
         if (first >= 0) {
@@ -1478,12 +1539,11 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
     float *co = cl + kConsumers * 16;
     ga.publish(cm, cl, co, warp, lane, g, 16);
     __syncthreads();
-    for (int idx = threadIdx.x; idx < g * D; idx += 128) {
-        const int h = idx / D, d = idx % D;
-        float mstar, lsum, osum;
-        merge4(cm, cl, co, D, 16, h, d, mstar, lsum, osum);
+    for (int idx = threadIdx.x; idx < g * (D / 4); idx += 128) {
+        const int h = idx / (D / 4), d = (idx % (D / 4)) * 4;
+        const Merged4 r = merge4(cm, cl, co, D, 16, h, d);
         const int64_t qrow = (int64_t)b * a.q_heads + kvh * g + h;
-        static_cast<T *>(a.out)[qrow * D + d] = kvc::Elem<T>::from_f32(osum / lsum);
+        store_out4(static_cast<T *>(a.out) + qrow * D + d, r);
     }
 }
 
@@ -2049,9 +2109,12 @@ template <typename T, int D>
 kvc_status launch_window_step(const WindowStepArgs &a, int batch, cudaStream_t stream)
 {
     const int64_t ntile_max = (a.capacity + kTile - 1) / kTile;
-    size_t smem = 1024 + (size_t)ntile_max * 2 * kTile * D * 2 + 16 * (D + 8) * 2 + 8 * ntile_max;
-    const size_t merge = 1024 + kConsumers * 16 * (2 + D) * sizeof(float);
-    smem = smem > merge ? smem : merge;
+    // tiles, query rows and barriers; the merge's (m, l, o) reuses the tiles
+    // and, for a window of one tile, part of the query rows after them (both
+    // done with by then; it never reaches the barriers)
+    const size_t tiles = (size_t)ntile_max * 2 * kTile * D * 2;
+    const size_t merge = (2 * kConsumers * 16 + (size_t)kConsumers * 16 * D) * sizeof(float);
+    const size_t smem = 1024 + (tiles > merge ? tiles : merge) + 16 * (D + 8) * 2 + 8 * ntile_max;
     const CUtensorMapDataType tt = std::is_same<T, __half>::value
                                        ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;

@@ -231,7 +231,7 @@ def test_window_step_host_checks(kvc):
     # lengths (5 x batch int32, 256-byte rounded) and the split partials
     assert wsz(2, 8, 2, 512, 64, 1) == 0 and wsz(2, 8, 2, 128, 256, 1) == 0
     assert wsz(2, 8, 2, 1024, 64, 1) == 256 + 256
-    assert wsz(8, 16, 8, 4096, 256, 1) == 256 + 8 * 16 * 8 * (256 + 2) * 4
+    assert wsz(8, 16, 8, 4096, 256, 1) == 256 + 8 * 16 * 4 * (256 + 2) * 4   # 1024-row splits
     for pol in (1, 2, 3):
         assert f(*base, none, 8, 16, 8, 4096, 256, 1, pol, 4096, 0.0, None, None, 0,
                  *nows) == 8
