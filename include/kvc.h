@@ -412,11 +412,12 @@ kvc_status kvc_gqa_decode_paged(void *out, const void *q, const void *k_pool,
  * bytes at G * 16 * head_dim.  Within a group, with D = head_dim:
  *   K element (row j, column d):  nb = j / 8, g = j % 8, kk = d / 16,
  *     dd = d % 16, lane = 4 g + (dd % 8) / 2,
- *     f = (nb * D / 16 + kk) * 4 + 2 (dd / 8) + dd % 2
- *   V element (row j, column c):  nn = c / 16, cc = c % 16,
- *     lane = 4 (cc % 8) + (j % 8) / 2, f = (nn * 2 + cc / 8) * 4 + 2 (j / 8) + j % 2
+ *     f = (2 kk + dd / 8) * 4 + 2 nb + dd % 2
+ *   V element (row j, column c):  mb = c / 16, cc = c % 16,
+ *     lane = 4 (cc % 8) + (j % 8) / 2, f = (2 mb + j / 8) * 4 + 2 (cc / 8) + j % 2
  *   byte = (f / 16) * 512 + lane * 16 + f % 16
- * (lane l's D / 2 bytes are the B fragments of its mma.m16n8k16 steps,
+ * (lane l's D / 2 bytes are the A fragments of its mma.m16n8k16 steps --
+ * the 16 rows are the MMA's M dimension, K as it is and V transposed --
  * stored as 16-byte pieces interleaved across the 32 lanes).
  */
 #define KVC_PAGE_QUANT 0x40000000

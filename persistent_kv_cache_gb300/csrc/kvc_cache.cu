@@ -533,21 +533,25 @@ shift_rows_kernel(char *__restrict__ k_rows, char *__restrict__ v_rows, kvc_leng
 // order of include/kvc.h (q8_k_pos / q8_v_pos below): the decode's lanes then
 // load their MMA operand bytes with 16-byte loads and no shuffling.
 
-// byte of element (row j, column d) within a 16-row group of a K payload
-__device__ __forceinline__ int q8_k_pos(int j, int d, int D)
+// byte of element (row j, column d) within a 16-row group of a K payload:
+// the A fragment of the scores' MMA over columns [16 kk, 16 kk + 16)
+// (rows = keys), word 2 kk + (dd / 8) of the lane, two keys of a column pair
+__device__ __forceinline__ int q8_k_pos(int j, int d)
 {
     const int nb = j >> 3, g = j & 7, kk = d >> 4, dd = d & 15;
     const int lane = 4 * g + ((dd & 7) >> 1);
-    const int fb = (nb * (D >> 4) + kk) * 4 + 2 * (dd >> 3) + (dd & 1);
+    const int fb = (2 * kk + (dd >> 3)) * 4 + 2 * nb + (dd & 1);
     return (fb >> 4) * 512 + lane * 16 + (fb & 15);
 }
 
-// byte of element (row j, column c) within a 16-row group of a V payload
-__device__ __forceinline__ int q8_v_pos(int j, int c, int D)
+// byte of element (row j, column c) within a 16-row group of a V payload:
+// the A fragment (V transposed, rows = columns of V) of the output's MMA
+// over columns [16 mb, 16 mb + 16), word 2 mb + (j / 8) of the lane
+__device__ __forceinline__ int q8_v_pos(int j, int c)
 {
-    const int nn = c >> 4, cc = c & 15;
+    const int mb = c >> 4, cc = c & 15;
     const int lane = 4 * (cc & 7) + ((j & 7) >> 1);
-    const int fb = (nn * 2 + (cc >> 3)) * 4 + 2 * (j >> 3) + (j & 1);
+    const int fb = (2 * mb + (j >> 3)) * 4 + 2 * (cc >> 3) + (j & 1);
     return (fb >> 4) * 512 + lane * 16 + (fb & 15);
 }
 struct QuantSpec {
@@ -592,7 +596,7 @@ quantize_pages_kernel(const T *__restrict__ k_pool, const T *__restrict__ v_pool
         for (int k = 0; k < 8; ++k) {
             const float t = __fdiv_rn(kvc::Elem<T>::to_f32(e[k]), q.scale);
             const float code = fminf(fmaxf(rintf(t) + zp, lo), hi);
-            grp[is_k ? q8_k_pos(row & 15, d0 + k, D) : q8_v_pos(row & 15, d0 + k, D)] =
+            grp[is_k ? q8_k_pos(row & 15, d0 + k) : q8_v_pos(row & 15, d0 + k)] =
                 (int8_t)((int)code - q.bias);
         }
     }

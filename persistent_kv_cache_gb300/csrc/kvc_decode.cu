@@ -106,330 +106,336 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// s - zp for the four signed bytes of w, exactly, as floats: byte b + 128 goes
-// into the low mantissa byte of 2^23 (0x4B000000), so the float is
-// 2^23 + 128 + b, and off = 2^23 + 128 + zp leaves b - zp (|b - zp| <= 255).
-__device__ __forceinline__ void s8x4_minus(uint32_t w, float off, float (&f)[4])
+// 8x8 16-bit matrix held as a fragment (thread t: row t / 4, columns
+// 2 (t % 4) and 2 (t % 4) + 1) -> the same fragment of its transpose
+__device__ __forceinline__ uint32_t movm_trans(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// s - zp for the four signed bytes of w, exactly, as two 16-bit pairs
+// (bytes 0, 1 -> lo; bytes 2, 3 -> hi): byte b + 128 goes into the low
+// mantissa byte of 2^23 (0x4B000000), so the float is 2^23 + 128 + b, and
+// one packed subtraction of off2 = (2^23 + 128 + zp) x 2 leaves b - zp for
+// two bytes at once (|b - zp| <= 255: exact in fp32 and in bf16 / f16).
+template <typename T>
+__device__ __forceinline__ void s8x4_to_pairs(uint32_t w, uint64_t off2, uint32_t &lo, uint32_t &hi)
 {
     const uint32_t u = w ^ 0x80808080u;
-    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - off;
-    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - off;
-    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)) - off;
-    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - off;
+    const uint32_t b0 = __byte_perm(u, 0x4B000000u, 0x7540);
+    const uint32_t b1 = __byte_perm(u, 0x4B000000u, 0x7541);
+    const uint32_t b2 = __byte_perm(u, 0x4B000000u, 0x7542);
+    const uint32_t b3 = __byte_perm(u, 0x4B000000u, 0x7543);
+    uint64_t p01, p23;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(p01) : "r"(b0), "r"(b1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(p23) : "r"(b2), "r"(b3));
+    asm("sub.rn.f32x2 %0, %0, %1;" : "+l"(p01) : "l"(off2));
+    asm("sub.rn.f32x2 %0, %0, %1;" : "+l"(p23) : "l"(off2));
+    float f0, f1, f2, f3;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f0), "=f"(f1) : "l"(p01));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f2), "=f"(f3) : "l"(p23));
+    lo = Mma<T>::pack(f0, f1);
+    hi = Mma<T>::pack(f2, f3);
 }
 
 // Attention state of one consumer warp over 64-row K/V tiles held in shared
-// memory (128-byte swizzled boxes of 64 columns, 8 KB per box): the GQA
-// group's query heads are the M = 16 rows of mma.sync m16n8k16, the warp
-// owns rows [16 w, 16 w + 16) of every tile, and (m, l, o) follow the online
-// softmax in the log2 domain.  Thread t holds heads t/4 and t/4 + 8.
-template <typename T, int D, bool QREG_ = (D <= 128), bool SHORTCUTS = false>
+// memory (128-byte swizzled boxes of 64 columns, 8 KB per box).  The warp
+// owns rows [16 w, 16 w + 16) of every tile.  Those 16 keys are the M = 16
+// rows of mma.sync m16n8k16 and the GQA group's query heads its N columns,
+// in HB blocks of 8 heads:
+//   scores   S^T[key][head]  = K[key][:] . Q[head][:]          (A = K, B = Q^T)
+//   output   O^T[dim][head] += V^T[dim][key] . P^T[key][head]  (A = V^T, B = P^T)
+// so a group of up to 8 heads costs one MMA per 16 keys x 16 columns for the
+// scores and one per 16 columns for the output, and padding heads (zero
+// queries, never published) take the N columns a group leaves free.
+// Thread t (gid = t / 4, tig = t % 4) holds, per head block, the scores of
+// keys gid and gid + 8 for heads 2 tig and 2 tig + 1, and the output of
+// columns 16 mb + gid and 16 mb + gid + 8 for those two heads.  (m, l)
+// follow the online softmax per head in the log2 domain; l sums this
+// thread's keys only, until publish().
+template <typename T, int D, int HB, bool QREG_ = true, bool SHORTCUTS = false>
 struct GroupAttn {
-    static constexpr int NB = D / 8;  // 8-column blocks of the output
-    // the query's A fragments stay in registers up to head_dim 128; at 256
-    // the output alone takes 128 registers a thread, so the fragments are
-    // read from the staged rows (one ldmatrix per 16 columns) instead
+    static constexpr int MB = D / 16;  // 16-column blocks of the head dim
+    // the query's B fragments stay in registers, or (QREG false: head_dim
+    // 256 with two head blocks, where the output alone takes 128 registers a
+    // thread) are read from the staged rows, two 16-column blocks an ldmatrix
     static constexpr bool QREG = QREG_;
-    uint32_t qa[QREG ? D / 16 : 1][4];
-    uint32_t q_addr;  // !QREG: this lane's ldmatrix row address in the staged rows
-    float o[NB][4];
-    float m_lo, m_hi, l_lo, l_hi;
-
-    // A fragment of query columns [16 kk, 16 kk + 16)
-    __device__ __forceinline__ void q_frag(int kk, uint32_t (&a)[4]) const
-    {
-        if constexpr (QREG) {
-            a[0] = qa[kk][0];
-            a[1] = qa[kk][1];
-            a[2] = qa[kk][2];
-            a[3] = qa[kk][3];
-        } else {
-            ldsm_x4(q_addr + kk * 32, a[0], a[1], a[2], a[3]);
-        }
-    }
+    uint32_t qb[QREG ? HB : 1][QREG ? MB : 1][2];
+    uint32_t q_addr, q_hstride;  // !QREG: this lane's ldmatrix row address; bytes per 8 heads
+    float o[HB][MB][4];
+    float m[HB][2], l[HB][2];
 
     __device__ __forceinline__ void init()
     {
 #pragma unroll
-        for (int n = 0; n < NB; ++n)
-            o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-        m_lo = m_hi = -INFINITY;
-        l_lo = l_hi = 0.f;
+        for (int hb = 0; hb < HB; ++hb) {
+#pragma unroll
+            for (int mb = 0; mb < MB; ++mb)
+                o[hb][mb][0] = o[hb][mb][1] = o[hb][mb][2] = o[hb][mb][3] = 0.f;
+            m[hb][0] = m[hb][1] = -INFINITY;
+            l[hb][0] = l[hb][1] = 0.f;
+        }
     }
 
-    // A fragments of the rotated query rows staged as qs[16][QS] (at D > 128
-    // the rows must stay in place while the tiles are attended)
+    // B fragments of query columns [16 kk, 16 kk + 32) of head block hb:
+    // f[0], f[1] for block kk, f[2], f[3] for block kk + 1 (kk even)
+    __device__ __forceinline__ void q_frag2(int hb, int kk, uint32_t (&f)[4]) const
+    {
+        if constexpr (QREG) {
+            f[0] = qb[hb][kk][0];
+            f[1] = qb[hb][kk][1];
+            f[2] = qb[hb][kk + 1][0];
+            f[3] = qb[hb][kk + 1][1];
+        } else {
+            ldsm_x4(q_addr + hb * q_hstride + kk * 32, f[0], f[1], f[2], f[3]);
+        }
+    }
+
+    // the rotated query rows staged as qs[16][QS] (heads >= g zero; at
+    // QREG false the rows must stay in place while the tiles are attended)
     __device__ __forceinline__ void load_q(const T *qs, int QS, int lane)
     {
         if constexpr (!QREG) {
-            // ldmatrix x4: lanes 8m..8m+7 address the rows of matrix m =
-            // (rows 0-7 | 8-15) x (columns 0-7 | 8-15) of a 16-column block
-            const int r = (lane & 7) + ((lane >> 3) & 1) * 8, c = (lane >> 4) * 8;
-            q_addr = kvc::smem_u32(qs + r * QS + c);
+            // ldmatrix x4: lanes 8 m .. 8 m + 7 address head rows 0-7 at
+            // columns 8 m .. 8 m + 7 of a 32-column span
+            q_addr = kvc::smem_u32(qs + (lane & 7) * QS + (lane >> 3) * 8);
+            q_hstride = 8 * QS * 2;
             return;
         }
-        const int row = lane >> 2, col = (lane & 3) * 2;
+        const int gid = lane >> 2, c = (lane & 3) * 2;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            qa[kk][0] = *reinterpret_cast<const uint32_t *>(&qs[row * QS + kk * 16 + col]);
-            qa[kk][1] = *reinterpret_cast<const uint32_t *>(&qs[(row + 8) * QS + kk * 16 + col]);
-            qa[kk][2] = *reinterpret_cast<const uint32_t *>(&qs[row * QS + kk * 16 + 8 + col]);
-            qa[kk][3] =
-                *reinterpret_cast<const uint32_t *>(&qs[(row + 8) * QS + kk * 16 + 8 + col]);
-        }
-    }
-
-    // o *= alpha per head row.  SHORTCUTS (the split kernel): skipped when
-    // every factor of the warp is exactly 1 (the running max did not move),
-    // which leaves o bit for bit as the multiplication would, and the key
-    // mask is skipped on tiles whose 16 keys are all visible -- fewer
-    // instructions where the consumer warps' work is the limit; the
-    // latency-bound window step measured faster without them
-    __device__ __forceinline__ void rescale(float al_lo, float al_hi)
-    {
-        if (SHORTCUTS && !__any_sync(0xffffffffu, al_lo != 1.f || al_hi != 1.f))
-            return;
+        for (int hb = 0; hb < HB; ++hb)
 #pragma unroll
-        for (int n = 0; n < NB; ++n) {
-            o[n][0] *= al_lo;
-            o[n][1] *= al_lo;
-            o[n][2] *= al_hi;
-            o[n][3] *= al_hi;
-        }
-    }
-
-    // Online-softmax update with raw scores sc of this warp's 16 keys (the
-    // same steps as in tile()): mask keys outside [lo, hi), raise m, rescale
-    // l and o, and pack P (times vscale) as the A fragment of the PV MMAs.
-    __device__ __forceinline__ void softmax_step(float (&sc)[2][4], int lane, int lo, int hi,
-                                                 float scale_log2, float vscale, uint32_t (&pa)[4])
-    {
-        float mx_lo = -INFINITY, mx_hi = -INFINITY;
-        const bool whole = SHORTCUTS && lo == 0 && hi == 16;  // every key visible
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int col = 8 * j + 2 * (lane & 3) + (e & 1);
-                float v = sc[j][e] * scale_log2;
-                if (!whole)
-                    v = (col >= lo && col < hi) ? v : -INFINITY;
-                sc[j][e] = v;
-                if (e < 2)
-                    mx_lo = fmaxf(mx_lo, v);
-                else
-                    mx_hi = fmaxf(mx_hi, v);
+            for (int kk = 0; kk < MB; ++kk) {
+                const T *r = qs + (8 * hb + gid) * QS + 16 * kk + c;
+                qb[hb][kk][0] = *reinterpret_cast<const uint32_t *>(r);
+                qb[hb][kk][1] = *reinterpret_cast<const uint32_t *>(r + 8);
             }
-        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-        const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-        // a row with nothing visible yet keeps m = -inf and contributes 0
-        const float ref_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
-        const float ref_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
-        const float al_lo = exp2f(m_lo - ref_lo), al_hi = exp2f(m_hi - ref_hi);
-        m_lo = mn_lo;
-        m_hi = mn_hi;
-        float ps_lo = 0.f, ps_hi = 0.f;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            sc[j][0] = exp2f(sc[j][0] - ref_lo);
-            sc[j][1] = exp2f(sc[j][1] - ref_lo);
-            sc[j][2] = exp2f(sc[j][2] - ref_hi);
-            sc[j][3] = exp2f(sc[j][3] - ref_hi);
-            ps_lo += sc[j][0] + sc[j][1];
-            ps_hi += sc[j][2] + sc[j][3];
-        }
-        l_lo = l_lo * al_lo + ps_lo;
-        l_hi = l_hi * al_hi + ps_hi;
-        rescale(al_lo, al_hi);
-        pa[0] = Mma<T>::pack(sc[0][0] * vscale, sc[0][1] * vscale);
-        pa[1] = Mma<T>::pack(sc[0][2] * vscale, sc[0][3] * vscale);
-        pa[2] = Mma<T>::pack(sc[1][0] * vscale, sc[1][1] * vscale);
-        pa[3] = Mma<T>::pack(sc[1][2] * vscale, sc[1][3] * vscale);
     }
 
-    // One tile: rows [lo, hi) of this warp's 16 rows are visible (the caller
+    // o *= alpha per head.  SHORTCUTS (the split kernel): skipped when every
+    // factor of the warp is exactly 1 (the running max did not move), which
+    // leaves o bit for bit as the multiplication would, and the key mask is
+    // skipped on tiles whose 16 keys are all visible -- fewer instructions
+    // where the consumer warps' work is the limit; the latency-bound window
+    // step measured faster without them
+    __device__ __forceinline__ void rescale(const float (&al)[HB][2])
+    {
+        if constexpr (SHORTCUTS) {
+            bool moved = false;
+#pragma unroll
+            for (int hb = 0; hb < HB; ++hb)
+                moved |= al[hb][0] != 1.f || al[hb][1] != 1.f;
+            if (!__any_sync(0xffffffffu, moved))
+                return;
+        }
+#pragma unroll
+        for (int hb = 0; hb < HB; ++hb)
+#pragma unroll
+            for (int mb = 0; mb < MB; ++mb) {
+                o[hb][mb][0] *= al[hb][0];
+                o[hb][mb][1] *= al[hb][1];
+                o[hb][mb][2] *= al[hb][0];
+                o[hb][mb][3] *= al[hb][1];
+            }
+    }
+
+    // Online-softmax update with the raw scores sc of this warp's 16 keys:
+    // mask keys outside [lo, hi), raise m, rescale l and o, and pack P (times
+    // vscale; VS false: times 1) as the B fragments of the output MMAs
+    template <bool VS>
+    __device__ __forceinline__ void softmax_step(float (&sc)[HB][4], int lane, int lo, int hi,
+                                                 float scale_log2, float vscale,
+                                                 uint32_t (&pb)[HB][2])
+    {
+        const int k0 = lane >> 2, k1 = k0 + 8;  // this thread's keys
+        const bool whole = SHORTCUTS && lo == 0 && hi == 16;  // every key visible
+        const bool in0 = whole || (k0 >= lo && k0 < hi);
+        const bool in1 = whole || (k1 >= lo && k1 < hi);
+        float al[HB][2];
+#pragma unroll
+        for (int hb = 0; hb < HB; ++hb)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float v0 = sc[hb][j] * scale_log2, v1 = sc[hb][2 + j] * scale_log2;
+                if (!whole) {
+                    v0 = in0 ? v0 : -INFINITY;
+                    v1 = in1 ? v1 : -INFINITY;
+                }
+                float mx = fmaxf(v0, v1);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float mn = fmaxf(m[hb][j], mx);
+                // a head with nothing visible yet keeps m = -inf and contributes 0
+                const float ref = mn == -INFINITY ? 0.f : mn;
+                al[hb][j] = exp2f(m[hb][j] - ref);
+                m[hb][j] = mn;
+                const float p0 = exp2f(v0 - ref), p1 = exp2f(v1 - ref);
+                l[hb][j] = l[hb][j] * al[hb][j] + (p0 + p1);
+                sc[hb][j] = p0;
+                sc[hb][2 + j] = p1;
+            }
+        rescale(al);
+#pragma unroll
+        for (int hb = 0; hb < HB; ++hb) {
+            const uint32_t x0 = VS ? Mma<T>::pack(sc[hb][0] * vscale, sc[hb][1] * vscale)
+                                   : Mma<T>::pack(sc[hb][0], sc[hb][1]);
+            const uint32_t x1 = VS ? Mma<T>::pack(sc[hb][2] * vscale, sc[hb][3] * vscale)
+                                   : Mma<T>::pack(sc[hb][2], sc[hb][3]);
+            pb[hb][0] = movm_trans(x0);  // P^T keys 2 tig, 2 tig + 1; head gid
+            pb[hb][1] = movm_trans(x1);  // keys 2 tig + 8, 2 tig + 9
+        }
+    }
+
+    // One tile: keys [lo, hi) of this warp's 16 rows are visible (the caller
     // guarantees that V rows at and past `hi` hold finite values).
     __device__ __forceinline__ void tile(uint32_t kb, uint32_t vb, int warp, int lane, int lo,
                                          int hi, float scale_log2)
     {
-        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float sc[HB][4];
+#pragma unroll
+        for (int hb = 0; hb < HB; ++hb)
+            sc[hb][0] = sc[hb][1] = sc[hb][2] = sc[hb][3] = 0.f;
+        // ldmatrix x4 of an A fragment: matrix m = lane / 8 holds keys
+        // 8 (m % 2) .. + 7 at columns 8 (m / 2) .. + 7 of the 16-column block
         const int mat = lane >> 3;
-        const int krow = 16 * warp + ((mat >> 1) << 3) + (lane & 7);
+        const int krow = 16 * warp + ((mat & 1) << 3) + (lane & 7);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const int cidx = 2 * kk + (mat & 1);
-            uint32_t r_0, r_1, r_2, r_3;
-            ldsm_x4(kb + (cidx >> 3) * 8192 + kvc::sw128(krow, cidx & 7), r_0, r_1, r_2, r_3);
-            if constexpr (QREG) {
-                Mma<T>::run(sc[0], qa[kk], r_0, r_1);
-                Mma<T>::run(sc[1], qa[kk], r_2, r_3);
-            } else {
+        for (int kk = 0; kk < MB; kk += 2) {
+            uint32_t qf[HB][4];
+#pragma unroll
+            for (int hb = 0; hb < HB; ++hb)
+                q_frag2(hb, kk, qf[hb]);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int cidx = 2 * (kk + u) + (mat >> 1);
                 uint32_t a[4];
-                q_frag(kk, a);
-                Mma<T>::run(sc[0], a, r_0, r_1);
-                Mma<T>::run(sc[1], a, r_2, r_3);
+                ldsm_x4(kb + (cidx >> 3) * 8192 + kvc::sw128(krow, cidx & 7), a[0], a[1], a[2],
+                        a[3]);
+#pragma unroll
+                for (int hb = 0; hb < HB; ++hb)
+                    Mma<T>::run(sc[hb], a, qf[hb][2 * u], qf[hb][2 * u + 1]);
             }
         }
-        float mx_lo = -INFINITY, mx_hi = -INFINITY;
-        const bool whole = SHORTCUTS && lo == 0 && hi == 16;  // every key visible
+        uint32_t pb[HB][2];
+        softmax_step<false>(sc, lane, lo, hi, scale_log2, 1.f, pb);
+        // A = V^T by transposing loads: matrix m holds keys 8 (m / 2) .. + 7
+        // at columns 8 (m % 2) .. + 7 of the 16-column block
+        const int vrow = 16 * warp + ((mat >> 1) << 3) + (lane & 7);
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+        for (int mb = 0; mb < MB; ++mb) {
+            const int cidx = 2 * mb + (mat & 1);
+            uint32_t a[4];
+            ldsm_x4_t(vb + (cidx >> 3) * 8192 + kvc::sw128(vrow, cidx & 7), a[0], a[1], a[2],
+                      a[3]);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int col = 8 * j + 2 * (lane & 3) + (e & 1);
-                float v = sc[j][e] * scale_log2;
-                if (!whole)
-                    v = (col >= lo && col < hi) ? v : -INFINITY;
-                sc[j][e] = v;
-                if (e < 2)
-                    mx_lo = fmaxf(mx_lo, v);
-                else
-                    mx_hi = fmaxf(mx_hi, v);
-            }
-        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-        const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-        // a row with nothing visible yet keeps m = -inf and contributes 0
-        const float ref_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
-        const float ref_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
-        const float al_lo = exp2f(m_lo - ref_lo), al_hi = exp2f(m_hi - ref_hi);
-        m_lo = mn_lo;
-        m_hi = mn_hi;
-        float ps_lo = 0.f, ps_hi = 0.f;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            sc[j][0] = exp2f(sc[j][0] - ref_lo);
-            sc[j][1] = exp2f(sc[j][1] - ref_lo);
-            sc[j][2] = exp2f(sc[j][2] - ref_hi);
-            sc[j][3] = exp2f(sc[j][3] - ref_hi);
-            ps_lo += sc[j][0] + sc[j][1];
-            ps_hi += sc[j][2] + sc[j][3];
-        }
-        l_lo = l_lo * al_lo + ps_lo;
-        l_hi = l_hi * al_hi + ps_hi;
-        rescale(al_lo, al_hi);
-        uint32_t pa[4];
-        pa[0] = Mma<T>::pack(sc[0][0], sc[0][1]);
-        pa[1] = Mma<T>::pack(sc[0][2], sc[0][3]);
-        pa[2] = Mma<T>::pack(sc[1][0], sc[1][1]);
-        pa[3] = Mma<T>::pack(sc[1][2], sc[1][3]);
-        const int vrow = 16 * warp + ((mat & 1) << 3) + (lane & 7);
-#pragma unroll
-        for (int nn = 0; nn < D / 16; ++nn) {
-            const int cidx = 2 * nn + (mat >> 1);
-            uint32_t r_0, r_1, r_2, r_3;
-            ldsm_x4_t(vb + (cidx >> 3) * 8192 + kvc::sw128(vrow, cidx & 7), r_0, r_1, r_2, r_3);
-            Mma<T>::run(o[2 * nn], pa, r_0, r_1);
-            Mma<T>::run(o[2 * nn + 1], pa, r_2, r_3);
+            for (int hb = 0; hb < HB; ++hb)
+                Mma<T>::run(o[hb][mb], a, pb[hb][0], pb[hb][1]);
         }
     }
 
     // One tile of an int8 page: kq / vq = this warp's 16-row group of the K
     // and V payloads in fragment order (kvc_quantize_pages): the lane's
-    // D / 2 bytes of each are the exact B fragments of its QK and PV MMAs,
-    // as 16-byte pieces interleaved across the warp (piece i of lane l at
-    // i * 512 + l * 16).  They become the integers s - zp in registers
-    // (koff / voff = 2^23 + 128 + zp); the scores take the page's K scale
-    // (folded into scale_log2) and the probabilities its V scale.  Every
-    // converted value is finite, and P is 0 past `hi`, so the rows past the
-    // split end need no zeroing.
+    // D / 2 bytes of each are the exact A fragments of its MMAs, as 16-byte
+    // pieces interleaved across the warp (piece i of lane l at i * 512 +
+    // l * 16), piece i holding 16-column blocks 2 i and 2 i + 1.  They become
+    // the integers s - zp in registers (koff2 / voff2 = (2^23 + 128 + zp) x 2);
+    // the scores take the page's K scale (folded into scale_log2) and the
+    // probabilities its V scale.  Every converted value is finite, and P is 0
+    // past `hi`, so the rows past the split end need no zeroing.
     __device__ __forceinline__ void tile_q8(const uint8_t *kq, const uint8_t *vq, int lane, int lo,
-                                            int hi, float scale_log2, float vscale, float koff,
-                                            float voff)
+                                            int hi, float scale_log2, float vscale, uint64_t koff2,
+                                            uint64_t voff2)
     {
-        constexpr int NU = D / 32;  // 16-byte pieces of a lane's fragment bytes
-        // (at D > 128 the pieces are loaded and used in two halves, to keep
-        // the registers for the output)
-        constexpr int HALVES = D > 128 ? 2 : 1;
-        constexpr int NH = NU / HALVES;
-        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        constexpr int NP = D / 32;  // 16-byte pieces of a lane's fragment bytes
+        float sc[HB][4];
 #pragma unroll
-        for (int hh = 0; hh < HALVES; ++hh) {
-            // K words: nb * (D / 16) + kk; half hh holds nb = hh when halved
-            uint4 kf[NH];
+        for (int hb = 0; hb < HB; ++hb)
+            sc[hb][0] = sc[hb][1] = sc[hb][2] = sc[hb][3] = 0.f;
 #pragma unroll
-            for (int i = 0; i < NH; ++i)
-                kf[i] = *reinterpret_cast<const uint4 *>(kq + (hh * NH + i) * 512 + lane * 16);
-            const uint32_t *kw = reinterpret_cast<const uint32_t *>(kf);
+        for (int p = 0; p < NP; ++p) {
+            // words: (block 2p, keys 0-7 | 8-15 at columns +0 / +8), (block 2p + 1, ...)
+            const uint4 w = *reinterpret_cast<const uint4 *>(kq + p * 512 + lane * 16);
+            uint32_t qf[HB][4];
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
+            for (int hb = 0; hb < HB; ++hb)
+                q_frag2(hb, 2 * p, qf[hb]);
+            uint32_t a[4];
+            s8x4_to_pairs<T>(w.x, koff2, a[0], a[1]);
+            s8x4_to_pairs<T>(w.y, koff2, a[2], a[3]);
 #pragma unroll
-                for (int nb = 0; nb < 2 / HALVES; ++nb) {
-                    const int nbg = HALVES == 2 ? hh : nb;
-                    uint32_t a[4];
-                    q_frag(kk, a);
-                    float f[4];
-                    s8x4_minus(kw[nb * (D / 16) + kk], koff, f);
-                    Mma<T>::run(sc[nbg], a, Mma<T>::pack(f[0], f[1]), Mma<T>::pack(f[2], f[3]));
-                }
+            for (int hb = 0; hb < HB; ++hb)
+                Mma<T>::run(sc[hb], a, qf[hb][0], qf[hb][1]);
+            s8x4_to_pairs<T>(w.z, koff2, a[0], a[1]);
+            s8x4_to_pairs<T>(w.w, koff2, a[2], a[3]);
+#pragma unroll
+            for (int hb = 0; hb < HB; ++hb)
+                Mma<T>::run(sc[hb], a, qf[hb][2], qf[hb][3]);
         }
-        uint32_t pa[4];
-        softmax_step(sc, lane, lo, hi, scale_log2, vscale, pa);
+        uint32_t pb[HB][2];
+        softmax_step<true>(sc, lane, lo, hi, scale_log2, vscale, pb);
 #pragma unroll
-        for (int hh = 0; hh < HALVES; ++hh) {
-            // V words: nn * 2 + nb; half hh holds nn in [hh D / 32, (hh + 1) D / 32)
-            uint4 vf[NH];
+        for (int p = 0; p < NP; ++p) {
+            // words: (columns of block 2p, keys 0-7), (block 2p, keys 8-15), (block 2p + 1, ...)
+            const uint4 w = *reinterpret_cast<const uint4 *>(vq + p * 512 + lane * 16);
+            uint32_t a[4];
+            s8x4_to_pairs<T>(w.x, voff2, a[0], a[1]);
+            s8x4_to_pairs<T>(w.y, voff2, a[2], a[3]);
 #pragma unroll
-            for (int i = 0; i < NH; ++i)
-                vf[i] = *reinterpret_cast<const uint4 *>(vq + (hh * NH + i) * 512 + lane * 16);
-            const uint32_t *vw = reinterpret_cast<const uint32_t *>(vf);
+            for (int hb = 0; hb < HB; ++hb)
+                Mma<T>::run(o[hb][2 * p], a, pb[hb][0], pb[hb][1]);
+            s8x4_to_pairs<T>(w.z, voff2, a[0], a[1]);
+            s8x4_to_pairs<T>(w.w, voff2, a[2], a[3]);
 #pragma unroll
-            for (int n2 = 0; n2 < D / 16 / HALVES; ++n2)
-#pragma unroll
-                for (int nb = 0; nb < 2; ++nb) {
-                    const int nn = hh * (D / 16 / HALVES) + n2;
-                    float f[4];
-                    s8x4_minus(vw[n2 * 2 + nb], voff, f);
-                    Mma<T>::run(o[2 * nn + nb], pa, Mma<T>::pack(f[0], f[1]),
-                                Mma<T>::pack(f[2], f[3]));
-                }
+            for (int hb = 0; hb < HB; ++hb)
+                Mma<T>::run(o[hb][2 * p + 1], a, pb[hb][0], pb[hb][1]);
         }
     }
 
-    // finish l across the quad and publish (m, l, o) of heads < g for the
-    // 4-warp merge: cm/cl [4][16], co [4][rows][D] (rows >= g)
+    // finish l across the warp's keys and publish (m, l, o) of heads < g for
+    // the 4-warp merge: cm/cl [4][16], co [4][rows][pitch] (rows >= g; a
+    // pitch of D + 4 floats keeps the stores of the four head pairs apart
+    // in the banks)
     __device__ __forceinline__ void publish(float *cm, float *cl, float *co, int warp, int lane,
-                                            int g, int rows)
+                                            int g, int rows, int pitch)
     {
-        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-        l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-        l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-        const int row = lane >> 2, col = 2 * (lane & 3);
-        if ((lane & 3) == 0) {
-            cm[warp * 16 + row] = m_lo;
-            cl[warp * 16 + row] = l_lo;
-            cm[warp * 16 + row + 8] = m_hi;
-            cl[warp * 16 + row + 8] = l_hi;
-        }
+        const int gid = lane >> 2, tig = lane & 3;
 #pragma unroll
-        for (int n = 0; n < NB; ++n) {
-            if (row < g) {
-                co[(warp * rows + row) * D + 8 * n + col] = o[n][0];
-                co[(warp * rows + row) * D + 8 * n + col + 1] = o[n][1];
+        for (int hb = 0; hb < HB; ++hb)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float s = l[hb][j];
+                s += __shfl_xor_sync(0xffffffffu, s, 4);
+                s += __shfl_xor_sync(0xffffffffu, s, 8);
+                s += __shfl_xor_sync(0xffffffffu, s, 16);
+                const int h = 8 * hb + 2 * tig + j;
+                if (gid == 0) {
+                    cm[warp * 16 + h] = m[hb][j];
+                    cl[warp * 16 + h] = s;
+                }
+                if (h < g) {
+                    float *dst = co + (warp * rows + h) * pitch + gid;
+#pragma unroll
+                    for (int mb = 0; mb < MB; ++mb) {
+                        dst[16 * mb] = o[hb][mb][j];
+                        dst[16 * mb + 8] = o[hb][mb][2 + j];
+                    }
+                }
             }
-            if (row + 8 < g) {
-                co[(warp * rows + row + 8) * D + 8 * n + col] = o[n][2];
-                co[(warp * rows + row + 8) * D + 8 * n + col + 1] = o[n][3];
-            }
-        }
     }
 };
-
 // merged (unnormalised o, l, reference max) of head h, columns [d, d + 4)
-// over the four warps' published partials (cm/cl [4][16], co [4][rows][D];
-// d a multiple of 4): one round of shared-memory loads, the partials of the
-// four columns read as one float4 per warp
+// over the four warps' published partials (cm/cl [4][16], co
+// [4][rows][pitch]; d a multiple of 4): one round of shared-memory loads,
+// the partials of the four columns read as one float4 per warp
 struct Merged4 {
     float mstar, lsum, o[4];
 };
 __device__ __forceinline__ Merged4 merge4(const float *cm, const float *cl, const float *co,
-                                          int D, int rows, int h, int d)
+                                          int pitch, int rows, int h, int d)
 {
     Merged4 r;
     float mw[kConsumers];
@@ -446,7 +452,7 @@ __device__ __forceinline__ Merged4 merge4(const float *cm, const float *cl, cons
     for (int w = 0; w < kConsumers; ++w) {
         const float f = exp2f(mw[w] - ref);
         r.lsum += cl[w * 16 + h] * f;
-        const float4 v = *reinterpret_cast<const float4 *>(co + (w * rows + h) * D + d);
+        const float4 v = *reinterpret_cast<const float4 *>(co + (w * rows + h) * pitch + d);
         r.o[0] += v.x * f;
         r.o[1] += v.y * f;
         r.o[2] += v.z * f;
@@ -612,11 +618,12 @@ template <int D, int MODE> __host__ __device__ constexpr bool decode_no_producer
     return D >= 256 && MODE != kPagedQ;
 }
 // the query's MMA fragments are held in registers, else read from shared
-// memory at every tile (head_dim 256; int8 pages, whose conversion work
-// wants the registers for a third CTA an SM)
-template <int D, int MODE> __host__ __device__ constexpr bool decode_q_in_registers()
+// memory at every tile: with two blocks of 8 heads at head_dim 256 (whose
+// output accumulator alone takes 128 registers a thread) and over int8 pages
+// (whose conversion work wants the registers for a third CTA an SM)
+template <int D, int HB, int MODE = kPlain> __host__ __device__ constexpr bool decode_q_in_registers()
 {
-    return D <= 128 && MODE != kPagedQ;
+    return HB == 1 || (D <= 128 && MODE != kPagedQ);
 }
 template <int D, int MODE> __host__ __device__ constexpr int decode_threads()
 {
@@ -643,7 +650,7 @@ template <int D, int MODE> __host__ __device__ constexpr int decode_smem_bytes()
 // (kPagedQ and head_dim 256: at most as many registers as the CTAs the
 // shared memory lets share an SM can hold -- two at head_dim 256, three
 // over int8 pages at head_dim 64 and 128)
-template <typename T, int D, int MODE>
+template <typename T, int D, int MODE, int HB>
 __global__ void __launch_bounds__(decode_threads<D, MODE>(),
                                   (MODE == kPagedQ || D >= 256) ? (D >= 256 ? 2 : 3) : 0)
 decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -922,7 +929,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
     }
     consumer_sync();
-    GroupAttn<T, D, decode_q_in_registers<D, MODE>(), true> ga;
+    GroupAttn<T, D, HB, decode_q_in_registers<D, HB, MODE>(), true> ga;
     ga.init();
     ga.load_q(qs, QS, lane);
     bool timed_out = false;
@@ -1005,10 +1012,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const float kz = __shfl_sync(0xffffffffu, my_p[1], pi);
             const float vs = __shfl_sync(0xffffffffu, my_p[2], pi);
             const float vz = __shfl_sync(0xffffffffu, my_p[3], pi);
-            if (my_lo < my_valid)
+            if (my_lo < my_valid) {
+                const uint32_t ko = __float_as_uint(8388608.f + 128.f + kz);
+                const uint32_t vo = __float_as_uint(8388608.f + 128.f + vz);
                 ga.tile_q8(kgen + warp * 16 * D, kgen + kTile * D + warp * 16 * D, lane, my_lo,
-                           my_valid, a.scale_log2 * ks, vs, 8388608.f + 128.f + kz,
-                           8388608.f + 128.f + vz);
+                           my_valid, a.scale_log2 * ks, vs, ((uint64_t)ko << 32) | ko,
+                           ((uint64_t)vo << 32) | vo);
+            }
         } else if (my_valid > 0) {
             if (my_valid < 16) {
                 // rows past the split end: zero V so that 0 * garbage stays 0
@@ -1049,12 +1059,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     float *cm = reinterpret_cast<float *>(stages);        // [4][16]
     float *cl = cm + kConsumers * 16;                      // [4][16]
     float *co = cl + kConsumers * 16;                      // [4][16][D]
-    ga.publish(cm, cl, co, warp, lane, g, 16);
+    ga.publish(cm, cl, co, warp, lane, g, 16, D + 4);
     consumer_sync();
     const int hq0 = kvh * g;
     for (int idx = threadIdx.x; idx < g * (D / 4); idx += 128) {
         const int h = idx / (D / 4), d = (idx % (D / 4)) * 4;
-        const Merged4 r = merge4(cm, cl, co, D, 16, h, d);
+        const Merged4 r = merge4(cm, cl, co, D + 4, 16, h, d);
         const int64_t qrow = (int64_t)b * a.q_heads + hq0 + h;
         if (nsplit == 1) {
             store_out4(static_cast<T *>(a.out) + qrow * D + d, r);
@@ -1230,7 +1240,7 @@ __host__ __device__ constexpr int64_t window_step_max_capacity(int D)
     return kWindowStepMaxElems / D;
 }
 
-template <typename T, int D>
+template <typename T, int D, int HB>
 __global__ void __launch_bounds__(128, D >= 256 ? 2 : 4)
 window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const WindowStepArgs a)
@@ -1457,7 +1467,7 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
     // 3-5. the tiles in order: wait for the tile, place what belongs in it,
     //      store it back when rows moved, run its attention
     __syncthreads();  // the barriers' initialisation is visible to all threads
-    GroupAttn<T, D> ga;
+    GroupAttn<T, D, HB, decode_q_in_registers<D, HB>()> ga;
     ga.init();
     ga.load_q(qs, QS, lane);
     // (a wait that runs out marks this thread; the loop goes on, skipping
@@ -1537,11 +1547,11 @@ window_step_kernel(const __grid_constant__ CUtensorMap tmap_k,
     float *cm = reinterpret_cast<float *>(smem);
     float *cl = cm + kConsumers * 16;
     float *co = cl + kConsumers * 16;
-    ga.publish(cm, cl, co, warp, lane, g, 16);
+    ga.publish(cm, cl, co, warp, lane, g, 16, D + 4);
     __syncthreads();
     for (int idx = threadIdx.x; idx < g * (D / 4); idx += 128) {
         const int h = idx / (D / 4), d = (idx % (D / 4)) * 4;
-        const Merged4 r = merge4(cm, cl, co, D, 16, h, d);
+        const Merged4 r = merge4(cm, cl, co, D + 4, 16, h, d);
         const int64_t qrow = (int64_t)b * a.q_heads + kvh * g + h;
         store_out4(static_cast<T *>(a.out) + qrow * D + d, r);
     }
@@ -1763,10 +1773,14 @@ kvc_status launch_decode16(void *out, const void *q, const void *k_cache, const 
     const size_t smem = 1024 + (size_t)(q8 ? decode_smem_bytes<D, kPagedQ>()
                                            : decode_smem_bytes<D, kPlain>());
     const int threads = q8 ? decode_threads<D, kPagedQ>() : decode_threads<D, kPlain>();
-    auto kern = fx                 ? decode_split_kernel<T, D, kFused>
-                : px && px->qk_pool ? decode_split_kernel<T, D, kPagedQ>
-                : px               ? decode_split_kernel<T, D, kPaged>
-                                   : decode_split_kernel<T, D, kPlain>;
+    // one block of 8 query heads per KV head up to a group of 8, two up to 16
+    const bool hb2 = a.group > 8;
+    auto kern = fx ? (hb2 ? decode_split_kernel<T, D, kFused, 2> : decode_split_kernel<T, D, kFused, 1>)
+                : q8 ? (hb2 ? decode_split_kernel<T, D, kPagedQ, 2>
+                            : decode_split_kernel<T, D, kPagedQ, 1>)
+                : px ? (hb2 ? decode_split_kernel<T, D, kPaged, 2> : decode_split_kernel<T, D, kPaged, 1>)
+                     : (hb2 ? decode_split_kernel<T, D, kPlain, 2>
+                            : decode_split_kernel<T, D, kPlain, 1>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return KVC_ERR_CUDA;
@@ -2113,7 +2127,7 @@ kvc_status launch_window_step(const WindowStepArgs &a, int batch, cudaStream_t s
     // and, for a window of one tile, part of the query rows after them (both
     // done with by then; it never reaches the barriers)
     const size_t tiles = (size_t)ntile_max * 2 * kTile * D * 2;
-    const size_t merge = (2 * kConsumers * 16 + (size_t)kConsumers * 16 * D) * sizeof(float);
+    const size_t merge = (2 * kConsumers * 16 + (size_t)kConsumers * 16 * (D + 4)) * sizeof(float);
     const size_t smem = 1024 + (tiles > merge ? tiles : merge) + 16 * (D + 8) * 2 + 8 * ntile_max;
     const CUtensorMapDataType tt = std::is_same<T, __half>::value
                                        ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
@@ -2125,7 +2139,7 @@ kvc_status launch_window_step(const WindowStepArgs &a, int batch, cudaStream_t s
     if (!kvc_host::encode_2d_bf16_sw128(&tk, a.k_cache, rows, D, kTile, tt) ||
         !kvc_host::encode_2d_bf16_sw128(&tv, a.v_cache, rows, D, kTile, tt))
         return KVC_ERR_CUDA;
-    auto kern = window_step_kernel<T, D>;
+    auto kern = a.group > 8 ? window_step_kernel<T, D, 2> : window_step_kernel<T, D, 1>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return KVC_ERR_CUDA;

@@ -40,10 +40,10 @@ def _positions(D, which):
     d = np.arange(D)[None, :]
     if which == "k":
         lane = 4 * (j % 8) + (d % 16 % 8) // 2
-        f = ((j // 8) * (D // 16) + d // 16) * 4 + 2 * (d % 16 // 8) + d % 2
+        f = (2 * (d // 16) + d % 16 // 8) * 4 + 2 * (j // 8) + d % 2
     else:
         lane = 4 * (d % 16 % 8) + (j % 8) // 2
-        f = ((d // 16) * 2 + d % 16 // 8) * 4 + 2 * (j // 8) + j % 2
+        f = (2 * (d // 16) + j // 8) * 4 + 2 * (d % 16 // 8) + j % 2
     return (f // 16) * 512 + lane * 16 + f % 16
 
 
