@@ -29,6 +29,7 @@
 // (batch row, kv head) finishes last: one launch per step.
 // fp32 path: attn_f32_kernel, one warp per query row on CUDA cores (also used
 // by the multi-token call for fp32).
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -215,36 +216,14 @@ struct GroupAttn {
             }
     }
 
-    // o *= alpha per head.  SHORTCUTS (the split kernel): skipped when every
-    // factor of the warp is exactly 1 (the running max did not move), which
-    // leaves o bit for bit as the multiplication would, and the key mask is
-    // skipped on tiles whose 16 keys are all visible -- fewer instructions
-    // where the consumer warps' work is the limit; the latency-bound window
-    // step measured faster without them
-    __device__ __forceinline__ void rescale(const float (&al)[HB][2])
-    {
-        if constexpr (SHORTCUTS) {
-            bool moved = false;
-#pragma unroll
-            for (int hb = 0; hb < HB; ++hb)
-                moved |= al[hb][0] != 1.f || al[hb][1] != 1.f;
-            if (!__any_sync(0xffffffffu, moved))
-                return;
-        }
-#pragma unroll
-        for (int hb = 0; hb < HB; ++hb)
-#pragma unroll
-            for (int mb = 0; mb < MB; ++mb) {
-                o[hb][mb][0] *= al[hb][0];
-                o[hb][mb][1] *= al[hb][1];
-                o[hb][mb][2] *= al[hb][0];
-                o[hb][mb][3] *= al[hb][1];
-            }
-    }
-
     // Online-softmax update with the raw scores sc of this warp's 16 keys:
-    // mask keys outside [lo, hi), raise m, rescale l and o, and pack P (times
-    // vscale; VS false: times 1) as the B fragments of the output MMAs
+    // mask keys outside [lo, hi), move the reference max, rescale l and o,
+    // and pack P (times vscale; VS false: times 1) as the B fragments of
+    // the output MMAs.  The reference max of a head moves only when the
+    // tile's max exceeds it by more than 8 (log2 units), so P stays below
+    // 2^8 and o and l are rescaled on few tiles after the first (O / l is
+    // the same for any reference).  SHORTCUTS (the split kernel): the key
+    // mask is skipped on tiles whose 16 keys are all visible.
     template <bool VS>
     __device__ __forceinline__ void softmax_step(float (&sc)[HB][4], int lane, int lo, int hi,
                                                  float scale_log2, float vscale,
@@ -254,7 +233,8 @@ struct GroupAttn {
         const bool whole = SHORTCUTS && lo == 0 && hi == 16;  // every key visible
         const bool in0 = whole || (k0 >= lo && k0 < hi);
         const bool in1 = whole || (k1 >= lo && k1 < hi);
-        float al[HB][2];
+        float mx[HB][2];
+        bool up = false;
 #pragma unroll
         for (int hb = 0; hb < HB; ++hb)
 #pragma unroll
@@ -264,23 +244,49 @@ struct GroupAttn {
                     v0 = in0 ? v0 : -INFINITY;
                     v1 = in1 ? v1 : -INFINITY;
                 }
-                float mx = fmaxf(v0, v1);
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float mn = fmaxf(m[hb][j], mx);
+                sc[hb][j] = v0;
+                sc[hb][2 + j] = v1;
+                float x = fmaxf(v0, v1);
+                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
+                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 8));
+                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 16));
+                mx[hb][j] = x;
+                // (false for a fully masked tile; true for the first visible
+                // keys of a head, whose m is still -inf)
+                up |= x > m[hb][j] + 8.f;
+            }
+        if (__any_sync(0xffffffffu, up)) {
+#pragma unroll
+            for (int hb = 0; hb < HB; ++hb) {
+                float al[2];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const bool u = mx[hb][j] > m[hb][j] + 8.f;
+                    const float mn = u ? mx[hb][j] : m[hb][j];
+                    al[j] = u ? exp2f(m[hb][j] - mn) : 1.f;
+                    m[hb][j] = mn;
+                    l[hb][j] *= al[j];
+                }
+#pragma unroll
+                for (int mb = 0; mb < MB; ++mb) {
+                    o[hb][mb][0] *= al[0];
+                    o[hb][mb][1] *= al[1];
+                    o[hb][mb][2] *= al[0];
+                    o[hb][mb][3] *= al[1];
+                }
+            }
+        }
+#pragma unroll
+        for (int hb = 0; hb < HB; ++hb) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
                 // a head with nothing visible yet keeps m = -inf and contributes 0
-                const float ref = mn == -INFINITY ? 0.f : mn;
-                al[hb][j] = exp2f(m[hb][j] - ref);
-                m[hb][j] = mn;
-                const float p0 = exp2f(v0 - ref), p1 = exp2f(v1 - ref);
-                l[hb][j] = l[hb][j] * al[hb][j] + (p0 + p1);
+                const float ref = m[hb][j] == -INFINITY ? 0.f : m[hb][j];
+                const float p0 = exp2f(sc[hb][j] - ref), p1 = exp2f(sc[hb][2 + j] - ref);
+                l[hb][j] += p0 + p1;
                 sc[hb][j] = p0;
                 sc[hb][2 + j] = p1;
             }
-        rescale(al);
-#pragma unroll
-        for (int hb = 0; hb < HB; ++hb) {
             const uint32_t x0 = VS ? Mma<T>::pack(sc[hb][0] * vscale, sc[hb][1] * vscale)
                                    : Mma<T>::pack(sc[hb][0], sc[hb][1]);
             const uint32_t x1 = VS ? Mma<T>::pack(sc[hb][2] * vscale, sc[hb][3] * vscale)
@@ -806,22 +812,29 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
             kvc::tma_prefetch_desc(&tmap_k);
             kvc::tma_prefetch_desc(&tmap_v);
             int pos = 0;  // slots: ring position of the next tile's first slot
+            // paged: the tile's page among the split's and its first row in
+            // that page, stepped per tile (q0 and the page size are
+            // multiples of the tile)
+            int ppi = 0, prow = MODE >= kPaged ? q0 % a.page_size : 0;
             for (int t = 0; t < ntiles; ++t) {
                 // the tile's first row in the tensor maps, and whether it is int8
                 int32_t y = 0;
                 bool q8 = false;
                 int64_t q8off = 0;
                 if constexpr (MODE >= kPaged) {
-                    const int r = q0 + t * kTile;  // logical row, a multiple of 64
-                    const int id = page_ids[r / a.page_size - page0];
+                    const int id = page_ids[ppi];
                     if constexpr (MODE == kPagedQ)
                         q8 = int8_page(id, a);
                     if (q8)
                         q8off = (((int64_t)(id & ~KVC_PAGE_QUANT) * a.kv_heads + kvh) *
-                                     a.page_size + r % a.page_size) * D;
+                                     a.page_size + prow) * D;
                     else
-                        y = (int32_t)(((int64_t)id * a.kv_heads + kvh) * a.page_size +
-                                      r % a.page_size);
+                        y = (int32_t)(((int64_t)id * a.kv_heads + kvh) * a.page_size + prow);
+                    prow += kTile;
+                    if (prow == a.page_size) {
+                        prow = 0;
+                        ++ppi;
+                    }
                 } else {
                     y = (int32_t)(row_base + tile_start(t));
                 }
@@ -955,13 +968,15 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
 
     int pos = 0;  // slots: ring position of the tile's first slot
+    // kPagedQ: the tile's page among the split's (pi) and its place in that
+    // page (tin, in 64-row tiles), stepped per tile without a division (q0
+    // and the page size are multiples of the tile)
+    const int tpp = MODE == kPagedQ ? a.page_size / kTile : 1;
+    int pi = 0, tin = MODE == kPagedQ ? (q0 / kTile) % tpp : 0;
     for (int t = 0; t < ntiles; ++t) {
         bool q8 = false;
-        int pi = 0;  // kPagedQ: the tile's page among the split's
-        if constexpr (MODE == kPagedQ) {
-            pi = (q0 + t * kTile) / a.page_size - q0 / a.page_size;
+        if constexpr (MODE == kPagedQ)
             q8 = (__shfl_sync(0xffffffffu, my_e, pi) & KVC_PAGE_QUANT) != 0;
-        }
         // the tile's K and V (16-bit), or its int8 K and V payloads (kgen)
         uint8_t *kgen, *vgen;
         int s0, s1;
@@ -1047,6 +1062,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 kvc::mbar_arrive(&empty[s1]);
         }
         pos += q8 ? 1 : 2;
+        if (MODE == kPagedQ && ++tin == tpp) {
+            tin = 0;
+            ++pi;
+        }
     }
     if (timed_out) {
         if (lane == 0) {
@@ -2119,6 +2138,24 @@ KVC_API kvc_status kvc_decode_step(void *out, const void *q, void *k_cache, void
 
 namespace {
 
+// shared memory of one SM (cached per device)
+size_t smem_per_sm()
+{
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 233472;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+                cudaSuccess ||
+            n <= 0)
+            n = 233472;
+        cached[dev].store(n, std::memory_order_relaxed);
+    }
+    return (size_t)n;
+}
+
 template <typename T, int D>
 kvc_status launch_window_step(const WindowStepArgs &a, int batch, cudaStream_t stream)
 {
@@ -2128,7 +2165,17 @@ kvc_status launch_window_step(const WindowStepArgs &a, int batch, cudaStream_t s
     // done with by then; it never reaches the barriers)
     const size_t tiles = (size_t)ntile_max * 2 * kTile * D * 2;
     const size_t merge = (2 * kConsumers * 16 + (size_t)kConsumers * 16 * (D + 4)) * sizeof(float);
-    const size_t smem = 1024 + (tiles > merge ? tiles : merge) + 16 * (D + 8) * 2 + 8 * ntile_max;
+    size_t smem = 1024 + (tiles > merge ? tiles : merge) + 16 * (D + 8) * 2 + 8 * ntile_max;
+    // a window that compacts on every step writes its rows back each step:
+    // at most four CTAs an SM, so that the next step's early CTAs (launched
+    // as this one's signal at entry allows) do not crowd this step's loads
+    // and stores in DRAM (five an SM measured 0.8 us slower a step on the
+    // 128-row window; without the write-back, five are slightly faster)
+    if (a.policy == KVC_WINDOWED) {
+        const size_t four_an_sm = smem_per_sm() / 5 + 1;  // a fifth CTA no longer fits
+        if (smem < four_an_sm)
+            smem = four_an_sm;
+    }
     const CUtensorMapDataType tt = std::is_same<T, __half>::value
                                        ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
