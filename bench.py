@@ -873,7 +873,7 @@ class PagedDecodeQ8(PagedDecode):
         if not with_kernels:
             return
         K = self.K
-        self.qk = torch.empty(self.n_q_pages, Hkv, P, D, dtype=torch.int8, device=dev)
+        self.qk = torch.empty(self.n_q_pages, Hkv, P, D, dtype=torch.uint8, device=dev)
         self.qv = torch.empty_like(self.qk)
         self.qp = torch.zeros(self.n_q_pages, 4, dtype=torch.float32, device=dev)
         if src:
@@ -911,7 +911,7 @@ class PagedDecodeQ8(PagedDecode):
         T = self.T[rows]
         full = (T - 1) // P
         n_q = max(1, int(full.sum()))
-        qk = np.zeros((n_q, w.kv_heads, P, w.head_dim), np.int8)
+        qk = np.zeros((n_q, w.kv_heads, P, w.head_dim), np.uint8)
         qv = np.zeros_like(qk)
         qp = np.zeros((n_q, 4), np.float32)
         tab = tab16.copy()

@@ -401,11 +401,11 @@ kvc_status kvc_gqa_decode_paged(void *out, const void *q, const void *k_pool,
  * heterogeneous paged KV": selected-block affine quantization; "Persistent
  * KV Cache and Decode Performance Roadmap", "Phase 3": cold pages to INT8,
  * recent tokens kept in the native type).  Int8 pages live in pools
- * qk_pool, qv_pool [n_qpool_pages, kv_heads, page_size, head_dim] (int8); a
+ * qk_pool, qv_pool [n_qpool_pages, kv_heads, page_size, head_dim] of bytes; a
  * block-table entry with KVC_PAGE_QUANT set names page
  * (entry & ~KVC_PAGE_QUANT) of these pools.  qparams is device float
  * [n_qpool_pages][4] = (k_scale, k_zp, v_scale, v_zp) per int8 page, so that
- * a stored byte s reconstructs as (s - zp) * scale.
+ * a stored byte u (unsigned) reconstructs as (u - zp) * scale.
  *
  * Payload order (the MMA fragment order of the decode): the page_size rows of
  * a (page, kv head) are cut into groups of 16; group G is 16 * head_dim
@@ -427,9 +427,11 @@ kvc_status kvc_gqa_decode_paged(void *out, const void *q, const void *k_pool,
  * KV head) becomes int8 page dst_pages[i], for i < n_pages:
  *     code = saturate(round_half_even(x / scale) + zero_point)
  * with x / scale in float32, saturated to [-128, 127] (INT8) or [0, 255]
- * (UINT8: *_unsigned != 0); the stored byte is code - bias (bias 0 for INT8,
- * 128 for UINT8) and qparams[dst] = (k_scale, k_zero_point - k_bias, v_scale,
- * v_zero_point - v_bias).  K and V may use different formats.
+ * (UINT8: *_unsigned != 0); the stored byte is the unsigned code + 128 - bias
+ * (bias 0 for INT8, 128 for UINT8: an INT8 code c is stored as c + 128, a
+ * UINT8 code as itself) and qparams[dst] = (k_scale, k_zero_point + 128 -
+ * k_bias, v_scale, v_zero_point + 128 - v_bias).  K and V may use different
+ * formats.
  * k_pool, v_pool     device [n_pool_pages, kv_heads, page_size, head_dim],
  *                    KVC_BF16 or KVC_F16.
  * src_pages, dst_pages  device int32 [n_pages]; a pair with an id outside its
@@ -451,9 +453,9 @@ kvc_status kvc_quantize_pages(const void *k_pool, const void *v_pool, void *qk_p
  * kvc_gqa_decode_paged_q -- kvc_gqa_decode_paged over a cache whose pages are
  * 16-bit (entries naming the k_pool / v_pool pages) or int8 (entries with
  * KVC_PAGE_QUANT).  An int8 tile is read at half the bytes and its
- * reconstruction (s - zp) * scale enters the attention with the page's
- * scale applied in float32 after the products: scores = k_scale * q . (s - zp),
- * values = v_scale * sum p (s - zp).  An entry outside its pool sets
+ * reconstruction (u - zp) * scale enters the attention with the page's
+ * scale applied in float32 after the products: scores = k_scale * q . (u - zp),
+ * values = v_scale * sum p (u - zp).  An entry outside its pool sets
  * KVC_DEV_INDEX_OOB (that row's output is undefined).  Same arguments and
  * limits as kvc_gqa_decode_paged plus the int8 pools, qparams (16-byte
  * aligned) and n_qpool_pages.

@@ -370,14 +370,15 @@ def dequantize_affine(codes, scale, zero_point):
 
 
 def quantize_page(page, scale, zero_point, unsigned=False):
-    """One page (any shape) of 16-bit bits or float32 values -> (stored int8
-    bytes, stored zero point).  The stored byte is the code minus a bias (0
-    for INT8, 128 for UINT8) and the stored zero point is zero_point minus the
-    same bias, so (stored - stored zero point) * scale is the reconstruction
-    for either code type."""
+    """One page (any shape) of 16-bit bits or float32 values -> (stored
+    bytes as uint8, stored zero point).  The stored byte is the code plus an
+    offset (128 for INT8, so that c in [-128, 127] becomes c + 128; 0 for
+    UINT8) and the stored zero point is zero_point plus the same offset, so
+    (stored - stored zero point) * scale is the reconstruction for either
+    code type."""
     codes = quantize_affine(to_f32(page), scale, zero_point, unsigned)
-    bias = 128 if unsigned else 0
-    return (codes - bias).astype(np.int8), int(zero_point) - bias
+    off = 0 if unsigned else 128
+    return (codes + off).astype(np.uint8), int(zero_point) + off
 
 
 def paged_rows_q(pool, qpool, qparams, which, block_table, n_rows, page_size):

@@ -528,8 +528,9 @@ shift_rows_kernel(char *__restrict__ k_rows, char *__restrict__ v_rows, kvc_leng
 
 // Page src[i] of a 16-bit pool -> int8 page dst[i], one CTA per (i, kv head,
 // K/V): code = saturate(rint(x / scale) + zp) with x / scale rounded once in
-// float32 and rint rounding ties to even, stored as code - bias (bias 128 for
-// UINT8, so that one int8 payload serves both code types), in the fragment
+// float32 and rint rounding ties to even, stored as the unsigned byte
+// code + 128 - bias (bias 128 for UINT8, 0 for INT8: one payload serves both
+// code types, and the decode places the byte as it is), in the fragment
 // order of include/kvc.h (q8_k_pos / q8_v_pos below): the decode's lanes then
 // load their MMA operand bytes with 16-byte loads and no shuffling.
 
@@ -562,7 +563,7 @@ struct QuantSpec {
 template <typename T>
 __global__ void __launch_bounds__(256)
 quantize_pages_kernel(const T *__restrict__ k_pool, const T *__restrict__ v_pool,
-                      int8_t *__restrict__ qk_pool, int8_t *__restrict__ qv_pool,
+                      uint8_t *__restrict__ qk_pool, uint8_t *__restrict__ qv_pool,
                       const int32_t *__restrict__ src_pages, const int32_t *__restrict__ dst_pages,
                       int64_t n_pool_pages, int64_t n_q_pages, int kv_heads, int D, int64_t slab,
                       QuantSpec kq, QuantSpec vq, float *__restrict__ qparams, int32_t *status)
@@ -578,26 +579,26 @@ quantize_pages_kernel(const T *__restrict__ k_pool, const T *__restrict__ v_pool
     const QuantSpec q = is_k ? kq : vq;
     if (threadIdx.x == 0 && h == 0) {
         qparams[(int64_t)dst * 4 + (is_k ? 0 : 2)] = q.scale;
-        qparams[(int64_t)dst * 4 + (is_k ? 1 : 3)] = (float)(q.zp - q.bias);
+        qparams[(int64_t)dst * 4 + (is_k ? 1 : 3)] = (float)(q.zp + 128 - q.bias);
     }
     // slab = page_size * head_dim elements of one (page, head), a multiple of 8
     const int64_t so = ((int64_t)src * kv_heads + h) * slab;
     const int64_t dof = ((int64_t)dst * kv_heads + h) * slab;
     const uint4 *in = reinterpret_cast<const uint4 *>((is_k ? k_pool : v_pool) + so);
-    int8_t *out = (is_k ? qk_pool : qv_pool) + dof;
+    uint8_t *out = (is_k ? qk_pool : qv_pool) + dof;
     const float lo = (float)q.lo, hi = (float)q.hi, zp = (float)q.zp;
     const int cpr = D / 8;  // 8-element chunks per row
     for (int64_t c = threadIdx.x; c < slab / 8; c += blockDim.x) {
         const uint4 x = in[c];
         const T *e = reinterpret_cast<const T *>(&x);
         const int row = (int)(c / cpr), d0 = (int)(c % cpr) * 8;
-        int8_t *grp = out + (int64_t)(row >> 4) * 16 * D;
+        uint8_t *grp = out + (int64_t)(row >> 4) * 16 * D;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const float t = __fdiv_rn(kvc::Elem<T>::to_f32(e[k]), q.scale);
             const float code = fminf(fmaxf(rintf(t) + zp, lo), hi);
             grp[is_k ? q8_k_pos(row & 15, d0 + k) : q8_v_pos(row & 15, d0 + k)] =
-                (int8_t)((int)code - q.bias);
+                (uint8_t)((int)code + 128 - q.bias);
         }
     }
 }
@@ -811,12 +812,12 @@ KVC_API kvc_status kvc_quantize_pages(const void *k_pool, const void *v_pool, vo
     if (dtype == KVC_BF16)
         quantize_pages_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
             static_cast<const __nv_bfloat16 *>(k_pool), static_cast<const __nv_bfloat16 *>(v_pool),
-            static_cast<int8_t *>(qk_pool), static_cast<int8_t *>(qv_pool), src_pages, dst_pages,
+            static_cast<uint8_t *>(qk_pool), static_cast<uint8_t *>(qv_pool), src_pages, dst_pages,
             n_pool_pages, n_qpool_pages, kv_heads, head_dim, slab, kq, vq, qparams, dev_status);
     else
         quantize_pages_kernel<__half><<<grid, 256, 0, stream>>>(
             static_cast<const __half *>(k_pool), static_cast<const __half *>(v_pool),
-            static_cast<int8_t *>(qk_pool), static_cast<int8_t *>(qv_pool), src_pages, dst_pages,
+            static_cast<uint8_t *>(qk_pool), static_cast<uint8_t *>(qv_pool), src_pages, dst_pages,
             n_pool_pages, n_qpool_pages, kv_heads, head_dim, slab, kq, vq, qparams, dev_status);
     return kvc_host::launch_status();
 }

@@ -107,6 +107,16 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// 16 bytes from shared memory (a 32-bit shared-window address)
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
 // 8x8 16-bit matrix held as a fragment (thread t: row t / 4, columns
 // 2 (t % 4) and 2 (t % 4) + 1) -> the same fragment of its transpose
 __device__ __forceinline__ uint32_t movm_trans(uint32_t x)
@@ -116,19 +126,18 @@ __device__ __forceinline__ uint32_t movm_trans(uint32_t x)
     return y;
 }
 
-// s - zp for the four signed bytes of w, exactly, as two 16-bit pairs
-// (bytes 0, 1 -> lo; bytes 2, 3 -> hi): byte b + 128 goes into the low
-// mantissa byte of 2^23 (0x4B000000), so the float is 2^23 + 128 + b, and
-// one packed subtraction of off2 = (2^23 + 128 + zp) x 2 leaves b - zp for
-// two bytes at once (|b - zp| <= 255: exact in fp32 and in bf16 / f16).
+// u - zp for the four unsigned bytes of w, exactly, as two 16-bit pairs
+// (bytes 0, 1 -> lo; bytes 2, 3 -> hi): byte u goes into the low mantissa
+// byte of 2^23 (0x4B000000), so the float is 2^23 + u, and one packed
+// subtraction of off2 = (2^23 + zp) x 2 leaves u - zp for two bytes at once
+// (|u - zp| <= 255: exact in fp32 and in bf16 / f16).
 template <typename T>
-__device__ __forceinline__ void s8x4_to_pairs(uint32_t w, uint64_t off2, uint32_t &lo, uint32_t &hi)
+__device__ __forceinline__ void u8x4_to_pairs(uint32_t w, uint64_t off2, uint32_t &lo, uint32_t &hi)
 {
-    const uint32_t u = w ^ 0x80808080u;
-    const uint32_t b0 = __byte_perm(u, 0x4B000000u, 0x7540);
-    const uint32_t b1 = __byte_perm(u, 0x4B000000u, 0x7541);
-    const uint32_t b2 = __byte_perm(u, 0x4B000000u, 0x7542);
-    const uint32_t b3 = __byte_perm(u, 0x4B000000u, 0x7543);
+    const uint32_t b0 = __byte_perm(w, 0x4B000000u, 0x7540);
+    const uint32_t b1 = __byte_perm(w, 0x4B000000u, 0x7541);
+    const uint32_t b2 = __byte_perm(w, 0x4B000000u, 0x7542);
+    const uint32_t b3 = __byte_perm(w, 0x4B000000u, 0x7543);
     uint64_t p01, p23;
     asm("mov.b64 %0, {%1, %2};" : "=l"(p01) : "r"(b0), "r"(b1));
     asm("mov.b64 %0, {%1, %2};" : "=l"(p23) : "r"(b2), "r"(b3));
@@ -343,16 +352,17 @@ struct GroupAttn {
         }
     }
 
-    // One tile of an int8 page: kq / vq = this warp's 16-row group of the K
-    // and V payloads in fragment order (kvc_quantize_pages): the lane's
+    // One tile of an int8 page: kq / vq = shared-memory addresses of this
+    // warp's 16-row group of the K and V payloads in fragment order
+    // (kvc_quantize_pages): the lane's
     // D / 2 bytes of each are the exact A fragments of its MMAs, as 16-byte
     // pieces interleaved across the warp (piece i of lane l at i * 512 +
     // l * 16), piece i holding 16-column blocks 2 i and 2 i + 1.  They become
-    // the integers s - zp in registers (koff2 / voff2 = (2^23 + 128 + zp) x 2);
+    // the integers u - zp in registers (koff2 / voff2 = (2^23 + zp) x 2);
     // the scores take the page's K scale (folded into scale_log2) and the
     // probabilities its V scale.  Every converted value is finite, and P is 0
     // past `hi`, so the rows past the split end need no zeroing.
-    __device__ __forceinline__ void tile_q8(const uint8_t *kq, const uint8_t *vq, int lane, int lo,
+    __device__ __forceinline__ void tile_q8(uint32_t kq, uint32_t vq, int lane, int lo,
                                             int hi, float scale_log2, float vscale, uint64_t koff2,
                                             uint64_t voff2)
     {
@@ -364,19 +374,19 @@ struct GroupAttn {
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
             // words: (block 2p, keys 0-7 | 8-15 at columns +0 / +8), (block 2p + 1, ...)
-            const uint4 w = *reinterpret_cast<const uint4 *>(kq + p * 512 + lane * 16);
+            const uint4 w = lds128(kq + p * 512 + lane * 16);
             uint32_t qf[HB][4];
 #pragma unroll
             for (int hb = 0; hb < HB; ++hb)
                 q_frag2(hb, 2 * p, qf[hb]);
             uint32_t a[4];
-            s8x4_to_pairs<T>(w.x, koff2, a[0], a[1]);
-            s8x4_to_pairs<T>(w.y, koff2, a[2], a[3]);
+            u8x4_to_pairs<T>(w.x, koff2, a[0], a[1]);
+            u8x4_to_pairs<T>(w.y, koff2, a[2], a[3]);
 #pragma unroll
             for (int hb = 0; hb < HB; ++hb)
                 Mma<T>::run(sc[hb], a, qf[hb][0], qf[hb][1]);
-            s8x4_to_pairs<T>(w.z, koff2, a[0], a[1]);
-            s8x4_to_pairs<T>(w.w, koff2, a[2], a[3]);
+            u8x4_to_pairs<T>(w.z, koff2, a[0], a[1]);
+            u8x4_to_pairs<T>(w.w, koff2, a[2], a[3]);
 #pragma unroll
             for (int hb = 0; hb < HB; ++hb)
                 Mma<T>::run(sc[hb], a, qf[hb][2], qf[hb][3]);
@@ -386,15 +396,15 @@ struct GroupAttn {
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
             // words: (columns of block 2p, keys 0-7), (block 2p, keys 8-15), (block 2p + 1, ...)
-            const uint4 w = *reinterpret_cast<const uint4 *>(vq + p * 512 + lane * 16);
+            const uint4 w = lds128(vq + p * 512 + lane * 16);
             uint32_t a[4];
-            s8x4_to_pairs<T>(w.x, voff2, a[0], a[1]);
-            s8x4_to_pairs<T>(w.y, voff2, a[2], a[3]);
+            u8x4_to_pairs<T>(w.x, voff2, a[0], a[1]);
+            u8x4_to_pairs<T>(w.y, voff2, a[2], a[3]);
 #pragma unroll
             for (int hb = 0; hb < HB; ++hb)
                 Mma<T>::run(o[hb][2 * p], a, pb[hb][0], pb[hb][1]);
-            s8x4_to_pairs<T>(w.z, voff2, a[0], a[1]);
-            s8x4_to_pairs<T>(w.w, voff2, a[2], a[3]);
+            u8x4_to_pairs<T>(w.z, voff2, a[0], a[1]);
+            u8x4_to_pairs<T>(w.w, voff2, a[2], a[3]);
 #pragma unroll
             for (int hb = 0; hb < HB; ++hb)
                 Mma<T>::run(o[hb][2 * p + 1], a, pb[hb][0], pb[hb][1]);
@@ -504,7 +514,7 @@ struct DecodeArgs {
     // int8 pages (kvc_gqa_decode_paged_q): a table entry with KVC_PAGE_QUANT
     // names page (entry & ~KVC_PAGE_QUANT) of these pools, read as
     // (stored - zp) * scale with qparams[page] = (k_scale, k_zp, v_scale, v_zp)
-    const int8_t *qk_pool, *qv_pool;
+    const uint8_t *qk_pool, *qv_pool;
     const float *qparams;
     int64_t n_q_pages;
 };
@@ -1028,11 +1038,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const float vs = __shfl_sync(0xffffffffu, my_p[2], pi);
             const float vz = __shfl_sync(0xffffffffu, my_p[3], pi);
             if (my_lo < my_valid) {
-                const uint32_t ko = __float_as_uint(8388608.f + 128.f + kz);
-                const uint32_t vo = __float_as_uint(8388608.f + 128.f + vz);
-                ga.tile_q8(kgen + warp * 16 * D, kgen + kTile * D + warp * 16 * D, lane, my_lo,
-                           my_valid, a.scale_log2 * ks, vs, ((uint64_t)ko << 32) | ko,
-                           ((uint64_t)vo << 32) | vo);
+                const uint32_t ko = __float_as_uint(8388608.f + kz);
+                const uint32_t vo = __float_as_uint(8388608.f + vz);
+                const uint32_t kq = kvc::smem_u32(kgen) + warp * 16 * D;
+                ga.tile_q8(kq, kq + kTile * D, lane, my_lo, my_valid, a.scale_log2 * ks, vs,
+                           ((uint64_t)ko << 32) | ko, ((uint64_t)vo << 32) | vo);
             }
         } else if (my_valid > 0) {
             if (my_valid < 16) {
@@ -1710,7 +1720,7 @@ struct PagedExtra {
     const int32_t *block_table;
     int max_pages, page_size;
     int64_t n_pool_pages;
-    const int8_t *qk_pool, *qv_pool;  // int8 pages (kvc_gqa_decode_paged_q), else NULL
+    const uint8_t *qk_pool, *qv_pool;  // int8 pages (kvc_gqa_decode_paged_q), else NULL
     const float *qparams;
     int64_t n_q_pages;
 };
@@ -1951,7 +1961,7 @@ KVC_API kvc_status kvc_gqa_decode_ring(void *out, const void *q, const void *k_c
 namespace {
 
 kvc_status paged_decode_entry(void *out, const void *q, const void *k_pool, const void *v_pool,
-                              const int8_t *qk_pool, const int8_t *qv_pool, const float *qparams,
+                              const uint8_t *qk_pool, const uint8_t *qv_pool, const float *qparams,
                               int64_t n_q_pages, const int32_t *block_table, int max_pages,
                               int64_t n_pool_pages, int page_size, kvc_lengths len, int batch,
                               int q_heads, int kv_heads, int head_dim, int dtype,
@@ -2048,8 +2058,8 @@ KVC_API kvc_status kvc_gqa_decode_paged_q(void *out, const void *q, const void *
         if (kvc_host::overlaps(qk_pool, qb, qv_pool, qb))
             return KVC_ERR_SHAPE;
     }
-    return paged_decode_entry(out, q, k_pool, v_pool, static_cast<const int8_t *>(qk_pool),
-                              static_cast<const int8_t *>(qv_pool), qparams, n_qpool_pages,
+    return paged_decode_entry(out, q, k_pool, v_pool, static_cast<const uint8_t *>(qk_pool),
+                              static_cast<const uint8_t *>(qv_pool), qparams, n_qpool_pages,
                               block_table, max_pages, n_pool_pages, page_size, len, batch,
                               q_heads, kv_heads, head_dim, dtype, local_window_size, scale,
                               rope_cos, rope_sin, rope_max_pos, workspace, workspace_bytes,

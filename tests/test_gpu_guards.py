@@ -188,8 +188,8 @@ def test_paged_append_quantize_and_decode(K):
     nk = synth.normal((B, Hkv, 1, D), 6, 3).to(dev())
     nv = synth.normal((B, Hkv, 1, D), 6, 4).to(dev())
     K.kvc_paged_append(kp.t, vp.t, nk, nv, table, L, rope=rd, status=st)
-    qk = Guarded((B * max_pages, Hkv, P, D), torch.int8)
-    qv = Guarded((B * max_pages, Hkv, P, D), torch.int8)
+    qk = Guarded((B * max_pages, Hkv, P, D), torch.uint8)
+    qv = Guarded((B * max_pages, Hkv, P, D), torch.uint8)
     qp = Guarded((B * max_pages, 4), torch.float32)
     src = torch.tensor([0, 1, 4], dtype=torch.int32, device=dev())
     K.kvc_quantize_pages(kp.t, vp.t, qk.t, qv.t, src, src, qp.t, 0.05, status=st)

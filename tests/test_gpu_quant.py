@@ -68,7 +68,7 @@ def _pools_np(qk, qv):
 
 
 def _q8_pools(n_q, Hkv, P, D):
-    qk = torch.full((n_q, Hkv, P, D), 77, dtype=torch.int8, device=dev())
+    qk = torch.full((n_q, Hkv, P, D), 77, dtype=torch.uint8, device=dev())
     qv = torch.full_like(qk, 77)
     qp = torch.zeros(n_q, 4, dtype=torch.float32, device=dev())
     return qk, qv, qp
@@ -105,9 +105,9 @@ def test_quantize_bits(K, orc, dtype):
         assert (qk[d_] == 77).all() and (qv[d_] == 77).all() and (qp[d_] == 0).all()
     # the tie page holds exact ties: both roundings of a tie must not appear
     codes = orc.quantize_affine(orc.to_f32(kb[3]), 0.25, 0)
-    assert np.array_equal(natural_order(qk[6].cpu().numpy(), "k").astype(np.int32), codes)
+    assert np.array_equal(natural_order(qk[6].cpu().numpy(), "k").astype(np.int32) - 128, codes)
     # and the saturating page reaches both ends
-    assert qk[1].max().item() == 127 and qk[1].min().item() == -128
+    assert qk[1].max().item() == 255 and qk[1].min().item() == 0
 
 
 def test_quantize_bad_pair(K):

@@ -58,11 +58,11 @@ def test_uint8_is_int8_with_shifted_zero_point():
     page = rng.normal(0, 0.5, (2, 64, 32)).astype(np.float32)
     s_u, z_u = oracle.quantize_page(page, 0.01, 128, unsigned=True)
     s_i, z_i = oracle.quantize_page(page, 0.01, 0, unsigned=False)
-    assert z_u == z_i == 0
+    assert z_u == z_i == 128
     assert np.array_equal(s_u, s_i)
     s_u, z_u = oracle.quantize_page(page, 0.02, 140, unsigned=True)
     s_i, z_i = oracle.quantize_page(page, 0.02, 12, unsigned=False)
-    assert z_u == z_i == 12 and np.array_equal(s_u, s_i)
+    assert z_u == z_i == 140 and np.array_equal(s_u, s_i)
 
 
 def _one_page_cache(k, v, P):
@@ -128,7 +128,7 @@ def test_unquantized_table_is_paged_attention():
     table = np.array([[3, 1, 5], [0, 2, 4]], np.int32)
     n = [150, 70]
     q = rng.normal(0, 1, (B, Hq, 1, D)).astype(np.float32)
-    qk = np.zeros((1, Hkv, P, D), np.int8)
+    qk = np.zeros((1, Hkv, P, D), np.uint8)
     qp = np.zeros((1, 4), np.float32)
     got, _ = oracle.paged_attention_q(q, kp, vp, qk, qk, qp, table, P, n, n)
     want, _ = oracle.paged_attention(q, kp, vp, table, P, n, n)
