@@ -24,6 +24,9 @@ Other workloads (--workload):
                   seed/append + tcgen05 chunk attention + copy-back
   window-prefill-inplace  the same step with the stage held in the cache's
                   own rows (no seed copy; the copy-back is an in-place shift)
+  window-prefill-hazard  the same step as one kvc_window_prefill_step call,
+                  which stages only the rows whose eviction the chunk sees
+  window-prefill-hazard-slack  the same with C = W + 64 (no row is staged)
   scatter         TensorScatter circular, (16, 8, 4096, 128) bf16, in place,
                   --chunk S in {1, 16, 64}; one step = one scatter call (the
                   line also reports the per-launch floor of a graph node)
@@ -484,6 +487,7 @@ class WindowPrefill(Workload):
     """Windowed chunked prefill through the C + S staging cache."""
     roofline_kernel = "kvc_gqa_prefill_chunk (tcgen05)"
     bound = "tensor"
+    slack = 0  # rows of capacity beyond the window (C = W + slack)
 
     def __init__(self, dev, seed=0, with_kernels=True, chunk=2048):
         import torch
@@ -494,7 +498,8 @@ class WindowPrefill(Workload):
         S = self.S = int(chunk or 2048)
         # the kernel's DRAM traffic depends on the chunk (grid and reuse)
         self.traffic_key = ("kvc_prefill.cu", f"prefill_tc_kernel@chunk{S}")
-        B, Hq, Hkv, D, C, W = w.batch, w.q_heads, w.kv_heads, w.head_dim, w.capacity, w.window
+        B, Hq, Hkv, D, W = w.batch, w.q_heads, w.kv_heads, w.head_dim, w.window
+        C = self.C = w.capacity + self.slack
         g = torch.Generator(device=dev)
         g.manual_seed(seed)
         bf = torch.bfloat16
@@ -545,7 +550,7 @@ class WindowPrefill(Workload):
 
     def step(self, i):
         K, w = self.K, self.w
-        K.kvc_seq_lengths(self.sk, self.S, w.capacity, 1, local_window_size=w.window, out=self.L,
+        K.kvc_seq_lengths(self.sk, self.S, self.C, 1, local_window_size=w.window, out=self.L,
                           status=self.st)
         K.kvc_window_append(self.kc, self.vc, self.nk, self.nv, self.L, 1, K.KVC_APPEND,
                             self.ks, self.vs, rope=self.rope, status=self.st)
@@ -561,7 +566,7 @@ class WindowPrefill(Workload):
     def config(self):
         w = self.w
         return {"workload": w.name, "batch": w.batch, "q_heads": w.q_heads,
-                "kv_heads": w.kv_heads, "head_dim": w.head_dim, "capacity": w.capacity,
+                "kv_heads": w.kv_heads, "head_dim": w.head_dim, "capacity": self.C,
                 "window": w.window, "past_len": f"U[{w.total_lo},{w.total_hi}]",
                 "chunk": self.S, "visible_flops_per_step": self.flops,
                 "kv_split": (getattr(self, "pws", None) is not None
@@ -580,19 +585,19 @@ class WindowPrefill(Workload):
         vc = synth.bits(self.vc[rows].cpu()).copy()
         cos, sin = (t.cpu().numpy() for t in self.rope)
         sk = (self.P[rows] + S - 1).astype(np.int32)
-        ks = np.zeros((len(rows), w.kv_heads, w.capacity + S, w.head_dim), np.uint16)
+        ks = np.zeros((len(rows), w.kv_heads, self.C + S, w.head_dim), np.uint16)
         vs = np.zeros_like(ks)
         if sync is not None:
             sync()  # the threads of a parallel sample start together
         t0 = time.perf_counter()
-        lens = oracle.seq_lengths(sk, S, w.capacity, 1)
+        lens = oracle.seq_lengths(sk, S, self.C, 1)
         oracle.window_append(kc, vc, synth.bits(self.nk_host[rows]),
                              synth.bits(self.nv_host[rows]), lens, 1, cos, sin, ks, vs)
         q = np.ascontiguousarray(synth.bits(self.q_host[rows])[:, :, S - 1:S])
         oracle.gqa_attention(q, ks, vs, (lens["cache_past"] + S).astype(np.int32),
                              lens["total_abs"], window=w.window, cos_cache=cos, sin_cache=sin)
         dt = time.perf_counter() - t0
-        Lp = np.minimum(self.P[rows], w.capacity)
+        Lp = np.minimum(self.P[rows], self.C)
         fl = 4 * w.q_heads * w.head_dim * int(np.minimum(Lp + S, w.window).sum())
         return dt, fl
 
@@ -647,6 +652,61 @@ class WindowPrefillInplace(WindowPrefill):
         c["workload"] = self.w.name + "-inplace-stage"
         c["l2"] = "cache + stage rows ~0.6 GB per step > L2"
         return c
+
+
+class WindowPrefillHazard(WindowPrefill):
+    """The windowed chunked-prefill step as one kvc_window_prefill_step call:
+    only the batch rows whose eviction the chunk would see go through the
+    C + S stage; a row that evicts nothing (its cache not yet full) appends
+    in place and its attention reads the cache.  The timed kernel is the
+    whole call (row movement, attention, copy-back)."""
+    roofline_kernel = "kvc_window_prefill_step (the whole call)"
+
+    def __init__(self, dev, seed=0, with_kernels=True, chunk=64):
+        super().__init__(dev, seed=seed, with_kernels=with_kernels, chunk=chunk)
+        w, S, e, C = self.w, self.S, self.e, self.C
+        B, Hkv, D, W = w.batch, w.kv_heads, w.head_dim, w.window
+        self.traffic_key = ("kvc_prefill.cu", f"window_prefill_step@c{C}-chunk{S}")
+        Lp = np.minimum(self.P, C)
+        E = np.maximum(0, Lp + S - C)
+        L = Lp - E + S
+        staged = (E > 0) & (E > Lp - W + 1)
+        moved = (E > 0) & ~staged
+        self.n_staged, self.n_moved = int(staged.sum()), int(moved.sum())
+        # staged rows: seed (Lp rows) and copy-back (L rows), read + written;
+        # rows that move in place: Lp - E rows read + written
+        self.stage_bytes = int(2 * Hkv * D * e * int((staged * (2 * Lp + 2 * L)).sum() +
+                                                      (moved * 2 * (Lp - E)).sum()))
+        self.bytes_per_step = self.stage_bytes + self.kernel_bytes + 2 * 2 * B * Hkv * S * D * e
+        self.kernel_bytes = self.bytes_per_step
+        if with_kernels:
+            self.launches_per_step = 6 + (1 if self.pws is not None else 0)
+
+    def step(self, i):
+        K, w = self.K, self.w
+        K.kvc_seq_lengths(self.sk, self.S, self.C, 1, local_window_size=w.window, out=self.L,
+                          status=self.st)
+        self.kernel(i)
+
+    def kernel(self, i):
+        self.K.kvc_window_prefill_step(self.out, self.q, self.kc, self.vc, self.nk, self.nv,
+                                       self.L, 1, self.w.window, self.ks, self.vs,
+                                       rope=self.rope, status=self.st, workspace=self.pws)
+
+    def config(self):
+        c = super().config()
+        c["workload"] = self.w.name + ("-hazard-staging" if not self.slack else
+                                       f"-c{self.C}-hazard-staging")
+        c["rows_staged"], c["rows_moved_in_place"] = self.n_staged, self.n_moved
+        return c
+
+
+class WindowPrefillHazardSlack(WindowPrefillHazard):
+    """The same with C = W + 64: once a row's cache is full, a chunk of 64
+    evicts 64 rows that none of its queries sees (64 <= Lp - W + 1), so no
+    row needs the stage: the old rows move down in place and the attention
+    reads the cache."""
+    slack = 64
 
 
 class Scatter(Workload):
@@ -1123,6 +1183,8 @@ WORKLOADS = {"contig-decode": ContigDecode, "contig-decode-unfused": ContigDecod
              "window-decode-drift": WindowDecodeDrift, "window-decode-ring": WindowDecodeRing,
              "window-decode-hot": WindowDecodeHot, "window-prefill": WindowPrefill,
              "window-prefill-inplace": WindowPrefillInplace,
+             "window-prefill-hazard": WindowPrefillHazard,
+             "window-prefill-hazard-slack": WindowPrefillHazardSlack,
              "paged-decode-int8": PagedDecodeQ8,
              "scatter-functional": ScatterFunctional,
              "scatter": Scatter}

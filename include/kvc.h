@@ -18,6 +18,8 @@
  *                          cache or ring)
  *     kvc_window_decode_step  the same for a windowed cache
  *     kvc_gqa_prefill_chunk  multi-token GQA attention over staged rows
+ *     kvc_window_prefill_step  a windowed multi-token step that stages only
+ *                          the rows whose eviction its chunk would see
  *     kvc_tensor_scatter   the ONNX TensorScatter cache update (linear/circular)
  *
  * Conventions shared by every entry point
@@ -70,7 +72,7 @@
 extern "C" {
 #endif
 
-#define KVC_ABI_VERSION 6
+#define KVC_ABI_VERSION 7
 
 typedef enum {
     KVC_OK = 0,
@@ -591,6 +593,55 @@ kvc_status kvc_gqa_prefill_chunk(void *out, const void *q, const void *k_rows, c
                                  int local_window_size, float scale, const float *rope_cos,
                                  const float *rope_sin, int64_t rope_max_pos, void *workspace,
                                  size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * kvc_window_prefill_step -- one whole step of S new tokens on a windowed or
+ * drifting cache of C rows: append, chunk attention and row movement, with
+ * the C + S stage used only for the rows that need it ("GQA support
+ * sliding_window_cache", CPU commit: "Staging for hazardous steps"; the
+ * decision is taken per batch row on the device, from the lengths).
+ *
+ * Batch row b with Lp = len.cache_past[b], E = len.evict[b] is hazardous
+ * when E > 0 and E > Lp - W + 1: the rows [0, E) that the step evicts
+ * include one that its first query (at stage row Lp) still sees.
+ *   hazardous rows:  kvc_window_append's staged pair -- stage[0, Lp) =
+ *                    cache[0, Lp), the new rows at stage[Lp, Lp + S), the
+ *                    attention over the stage, cache[0, L) = stage[E, Lp + S);
+ *   the other rows:  cache rows [E, Lp) move to [0, Lp - E) in place, the new
+ *                    rows go to [Lp - E, L), and the attention reads the
+ *                    cache; no stage traffic (E = 0: only the new rows).
+ * Either way the cache ends byte for byte as kvc_window_append leaves it and
+ * the output is the attention of kvc_gqa_prefill_chunk over the stage (up to
+ * floating-point summation order).  A row rejected by kvc_seq_lengths
+ * (lengths -1) or for its RoPE range is left as kvc_window_append leaves it.
+ *
+ * out, q          device [batch, q_heads, new_tokens, head_dim].
+ * k_cache, v_cache  device [batch, kv_heads, capacity, head_dim].
+ * new_k, new_v    device [batch, kv_heads, new_tokens, head_dim].
+ * k_stage, v_stage  device [batch, kv_heads, capacity + new_tokens, head_dim]
+ *                 for S > 1 (only hazardous rows write or read them); may be
+ *                 NULL for S = 1, which never stages.
+ * len             kvc_seq_lengths outputs for this S, C, policy and window.
+ * windowed        KVC_WINDOWED or KVC_DRIFTING; 0 < local_window_size <= C
+ *                 (KVC_ERR_WINDOW).
+ * workspace       kvc_gqa_prefill_workspace_size(batch, q_heads, kv_heads,
+ *                 new_tokens, capacity, head_dim, dtype, local_window_size)
+ *                 bytes, or NULL (as kvc_gqa_prefill_chunk).
+ * Supported: KVC_BF16/KVC_F16 with head_dim in {64, 128, 256} and
+ * q_heads / kv_heads in {1, 2, 4, 8, 16}; KVC_F32 with head_dim <= 256
+ * (there every row of an S > 1 step is staged).  head_dim * element size a
+ * multiple of 16 bytes (KVC_ERR_UNSUPPORTED); buffers 16-byte aligned.
+ * Launches: the row movement before the attention (stage seed, in-place
+ * move, new rows), the attention (+ its merge), and the copy-back.
+ */
+kvc_status kvc_window_prefill_step(void *out, const void *q, void *k_cache, void *v_cache,
+                                   const void *new_k, const void *new_v, void *k_stage,
+                                   void *v_stage, kvc_lengths len, int batch, int q_heads,
+                                   int kv_heads, int new_tokens, int64_t capacity, int head_dim,
+                                   int dtype, int windowed, int local_window_size, float scale,
+                                   const float *rope_cos, const float *rope_sin,
+                                   int64_t rope_max_pos, void *workspace, size_t workspace_bytes,
+                                   int32_t *dev_status, void *stream);
 
 /* Bytes of workspace kvc_gqa_prefill_chunk uses for these sizes on the
  * current device (0: it would not split). */

@@ -101,17 +101,27 @@ struct PageTable {
     int64_t n_pages;
 };
 
+// the second destination of new_rows_kernel's hazard-step mode: rows that
+// step_staged() marks go to a stage of `rows` rows a head at cache_past + i
+struct AltRows {
+    void *k, *v;
+    int64_t rows;
+    int window;
+};
+
 // grid: x over (i, pair-vector) of one (b, head) slice, y = b * Hkv + h, z = K/V
 // dst row of token i, in a buffer with dst_rows rows/head: P + i (base_mode
 // 0), cache_past + i (1), (P + i) mod dst_rows for a ring (2, where only the
-// last dst_rows tokens are written), or row P + i of a paged cache (3)
+// last dst_rows tokens are written), row P + i of a paged cache (3), or
+// (4, kvc_window_prefill_step) cache_past - evict + i of the cache, or
+// cache_past + i of the stage `alt` for a row that step_staged() marks
 template <typename T, int VEC>
 __global__ void __launch_bounds__(128)
 new_rows_kernel(T *__restrict__ k_dst, T *__restrict__ v_dst, const T *__restrict__ new_k,
                 const T *__restrict__ new_v, kvc_lengths len, int kv_heads, int S, int D,
                 int64_t dst_rows, int base_mode, const float *__restrict__ cos_t,
                 const float *__restrict__ sin_t, int64_t rope_max_pos, int32_t *status,
-                PageTable pt)
+                PageTable pt, AltRows alt)
 {
     const int slice = blockIdx.y;
     const int b = slice / kv_heads;
@@ -129,7 +139,17 @@ new_rows_kernel(T *__restrict__ k_dst, T *__restrict__ v_dst, const T *__restric
     const bool ring = base_mode == 2, paged = base_mode == 3;
     const bool lead = threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0 &&
                       slice % kv_heads == 0;
-    const int base = base_mode == 1 ? len.cache_past[b] : P;
+    int base = base_mode == 1 ? len.cache_past[b] : P;
+    if (base_mode == 4) {
+        base = len.cache_past[b];
+        if (kvc::step_staged(base, len.evict[b], alt.window)) {
+            k_dst = static_cast<T *>(alt.k);
+            v_dst = static_cast<T *>(alt.v);
+            dst_rows = alt.rows;
+        } else {
+            base -= len.evict[b];
+        }
+    }
     if (base < 0 || (!ring && (int64_t)base + S > dst_rows)) {
         // lengths computed for another capacity: refuse rather than overrun
         if (lead)
@@ -178,19 +198,23 @@ new_rows_kernel(T *__restrict__ k_dst, T *__restrict__ v_dst, const T *__restric
 // dst.  copy_back = 0: stage seed, src0 = 0, n = Lp.  copy_back = 1: src0 = E,
 // n = L.  Row counts come from the device lengths; the grid covers the
 // largest possible range.
+// hazard_w > 0 (kvc_window_prefill_step): only the rows step_staged() marks
+// for that window.
 template <typename V>
 __global__ void __launch_bounds__(256)
 copy_range_kernel(char *__restrict__ k_dst, char *__restrict__ v_dst,
                   const char *__restrict__ k_src, const char *__restrict__ v_src,
                   kvc_lengths len, int kv_heads, int64_t row_bytes, int64_t dst_rows,
                   int64_t src_rows, int copy_back, int64_t rope_limit_rows, int S,
-                  int32_t *status)
+                  int32_t *status, int hazard_w)
 {
     const int slice = blockIdx.y;
     const int b = slice / kv_heads;
     const bool is_k = blockIdx.z == 0;
     const int L = len.cache_total[b];
     if (L < 0)
+        return;
+    if (hazard_w > 0 && !kvc::step_staged(len.cache_past[b], len.evict[b], hazard_w))
         return;
     // a row rejected for its RoPE range is rejected as a whole
     if (rope_limit_rows >= 0 && (int64_t)len.past_abs[b] + S > rope_limit_rows)
@@ -456,10 +480,13 @@ constexpr int kShiftSlots = 6;
 constexpr int kShiftChunk = 32768;
 constexpr int kShiftSmem = kShiftSlots * kShiftChunk + kShiftSlots * 8 + 128;
 
+// pre_w > 0 (kvc_window_prefill_step, before the new rows are written): the
+// rows step_staged() leaves to the cache move [E, Lp) to [0, Lp - E) of a
+// cache of rows_per_head = C rows a head, the others stay.
 __global__ void __launch_bounds__(32)
 shift_rows_kernel(char *__restrict__ k_rows, char *__restrict__ v_rows, kvc_lengths len,
                   int kv_heads, int64_t row_bytes, int64_t rows_per_head, int S,
-                  int64_t rope_limit_rows, int32_t *status)
+                  int64_t rope_limit_rows, int32_t *status, int pre_w)
 {
     extern __shared__ uint8_t shift_smem_raw[];
     if (threadIdx.x != 0)
@@ -475,12 +502,18 @@ shift_rows_kernel(char *__restrict__ k_rows, char *__restrict__ v_rows, kvc_leng
         return;
     const int64_t E = len.evict[b];
     const int64_t Lp = len.cache_past[b];
-    if (E < 0 || Lp < 0 || Lp + S > rows_per_head || E + L != Lp + S) {
+    if (E < 0 || Lp < 0 || E + L != Lp + S ||
+        (pre_w > 0 ? L > rows_per_head : Lp + S > rows_per_head)) {
         if (is_k && slice % kv_heads == 0)
             kvc::raise_status(status, KVC_DEV_CAPACITY);
         return;
     }
-    if (E == 0 || L == 0)
+    if (pre_w > 0 && kvc::step_staged(Lp, E, pre_w))
+        return;  // a staged row: its rows move in the copy-back
+    // rows that move: the L rows of the stage held in place, or the Lp - E
+    // old rows that stay in the cache
+    const int64_t nrows = pre_w > 0 ? Lp - E : L;
+    if (E == 0 || nrows == 0)
         return;  // the rows are already in place
     uint8_t *ring = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(shift_smem_raw) + 127) & ~uintptr_t(127));
@@ -490,7 +523,7 @@ shift_rows_kernel(char *__restrict__ k_rows, char *__restrict__ v_rows, kvc_leng
     kvc::fence_mbar_init();
     char *dst = (is_k ? k_rows : v_rows) + (int64_t)slice * rows_per_head * row_bytes;
     const char *src = dst + E * row_bytes;
-    const int64_t n = (int64_t)L * row_bytes;
+    const int64_t n = nrows * row_bytes;
     const int64_t nchunks = (n + kShiftChunk - 1) / kShiftChunk;
     auto chunk_bytes = [&](int64_t c) -> uint32_t {
         const int64_t rest = n - c * kShiftChunk;
@@ -603,12 +636,14 @@ quantize_pages_kernel(const T *__restrict__ k_pool, const T *__restrict__ v_pool
     }
 }
 
+// hazard_w > 0: the rows of kvc_window_prefill_step with that window (a
+// windowed cache and S > 1; see kvc_host::hazard_rows)
 template <typename T>
 kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const void *new_v,
                         void *k_stage, void *v_stage, const kvc_lengths &len, int batch,
                         int kv_heads, int S, int64_t C, int D, int windowed, int phase,
                         const float *cos_t, const float *sin_t, int64_t rope_max_pos,
-                        int32_t *status, cudaStream_t stream)
+                        int32_t *status, cudaStream_t stream, int hazard_w = 0)
 {
     constexpr int VEC = 16 / sizeof(T);
     const int slices = batch * kv_heads;
@@ -618,7 +653,8 @@ kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const v
     const T *nk = static_cast<const T *>(new_k);
     const T *nv = static_cast<const T *>(new_v);
     auto launch_new_rows = [&](T *kd, T *vd, int64_t dst_rows, int base_mode,
-                               PageTable pt = PageTable{nullptr, 0, 0, 0}) {
+                               PageTable pt = PageTable{nullptr, 0, 0, 0},
+                               AltRows alt = AltRows{nullptr, nullptr, 0, 0}) {
         const int pairs = vec_ok ? D / (2 * VEC) : D / 2;
         const int64_t work = (int64_t)S * pairs;
         int gx = (int)((work + 127) / 128);
@@ -627,14 +663,16 @@ kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const v
         if (vec_ok)
             new_rows_kernel<T, VEC><<<grid, 128, 0, stream>>>(kd, vd, nk, nv, len, kv_heads, S, D,
                                                               dst_rows, base_mode, cos_t,
-                                                              sin_t, rope_max_pos, status, pt);
+                                                              sin_t, rope_max_pos, status, pt,
+                                                              alt);
         else
             new_rows_kernel<T, 1><<<grid, 128, 0, stream>>>(kd, vd, nk, nv, len, kv_heads, S, D,
                                                             dst_rows, base_mode, cos_t,
-                                                            sin_t, rope_max_pos, status, pt);
+                                                            sin_t, rope_max_pos, status, pt,
+                                                            alt);
     };
     auto launch_copy = [&](char *kd, char *vd, const char *ks, const char *vs, int64_t dst_rows,
-                           int64_t src_rows, int copy_back, int64_t max_rows) {
+                           int64_t src_rows, int copy_back, int64_t max_rows, int hazard_w = 0) {
         const int64_t row_bytes = (int64_t)D * sizeof(T);
         const int64_t max_v = max_rows * row_bytes / 16;
         int gx = (int)((max_v + 511) / 512);
@@ -645,12 +683,13 @@ kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const v
         if (row_bytes % 16 == 0)
             copy_range_kernel<uint4><<<grid, 256, 0, stream>>>(kd, vd, ks, vs, len, kv_heads,
                                                                row_bytes, dst_rows, src_rows,
-                                                               copy_back, rope_rows, S, status);
+                                                               copy_back, rope_rows, S, status,
+                                                               hazard_w);
         else
             copy_range_kernel<uint32_t><<<grid, 256, 0, stream>>>(kd, vd, ks, vs, len, kv_heads,
                                                                   row_bytes, dst_rows, src_rows,
                                                                   copy_back, rope_rows, S,
-                                                                  status);
+                                                                  status, hazard_w);
     };
 
     if (windowed == KVC_CONTIGUOUS || windowed == KVC_RING) {
@@ -691,6 +730,21 @@ kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const v
                                    rope_max_pos, status) != cudaSuccess)
                 return KVC_ERR_CUDA;
         }
+    } else if (hazard_w > 0 && phase == KVC_APPEND) {
+        // kvc_window_prefill_step: staged rows seed the stage; the others
+        // move their old rows down in the cache; then every row's new rows
+        // go where its attention will read them
+        launch_copy(static_cast<char *>(k_stage), static_cast<char *>(v_stage),
+                    reinterpret_cast<const char *>(kc), reinterpret_cast<const char *>(vc), C + S,
+                    C, 0, C, hazard_w);
+        if (cudaFuncSetAttribute(shift_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kShiftSmem) != cudaSuccess)
+            return KVC_ERR_CUDA;
+        shift_rows_kernel<<<dim3(slices, 2), 32, kShiftSmem, stream>>>(
+            reinterpret_cast<char *>(kc), reinterpret_cast<char *>(vc), len, kv_heads,
+            (int64_t)D * sizeof(T), C, S, cos_t ? rope_max_pos : -1, status, hazard_w);
+        launch_new_rows(kc, vc, C, 4, PageTable{nullptr, 0, 0, 0},
+                        AltRows{k_stage, v_stage, C + S, hazard_w});
     } else if (phase == KVC_APPEND) {
         launch_copy(static_cast<char *>(k_stage), static_cast<char *>(v_stage),
                     reinterpret_cast<const char *>(kc), reinterpret_cast<const char *>(vc), C + S,
@@ -699,7 +753,7 @@ kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const v
     } else {
         launch_copy(reinterpret_cast<char *>(kc), reinterpret_cast<char *>(vc),
                     static_cast<const char *>(k_stage), static_cast<const char *>(v_stage), C,
-                    C + S, 1, C);
+                    C + S, 1, C, hazard_w);
     }
     return kvc_host::launch_status();
 }
@@ -726,11 +780,11 @@ kvc_status append_stage_rows(void *k_rows, void *v_rows, const void *new_k, cons
     if (vec_ok)
         new_rows_kernel<T, VEC><<<grid, 128, 0, stream>>>(kd, vd, nk, nv, len, kv_heads, S, D,
                                                           rows_per_head, 1, cos_t, sin_t,
-                                                          rope_max_pos, status, none);
+                                                          rope_max_pos, status, none, AltRows{});
     else
         new_rows_kernel<T, 1><<<grid, 128, 0, stream>>>(kd, vd, nk, nv, len, kv_heads, S, D,
                                                         rows_per_head, 1, cos_t, sin_t,
-                                                        rope_max_pos, status, none);
+                                                        rope_max_pos, status, none, AltRows{});
     return kvc_host::launch_status();
 }
 
@@ -755,11 +809,11 @@ kvc_status paged_append_typed(void *k_pool, void *v_pool, const void *new_k, con
     if (vec_ok)
         new_rows_kernel<T, VEC><<<grid, 128, 0, stream>>>(kp, vp, nk, nv, len, kv_heads, S, D,
                                                           capacity, 3, cos_t, sin_t,
-                                                          rope_max_pos, status, pt);
+                                                          rope_max_pos, status, pt, AltRows{});
     else
         new_rows_kernel<T, 1><<<grid, 128, 0, stream>>>(kp, vp, nk, nv, len, kv_heads, S, D,
                                                         capacity, 3, cos_t, sin_t, rope_max_pos,
-                                                        status, pt);
+                                                        status, pt, AltRows{});
     return kvc_host::launch_status();
 }
 
@@ -890,7 +944,7 @@ KVC_API kvc_status kvc_window_append_inplace(void *k_rows, void *v_rows, const v
     shift_rows_kernel<<<dim3(slices, 2), 32, kShiftSmem, stream>>>(
         static_cast<char *>(k_rows), static_cast<char *>(v_rows), len, kv_heads,
         (int64_t)head_dim * eb, rows_per_head, new_tokens, rope_cos ? rope_max_pos : -1,
-        dev_status);
+        dev_status, 0);
     return kvc_host::launch_status();
 }
 
@@ -1034,3 +1088,27 @@ KVC_API kvc_status kvc_paged_append(void *k_pool, void *v_pool, const void *new_
                                           rope_max_pos, dev_status, st);
     }
 }
+
+namespace kvc_host {
+
+kvc_status hazard_rows(void *k_cache, void *v_cache, const void *new_k, const void *new_v,
+                       void *k_stage, void *v_stage, const kvc_lengths &len, int batch,
+                       int kv_heads, int S, int64_t C, int D, int dtype, int window, int phase,
+                       const float *cos_t, const float *sin_t, int64_t rope_max_pos,
+                       int32_t *status, cudaStream_t stream)
+{
+    switch (dtype) {
+    case KVC_BF16:
+        return append_typed<__nv_bfloat16>(k_cache, v_cache, new_k, new_v, k_stage, v_stage, len,
+                                           batch, kv_heads, S, C, D, KVC_WINDOWED, phase, cos_t,
+                                           sin_t, rope_max_pos, status, stream, window);
+    case KVC_F16:
+        return append_typed<__half>(k_cache, v_cache, new_k, new_v, k_stage, v_stage, len, batch,
+                                    kv_heads, S, C, D, KVC_WINDOWED, phase, cos_t, sin_t,
+                                    rope_max_pos, status, stream, window);
+    default:
+        return KVC_ERR_UNSUPPORTED;
+    }
+}
+
+} // namespace kvc_host

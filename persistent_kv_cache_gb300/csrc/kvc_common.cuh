@@ -73,6 +73,17 @@ __host__ __device__ __forceinline__ void cache_lengths(int policy, int64_t T, in
     }
 }
 
+// Does a windowed step of S new tokens need the C + S stage ("GQA support
+// sliding_window_cache", CPU commit: staging for hazardous steps)?  Its first
+// query (row Lp of the stage) sees rows from Lp - W + 1 on; the step evicts
+// rows [0, E).  When none of those is visible (E <= Lp - W + 1, E = 0
+// included), the rows can move first and the chunk attend over the cache
+// itself; otherwise the stage keeps the evicted rows for the attention.
+__host__ __device__ __forceinline__ bool step_staged(int64_t Lp, int64_t E, int64_t W)
+{
+    return E > 0 && E > Lp - W + 1;
+}
+
 // --------------------------------------------------------------------------
 // element types
 // --------------------------------------------------------------------------
@@ -342,6 +353,17 @@ inline bool lengths_ok(const kvc_lengths &l)
 
 // number of SMs of the current device (cached per device)
 int sm_count();
+
+// The row movement of kvc_window_prefill_step (kvc_cache.cu), before the
+// chunk attention (phase KVC_APPEND) or after it (KVC_COPY_BACK): rows that
+// step_staged() marks seed the stage / copy back from it as in
+// kvc_window_append; the others move rows [E, Lp) of the cache to [0, Lp - E)
+// in place and take the new rows at [Lp - E, L).
+kvc_status hazard_rows(void *k_cache, void *v_cache, const void *new_k, const void *new_v,
+                       void *k_stage, void *v_stage, const kvc_lengths &len, int batch,
+                       int kv_heads, int S, int64_t C, int D, int dtype, int window, int phase,
+                       const float *cos_t, const float *sin_t, int64_t rope_max_pos,
+                       int32_t *status, cudaStream_t stream);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point
 // (no link-time dependency on libcuda)

@@ -262,7 +262,36 @@ struct PrefillArgs {
     // prefill_combine_kernel.  nsplit == 1: the output is written directly.
     int nsplit;
     float *ws_o, *ws_m, *ws_l;  // [nsplit][batch * q_heads * S] (x D for o)
+    // kvc_window_prefill_step (hazard_w = the window, else 0): a row that
+    // kvc::step_staged() marks reads the stage (tmap_k2 / tmap_v2, alt_rows
+    // rows a head, its chunk at rows [Lp, Lp + S)); any other row was moved
+    // and appended in the cache itself (rows_per_head = C rows a head, its
+    // chunk at rows [Lp - E, L))
+    int hazard_w;
+    int64_t alt_rows;
 };
+
+// The rows the chunk of batch row b attends: the row of its first query (a
+// position P at row Lp, so key row r holds position P - Lp + r), the row
+// pitch of the buffer it reads and whether that buffer is the stage.  False
+// when the lengths do not fit that buffer.
+__device__ __forceinline__ bool chunk_rows(const PrefillArgs &a, int b, int &Lp, int64_t &pitch,
+                                           bool &alt)
+{
+    Lp = a.len.cache_past[b];
+    pitch = a.rows_per_head;
+    alt = false;
+    if (a.hazard_w > 0) {
+        const int E = a.len.evict[b];
+        if (kvc::step_staged(Lp, E, a.hazard_w)) {
+            alt = true;
+            pitch = a.alt_rows;
+        } else {
+            Lp -= E;
+        }
+    }
+    return Lp >= 0 && (int64_t)Lp + a.S <= pitch;
+}
 
 template <int D> struct PrefillSmem {
     // A TMA operation costs about the same for 16 KB as for 32 KB, so each
@@ -348,6 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v,
+                  const __grid_constant__ CUtensorMap tmap_k2,
+                  const __grid_constant__ CUtensorMap tmap_v2,
                   const __grid_constant__ CUtensorMap tmap_o, const PrefillArgs a)
 {
     using SM = PrefillSmem<D>;
@@ -409,14 +440,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         leave();
         return;
     }
-    const int Lp = a.len.cache_past[b];
+    int Lp;
+    int64_t pitch;
+    bool alt;
     const int P = a.len.past_abs[b];
-    if (Lp < 0 || (int64_t)Lp + S > a.rows_per_head) {
+    if (!chunk_rows(a, b, Lp, pitch, alt)) {
         if (threadIdx.x == 0 && qblk == 0 && kvh == 0)
             kvc::raise_status(a.status, KVC_DEV_CAPACITY);
         leave();
         return;
     }
+    const CUtensorMap *map_k = alt ? &tmap_k2 : &tmap_k;
+    const CUtensorMap *map_v = alt ? &tmap_v2 : &tmap_v;
     if (a.cos_t && (int64_t)P + S > a.rope_max_pos) {
         if (threadIdx.x == 0 && qblk == 0 && kvh == 0)
             kvc::raise_status(a.status, KVC_DEV_ROPE_RANGE);
@@ -457,7 +492,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     lo += t0 * kBN;
     const int ntiles = t1 - t0;
     const int nslabs = 2 * ntiles * NST;
-    const int64_t row_base = ((int64_t)b * a.kv_heads + kvh) * a.rows_per_head;
+    const int64_t row_base = ((int64_t)b * a.kv_heads + kvh) * pitch;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSLAB; ++i) {
@@ -488,8 +523,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         // one 3-D box per ring slot: a K slab is DB column blocks of 128 rows,
         // a V slab is KPS rows of every column block (128-byte swizzled rows)
         if (lane == 0) {
-            kvc::tma_prefetch_desc(&tmap_k);
-            kvc::tma_prefetch_desc(&tmap_v);
+            kvc::tma_prefetch_desc(map_k);
+            kvc::tma_prefetch_desc(map_v);
             int issued = 0;
             for (int q = 0; q < nslabs; ++q) {
                 const int slot = q % NSLAB;
@@ -504,9 +539,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 const int32_t y0 = (int32_t)(row_base + lo + tile * kBN);
                 kvc::mbar_arrive_expect_tx(&full[slot], SM::SLAB);
                 if (!is_v)
-                    kvc::tma_load_3d(dst, &tmap_k, 0, y0, sl * DB, &full[slot]);
+                    kvc::tma_load_3d(dst, map_k, 0, y0, sl * DB, &full[slot]);
                 else
-                    kvc::tma_load_3d(dst, &tmap_v, 0, y0 + sl * KPS, 0, &full[slot]);
+                    kvc::tma_load_3d(dst, map_v, 0, y0 + sl * KPS, 0, &full[slot]);
                 issued = q + 1;
             }
             if (*abort_flag) {
@@ -877,9 +912,11 @@ prefill_combine_kernel(const PrefillArgs a)
     const int L = a.len.cache_total[b];
     if (L < 0)
         return;
-    const int Lp = a.len.cache_past[b];
+    int Lp;
+    int64_t pitch;
+    bool alt;
     const int P = a.len.past_abs[b];
-    if (Lp < 0 || (int64_t)Lp + a.S > a.rows_per_head)
+    if (!chunk_rows(a, b, Lp, pitch, alt))
         return;
     if (a.cos_t && (int64_t)P + a.S > a.rope_max_pos)
         return;
@@ -934,12 +971,21 @@ size_t prefill_ws_bytes(int nsplit, int batch, int q_heads, int S, int head_dim)
     return (size_t)nsplit * batch * q_heads * S * (head_dim + 2) * sizeof(float);
 }
 
+// the second K/V source of kvc_window_prefill_step (hazard_w = the window;
+// 0 or NULL pointers: none)
+struct AltSource {
+    const void *k, *v;
+    int64_t rows;
+    int hazard_w;
+};
+
 template <typename T, int D>
 kvc_status launch_prefill_tc(void *out, const void *q, const void *k_rows, const void *v_rows,
                              int64_t R, const kvc_lengths &len, int batch, int q_heads,
                              int kv_heads, int S, int window, float scale, const float *cos_t,
                              const float *sin_t, int64_t rope_max_pos, void *workspace,
-                             size_t workspace_bytes, int32_t *status, cudaStream_t stream)
+                             size_t workspace_bytes, int32_t *status, cudaStream_t stream,
+                             const AltSource &alt)
 {
     using SM = PrefillSmem<D>;
     const uint64_t rows = (uint64_t)batch * kv_heads * R;
@@ -948,9 +994,18 @@ kvc_status launch_prefill_tc(void *out, const void *q, const void *k_rows, const
     const CUtensorMapDataType tt = std::is_same<T, __half>::value
                                        ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    CUtensorMap tq, tk, tv, to;
+    CUtensorMap tq, tk, tv, tk2, tv2, to;
+    // the stage, when the step has one (no stage: S = 1, no row is staged)
+    const bool has_alt = alt.hazard_w > 0 && alt.k && alt.v;
+    const int64_t R2 = has_alt ? alt.rows : R;
+    const uint64_t rows2 = (uint64_t)batch * kv_heads * R2;
+    if (rows2 > (uint64_t)INT32_MAX)
+        return KVC_ERR_SHAPE;
     if (!kvc_host::encode_3d_sw128(&tk, k_rows, rows, D, kBN, SM::DB, tt) ||
         !kvc_host::encode_3d_sw128(&tv, v_rows, rows, D, SM::KPS, D / 64, tt) ||
+        !kvc_host::encode_3d_sw128(&tk2, has_alt ? alt.k : k_rows, rows2, D, kBN, SM::DB, tt) ||
+        !kvc_host::encode_3d_sw128(&tv2, has_alt ? alt.v : v_rows, rows2, D, SM::KPS, D / 64,
+                                   tt) ||
         !kvc_host::encode_4d_blocks_sw128(&tq, q, (uint64_t)batch * q_heads, (uint64_t)S, D,
                                           sizeof(T), (uint32_t)(kBM / (q_heads / kv_heads)),
                                           (uint32_t)(q_heads / kv_heads), tt))
@@ -975,6 +1030,8 @@ kvc_status launch_prefill_tc(void *out, const void *q, const void *k_rows, const
     a.ws_l = a.ws_m ? a.ws_m + (int64_t)a.nsplit * rows_total : nullptr;
     a.S = S;
     a.rows_per_head = R;
+    a.hazard_w = alt.hazard_w > 0 ? alt.hazard_w : 0;
+    a.alt_rows = R2;
     a.window = window;
     a.scale_log2 = scale * kLog2e;
     a.cos_t = cos_t;
@@ -1005,7 +1062,7 @@ kvc_status launch_prefill_tc(void *out, const void *q, const void *k_rows, const
         return KVC_ERR_CUDA;
     const int qblocks = (S + a.qb_rows - 1) / a.qb_rows;
     dim3 grid(qblocks * a.nsplit, kv_heads, batch);
-    kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, a);
+    kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, tk2, tv2, to, a);
     if (a.nsplit > 1)
         prefill_combine_kernel<T, D><<<(unsigned)((rows_total + 3) / 4), 128, 0, stream>>>(a);
     return kvc_host::launch_status();
@@ -1015,18 +1072,19 @@ template <typename T>
 kvc_status dispatch_prefill16(int D, void *out, const void *q, const void *k, const void *v,
                               int64_t R, const kvc_lengths &len, int B, int Hq, int Hkv, int S,
                               int W, float scale, const float *cs, const float *sn, int64_t rmax,
-                              void *ws, size_t ws_bytes, int32_t *st, cudaStream_t stream)
+                              void *ws, size_t ws_bytes, int32_t *st, cudaStream_t stream,
+                              const AltSource &alt = AltSource{nullptr, nullptr, 0, 0})
 {
     switch (D) {
     case 64:
         return launch_prefill_tc<T, 64>(out, q, k, v, R, len, B, Hq, Hkv, S, W, scale, cs, sn,
-                                        rmax, ws, ws_bytes, st, stream);
+                                        rmax, ws, ws_bytes, st, stream, alt);
     case 128:
         return launch_prefill_tc<T, 128>(out, q, k, v, R, len, B, Hq, Hkv, S, W, scale, cs, sn,
-                                         rmax, ws, ws_bytes, st, stream);
+                                         rmax, ws, ws_bytes, st, stream, alt);
     case 256:
         return launch_prefill_tc<T, 256>(out, q, k, v, R, len, B, Hq, Hkv, S, W, scale, cs, sn,
-                                         rmax, ws, ws_bytes, st, stream);
+                                         rmax, ws, ws_bytes, st, stream, alt);
     default:
         return KVC_ERR_UNSUPPORTED;
     }
@@ -1107,4 +1165,115 @@ KVC_API kvc_status kvc_gqa_prefill_chunk(void *out, const void *q, const void *k
                                       q_heads, kv_heads, new_tokens, local_window_size, scale,
                                       rope_cos, rope_sin, rope_max_pos, workspace,
                                       workspace_bytes, dev_status, stream);
+}
+
+KVC_API kvc_status kvc_window_prefill_step(void *out, const void *q, void *k_cache, void *v_cache,
+                                           const void *new_k, const void *new_v, void *k_stage,
+                                           void *v_stage, kvc_lengths len, int batch,
+                                           int q_heads, int kv_heads, int new_tokens,
+                                           int64_t capacity, int head_dim, int dtype,
+                                           int windowed, int local_window_size, float scale,
+                                           const float *rope_cos, const float *rope_sin,
+                                           int64_t rope_max_pos, void *workspace,
+                                           size_t workspace_bytes, int32_t *dev_status,
+                                           void *stream_)
+{
+    const int eb = kvc_host::elem_bytes_of(dtype);
+    if (eb == 0)
+        return KVC_ERR_DTYPE;
+    if (batch < 0 || q_heads < 1 || kv_heads < 1 || q_heads % kv_heads != 0 || new_tokens < 1 ||
+        head_dim < 2 || (head_dim & 1))
+        return KVC_ERR_SHAPE;
+    if (windowed != KVC_WINDOWED && windowed != KVC_DRIFTING)
+        return KVC_ERR_UNSUPPORTED;
+    if (capacity < 1 || capacity + new_tokens > (int64_t)INT32_MAX)
+        return KVC_ERR_CAPACITY;
+    if (local_window_size < 1 || local_window_size > capacity)
+        return KVC_ERR_WINDOW;
+    if ((rope_cos == nullptr) != (rope_sin == nullptr))
+        return KVC_ERR_NULL;
+    if (rope_cos && rope_max_pos < 1)
+        return KVC_ERR_SHAPE;
+    const int g = q_heads / kv_heads;
+    if (dtype == KVC_F32) {
+        if (head_dim > 256)
+            return KVC_ERR_UNSUPPORTED;
+    } else if ((head_dim != 64 && head_dim != 128 && head_dim != 256) ||
+               (g != 1 && g != 2 && g != 4 && g != 8 && g != 16)) {
+        return KVC_ERR_UNSUPPORTED;
+    }
+    if (((int64_t)head_dim * eb) % 16 != 0)
+        return KVC_ERR_UNSUPPORTED;
+    if (batch == 0)
+        return KVC_OK;
+    const bool staged = new_tokens > 1;
+    if (!out || !q || !k_cache || !v_cache || !new_k || !new_v || !kvc_host::lengths_ok(len) ||
+        (staged && (!k_stage || !v_stage)))
+        return KVC_ERR_NULL;
+    for (const void *p : {(const void *)out, q, (const void *)k_cache, (const void *)v_cache,
+                          new_k, new_v, (const void *)(staged ? k_stage : nullptr),
+                          (const void *)(staged ? v_stage : nullptr)})
+        if (p && !kvc_host::aligned16(p))
+            return KVC_ERR_ALIGN;
+    if (rope_cos && (!kvc_host::aligned16(rope_cos) || !kvc_host::aligned16(rope_sin)))
+        return KVC_ERR_ALIGN;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return KVC_ERR_ALIGN;
+    const size_t cache_bytes = (size_t)batch * kv_heads * capacity * head_dim * eb;
+    if (kvc_host::overlaps(k_cache, cache_bytes, v_cache, cache_bytes))
+        return KVC_ERR_SHAPE;
+    if (staged) {
+        const size_t st = (size_t)batch * kv_heads * (capacity + new_tokens) * head_dim * eb;
+        if (kvc_host::overlaps(k_stage, st, v_stage, st) ||
+            kvc_host::overlaps(k_stage, st, k_cache, cache_bytes) ||
+            kvc_host::overlaps(v_stage, st, v_cache, cache_bytes) ||
+            kvc_host::overlaps(k_stage, st, v_cache, cache_bytes) ||
+            kvc_host::overlaps(v_stage, st, k_cache, cache_bytes))
+            return KVC_ERR_SHAPE;
+    }
+    if (scale == 0.f)
+        scale = 1.0f / sqrtf((float)head_dim);
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const int S = new_tokens, W = local_window_size;
+    kvc_status st;
+    if (dtype == KVC_F32) {
+        // the CUDA-core path: every row through the stage (S = 1: the
+        // in-place compaction and one query over the cache)
+        st = kvc_window_append(k_cache, v_cache, new_k, new_v, k_stage, v_stage, len, batch,
+                               kv_heads, S, capacity, head_dim, dtype, windowed, KVC_APPEND,
+                               rope_cos, rope_sin, rope_max_pos, dev_status, stream);
+        if (st != KVC_OK)
+            return st;
+        st = staged ? kvc_f32::launch(out, q, k_stage, v_stage, capacity + S, len, batch, q_heads,
+                                      kv_heads, S, head_dim, W, scale, rope_cos, rope_sin,
+                                      rope_max_pos, 1, dev_status, stream)
+                    : kvc_f32::launch(out, q, k_cache, v_cache, capacity, len, batch, q_heads,
+                                      kv_heads, 1, head_dim, W, scale, rope_cos, rope_sin,
+                                      rope_max_pos, 0, dev_status, stream);
+        if (st != KVC_OK || !staged)
+            return st;
+        return kvc_window_append(k_cache, v_cache, nullptr, nullptr, k_stage, v_stage, len, batch,
+                                 kv_heads, S, capacity, head_dim, dtype, windowed, KVC_COPY_BACK,
+                                 rope_cos, rope_sin, rope_max_pos, dev_status, stream);
+    }
+    st = kvc_host::hazard_rows(k_cache, v_cache, new_k, new_v, k_stage, v_stage, len, batch,
+                               kv_heads, S, capacity, head_dim, dtype, W, KVC_APPEND, rope_cos,
+                               rope_sin, rope_max_pos, dev_status, stream);
+    if (st != KVC_OK)
+        return st;
+    const AltSource alt{staged ? k_stage : nullptr, staged ? v_stage : nullptr, capacity + S, W};
+    st = dtype == KVC_BF16
+             ? dispatch_prefill16<__nv_bfloat16>(head_dim, out, q, k_cache, v_cache, capacity,
+                                                 len, batch, q_heads, kv_heads, S, W, scale,
+                                                 rope_cos, rope_sin, rope_max_pos, workspace,
+                                                 workspace_bytes, dev_status, stream, alt)
+             : dispatch_prefill16<__half>(head_dim, out, q, k_cache, v_cache, capacity, len,
+                                          batch, q_heads, kv_heads, S, W, scale, rope_cos,
+                                          rope_sin, rope_max_pos, workspace, workspace_bytes,
+                                          dev_status, stream, alt);
+    if (st != KVC_OK || !staged)
+        return st;
+    return kvc_host::hazard_rows(k_cache, v_cache, nullptr, nullptr, k_stage, v_stage, len, batch,
+                                 kv_heads, S, capacity, head_dim, dtype, W, KVC_COPY_BACK, rope_cos,
+                                 rope_sin, rope_max_pos, dev_status, stream);
 }

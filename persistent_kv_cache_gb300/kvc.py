@@ -38,8 +38,8 @@ EXPORTS = ("kvc_tensor_scatter", "kvc_seq_lengths", "kvc_window_append", "kvc_gq
            "kvc_window_decode_step_workspace_size",
            "kvc_paged_append", "kvc_gqa_decode_paged", "kvc_window_append_inplace",
            "kvc_quantize_pages", "kvc_gqa_decode_paged_q",
-           "kvc_gqa_prefill_chunk", "kvc_gqa_prefill_workspace_size", "kvc_status_string",
-           "kvc_abi_version")
+           "kvc_gqa_prefill_chunk", "kvc_gqa_prefill_workspace_size", "kvc_window_prefill_step",
+           "kvc_status_string", "kvc_abi_version")
 KVC_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 KVC_PAGE_QUANT = 0x40000000  # block-table flag: the entry names an int8 page
 
@@ -119,6 +119,8 @@ def library() -> ctypes.CDLL:
             "kvc_gqa_prefill_chunk": [P, P, P, P, I64, L, I, I, I, I, I, I, I, F, P, P, I64, P, SZ,
                                       P, P],
             "kvc_gqa_prefill_workspace_size": [I, I, I, I, I64, I, I, I],
+            "kvc_window_prefill_step": [P, P, P, P, P, P, P, P, L, I, I, I, I, I64, I, I, I, I,
+                                        F, P, P, I64, P, SZ, P, P],
             "kvc_status_string": [I],
             "kvc_abi_version": [],
         }
@@ -420,3 +422,25 @@ def kvc_status_string(code: int) -> str:
 
 def kvc_abi_version() -> int:
     return library().kvc_abi_version()
+
+
+def kvc_window_prefill_step(out, q, k_cache, v_cache, new_k, new_v, lengths, windowed,
+                            local_window_size, k_stage=None, v_stage=None, scale=0.0, rope=None,
+                            status=None, stream=None, workspace="auto"):
+    """One windowed S-token step that stages only the rows whose eviction its
+    chunk would see (include/kvc.h).  k_stage/v_stage: [B, Hkv, C + S, D]
+    (needed for S > 1).  workspace: "auto" allocates what the attention can
+    use, None runs it unsplit."""
+    B, Hq, S, D = q.shape
+    _, Hkv, C, _ = k_cache.shape
+    if isinstance(workspace, str):
+        n = library().kvc_gqa_prefill_workspace_size(B, Hq, Hkv, S, C, D, _dtype_code(q),
+                                                     local_window_size)
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+    cs, sn, rmax = _rope(rope)
+    _check("kvc_window_prefill_step", library().kvc_window_prefill_step(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(new_k), _ptr(new_v),
+        _ptr(k_stage), _ptr(v_stage), lengths.c(), B, Hq, Hkv, S, C, D, _dtype_code(q),
+        int(windowed), local_window_size, scale, cs, sn, rmax, _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _ptr(status), _stream(stream)))
+    return out

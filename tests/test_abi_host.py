@@ -45,7 +45,7 @@ def test_binding_rejects_host_tensors(kvc):
 
 
 def test_version_and_strings(kvc):
-    assert kvc.kvc_abi_version() == 6
+    assert kvc.kvc_abi_version() == 7
     assert kvc.kvc_status_string(0) == "ok"
     assert "window" in kvc.kvc_status_string(7)
 
@@ -295,3 +295,31 @@ def test_decode_paged_q_host_checks(kvc):
     assert f(*pools[:6], FAKE * 4 + 4, 8, *tail) == 4                # qparams alignment
     assert f(*pools[:4], 4 << 32, (4 << 32) + 16, pools[6], 8, *tail) == 2  # int8 pools overlap
     assert f(*pools, 8, *tail[:3], 48, *tail[4:]) == 2               # page not a multiple of 64
+
+
+def test_window_prefill_step_host_checks(kvc):
+    """kvc_window_prefill_step: policy, window, stage, shape and alignment
+    checks return before anything is enqueued."""
+    lib = kvc.library()
+    f = lib.kvc_window_prefill_step
+    L = _lengths(kvc)
+    FAR = FAKE << 12  # the stage: far from the cache pointers
+    # out, q, k_cache, v_cache, new_k, new_v, k_stage, v_stage
+    ptrs = [FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, FAR, FAR * 2]
+    # batch, q_heads, kv_heads, S, C, D, dtype, policy, W, scale, cos, sin, rmax
+    ok = [2, 8, 2, 16, 64, 64, 1, 1, 48, 0.0, None, None, 0]
+    tail = [None, 0, None, None]  # workspace, bytes, status, stream
+    call = lambda p, a: f(*p, L, *a, *tail)
+    assert call(ptrs, ok[:7] + [0] + ok[8:]) == 5                 # contiguous: not this call
+    assert call(ptrs, ok[:7] + [3] + ok[8:]) == 5                 # ring: not this call
+    assert call(ptrs, ok[:8] + [0] + ok[9:]) == 7                 # W < 1
+    assert call(ptrs, ok[:8] + [65] + ok[9:]) == 7                # W > C
+    assert call(ptrs[:6] + [None, None], ok) == 1                 # S > 1 without a stage
+    assert call(ptrs, ok[:3] + [0] + ok[4:]) == 2                 # S = 0
+    assert call(ptrs, ok[:6] + [9] + ok[7:]) == 3                 # dtype
+    assert call(ptrs, ok[:5] + [96] + ok[6:]) == 5                # head_dim 96 (16-bit)
+    assert call([FAKE + 8] + ptrs[1:], ok) == 4                   # out alignment
+    assert call(ptrs, ok[:4] + [0] + ok[5:]) == 6                 # C < 1
+    # the stage overlapping the cache
+    assert call(ptrs[:6] + [FAKE * 3, FAR * 2], ok) == 2
+    assert call(ptrs, [0] + ok[1:]) == 0                          # empty batch: nothing to do
