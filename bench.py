@@ -45,8 +45,9 @@ Other workloads (--workload):
                   decode + merge; the roofline kernel is the compaction
 
 The default one-GPU run also times window-prefill at S = 2048 and S = 64,
-window-decode, scatter-functional (S = 64), ring-decode-d256 and
-window-decode-d256, each as an
+window-decode, scatter-functional (S = 64), ring-decode-d256,
+window-decode-d256, paged-decode-int8 and window-prefill-hazard (S = 64),
+each as an
 entry of the line's "secondary" list with its own roofline, clocks and CPU
 baseline (--no-secondary leaves them out).  Before each timed region the
 step graph is replayed for --soak seconds (default 1) so that the clock
@@ -1244,7 +1245,8 @@ _MAX_STEPS = ("window-decode", "window-decode-unfused", "window-decode-drift",
 # "secondary" list: (workload, chunk)
 SECONDARY = (("window-prefill", 2048), ("window-prefill", 64), ("window-decode", None),
              ("scatter-functional", 64), ("ring-decode-d256", None),
-             ("window-decode-d256", None))
+             ("window-decode-d256", None), ("paged-decode-int8", None),
+             ("window-prefill-hazard", 64))
 
 
 def make_workload(name, dev, seed, chunk, n_steps):
