@@ -150,6 +150,34 @@ __device__ __forceinline__ void u8x4_to_pairs(uint32_t w, uint64_t off2, uint32_
     hi = Mma<T>::pack(f2, f3);
 }
 
+// f16: byte u under the high byte 0x64 is the half 1024 + u (spacing 1 in
+// [1024, 2048)), one byte permute for two codes, and one f16x2 subtraction
+// of off2 = (1024 + zp) x 2 leaves u - zp exactly -- the same halves as the
+// float route above, at a third of its ALU work
+template <>
+__device__ __forceinline__ void u8x4_to_pairs<__half>(uint32_t w, uint64_t off2, uint32_t &lo,
+                                                      uint32_t &hi)
+{
+    const uint32_t l = __byte_perm(w, 0x64646464u, 0x4140);
+    const uint32_t h = __byte_perm(w, 0x64646464u, 0x4342);
+    const uint32_t o = (uint32_t)off2;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(l), "r"(o));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(h), "r"(o));
+}
+
+// the per-tile constant off2 of u8x4_to_pairs<T> for a zero point zp
+// (an integer in [0, 255])
+template <typename T> __device__ __forceinline__ uint64_t q8_offset(float zp)
+{
+    if constexpr (std::is_same<T, __half>::value) {
+        const __half2 h = __float2half2_rn(1024.f + zp);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    } else {
+        const uint32_t f = __float_as_uint(8388608.f + zp);
+        return ((uint64_t)f << 32) | f;
+    }
+}
+
 // Attention state of one consumer warp over 64-row K/V tiles held in shared
 // memory (128-byte swizzled boxes of 64 columns, 8 KB per box).  The warp
 // owns rows [16 w, 16 w + 16) of every tile.  Those 16 keys are the M = 16
@@ -358,7 +386,7 @@ struct GroupAttn {
     // D / 2 bytes of each are the exact A fragments of its MMAs, as 16-byte
     // pieces interleaved across the warp (piece i of lane l at i * 512 +
     // l * 16), piece i holding 16-column blocks 2 i and 2 i + 1.  They become
-    // the integers u - zp in registers (koff2 / voff2 = (2^23 + zp) x 2);
+    // the integers u - zp in registers (koff2 / voff2 from q8_offset);
     // the scores take the page's K scale (folded into scale_log2) and the
     // probabilities its V scale.  Every converted value is finite, and P is 0
     // past `hi`, so the rows past the split end need no zeroing.
@@ -1038,11 +1066,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const float vs = __shfl_sync(0xffffffffu, my_p[2], pi);
             const float vz = __shfl_sync(0xffffffffu, my_p[3], pi);
             if (my_lo < my_valid) {
-                const uint32_t ko = __float_as_uint(8388608.f + kz);
-                const uint32_t vo = __float_as_uint(8388608.f + vz);
                 const uint32_t kq = kvc::smem_u32(kgen) + warp * 16 * D;
                 ga.tile_q8(kq, kq + kTile * D, lane, my_lo, my_valid, a.scale_log2 * ks, vs,
-                           ((uint64_t)ko << 32) | ko, ((uint64_t)vo << 32) | vo);
+                           q8_offset<T>(kz), q8_offset<T>(vz));
             }
         } else if (my_valid > 0) {
             if (my_valid < 16) {

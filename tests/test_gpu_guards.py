@@ -11,7 +11,8 @@ Families: seq_lengths; TensorScatter in place and functional; the append
 staging seed and copy-back); the in-place stage; the paged append and the
 int8 page conversion; decode (plain, ring, paged, int8 pages, no-alloc) with
 its workspace; the fused steps (contiguous, ring, small and large windows);
-the chunk attention with its workspace.  Tiny shapes, plus the full-size
+the chunk attention with its workspace; the windowed step that stages
+only hazardous rows (kvc_window_prefill_step).  Tiny shapes, plus the full-size
 workloads of the contiguous decode step, the chunked prefill (S = 64) and
 the functional TensorScatter.
 """
@@ -342,3 +343,40 @@ def test_full_size_functional_scatter(K):
     present = Guarded(shape, torch.bfloat16)
     K.kvc_tensor_scatter(present.t, past, upd, wi, mode=K.KVC_CIRCULAR)
     present.check("present")
+
+
+@pytest.mark.parametrize("policy,D,C,W,S", [(1, 64, 48, 40, 32), (2, 128, 48, 40, 5),
+                                           (1, 256, 4160, 4096, 64), (2, 64, 40, 24, 1)])
+def test_window_prefill_step(K, policy, D, C, W, S):
+    """kvc_window_prefill_step: the rows it stages (seed, attention,
+    copy-back), the rows it moves and appends in place, and its workspace --
+    batch rows that fill, that evict only what no query sees and that stage,
+    over consecutive steps."""
+    B, Hkv, g = 3, 2, 2
+    Hq = Hkv * g
+    T = np.array([0, C - S, 3 * C + 7])
+    st = status()
+    rd = rope(T.max() + 3 * S + 2, D)
+    kc = guarded(synth.normal((B, Hkv, C, D), 12, 1))
+    vc = guarded(synth.normal((B, Hkv, C, D), 12, 2))
+    ks = Guarded((B, Hkv, C + S, D), torch.bfloat16) if S > 1 else None
+    vs = Guarded((B, Hkv, C + S, D), torch.bfloat16) if S > 1 else None
+    out = Guarded((B, Hq, S, D), torch.bfloat16)
+    L, gl = glengths(K, B)
+    n = K.library().kvc_gqa_prefill_workspace_size(B, Hq, Hkv, S, C, D, K.KVC_BF16, W)
+    gws = Guarded((max(n, 256),), torch.uint8)
+    for s in range(3):
+        sk = torch.from_numpy((T + (s + 1) * S - 1).astype(np.int32)).to(dev())
+        K.kvc_seq_lengths(sk, S, C, policy, local_window_size=W, out=L, status=st)
+        K.kvc_window_prefill_step(out.t, synth.normal((B, Hq, S, D), 12, 10 + s).to(dev()),
+                                  kc.t, vc.t, synth.normal((B, Hkv, S, D), 12, 20 + s).to(dev()),
+                                  synth.normal((B, Hkv, S, D), 12, 30 + s).to(dev()), L, policy,
+                                  W, None if ks is None else ks.t, None if vs is None else vs.t,
+                                  rope=rd, status=st, workspace=gws.t if n else None)
+    for gd, what in ((kc, "k cache"), (vc, "v cache"), (out, "out"), (gl, "lengths"),
+                     (gws, "workspace")):
+        gd.check(what)
+    if ks is not None:
+        ks.check("k stage")
+        vs.check("v stage")
+    assert st.item() == 0

@@ -160,29 +160,38 @@ def _quantize_table(K, table, n_rows, P, kp_d, vp_d, qk, qv, qp, ks, kz, ku, vs,
     return new
 
 
-@pytest.mark.parametrize("D,zp,uns", [(128, 0, False), (64, 128, True), (256, 3, False)])
-def test_grid_values_equal_16bit_decode(K, D, zp, uns):
-    """Every value k * 2^-5 (|k| <= 100): the int8 pages reconstruct exactly
-    and the int8 decode equals the 16-bit paged decode bit for bit."""
+@pytest.mark.parametrize("D,zp,uns,dtype,vsc", [(128, 0, False, torch.bfloat16, 1 / 32),
+                                                (64, 128, True, torch.bfloat16, 1 / 32),
+                                                (256, 3, False, torch.bfloat16, 1 / 32),
+                                                (128, 7, False, torch.float16, 1.0),
+                                                (64, 150, True, torch.float16, 1.0)])
+def test_grid_values_equal_16bit_decode(K, D, zp, uns, dtype, vsc):
+    """K values k * 2^-5 and V values k * vsc (|k| <= 100): the int8 pages
+    reconstruct exactly and the int8 decode equals the 16-bit paged decode
+    bit for bit (bf16 pages: the codes reach the MMAs through float; fp16:
+    through the half 1024 + code).  The int8 path applies a page's V scale to
+    the probabilities before they are packed; in fp16 a small product falls
+    below the normal range and rounds differently from the unscaled
+    probability of 16-bit pages, so the fp16 cases keep a V scale of 1."""
     B, Hkv, g, P, max_pages = 4, 2, 4, 64, 8
     Hq = Hkv * g
     n_pool = B * max_pages + 3
-    grid = lambda s: (synth.randint(-100, 101, (n_pool, Hkv, P, D), 62, s).float() / 32).to(
-        torch.bfloat16)
-    kp, vp, table = _paged_setup(B, Hkv, D, P, max_pages, 3, 62, torch.bfloat16,
-                                 values=(grid(1), grid(2)))
+    grid = lambda s, sc: (synth.randint(-100, 101, (n_pool, Hkv, P, D), 62, s).float() *
+                          sc).to(dtype)
+    kp, vp, table = _paged_setup(B, Hkv, D, P, max_pages, 3, 62, dtype,
+                                 values=(grid(1, 1 / 32), grid(2, vsc)))
     gk, gv = kp.to(dev()), vp.to(dev())
     T = np.array([1, 64, 300, 512])
     qk, qv, qp = _q8_pools(B * max_pages, Hkv, P, D)
-    qtab = _quantize_table(K, table, T, P, gk, gv, qk, qv, qp, 1 / 32, zp, uns, 1 / 32, zp, uns,
+    qtab = _quantize_table(K, table, T, P, gk, gv, qk, qv, qp, 1 / 32, zp, uns, vsc, zp, uns,
                            keep_last=False)
     cos, sin = synth.rope_cache(1024, D)
     rope_d = (cos.to(dev()), sin.to(dev()))
-    q = synth.normal((B, Hq, 1, D), 62, 3).to(dev())
+    q = synth.normal((B, Hq, 1, D), 62, 3, dtype).to(dev())
     st = status()
     L = K.kvc_seq_lengths(torch.from_numpy((T - 1).astype(np.int32)).to(dev()), 1,
                           max_pages * P, K.KVC_CONTIGUOUS, status=st)
-    o16 = torch.empty(B, Hq, 1, D, dtype=torch.bfloat16, device=dev())
+    o16 = torch.empty(B, Hq, 1, D, dtype=dtype, device=dev())
     o8 = torch.full_like(o16, float("nan"))
     K.kvc_gqa_decode_paged(o16, q, gk, gv, torch.from_numpy(table).to(dev()), L, rope=rope_d,
                            status=st)
