@@ -169,3 +169,43 @@ def test_window_prefill_workload_s64(K, orc):
     staged, _ = _step(K, orc, gk, gv, wk, wv, T, S, C, W, 1, torch.bfloat16, 72, (cos, sin), Hq,
                       sample=(0, 31, 32, 63))
     assert not staged[0] and not staged[1] and staged[2]
+
+
+def test_rejected_rows_untouched(K, orc):
+    """A row whose seqlens_k is out of range and a row past the rotary table
+    are left as they were (cache and stage) and flagged; the valid rows of
+    the same call are exact."""
+    B, Hkv, g, D, C, W, S = 3, 2, 2, 64, 48, 40, 16
+    kc = synth.normal((B, Hkv, C, D), 90, 1)
+    vc = synth.normal((B, Hkv, C, D), 90, 2)
+    nk = synth.normal((B, Hkv, S, D), 90, 3)
+    nv = synth.normal((B, Hkv, S, D), 90, 4)
+    q = synth.normal((B, Hkv * g, S, D), 90, 5)
+    cos, sin = synth.rope_cache(200, D)
+    sk = np.array([100 + S - 1, S - 2, 400 + S - 1], np.int32)  # valid, T < S, past the table
+    st = status()
+    gk, gv = kc.to(dev()), vc.to(dev())
+    L = K.kvc_seq_lengths(torch.from_numpy(sk).to(dev()), S, C, 1, local_window_size=W, status=st)
+    ks = torch.zeros(B, Hkv, C + S, D, dtype=torch.bfloat16, device=dev())
+    vs = torch.zeros_like(ks)
+    out = torch.zeros(B, Hkv * g, S, D, dtype=torch.bfloat16, device=dev())
+    K.kvc_window_prefill_step(out, q.to(dev()), gk, gv, nk.to(dev()), nv.to(dev()), L, 1, W, ks,
+                              vs, rope=(cos.to(dev()), sin.to(dev())), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == K.KVC_DEV_SEQLEN_RANGE | K.KVC_DEV_ROPE_RANGE, st.item()
+    for b in (1, 2):
+        assert torch.equal(gk[b].cpu(), kc[b]) and torch.equal(gv[b].cpu(), vc[b]), b
+        assert not ks[b].any() and not vs[b].any(), b
+    # the valid row against the oracle
+    lens = orc.seq_lengths(sk[:1], S, C, 1, W)
+    wk, wv = synth.bits(kc[:1]).copy(), synth.bits(vc[:1]).copy()
+    wks = np.zeros((1, Hkv, C + S, D), np.uint16)
+    wvs = np.zeros_like(wks)
+    orc.window_append(wk, wv, synth.bits(nk[:1]), synth.bits(nv[:1]), lens, 1, cos.numpy(),
+                      sin.numpy(), wks, wvs)
+    assert_bytes_equal(gk[:1], wk, "k cache row 0")
+    assert_bytes_equal(gv[:1], wv, "v cache row 0")
+    want, _ = orc.gqa_attention(synth.bits(q[:1]), wks, wvs,
+                                (lens["cache_past"] + S).astype(np.int32), lens["total_abs"],
+                                window=W, cos_cache=cos.numpy(), sin_cache=sin.numpy())
+    assert_close(out[:1], want, 2e-2, "row 0")
