@@ -9,7 +9,9 @@ around the capacity and the window, for
 * kvc_decode_step (contiguous and ring) and kvc_window_decode_step (every
   windowed policy, small windows);
 * multi-token chunks (kvc_gqa_prefill_chunk over the stage or a contiguous
-  cache, split and unsplit), sampled queries of every row.
+  cache, split and unsplit), sampled queries of every row;
+* whole windowed steps through kvc_window_prefill_step (only hazardous rows
+  staged), two in a row.
 
 Every cache byte is compared; attention within 2e-2 (bf16/fp16).
 """
@@ -296,3 +298,76 @@ def test_fuzz_prefill_chunks(K, orc, seed):
         want, _ = orc.gqa_attention(qi, rk, rv, n, tot, window=Wd, cos_cache=cn, sin_cache=sn)
         assert_close(out[:, :, i:i + 1], want, 2e-2,
                      f"prefill query {i} {(D, g, Hkv, B, C, W, S, policy, ws)}")
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_fuzz_window_prefill_step(K, orc, seed):
+    """Random steps of kvc_window_prefill_step: head_dim {64, 128, 256},
+    group {1, 2, 4, 8, 16}, windowed or drifting, capacities with and
+    without slack above the window, chunks from 1 token to past the gap and
+    the capacity, totals that fill, evict visibly and evict invisibly; two
+    steps in a row, with and without the KV-split workspace."""
+    rng = np.random.default_rng(9100 + seed)
+    D = int(rng.choice([64, 128, 256]))
+    g = int(rng.choice([1, 2, 4, 8, 16]))
+    Hkv = int(rng.integers(1, 3))
+    B = int(rng.integers(1, 5))
+    policy = int(rng.choice([1, 2]))
+    W = int(rng.integers(8, 600))
+    C = W + int(rng.choice([0, int(rng.integers(1, 70)), int(rng.integers(70, 400))]))
+    S = int(rng.choice([1, int(rng.integers(2, 20)), int(rng.integers(20, 200)), C + 3]))
+    Hq = Hkv * g
+    dtype = torch.bfloat16 if rng.random() < 0.7 else torch.float16
+    ws = "auto" if rng.random() < 0.5 else None
+    T0 = np.array([int(rng.choice([0, int(rng.integers(0, C)), C - S // 2,
+                                   int(rng.integers(C, 5 * C))])) for _ in range(B)])
+    T0 = np.maximum(T0, 0)
+    cos, sin = synth.rope_cache(int(T0.max()) + 2 * S + 2, D)
+    rope_d = (cos.to(dev()), sin.to(dev()))
+    cn, sn = cos.numpy(), sin.numpy()
+    kc = synth.normal((B, Hkv, C, D), 90 + seed, 1, dtype)
+    vc = synth.normal((B, Hkv, C, D), 90 + seed, 2, dtype)
+    gk, gv = kc.to(dev()), vc.to(dev())
+    wk, wv = synth.bits(kc).copy(), synth.bits(vc).copy()
+    st = status()
+    T = T0
+    what = (D, g, Hkv, B, C, W, S, policy, ws, T0.tolist())
+    for step in range(2):
+        nk = synth.normal((B, Hkv, S, D), 90 + seed, 10 + step, dtype)
+        nv = synth.normal((B, Hkv, S, D), 90 + seed, 20 + step, dtype)
+        q = synth.normal((B, Hq, S, D), 90 + seed, 30 + step, dtype)
+        sk = (T + S - 1).astype(np.int32)
+        L = K.kvc_seq_lengths(torch.from_numpy(sk).to(dev()), S, C, policy,
+                              local_window_size=W, status=st)
+        ks = vs = None
+        if S > 1:
+            ks = torch.full((B, Hkv, C + S, D), float("nan"), dtype=dtype, device=dev())
+            vs = torch.full_like(ks, float("nan"))
+        out = torch.empty(B, Hq, S, D, dtype=dtype, device=dev())
+        K.kvc_window_prefill_step(out, q.to(dev()), gk, gv, nk.to(dev()), nv.to(dev()), L,
+                                  policy, W, ks, vs, rope=rope_d, status=st, workspace=ws)
+        torch.cuda.synchronize()
+        assert st.item() == 0, what
+        lens = orc.seq_lengths(sk, S, C, policy, W)
+        if S > 1:
+            wks = np.zeros((B, Hkv, C + S, D), dtype=wk.dtype)
+            wvs = np.zeros_like(wks)
+            orc.window_append(wk, wv, synth.bits(nk), synth.bits(nv), lens, policy, cn, sn, wks,
+                              wvs)
+            rk, rv = wks, wvs
+        else:
+            orc.window_append(wk, wv, synth.bits(nk), synth.bits(nv), lens, policy, cn, sn)
+            rk, rv = wk, wv
+        assert_bytes_equal(gk, wk, f"step {step} k cache {what}")
+        assert_bytes_equal(gv, wv, f"step {step} v cache {what}")
+        qb = synth.bits(q)
+        for i in sorted({0, S - 1, S // 2, int(rng.integers(0, S))}):
+            if S > 1:
+                n = (lens["cache_past"] + i + 1).astype(np.int32)
+            else:
+                n = lens["cache_total"]
+            tot = (lens["past_abs"] + i + 1).astype(np.int32)
+            want, _ = orc.gqa_attention(np.ascontiguousarray(qb[:, :, i:i + 1]), rk, rv, n, tot,
+                                        window=W, cos_cache=cn, sin_cache=sn)
+            assert_close(out[:, :, i:i + 1], want, 2e-2, f"step {step} query {i} {what}")
+        T = T + S
