@@ -657,10 +657,12 @@ class WindowPrefillInplace(WindowPrefill):
 
 class WindowPrefillHazard(WindowPrefill):
     """The windowed chunked-prefill step as one kvc_window_prefill_step call:
-    only the batch rows whose eviction the chunk would see go through the
-    C + S stage; a row that evicts nothing (its cache not yet full) appends
-    in place and its attention reads the cache.  The timed kernel is the
-    whole call (row movement, attention, copy-back)."""
+    only the batch rows whose eviction the chunk would see use the stage,
+    and those only for their new rows and the 127 old rows below them (the
+    attention reads older tiles from the cache, and the copy-back is one
+    in-place move of the window plus the new rows); a row that evicts
+    nothing (its cache not yet full) appends in place and its attention
+    reads the cache.  The timed kernel is the whole call."""
     roofline_kernel = "kvc_window_prefill_step (the whole call)"
 
     def __init__(self, dev, seed=0, with_kernels=True, chunk=64):
@@ -674,9 +676,14 @@ class WindowPrefillHazard(WindowPrefill):
         staged = (E > 0) & (E > Lp - W + 1)
         moved = (E > 0) & ~staged
         self.n_staged, self.n_moved = int(staged.sum()), int(moved.sum())
-        # staged rows: seed (Lp rows) and copy-back (L rows), read + written;
-        # rows that move in place: Lp - E rows read + written
-        self.stage_bytes = int(2 * Hkv * D * e * int((staged * (2 * Lp + 2 * L)).sum() +
+        # rows read + written: a staged row seeds the 127 old rows below its
+        # new ones, moves its kept old rows down after the attention and
+        # copies its kept new rows back; a row that moves in place moves its
+        # Lp - E old rows
+        kept_old = np.maximum(Lp - E, 0)
+        kept_new = Lp + S - np.maximum(E, Lp)
+        staged_rows = np.minimum(Lp, 127) + kept_old + kept_new
+        self.stage_bytes = int(2 * Hkv * D * e * int((staged * 2 * staged_rows).sum() +
                                                       (moved * 2 * (Lp - E)).sum()))
         self.bytes_per_step = self.stage_bytes + self.kernel_bytes + 2 * 2 * B * Hkv * S * D * e
         self.kernel_bytes = self.bytes_per_step

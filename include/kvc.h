@@ -604,9 +604,15 @@ kvc_status kvc_gqa_prefill_chunk(void *out, const void *q, const void *k_rows, c
  * Batch row b with Lp = len.cache_past[b], E = len.evict[b] is hazardous
  * when E > 0 and E > Lp - W + 1: the rows [0, E) that the step evicts
  * include one that its first query (at stage row Lp) still sees.
- *   hazardous rows:  kvc_window_append's staged pair -- stage[0, Lp) =
- *                    cache[0, Lp), the new rows at stage[Lp, Lp + S), the
- *                    attention over the stage, cache[0, L) = stage[E, Lp + S);
+ *   hazardous rows:  the new rows go to stage[Lp, Lp + S) and the 127 old
+ *                    rows below them to stage[Lp - 127, Lp) (fewer when Lp <
+ *                    127); the attention reads its 128-key tiles that lie
+ *                    below Lp from the cache and the others from the stage;
+ *                    then cache rows [E, Lp) move to [0, Lp - E) in place
+ *                    and stage rows [max(E, Lp), Lp + S) follow them -- the
+ *                    rows and results of kvc_window_append's staged pair at
+ *                    about half its row traffic (the seed and copy-back of
+ *                    the whole window become one move of it);
  *   the other rows:  cache rows [E, Lp) move to [0, Lp - E) in place, the new
  *                    rows go to [Lp - E, L), and the attention reads the
  *                    cache; no stage traffic (E = 0: only the new rows).
@@ -619,8 +625,9 @@ kvc_status kvc_gqa_prefill_chunk(void *out, const void *q, const void *k_rows, c
  * k_cache, v_cache  device [batch, kv_heads, capacity, head_dim].
  * new_k, new_v    device [batch, kv_heads, new_tokens, head_dim].
  * k_stage, v_stage  device [batch, kv_heads, capacity + new_tokens, head_dim]
- *                 for S > 1 (only hazardous rows write or read them); may be
- *                 NULL for S = 1, which never stages.
+ *                 for S > 1, rows indexed as the cache's (only hazardous rows
+ *                 write or read them, at most 127 + S rows each); may be NULL
+ *                 for S = 1, which never stages.
  * len             kvc_seq_lengths outputs for this S, C, policy and window.
  * windowed        KVC_WINDOWED or KVC_DRIFTING; 0 < local_window_size <= C
  *                 (KVC_ERR_WINDOW).

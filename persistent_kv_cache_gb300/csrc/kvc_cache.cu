@@ -199,7 +199,9 @@ new_rows_kernel(T *__restrict__ k_dst, T *__restrict__ v_dst, const T *__restric
 // n = L.  Row counts come from the device lengths; the grid covers the
 // largest possible range.
 // hazard_w > 0 (kvc_window_prefill_step): only the rows step_staged() marks
-// for that window.
+// for that window, and only what they need: the seed copies rows
+// [Lp - kStageSeedRows, Lp) to the same rows of the stage, the copy-back
+// stage rows [max(E, Lp), Lp + S) to cache rows from max(E, Lp) - E on.
 template <typename V>
 __global__ void __launch_bounds__(256)
 copy_range_kernel(char *__restrict__ k_dst, char *__restrict__ v_dst,
@@ -219,9 +221,21 @@ copy_range_kernel(char *__restrict__ k_dst, char *__restrict__ v_dst,
     // a row rejected for its RoPE range is rejected as a whole
     if (rope_limit_rows >= 0 && (int64_t)len.past_abs[b] + S > rope_limit_rows)
         return;
-    const int64_t src0 = copy_back ? len.evict[b] : 0;
-    const int64_t n = copy_back ? L : len.cache_past[b];
-    if (src0 < 0 || n < 0 || n > dst_rows || src0 + n > src_rows) {
+    int64_t src0 = copy_back ? len.evict[b] : 0, dst0 = 0;
+    int64_t n = copy_back ? L : len.cache_past[b];
+    if (hazard_w > 0) {
+        const int64_t Lp = len.cache_past[b], E = len.evict[b];
+        if (copy_back) {
+            const int64_t first = E > Lp ? E : Lp;  // the kept rows that come from the stage
+            src0 = first;
+            dst0 = first - E;
+            n = Lp + S - first;
+        } else {
+            src0 = dst0 = Lp > kvc::kStageSeedRows ? Lp - kvc::kStageSeedRows : 0;
+            n = Lp - src0;
+        }
+    }
+    if (src0 < 0 || dst0 < 0 || n < 0 || dst0 + n > dst_rows || src0 + n > src_rows) {
         if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0 && slice % kv_heads == 0)
             kvc::raise_status(status, KVC_DEV_CAPACITY);
         return;
@@ -229,7 +243,8 @@ copy_range_kernel(char *__restrict__ k_dst, char *__restrict__ v_dst,
     const int64_t nv = n * row_bytes / (int64_t)sizeof(V);
     const V *src = reinterpret_cast<const V *>((is_k ? k_src : v_src) +
                                                ((int64_t)slice * src_rows + src0) * row_bytes);
-    V *dst = reinterpret_cast<V *>((is_k ? k_dst : v_dst) + (int64_t)slice * dst_rows * row_bytes);
+    V *dst = reinterpret_cast<V *>((is_k ? k_dst : v_dst) +
+                                   ((int64_t)slice * dst_rows + dst0) * row_bytes);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     for (; i + stride < nv; i += 2 * stride) {
@@ -480,13 +495,14 @@ constexpr int kShiftSlots = 6;
 constexpr int kShiftChunk = 32768;
 constexpr int kShiftSmem = kShiftSlots * kShiftChunk + kShiftSlots * 8 + 128;
 
-// pre_w > 0 (kvc_window_prefill_step, before the new rows are written): the
-// rows step_staged() leaves to the cache move [E, Lp) to [0, Lp - E) of a
-// cache of rows_per_head = C rows a head, the others stay.
+// hazard_w > 0 (kvc_window_prefill_step): rows [E, Lp) of a cache of
+// rows_per_head = C rows a head move to [0, Lp - E) -- before the attention
+// (staged_rows 0) for the rows step_staged() leaves to the cache, after it
+// (staged_rows 1) for the rows it marks; the other rows stay.
 __global__ void __launch_bounds__(32)
 shift_rows_kernel(char *__restrict__ k_rows, char *__restrict__ v_rows, kvc_lengths len,
                   int kv_heads, int64_t row_bytes, int64_t rows_per_head, int S,
-                  int64_t rope_limit_rows, int32_t *status, int pre_w)
+                  int64_t rope_limit_rows, int32_t *status, int hazard_w, int staged_rows)
 {
     extern __shared__ uint8_t shift_smem_raw[];
     if (threadIdx.x != 0)
@@ -503,16 +519,16 @@ shift_rows_kernel(char *__restrict__ k_rows, char *__restrict__ v_rows, kvc_leng
     const int64_t E = len.evict[b];
     const int64_t Lp = len.cache_past[b];
     if (E < 0 || Lp < 0 || E + L != Lp + S ||
-        (pre_w > 0 ? L > rows_per_head : Lp + S > rows_per_head)) {
+        (hazard_w > 0 ? L > rows_per_head : Lp + S > rows_per_head)) {
         if (is_k && slice % kv_heads == 0)
             kvc::raise_status(status, KVC_DEV_CAPACITY);
         return;
     }
-    if (pre_w > 0 && kvc::step_staged(Lp, E, pre_w))
-        return;  // a staged row: its rows move in the copy-back
+    if (hazard_w > 0 && kvc::step_staged(Lp, E, hazard_w) != (staged_rows != 0))
+        return;  // the other kind of row
     // rows that move: the L rows of the stage held in place, or the Lp - E
-    // old rows that stay in the cache
-    const int64_t nrows = pre_w > 0 ? Lp - E : L;
+    // old rows that stay in the cache (none when the step evicts them all)
+    const int64_t nrows = hazard_w > 0 ? (Lp > E ? Lp - E : 0) : L;
     if (E == 0 || nrows == 0)
         return;  // the rows are already in place
     uint8_t *ring = reinterpret_cast<uint8_t *>(
@@ -736,15 +752,27 @@ kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const v
         // go where its attention will read them
         launch_copy(static_cast<char *>(k_stage), static_cast<char *>(v_stage),
                     reinterpret_cast<const char *>(kc), reinterpret_cast<const char *>(vc), C + S,
-                    C, 0, C, hazard_w);
+                    C, 0, kvc::kStageSeedRows, hazard_w);
         if (cudaFuncSetAttribute(shift_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kShiftSmem) != cudaSuccess)
             return KVC_ERR_CUDA;
         shift_rows_kernel<<<dim3(slices, 2), 32, kShiftSmem, stream>>>(
             reinterpret_cast<char *>(kc), reinterpret_cast<char *>(vc), len, kv_heads,
-            (int64_t)D * sizeof(T), C, S, cos_t ? rope_max_pos : -1, status, hazard_w);
+            (int64_t)D * sizeof(T), C, S, cos_t ? rope_max_pos : -1, status, hazard_w, 0);
         launch_new_rows(kc, vc, C, 4, PageTable{nullptr, 0, 0, 0},
                         AltRows{k_stage, v_stage, C + S, hazard_w});
+    } else if (hazard_w > 0) {
+        // kvc_window_prefill_step's copy-back: the staged rows' old rows
+        // move down in the cache, then their new rows follow from the stage
+        if (cudaFuncSetAttribute(shift_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kShiftSmem) != cudaSuccess)
+            return KVC_ERR_CUDA;
+        shift_rows_kernel<<<dim3(slices, 2), 32, kShiftSmem, stream>>>(
+            reinterpret_cast<char *>(kc), reinterpret_cast<char *>(vc), len, kv_heads,
+            (int64_t)D * sizeof(T), C, S, cos_t ? rope_max_pos : -1, status, hazard_w, 1);
+        launch_copy(reinterpret_cast<char *>(kc), reinterpret_cast<char *>(vc),
+                    static_cast<const char *>(k_stage), static_cast<const char *>(v_stage), C,
+                    C + S, 1, S, hazard_w);
     } else if (phase == KVC_APPEND) {
         launch_copy(static_cast<char *>(k_stage), static_cast<char *>(v_stage),
                     reinterpret_cast<const char *>(kc), reinterpret_cast<const char *>(vc), C + S,
@@ -753,7 +781,7 @@ kvc_status append_typed(void *k_cache, void *v_cache, const void *new_k, const v
     } else {
         launch_copy(reinterpret_cast<char *>(kc), reinterpret_cast<char *>(vc),
                     static_cast<const char *>(k_stage), static_cast<const char *>(v_stage), C,
-                    C + S, 1, C, hazard_w);
+                    C + S, 1, C);
     }
     return kvc_host::launch_status();
 }
@@ -944,7 +972,7 @@ KVC_API kvc_status kvc_window_append_inplace(void *k_rows, void *v_rows, const v
     shift_rows_kernel<<<dim3(slices, 2), 32, kShiftSmem, stream>>>(
         static_cast<char *>(k_rows), static_cast<char *>(v_rows), len, kv_heads,
         (int64_t)head_dim * eb, rows_per_head, new_tokens, rope_cos ? rope_max_pos : -1,
-        dev_status, 0);
+        dev_status, 0, 0);
     return kvc_host::launch_status();
 }
 

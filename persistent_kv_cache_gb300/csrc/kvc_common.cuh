@@ -84,6 +84,13 @@ __host__ __device__ __forceinline__ bool step_staged(int64_t Lp, int64_t E, int6
     return E > 0 && E > Lp - W + 1;
 }
 
+// A staged row of kvc_window_prefill_step keeps its old rows [0, Lp) in the
+// cache while its chunk attends: the attention reads a 128-key tile from
+// the cache when the tile lies below Lp and from the stage otherwise, so
+// the stage needs the new rows and, below them, only the old rows a tile
+// reaching Lp can start at: rows [Lp - kStageSeedRows, Lp).
+constexpr int kStageSeedRows = 127;
+
 // --------------------------------------------------------------------------
 // element types
 // --------------------------------------------------------------------------
@@ -354,11 +361,14 @@ inline bool lengths_ok(const kvc_lengths &l)
 // number of SMs of the current device (cached per device)
 int sm_count();
 
-// The row movement of kvc_window_prefill_step (kvc_cache.cu), before the
-// chunk attention (phase KVC_APPEND) or after it (KVC_COPY_BACK): rows that
-// step_staged() marks seed the stage / copy back from it as in
-// kvc_window_append; the others move rows [E, Lp) of the cache to [0, Lp - E)
-// in place and take the new rows at [Lp - E, L).
+// The row movement of kvc_window_prefill_step (kvc_cache.cu).  Before the
+// chunk attention (phase KVC_APPEND): a row that step_staged() marks copies
+// its old rows [Lp - kStageSeedRows, Lp) to the same rows of the stage and
+// takes its new rows at stage rows [Lp, Lp + S); any other row moves rows
+// [E, Lp) of the cache to [0, Lp - E) in place and takes the new rows at
+// [Lp - E, L).  After it (KVC_COPY_BACK), a staged row moves its cache rows
+// [E, Lp) to [0, Lp - E) and copies stage rows [max(E, Lp), Lp + S) after
+// them.
 kvc_status hazard_rows(void *k_cache, void *v_cache, const void *new_k, const void *new_v,
                        void *k_stage, void *v_stage, const kvc_lengths &len, int batch,
                        int kv_heads, int S, int64_t C, int D, int dtype, int window, int phase,

@@ -263,18 +263,22 @@ struct PrefillArgs {
     int nsplit;
     float *ws_o, *ws_m, *ws_l;  // [nsplit][batch * q_heads * S] (x D for o)
     // kvc_window_prefill_step (hazard_w = the window, else 0): a row that
-    // kvc::step_staged() marks reads the stage (tmap_k2 / tmap_v2, alt_rows
-    // rows a head, its chunk at rows [Lp, Lp + S)); any other row was moved
-    // and appended in the cache itself (rows_per_head = C rows a head, its
-    // chunk at rows [Lp - E, L))
+    // kvc::step_staged() marks keeps its old rows in the cache and its new
+    // ones in the stage (tmap_k2 / tmap_v2, alt_rows rows a head, the chunk
+    // at rows [Lp, Lp + S), the old rows [Lp - kStageSeedRows, Lp) copied
+    // there too): a 128-key tile below Lp is read from the cache, any other
+    // from the stage; any other row was moved and appended in the cache
+    // itself (rows_per_head = C rows a head, its chunk at rows [Lp - E, L))
     int hazard_w;
     int64_t alt_rows;
 };
+static_assert(kvc::kStageSeedRows == kBN - 1,
+              "a key tile that reaches the new rows starts at most kBN - 1 rows below them");
 
 // The rows the chunk of batch row b attends: the row of its first query (a
 // position P at row Lp, so key row r holds position P - Lp + r), the row
-// pitch of the buffer it reads and whether that buffer is the stage.  False
-// when the lengths do not fit that buffer.
+// pitch of the buffer holding its new rows and whether that buffer is the
+// stage.  False when the lengths do not fit that buffer.
 __device__ __forceinline__ bool chunk_rows(const PrefillArgs &a, int b, int &Lp, int64_t &pitch,
                                            bool &alt)
 {
@@ -450,8 +454,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         leave();
         return;
     }
-    const CUtensorMap *map_k = alt ? &tmap_k2 : &tmap_k;
-    const CUtensorMap *map_v = alt ? &tmap_v2 : &tmap_v;
+    // a staged row reads its tiles below Lp from the cache (C rows a head)
+    // and the rest from the stage
+    const int64_t cache_base = ((int64_t)b * a.kv_heads + kvh) * a.rows_per_head;
     if (a.cos_t && (int64_t)P + S > a.rope_max_pos) {
         if (threadIdx.x == 0 && qblk == 0 && kvh == 0)
             kvc::raise_status(a.status, KVC_DEV_ROPE_RANGE);
@@ -523,8 +528,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         // one 3-D box per ring slot: a K slab is DB column blocks of 128 rows,
         // a V slab is KPS rows of every column block (128-byte swizzled rows)
         if (lane == 0) {
-            kvc::tma_prefetch_desc(map_k);
-            kvc::tma_prefetch_desc(map_v);
+            kvc::tma_prefetch_desc(&tmap_k);
+            kvc::tma_prefetch_desc(&tmap_v);
+            if (alt) {
+                kvc::tma_prefetch_desc(&tmap_k2);
+                kvc::tma_prefetch_desc(&tmap_v2);
+            }
             int issued = 0;
             for (int q = 0; q < nslabs; ++q) {
                 const int slot = q % NSLAB;
@@ -536,12 +545,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 slab_group(q / NST, ntiles, is_v, tile);
                 const int sl = q % NST;
                 uint8_t *dst = smem + SM::RING_OFF + slot * SM::SLAB;
-                const int32_t y0 = (int32_t)(row_base + lo + tile * kBN);
+                const int r0 = lo + tile * kBN;  // the tile's first key row
+                const bool stage = alt && r0 + kBN > Lp;
+                const int32_t y0 = (int32_t)((stage ? row_base : cache_base) + r0);
                 kvc::mbar_arrive_expect_tx(&full[slot], SM::SLAB);
                 if (!is_v)
-                    kvc::tma_load_3d(dst, map_k, 0, y0, sl * DB, &full[slot]);
+                    kvc::tma_load_3d(dst, stage ? &tmap_k2 : &tmap_k, 0, y0, sl * DB, &full[slot]);
                 else
-                    kvc::tma_load_3d(dst, map_v, 0, y0 + sl * KPS, 0, &full[slot]);
+                    kvc::tma_load_3d(dst, stage ? &tmap_v2 : &tmap_v, 0, y0 + sl * KPS, 0,
+                                     &full[slot]);
                 issued = q + 1;
             }
             if (*abort_flag) {

@@ -84,11 +84,19 @@ def _step(K, orc, gk, gv, wk, wv, T, S, C, W, policy, dtype, seed, rope, Hq, sam
         sent = np.full(ks[0].numel() * ks.element_size(), SENTINEL, np.uint8)
         for b in range(B):
             if staged[b]:
-                n = int(lens["cache_past"][b]) + S
-                assert_bytes_equal(ks[b, :, :n], np.ascontiguousarray(wks[b, :, :n]),
+                # the 16-bit path stages the new rows and the 127 old rows
+                # below them (its attention reads older tiles from the
+                # cache); fp32 stages the whole window
+                Lp = int(lens["cache_past"][b])
+                s0 = 0 if dtype == torch.float32 else max(0, Lp - 127)
+                n = Lp + S
+                assert_bytes_equal(ks[b, :, s0:n], np.ascontiguousarray(wks[b, :, s0:n]),
                                    f"k stage row {b}")
-                assert_bytes_equal(vs[b, :, :n], np.ascontiguousarray(wvs[b, :, :n]),
+                assert_bytes_equal(vs[b, :, s0:n], np.ascontiguousarray(wvs[b, :, s0:n]),
                                    f"v stage row {b}")
+                for s_ in (ks, vs):
+                    got = s_[b, :, :s0].contiguous().view(torch.uint8).cpu().numpy().ravel()
+                    assert (got == SENTINEL).all(), f"row {b} staged rows below Lp - 127"
             else:
                 for s_ in (ks, vs):
                     got = s_[b].contiguous().view(torch.uint8).cpu().numpy().ravel()
