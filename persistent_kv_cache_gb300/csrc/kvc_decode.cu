@@ -10,10 +10,11 @@
 //   * warp 4 is the producer: one lane issues 2-D TMA loads of 64-row K and V
 //     tiles (128-byte swizzled boxes of 64 columns) into an NS-stage ring of
 //     shared-memory buffers guarded by full/empty mbarriers;
-//   * warps 0-3 consume 16 rows of every tile each: S = Q K^T and O += P V on
-//     the tensor cores (mma.sync m16n8k16, fp32 accumulate) with the GQA group's
-//     query heads as the M dimension, online softmax in registers with quad
-//     shuffles, then a 4-way (m, l, o) merge through shared memory;
+//   * warps 0-3 consume 16 rows of every tile each: S^T = K Q^T and
+//     O^T += V^T P^T on the tensor cores (mma.sync m16n8k16, fp32 accumulate)
+//     with the warp's 16 keys as the M dimension and the GQA group's query
+//     heads as N, online softmax in registers with shuffles across the
+//     warp's key lanes, then a 4-way (m, l, o) merge through shared memory;
 //   * a split whose row holds more than one split writes (m, l, o) partials to
 //     the workspace and decode_combine_kernel merges them; a single split
 //     writes the output directly.
@@ -25,8 +26,7 @@
 // The fused step (kvc_decode_step) runs the same kernel with the lengths
 // derived inline from seqlens_k, the new K/V row patched into the last tile
 // in shared memory (and stored to the cache) by the split that owns the
-// newest position, and the split merge done by whichever split of a
-// (batch row, kv head) finishes last: one launch per step.
+// newest position; the split merge is a second launch.
 // fp32 path: attn_f32_kernel, one warp per query row on CUDA cores (also used
 // by the multi-token call for fp32).
 #include <atomic>
@@ -651,12 +651,13 @@ template <int D, int MODE> __host__ __device__ constexpr int decode_slot_bytes()
 {
     return decode_uses_slots<D, MODE>() ? kTile * D * 2 : 2 * kTile * D * 2;
 }
-// At head_dim 256 the output accumulator alone takes 128 registers a
-// thread: the split kernel then runs without a producer warp (four consumer
-// warps, two CTAs an SM, so that a thread may hold up to 255 registers), and
-// the warp that releases a ring slot last issues that slot's next load.
-// (Over int8 pages, where the consumer warps' conversion work is the limit,
-// the same scheme measured slower: the issuing lane stalls its warp.)
+// At head_dim 256 the split kernel runs without a producer warp (four
+// consumer warps, two CTAs an SM, up to 255 registers a thread: 64 of them
+// the output accumulator of a head block, 128 of two), and the warp that
+// releases a ring slot last issues that slot's next load -- measured faster
+// than a fifth, producer warp, with or without spills.  (Over int8 pages,
+// where the consumer warps' conversion work is the limit, the same scheme
+// measured slower: the issuing lane stalls its warp.)
 template <int D, int MODE> __host__ __device__ constexpr bool decode_no_producer()
 {
     return D >= 256 && MODE != kPagedQ;
