@@ -64,6 +64,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import subprocess
 import sys
 import time
@@ -1228,16 +1229,25 @@ def host_cores():
         return os.cpu_count() or 1
 
 
+def source_digest(path):
+    """sha256 of a CUDA source's code: comments removed and whitespace
+    collapsed, so that an edit of comments alone keeps a capture valid."""
+    text = open(path, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()
+
+
 def kernel_traffic(key):
     """DRAM bytes per launch recorded from an ncu capture, or None when the
-    kernel's source changed since."""
+    kernel's source code changed since."""
     kernel_file, name = key
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             rec = json.load(f)[name]
-        src = open(os.path.join(ROOT, "persistent_kv_cache_gb300", "csrc", kernel_file), "rb").read()
-        if rec["source_sha256"] != hashlib.sha256(src).hexdigest():
+        src = os.path.join(ROOT, "persistent_kv_cache_gb300", "csrc", kernel_file)
+        if rec["source_sha256"] != source_digest(src):
             return None
         return rec["dram_bytes_per_launch"]
     except (OSError, KeyError, ValueError):
