@@ -107,6 +107,20 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// consumer_sync() that also returns whether v holds in every consumer thread
+__device__ __forceinline__ bool consumer_all(bool v)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\t"
+                 "setp.ne.u32 p, %1, 0;\n\t"
+                 "bar.red.and.pred q, 1, 128, p;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)v)
+                 : "memory");
+    return r != 0;
+}
+
 // 16 bytes from shared memory (a 32-bit shared-window address)
 __device__ __forceinline__ uint4 lds128(uint32_t addr)
 {
@@ -202,6 +216,9 @@ struct GroupAttn {
     static constexpr bool QREG = QREG_;
     uint32_t qb[QREG ? HB : 1][QREG ? MB : 1][2];
     uint32_t q_addr, q_hstride;  // !QREG: this lane's ldmatrix row address; bytes per 8 heads
+    // int8 tiles of a bf16 cache: this lane's ldmatrix row address in the
+    // fp16 copy of the query rows (load_q16)
+    uint32_t q16_addr;
     float o[HB][MB][4];
     float m[HB][2], l[HB][2];
 
@@ -229,6 +246,19 @@ struct GroupAttn {
         } else {
             ldsm_x4(q_addr + hb * q_hstride + kk * 32, f[0], f[1], f[2], f[3]);
         }
+    }
+
+    // fp16 B fragments of query columns [16 kk, 16 kk + 32) of head block hb
+    // from the fp16 copy of the rows
+    __device__ __forceinline__ void q16_frag2(int hb, int kk, uint32_t (&f)[4]) const
+    {
+        ldsm_x4(q16_addr + hb * 8 * (D + 8) * 2 + kk * 32, f[0], f[1], f[2], f[3]);
+    }
+    // the fp16 copy [16][D + 8] of the query rows, for the int8 tiles of a
+    // bf16 cache (a bf16 query element is exact in fp16 down to 2^-14)
+    __device__ __forceinline__ void load_q16(const __half *qs16, int lane)
+    {
+        q16_addr = kvc::smem_u32(qs16 + (lane & 7) * (D + 8) + (lane >> 3) * 8);
     }
 
     // the rotated query rows staged as qs[16][QS] (heads >= g zero; at
@@ -386,14 +416,23 @@ struct GroupAttn {
     // D / 2 bytes of each are the exact A fragments of its MMAs, as 16-byte
     // pieces interleaved across the warp (piece i of lane l at i * 512 +
     // l * 16), piece i holding 16-column blocks 2 i and 2 i + 1.  They become
-    // the integers u - zp in registers (koff2 / voff2 from q8_offset);
-    // the scores take the page's K scale (folded into scale_log2) and the
-    // probabilities its V scale.  Every converted value is finite, and P is 0
-    // past `hi`, so the rows past the split end need no zeroing.
+    // the integers u - zp in registers: the K codes as fp16 halves for fp16
+    // MMAs with the query when F16S (koff2 = q8_offset<__half>(zp); for a
+    // bf16 cache the query's fp16 copy, load_q16, holding the same values:
+    // the products are the same exact values as with bf16 operands, at a
+    // third of the conversion work), else as T (q8_offset<T>); the V codes as
+    // T (voff2 = q8_offset<T>(zp)) beside the probabilities; the scores take
+    // the page's K scale (folded into scale_log2) and the probabilities its V
+    // scale.  Every converted value is finite, and P is 0 past `hi`, so the
+    // rows past the split end need no zeroing.
+    template <bool F16S>
     __device__ __forceinline__ void tile_q8(uint32_t kq, uint32_t vq, int lane, int lo,
                                             int hi, float scale_log2, float vscale, uint64_t koff2,
                                             uint64_t voff2)
     {
+        // fp16 scores (for a bf16 cache: only when its query is exact in
+        // fp16; otherwise the K codes take T's own, exact route)
+        using KT = typename std::conditional<F16S, __half, T>::type;
         constexpr int NP = D / 32;  // 16-byte pieces of a lane's fragment bytes
         float sc[HB][4];
 #pragma unroll
@@ -405,19 +444,23 @@ struct GroupAttn {
             const uint4 w = lds128(kq + p * 512 + lane * 16);
             uint32_t qf[HB][4];
 #pragma unroll
-            for (int hb = 0; hb < HB; ++hb)
-                q_frag2(hb, 2 * p, qf[hb]);
+            for (int hb = 0; hb < HB; ++hb) {
+                if constexpr (F16S && std::is_same<T, __nv_bfloat16>::value)
+                    q16_frag2(hb, 2 * p, qf[hb]);
+                else
+                    q_frag2(hb, 2 * p, qf[hb]);
+            }
             uint32_t a[4];
-            u8x4_to_pairs<T>(w.x, koff2, a[0], a[1]);
-            u8x4_to_pairs<T>(w.y, koff2, a[2], a[3]);
+            u8x4_to_pairs<KT>(w.x, koff2, a[0], a[1]);
+            u8x4_to_pairs<KT>(w.y, koff2, a[2], a[3]);
 #pragma unroll
             for (int hb = 0; hb < HB; ++hb)
-                Mma<T>::run(sc[hb], a, qf[hb][0], qf[hb][1]);
-            u8x4_to_pairs<T>(w.z, koff2, a[0], a[1]);
-            u8x4_to_pairs<T>(w.w, koff2, a[2], a[3]);
+                Mma<KT>::run(sc[hb], a, qf[hb][0], qf[hb][1]);
+            u8x4_to_pairs<KT>(w.z, koff2, a[0], a[1]);
+            u8x4_to_pairs<KT>(w.w, koff2, a[2], a[3]);
 #pragma unroll
             for (int hb = 0; hb < HB; ++hb)
-                Mma<T>::run(sc[hb], a, qf[hb][2], qf[hb][3]);
+                Mma<KT>::run(sc[hb], a, qf[hb][2], qf[hb][3]);
         }
         uint32_t pb[HB][2];
         softmax_step<true>(sc, lane, lo, hi, scale_log2, vscale, pb);
@@ -681,7 +724,7 @@ template <int D, int MODE> __host__ __device__ constexpr int decode_smem_bytes()
 {
     return decode_ring_slots<D, MODE>() * decode_slot_bytes<D, MODE>() + 16 * (D + 8) * 2 +
            2 * decode_ring_slots<D, MODE>() * 8 + 16 + 32 * 4 + 2 * D * 2 +
-           4 * decode_ring_slots<D, MODE>();
+           4 * decode_ring_slots<D, MODE>() + (MODE == kPagedQ ? 16 + 16 * (D + 8) * 2 : 0);
 }
 
 // One CTA per (split, kv head, batch row) for kvc_gqa_decode,
@@ -722,6 +765,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     T *newrow = reinterpret_cast<T *>(page_ids + 32);
     // NOPROD: how many warps have released each slot in its current round
     int *released = reinterpret_cast<int *>(newrow + 2 * D);
+    // kPagedQ: the query rows as fp16 [16][QS] for the int8 tiles' scores
+    __half *qs16 = reinterpret_cast<__half *>(
+        (reinterpret_cast<uintptr_t>(released + NBAR) + 15) & ~uintptr_t(15));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -933,6 +979,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     // ---------------- consumers ----------------
     const int g = a.group;
+    bool q16_exact = true;  // kPagedQ: every query element is exact in fp16
     {
         // rotated query rows of the group (rows >= g stay zero)
         const T *qg = static_cast<const T *>(a.q) + ((int64_t)b * a.q_heads + kvh * g) * D;
@@ -947,8 +994,19 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 if (cs)
                     kvc::rope_pair(lo, hi, cs[i], sn[i]);
             }
-            qs[h * QS + i] = kvc::Elem<T>::from_f32(lo);
-            qs[h * QS + i + D / 2] = kvc::Elem<T>::from_f32(hi);
+            const T tlo = kvc::Elem<T>::from_f32(lo), thi = kvc::Elem<T>::from_f32(hi);
+            qs[h * QS + i] = tlo;
+            qs[h * QS + i + D / 2] = thi;
+            if constexpr (MODE == kPagedQ) {
+                // the same (T-rounded) values in fp16: exact for 0 and for
+                // magnitudes in [2^-17, 65504] (8 significant bits of a bf16
+                // value fit an fp16 normal or subnormal there)
+                const float flo = kvc::Elem<T>::to_f32(tlo), fhi = kvc::Elem<T>::to_f32(thi);
+                qs16[h * QS + i] = __float2half_rn(flo);
+                qs16[h * QS + i + D / 2] = __float2half_rn(fhi);
+                q16_exact &= (flo == 0.f || (fabsf(flo) >= 0x1p-17f && fabsf(flo) <= 65504.f)) &&
+                             (fhi == 0.f || (fabsf(fhi) >= 0x1p-17f && fabsf(fhi) <= 65504.f));
+            }
         }
         if constexpr (MODE == kFused) {
             // the CTA whose split ends at the newest position (tot - 1) appends
@@ -980,10 +1038,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
             }
         }
     }
-    consumer_sync();
+    // kPagedQ: the int8 tiles take fp16 scores when the whole query of the
+    // group is exact in fp16 (always for an fp16 cache)
+    const bool f16s = consumer_all(q16_exact);
     GroupAttn<T, D, HB, decode_q_in_registers<D, HB, MODE>(), true> ga;
     ga.init();
     ga.load_q(qs, QS, lane);
+    if constexpr (MODE == kPagedQ)
+        ga.load_q16(qs16, lane);
     bool timed_out = false;
     // kPagedQ: lane l holds the split's l-th table entry and, for an int8
     // page, its (k_scale, k_zp, v_scale, v_zp); a tile takes them by shuffle
@@ -1068,8 +1130,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
             const float vz = __shfl_sync(0xffffffffu, my_p[3], pi);
             if (my_lo < my_valid) {
                 const uint32_t kq = kvc::smem_u32(kgen) + warp * 16 * D;
-                ga.tile_q8(kq, kq + kTile * D, lane, my_lo, my_valid, a.scale_log2 * ks, vs,
-                           q8_offset<T>(kz), q8_offset<T>(vz));
+                if (f16s)
+                    ga.template tile_q8<true>(kq, kq + kTile * D, lane, my_lo, my_valid,
+                                              a.scale_log2 * ks, vs, q8_offset<__half>(kz),
+                                              q8_offset<T>(vz));
+                else
+                    ga.template tile_q8<false>(kq, kq + kTile * D, lane, my_lo, my_valid,
+                                               a.scale_log2 * ks, vs, q8_offset<T>(kz),
+                                               q8_offset<T>(vz));
             }
         } else if (my_valid > 0) {
             if (my_valid < 16) {

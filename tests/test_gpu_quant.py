@@ -160,19 +160,27 @@ def _quantize_table(K, table, n_rows, P, kp_d, vp_d, qk, qv, qp, ks, kz, ku, vs,
     return new
 
 
-@pytest.mark.parametrize("D,zp,uns,dtype,vsc", [(128, 0, False, torch.bfloat16, 1 / 32),
-                                                (64, 128, True, torch.bfloat16, 1 / 32),
-                                                (256, 3, False, torch.bfloat16, 1 / 32),
-                                                (128, 7, False, torch.float16, 1.0),
-                                                (64, 150, True, torch.float16, 1.0)])
-def test_grid_values_equal_16bit_decode(K, D, zp, uns, dtype, vsc):
+@pytest.mark.parametrize("D,zp,uns,dtype,vsc,qsc", [(128, 0, False, torch.bfloat16, 1 / 32, 1),
+                                                    (64, 128, True, torch.bfloat16, 1 / 32, 1),
+                                                    (256, 3, False, torch.bfloat16, 1 / 32, 1),
+                                                    (128, 0, False, torch.bfloat16, 1 / 32,
+                                                     2.0**-20),
+                                                    (64, 9, False, torch.bfloat16, 1 / 32,
+                                                     2.0**17),
+                                                    (128, 7, False, torch.float16, 1.0, 1),
+                                                    (64, 150, True, torch.float16, 1.0, 1)])
+def test_grid_values_equal_16bit_decode(K, D, zp, uns, dtype, vsc, qsc):
     """K values k * 2^-5 and V values k * vsc (|k| <= 100): the int8 pages
     reconstruct exactly and the int8 decode equals the 16-bit paged decode
-    bit for bit (bf16 pages: the codes reach the MMAs through float; fp16:
-    through the half 1024 + code).  The int8 path applies a page's V scale to
-    the probabilities before they are packed; in fp16 a small product falls
-    below the normal range and rounds differently from the unscaled
-    probability of 16-bit pages, so the fp16 cases keep a V scale of 1."""
+    bit for bit (bf16 pages: the K codes meet an fp16 copy of the query, the
+    V codes reach the MMAs through float; fp16: through the half 1024 +
+    code).  The int8 path applies a page's V scale to the probabilities
+    before they are packed; in fp16 a small product falls below the normal
+    range and rounds differently from the unscaled probability of 16-bit
+    pages, so the fp16 cases keep a V scale of 1.  qsc scales two query
+    heads (of two groups) out of fp16's exact range, 2^-20 below it and
+    2^17 above it: those groups keep the exact bf16 route and still match
+    bit for bit."""
     B, Hkv, g, P, max_pages = 4, 2, 4, 64, 8
     Hq = Hkv * g
     n_pool = B * max_pages + 3
@@ -187,7 +195,10 @@ def test_grid_values_equal_16bit_decode(K, D, zp, uns, dtype, vsc):
                            keep_last=False)
     cos, sin = synth.rope_cache(1024, D)
     rope_d = (cos.to(dev()), sin.to(dev()))
-    q = synth.normal((B, Hq, 1, D), 62, 3, dtype).to(dev())
+    q = synth.normal((B, Hq, 1, D), 62, 3, dtype)
+    q[0, 1] *= qsc
+    q[2, g + 2] *= qsc
+    q = q.to(dev())
     st = status()
     L = K.kvc_seq_lengths(torch.from_numpy((T - 1).astype(np.int32)).to(dev()), 1,
                           max_pages * P, K.KVC_CONTIGUOUS, status=st)
@@ -199,6 +210,7 @@ def test_grid_values_equal_16bit_decode(K, D, zp, uns, dtype, vsc):
                              rope=rope_d, status=st)
     torch.cuda.synchronize()
     assert st.item() == 0
+    assert torch.isfinite(o16).all()
     assert torch.equal(o8, o16)
 
 
