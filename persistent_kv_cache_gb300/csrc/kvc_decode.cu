@@ -30,6 +30,7 @@
 // fp32 path: attn_f32_kernel, one warp per query row on CUDA cores (also used
 // by the multi-token call for fp32).
 #include <atomic>
+#include <cfloat>
 #include <mutex>
 #include <type_traits>
 
@@ -89,6 +90,15 @@ template <> struct Mma<__half> {
         return *reinterpret_cast<uint32_t *>(&v);
     }
 };
+
+// (lo, hi) rounded to bf16 and handed on as an fp16 pair: the same numbers
+// whenever each rounded value is 0 or of magnitude in [2^-17, 65504] (its 8
+// significant bits fit an fp16 normal or subnormal there)
+__device__ __forceinline__ uint32_t pack_bf16_as_f16(float lo, float hi)
+{
+    const uint32_t b = Mma<__nv_bfloat16>::pack(lo, hi);
+    return Mma<__half>::pack(__uint_as_float(b << 16), __uint_as_float(b & 0xffff0000u));
+}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                         uint32_t &r3)
@@ -286,12 +296,13 @@ struct GroupAttn {
     // Online-softmax update with the raw scores sc of this warp's 16 keys:
     // mask keys outside [lo, hi), move the reference max, rescale l and o,
     // and pack P (times vscale; VS false: times 1) as the B fragments of
-    // the output MMAs.  The reference max of a head moves only when the
-    // tile's max exceeds it by more than 8 (log2 units), so P stays below
-    // 2^8 and o and l are rescaled on few tiles after the first (O / l is
-    // the same for any reference).  SHORTCUTS (the split kernel): the key
-    // mask is skipped on tiles whose 16 keys are all visible.
-    template <bool VS>
+    // the output MMAs, in T or, F16P, rounded to bf16 and handed on as fp16
+    // (pack_bf16_as_f16).  The reference max of a head moves only when the
+    // tile's max exceeds it by more than 8 (log2 units), so P stays at or
+    // below 2^8 and o and l are rescaled on few tiles after the first (O / l
+    // is the same for any reference).  SHORTCUTS (the split kernel): the
+    // key mask is skipped on tiles whose 16 keys are all visible.
+    template <bool VS, bool F16P = false>
     __device__ __forceinline__ void softmax_step(float (&sc)[HB][4], int lane, int lo, int hi,
                                                  float scale_log2, float vscale,
                                                  uint32_t (&pb)[HB][2])
@@ -354,19 +365,26 @@ struct GroupAttn {
                 sc[hb][j] = p0;
                 sc[hb][2 + j] = p1;
             }
-            const uint32_t x0 = VS ? Mma<T>::pack(sc[hb][0] * vscale, sc[hb][1] * vscale)
-                                   : Mma<T>::pack(sc[hb][0], sc[hb][1]);
-            const uint32_t x1 = VS ? Mma<T>::pack(sc[hb][2] * vscale, sc[hb][3] * vscale)
-                                   : Mma<T>::pack(sc[hb][2], sc[hb][3]);
+            const float f = VS ? vscale : 1.f;
+            uint32_t x0, x1;
+            if constexpr (F16P) {
+                x0 = pack_bf16_as_f16(sc[hb][0] * f, sc[hb][1] * f);
+                x1 = pack_bf16_as_f16(sc[hb][2] * f, sc[hb][3] * f);
+            } else {
+                x0 = Mma<T>::pack(sc[hb][0] * f, sc[hb][1] * f);
+                x1 = Mma<T>::pack(sc[hb][2] * f, sc[hb][3] * f);
+            }
             pb[hb][0] = movm_trans(x0);  // P^T keys 2 tig, 2 tig + 1; head gid
             pb[hb][1] = movm_trans(x1);  // keys 2 tig + 8, 2 tig + 9
         }
     }
 
     // One tile: keys [lo, hi) of this warp's 16 rows are visible (the caller
-    // guarantees that V rows at and past `hi` hold finite values).
+    // guarantees that V rows at and past `hi` hold finite values); VS: P is
+    // multiplied by vscale (a power of two) before it is packed.
+    template <bool VS = false>
     __device__ __forceinline__ void tile(uint32_t kb, uint32_t vb, int warp, int lane, int lo,
-                                         int hi, float scale_log2)
+                                         int hi, float scale_log2, float vscale = 1.f)
     {
         float sc[HB][4];
 #pragma unroll
@@ -394,7 +412,7 @@ struct GroupAttn {
             }
         }
         uint32_t pb[HB][2];
-        softmax_step<false>(sc, lane, lo, hi, scale_log2, 1.f, pb);
+        softmax_step<VS>(sc, lane, lo, hi, scale_log2, vscale, pb);
         // A = V^T by transposing loads: matrix m holds keys 8 (m / 2) .. + 7
         // at columns 8 (m % 2) .. + 7 of the 16-column block
         const int vrow = 16 * warp + ((mat >> 1) << 3) + (lane & 7);
@@ -416,23 +434,24 @@ struct GroupAttn {
     // D / 2 bytes of each are the exact A fragments of its MMAs, as 16-byte
     // pieces interleaved across the warp (piece i of lane l at i * 512 +
     // l * 16), piece i holding 16-column blocks 2 i and 2 i + 1.  They become
-    // the integers u - zp in registers: the K codes as fp16 halves for fp16
-    // MMAs with the query when F16S (koff2 = q8_offset<__half>(zp); for a
-    // bf16 cache the query's fp16 copy, load_q16, holding the same values:
-    // the products are the same exact values as with bf16 operands, at a
-    // third of the conversion work), else as T (q8_offset<T>); the V codes as
-    // T (voff2 = q8_offset<T>(zp)) beside the probabilities; the scores take
-    // the page's K scale (folded into scale_log2) and the probabilities its V
-    // scale.  Every converted value is finite, and P is 0 past `hi`, so the
-    // rows past the split end need no zeroing.
+    // the integers u - zp in registers, as fp16 halves for f16 MMAs (a third
+    // of the conversion work of the bf16 route).  The K codes meet the query
+    // when F16S (koff2 = q8_offset<__half>(zp); for a bf16 cache the query's
+    // fp16 copy, load_q16, holding the same values, so the products are the
+    // same exact numbers as with bf16 operands), else they take T's route
+    // (q8_offset<T>).  The V codes (voff2 = q8_offset<__half>(zp)) meet the
+    // probabilities times vscale -- the page's V scale, for a bf16 cache
+    // times the CTA's power of two -- rounded as T and, for a bf16 cache,
+    // handed on as fp16 (pack_bf16_as_f16).  The page's K scale is folded
+    // into scale_log2.  Every converted value is finite, and P is 0 past
+    // `hi`, so the rows past the split end need no zeroing.
     template <bool F16S>
     __device__ __forceinline__ void tile_q8(uint32_t kq, uint32_t vq, int lane, int lo,
                                             int hi, float scale_log2, float vscale, uint64_t koff2,
                                             uint64_t voff2)
     {
-        // fp16 scores (for a bf16 cache: only when its query is exact in
-        // fp16; otherwise the K codes take T's own, exact route)
         using KT = typename std::conditional<F16S, __half, T>::type;
+        constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
         constexpr int NP = D / 32;  // 16-byte pieces of a lane's fragment bytes
         float sc[HB][4];
 #pragma unroll
@@ -445,7 +464,7 @@ struct GroupAttn {
             uint32_t qf[HB][4];
 #pragma unroll
             for (int hb = 0; hb < HB; ++hb) {
-                if constexpr (F16S && std::is_same<T, __nv_bfloat16>::value)
+                if constexpr (F16S && kBf16)
                     q16_frag2(hb, 2 * p, qf[hb]);
                 else
                     q_frag2(hb, 2 * p, qf[hb]);
@@ -463,31 +482,31 @@ struct GroupAttn {
                 Mma<KT>::run(sc[hb], a, qf[hb][2], qf[hb][3]);
         }
         uint32_t pb[HB][2];
-        softmax_step<true>(sc, lane, lo, hi, scale_log2, vscale, pb);
+        softmax_step<true, kBf16>(sc, lane, lo, hi, scale_log2, vscale, pb);
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
             // words: (columns of block 2p, keys 0-7), (block 2p, keys 8-15), (block 2p + 1, ...)
             const uint4 w = lds128(vq + p * 512 + lane * 16);
             uint32_t a[4];
-            u8x4_to_pairs<T>(w.x, voff2, a[0], a[1]);
-            u8x4_to_pairs<T>(w.y, voff2, a[2], a[3]);
+            u8x4_to_pairs<__half>(w.x, voff2, a[0], a[1]);
+            u8x4_to_pairs<__half>(w.y, voff2, a[2], a[3]);
 #pragma unroll
             for (int hb = 0; hb < HB; ++hb)
-                Mma<T>::run(o[hb][2 * p], a, pb[hb][0], pb[hb][1]);
-            u8x4_to_pairs<T>(w.z, voff2, a[0], a[1]);
-            u8x4_to_pairs<T>(w.w, voff2, a[2], a[3]);
+                Mma<__half>::run(o[hb][2 * p], a, pb[hb][0], pb[hb][1]);
+            u8x4_to_pairs<__half>(w.z, voff2, a[0], a[1]);
+            u8x4_to_pairs<__half>(w.w, voff2, a[2], a[3]);
 #pragma unroll
             for (int hb = 0; hb < HB; ++hb)
-                Mma<T>::run(o[hb][2 * p + 1], a, pb[hb][0], pb[hb][1]);
+                Mma<__half>::run(o[hb][2 * p + 1], a, pb[hb][0], pb[hb][1]);
         }
     }
 
-    // finish l across the warp's keys and publish (m, l, o) of heads < g for
-    // the 4-warp merge: cm/cl [4][16], co [4][rows][pitch] (rows >= g; a
-    // pitch of D + 4 floats keeps the stores of the four head pairs apart
-    // in the banks)
+    // finish l across the warp's keys and publish (m, l, o * oscale) of
+    // heads < g for the 4-warp merge: cm/cl [4][16], co [4][rows][pitch]
+    // (rows >= g; a pitch of D + 4 floats keeps the stores of the four head
+    // pairs apart in the banks)
     __device__ __forceinline__ void publish(float *cm, float *cl, float *co, int warp, int lane,
-                                            int g, int rows, int pitch)
+                                            int g, int rows, int pitch, float oscale = 1.f)
     {
         const int gid = lane >> 2, tig = lane & 3;
 #pragma unroll
@@ -507,8 +526,8 @@ struct GroupAttn {
                     float *dst = co + (warp * rows + h) * pitch + gid;
 #pragma unroll
                     for (int mb = 0; mb < MB; ++mb) {
-                        dst[16 * mb] = o[hb][mb][j];
-                        dst[16 * mb + 8] = o[hb][mb][2 + j];
+                        dst[16 * mb] = o[hb][mb][j] * oscale;
+                        dst[16 * mb + 8] = o[hb][mb][2 + j] * oscale;
                     }
                 }
             }
@@ -1067,6 +1086,25 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
             }
         }
     }
+    // kPagedQ over a bf16 cache: the probabilities reach the int8 tiles' V
+    // MMAs as fp16, multiplied by pscale = 2^k, which takes the largest V
+    // scale of the split's int8 pages into [2^6, 2^7), so that P * scale *
+    // 2^k stays at or below 2^15 (P <= 2^8) and small probabilities keep
+    // their bits; the 16-bit tiles' P takes the same factor and o is scaled
+    // back by 2^-k when it is published (both exact)
+    float pscale = 1.f, oscale = 1.f;
+    if constexpr (MODE == kPagedQ && std::is_same<T, __nv_bfloat16>::value) {
+        float vmax = my_e != 0 ? my_p[2] : 0.f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
+        if (vmax > 0.f && vmax <= FLT_MAX) {
+            const int e = (int)((__float_as_uint(vmax) >> 23) & 0xffu) - 127;
+            const int k = max(-64, min(64, 6 - e));
+            pscale = __uint_as_float((uint32_t)(127 + k) << 23);
+            oscale = __uint_as_float((uint32_t)(127 - k) << 23);
+        }
+    }
 
     int pos = 0;  // slots: ring position of the tile's first slot
     // kPagedQ: the tile's page among the split's (pi) and its place in that
@@ -1132,12 +1170,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const uint32_t kq = kvc::smem_u32(kgen) + warp * 16 * D;
                 if (f16s)
                     ga.template tile_q8<true>(kq, kq + kTile * D, lane, my_lo, my_valid,
-                                              a.scale_log2 * ks, vs, q8_offset<__half>(kz),
-                                              q8_offset<T>(vz));
+                                              a.scale_log2 * ks, vs * pscale,
+                                              q8_offset<__half>(kz), q8_offset<__half>(vz));
                 else
                     ga.template tile_q8<false>(kq, kq + kTile * D, lane, my_lo, my_valid,
-                                               a.scale_log2 * ks, vs, q8_offset<T>(kz),
-                                               q8_offset<T>(vz));
+                                               a.scale_log2 * ks, vs * pscale, q8_offset<T>(kz),
+                                               q8_offset<__half>(vz));
             }
         } else if (my_valid > 0) {
             if (my_valid < 16) {
@@ -1151,9 +1189,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 __syncwarp();
                 wrote = true;
             }
-            if (my_lo < my_valid)
-                ga.tile(kvc::smem_u32(kgen), kvc::smem_u32(vgen), warp, lane, my_lo, my_valid,
-                        a.scale_log2);
+            if (my_lo < my_valid) {
+                if constexpr (MODE == kPagedQ && std::is_same<T, __nv_bfloat16>::value)
+                    ga.template tile<true>(kvc::smem_u32(kgen), kvc::smem_u32(vgen), warp, lane,
+                                           my_lo, my_valid, a.scale_log2, pscale);
+                else
+                    ga.tile(kvc::smem_u32(kgen), kvc::smem_u32(vgen), warp, lane, my_lo,
+                            my_valid, a.scale_log2);
+            }
         }
         if (wrote)
             kvc::fence_proxy_async_smem();
@@ -1183,7 +1226,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
     float *cm = reinterpret_cast<float *>(stages);        // [4][16]
     float *cl = cm + kConsumers * 16;                      // [4][16]
     float *co = cl + kConsumers * 16;                      // [4][16][D]
-    ga.publish(cm, cl, co, warp, lane, g, 16, D + 4);
+    ga.publish(cm, cl, co, warp, lane, g, 16, D + 4, oscale);
     consumer_sync();
     const int hq0 = kvh * g;
     for (int idx = threadIdx.x; idx < g * (D / 4); idx += 128) {

@@ -172,15 +172,16 @@ def _quantize_table(K, table, n_rows, P, kp_d, vp_d, qk, qv, qp, ks, kz, ku, vs,
 def test_grid_values_equal_16bit_decode(K, D, zp, uns, dtype, vsc, qsc):
     """K values k * 2^-5 and V values k * vsc (|k| <= 100): the int8 pages
     reconstruct exactly and the int8 decode equals the 16-bit paged decode
-    bit for bit (bf16 pages: the K codes meet an fp16 copy of the query, the
-    V codes reach the MMAs through float; fp16: through the half 1024 +
-    code).  The int8 path applies a page's V scale to the probabilities
-    before they are packed; in fp16 a small product falls below the normal
-    range and rounds differently from the unscaled probability of 16-bit
-    pages, so the fp16 cases keep a V scale of 1.  qsc scales two query
-    heads (of two groups) out of fp16's exact range, 2^-20 below it and
-    2^17 above it: those groups keep the exact bf16 route and still match
-    bit for bit."""
+    bit for bit.  Every code reaches an f16 MMA as the half 1024 + code
+    minus the zero point; for bf16 pages the K codes meet an fp16 copy of
+    the query and the V codes the bf16-rounded probabilities (times the V
+    scale and a power of two) handed on as fp16.  The int8 path applies a
+    page's V scale to the probabilities before they are packed; in fp16 a
+    small product falls below the normal range and rounds differently from
+    the unscaled probability of 16-bit pages, so the fp16 cases keep a V
+    scale of 1.  qsc scales two query heads (of two groups) out of fp16's
+    exact range, 2^-20 below it and 2^17 above it: those groups' K codes
+    keep the bf16 route, and they still match bit for bit."""
     B, Hkv, g, P, max_pages = 4, 2, 4, 64, 8
     Hq = Hkv * g
     n_pool = B * max_pages + 3
@@ -279,6 +280,58 @@ def test_mixed_tables(K, orc, P, D, g, W, dtype, uns):
                                     qp.cpu().numpy(), qtab, P, T, T, window=W,
                                     cos_cache=cos.numpy(), sin_cache=sin.numpy())
     assert_close(out, want, 2e-2, "mixed table")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_page_scales_differ(K, orc, dtype):
+    """Pages of one split quantized with V scales four decades apart (and K
+    scales likewise), 16-bit pages among them: the decode scales each int8
+    tile's probabilities by its own page's V scale (a bf16 cache by a common
+    power of two on top, chosen from the split's largest V scale and taken
+    out of the output again), so every page still meets the oracle."""
+    B, Hkv, g, D, P, max_pages = 3, 2, 4, 128, 64, 10
+    Hq = Hkv * g
+    kp, vp, table = _paged_setup(B, Hkv, D, P, max_pages, 2, 67, dtype)
+    gk, gv = kp.to(dev()), vp.to(dev())
+    T = np.array([max_pages * P, 300, 7 * P + 5])
+    qk, qv, qp = _q8_pools(B * max_pages, Hkv, P, D)
+    v_scales = [0.0007, 0.013, 5.0, 0.04, 0.9]
+    k_scales = [0.02, 0.3, 0.004, 0.05, 0.011]
+    qtab, n_q = table.copy(), 0
+    for i in range(len(v_scales)):
+        src, dst = [], []
+        for b in range(B):
+            for j in range(i, (int(T[b]) + P - 1) // P - 1, len(v_scales)):
+                if (b, j) == (0, 3):
+                    continue                       # stays a 16-bit page
+                src.append(int(table[b, j]))
+                dst.append(n_q)
+                qtab[b, j] = K.KVC_PAGE_QUANT | n_q
+                n_q += 1
+        if src:
+            st = status()
+            K.kvc_quantize_pages(gk, gv, qk, qv, torch.tensor(src, dtype=torch.int32,
+                                                              device=dev()),
+                                 torch.tensor(dst, dtype=torch.int32, device=dev()), qp,
+                                 k_scales[i], 0, False, v_scales[i], 5, False, status=st)
+            torch.cuda.synchronize()
+            assert st.item() == 0
+    cos, sin = synth.rope_cache(max_pages * P + 1, D)
+    rope_d = (cos.to(dev()), sin.to(dev()))
+    q = synth.normal((B, Hq, 1, D), 67, 9, dtype)
+    st = status()
+    L = K.kvc_seq_lengths(torch.from_numpy((T - 1).astype(np.int32)).to(dev()), 1,
+                          max_pages * P, K.KVC_CONTIGUOUS, status=st)
+    out = torch.full((B, Hq, 1, D), float("nan"), dtype=dtype, device=dev())
+    K.kvc_gqa_decode_paged_q(out, q.to(dev()), gk, gv, qk, qv, qp,
+                             torch.from_numpy(qtab).to(dev()), L, rope=rope_d, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    nqk, nqv = _pools_np(qk, qv)
+    want, _ = orc.paged_attention_q(synth.bits(q), synth.bits(kp), synth.bits(vp), nqk, nqv,
+                                    qp.cpu().numpy(), qtab, P, T, T,
+                                    cos_cache=cos.numpy(), sin_cache=sin.numpy())
+    assert_close(out, want, 2e-2, "per-page scales")
 
 
 def test_bad_int8_entry(K):
