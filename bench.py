@@ -184,43 +184,100 @@ def barrier(world: int):
 # workloads
 # --------------------------------------------------------------------------
 
+E2E_COPIES = {
+    False: "every step copies its inputs in from pinned host memory and its result out, "
+           "on the compute stream",
+    True: "every step copies its inputs in from pinned host memory and its result out, "
+          "on two copy streams with doubled device buffers, overlapped with the "
+          "neighbouring steps' compute"}
+
+
 class Workload:
     """Common end-to-end pass: per step, copy the step's inputs from pinned
     host memory, run the step through the public API, copy the result back;
-    all inside the timed region."""
+    all inside the timed region.  With e2e_overlap the copies run on streams
+    of their own and the device buffers are doubled, so that step i + 1's
+    inputs travel while step i computes and step i's result travels while
+    step i + 1 computes (events keep every buffer from being overwritten
+    while in use); that costs about ten more host calls a step, so it is
+    taken by the workloads whose step lasts clearly longer than their host
+    side (about 90 us and up), and the others copy on the compute stream."""
     e = 2  # bytes per bf16 element
+    e2e_overlap = False
+    # False where the result read back is a view of state the next step
+    # updates in place: that step then waits for the read-back
+    out_double = True
 
     def e2e_setup(self):
         """The step's inputs travel as one pinned host buffer and one copy:
         every device input is re-pointed (in place, so the workload keeps
-        using the same tensor objects) at its slice of one device buffer."""
+        using the same tensor objects) at its slice of the device buffer the
+        step uses (one, or two taken in turn)."""
         torch = self.torch
-        offs, n = [], 0
+        self._offs, n = [], 0
         for t in self.host_inputs:
-            offs.append(n)
+            self._offs.append(n)
             n += (t.numel() * t.element_size() + 255) // 256 * 256
         self.h_pack = torch.empty(n, dtype=torch.uint8).pin_memory()
         dev = self.device_inputs[0].device
-        self.d_pack = torch.empty(n, dtype=torch.uint8, device=dev)
-        for h, d, o in zip(self.host_inputs, self.device_inputs, offs):
+        for h, o in zip(self.host_inputs, self._offs):
             nb = h.numel() * h.element_size()
             self.h_pack[o:o + nb].copy_(h.contiguous().view(-1).view(torch.uint8))
-            d.set_(self.d_pack.untyped_storage(), o // d.element_size(), d.shape, d.stride())
-        self.d_pack.copy_(self.h_pack)
-        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        nbuf = 2 if self.e2e_overlap else 1
+        self.d_packs = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(nbuf)]
+        for d in self.d_packs:
+            d.copy_(self.h_pack)
+        self._point_inputs(0)
+        two = self.e2e_overlap and self.out_double
+        self.outs = [self.out, torch.empty_like(self.out) if two else self.out]
+        self.h_outs = [torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+                       for _ in range(nbuf)]
+        if self.e2e_overlap:
+            self.s_in, self.s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+            self.ev_in, self.ev_comp, self.ev_out = ([torch.cuda.Event() for _ in range(2)]
+                                                     for _ in range(3))
+        self._n = 0
         self.h2d = n
-        self.d2h = self.h_out.numel() * self.h_out.element_size()
+        self.d2h = self.h_outs[0].numel() * self.h_outs[0].element_size()
+
+    def _point_inputs(self, k):
+        for d, o in zip(self.device_inputs, self._offs):
+            d.set_(self.d_packs[k].untyped_storage(), o // d.element_size(), d.shape, d.stride())
 
     def e2e_step(self, i):
-        self.d_pack.copy_(self.h_pack, non_blocking=True)
+        if not self.e2e_overlap:
+            self.d_packs[0].copy_(self.h_pack, non_blocking=True)
+            self.step(i)
+            self.h_outs[0].copy_(self.out, non_blocking=True)
+            return
+        torch = self.torch
+        k, first = self._n % 2, self._n < 2
+        comp = torch.cuda.current_stream()
+        with torch.cuda.stream(self.s_in):
+            if not first:
+                self.s_in.wait_event(self.ev_comp[k])   # step n - 2 is done with buffer k
+            self.d_packs[k].copy_(self.h_pack, non_blocking=True)
+            self.ev_in[k].record(self.s_in)
+        comp.wait_event(self.ev_in[k])
+        if self._n > 0:
+            # the result buffer this step writes has been read back
+            comp.wait_event(self.ev_out[k if self.out_double else 1 - k])
+        self._point_inputs(k)
+        self.out = self.outs[k]
         self.step(i)
-        self.h_out.copy_(self.out, non_blocking=True)
+        self.ev_comp[k].record(comp)
+        with torch.cuda.stream(self.s_out):
+            self.s_out.wait_event(self.ev_comp[k])
+            self.h_outs[k].copy_(self.out, non_blocking=True)
+            self.ev_out[k].record(self.s_out)
+        self._n += 1
 
 
 class ContigDecode(Workload):
     """Contiguous persistent-cache GQA decode, one-token append then attention.
     fused=True runs each step as one kvc_decode_step launch; otherwise as
     kvc_seq_lengths + kvc_window_append + kvc_gqa_decode (split + merge)."""
+    e2e_overlap = True   # a step of about 93 us
     bound = "hbm"
     fused = True
 
@@ -487,6 +544,7 @@ class WindowDecode(Workload):
 
 class WindowPrefill(Workload):
     """Windowed chunked prefill through the C + S staging cache."""
+    e2e_overlap = True   # steps of 0.15 to 1 ms
     roofline_kernel = "kvc_gqa_prefill_chunk (tcgen05)"
     bound = "tensor"
     slack = 0  # rows of capacity beyond the window (C = W + slack)
@@ -723,6 +781,7 @@ class Scatter(Workload):
     or (functional) into a separate present cache."""
     bound = "hbm"
     in_place = True
+    out_double = False  # the result read back is a slice of present
 
     def __init__(self, dev, seed=0, with_kernels=True, chunk=64, max_steps=4096):
         import torch
@@ -914,6 +973,7 @@ class PagedDecodeQ8(PagedDecode):
     one held as int8 (affine, scale 0.04, zero point 0 for K and V; the
     newest page, where the step appends, stays 16-bit): one step =
     kvc_seq_lengths + kvc_paged_append + kvc_gqa_decode_paged_q (+ merge)."""
+    e2e_overlap = False  # a step of about 68 us: the plain loop is faster
     k_scale = v_scale = 0.04
 
     def __init__(self, dev, seed=0, with_kernels=True, chunk=None):
@@ -1123,6 +1183,7 @@ class WindowDecode256(RingDecode256):
     U[1, 20000]): lengths, the in-place compaction of the whole window by one
     row plus the RoPE append (a cluster of eight CTAs per slice), then the
     split decode and merge.  The roofline kernel is the compaction."""
+    e2e_overlap = True   # a step of about 112 us
     roofline_kernel = "kvc_window_append, S = 1 (cluster compaction)"
     traffic_key = ("kvc_cache.cu", "compact_cluster_kernel@window_d256")
 
@@ -1435,7 +1496,8 @@ def secondary_entry(name, chunk, args, dev, peaks, peak_kind):
              "steps_per_s": args.steps / sec,
              "tokens_per_s": wl.tokens_per_step * args.steps / sec,
              "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": wl.h2d,
-                     "d2h_bytes_per_step": wl.d2h, "steps_per_s": args.steps / r["e2e_s"]},
+                     "d2h_bytes_per_step": wl.d2h, "steps_per_s": args.steps / r["e2e_s"],
+                     "copies": E2E_COPIES[wl.e2e_overlap]},
              "roofline": roof, "replay_stats": r["replay_stats"],
              "cpu_baseline": cpu_baseline_of(wl, parallel=(2.0, 6.0), single=None),
              "gpu_launches": wl.launches_per_step * args.steps, "clocks": r["clocks"],
@@ -1477,7 +1539,8 @@ def run_ours(args):
         "steps_per_s": args.steps * world / sec,
         "tokens_per_s": wl.tokens_per_step * args.steps * world / sec,
         "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": wl.h2d,
-                "d2h_bytes_per_step": wl.d2h, "steps_per_s": args.steps * world / e2e_s},
+                "d2h_bytes_per_step": wl.d2h, "steps_per_s": args.steps * world / e2e_s,
+                "copies": E2E_COPIES[wl.e2e_overlap]},
         "roofline": roof,
         "replay_stats": r["replay_stats"],
         "cpu_baseline": cpu,
