@@ -265,7 +265,8 @@ struct GroupAttn {
         ldsm_x4(q16_addr + hb * 8 * (D + 8) * 2 + kk * 32, f[0], f[1], f[2], f[3]);
     }
     // the fp16 copy [16][D + 8] of the query rows, for the int8 tiles of a
-    // bf16 cache (a bf16 query element is exact in fp16 down to 2^-14)
+    // bf16 cache (used only when every element is 0 or of magnitude in
+    // [2^-17, 65504], where a bf16 value is exact in fp16)
     __device__ __forceinline__ void load_q16(const __half *qs16, int lane)
     {
         q16_addr = kvc::smem_u32(qs16 + (lane & 7) * (D + 8) + (lane >> 3) * 8);
